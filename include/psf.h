@@ -1,0 +1,198 @@
+/*
+ * psf.h -- C ABI of the packed-sequence flash-attention library (libpsf.so).
+ *
+ * Exact softmax attention over packed variable-length sequences on one GB300
+ * (sm_103a): forward returning out and an fp32 log-sum-exp, backward from
+ * caller-supplied out/lse returning dQ and dK/dV reduced to the KV heads, and
+ * the doc-ids -> varlen-segment builder that feeds them.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Pointers are DEVICE pointers owned by the caller; the library allocates
+ *    nothing. Outputs and workspaces are caller-allocated. Tensor base pointers
+ *    must be 16-byte aligned (a TMA requirement).
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *    Every call is asynchronous on that stream.
+ *  - Return value: PSF_OK (0) after a successful launch, or a negative code.
+ *    No exception crosses the ABI. psf_last_error() gives a message for the
+ *    last failing call on the calling thread.
+ *  - Kernel-side faults in the caller's data (bad segment arrays) and pipeline
+ *    waits that ran out are recorded in a per-device status word that
+ *    psf_device_status() returns after synchronising the device.
+ *  - dtype: bf16 inputs and outputs (`out`, `dq`, `dk`, `dv`); lse and the
+ *    row-dot Delta are fp32.
+ *  - Head dims (Dqk, Dv) supported: (64,64), (128,128), (192,128), (512,512).
+ *  - GQA: Hq % Hkv == 0; query head h uses KV head h / (Hq / Hkv).
+ *  - Causal masks are aligned to the bottom-right corner of each segment
+ *    (dense: of the Nq x Nk matrix): local query i of a segment with m queries
+ *    and n keys sees local key j iff j <= i + (n - m).
+ *  - window_left > 0 is a left window that counts the current token: key j is
+ *    visible only if j >= i + (n - m) - window_left + 1. window_left < 0 (for
+ *    example INT32_MIN, the pages' "no window" sentinel) means unbounded;
+ *    window_left == 0 is rejected with PSF_EINVAL.
+ *  - Query rows covered by no segment, and rows that see no key, get out = 0
+ *    and lse = -inf; the backward treats lse = -inf as zero probability.
+ *  - scale must be finite and > 0.
+ */
+#ifndef PSF_H_
+#define PSF_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PSF_OK 0
+#define PSF_EINVAL (-1)        /* bad argument: shape, null pointer, alignment, window == 0, scale */
+#define PSF_EUNSUPPORTED (-2)  /* no kernel for this head-dim pair, or the device is not sm_103 */
+#define PSF_ECUDA (-3)         /* a CUDA runtime call (launch, tensor-map encode) failed */
+#define PSF_EDEVICE_ARGS (-4)  /* kernel-side validation rejected the segment arrays */
+#define PSF_ETIMEOUT (-5)      /* a pipeline wait inside a kernel exceeded its limit */
+#define PSF_EWORKSPACE (-6)    /* workspace pointer null or smaller than the size query */
+
+/* Tensor layouts accepted by the varlen calls. */
+#define PSF_LAYOUT_THD 0  /* packed [T, H, D]; lse [H, T]                                */
+#define PSF_LAYOUT_BHSD 1 /* batched [B, H, S, D]; lse [B, H, S]; rows are b * S + s     */
+
+/* Message for the last failing call on this thread (never NULL). */
+const char* psf_last_error(void);
+
+/* 1 if the current device is an sm_103 GPU this library was built for, else 0. */
+int psf_device_supported(void);
+
+/*
+ * Synchronise the current device and return the first kernel-side status
+ * recorded since the last clear: PSF_OK, PSF_EDEVICE_ARGS or PSF_ETIMEOUT.
+ * clear != 0 resets it to PSF_OK.
+ */
+int psf_device_status(int clear);
+
+/* Upper bound, in nanoseconds, of every pipeline wait inside the kernels
+ * (default 2e9, or $PSF_WAIT_LIMIT_NS when set at load time). */
+void psf_set_wait_limit_ns(uint64_t ns);
+
+/*
+ * Workspace sizes in bytes. total_q_rows / total_k_rows count the flattened
+ * query / key rows (T for THD, B * S for BHSD); nseg is the number of segments
+ * (or the capacity passed to the builder).
+ */
+size_t psf_attn_fwd_workspace_size(int64_t total_q_rows, int nseg);
+size_t psf_attn_bwd_workspace_size(int64_t total_q_rows, int64_t total_k_rows, int nseg, int Hq, int Dqk);
+
+/*
+ * Varlen forward.           [ffpa_attention page, `_ffpa_varlen_fwd`: packed THD
+ *                            inputs, cu_q/cu_k/max_q/max_k/scale/causal, returns
+ *                            (out[T,Hq,D], lse[Hq,T]); left window per the
+ *                            attention utils page, `window_size`]
+ *  q [Tq,Hq,Dqk], k [Tk,Hkv,Dqk], v [Tk,Hkv,Dv] -> out [Tq,Hq,Dv], lse [Hq,Tq]
+ *  (layout PSF_LAYOUT_THD), or the BHSD forms with Tq = B*Sq, Tk = B*Sk and
+ *  lse [B,Hq,Sq] (layout PSF_LAYOUT_BHSD; a segment must not cross a batch row).
+ *  cu_q / cu_k: int32 [nseg+1] device arrays of exclusive prefix sums over the
+ *  flattened rows; segment s pairs queries [cu_q[s], cu_q[s+1]) with keys
+ *  [cu_k[s], cu_k[s+1]); zero-length segments are allowed.
+ *  dev_meta: nullable int32[3] device array {nseg, max_q, max_k} written by
+ *  psf_build_doc_segments; when given, the segment count and maxima are read
+ *  from it on the device and `nseg` is only the capacity of cu_q/cu_k.
+ *  max_q / max_k: the longest segment lengths (ignored when dev_meta is given);
+ *  a longer segment is a PSF_EDEVICE_ARGS device status.
+ *  workspace: psf_attn_fwd_workspace_size(Tq, nseg) bytes.
+ */
+int psf_attn_varlen_fwd(const void* q, const void* k, const void* v, void* out, float* lse, const int32_t* cu_q,
+                        const int32_t* cu_k, const int32_t* dev_meta, int nseg, int max_q, int max_k, int layout,
+                        int B, int Sq, int Sk, int Hq, int Hkv, int Dqk, int Dv, float scale, int causal,
+                        int32_t window_left, void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Varlen backward from caller-supplied out / lse.
+ *                           [ffpa_attention page, `_ffpa_varlen_bwd`: "using the
+ *                            caller-supplied out/lse. Returns (dq, dk, dv)"]
+ *  Same layouts and segment rules as the forward. dout has the layout of out.
+ *  dq has q's layout; dk / dv have k's / v's layout (Hkv heads: the gradients of
+ *  the Hq / Hkv query heads sharing a KV head are summed on chip).
+ *  Keys that no query sees get dk = dv = 0; query rows outside every segment
+ *  get dq = 0.
+ *  workspace: psf_attn_bwd_workspace_size(Tq, Tk, nseg, Hq, Dqk) bytes (holds
+ *  the fp32 dQ accumulator, Delta = rowsum(dO * out) and the tile schedule).
+ */
+int psf_attn_varlen_bwd(const void* dout, const void* q, const void* k, const void* v, const void* out,
+                        const float* lse, void* dq, void* dk, void* dv, const int32_t* cu_q, const int32_t* cu_k,
+                        const int32_t* dev_meta, int nseg, int max_q, int max_k, int layout, int B, int Sq, int Sk,
+                        int Hq, int Hkv, int Dqk, int Dv, float scale, int causal, int32_t window_left,
+                        void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Dense forward on SDPA-layout tensors.
+ *                           [ffpa_attention page, `_ffpa_dense_fwd`: [B,H,N,D]
+ *                            inputs, returns (out[B,Hq,Nq,D], lse[B,Hq,Nq] fp32),
+ *                            GQA and causal/non-causal handled internally;
+ *                            fa4 page, `causal_fa4_attention`]
+ *  q [B,Hq,Nq,Dqk], k [B,Hkv,Nk,Dqk], v [B,Hkv,Nk,Dv], out [B,Hq,Nq,Dv],
+ *  lse [B,Hq,Nq]. Causal is bottom-right aligned when Nq != Nk.
+ *  workspace: psf_attn_fwd_workspace_size(B * Nq, B) bytes.
+ */
+int psf_attn_dense_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq, int Hkv,
+                       int Nq, int Nk, int Dqk, int Dv, float scale, int causal, int32_t window_left,
+                       void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Dense backward.           [ffpa_attention page, `_ffpa_dense_bwd`: returns
+ *                            (dq, dk, dv) in [B,H,N,D], dK/dV reduced to Hkv]
+ *  workspace: psf_attn_bwd_workspace_size(B * Nq, B * Nk, B, Hq, Dqk) bytes.
+ */
+int psf_attn_dense_bwd(const void* dout, const void* q, const void* k, const void* v, const void* out,
+                       const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Nq, int Nk,
+                       int Dqk, int Dv, float scale, int causal, int32_t window_left, void* workspace,
+                       size_t ws_bytes, void* stream);
+
+/*
+ * Doc ids -> varlen segments, on the GPU.
+ *                           [fa4 page, module docstring bullets 1-3,
+ *                            `_varlen_segments`, `_varlen_layout`]
+ *  kv_doc_ids: int32 [B, Sk] document ids (1-based, 0 = padding) of all keys.
+ *  The local query shard is [q_global_start, q_global_start + q_length) of
+ *  every row. Every maximal run of equal id (padding runs included) is split at
+ *  the end of the shard; each piece contributes its overlap with the shard as
+ *  queries and all of its tokens as keys; pieces without queries become
+ *  zero-query segments, so the key segments tile the flattened [B * Sk] rows
+ *  and the query segments tile [B * q_length]. Segments are listed row-major.
+ *  Outputs: cu_q, cu_k (int32, capacity + 1 entries each, prefix sums),
+ *  dev_meta int32[3] = {nseg, max_q, max_k}, and seg_is_pad (nullable, uint8
+ *  [capacity]: 1 for a segment cut from a padding run).
+ *  capacity: room in cu_q / cu_k; B * Sk + B always suffices. Too small a
+ *  capacity is a PSF_EDEVICE_ARGS device status (dev_meta[0] is then 0).
+ *  Requires 0 <= q_global_start, q_global_start + q_length <= Sk.
+ */
+int psf_build_doc_segments(const int32_t* kv_doc_ids, int B, int Sk, int q_length, int q_global_start,
+                           int32_t* cu_q, int32_t* cu_k, int capacity, int32_t* dev_meta, uint8_t* seg_is_pad,
+                           void* stream);
+
+/*
+ * Zero the padding queries of a document-causal result: rows whose query
+ * document id is 0 get out = 0 and lse = -inf.
+ *                           [fa4 page, `document_causal_fa4_attention`:
+ *                            "padding queries are zero"; cp_attention page,
+ *                            lse "-inf for non-participating rows"]
+ *  q_doc_ids: int32 [B, Lq]; out / lse in `layout` with S = Lq.
+ */
+int psf_pad_fixup(void* out, float* lse, const int32_t* q_doc_ids, int layout, int B, int Lq, int Hq, int Dv,
+                  void* stream);
+
+/*
+ * Merge two partial attention results computed over disjoint key sets.
+ *                           [cp_attention page, "-inf-safe online-softmax merge"]
+ *  l = logaddexp(l1, l2); o = o1 * exp(l1 - l) + o2 * exp(l2 - l), in fp32. A
+ *  row with both inputs -inf gives o = 0, l = -inf (never NaN).
+ *  o1, o2: bf16 [T, H, D]; l1, l2: fp32 [H, T] (PSF_LAYOUT_THD only).
+ *  Outputs: o_f32 (nullable) fp32 [T,H,D], o_bf16 (nullable) bf16 [T,H,D],
+ *  l fp32 [H,T]. Outputs may alias neither input.
+ */
+int psf_lse_merge(const void* o1, const float* l1, const void* o2, const float* l2, float* o_f32, void* o_bf16,
+                  float* l, int T, int H, int D, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PSF_H_ */

@@ -1,0 +1,268 @@
+"""Python binding of libpsf.so: argument marshalling only.
+
+Every function allocates its outputs and workspace with torch (device memory
+and the current stream are all torch provides) and calls the C ABI; every step
+of the computation runs in the library's CUDA kernels. Non-zero return codes
+raise ``PSFError`` (a ``ValueError``).
+
+Layouts follow the pages:
+  * varlen: packed ``[T, H, D]`` with ``lse [H, T]``
+    [ffpa_attention page, ``_ffpa_varlen_fwd``];
+  * dense: ``[B, H, N, D]`` with ``lse [B, H, N]``
+    [ffpa_attention page, ``_ffpa_dense_fwd``];
+  * document-causal: ``[B, H, S, D]`` (or packed ``[S, H, D]`` for one row)
+    [fa4 page, ``document_causal_fa4_attention``].
+"""
+from __future__ import annotations
+
+import torch
+
+from . import _lib
+from ._lib import PSF_LAYOUT_BHSD, PSF_LAYOUT_THD, check
+
+NO_WINDOW = -(2 ** 31)  # the pages' "no window" sentinel
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream():
+    return torch.cuda.current_stream().cuda_stream
+
+
+def _window(window) -> int:
+    if window is None:
+        return NO_WINDOW
+    return int(window)
+
+
+def _need(t, name, dtype=None):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+def _i32(t, name):
+    _need(t, name, torch.int32)
+    return t
+
+
+def device_status(clear: bool = True) -> int:
+    """Synchronise and return the kernel-side status (0, PSF_EDEVICE_ARGS or PSF_ETIMEOUT)."""
+    return _lib.load().psf_device_status(1 if clear else 0)
+
+
+def check_device_status() -> None:
+    rc = device_status(True)
+    check(rc)
+
+
+def set_wait_limit_ns(ns: int) -> None:
+    _lib.load().psf_set_wait_limit_ns(int(ns))
+
+
+def fwd_workspace_size(total_q_rows: int, nseg: int) -> int:
+    return int(_lib.load().psf_attn_fwd_workspace_size(int(total_q_rows), int(nseg)))
+
+
+def bwd_workspace_size(total_q_rows: int, total_k_rows: int, nseg: int, Hq: int, Dqk: int) -> int:
+    return int(_lib.load().psf_attn_bwd_workspace_size(int(total_q_rows), int(total_k_rows), int(nseg), int(Hq),
+                                                       int(Dqk)))
+
+
+def _workspace(nbytes: int, device) -> torch.Tensor:
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+# ---------------------------------------------------------------------------
+# varlen (packed THD, or BHSD rows when layout="bhsd")
+
+def _varlen_dims(q, k, v, layout):
+    if layout == "thd":
+        Tq, Hq, Dqk = q.shape
+        Tk, Hkv, _ = k.shape
+        return PSF_LAYOUT_THD, 1, Tq, Tk, Hq, Hkv, Dqk, v.shape[2]
+    B, Hq, Sq, Dqk = q.shape
+    Hkv, Sk = k.shape[1], k.shape[2]
+    return PSF_LAYOUT_BHSD, B, Sq, Sk, Hq, Hkv, Dqk, v.shape[3]
+
+
+def attn_varlen_fwd(q, k, v, cu_q, cu_k, max_q, max_k, scale, causal, window=None, dev_meta=None,
+                    layout="thd", out=None, lse=None, workspace=None):
+    """Packed varlen forward -> (out, lse). cu_q/cu_k int32 [nseg+1] on the device."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, torch.bfloat16)
+    _i32(cu_q, "cu_q")
+    _i32(cu_k, "cu_k")
+    lay, B, Sq, Sk, Hq, Hkv, Dqk, Dv = _varlen_dims(q, k, v, layout)
+    nseg = cu_q.numel() - 1
+    if out is None:
+        out = torch.empty(*q.shape[:-1], Dv, dtype=q.dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty((Hq, Sq) if lay == PSF_LAYOUT_THD else (B, Hq, Sq), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = _workspace(fwd_workspace_size(B * Sq, nseg), q.device)
+    rc = _lib.load().psf_attn_varlen_fwd(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(cu_q), _ptr(cu_k), _ptr(dev_meta), nseg,
+        int(max_q), int(max_k), lay, B, Sq, Sk, Hq, Hkv, Dqk, Dv, float(scale), int(bool(causal)), _window(window),
+        _ptr(workspace), workspace.numel(), _stream())
+    check(rc)
+    return out, lse
+
+
+def attn_varlen_bwd(dout, q, k, v, out, lse, cu_q, cu_k, max_q, max_k, scale, causal, window=None,
+                    dev_meta=None, layout="thd", workspace=None):
+    """Packed varlen backward from caller-supplied out/lse -> (dq, dk, dv)."""
+    for t, n in ((dout, "dout"), (q, "q"), (k, "k"), (v, "v"), (out, "out")):
+        _need(t, n, torch.bfloat16)
+    _need(lse, "lse", torch.float32)
+    _i32(cu_q, "cu_q")
+    _i32(cu_k, "cu_k")
+    lay, B, Sq, Sk, Hq, Hkv, Dqk, Dv = _varlen_dims(q, k, v, layout)
+    nseg = cu_q.numel() - 1
+    dq = torch.empty_like(q)
+    dk = torch.empty_like(k)
+    dv = torch.empty_like(v)
+    if workspace is None:
+        workspace = _workspace(bwd_workspace_size(B * Sq, B * Sk, nseg, Hq, Dqk), q.device)
+    rc = _lib.load().psf_attn_varlen_bwd(
+        _ptr(dout), _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(cu_q),
+        _ptr(cu_k), _ptr(dev_meta), nseg, int(max_q), int(max_k), lay, B, Sq, Sk, Hq, Hkv, Dqk, Dv, float(scale),
+        int(bool(causal)), _window(window), _ptr(workspace), workspace.numel(), _stream())
+    check(rc)
+    return dq, dk, dv
+
+
+# ---------------------------------------------------------------------------
+# dense [B, H, N, D]
+
+def attn_dense_fwd(q, k, v, scale, causal, window=None, workspace=None):
+    """Dense forward -> (out [B,Hq,Nq,Dv], lse [B,Hq,Nq] fp32)."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, torch.bfloat16)
+    B, Hq, Nq, Dqk = q.shape
+    Hkv, Nk = k.shape[1], k.shape[2]
+    Dv = v.shape[3]
+    out = torch.empty(B, Hq, Nq, Dv, dtype=q.dtype, device=q.device)
+    lse = torch.empty(B, Hq, Nq, dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = _workspace(fwd_workspace_size(B * Nq, B), q.device)
+    rc = _lib.load().psf_attn_dense_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, Nq, Nk, Dqk,
+                                        Dv, float(scale), int(bool(causal)), _window(window), _ptr(workspace),
+                                        workspace.numel(), _stream())
+    check(rc)
+    return out, lse
+
+
+def attn_dense_bwd(dout, q, k, v, out, lse, scale, causal, window=None, workspace=None):
+    """Dense backward -> (dq, dk, dv) in [B,H,N,D], dk/dv at Hkv heads."""
+    for t, n in ((dout, "dout"), (q, "q"), (k, "k"), (v, "v"), (out, "out")):
+        _need(t, n, torch.bfloat16)
+    _need(lse, "lse", torch.float32)
+    B, Hq, Nq, Dqk = q.shape
+    Hkv, Nk = k.shape[1], k.shape[2]
+    Dv = v.shape[3]
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    if workspace is None:
+        workspace = _workspace(bwd_workspace_size(B * Nq, B * Nk, B, Hq, Dqk), q.device)
+    rc = _lib.load().psf_attn_dense_bwd(_ptr(dout), _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dq),
+                                        _ptr(dk), _ptr(dv), B, Hq, Hkv, Nq, Nk, Dqk, Dv, float(scale),
+                                        int(bool(causal)), _window(window), _ptr(workspace), workspace.numel(),
+                                        _stream())
+    check(rc)
+    return dq, dk, dv
+
+
+# ---------------------------------------------------------------------------
+# segment builder, pad fixup, merge
+
+def build_doc_segments(kv_doc_ids, q_length, q_global_start, capacity=None, want_pad_flags=False):
+    """Doc ids [B, Sk] int32 (device) -> (cu_q, cu_k, dev_meta, seg_is_pad).
+
+    dev_meta = int32 [nseg, max_q, max_k] on the device; cu arrays hold
+    capacity + 1 entries of which the first nseg + 1 are meaningful.
+    """
+    _i32(kv_doc_ids, "kv_doc_ids")
+    if kv_doc_ids.dim() == 1:
+        kv_doc_ids = kv_doc_ids[None]
+    B, Sk = kv_doc_ids.shape
+    if capacity is None:
+        capacity = B * Sk + B
+    dev = kv_doc_ids.device
+    cu_q = torch.empty(capacity + 1, dtype=torch.int32, device=dev)
+    cu_k = torch.empty(capacity + 1, dtype=torch.int32, device=dev)
+    meta = torch.empty(3, dtype=torch.int32, device=dev)
+    pad = torch.empty(max(capacity, 1), dtype=torch.uint8, device=dev) if want_pad_flags else None
+    rc = _lib.load().psf_build_doc_segments(_ptr(kv_doc_ids), B, Sk, int(q_length), int(q_global_start),
+                                            _ptr(cu_q), _ptr(cu_k), int(capacity), _ptr(meta), _ptr(pad), _stream())
+    check(rc)
+    return cu_q, cu_k, meta, pad
+
+
+def pad_fixup(out, lse, q_doc_ids, layout="thd"):
+    """In place: rows with query doc id 0 get out = 0 and lse = -inf."""
+    _need(out, "out", torch.bfloat16)
+    _need(lse, "lse", torch.float32)
+    _i32(q_doc_ids, "q_doc_ids")
+    if layout == "thd":
+        Lq, Hq, Dv = out.shape
+        B, lay = 1, PSF_LAYOUT_THD
+    else:
+        B, Hq, Lq, Dv = out.shape
+        lay = PSF_LAYOUT_BHSD
+    rc = _lib.load().psf_pad_fixup(_ptr(out), _ptr(lse), _ptr(q_doc_ids), lay, B, Lq, Hq, Dv, _stream())
+    check(rc)
+    return out, lse
+
+
+def lse_merge(o1, l1, o2, l2, want_f32=True, want_bf16=False):
+    """Merge two partial results over disjoint keys: o [T,H,D] bf16, l [H,T] fp32."""
+    for t, n in ((o1, "o1"), (o2, "o2")):
+        _need(t, n, torch.bfloat16)
+    for t, n in ((l1, "l1"), (l2, "l2")):
+        _need(t, n, torch.float32)
+    T, H, D = o1.shape
+    of = torch.empty(T, H, D, dtype=torch.float32, device=o1.device) if want_f32 else None
+    ob = torch.empty(T, H, D, dtype=torch.bfloat16, device=o1.device) if want_bf16 else None
+    l = torch.empty(H, T, dtype=torch.float32, device=o1.device)
+    rc = _lib.load().psf_lse_merge(_ptr(o1), _ptr(l1), _ptr(o2), _ptr(l2), _ptr(of), _ptr(ob), _ptr(l), T, H, D,
+                                   _stream())
+    check(rc)
+    return of, ob, l
+
+
+# ---------------------------------------------------------------------------
+# document-causal composition [fa4 page, document_causal_fa4_attention]
+
+def document_causal_attention(q, k, v, q_doc_ids, kv_doc_ids, q_global_start, scale, window=None):
+    """Causal per-document attention of a local query shard against global keys.
+
+    q [B, Hq, Lq, Dqk], k [B, Hkv, Sk, Dqk], v [B, Hkv, Sk, Dv] (or packed
+    [Lq, Hq, Dqk] / [Sk, Hkv, D] for a single row); doc ids [B, Lq] / [B, Sk]
+    int32, 1-based, 0 = padding. Returns (out, lse, segments) where padding
+    queries are zero with lse -inf, and segments = (cu_q, cu_k, dev_meta) for
+    the backward. No host synchronisation: the segment count stays on the device.
+    """
+    layout = "thd" if q.dim() == 3 else "bhsd"
+    if kv_doc_ids.dim() == 1:
+        kv_doc_ids = kv_doc_ids[None]
+    if q_doc_ids.dim() == 1:
+        q_doc_ids = q_doc_ids[None]
+    Lq = q.shape[0] if layout == "thd" else q.shape[2]
+    cu_q, cu_k, meta, _ = build_doc_segments(kv_doc_ids, Lq, q_global_start)
+    cap = cu_q.numel() - 1
+    out, lse = attn_varlen_fwd(q, k, v, cu_q, cu_k, -1, -1, scale, True, window, dev_meta=meta, layout=layout)
+    pad_fixup(out, lse, q_doc_ids, layout)
+    return out, lse, (cu_q, cu_k, meta)
+
+
+def document_causal_attention_backward(dout, q, k, v, out, lse, segments, scale, window=None):
+    """Backward of document_causal_attention from its out/lse -> (dq, dk, dv)."""
+    layout = "thd" if q.dim() == 3 else "bhsd"
+    cu_q, cu_k, meta = segments
+    return attn_varlen_bwd(dout, q, k, v, out, lse, cu_q, cu_k, -1, -1, scale, True, window, dev_meta=meta,
+                           layout=layout)

@@ -1,0 +1,434 @@
+// api.cu -- the C ABI declared in include/psf.h: argument validation, workspace
+// carving, tensor-map construction and kernel launches. Nothing here computes
+// attention; every step runs in the kernels of fwd.cu, bwd.cu and aux.cu.
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <stdlib.h>
+
+#include <mutex>
+#include <string>
+
+#include "../../include/psf.h"
+#include "bwd.cuh"
+#include "fwd.cuh"
+#include "launch.h"
+#include "tmap.h"
+
+using namespace psf;
+
+namespace {
+
+thread_local std::string g_last_error = "no error";
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* where) {
+  return fail(PSF_ECUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+uint64_t initial_wait_limit() {
+  const char* s = getenv("PSF_WAIT_LIMIT_NS");
+  if (s && *s) {
+    unsigned long long v = strtoull(s, nullptr, 10);
+    if (v > 0) return v;
+  }
+  return 2000000000ull;
+}
+uint64_t g_wait_limit_ns = initial_wait_limit();
+
+// Per-device status word the kernels record faults in (first fault wins).
+__device__ int g_psf_status;
+
+constexpr int kMaxDevices = 64;
+struct DeviceInfo {
+  bool ready = false;
+  int sms = 0;
+  int major = 0, minor = 0;
+  int* status = nullptr;
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+int device_info(DeviceInfo** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(PSF_EUNSUPPORTED, "device index %d out of range", dev);
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.ready) {
+    if ((e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute");
+    void* p = nullptr;
+    if ((e = cudaGetSymbolAddress(&p, g_psf_status)) != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress");
+    d.status = static_cast<int*>(p);
+    d.ready = true;
+  }
+  if (!(d.major == 10 && d.minor == 3))
+    return fail(PSF_EUNSUPPORTED, "device compute capability %d.%d; this build targets sm_103a", d.major, d.minor);
+  *out = &d;
+  return PSF_OK;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+bool supported_dims(int dqk, int dv) {
+  return (dqk == 64 && dv == 64) || (dqk == 128 && dv == 128) || (dqk == 192 && dv == 128) ||
+         (dqk == 512 && dv == 512);
+}
+
+// Element strides (batch, row, head) of a [rows, H, D] (THD) or [B, H, S, D]
+// (BHSD) tensor, and of the matching lse ([H, rows] or [B, H, S]).
+struct View {
+  int64_t sb, ss, sh;
+};
+View tensor_view(int layout, int S, int H, int D) {
+  if (layout == PSF_LAYOUT_THD) return View{(int64_t)S * H * D, (int64_t)H * D, (int64_t)D};
+  return View{(int64_t)H * S * D, (int64_t)D, (int64_t)S * D};
+}
+View lse_view(int layout, int S, int H) {
+  if (layout == PSF_LAYOUT_THD) return View{(int64_t)H * S, 1, (int64_t)S};
+  return View{(int64_t)H * S, 1, (int64_t)S};
+}
+
+struct FwdWorkspace {
+  int* n_items;
+  int* seg_prefix;
+  int2* items;
+  int item_cap;
+};
+size_t fwd_ws_layout(int64_t rows, int nseg, FwdWorkspace* w, void* base) {
+  const int64_t cap = (rows + kBM - 1) / kBM + nseg + 1;
+  size_t off = 256;
+  size_t prefix_off = off;
+  off += align256(sizeof(int) * (size_t)(nseg + 2));
+  size_t items_off = off;
+  off += align256(sizeof(int2) * (size_t)cap);
+  if (w && base) {
+    char* b = static_cast<char*>(base);
+    w->n_items = reinterpret_cast<int*>(b);
+    w->seg_prefix = reinterpret_cast<int*>(b + prefix_off);
+    w->items = reinterpret_cast<int2*>(b + items_off);
+    w->item_cap = (int)cap;
+  }
+  return off;
+}
+
+struct BwdWorkspace {
+  FwdWorkspace sched;
+  float* delta;
+  float* dq_acc;
+};
+size_t bwd_ws_layout(int64_t q_rows, int64_t k_rows, int nseg, int Hq, int Dqk, BwdWorkspace* w, void* base) {
+  size_t off = fwd_ws_layout(k_rows, nseg, w ? &w->sched : nullptr, base);
+  size_t delta_off = off;
+  off += align256(sizeof(float) * (size_t)Hq * (size_t)q_rows);
+  size_t acc_off = off;
+  off += align256(sizeof(float) * (size_t)q_rows * Hq * Dqk);
+  if (w && base) {
+    w->delta = reinterpret_cast<float*>(static_cast<char*>(base) + delta_off);
+    w->dq_acc = reinterpret_cast<float*>(static_cast<char*>(base) + acc_off);
+  }
+  return off;
+}
+
+int check_common(int layout, int B, int Sq, int Sk, int Hq, int Hkv, int Dqk, int Dv, float scale, int32_t window,
+                 int nseg) {
+  if (layout != PSF_LAYOUT_THD && layout != PSF_LAYOUT_BHSD) return fail(PSF_EINVAL, "unknown layout %d", layout);
+  if (B < 1 || Sq < 0 || Sk < 0) return fail(PSF_EINVAL, "bad sizes B=%d Sq=%d Sk=%d", B, Sq, Sk);
+  if (layout == PSF_LAYOUT_THD && B != 1) return fail(PSF_EINVAL, "packed THD layout takes B = 1 (got %d)", B);
+  if ((int64_t)B * Sq > 0x7fffffff || (int64_t)B * Sk > 0x7fffffff)
+    return fail(PSF_EINVAL, "more than 2^31 - 1 rows");
+  if (Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return fail(PSF_EINVAL, "Hq=%d must be a positive multiple of Hkv=%d", Hq, Hkv);
+  if (!supported_dims(Dqk, Dv))
+    return fail(PSF_EUNSUPPORTED, "head dims (Dqk=%d, Dv=%d) not in {(64,64),(128,128),(192,128),(512,512)}", Dqk, Dv);
+  if (window == 0) return fail(PSF_EINVAL, "window_left == 0 is undefined (use > 0, or < 0 for none)");
+  if (!(scale > 0.f) || !isfinite(scale)) return fail(PSF_EINVAL, "scale must be finite and > 0 (got %g)", (double)scale);
+  if (nseg < 0) return fail(PSF_EINVAL, "nseg < 0");
+  return PSF_OK;
+}
+
+int make_bf16_map(CUtensorMap* m, const void* base, int D, int S, int H, int B, const View& v, int box_d) {
+  int rc = make_tmap_4d(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, D, S, H, B, v.ss, v.sh, v.sb, box_d, kBM,
+                        CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc) return fail(PSF_ECUDA, "cuTensorMapEncodeTiled failed (%d) for a [%d,%d,%d,%d] view", rc, B, H, S, D);
+  return PSF_OK;
+}
+
+int attn_fwd_impl(const void* q, const void* k, const void* v, void* out, float* lse, const int32_t* cu_q,
+                  const int32_t* cu_k, const int32_t* dev_meta, int nseg, int max_q, int max_k, int layout, int B,
+                  int Sq, int Sk, int Hq, int Hkv, int Dqk, int Dv, float scale, int causal, int32_t window, void* ws,
+                  size_t ws_bytes, void* stream) {
+  int rc = check_common(layout, B, Sq, Sk, Hq, Hkv, Dqk, Dv, scale, window, nseg);
+  if (rc) return rc;
+  const int64_t q_rows = (int64_t)B * Sq, k_rows = (int64_t)B * Sk;
+  if (q_rows == 0) return PSF_OK;
+  if (!q || !out || !lse || (k_rows > 0 && (!k || !v))) return fail(PSF_EINVAL, "null tensor pointer");
+  if (!aligned16(q) || !aligned16(out) || (k_rows > 0 && (!aligned16(k) || !aligned16(v))))
+    return fail(PSF_EINVAL, "tensor base pointers must be 16-byte aligned");
+  if ((cu_q == nullptr) != (cu_k == nullptr)) return fail(PSF_EINVAL, "cu_q and cu_k must both be given");
+  const size_t need = fwd_ws_layout(q_rows, nseg, nullptr, nullptr);
+  if (!ws || ws_bytes < need) return fail(PSF_EWORKSPACE, "forward workspace needs %zu bytes (got %zu)", need, ws_bytes);
+  DeviceInfo* dev = nullptr;
+  if ((rc = device_info(&dev))) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+  FwdWorkspace w;
+  fwd_ws_layout(q_rows, nseg, &w, ws);
+  SegInfo g{cu_q, cu_k, dev_meta, nseg, max_q, max_k, B, Sq, Sk, causal ? 1 : 0, window > 0 ? (int)window : 0};
+  cudaError_t e = launch_schedule(g, 0, w.items, w.n_items, w.seg_prefix, w.item_cap, dev->status, st);
+  if (e != cudaSuccess) return cuda_fail(e, "schedule launch");
+  const View vq = tensor_view(layout, Sq, Hq, Dqk), vk = tensor_view(layout, Sk, Hkv, Dqk);
+  const View vv = tensor_view(layout, Sk, Hkv, Dv), vo = tensor_view(layout, Sq, Hq, Dv);
+  const View vl = lse_view(layout, Sq, Hq);
+  e = launch_fwd_tail(g, static_cast<__nv_bfloat16*>(out), vo.sb, vo.ss, vo.sh, lse, vl.sb, vl.sh, Hq, Dv, st);
+  if (e != cudaSuccess) return cuda_fail(e, "tail launch");
+
+  FwdParams p;
+  memset(&p, 0, sizeof(p));
+  if ((rc = make_bf16_map(&p.tm_q, q, Dqk, Sq, Hq, B, vq, 64))) return rc;
+  if (k_rows > 0) {
+    if ((rc = make_bf16_map(&p.tm_k, k, Dqk, Sk, Hkv, B, vk, 64))) return rc;
+    if ((rc = make_bf16_map(&p.tm_v, v, Dv, Sk, Hkv, B, vv, 64))) return rc;
+  }
+  p.seg = g;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.o_sb = vo.sb;
+  p.o_ss = vo.ss;
+  p.o_sh = vo.sh;
+  p.lse = lse;
+  p.l_sb = vl.sb;
+  p.l_sh = vl.sh;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.dv_parts = Dv == 512 ? 2 : 1;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.items = w.items;
+  p.n_items = w.n_items;
+  p.status = dev->status;
+  p.limit_ns = g_wait_limit_ns;
+  const int64_t max_work = (int64_t)w.item_cap * Hq * p.dv_parts;
+  const int grid = (int)(max_work < dev->sms ? max_work : dev->sms);
+  e = launch_fwd(p, Dqk, Dv / p.dv_parts, grid, st);
+  if (e != cudaSuccess) return cuda_fail(e, "forward launch");
+  return PSF_OK;
+}
+
+int attn_bwd_impl(const void* dout, const void* q, const void* k, const void* v, const void* out, const float* lse,
+                  void* dq, void* dk, void* dv, const int32_t* cu_q, const int32_t* cu_k, const int32_t* dev_meta,
+                  int nseg, int max_q, int max_k, int layout, int B, int Sq, int Sk, int Hq, int Hkv, int Dqk, int Dv,
+                  float scale, int causal, int32_t window, void* ws, size_t ws_bytes, void* stream) {
+  int rc = check_common(layout, B, Sq, Sk, Hq, Hkv, Dqk, Dv, scale, window, nseg);
+  if (rc) return rc;
+  if (bwd_smem_bytes(Dqk, Dv) < 0)
+    return fail(PSF_EUNSUPPORTED, "backward for (Dqk=%d, Dv=%d) is not built", Dqk, Dv);
+  const int64_t q_rows = (int64_t)B * Sq, k_rows = (int64_t)B * Sk;
+  if (q_rows == 0 && k_rows == 0) return PSF_OK;
+  const void* ptrs[] = {dout, q, out, dq};
+  for (const void* x : ptrs)
+    if (q_rows > 0 && (!x || !aligned16(x))) return fail(PSF_EINVAL, "null or unaligned query-side tensor");
+  const void* kptrs[] = {k, v, dk, dv};
+  for (const void* x : kptrs)
+    if (k_rows > 0 && (!x || !aligned16(x))) return fail(PSF_EINVAL, "null or unaligned key-side tensor");
+  if (q_rows > 0 && !lse) return fail(PSF_EINVAL, "null lse");
+  if ((cu_q == nullptr) != (cu_k == nullptr)) return fail(PSF_EINVAL, "cu_q and cu_k must both be given");
+  const size_t need = bwd_ws_layout(q_rows, k_rows, nseg, Hq, Dqk, nullptr, nullptr);
+  if (!ws || ws_bytes < need) return fail(PSF_EWORKSPACE, "backward workspace needs %zu bytes (got %zu)", need, ws_bytes);
+  DeviceInfo* dev = nullptr;
+  if ((rc = device_info(&dev))) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+  BwdWorkspace w;
+  bwd_ws_layout(q_rows, k_rows, nseg, Hq, Dqk, &w, ws);
+  SegInfo g{cu_q, cu_k, dev_meta, nseg, max_q, max_k, B, Sq, Sk, causal ? 1 : 0, window > 0 ? (int)window : 0};
+  const View vq = tensor_view(layout, Sq, Hq, Dqk), vk = tensor_view(layout, Sk, Hkv, Dqk);
+  const View vv = tensor_view(layout, Sk, Hkv, Dv), vo = tensor_view(layout, Sq, Hq, Dv);
+  const View vl = lse_view(layout, Sq, Hq);
+  cudaError_t e = launch_schedule(g, 1, w.sched.items, w.sched.n_items, w.sched.seg_prefix, w.sched.item_cap,
+                                  dev->status, st);
+  if (e != cudaSuccess) return cuda_fail(e, "schedule launch");
+  e = launch_bwd_pre(g, static_cast<const __nv_bfloat16*>(dout), static_cast<const __nv_bfloat16*>(out), vo.sb,
+                     vo.ss, vo.sh, w.delta, w.dq_acc, Hq, Dqk, Dv, static_cast<__nv_bfloat16*>(dk),
+                     static_cast<__nv_bfloat16*>(dv), vk.sb, vk.ss, vk.sh, vv.sb, vv.ss, vv.sh, Hkv, st);
+  if (e != cudaSuccess) return cuda_fail(e, "preprocess launch");
+
+  if (k_rows > 0) {
+    BwdParams p;
+    memset(&p, 0, sizeof(p));
+    if (q_rows > 0) {
+      if ((rc = make_bf16_map(&p.tm_q, q, Dqk, Sq, Hq, B, vq, 64))) return rc;
+      if ((rc = make_bf16_map(&p.tm_do, dout, Dv, Sq, Hq, B, vo, 64))) return rc;
+      const View va{(int64_t)Sq * Hq * Dqk, (int64_t)Hq * Dqk, (int64_t)Dqk};
+      int r2 = make_tmap_4d(&p.tm_dq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, w.dq_acc, Dqk, Sq, Hq, B, va.ss, va.sh,
+                            va.sb, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B);
+      if (r2) return fail(PSF_ECUDA, "cuTensorMapEncodeTiled failed (%d) for the dQ accumulator", r2);
+    }
+    if ((rc = make_bf16_map(&p.tm_k, k, Dqk, Sk, Hkv, B, vk, 64))) return rc;
+    if ((rc = make_bf16_map(&p.tm_v, v, Dv, Sk, Hkv, B, vv, 64))) return rc;
+    p.seg = g;
+    p.lse = lse;
+    p.l_sb = vl.sb;
+    p.l_sh = vl.sh;
+    p.delta = w.delta;
+    p.q_rows = (int)q_rows;
+    p.dk = static_cast<__nv_bfloat16*>(dk);
+    p.k_sb = vk.sb;
+    p.k_ss = vk.ss;
+    p.k_sh = vk.sh;
+    p.dv = static_cast<__nv_bfloat16*>(dv);
+    p.v_sb = vv.sb;
+    p.v_ss = vv.ss;
+    p.v_sh = vv.sh;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.scale = scale;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.items = w.sched.items;
+    p.n_items = w.sched.n_items;
+    p.status = dev->status;
+    p.limit_ns = g_wait_limit_ns;
+    const int64_t max_work = (int64_t)w.sched.item_cap * Hkv;
+    const int grid = (int)(max_work < dev->sms ? max_work : dev->sms);
+    e = launch_bwd(p, Dqk, Dv, grid, st);
+    if (e != cudaSuccess) return cuda_fail(e, "backward launch");
+  }
+  if (q_rows > 0) {
+    e = launch_dq_convert(w.dq_acc, static_cast<__nv_bfloat16*>(dq), B, Sq, Hq, Dqk, vq.sb, vq.ss, vq.sh, scale, st);
+    if (e != cudaSuccess) return cuda_fail(e, "dQ convert launch");
+  }
+  return PSF_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* psf_last_error(void) { return g_last_error.c_str(); }
+
+int psf_device_supported(void) {
+  DeviceInfo* d = nullptr;
+  return device_info(&d) == PSF_OK ? 1 : 0;
+}
+
+int psf_device_status(int clear) {
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+  int v = 0;
+  if ((e = cudaMemcpyFromSymbol(&v, g_psf_status, sizeof(int))) != cudaSuccess) return cuda_fail(e, "status read");
+  if (clear) {
+    int z = 0;
+    if ((e = cudaMemcpyToSymbol(g_psf_status, &z, sizeof(int))) != cudaSuccess) return cuda_fail(e, "status clear");
+  }
+  if (v == PSF_EDEVICE_ARGS) return fail(v, "kernel-side validation rejected the segment arrays");
+  if (v == PSF_ETIMEOUT) return fail(v, "a pipeline wait inside a kernel exceeded its limit");
+  return v;
+}
+
+void psf_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns = ns > 0 ? ns : 1; }
+
+size_t psf_attn_fwd_workspace_size(int64_t total_q_rows, int nseg) {
+  if (total_q_rows < 0 || nseg < 0) return 0;
+  return fwd_ws_layout(total_q_rows, nseg, nullptr, nullptr);
+}
+
+size_t psf_attn_bwd_workspace_size(int64_t total_q_rows, int64_t total_k_rows, int nseg, int Hq, int Dqk) {
+  if (total_q_rows < 0 || total_k_rows < 0 || nseg < 0 || Hq < 1 || Dqk < 1) return 0;
+  return bwd_ws_layout(total_q_rows, total_k_rows, nseg, Hq, Dqk, nullptr, nullptr);
+}
+
+int psf_attn_varlen_fwd(const void* q, const void* k, const void* v, void* out, float* lse, const int32_t* cu_q,
+                        const int32_t* cu_k, const int32_t* dev_meta, int nseg, int max_q, int max_k, int layout,
+                        int B, int Sq, int Sk, int Hq, int Hkv, int Dqk, int Dv, float scale, int causal,
+                        int32_t window_left, void* workspace, size_t ws_bytes, void* stream) {
+  if (!cu_q || !cu_k) return fail(PSF_EINVAL, "varlen calls need cu_q and cu_k");
+  return attn_fwd_impl(q, k, v, out, lse, cu_q, cu_k, dev_meta, nseg, max_q, max_k, layout, B, Sq, Sk, Hq, Hkv, Dqk,
+                       Dv, scale, causal, window_left, workspace, ws_bytes, stream);
+}
+
+int psf_attn_varlen_bwd(const void* dout, const void* q, const void* k, const void* v, const void* out,
+                        const float* lse, void* dq, void* dk, void* dv, const int32_t* cu_q, const int32_t* cu_k,
+                        const int32_t* dev_meta, int nseg, int max_q, int max_k, int layout, int B, int Sq, int Sk,
+                        int Hq, int Hkv, int Dqk, int Dv, float scale, int causal, int32_t window_left,
+                        void* workspace, size_t ws_bytes, void* stream) {
+  if (!cu_q || !cu_k) return fail(PSF_EINVAL, "varlen calls need cu_q and cu_k");
+  return attn_bwd_impl(dout, q, k, v, out, lse, dq, dk, dv, cu_q, cu_k, dev_meta, nseg, max_q, max_k, layout, B, Sq,
+                       Sk, Hq, Hkv, Dqk, Dv, scale, causal, window_left, workspace, ws_bytes, stream);
+}
+
+int psf_attn_dense_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq, int Hkv,
+                       int Nq, int Nk, int Dqk, int Dv, float scale, int causal, int32_t window_left,
+                       void* workspace, size_t ws_bytes, void* stream) {
+  return attn_fwd_impl(q, k, v, out, lse, nullptr, nullptr, nullptr, B, Nq, Nk, PSF_LAYOUT_BHSD, B, Nq, Nk, Hq, Hkv,
+                       Dqk, Dv, scale, causal, window_left, workspace, ws_bytes, stream);
+}
+
+int psf_attn_dense_bwd(const void* dout, const void* q, const void* k, const void* v, const void* out,
+                       const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Nq, int Nk,
+                       int Dqk, int Dv, float scale, int causal, int32_t window_left, void* workspace,
+                       size_t ws_bytes, void* stream) {
+  return attn_bwd_impl(dout, q, k, v, out, lse, dq, dk, dv, nullptr, nullptr, nullptr, B, Nq, Nk, PSF_LAYOUT_BHSD, B,
+                       Nq, Nk, Hq, Hkv, Dqk, Dv, scale, causal, window_left, workspace, ws_bytes, stream);
+}
+
+int psf_build_doc_segments(const int32_t* kv_doc_ids, int B, int Sk, int q_length, int q_global_start,
+                           int32_t* cu_q, int32_t* cu_k, int capacity, int32_t* dev_meta, uint8_t* seg_is_pad,
+                           void* stream) {
+  if (B < 1 || Sk < 0 || q_length < 0 || q_global_start < 0 || (int64_t)q_global_start + q_length > Sk)
+    return fail(PSF_EINVAL, "need B >= 1 and 0 <= q_global_start <= q_global_start + q_length <= Sk");
+  if ((int64_t)B * (Sk + 1) > 0x7fffffff) return fail(PSF_EINVAL, "too many rows");
+  if (!cu_q || !cu_k || !dev_meta || (Sk > 0 && !kv_doc_ids)) return fail(PSF_EINVAL, "null pointer");
+  if (capacity < 0) return fail(PSF_EINVAL, "capacity < 0");
+  DeviceInfo* dev = nullptr;
+  int rc = device_info(&dev);
+  if (rc) return rc;
+  cudaError_t e = launch_build_segments(kv_doc_ids, B, Sk, q_length, q_global_start, cu_q, cu_k, capacity, dev_meta,
+                                        seg_is_pad, dev->status, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PSF_OK : cuda_fail(e, "builder launch");
+}
+
+int psf_pad_fixup(void* out, float* lse, const int32_t* q_doc_ids, int layout, int B, int Lq, int Hq, int Dv,
+                  void* stream) {
+  if (layout != PSF_LAYOUT_THD && layout != PSF_LAYOUT_BHSD) return fail(PSF_EINVAL, "unknown layout");
+  if (B < 1 || Lq < 0 || Hq < 1 || Dv < 8 || Dv % 8) return fail(PSF_EINVAL, "bad sizes");
+  if (layout == PSF_LAYOUT_THD && B != 1) return fail(PSF_EINVAL, "packed THD layout takes B = 1");
+  if (Lq == 0) return PSF_OK;
+  if (!out || !lse || !q_doc_ids || !aligned16(out)) return fail(PSF_EINVAL, "null or unaligned pointer");
+  DeviceInfo* dev = nullptr;
+  int rc = device_info(&dev);
+  if (rc) return rc;
+  const View vo = tensor_view(layout, Lq, Hq, Dv), vl = lse_view(layout, Lq, Hq);
+  cudaError_t e = launch_pad_fixup(static_cast<__nv_bfloat16*>(out), lse, q_doc_ids, B, Lq, Hq, Dv, vo.sb, vo.ss,
+                                   vo.sh, vl.sb, vl.sh, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PSF_OK : cuda_fail(e, "pad fixup launch");
+}
+
+int psf_lse_merge(const void* o1, const float* l1, const void* o2, const float* l2, float* o_f32, void* o_bf16,
+                  float* l, int T, int H, int D, void* stream) {
+  if (T < 0 || H < 1 || D < 8 || D % 8) return fail(PSF_EINVAL, "bad sizes");
+  if (T == 0) return PSF_OK;
+  if (!o1 || !o2 || !l1 || !l2 || !l || (!o_f32 && !o_bf16)) return fail(PSF_EINVAL, "null pointer");
+  if (!aligned16(o1) || !aligned16(o2) || (o_f32 && !aligned16(o_f32)) || (o_bf16 && !aligned16(o_bf16)))
+    return fail(PSF_EINVAL, "unaligned pointer");
+  DeviceInfo* dev = nullptr;
+  int rc = device_info(&dev);
+  if (rc) return rc;
+  cudaError_t e = launch_lse_merge(static_cast<const __nv_bfloat16*>(o1), l1, static_cast<const __nv_bfloat16*>(o2),
+                                   l2, o_f32, static_cast<__nv_bfloat16*>(o_bf16), l, T, H, D,
+                                   static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PSF_OK : cuda_fail(e, "merge launch");
+}
+
+}  // extern "C"

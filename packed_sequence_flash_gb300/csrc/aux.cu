@@ -1,0 +1,415 @@
+// aux.cu -- memory-bound kernels around the attention kernels: the tile
+// schedulers, the doc-id segment builder, pad fixup, lse merge, the backward
+// preprocess (Delta = rowsum(dO * O), zeroed accumulators) and the dQ convert.
+#include <math_constants.h>
+
+#include "launch.h"
+
+namespace psf {
+
+namespace {
+
+constexpr int kScanThreads = 1024;
+constexpr int kBuckets = 1024;
+
+// Exclusive block-wide prefix sum over kScanThreads threads; *total gets the sum.
+__device__ int block_excl_scan(int v, int* total) {
+  __shared__ int warp_tot[32];
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_tot[wid] = x;
+  __syncthreads();
+  if (wid == 0) {
+    int t = warp_tot[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, t, o);
+      if (lane >= o) t += y;
+    }
+    warp_tot[lane] = t;
+  }
+  __syncthreads();
+  int res = (wid > 0 ? warp_tot[wid - 1] : 0) + x - v;
+  *total = warp_tot[31];
+  __syncthreads();
+  return res;
+}
+
+__device__ int block_max(int v) {
+  __shared__ int warp_max[32];
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+  if (lane == 0) warp_max[wid] = v;
+  __syncthreads();
+  int r = warp_max[0];
+  for (int i = 1; i < 32; ++i) r = max(r, warp_max[i]);
+  __syncthreads();
+  return r;
+}
+
+// Largest s in [0, nseg) with prefix[s] <= x.
+__device__ int find_segment(const int* prefix, int nseg, int x) {
+  int lo = 0, hi = nseg - 1;
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if (prefix[mid] <= x)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  return lo;
+}
+
+__device__ int tile_cost(const SegInfo& g, int s, int t, int over_keys) {
+  int m = cu_q_at(g, s + 1) - cu_q_at(g, s);
+  int n = cu_k_at(g, s + 1) - cu_k_at(g, s);
+  int lo, hi;
+  if (over_keys) {
+    q_range_for_kv_tile(m, n, t * kBN, g.causal, g.window, lo, hi);
+    return hi > lo ? ceil_div(hi, kBM) - lo / kBM : 0;
+  }
+  kv_range_for_q_tile(m, n, t * kBM, g.causal, g.window, lo, hi);
+  return hi > lo ? ceil_div(hi, kBN) - lo / kBN : 0;
+}
+
+__global__ void __launch_bounds__(kScanThreads) schedule_kernel(SegInfo g, int over_keys, int2* items, int* n_items,
+                                                                int* seg_prefix, int item_cap, int* status) {
+  __shared__ int hist[kBuckets];
+  __shared__ int start[kBuckets];
+  __shared__ int bad;
+  const int tid = threadIdx.x;
+  const int nseg = seg_count(g);
+  const int max_q = g.dev_meta ? g.dev_meta[1] : g.max_q;
+  const int max_k = g.dev_meta ? g.dev_meta[2] : g.max_k;
+  const int Tq = g.B * g.Sq, Tk = g.B * g.Sk;
+  hist[tid] = 0;
+  if (tid == 0) bad = (g.cu_q && nseg >= 0 && (g.cu_q[0] != 0 || g.cu_k[0] != 0)) ? 1 : 0;
+  __syncthreads();
+  int carry = 0;
+  for (int base = 0; base < nseg; base += kScanThreads) {
+    const int s = base + tid;
+    int cnt = 0;
+    if (s < nseg) {
+      const int q0 = cu_q_at(g, s), q1 = cu_q_at(g, s + 1);
+      const int k0 = cu_k_at(g, s), k1 = cu_k_at(g, s + 1);
+      const int m = q1 - q0, n = k1 - k0;
+      bool ok = m >= 0 && n >= 0 && q1 <= Tq && k1 <= Tk && (max_q < 0 || m <= max_q) && (max_k < 0 || n <= max_k);
+      if (ok && g.B > 1)
+        ok = (m == 0 || q0 / g.Sq == (q1 - 1) / g.Sq) && (n == 0 || k0 / g.Sk == (k1 - 1) / g.Sk);
+      if (!ok) bad = 1;
+      else cnt = over_keys ? ceil_div(n, kBN) : ceil_div(m, kBM);
+    }
+    int tot;
+    const int ex = block_excl_scan(cnt, &tot);
+    if (s < nseg) seg_prefix[s] = carry + ex;
+    carry += tot;
+  }
+  if (tid == 0) seg_prefix[nseg] = carry;
+  __syncthreads();
+  if (bad || carry > item_cap) {
+    if (tid == 0) {
+      record_status(status, kStatusDeviceArgs);
+      *n_items = 0;
+    }
+    return;
+  }
+  for (int x = tid; x < carry; x += kScanThreads) {
+    const int s = find_segment(seg_prefix, nseg, x);
+    const int c = tile_cost(g, s, x - seg_prefix[s], over_keys);
+    atomicAdd(&hist[min(c, kBuckets - 1)], 1);
+  }
+  __syncthreads();
+  // Heaviest bucket first: start[b] = number of items in buckets above b.
+  int tot;
+  const int rb = kBuckets - 1 - tid;
+  const int ex = block_excl_scan(hist[rb], &tot);
+  start[rb] = ex;
+  hist[rb] = 0;
+  __syncthreads();
+  for (int x = tid; x < carry; x += kScanThreads) {
+    const int s = find_segment(seg_prefix, nseg, x);
+    const int t = x - seg_prefix[s];
+    const int b = min(tile_cost(g, s, t, over_keys), kBuckets - 1);
+    const int pos = start[b] + atomicAdd(&hist[b], 1);
+    items[pos] = make_int2(s, t);
+  }
+  if (tid == 0) *n_items = carry;
+}
+
+__global__ void fwd_tail_kernel(SegInfo g, __nv_bfloat16* out, int64_t o_sb, int64_t o_ss, int64_t o_sh, float* lse,
+                                int64_t l_sb, int64_t l_sh, int Hq, int Dv) {
+  const int nseg = seg_count(g);
+  const int first = cu_q_at(g, nseg);
+  const int64_t rows = (int64_t)g.B * g.Sq - first;
+  if (rows <= 0) return;
+  const int groups = Dv / 8;
+  const int64_t total = rows * Hq * groups;
+  for (int64_t x = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; x < total; x += (int64_t)gridDim.x * blockDim.x) {
+    const int gidx = (int)(x % groups);
+    const int64_t rh = x / groups;
+    const int h = (int)(rh % Hq);
+    const int f = first + (int)(rh / Hq);
+    const int b = f / g.Sq, s = f - b * g.Sq;
+    reinterpret_cast<uint4*>(out + b * o_sb + (int64_t)s * o_ss + h * o_sh)[gidx] = make_uint4(0, 0, 0, 0);
+    if (gidx == 0) lse[b * l_sb + h * l_sh + s] = -CUDART_INF_F;
+  }
+}
+
+// Builder: a new piece starts where the id changes, at position 0, and at the
+// end of the query shard; each piece is one segment.
+constexpr int kBuildPer = 8;
+__global__ void __launch_bounds__(kScanThreads) build_segments_kernel(const int32_t* ids, int B, int Sk, int Lq,
+                                                                      int q0, int32_t* cu_q, int32_t* cu_k,
+                                                                      int capacity, int32_t* meta, uint8_t* is_pad,
+                                                                      int* status) {
+  const int tid = threadIdx.x;
+  const int q_end = q0 + Lq;
+  int offset = 0;
+  for (int b = 0; b < B; ++b) {
+    const int32_t* row = ids + (size_t)b * Sk;
+    for (int base = 0; base < Sk; base += kScanThreads * kBuildPer) {
+      const int j0 = base + tid * kBuildPer;
+      uint32_t flags = 0;
+      int cnt = 0;
+#pragma unroll
+      for (int e = 0; e < kBuildPer; ++e) {
+        const int j = j0 + e;
+        if (j < Sk && (j == 0 || j == q_end || row[j] != row[j - 1])) {
+          flags |= 1u << e;
+          ++cnt;
+        }
+      }
+      int tot;
+      int idx = offset + block_excl_scan(cnt, &tot);
+#pragma unroll
+      for (int e = 0; e < kBuildPer; ++e) {
+        if (flags & (1u << e)) {
+          const int j = j0 + e;
+          if (idx < capacity) {
+            cu_k[idx] = b * Sk + j;
+            cu_q[idx] = b * Lq + min(max(j - q0, 0), Lq);
+            if (is_pad) is_pad[idx] = row[j] == 0 ? 1 : 0;
+          }
+          ++idx;
+        }
+      }
+      offset += tot;
+    }
+  }
+  const int nseg = offset;
+  if (nseg > capacity) {
+    if (tid == 0) {
+      record_status(status, kStatusDeviceArgs);
+      meta[0] = meta[1] = meta[2] = 0;
+    }
+    return;
+  }
+  if (tid == 0) {
+    cu_q[nseg] = B * Lq;
+    cu_k[nseg] = B * Sk;
+  }
+  __syncthreads();
+  int mq = 0, mk = 0;
+  for (int i = tid; i < nseg; i += kScanThreads) {
+    mq = max(mq, cu_q[i + 1] - cu_q[i]);
+    mk = max(mk, cu_k[i + 1] - cu_k[i]);
+  }
+  mq = block_max(mq);
+  mk = block_max(mk);
+  if (tid == 0) {
+    meta[0] = nseg;
+    meta[1] = mq;
+    meta[2] = mk;
+  }
+}
+
+__global__ void pad_fixup_kernel(__nv_bfloat16* out, float* lse, const int32_t* qids, int B, int Lq, int Hq, int Dv,
+                                 int64_t o_sb, int64_t o_ss, int64_t o_sh, int64_t l_sb, int64_t l_sh) {
+  const int groups = Dv / 8;
+  const int64_t total = (int64_t)B * Lq * Hq * groups;
+  for (int64_t x = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; x < total; x += (int64_t)gridDim.x * blockDim.x) {
+    const int gidx = (int)(x % groups);
+    const int64_t rh = x / groups;
+    const int h = (int)(rh % Hq);
+    const int64_t f = rh / Hq;
+    if (qids[f] != 0) continue;
+    const int b = (int)(f / Lq), s = (int)(f - (int64_t)b * Lq);
+    reinterpret_cast<uint4*>(out + b * o_sb + (int64_t)s * o_ss + h * o_sh)[gidx] = make_uint4(0, 0, 0, 0);
+    if (gidx == 0) lse[b * l_sb + h * l_sh + s] = -CUDART_INF_F;
+  }
+}
+
+__global__ void lse_merge_kernel(const __nv_bfloat16* o1, const float* l1, const __nv_bfloat16* o2, const float* l2,
+                                 float* of, __nv_bfloat16* ob, float* l, int T, int H, int D) {
+  const int groups = D / 8;
+  const int64_t total = (int64_t)T * H * groups;
+  for (int64_t x = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; x < total; x += (int64_t)gridDim.x * blockDim.x) {
+    const int gidx = (int)(x % groups);
+    const int64_t th = x / groups;
+    const int h = (int)(th % H);
+    const int t = (int)(th / H);
+    const float a = l1[(int64_t)h * T + t], c = l2[(int64_t)h * T + t];
+    const float mx = fmaxf(a, c);
+    const float lm = mx == -CUDART_INF_F ? -CUDART_INF_F : mx + logf(expf(a - mx) + expf(c - mx));
+    const float wa = lm == -CUDART_INF_F ? 0.f : expf(a - lm);
+    const float wc = lm == -CUDART_INF_F ? 0.f : expf(c - lm);
+    const int64_t off = th * D + gidx * 8;
+    uint4 ua = *reinterpret_cast<const uint4*>(o1 + off);
+    uint4 uc = *reinterpret_cast<const uint4*>(o2 + off);
+    const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&ua);
+    const __nv_bfloat162* pc = reinterpret_cast<const __nv_bfloat162*>(&uc);
+    float r[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float2 fa = __bfloat1622float2(pa[j]), fc = __bfloat1622float2(pc[j]);
+      r[2 * j] = wa * fa.x + wc * fc.x;
+      r[2 * j + 1] = wa * fa.y + wc * fc.y;
+    }
+    if (of) {
+      reinterpret_cast<float4*>(of + off)[0] = make_float4(r[0], r[1], r[2], r[3]);
+      reinterpret_cast<float4*>(of + off)[1] = make_float4(r[4], r[5], r[6], r[7]);
+    }
+    if (ob)
+      *reinterpret_cast<uint4*>(ob + off) =
+          make_uint4(pack_bf16x2(r[0], r[1]), pack_bf16x2(r[2], r[3]), pack_bf16x2(r[4], r[5]), pack_bf16x2(r[6], r[7]));
+    if (gidx == 0) l[(int64_t)h * T + t] = lm;
+  }
+}
+
+// One warp per (row, head): Delta = sum_d dO * O in fp32. Then grid-stride
+// zeroing of the dQ accumulator and of dK / dV rows no segment covers.
+__global__ void bwd_pre_kernel(SegInfo g, const __nv_bfloat16* dout, const __nv_bfloat16* out, int64_t o_sb,
+                               int64_t o_ss, int64_t o_sh, float* delta, float* dq_acc, int Hq, int Dqk, int Dv,
+                               __nv_bfloat16* dk, __nv_bfloat16* dv, int64_t k_sb, int64_t k_ss, int64_t k_sh,
+                               int64_t v_sb, int64_t v_ss, int64_t v_sh, int Hkv) {
+  const int64_t rows = (int64_t)g.B * g.Sq;
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x / 32);
+  for (int64_t wrk = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) / 32; wrk < rows * Hq; wrk += nwarps) {
+    const int h = (int)(wrk % Hq);
+    const int64_t f = wrk / Hq;
+    const int b = (int)(f / g.Sq), s = (int)(f - (int64_t)b * g.Sq);
+    const int64_t off = b * o_sb + (int64_t)s * o_ss + h * o_sh;
+    float acc = 0.f;
+    for (int d = lane * 8; d < Dv; d += 256) {
+      uint4 ug = *reinterpret_cast<const uint4*>(dout + off + d);
+      uint4 uo = *reinterpret_cast<const uint4*>(out + off + d);
+      const __nv_bfloat162* pg = reinterpret_cast<const __nv_bfloat162*>(&ug);
+      const __nv_bfloat162* po = reinterpret_cast<const __nv_bfloat162*>(&uo);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        float2 a = __bfloat1622float2(pg[j]), c = __bfloat1622float2(po[j]);
+        acc = fmaf(a.x, c.x, acc);
+        acc = fmaf(a.y, c.y, acc);
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) delta[(int64_t)h * rows + f] = acc;
+  }
+  const int64_t tid = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+  const int64_t nthr = (int64_t)gridDim.x * blockDim.x;
+  const int64_t n4 = rows * Hq * Dqk / 4;
+  for (int64_t x = tid; x < n4; x += nthr) reinterpret_cast<float4*>(dq_acc)[x] = make_float4(0.f, 0.f, 0.f, 0.f);
+  const int first = cu_k_at(g, seg_count(g));
+  const int64_t krows = (int64_t)g.B * g.Sk - first;
+  if (krows > 0) {
+    const int gk = Dqk / 8, gv = Dv / 8;
+    const int64_t nk = krows * Hkv * (gk + gv);
+    for (int64_t x = tid; x < nk; x += nthr) {
+      int64_t rh = x / (gk + gv);
+      int gidx = (int)(x - rh * (gk + gv));
+      const int h = (int)(rh % Hkv);
+      const int f = first + (int)(rh / Hkv);
+      const int b = f / g.Sk, s = f - b * g.Sk;
+      if (gidx < gk)
+        reinterpret_cast<uint4*>(dk + b * k_sb + (int64_t)s * k_ss + h * k_sh)[gidx] = make_uint4(0, 0, 0, 0);
+      else
+        reinterpret_cast<uint4*>(dv + b * v_sb + (int64_t)s * v_ss + h * v_sh)[gidx - gk] = make_uint4(0, 0, 0, 0);
+    }
+  }
+}
+
+__global__ void dq_convert_kernel(const float* dq_acc, __nv_bfloat16* dq, int B, int Sq, int Hq, int Dqk,
+                                  int64_t q_sb, int64_t q_ss, int64_t q_sh, float scale) {
+  const int groups = Dqk / 8;
+  const int64_t total = (int64_t)B * Sq * Hq * groups;
+  for (int64_t x = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; x < total; x += (int64_t)gridDim.x * blockDim.x) {
+    const int gidx = (int)(x % groups);
+    const int64_t rh = x / groups;
+    const int h = (int)(rh % Hq);
+    const int64_t f = rh / Hq;
+    const int b = (int)(f / Sq), s = (int)(f - (int64_t)b * Sq);
+    const float4 a = reinterpret_cast<const float4*>(dq_acc + rh * Dqk)[2 * gidx];
+    const float4 c = reinterpret_cast<const float4*>(dq_acc + rh * Dqk)[2 * gidx + 1];
+    reinterpret_cast<uint4*>(dq + b * q_sb + (int64_t)s * q_ss + h * q_sh)[gidx] =
+        make_uint4(pack_bf16x2(a.x * scale, a.y * scale), pack_bf16x2(a.z * scale, a.w * scale),
+                   pack_bf16x2(c.x * scale, c.y * scale), pack_bf16x2(c.z * scale, c.w * scale));
+  }
+}
+
+int grid_for(int64_t work, int threads) {
+  int64_t g = (work + threads - 1) / threads;
+  if (g < 1) g = 1;
+  if (g > 152 * 16) g = 152 * 16;
+  return (int)g;
+}
+
+}  // namespace
+
+cudaError_t launch_schedule(const SegInfo& g, int over_keys, int2* items, int* n_items, int* seg_prefix, int item_cap,
+                            int* status, cudaStream_t st) {
+  schedule_kernel<<<1, kScanThreads, 0, st>>>(g, over_keys, items, n_items, seg_prefix, item_cap, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fwd_tail(const SegInfo& g, __nv_bfloat16* out, int64_t o_sb, int64_t o_ss, int64_t o_sh, float* lse,
+                            int64_t l_sb, int64_t l_sh, int Hq, int Dv, cudaStream_t st) {
+  fwd_tail_kernel<<<grid_for((int64_t)g.B * g.Sq * Hq * (Dv / 8), 256), 256, 0, st>>>(g, out, o_sb, o_ss, o_sh, lse,
+                                                                                     l_sb, l_sh, Hq, Dv);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_build_segments(const int32_t* ids, int B, int Sk, int Lq, int q0, int32_t* cu_q, int32_t* cu_k,
+                                  int capacity, int32_t* meta, uint8_t* seg_is_pad, int* status, cudaStream_t st) {
+  build_segments_kernel<<<1, kScanThreads, 0, st>>>(ids, B, Sk, Lq, q0, cu_q, cu_k, capacity, meta, seg_is_pad,
+                                                    status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pad_fixup(__nv_bfloat16* out, float* lse, const int32_t* qids, int B, int Lq, int Hq, int Dv,
+                             int64_t o_sb, int64_t o_ss, int64_t o_sh, int64_t l_sb, int64_t l_sh, cudaStream_t st) {
+  pad_fixup_kernel<<<grid_for((int64_t)B * Lq * Hq * (Dv / 8), 256), 256, 0, st>>>(out, lse, qids, B, Lq, Hq, Dv, o_sb,
+                                                                                  o_ss, o_sh, l_sb, l_sh);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_lse_merge(const __nv_bfloat16* o1, const float* l1, const __nv_bfloat16* o2, const float* l2,
+                             float* of, __nv_bfloat16* ob, float* l, int T, int H, int D, cudaStream_t st) {
+  lse_merge_kernel<<<grid_for((int64_t)T * H * (D / 8), 256), 256, 0, st>>>(o1, l1, o2, l2, of, ob, l, T, H, D);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_pre(const SegInfo& g, const __nv_bfloat16* dout, const __nv_bfloat16* out, int64_t o_sb,
+                           int64_t o_ss, int64_t o_sh, float* delta, float* dq_acc, int Hq, int Dqk, int Dv,
+                           __nv_bfloat16* dk, __nv_bfloat16* dv, int64_t k_sb, int64_t k_ss, int64_t k_sh,
+                           int64_t v_sb, int64_t v_ss, int64_t v_sh, int Hkv, cudaStream_t st) {
+  bwd_pre_kernel<<<grid_for((int64_t)g.B * g.Sq * Hq * 32, 256), 256, 0, st>>>(
+      g, dout, out, o_sb, o_ss, o_sh, delta, dq_acc, Hq, Dqk, Dv, dk, dv, k_sb, k_ss, k_sh, v_sb, v_ss, v_sh, Hkv);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dq_convert(const float* dq_acc, __nv_bfloat16* dq, int B, int Sq, int Hq, int Dqk, int64_t q_sb,
+                              int64_t q_ss, int64_t q_sh, float scale, cudaStream_t st) {
+  dq_convert_kernel<<<grid_for((int64_t)B * Sq * Hq * (Dqk / 8), 256), 256, 0, st>>>(dq_acc, dq, B, Sq, Hq, Dqk, q_sb,
+                                                                                    q_ss, q_sh, scale);
+  return cudaGetLastError();
+}
+
+}  // namespace psf

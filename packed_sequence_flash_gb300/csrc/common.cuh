@@ -1,0 +1,96 @@
+// common.cuh -- parameter blocks, bounded pipeline waits and segment/tile
+// arithmetic shared by the attention kernels.
+#pragma once
+
+#include <stdint.h>
+
+#include "ptx.cuh"
+
+namespace psf {
+
+constexpr int kBM = 128;  // query rows per tile (TMEM lanes)
+constexpr int kBN = 128;  // key rows per tile
+constexpr int kChunkBytes = 16384;  // one TMA box: 128 rows x 64 bf16, 128-byte swizzled
+
+// Status codes mirrored from the public header.
+constexpr int kStatusDeviceArgs = -4;
+constexpr int kStatusTimeout = -5;
+
+// Segment description as the kernels see it. Rows are flattened (b * S + s);
+// a null cu array means "one segment per batch row" (dense attention).
+struct SegInfo {
+  const int32_t* cu_q;
+  const int32_t* cu_k;
+  const int32_t* dev_meta;  // nullable {nseg, max_q, max_k}
+  int nseg;                 // count, or the capacity when dev_meta is given
+  int max_q, max_k;
+  int B, Sq, Sk;            // batches and rows per batch of the q / k tensors
+  int causal;
+  int window;               // > 0: left window counting the current token
+};
+
+__device__ __forceinline__ int seg_count(const SegInfo& g) {
+  if (!g.dev_meta) return g.nseg;
+  int n = g.dev_meta[0];
+  return n < 0 ? 0 : (n > g.nseg ? g.nseg : n);
+}
+__device__ __forceinline__ int cu_q_at(const SegInfo& g, int s) { return g.cu_q ? g.cu_q[s] : s * g.Sq; }
+__device__ __forceinline__ int cu_k_at(const SegInfo& g, int s) { return g.cu_k ? g.cu_k[s] : s * g.Sk; }
+
+// Keys [lo, hi) (segment-local) that some query of rows [i0, i0 + kBM) can see.
+__device__ __forceinline__ void kv_range_for_q_tile(int m, int n, int i0, int causal, int window, int& lo, int& hi) {
+  int i1 = min(i0 + kBM, m);
+  int delta = n - m;
+  hi = causal ? min(n, i1 + delta) : n;
+  lo = window > 0 ? max(0, i0 + delta - window + 1) : 0;
+  if (hi < lo) hi = lo;
+}
+// Queries [lo, hi) (segment-local) that some key of rows [j0, j0 + kBN) is seen by.
+__device__ __forceinline__ void q_range_for_kv_tile(int m, int n, int j0, int causal, int window, int& lo, int& hi) {
+  int j1 = min(j0 + kBN, n);
+  int delta = n - m;
+  lo = causal ? max(0, j0 - delta) : 0;
+  hi = window > 0 ? min(m, j1 - 1 - delta + window) : m;
+  if (hi < lo) hi = lo;
+}
+__device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// Pipeline control: every wait is bounded. A wait that runs out records
+// kStatusTimeout, raises the CTA-wide abort flag and returns false; the other
+// roles notice the flag at their next wait and wind down, so the CTA always
+// reaches its final barrier, drains its own asynchronous work and frees TMEM.
+struct Ctl {
+  int* status;
+  uint64_t limit_ns;
+  volatile int* abort_flag;  // shared memory
+};
+
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, const Ctl& c) {
+  if (mbar_test(bar, parity)) return true;
+  uint64_t t0 = globaltimer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 128; ++i)
+      if (mbar_test(bar, parity)) return true;
+    if (*c.abort_flag) return false;
+    if (globaltimer_ns() - t0 > c.limit_ns) {
+      atomicCAS(c.status, 0, kStatusTimeout);
+      *c.abort_flag = 1;
+      return false;
+    }
+  }
+}
+// Drain-only wait used while winding down after an abort: bounded, no flag.
+__device__ __forceinline__ void wait_bar_drain(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  uint64_t t0 = globaltimer_ns();
+  while (!mbar_test(bar, parity))
+    if (globaltimer_ns() - t0 > limit_ns) return;
+}
+
+__device__ __forceinline__ void record_status(int* status, int code) { atomicCAS(status, 0, code); }
+
+// Byte offset of 16-byte granule g (0..7) of row r inside a 128-byte-swizzled
+// chunk of 128-byte rows (the layout TMA writes with CU_TENSOR_MAP_SWIZZLE_128B).
+__device__ __forceinline__ uint32_t sw128_offset(int r, int g) { return (uint32_t)(r * 128 + ((g ^ (r & 7)) << 4)); }
+
+}  // namespace psf

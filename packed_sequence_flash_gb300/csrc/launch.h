@@ -1,0 +1,42 @@
+// launch.h -- host-side launchers shared between the translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace psf {
+
+struct FwdParams;
+struct BwdParams;
+
+// Heaviest-first work list over query tiles (over_keys = 0) or key tiles
+// (over_keys = 1) of every segment; validates the segment arrays.
+cudaError_t launch_schedule(const SegInfo& g, int over_keys, int2* items, int* n_items, int* seg_prefix,
+                            int item_cap, int* status, cudaStream_t st);
+// out = 0 and lse = -inf for query rows at or past cu_q[nseg].
+cudaError_t launch_fwd_tail(const SegInfo& g, __nv_bfloat16* out, int64_t o_sb, int64_t o_ss, int64_t o_sh, float* lse,
+                            int64_t l_sb, int64_t l_sh, int Hq, int Dv, cudaStream_t st);
+cudaError_t launch_fwd(const FwdParams& p, int dqk, int dvc, int grid, cudaStream_t st);
+cudaError_t launch_bwd(const BwdParams& p, int dqk, int dv, int grid, cudaStream_t st);
+int fwd_smem_bytes(int dqk, int dvc);
+int bwd_smem_bytes(int dqk, int dv);
+
+cudaError_t launch_build_segments(const int32_t* ids, int B, int Sk, int Lq, int q0, int32_t* cu_q, int32_t* cu_k,
+                                  int capacity, int32_t* meta, uint8_t* seg_is_pad, int* status, cudaStream_t st);
+cudaError_t launch_pad_fixup(__nv_bfloat16* out, float* lse, const int32_t* qids, int B, int Lq, int Hq, int Dv,
+                             int64_t o_sb, int64_t o_ss, int64_t o_sh, int64_t l_sb, int64_t l_sh, cudaStream_t st);
+cudaError_t launch_lse_merge(const __nv_bfloat16* o1, const float* l1, const __nv_bfloat16* o2, const float* l2,
+                             float* of, __nv_bfloat16* ob, float* l, int T, int H, int D, cudaStream_t st);
+// Delta = rowsum(dO * O) (fp32, [Hq][rows]); zero the fp32 dQ accumulator; zero
+// dK / dV rows at or past cu_k[nseg].
+cudaError_t launch_bwd_pre(const SegInfo& g, const __nv_bfloat16* dout, const __nv_bfloat16* out, int64_t o_sb,
+                           int64_t o_ss, int64_t o_sh, float* delta, float* dq_acc, int Hq, int Dqk, int Dv,
+                           __nv_bfloat16* dk, __nv_bfloat16* dv, int64_t k_sb, int64_t k_ss, int64_t k_sh,
+                           int64_t v_sb, int64_t v_ss, int64_t v_sh, int Hkv, cudaStream_t st);
+// dQ = scale * dQacc in bf16 with q's layout.
+cudaError_t launch_dq_convert(const float* dq_acc, __nv_bfloat16* dq, int B, int Sq, int Hq, int Dqk, int64_t q_sb,
+                              int64_t q_ss, int64_t q_sh, float scale, cudaStream_t st);
+
+}  // namespace psf

@@ -1,0 +1,199 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on the
+same seeded inputs, at sizes that span several 128-row tiles and ragged tails.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import packed_sequence_flash_gb300 as psf
+from packed_sequence_flash_gb300 import inputs
+from gpu_helpers import assert_fwd, assert_grads, cuda, doc_case
+
+pytestmark = pytest.mark.gpu
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _build_gpu(ids, Lq, q0):
+    ids_t = torch.as_tensor(np.asarray(ids, np.int32)).to("cuda")
+    cu_q, cu_k, meta, pad = psf.build_doc_segments(ids_t, Lq, q0, want_pad_flags=True)
+    m = meta.cpu().tolist()
+    n = m[0]
+    return cu_q[: n + 1].cpu().numpy(), cu_k[: n + 1].cpu().numpy(), m[1], m[2], pad[:n].cpu().numpy()
+
+
+# ---------------------------------------------------------------- builder (bit-exact)
+
+def test_builder_golden_examples_bit_exact():
+    with open(os.path.join(GOLDEN, "builder_examples.json")) as fh:
+        cases = json.load(fh)["cases"]
+    for c in cases:
+        cu_q, cu_k, mq, mk, pad = _build_gpu(c["doc_ids"], c["q_length"], c["q_global_start"])
+        assert cu_q.tolist() == c["cu_q"] and cu_k.tolist() == c["cu_k"], c
+        assert (mq, mk) == (c["max_q"], c["max_k"])
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_builder_random_maps_bit_exact(seed):
+    r = np.random.default_rng(seed)
+    B = int(r.integers(1, 4))
+    S = int(r.integers(1, 20000))
+    ids = np.zeros((B, S), np.int32)
+    for b in range(B):
+        pos, d = 0, 1
+        while pos < S:
+            n = int(r.integers(1, 3000))
+            ids[b, pos:pos + n] = 0 if r.random() < 0.2 else d
+            d += 1
+            pos += n
+    q0 = int(r.integers(0, S))
+    Lq = int(r.integers(0, S - q0 + 1))
+    got = _build_gpu(ids, Lq, q0)
+    ref = oracle.build_segments(ids, Lq, q0)
+    np.testing.assert_array_equal(got[0], ref[0])
+    np.testing.assert_array_equal(got[1], ref[1])
+    assert (got[2], got[3]) == (ref[2], ref[3])
+    starts = ref[1][:-1]
+    np.testing.assert_array_equal(got[4], (ids.reshape(-1)[starts] == 0).astype(np.uint8))
+
+
+@pytest.mark.parametrize("cfg", [2, 4, 5])
+def test_builder_full_size_configs_bit_exact(cfg):
+    w = inputs.config(cfg, seed=0)
+    Lq = w.q.shape[0]
+    got = _build_gpu(w.doc_ids, Lq, w.q_global_start)
+    ref = oracle.build_segments(w.doc_ids, Lq, w.q_global_start)
+    for a, b in zip(got[:4], ref):
+        np.testing.assert_array_equal(np.asarray(a), np.asarray(b))
+
+
+def test_builder_capacity_too_small_reports_device_args():
+    ids = torch.tensor([[1, 1, 2, 2, 3]], dtype=torch.int32, device="cuda")
+    psf.build_doc_segments(ids, 5, 0, capacity=2)
+    assert psf.device_status() == -4
+
+
+# ---------------------------------------------------------------- forward + backward, varlen
+
+def _rand_segments(r, nseg, max_len, allow_empty=True):
+    mq = r.integers(0 if allow_empty else 1, max_len, size=nseg)
+    mk = r.integers(0 if allow_empty else 1, max_len, size=nseg)
+    cu_q = np.concatenate([[0], np.cumsum(mq)]).astype(np.int32)
+    cu_k = np.concatenate([[0], np.cumsum(mk)]).astype(np.int32)
+    return cu_q, cu_k
+
+
+def _varlen_case(seed, Dqk, Dv, Hq, Hkv, causal, window, nseg=5, max_len=400, tail_q=0, tail_k=0):
+    r = np.random.default_rng(seed)
+    cu_q, cu_k = _rand_segments(r, nseg, max_len)
+    Tq, Tk = int(cu_q[-1]) + tail_q, int(cu_k[-1]) + tail_k
+    q = inputs.randn_bf16((Tq, Hq, Dqk), seed * 7 + 1)
+    k = inputs.randn_bf16((Tk, Hkv, Dqk), seed * 7 + 2)
+    v = inputs.randn_bf16((Tk, Hkv, Dv), seed * 7 + 3)
+    do = inputs.randn_bf16((Tq, Hq, Dv), seed * 7 + 4)
+    scale = 1.0 / np.sqrt(Dqk)
+    cq, ck = torch.from_numpy(cu_q).cuda(), torch.from_numpy(cu_k).cuda()
+    mq, mk = int(np.diff(cu_q).max()), int(np.diff(cu_k).max())
+    out, lse = psf.attn_varlen_fwd(cuda(q), cuda(k), cuda(v), cq, ck, mq, mk, scale, causal, window)
+    out_o, lse_o = oracle.attn_fwd_segments(q, k, v, cu_q, cu_k, scale, causal, window)
+    assert_fwd(out, lse, out_o, lse_o)
+    grads = psf.attn_varlen_bwd(cuda(do), cuda(q), cuda(k), cuda(v), out, lse, cq, ck, mq, mk, scale, causal,
+                                window)
+    ref = oracle.attn_bwd_segments(do, q, k, v, out_o, lse_o, cu_q, cu_k, scale, causal, window)
+    assert_grads(grads, ref)
+    assert psf.device_status() == 0
+
+
+@pytest.mark.parametrize("dims", [(64, 64), (128, 128), (192, 128)])
+@pytest.mark.parametrize("causal,window", [(True, None), (False, None), (True, 97), (False, 150)])
+def test_varlen_fwd_bwd_matches_oracle(dims, causal, window):
+    _varlen_case(3, dims[0], dims[1], 4, 2, causal, window)
+
+
+def test_varlen_gqa_ratio_4_with_uncovered_tail_rows():
+    _varlen_case(5, 128, 128, 8, 2, True, None, nseg=4, max_len=300, tail_q=37, tail_k=21)
+
+
+def test_varlen_many_small_and_empty_segments():
+    _varlen_case(11, 128, 128, 2, 1, True, None, nseg=40, max_len=40)
+
+
+# ---------------------------------------------------------------- document-causal composition
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_document_causal_small_rows(seed):
+    w = inputs.small_document_workload(900, 4, 2, 128, 128, seed, max_len=350, pad_tail=61)
+    doc_case(w)
+
+
+def test_document_causal_shard_and_window():
+    w = inputs.small_document_workload(1000, 4, 4, 192, 128, 2, q_global_start=400, max_len=500, pad_tail=33)
+    doc_case(w, window=150)
+
+
+def test_document_causal_d64_window_one():
+    w = inputs.small_document_workload(500, 2, 1, 64, 64, 3, max_len=200)
+    doc_case(w, window=1)
+
+
+# ---------------------------------------------------------------- dense
+
+def _dense_case(B, Hq, Hkv, Nq, Nk, Dqk, Dv, causal, window=None, seed=0, factor=1.0):
+    w = inputs.dense_workload(B, Hq, Hkv, Nq, Nk, Dqk, Dv, seed, factor=factor, causal=causal)
+    q, k, v, do = (cuda(t) for t in (w.q, w.k, w.v, w.dout))
+    out, lse = psf.attn_dense_fwd(q, k, v, w.scale, causal, window)
+    out_o, lse_o = oracle.attn_fwd_dense(w.q, w.k, w.v, w.scale, causal, window)
+    assert_fwd(out, lse, out_o, lse_o)
+    if Dqk == 512:
+        return
+    grads = psf.attn_dense_bwd(do, q, k, v, out, lse, w.scale, causal, window)
+    ref = oracle.attn_bwd_dense(w.dout, w.q, w.k, w.v, out_o, lse_o, w.scale, causal, window)
+    assert_grads(grads, ref)
+    assert psf.device_status() == 0
+
+
+def test_dense_config1_exact_shape():
+    _dense_case(1, 2, 1, 128, 128, 64, 64, True)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_dense_rectangular_batched(causal):
+    _dense_case(2, 4, 2, 200, 333, 128, 128, causal, seed=1)
+
+
+def test_dense_more_queries_than_keys_bottom_right():
+    _dense_case(1, 2, 2, 300, 130, 128, 128, True, seed=2)
+
+
+def test_dense_d512_forward():
+    _dense_case(1, 4, 2, 300, 300, 512, 512, True, seed=3, factor=0.5)
+
+
+# ---------------------------------------------------------------- pad fixup and merge
+
+def test_pad_fixup_zeroes_pad_rows():
+    w = inputs.small_document_workload(400, 2, 2, 64, 64, 4, max_len=100, pad_tail=50)
+    doc_case(w, check_bwd=False)
+
+
+def test_lse_merge_matches_oracle_and_neg_inf_rows():
+    r = np.random.default_rng(0)
+    T, H, D = 300, 4, 128
+    o1 = inputs.randn_bf16((T, H, D), 1)
+    o2 = inputs.randn_bf16((T, H, D), 2)
+    l1 = torch.from_numpy(r.standard_normal((H, T)).astype(np.float32))
+    l2 = torch.from_numpy(r.standard_normal((H, T)).astype(np.float32))
+    l1[:, :10] = -np.inf
+    l2[:, 5:15] = -np.inf
+    of, ob, l = psf.lse_merge(cuda(o1), cuda(l1), cuda(o2), cuda(l2), want_f32=True, want_bf16=True)
+    o_ref, l_ref = oracle.lse_merge(o1, l1, o2, l2)
+    assert np.max(np.abs(of.cpu().numpy() - o_ref)) < 1e-5
+    assert np.max(np.abs(ob.float().cpu().numpy() - o_ref)) < 2e-2
+    lg = l.cpu().numpy()
+    assert np.array_equal(np.isneginf(lg), np.isneginf(l_ref))
+    fin = np.isfinite(l_ref)
+    assert np.max(np.abs(lg[fin] - l_ref[fin])) < 1e-5
+    assert not np.isnan(of.cpu().numpy()).any()
