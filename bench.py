@@ -1,0 +1,416 @@
+"""Benchmark of the packed document-causal attention hot path on one GB300.
+
+One step is the whole path over one batch of synthetic input already resident
+in HBM: the doc-ids -> segment builder, the forward (schedule, uncovered-row
+fill, attention), the pad fixup, and the backward (schedule, Delta preprocess,
+attention backward, dQ convert). The workload is 8192 packed tokens with
+document lengths uniform in [64, 2048] (tail padded), Hq=16, Hkv=4, D=128,
+bf16, scale 1/sqrt(128).
+
+Metric: forward + backward TFLOP/s counting only unmasked work (pad queries and
+zero-query segments excluded): forward 2 (Dqk + Dv) and backward
+(6 Dqk + 4 Dv) flops per visible (query, key) pair per query head.
+
+  python bench.py [--gpus N --steps K --warmup W]      our CUDA path
+  python bench.py --impl reference ...                  the fp64 CPU oracle
+
+Under torchrun (N > 1) every rank runs its own replica on its own GPU (no
+collective on the data path; weak scaling); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from packed_sequence_flash_gb300 import inputs  # noqa: E402
+
+METRIC = "varlen doc-causal attention fwd/bwd TFLOP/s (bf16) and % of GB300 tensor peak"
+UNIT = "TFLOP/s"
+FALLBACK_BF16_TFLOPS = 1900.0
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 256 << 20
+# dram__bytes_read.sum + dram__bytes_write.sum per launch of the backward main
+# kernel from one ncu capture, keyed by a hash of the kernel sources it was
+# taken on; reported as null once the sources change.
+NCU_TRAFFIC = {}  # filled in once a capture of the current sources exists
+
+
+def kernel_source_hash(files=("bwd.cuh", "common.cuh", "ptx.cuh")) -> str:
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "packed_sequence_flash_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def visible_pairs(doc_ids: np.ndarray, q0: int, Lq: int, window=None) -> int:
+    """Pairs (query, key) a non-padding query of the shard sees, summed over rows."""
+    total = 0
+    for row in np.asarray(doc_ids):
+        S = row.shape[0]
+        change = np.ones(S, bool)
+        change[1:] = row[1:] != row[:-1]
+        run_start = np.maximum.accumulate(np.where(change, np.arange(S), 0))
+        p = np.arange(q0, q0 + Lq)
+        cnt = p - run_start[p] + 1
+        if window:
+            cnt = np.minimum(cnt, window)
+        total += int(cnt[row[p] != 0].sum())
+    return total
+
+
+def workload_flops(w):
+    Lq = w.q.shape[0]
+    Hq, Dqk, Dv = w.q.shape[1], w.q.shape[2], w.v.shape[2]
+    pairs = visible_pairs(w.doc_ids, w.q_global_start, Lq, w.window) * Hq
+    return pairs, pairs * 2 * (Dqk + Dv), pairs * (6 * Dqk + 4 * Dv)
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            with open(path) as fh:
+                return json.load(fh), "measured"
+        except Exception:
+            pass
+    return {}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples every 200 ms while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.rows = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200",
+                 "-i", str(gpu_index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, ValueError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def mark(self):
+        return time.time()
+
+    def summary(self, t0, t1):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=2)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = [r for t, r in self.rows if t0 - 0.1 <= t <= t1 + 0.25] or [r for _, r in self.rows[-3:]]
+        if not rows:
+            return None
+        sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[4:8]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def cpu_sample_workload(w, frac=0.25, offset_docs=0):
+    """The first documents (from offset_docs on) covering about `frac` of the
+    visible pairs, as a workload of its own (same distribution, exact flops)."""
+    lengths = w.extra["lengths"]
+    total = sum(n * (n + 1) // 2 for n in lengths)
+    pos = sum(lengths[:offset_docs])
+    start = pos
+    pairs = 0
+    i = offset_docs
+    while i < len(lengths) and pairs < frac * total:
+        pairs += lengths[i] * (lengths[i] + 1) // 2
+        pos += lengths[i]
+        i += 1
+    sub = inputs.Workload(f"{w.name}[docs {offset_docs}..{i - 1}]", "document", w.q[start:pos], w.k[start:pos],
+                          w.v[start:pos], w.dout[start:pos], w.scale, True, w.window,
+                          w.doc_ids[:, start:pos] - w.doc_ids[0, start] + 1, 0)
+    return sub, i - offset_docs
+
+
+def run_oracle(sub, nthreads):
+    import oracle
+
+    t = time.perf_counter()
+    out, lse = oracle.attn_fwd_document(sub.q, sub.k, sub.v, sub.doc_ids, 0, sub.scale, sub.window,
+                                        nthreads=nthreads)
+    oracle.attn_bwd_document(sub.dout, sub.q, sub.k, sub.v, out, lse, sub.doc_ids, 0, sub.scale, sub.window,
+                             nthreads=nthreads)
+    return time.perf_counter() - t
+
+
+def cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(w):
+    sub, ndocs = cpu_sample_workload(w, 1.0)
+    _, f, b = workload_flops(sub)
+    c = cores()
+    secs = run_oracle(sub, c)
+    return {"value": (f + b) / secs / 1e12, "unit": UNIT, "cores": c, "kind": "oracle",
+            "sample": f"fp64 oracle fwd+bwd on all {ndocs} documents of the step ({sub.q.shape[0]} tokens, "
+                      f"{(f + b) / 1e9:.1f} GFLOP), once, {secs:.1f} s"}
+
+
+def config_dict(w, args, pairs, n_docs):
+    return {"workload": w.name, "tokens": int(w.k.shape[0]), "q_tokens": int(w.q.shape[0]),
+            "q_global_start": int(w.q_global_start), "Hq": int(w.q.shape[1]), "Hkv": int(w.k.shape[1]),
+            "Dqk": int(w.q.shape[2]), "Dv": int(w.v.shape[2]), "window": w.window, "documents": n_docs,
+            "visible_pairs_x_heads": int(pairs), "seed": args.seed, "l2": "flushed between steps (256 MiB write)"}
+
+
+# ---------------------------------------------------------------------------
+
+def reference_arm(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    w = inputs.config(args.config, args.seed)
+    pairs, _, _ = workload_flops(w)
+    c = cores()
+    total_f, total_s = 0.0, 0.0
+    per = []
+    ndocs_total = len(w.extra["lengths"])
+    for s in range(args.warmup + args.steps):
+        sub, nd = cpu_sample_workload(w, 0.06, offset_docs=s % max(ndocs_total - 1, 1))
+        _, f, b = workload_flops(sub)
+        secs = run_oracle(sub, c)
+        if s >= args.warmup:
+            total_f += f + b
+            total_s += secs
+            per.append(secs)
+    value = total_f / total_s / 1e12
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": config_dict(w, args, pairs, ndocs_total),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": c, "kind": "oracle",
+                             "sample": "each step: fp64 oracle fwd+bwd on a run of whole documents covering "
+                                       "about 6% of the workload's pairs, rotating through the row"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line))
+    return 0
+
+
+def our_arm(args):
+    import torch
+
+    import packed_sequence_flash_gb300 as psf
+    from packed_sequence_flash_gb300 import _lib
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    lib = _lib.load()
+
+    w = inputs.config(args.config, args.seed + rank)
+    pairs, f_fwd, f_bwd = workload_flops(w)
+    flops = f_fwd + f_bwd
+    Lq = w.q.shape[0]
+    q, k, v, do = (t.to(dev) for t in (w.q, w.k, w.v, w.dout))
+    ids = torch.from_numpy(np.ascontiguousarray(w.doc_ids)).to(dev)
+    qids = ids[:, w.q_global_start:w.q_global_start + Lq].contiguous()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def step(qq, kk, vv, dd, ii, qi):
+        out, lse, seg = psf.document_causal_attention(qq, kk, vv, qi, ii, w.q_global_start, w.scale, w.window)
+        grads = psf.document_causal_attention_backward(dd, qq, kk, vv, out, lse, seg, w.scale, w.window)
+        return out, lse, grads
+
+    for _ in range(args.warmup):
+        step(q, k, v, do, ids, qids)
+    torch.cuda.synchronize()
+    if psf.device_status() != 0:
+        raise RuntimeError("device status after warm-up is not OK")
+
+    # ---- device-timed steps (inputs resident in HBM)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    stops = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    sampler = ClockSampler(dev.index) if rank == 0 else None
+    time.sleep(0.3)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    lib.psf_kernel_timing(1)
+    for i in range(args.steps):
+        flush.zero_()
+        starts[i].record()
+        step(q, k, v, do, ids, qids)
+        stops[i].record()
+    torch.cuda.synchronize()
+    lib.psf_kernel_timing(0)
+    t1 = time.time()
+    if dist:
+        dist.barrier()
+    clocks = sampler.summary(t0, t1) if sampler else None
+    per_step = [a.elapsed_time(b) for a, b in zip(starts, stops)]
+    ms = statistics.mean(per_step)
+    kt = {}
+    for kind, name in ((0, "fwd"), (1, "bwd")):
+        tot = ctypes_double()
+        n = ctypes_int()
+        _lib.check(lib.psf_kernel_times_ms(kind, tot, n))
+        kt[name] = (tot.value, n.value)
+    if psf.device_status() != 0:
+        raise RuntimeError("device status after the timed steps is not OK")
+    ms_max = ms
+    if dist:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_max = float(t.item())
+
+    # ---- end to end through the public API: pinned host inputs in, results out
+    hq, hk, hv, hd = (t.pin_memory() for t in (w.q, w.k, w.v, w.dout))
+    hids = torch.from_numpy(np.ascontiguousarray(w.doc_ids)).pin_memory()
+    dq_, dk_, dv_, dd_ = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v), torch.empty_like(do)
+    di_ = torch.empty_like(ids)
+    res_host = None
+    e2e_steps = max(3, min(args.steps, 50))
+    e_start = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
+    e_stop = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hd, hids))
+    d2h = 0
+    for i in range(e2e_steps + 1):
+        flush.zero_()
+        rec = i > 0
+        if rec:
+            e_start[i - 1].record()
+        for dst, src in ((dq_, hq), (dk_, hk), (dv_, hv), (dd_, hd), (di_, hids)):
+            dst.copy_(src, non_blocking=True)
+        qi_ = di_[:, w.q_global_start:w.q_global_start + Lq].contiguous()
+        out, lse, grads = step(dq_, dk_, dv_, dd_, di_, qi_)
+        results = (out, lse) + tuple(grads)
+        if res_host is None:
+            res_host = [torch.empty(r.shape, dtype=r.dtype, pin_memory=True) for r in results]
+            d2h = sum(r.numel() * r.element_size() for r in results)
+        for hdst, r in zip(res_host, results):
+            hdst.copy_(r, non_blocking=True)
+        if rec:
+            e_stop[i - 1].record()
+    torch.cuda.synchronize()
+    e2e_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(e_start, e_stop))
+    if dist:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return 0
+
+    peaks, src = measured_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS)) if src == "measured" else FALLBACK_BF16_TFLOPS
+    fwd_ms = kt["fwd"][0] / max(kt["fwd"][1], 1)
+    bwd_ms = kt["bwd"][0] / max(kt["bwd"][1], 1)
+    roof = {}
+    for name, kms, kfl in (("attn_fwd_kernel", fwd_ms, f_fwd), ("attn_bwd_kernel", bwd_ms, f_bwd)):
+        ach = kfl / (kms * 1e-3) / 1e12 if kms > 0 else 0.0
+        roof[name] = {"bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s",
+                      "frac": ach / peak, "ms_per_launch": kms,
+                      "peak_source": f"bf16 dense burst, {'of measured' if src == 'measured' else 'of fallback'}"}
+    dominant = "attn_bwd_kernel" if bwd_ms >= fwd_ms else "attn_fwd_kernel"
+    roofline = dict(roof[dominant])
+    roofline["kernel"] = dominant
+    h = kernel_source_hash()
+    roofline["traffic"] = NCU_TRAFFIC.get(h) if dominant == "attn_bwd_kernel" else None
+    other = [n for n in roof if n != dominant][0]
+
+    value = world * flops / (ms_max * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "impl": "ours",
+        "config": dict(config_dict(w, args, pairs, len(w.extra["lengths"])),
+                       parallelism=f"replicas{world}" if world > 1 else "single GPU"),
+        "fwd_tflops": f_fwd / (fwd_ms * 1e-3) / 1e12 if fwd_ms > 0 else None,
+        "bwd_tflops": f_bwd / (bwd_ms * 1e-3) / 1e12 if bwd_ms > 0 else None,
+        "step_ms_spread": {"min": min(per_step), "median": statistics.median(per_step), "max": max(per_step)},
+        "roofline": roofline, "roofline_other": dict(roof[other], kernel=other),
+        "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms},
+        "gpu_launches": 9 * args.steps,
+        "clocks": clocks,
+    }
+    if world == 1 and not args.no_cpu:
+        line["cpu_baseline"] = cpu_baseline(w)
+    print(json.dumps(line))
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+def ctypes_double():
+    import ctypes
+
+    return ctypes.c_double(0.0)
+
+
+def ctypes_int():
+    import ctypes
+
+    return ctypes.c_int(0)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", type=int, default=2, help="workload number (2 = the headline workload)")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return reference_arm(args)
+    return our_arm(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

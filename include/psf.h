@@ -74,6 +74,17 @@ int psf_device_status(int clear);
 void psf_set_wait_limit_ns(uint64_t ns);
 
 /*
+ * Kernel timing for profiling. psf_kernel_timing(1) clears the record and
+ * starts it: from then on every attention call records two CUDA events on its
+ * stream, immediately before and after its main kernel (kind 0: forward main
+ * kernel, kind 1: backward main kernel). psf_kernel_timing(0) stops recording.
+ * psf_kernel_times_ms() waits for the recorded events of `kind` and returns
+ * their summed device time in *total_ms and their number in *launches.
+ */
+int psf_kernel_timing(int enable);
+int psf_kernel_times_ms(int kind, double* total_ms, int* launches);
+
+/*
  * Workspace sizes in bytes. total_q_rows / total_k_rows count the flattened
  * query / key rows (T for THD, B * S for BHSD); nseg is the number of segments
  * (or the capacity passed to the builder).

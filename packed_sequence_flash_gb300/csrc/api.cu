@@ -8,6 +8,7 @@
 
 #include <mutex>
 #include <string>
+#include <vector>
 
 #include "../../include/psf.h"
 #include "bwd.cuh"
@@ -79,6 +80,40 @@ int device_info(DeviceInfo** out) {
     return fail(PSF_EUNSUPPORTED, "device compute capability %d.%d; this build targets sm_103a", d.major, d.minor);
   *out = &d;
   return PSF_OK;
+}
+
+// Optional event pairs around the main kernels (profiling only).
+struct TimedLaunch {
+  int kind;
+  cudaEvent_t start, stop;
+};
+std::mutex g_timing_mu;
+bool g_timing_on = false;
+std::vector<TimedLaunch> g_timed;
+
+bool timing_begin(int kind, cudaStream_t st, TimedLaunch* t) {
+  std::lock_guard<std::mutex> lk(g_timing_mu);
+  if (!g_timing_on) return false;
+  t->kind = kind;
+  if (cudaEventCreate(&t->start) != cudaSuccess) return false;
+  if (cudaEventCreate(&t->stop) != cudaSuccess) {
+    cudaEventDestroy(t->start);
+    return false;
+  }
+  cudaEventRecord(t->start, st);
+  return true;
+}
+void timing_end(TimedLaunch* t, cudaStream_t st) {
+  cudaEventRecord(t->stop, st);
+  std::lock_guard<std::mutex> lk(g_timing_mu);
+  g_timed.push_back(*t);
+}
+void timing_clear_locked() {
+  for (auto& t : g_timed) {
+    cudaEventDestroy(t.start);
+    cudaEventDestroy(t.stop);
+  }
+  g_timed.clear();
 }
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -222,7 +257,10 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, void* out, float*
   p.limit_ns = g_wait_limit_ns;
   const int64_t max_work = (int64_t)w.item_cap * Hq * p.dv_parts;
   const int grid = (int)(max_work < dev->sms ? max_work : dev->sms);
+  TimedLaunch tl;
+  const bool timed = timing_begin(0, st, &tl);
   e = launch_fwd(p, Dqk, Dv / p.dv_parts, grid, st);
+  if (timed) timing_end(&tl, st);
   if (e != cudaSuccess) return cuda_fail(e, "forward launch");
   return PSF_OK;
 }
@@ -302,7 +340,10 @@ int attn_bwd_impl(const void* dout, const void* q, const void* k, const void* v,
     p.limit_ns = g_wait_limit_ns;
     const int64_t max_work = (int64_t)w.sched.item_cap * Hkv;
     const int grid = (int)(max_work < dev->sms ? max_work : dev->sms);
+    TimedLaunch tl;
+    const bool timed = timing_begin(1, st, &tl);
     e = launch_bwd(p, Dqk, Dv, grid, st);
+    if (timed) timing_end(&tl, st);
     if (e != cudaSuccess) return cuda_fail(e, "backward launch");
   }
   if (q_rows > 0) {
@@ -338,6 +379,32 @@ int psf_device_status(int clear) {
 }
 
 void psf_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns = ns > 0 ? ns : 1; }
+
+int psf_kernel_timing(int enable) {
+  std::lock_guard<std::mutex> lk(g_timing_mu);
+  if (enable) timing_clear_locked();
+  g_timing_on = enable != 0;
+  return PSF_OK;
+}
+
+int psf_kernel_times_ms(int kind, double* total_ms, int* launches) {
+  if (!total_ms || !launches) return fail(PSF_EINVAL, "null output pointer");
+  std::lock_guard<std::mutex> lk(g_timing_mu);
+  double sum = 0.0;
+  int n = 0;
+  for (auto& t : g_timed) {
+    if (t.kind != kind) continue;
+    cudaError_t e = cudaEventSynchronize(t.stop);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaEventSynchronize");
+    float ms = 0.f;
+    if ((e = cudaEventElapsedTime(&ms, t.start, t.stop)) != cudaSuccess) return cuda_fail(e, "cudaEventElapsedTime");
+    sum += ms;
+    ++n;
+  }
+  *total_ms = sum;
+  *launches = n;
+  return PSF_OK;
+}
 
 size_t psf_attn_fwd_workspace_size(int64_t total_q_rows, int nseg) {
   if (total_q_rows < 0 || nseg < 0) return 0;
