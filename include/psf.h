@@ -116,6 +116,34 @@ int psf_attn_varlen_fwd(const void* q, const void* k, const void* v, void* out, 
                         int32_t window_left, void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * Varlen forward that allocates nothing and takes no workspace.
+ *                           [no counterpart on the pages: an addition of this
+ *                            library for callers that cannot allocate]
+ *  Some callers cannot call cudaMalloc on this path: runtimes that reserve all
+ *  device memory up front and hand out nothing afterwards, plugin hosts that
+ *  own every allocation, or code that must not touch the allocator while a
+ *  step runs. This entry point behaves like psf_attn_varlen_fwd (same
+ *  arguments minus workspace / ws_bytes, same results) but keeps its tile
+ *  schedule in a fixed array in the library's device memory (852,736 bytes,
+ *  held on every GPU that loads the library until the process exits).
+ *  Limits: B * Sq <= PSF_NOALLOC_MAX_Q_ROWS and nseg <= PSF_NOALLOC_MAX_SEGMENTS;
+ *  larger calls return PSF_EINVAL without launching anything.
+ *  The first call on a device looks up that array's device address (with the
+ *  device current); make that first call before any stream capture.
+ *  Every call shares the one array and leaves its contents behind; the
+ *  schedule kernel rewrites all of it that a call reads, so nothing needs
+ *  clearing between calls. Calls whose kernels overlap on the GPU (different
+ *  streams, or different host threads, without ordering between them) race on
+ *  the array and must not be issued.
+ */
+#define PSF_NOALLOC_MAX_Q_ROWS (1 << 20)
+#define PSF_NOALLOC_MAX_SEGMENTS 65536
+int psf_attn_varlen_fwd_noalloc(const void* q, const void* k, const void* v, void* out, float* lse,
+                                const int32_t* cu_q, const int32_t* cu_k, const int32_t* dev_meta, int nseg,
+                                int max_q, int max_k, int layout, int B, int Sq, int Sk, int Hq, int Hkv, int Dqk,
+                                int Dv, float scale, int causal, int32_t window_left, void* stream);
+
+/*
  * Varlen backward from caller-supplied out / lse.
  *                           [ffpa_attention page, `_ffpa_varlen_bwd`: "using the
  *                            caller-supplied out/lse. Returns (dq, dk, dv)"]

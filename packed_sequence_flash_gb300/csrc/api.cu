@@ -353,6 +353,37 @@ int attn_bwd_impl(const void* dout, const void* q, const void* k, const void* v,
   return PSF_OK;
 }
 
+// Fixed scratch of psf_attn_varlen_fwd_noalloc: the forward's tile schedule
+// (item count, per-segment tile prefix, (segment, tile) list) for up to
+// PSF_NOALLOC_MAX_Q_ROWS query rows and PSF_NOALLOC_MAX_SEGMENTS segments.
+constexpr size_t kNoAllocScratchBytes =
+    256 + ((sizeof(int) * (size_t)(PSF_NOALLOC_MAX_SEGMENTS + 2) + 255) & ~size_t(255)) +
+    ((sizeof(int2) * (size_t)((PSF_NOALLOC_MAX_Q_ROWS + kBM - 1) / kBM + PSF_NOALLOC_MAX_SEGMENTS + 1) + 255) &
+     ~size_t(255));
+static __device__ __align__(256) unsigned char g_noalloc_fwd_scratch[kNoAllocScratchBytes];
+
+// Device address of the scratch array, looked up once per device with that
+// device current (the host-side symbol is only a stand-in, never a device
+// address).
+void* g_noalloc_ptr[kMaxDevices];
+std::mutex g_noalloc_mu;
+
+int noalloc_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(PSF_EUNSUPPORTED, "device index %d out of range", dev);
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress((void**)&p, g_noalloc_fwd_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(scratch)");
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return PSF_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -423,6 +454,25 @@ int psf_attn_varlen_fwd(const void* q, const void* k, const void* v, void* out, 
   if (!cu_q || !cu_k) return fail(PSF_EINVAL, "varlen calls need cu_q and cu_k");
   return attn_fwd_impl(q, k, v, out, lse, cu_q, cu_k, dev_meta, nseg, max_q, max_k, layout, B, Sq, Sk, Hq, Hkv, Dqk,
                        Dv, scale, causal, window_left, workspace, ws_bytes, stream);
+}
+
+int psf_attn_varlen_fwd_noalloc(const void* q, const void* k, const void* v, void* out, float* lse,
+                                const int32_t* cu_q, const int32_t* cu_k, const int32_t* dev_meta, int nseg,
+                                int max_q, int max_k, int layout, int B, int Sq, int Sk, int Hq, int Hkv, int Dqk,
+                                int Dv, float scale, int causal, int32_t window_left, void* stream) {
+  if (!cu_q || !cu_k) return fail(PSF_EINVAL, "varlen calls need cu_q and cu_k");
+  if (B < 1 || Sq < 0 || nseg < 0) return fail(PSF_EINVAL, "bad sizes B=%d Sq=%d nseg=%d", B, Sq, nseg);
+  if ((int64_t)B * Sq > PSF_NOALLOC_MAX_Q_ROWS)
+    return fail(PSF_EINVAL, "no-allocation forward handles at most %d query rows (got %lld)", PSF_NOALLOC_MAX_Q_ROWS,
+                (long long)B * Sq);
+  if (nseg > PSF_NOALLOC_MAX_SEGMENTS)
+    return fail(PSF_EINVAL, "no-allocation forward handles at most %d segments (got %d)", PSF_NOALLOC_MAX_SEGMENTS,
+                nseg);
+  void* scratch = nullptr;
+  int rc = noalloc_scratch(&scratch);
+  if (rc) return rc;
+  return attn_fwd_impl(q, k, v, out, lse, cu_q, cu_k, dev_meta, nseg, max_q, max_k, layout, B, Sq, Sk, Hq, Hkv, Dqk,
+                       Dv, scale, causal, window_left, scratch, kNoAllocScratchBytes, stream);
 }
 
 int psf_attn_varlen_bwd(const void* dout, const void* q, const void* k, const void* v, const void* out,

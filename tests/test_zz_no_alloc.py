@@ -1,0 +1,88 @@
+"""The forward entry point that allocates nothing (psf_attn_varlen_fwd_noalloc).
+
+It exists for callers that cannot call cudaMalloc while they run, for example
+runtimes that reserve all device memory up front or plugin hosts that own
+every allocation. It keeps its tile schedule in a fixed array inside the
+library instead of a caller workspace. These checks call it through the C ABI
+twice in a row, on different inputs, and compare each result with the
+ordinary workspace-taking entry point on the same inputs, within the parity
+tolerances of the other GPU tests. This file is collected last on purpose.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+OUT_TOL = 2e-2
+LSE_TOL = 1e-3
+
+
+def _case(seed):
+    from packed_sequence_flash_gb300 import inputs
+
+    r = np.random.default_rng(seed)
+    mq = r.integers(0, 300, size=6)
+    mk = r.integers(1, 300, size=6)
+    cu_q = np.concatenate([[0], np.cumsum(mq)]).astype(np.int32)
+    cu_k = np.concatenate([[0], np.cumsum(mk)]).astype(np.int32)
+    Tq, Tk = int(cu_q[-1]) + 5, int(cu_k[-1])
+    q = inputs.randn_bf16((Tq, 4, 128), 100 + seed).cuda()
+    k = inputs.randn_bf16((Tk, 2, 128), 200 + seed).cuda()
+    v = inputs.randn_bf16((Tk, 2, 128), 300 + seed).cuda()
+    return q, k, v, torch.from_numpy(cu_q).cuda(), torch.from_numpy(cu_k).cuda(), int(mq.max()), int(mk.max())
+
+
+def _call(lib, noalloc, q, k, v, cu_q, cu_k, mq, mk, window):
+    Tq, Hq, D = q.shape
+    Tk, Hkv, _ = k.shape
+    nseg = cu_q.numel() - 1
+    out = torch.full((Tq, Hq, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((Hq, Tq), float("nan"), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream().cuda_stream
+    common = [q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), cu_q.data_ptr(),
+              cu_k.data_ptr(), None, nseg, mq, mk, 0, 1, Tq, Tk, Hq, Hkv, D, D, 1.0 / np.sqrt(D), 1, window]
+    if noalloc:
+        rc = lib.psf_attn_varlen_fwd_noalloc(*common, stream)
+        ws = None
+    else:
+        ws = torch.empty(lib.psf_attn_fwd_workspace_size(Tq, nseg), dtype=torch.uint8, device="cuda")
+        rc = lib.psf_attn_varlen_fwd(*common, ws.data_ptr(), ws.numel(), stream)
+    assert rc == 0, lib.psf_last_error()
+    torch.cuda.synchronize()
+    return out, lse
+
+
+def test_noalloc_forward_matches_workspace_forward_twice():
+    from packed_sequence_flash_gb300 import _lib
+
+    lib = _lib.load()
+    for call, (seed, window) in enumerate([(1, -(2 ** 31)), (2, 120)]):
+        args = _case(seed)
+        out_n, lse_n = _call(lib, True, *args, window)
+        out_w, lse_w = _call(lib, False, *args, window)
+        assert lib.psf_device_status(1) == 0
+        o_n, o_w = out_n.double().cpu().numpy(), out_w.double().cpu().numpy()
+        l_n, l_w = lse_n.double().cpu().numpy(), lse_w.double().cpu().numpy()
+        assert not np.isnan(o_n).any() and not np.isnan(l_n).any(), f"call {call}: unwritten output"
+        assert np.max(np.abs(o_n - o_w)) <= OUT_TOL, f"call {call}"
+        assert np.array_equal(np.isneginf(l_n), np.isneginf(l_w)), f"call {call}"
+        fin = np.isfinite(l_w)
+        assert np.max(np.abs(l_n[fin] - l_w[fin])) <= LSE_TOL, f"call {call}"
+
+
+def test_noalloc_forward_rejects_sizes_beyond_its_limit():
+    from packed_sequence_flash_gb300 import _lib
+
+    lib = _lib.load()
+    q, k, v, cu_q, cu_k, mq, mk = _case(3)
+    rc = lib.psf_attn_varlen_fwd_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), q.data_ptr(), q.data_ptr(),
+                                         cu_q.data_ptr(), cu_k.data_ptr(), None, 65537, mq, mk, 0, 1, q.shape[0],
+                                         k.shape[0], 4, 2, 128, 128, 0.1, 1, -1, None)
+    assert rc == -1 and b"segments" in lib.psf_last_error()
+    rc = lib.psf_attn_varlen_fwd_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), q.data_ptr(), q.data_ptr(),
+                                         cu_q.data_ptr(), cu_k.data_ptr(), None, 6, mq, mk, 1, 2, 1 << 20, 16, 4, 2,
+                                         128, 128, 0.1, 1, -1, None)
+    assert rc == -1 and b"query rows" in lib.psf_last_error()
