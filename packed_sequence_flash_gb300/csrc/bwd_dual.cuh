@@ -1,0 +1,430 @@
+// bwd_dual.cuh -- attention backward for Dqk, Dv <= 128 (sm_103a).
+//   [nemo_automodel.components.attention.ffpa_attention, `_ffpa_varlen_bwd`,
+//    `_ffpa_dense_bwd`: gradients from the caller-supplied out/lse, dK/dV
+//    reduced to the KV heads]
+//
+// Same arithmetic as bwd.cuh, laid out for head dims up to 128 so that every
+// operand stream overlaps the tensor core:
+//   TMEM   dV [0, Dv) | dK [Dv, Dv + Dqk) | region A [256, 384) | region B [384, 512)
+//          Step g writes S^T into one region (X) and dP^T into the other (Y);
+//          the roles swap every step. P^T (bf16) is written back over the
+//          first 64 columns of X and feeds dV += P^T dO as the TMEM operand;
+//          dQ = dS K then lands in X (the MMAs run in issue order, so dQ
+//          overwrites P^T only after dV has read it).
+//   SMEM   K, V resident per key tile; Q double-buffered; dO single-buffered
+//          but released right after dV, its last reader, so the next tile's
+//          dO loads while dK and dQ run; dS^T (bf16, 128-byte swizzled) read
+//          K-major by dK and M-major by dQ; the dQ read-out stages its fp32
+//          boxes in the dS^T buffer once the dQ MMA has consumed it.
+//   Warps  0 TMA producer, 1 MMA issuer, 2 TMEM allocator, 4-7 compute
+//          (thread = key row: P, dS, and the dK/dV epilogue), 8-11 dQ read-out
+//          (TMA reduce-add of 32 x 32 fp32 boxes into the global accumulator).
+// The compute warps prefetch the next step's lse and Delta into registers.
+#pragma once
+
+#include <math_constants.h>
+
+#include "bwd.cuh"
+
+namespace psf {
+
+template <int DQK, int DV>
+struct BwdDualCfg {
+  static constexpr int KCH = DQK / 64;
+  static constexpr int VCH = DV / 64;
+  static constexpr int K_OFF = 0;
+  static constexpr int V_OFF = K_OFF + KCH * kChunkBytes;
+  static constexpr int Q_OFF = V_OFF + VCH * kChunkBytes;  // two slots
+  static constexpr int Q_SLOT = KCH * kChunkBytes;
+  static constexpr int DO_OFF = Q_OFF + 2 * Q_SLOT;
+  static constexpr int DS_OFF = DO_OFF + VCH * kChunkBytes;  // dS^T; later the dQ staging (4 warps x 2 x 4 KB)
+  static constexpr int ROWV_OFF = DS_OFF + 2 * kChunkBytes;
+  static constexpr int SMEM_BYTES = ROWV_OFF + 2 * 4 * 128 * 4 + 1024;
+  static constexpr int T_DV = 0;
+  static constexpr int T_DK = DV;
+  static constexpr int T_A = 256;
+  static constexpr int T_B = 384;
+  static_assert(DQK <= 128 && DV <= 128, "dual-region plan needs Dqk, Dv <= 128");
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+};
+
+template <int DQK, int DV>
+__global__ void __launch_bounds__(384, 1) attn_bwd_dual_kernel(const __grid_constant__ BwdParams p) {
+  using C = BwdDualCfg<DQK, DV>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  float* lse_s = reinterpret_cast<float*>(smem + C::ROWV_OFF);  // [4 warps][128]
+  float* dl_s = lse_s + 4 * 128;
+
+  __shared__ uint64_t kv_full, kv_empty, q_full[2], q_empty[2], do_full, do_empty, s_full, dp_full, ds_full,
+      ds_free, dq_full, dq_free, stg_free, acc_done, acc_free, drain;
+  __shared__ uint32_t tmem_base_smem;
+  __shared__ int abort_flag;
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (threadIdx.x == 0) {
+    mbar_init(&kv_full, 1);
+    mbar_init(&kv_empty, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&q_full[i], 1);
+      mbar_init(&q_empty[i], 1);
+    }
+    mbar_init(&do_full, 1);
+    mbar_init(&do_empty, 1);
+    mbar_init(&s_full, 1);
+    mbar_init(&dp_full, 1);
+    mbar_init(&ds_full, 4);
+    mbar_init(&ds_free, 1);
+    mbar_init(&dq_full, 1);
+    mbar_init(&dq_free, 4);
+    mbar_init(&stg_free, 4);
+    mbar_init(&acc_done, 1);
+    mbar_init(&acc_free, 4);
+    mbar_init(&drain, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(&tmem_base_smem, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_smem;
+  const Ctl ctl{p.status, p.limit_ns, &abort_flag};
+  const int total = (*p.n_items) * p.Hkv;
+  const int G = p.Hq / p.Hkv;
+  const uint32_t sbase = smem_u32(smem);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&p.tm_q);
+      tma_prefetch_desc(&p.tm_k);
+      tma_prefetch_desc(&p.tm_v);
+      tma_prefetch_desc(&p.tm_do);
+      uint32_t nz = 0, gstep = 0;
+      bool ok = true;
+      for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+        const BwdItem t = bwd_decode(p, w);
+        if (t.nqt == 0) continue;
+        if (!wait_bar(&kv_empty, (nz & 1) ^ 1, ctl)) break;
+        mbar_arrive_expect_tx(&kv_full, (C::KCH + C::VCH) * kChunkBytes);
+        const int fk = t.ck0 + t.kt * kBN, bk = fk / p.seg.Sk, sk = fk - bk * p.seg.Sk;
+        for (int c = 0; c < C::KCH; ++c)
+          tma_load_4d(smem + C::K_OFF + c * kChunkBytes, &p.tm_k, &kv_full, c * 64, sk, t.hk, bk);
+        for (int c = 0; c < C::VCH; ++c)
+          tma_load_4d(smem + C::V_OFF + c * kChunkBytes, &p.tm_v, &kv_full, c * 64, sk, t.hk, bk);
+        ++nz;
+        for (int h = t.hk * G; h < (t.hk + 1) * G && ok; ++h) {
+          for (int qt = t.qt0; qt < t.qt0 + t.nqt; ++qt, ++gstep) {
+            const int fq = t.cq0 + qt * kBM, bq = fq / p.seg.Sq, sq = fq - bq * p.seg.Sq;
+            const int qs = gstep & 1;
+            if (!wait_bar(&q_empty[qs], ((gstep >> 1) & 1) ^ 1, ctl)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&q_full[qs], C::KCH * kChunkBytes);
+            for (int c = 0; c < C::KCH; ++c)
+              tma_load_4d(smem + C::Q_OFF + qs * C::Q_SLOT + c * kChunkBytes, &p.tm_q, &q_full[qs], c * 64, sq, h,
+                          bq);
+            if (!wait_bar(&do_empty, (gstep & 1) ^ 1, ctl)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&do_full, C::VCH * kChunkBytes);
+            for (int c = 0; c < C::VCH; ++c)
+              tma_load_4d(smem + C::DO_OFF + c * kChunkBytes, &p.tm_do, &do_full, c * 64, sq, h, bq);
+          }
+        }
+      }
+      if (nz > 0) wait_bar_drain(&kv_full, (nz - 1) & 1, p.limit_ns);
+      for (uint32_t i = gstep > 2 ? gstep - 2 : 0; i < gstep; ++i) wait_bar_drain(&q_full[i & 1], (i >> 1) & 1, p.limit_ns);
+      if (gstep > 0) wait_bar_drain(&do_full, (gstep - 1) & 1, p.limit_ns);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t id_sq = idesc_bf16_f32(128, 128, 0, 0);  // S^T = K Q^T, dP^T = V dO^T
+      constexpr uint32_t id_dv = idesc_bf16_f32(128, DV, 0, 1);   // dV += P^T (TMEM) dO
+      constexpr uint32_t id_dk = idesc_bf16_f32(128, DQK, 0, 1);  // dK += dS^T Q
+      constexpr uint32_t id_dq = idesc_bf16_f32(128, DQK, 1, 1);  // dQ  = dS K
+      const uint32_t k_a = sbase + C::K_OFF, v_a = sbase + C::V_OFF, q_a0 = sbase + C::Q_OFF;
+      const uint32_t do_a = sbase + C::DO_OFF, ds_a = sbase + C::DS_OFF;
+      uint32_t nz = 0, gstep = 0;
+      bool ok = true;
+      for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+        const BwdItem t = bwd_decode(p, w);
+        if (t.nqt == 0) continue;
+        if (!wait_bar(&kv_full, nz & 1, ctl)) break;
+        if (nz > 0 && !wait_bar(&acc_free, (nz - 1) & 1, ctl)) break;
+        tc_fence_after();
+        const int nsteps = G * t.nqt;
+        for (int k = 0; k < nsteps && ok; ++k, ++gstep) {
+          const int qs = gstep & 1;
+          const uint32_t q_a = q_a0 + qs * C::Q_SLOT;
+          const uint32_t rx = tmem + ((gstep & 1) ? C::T_B : C::T_A);
+          const uint32_t ry = tmem + ((gstep & 1) ? C::T_A : C::T_B);
+          if (!wait_bar(&q_full[qs], (gstep >> 1) & 1, ctl)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          for (int c = 0; c < C::KCH; ++c) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_ss(rx, sdesc_sw128(k_a + c * kChunkBytes + kk * 32, 16, 1024),
+                     sdesc_sw128(q_a + c * kChunkBytes + kk * 32, 16, 1024), id_sq, (c | kk) != 0);
+          }
+          mma_commit(&s_full);
+          if (!wait_bar(&do_full, gstep & 1, ctl) || (gstep > 0 && !wait_bar(&dq_free, (gstep - 1) & 1, ctl))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          for (int c = 0; c < C::VCH; ++c) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_ss(ry, sdesc_sw128(v_a + c * kChunkBytes + kk * 32, 16, 1024),
+                     sdesc_sw128(do_a + c * kChunkBytes + kk * 32, 16, 1024), id_sq, (c | kk) != 0);
+          }
+          mma_commit(&dp_full);
+          if (!wait_bar(&ds_full, gstep & 1, ctl)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t first = (k == 0) ? 1u : 0u;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ts(tmem + C::T_DV, rx + kk * 8, sdesc_sw128(do_a + kk * 2048, kChunkBytes, 1024), id_dv,
+                   !(first && kk == 0));
+          mma_commit(&do_empty);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ss(tmem + C::T_DK, sdesc_sw128(ds_a + (kk >> 2) * kChunkBytes + (kk & 3) * 32, 16, 1024),
+                   sdesc_sw128(q_a + kk * 2048, kChunkBytes, 1024), id_dk, !(first && kk == 0));
+          mma_commit(&q_empty[qs]);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ss(rx, sdesc_sw128(ds_a + kk * 2048, kChunkBytes, 1024), sdesc_sw128(k_a + kk * 2048, kChunkBytes, 1024),
+                   id_dq, kk > 0);
+          mma_commit(&dq_full);
+          mma_commit(&ds_free);
+        }
+        if (!ok) break;
+        mma_commit(&acc_done);
+        mma_commit(&kv_empty);
+        ++nz;
+      }
+      mma_commit(&drain);
+      wait_bar_drain(&drain, 0, p.limit_ns);
+    }
+  } else if (warp >= 4 && warp < 8) {
+    // ------------------------------------------------------------ compute warpgroup
+    const int wq = warp - 4;
+    const int r = threadIdx.x - 128;  // key row within the tile
+    const uint32_t lane_base = (uint32_t)(32 * wq) << 16;
+    float* my_lse = lse_s + wq * 128;
+    float* my_dl = dl_s + wq * 128;
+    uint8_t* ds_s = smem + C::DS_OFF;
+    const float sl2 = p.scale_log2;
+    uint32_t nz = 0, gstep = 0;
+    bool ok = true;
+    // lse * log2(e) (+inf where the row carries no probability) and Delta of
+    // 4 query columns per lane for one step.
+    auto fetch_rows = [&](const BwdItem& t, int h, int i0, float (&lv)[4], float (&dv)[4]) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int qc = lane * 4 + e;
+        const int f = t.cq0 + i0 + qc;
+        lv[e] = CUDART_INF_F;
+        dv[e] = 0.f;
+        if (i0 + qc < t.m && f < p.q_rows) {
+          const int bq = f / p.seg.Sq, sq = f - bq * p.seg.Sq;
+          const float x = p.lse[bq * p.l_sb + h * p.l_sh + sq];
+          lv[e] = x == -CUDART_INF_F ? CUDART_INF_F : x * 1.4426950408889634f;
+          dv[e] = p.delta[(int64_t)h * p.q_rows + f];
+        }
+      }
+    };
+    for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+      const BwdItem t = bwd_decode(p, w);
+      const int j = t.kt * kBN + r;  // segment-local key index
+      const bool valid = j < t.n;
+      const int fk = t.ck0 + j, bk = fk / p.seg.Sk, sk = fk - bk * p.seg.Sk;
+      __nv_bfloat16* dk_row = p.dk + bk * p.k_sb + (int64_t)sk * p.k_ss + t.hk * p.k_sh;
+      __nv_bfloat16* dv_row = p.dv + bk * p.v_sb + (int64_t)sk * p.v_ss + t.hk * p.v_sh;
+      if (t.nqt == 0) {
+        if (valid) {
+          for (int c = 0; c < DQK / 8; ++c) reinterpret_cast<uint4*>(dk_row)[c] = make_uint4(0, 0, 0, 0);
+          for (int c = 0; c < DV / 8; ++c) reinterpret_cast<uint4*>(dv_row)[c] = make_uint4(0, 0, 0, 0);
+        }
+        continue;
+      }
+      const int delta = t.n - t.m;
+      const int nsteps = G * t.nqt;
+      float nlv[4], ndv[4];
+      fetch_rows(t, t.hk * G, t.qt0 * kBM, nlv, ndv);
+      for (int k = 0; k < nsteps && ok; ++k, ++gstep) {
+        const int h = t.hk * G + k / t.nqt;
+        const int i0 = (t.qt0 + k % t.nqt) * kBM;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          my_lse[lane * 4 + e] = nlv[e];
+          my_dl[lane * 4 + e] = ndv[e];
+        }
+        __syncwarp();
+        if (k + 1 < nsteps) fetch_rows(t, t.hk * G + (k + 1) / t.nqt, (t.qt0 + (k + 1) % t.nqt) * kBM, nlv, ndv);
+        // Per-key visible query columns [q_lo, q_hi) of this tile.
+        int q_lo = p.seg.causal ? j - delta - i0 : -0x40000000;
+        int q_hi = t.m - i0;
+        if (p.seg.window > 0) q_hi = min(q_hi, j - delta + p.seg.window - i0);
+        if (!valid) q_lo = q_hi = 0;
+        const bool masked = q_lo > 0 || q_hi < kBM;
+        if (!wait_bar(&s_full, gstep & 1, ctl) || !wait_bar(&dp_full, gstep & 1, ctl)) {
+          ok = false;
+          break;
+        }
+        if (gstep > 0 && (!wait_bar(&ds_free, (gstep - 1) & 1, ctl) || !wait_bar(&stg_free, (gstep - 1) & 1, ctl))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t rx = tmem + lane_base + ((gstep & 1) ? C::T_B : C::T_A);
+        const uint32_t ry = tmem + lane_base + ((gstep & 1) ? C::T_A : C::T_B);
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t sv[32], pv[32];
+          tmem_ld32(rx + c * 32, sv);
+          tmem_ld32(ry + c * 32, pv);
+          uint32_t pk[16], dk2[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            float pr[2], dr[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const int qc = c * 32 + 2 * e + u;
+              float pe = ex2_approx(fmaf(__uint_as_float(sv[2 * e + u]), sl2, -my_lse[qc]));
+              if (masked && (qc < q_lo || qc >= q_hi)) pe = 0.f;
+              pr[u] = pe;
+              dr[u] = pe * (__uint_as_float(pv[2 * e + u]) - my_dl[qc]);
+            }
+            pk[e] = pack_bf16x2(pr[0], pr[1]);
+            dk2[e] = pack_bf16x2(dr[0], dr[1]);
+          }
+          // P^T (bf16) over the S^T columns already read: chunk c -> columns [16c, 16c + 16).
+          tmem_st16(rx + c * 16, pk);
+          const int chunk = c >> 1, g0 = (c & 1) * 4;
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            *reinterpret_cast<uint4*>(ds_s + chunk * kChunkBytes + sw128_offset(r, g0 + u)) =
+                make_uint4(dk2[4 * u], dk2[4 * u + 1], dk2[4 * u + 2], dk2[4 * u + 3]);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ds_full);
+      }
+      if (!ok) break;
+      // dK / dV epilogue for this key tile.
+      if (!wait_bar(&acc_done, nz & 1, ctl)) break;
+      tc_fence_after();
+#pragma unroll 1
+      for (int c = 0; c < DV / 32; ++c) {
+        uint32_t a[32];
+        tmem_ld32(tmem + lane_base + C::T_DV + c * 32, a);
+        if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(dv_row + c * 32);
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            dst[u] = make_uint4(pack_bf16x2(__uint_as_float(a[8 * u]), __uint_as_float(a[8 * u + 1])),
+                                pack_bf16x2(__uint_as_float(a[8 * u + 2]), __uint_as_float(a[8 * u + 3])),
+                                pack_bf16x2(__uint_as_float(a[8 * u + 4]), __uint_as_float(a[8 * u + 5])),
+                                pack_bf16x2(__uint_as_float(a[8 * u + 6]), __uint_as_float(a[8 * u + 7])));
+        }
+      }
+      const float sc = p.scale;
+#pragma unroll 1
+      for (int c = 0; c < DQK / 32; ++c) {
+        uint32_t a[32];
+        tmem_ld32(tmem + lane_base + C::T_DK + c * 32, a);
+        if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(dk_row + c * 32);
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            dst[u] = make_uint4(pack_bf16x2(__uint_as_float(a[8 * u]) * sc, __uint_as_float(a[8 * u + 1]) * sc),
+                                pack_bf16x2(__uint_as_float(a[8 * u + 2]) * sc, __uint_as_float(a[8 * u + 3]) * sc),
+                                pack_bf16x2(__uint_as_float(a[8 * u + 4]) * sc, __uint_as_float(a[8 * u + 5]) * sc),
+                                pack_bf16x2(__uint_as_float(a[8 * u + 6]) * sc, __uint_as_float(a[8 * u + 7]) * sc));
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_free);
+      ++nz;
+    }
+  } else if (warp >= 8) {
+    // ------------------------------------------------------------ dQ read-out
+    const int wq = warp - 8;
+    const uint32_t lane_base = (uint32_t)(32 * wq) << 16;
+    uint8_t* stg = smem + C::DS_OFF + wq * 8192;  // two 4 KB boxes per warp
+    uint32_t gstep = 0;
+    bool ok = true;
+    for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+      const BwdItem t = bwd_decode(p, w);
+      if (t.nqt == 0) continue;
+      for (int h = t.hk * G; h < (t.hk + 1) * G && ok; ++h) {
+        for (int qt = t.qt0; qt < t.qt0 + t.nqt; ++qt, ++gstep) {
+          if (!wait_bar(&dq_full, gstep & 1, ctl)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t rq = tmem + lane_base + ((gstep & 1) ? C::T_B : C::T_A);
+          const int fq = t.cq0 + qt * kBM + 32 * wq, bq = fq / p.seg.Sq, sq = fq - bq * p.seg.Sq;
+#pragma unroll 1
+          for (int c = 0; c < DQK / 32; ++c) {
+            uint32_t a[32];
+            tmem_ld32(rq + c * 32, a);
+            if (c == DQK / 32 - 1) {
+              // Every TMEM read of this step is done: the region can take the next dP.
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&dq_free);
+            }
+            uint8_t* box = stg + (c & 1) * 4096;
+            if (c >= 2) {
+              if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+              __syncwarp();
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+              *reinterpret_cast<uint4*>(box + sw128_offset(lane, u)) =
+                  make_uint4(a[4 * u], a[4 * u + 1], a[4 * u + 2], a[4 * u + 3]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_reduce_add_4d(&p.tm_dq, box, c * 32, sq, h, bq);
+              bulk_commit_group();
+            }
+          }
+          // The staging boxes live in the dS^T buffer: free them for the next dS^T.
+          if (lane == 0) bulk_wait_group_read0();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&stg_free);
+        }
+      }
+    }
+    if (lane == 0) bulk_wait_group0();
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace psf

@@ -311,29 +311,38 @@ __global__ void __launch_bounds__(256, 1) attn_fwd_kernel(const __grid_constant_
 #pragma unroll
           for (int j = 0; j < 128; ++j) s[j] = (j < lo_c || j >= hi_c) ? -CUDART_INF_F : s[j];
         }
-        float mx = s[0];
+        // Row maximum with eight independent chains (one warp per SM
+        // sub-partition: latency, not throughput, bounds a single chain).
+        float m8[8];
 #pragma unroll
-        for (int j = 1; j < 128; ++j) mx = fmaxf(mx, s[j]);
+        for (int u = 0; u < 8; ++u) m8[u] = s[u];
+#pragma unroll
+        for (int j = 8; j < 128; ++j) m8[j & 7] = fmaxf(m8[j & 7], s[j]);
+        float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
         mx *= sl2;
         const float m_new = (mx > m_used + 8.f) ? mx : m_used;
         const float alpha = (m_new == m_used) ? 1.f : ex2_approx(m_used - m_new);
         const float base = (m_new == -CUDART_INF_F) ? 0.f : m_new;
-        float rs = 0.f;
+        float r8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         uint32_t pa[32], pb2[32];
+        const float2 sl2x2 = make_float2(sl2, sl2), nbase = make_float2(-base, -base);
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
-          float e0 = ex2_approx(fmaf(s[2 * j], sl2, -base));
-          float e1 = ex2_approx(fmaf(s[2 * j + 1], sl2, -base));
-          rs += e0 + e1;
+          const float2 x = fma2(make_float2(s[2 * j], s[2 * j + 1]), sl2x2, nbase);
+          const float e0 = ex2_approx(x.x), e1 = ex2_approx(x.y);
+          r8[(2 * j) & 7] += e0;
+          r8[(2 * j + 1) & 7] += e1;
           pa[j] = pack_bf16x2(e0, e1);
         }
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
-          float e0 = ex2_approx(fmaf(s[64 + 2 * j], sl2, -base));
-          float e1 = ex2_approx(fmaf(s[64 + 2 * j + 1], sl2, -base));
-          rs += e0 + e1;
+          const float2 x = fma2(make_float2(s[64 + 2 * j], s[64 + 2 * j + 1]), sl2x2, nbase);
+          const float e0 = ex2_approx(x.x), e1 = ex2_approx(x.y);
+          r8[(2 * j) & 7] += e0;
+          r8[(2 * j + 1) & 7] += e1;
           pb2[j] = pack_bf16x2(e0, e1);
         }
+        const float rs = ((r8[0] + r8[1]) + (r8[2] + r8[3])) + ((r8[4] + r8[5]) + (r8[6] + r8[7]));
         if (jj > 0) {
           // O must hold PV(jj-1) before it is rescaled.
           if (!wait_bar(&pv_done, pvcnt & 1, ctl)) {
