@@ -338,11 +338,9 @@ int attn_bwd_impl(const void* dout, const void* q, const void* k, const void* v,
     p.n_items = w.sched.n_items;
     p.status = dev->status;
     p.limit_ns = g_wait_limit_ns;
-    const int64_t max_work = (int64_t)w.sched.item_cap * Hkv;
-    const int grid = (int)(max_work < dev->sms ? max_work : dev->sms);
     TimedLaunch tl;
     const bool timed = timing_begin(1, st, &tl);
-    e = launch_bwd(p, Dqk, Dv, grid, st);
+    e = launch_bwd(p, Dqk, Dv, dev->sms, w.sched.item_cap, st);
     if (timed) timing_end(&tl, st);
     if (e != cudaSuccess) return cuda_fail(e, "backward launch");
   }

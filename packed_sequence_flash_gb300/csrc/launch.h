@@ -19,7 +19,7 @@ cudaError_t launch_schedule(const SegInfo& g, int over_keys, int2* items, int* n
 cudaError_t launch_fwd_tail(const SegInfo& g, __nv_bfloat16* out, int64_t o_sb, int64_t o_ss, int64_t o_sh, float* lse,
                             int64_t l_sb, int64_t l_sh, int Hq, int Dv, cudaStream_t st);
 cudaError_t launch_fwd(const FwdParams& p, int dqk, int dvc, int grid, cudaStream_t st);
-cudaError_t launch_bwd(const BwdParams& p, int dqk, int dv, int grid, cudaStream_t st);
+cudaError_t launch_bwd(const BwdParams& p, int dqk, int dv, int sms, int item_cap, cudaStream_t st);
 int fwd_smem_bytes(int dqk, int dvc);
 int bwd_smem_bytes(int dqk, int dv);
 
