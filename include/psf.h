@@ -90,7 +90,8 @@ int psf_kernel_times_ms(int kind, double* total_ms, int* launches);
  * (or the capacity passed to the builder).
  */
 size_t psf_attn_fwd_workspace_size(int64_t total_q_rows, int nseg);
-size_t psf_attn_bwd_workspace_size(int64_t total_q_rows, int64_t total_k_rows, int nseg, int Hq, int Dqk);
+size_t psf_attn_bwd_workspace_size(int64_t total_q_rows, int64_t total_k_rows, int nseg, int Hq, int Hkv, int Dqk,
+                                   int Dv);
 
 /*
  * Varlen forward.           [ffpa_attention page, `_ffpa_varlen_fwd`: packed THD
@@ -152,8 +153,9 @@ int psf_attn_varlen_fwd_noalloc(const void* q, const void* k, const void* v, voi
  *  the Hq / Hkv query heads sharing a KV head are summed on chip).
  *  Keys that no query sees get dk = dv = 0; query rows outside every segment
  *  get dq = 0.
- *  workspace: psf_attn_bwd_workspace_size(Tq, Tk, nseg, Hq, Dqk) bytes (holds
- *  the fp32 dQ accumulator, Delta = rowsum(dO * out) and the tile schedule).
+ *  workspace: psf_attn_bwd_workspace_size(Tq, Tk, nseg, Hq, Hkv, Dqk, Dv) bytes
+ *  (holds the fp32 dQ, dK and dV accumulators, Delta = rowsum(dO * out) and the
+ *  tile schedule).
  */
 int psf_attn_varlen_bwd(const void* dout, const void* q, const void* k, const void* v, const void* out,
                         const float* lse, void* dq, void* dk, void* dv, const int32_t* cu_q, const int32_t* cu_k,
@@ -178,7 +180,7 @@ int psf_attn_dense_fwd(const void* q, const void* k, const void* v, void* out, f
 /*
  * Dense backward.           [ffpa_attention page, `_ffpa_dense_bwd`: returns
  *                            (dq, dk, dv) in [B,H,N,D], dK/dV reduced to Hkv]
- *  workspace: psf_attn_bwd_workspace_size(B * Nq, B * Nk, B, Hq, Dqk) bytes.
+ *  workspace: psf_attn_bwd_workspace_size(B * Nq, B * Nk, B, Hq, Hkv, Dqk, Dv) bytes.
  */
 int psf_attn_dense_bwd(const void* dout, const void* q, const void* k, const void* v, const void* out,
                        const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Nq, int Nk,

@@ -69,9 +69,10 @@ def fwd_workspace_size(total_q_rows: int, nseg: int) -> int:
     return int(_lib.load().psf_attn_fwd_workspace_size(int(total_q_rows), int(nseg)))
 
 
-def bwd_workspace_size(total_q_rows: int, total_k_rows: int, nseg: int, Hq: int, Dqk: int) -> int:
+def bwd_workspace_size(total_q_rows: int, total_k_rows: int, nseg: int, Hq: int, Hkv: int, Dqk: int,
+                       Dv: int) -> int:
     return int(_lib.load().psf_attn_bwd_workspace_size(int(total_q_rows), int(total_k_rows), int(nseg), int(Hq),
-                                                       int(Dqk)))
+                                                       int(Hkv), int(Dqk), int(Dv)))
 
 
 def _workspace(nbytes: int, device) -> torch.Tensor:
@@ -128,7 +129,7 @@ def attn_varlen_bwd(dout, q, k, v, out, lse, cu_q, cu_k, max_q, max_k, scale, ca
     dk = torch.empty_like(k)
     dv = torch.empty_like(v)
     if workspace is None:
-        workspace = _workspace(bwd_workspace_size(B * Sq, B * Sk, nseg, Hq, Dqk), q.device)
+        workspace = _workspace(bwd_workspace_size(B * Sq, B * Sk, nseg, Hq, Hkv, Dqk, Dv), q.device)
     rc = _lib.load().psf_attn_varlen_bwd(
         _ptr(dout), _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(cu_q),
         _ptr(cu_k), _ptr(dev_meta), nseg, int(max_q), int(max_k), lay, B, Sq, Sk, Hq, Hkv, Dqk, Dv, float(scale),
@@ -168,7 +169,7 @@ def attn_dense_bwd(dout, q, k, v, out, lse, scale, causal, window=None, workspac
     Dv = v.shape[3]
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     if workspace is None:
-        workspace = _workspace(bwd_workspace_size(B * Nq, B * Nk, B, Hq, Dqk), q.device)
+        workspace = _workspace(bwd_workspace_size(B * Nq, B * Nk, B, Hq, Hkv, Dqk, Dv), q.device)
     rc = _lib.load().psf_attn_dense_bwd(_ptr(dout), _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dq),
                                         _ptr(dk), _ptr(dv), B, Hq, Hkv, Nq, Nk, Dqk, Dv, float(scale),
                                         int(bool(causal)), _window(window), _ptr(workspace), workspace.numel(),

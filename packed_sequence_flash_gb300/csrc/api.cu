@@ -163,22 +163,50 @@ size_t fwd_ws_layout(int64_t rows, int nseg, FwdWorkspace* w, void* base) {
 }
 
 struct BwdWorkspace {
-  FwdWorkspace sched;
+  int* n_items;
+  int* seg_prefix;
+  int4* items;
+  int item_cap;
   float* delta;
   float* dq_acc;
+  float* dk_acc;
+  float* dv_acc;
 };
-size_t bwd_ws_layout(int64_t q_rows, int64_t k_rows, int nseg, int Hq, int Dqk, BwdWorkspace* w, void* base) {
-  size_t off = fwd_ws_layout(k_rows, nseg, w ? &w->sched : nullptr, base);
-  size_t delta_off = off;
+// Heavy key tiles are split into at most this many sub-ranges' worth of work
+// per SM (see bwd_schedule_kernel); the item capacity follows from it.
+constexpr int kSplitPerSm = 2;
+size_t bwd_ws_layout(int64_t q_rows, int64_t k_rows, int nseg, int Hq, int Hkv, int Dqk, int Dv, int sms,
+                     BwdWorkspace* w, void* base) {
+  const int64_t cap = (k_rows + kBN - 1) / kBN + nseg + (int64_t)kSplitPerSm * sms + 2;
+  size_t off = 256;
+  const size_t prefix_off = off;
+  off += align256(sizeof(int) * (size_t)(nseg + 2));
+  const size_t items_off = off;
+  off += align256(sizeof(int4) * (size_t)cap);
+  const size_t delta_off = off;
   off += align256(sizeof(float) * (size_t)Hq * (size_t)q_rows);
-  size_t acc_off = off;
+  const size_t dq_off = off;
   off += align256(sizeof(float) * (size_t)q_rows * Hq * Dqk);
+  const size_t dk_off = off;
+  off += align256(sizeof(float) * (size_t)k_rows * Hkv * Dqk);
+  const size_t dv_off = off;
+  off += align256(sizeof(float) * (size_t)k_rows * Hkv * Dv);
   if (w && base) {
-    w->delta = reinterpret_cast<float*>(static_cast<char*>(base) + delta_off);
-    w->dq_acc = reinterpret_cast<float*>(static_cast<char*>(base) + acc_off);
+    char* b = static_cast<char*>(base);
+    w->n_items = reinterpret_cast<int*>(b);
+    w->seg_prefix = reinterpret_cast<int*>(b + prefix_off);
+    w->items = reinterpret_cast<int4*>(b + items_off);
+    w->item_cap = (int)cap;
+    w->delta = reinterpret_cast<float*>(b + delta_off);
+    w->dq_acc = reinterpret_cast<float*>(b + dq_off);
+    w->dk_acc = reinterpret_cast<float*>(b + dk_off);
+    w->dv_acc = reinterpret_cast<float*>(b + dv_off);
   }
   return off;
 }
+// The workspace size query must not depend on the device; size it for the
+// largest SM count this library targets.
+constexpr int kMaxSms = 160;
 
 int check_common(int layout, int B, int Sq, int Sk, int Hq, int Hkv, int Dqk, int Dv, float scale, int32_t window,
                  int nseg) {
@@ -283,23 +311,28 @@ int attn_bwd_impl(const void* dout, const void* q, const void* k, const void* v,
     if (k_rows > 0 && (!x || !aligned16(x))) return fail(PSF_EINVAL, "null or unaligned key-side tensor");
   if (q_rows > 0 && !lse) return fail(PSF_EINVAL, "null lse");
   if ((cu_q == nullptr) != (cu_k == nullptr)) return fail(PSF_EINVAL, "cu_q and cu_k must both be given");
-  const size_t need = bwd_ws_layout(q_rows, k_rows, nseg, Hq, Dqk, nullptr, nullptr);
+  const size_t need = bwd_ws_layout(q_rows, k_rows, nseg, Hq, Hkv, Dqk, Dv, kMaxSms, nullptr, nullptr);
   if (!ws || ws_bytes < need) return fail(PSF_EWORKSPACE, "backward workspace needs %zu bytes (got %zu)", need, ws_bytes);
   DeviceInfo* dev = nullptr;
   if ((rc = device_info(&dev))) return rc;
+  if (dev->sms > kMaxSms) return fail(PSF_EUNSUPPORTED, "more than %d SMs", kMaxSms);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
+  // Head dims up to 128 run the kernel that adds dK/dV partial sums into fp32
+  // accumulators, which lets heavy key tiles be split across SMs.
+  const bool accumulate = Dqk <= 128 && Dv <= 128;
   BwdWorkspace w;
-  bwd_ws_layout(q_rows, k_rows, nseg, Hq, Dqk, &w, ws);
+  bwd_ws_layout(q_rows, k_rows, nseg, Hq, Hkv, Dqk, Dv, dev->sms, &w, ws);
   SegInfo g{cu_q, cu_k, dev_meta, nseg, max_q, max_k, B, Sq, Sk, causal ? 1 : 0, window > 0 ? (int)window : 0};
   const View vq = tensor_view(layout, Sq, Hq, Dqk), vk = tensor_view(layout, Sk, Hkv, Dqk);
   const View vv = tensor_view(layout, Sk, Hkv, Dv), vo = tensor_view(layout, Sq, Hq, Dv);
   const View vl = lse_view(layout, Sq, Hq);
-  cudaError_t e = launch_schedule(g, 1, w.sched.items, w.sched.n_items, w.sched.seg_prefix, w.sched.item_cap,
-                                  dev->status, st);
+  cudaError_t e = launch_bwd_schedule(g, Hq / Hkv, Hkv, accumulate ? kSplitPerSm * dev->sms : 0, w.items,
+                                      w.n_items, w.seg_prefix, w.item_cap, dev->status, st);
   if (e != cudaSuccess) return cuda_fail(e, "schedule launch");
   e = launch_bwd_pre(g, static_cast<const __nv_bfloat16*>(dout), static_cast<const __nv_bfloat16*>(out), vo.sb,
-                     vo.ss, vo.sh, w.delta, w.dq_acc, Hq, Dqk, Dv, static_cast<__nv_bfloat16*>(dk),
+                     vo.ss, vo.sh, w.delta, w.dq_acc, Hq, Dqk, Dv, accumulate ? w.dk_acc : nullptr,
+                     accumulate ? w.dv_acc : nullptr, static_cast<__nv_bfloat16*>(dk),
                      static_cast<__nv_bfloat16*>(dv), vk.sb, vk.ss, vk.sh, vv.sb, vv.ss, vv.sh, Hkv, st);
   if (e != cudaSuccess) return cuda_fail(e, "preprocess launch");
 
@@ -309,10 +342,16 @@ int attn_bwd_impl(const void* dout, const void* q, const void* k, const void* v,
     if (q_rows > 0) {
       if ((rc = make_bf16_map(&p.tm_q, q, Dqk, Sq, Hq, B, vq, 64))) return rc;
       if ((rc = make_bf16_map(&p.tm_do, dout, Dv, Sq, Hq, B, vo, 64))) return rc;
-      const View va{(int64_t)Sq * Hq * Dqk, (int64_t)Hq * Dqk, (int64_t)Dqk};
-      int r2 = make_tmap_4d(&p.tm_dq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, w.dq_acc, Dqk, Sq, Hq, B, va.ss, va.sh,
-                            va.sb, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B);
+      int r2 = make_tmap_4d(&p.tm_dq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, w.dq_acc, Dqk, Sq, Hq, B, (int64_t)Hq * Dqk,
+                            Dqk, (int64_t)Sq * Hq * Dqk, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B);
       if (r2) return fail(PSF_ECUDA, "cuTensorMapEncodeTiled failed (%d) for the dQ accumulator", r2);
+    }
+    if (accumulate) {
+      int r2 = make_tmap_4d(&p.tm_dk, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, w.dk_acc, Dqk, Sk, Hkv, B,
+                            (int64_t)Hkv * Dqk, Dqk, (int64_t)Sk * Hkv * Dqk, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B);
+      r2 |= make_tmap_4d(&p.tm_dv, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, w.dv_acc, Dv, Sk, Hkv, B, (int64_t)Hkv * Dv,
+                         Dv, (int64_t)Sk * Hkv * Dv, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B);
+      if (r2) return fail(PSF_ECUDA, "cuTensorMapEncodeTiled failed for the dK/dV accumulators");
     }
     if ((rc = make_bf16_map(&p.tm_k, k, Dqk, Sk, Hkv, B, vk, 64))) return rc;
     if ((rc = make_bf16_map(&p.tm_v, v, Dv, Sk, Hkv, B, vv, 64))) return rc;
@@ -334,20 +373,21 @@ int attn_bwd_impl(const void* dout, const void* q, const void* k, const void* v,
     p.Hkv = Hkv;
     p.scale = scale;
     p.scale_log2 = scale * 1.4426950408889634f;
-    p.items = w.sched.items;
-    p.n_items = w.sched.n_items;
+    p.items = w.items;
+    p.n_items = w.n_items;
     p.status = dev->status;
     p.limit_ns = g_wait_limit_ns;
     TimedLaunch tl;
     const bool timed = timing_begin(1, st, &tl);
-    e = launch_bwd(p, Dqk, Dv, dev->sms, w.sched.item_cap, st);
+    e = launch_bwd(p, Dqk, Dv, dev->sms, w.item_cap, st);
     if (timed) timing_end(&tl, st);
     if (e != cudaSuccess) return cuda_fail(e, "backward launch");
   }
-  if (q_rows > 0) {
-    e = launch_dq_convert(w.dq_acc, static_cast<__nv_bfloat16*>(dq), B, Sq, Hq, Dqk, vq.sb, vq.ss, vq.sh, scale, st);
-    if (e != cudaSuccess) return cuda_fail(e, "dQ convert launch");
-  }
+  e = launch_bwd_convert(w.dq_acc, static_cast<__nv_bfloat16*>(dq), q_rows > 0, B, Sq, Hq, Dqk, vq.sb, vq.ss, vq.sh,
+                         accumulate ? w.dk_acc : nullptr, static_cast<__nv_bfloat16*>(dk),
+                         accumulate ? w.dv_acc : nullptr, static_cast<__nv_bfloat16*>(dv), Sk, Hkv, Dv, vk.sb, vk.ss,
+                         vk.sh, vv.sb, vv.ss, vv.sh, scale, st);
+  if (e != cudaSuccess) return cuda_fail(e, "convert launch");
   return PSF_OK;
 }
 
@@ -440,9 +480,10 @@ size_t psf_attn_fwd_workspace_size(int64_t total_q_rows, int nseg) {
   return fwd_ws_layout(total_q_rows, nseg, nullptr, nullptr);
 }
 
-size_t psf_attn_bwd_workspace_size(int64_t total_q_rows, int64_t total_k_rows, int nseg, int Hq, int Dqk) {
-  if (total_q_rows < 0 || total_k_rows < 0 || nseg < 0 || Hq < 1 || Dqk < 1) return 0;
-  return bwd_ws_layout(total_q_rows, total_k_rows, nseg, Hq, Dqk, nullptr, nullptr);
+size_t psf_attn_bwd_workspace_size(int64_t total_q_rows, int64_t total_k_rows, int nseg, int Hq, int Hkv, int Dqk,
+                                   int Dv) {
+  if (total_q_rows < 0 || total_k_rows < 0 || nseg < 0 || Hq < 1 || Hkv < 1 || Dqk < 1 || Dv < 1) return 0;
+  return bwd_ws_layout(total_q_rows, total_k_rows, nseg, Hq, Hkv, Dqk, Dv, kMaxSms, nullptr, nullptr);
 }
 
 int psf_attn_varlen_fwd(const void* q, const void* k, const void* v, void* out, float* lse, const int32_t* cu_q,

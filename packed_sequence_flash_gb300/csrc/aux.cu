@@ -1,6 +1,7 @@
 // aux.cu -- memory-bound kernels around the attention kernels: the tile
 // schedulers, the doc-id segment builder, pad fixup, lse merge, the backward
-// preprocess (Delta = rowsum(dO * O), zeroed accumulators) and the dQ convert.
+// preprocess (Delta = rowsum(dO * O), zeroed accumulators) and the backward
+// convert (fp32 accumulators -> bf16 dQ, dK, dV).
 #include <math_constants.h>
 
 #include "launch.h"
@@ -142,6 +143,108 @@ __global__ void __launch_bounds__(kScanThreads) schedule_kernel(SegInfo g, int o
   if (tid == 0) *n_items = carry;
 }
 
+// Backward work list: key tiles, each cut into sub-ranges of its G * nqt
+// (query head, query tile) steps when it holds more than its share of the
+// total (split_target > 0: aim at split_target sub-items' worth of steps),
+// heaviest first. Items are (segment, key tile, first step, end step).
+__global__ void __launch_bounds__(kScanThreads) bwd_schedule_kernel(SegInfo g, int G, int Hkv, int split_target,
+                                                                    int4* items, int* n_items, int* seg_prefix,
+                                                                    int item_cap, int* status) {
+  __shared__ int hist[kBuckets];
+  __shared__ int start[kBuckets];
+  __shared__ int bad;
+  __shared__ unsigned long long total_steps;
+  const int tid = threadIdx.x;
+  const int nseg = seg_count(g);
+  const int max_q = g.dev_meta ? g.dev_meta[1] : g.max_q;
+  const int max_k = g.dev_meta ? g.dev_meta[2] : g.max_k;
+  const int Tq = g.B * g.Sq, Tk = g.B * g.Sk;
+  hist[tid] = 0;
+  if (tid == 0) {
+    bad = (g.cu_q && nseg >= 0 && (g.cu_q[0] != 0 || g.cu_k[0] != 0)) ? 1 : 0;
+    total_steps = 0;
+  }
+  __syncthreads();
+  int carry = 0;
+  for (int base = 0; base < nseg; base += kScanThreads) {
+    const int s = base + tid;
+    int cnt = 0;
+    if (s < nseg) {
+      const int q0 = cu_q_at(g, s), q1 = cu_q_at(g, s + 1);
+      const int k0 = cu_k_at(g, s), k1 = cu_k_at(g, s + 1);
+      const int m = q1 - q0, n = k1 - k0;
+      bool ok = m >= 0 && n >= 0 && q1 <= Tq && k1 <= Tk && (max_q < 0 || m <= max_q) && (max_k < 0 || n <= max_k);
+      if (ok && g.B > 1)
+        ok = (m == 0 || q0 / g.Sq == (q1 - 1) / g.Sq) && (n == 0 || k0 / g.Sk == (k1 - 1) / g.Sk);
+      if (!ok) bad = 1;
+      else cnt = ceil_div(n, kBN);
+    }
+    int tot;
+    const int ex = block_excl_scan(cnt, &tot);
+    if (s < nseg) seg_prefix[s] = carry + ex;
+    carry += tot;
+  }
+  if (tid == 0) seg_prefix[nseg] = carry;
+  __syncthreads();
+  if (bad) {
+    if (tid == 0) {
+      record_status(status, kStatusDeviceArgs);
+      *n_items = 0;
+    }
+    return;
+  }
+  unsigned long long mine = 0;
+  for (int x = tid; x < carry; x += kScanThreads) {
+    const int s = find_segment(seg_prefix, nseg, x);
+    mine += (unsigned long long)G * tile_cost(g, s, x - seg_prefix[s], 1);
+  }
+  atomicAdd(&total_steps, mine);
+  __syncthreads();
+  int smax = 0x7fffffff;
+  if (split_target > 0) {
+    const unsigned long long want = (total_steps * (unsigned long long)Hkv + split_target - 1) / split_target;
+    smax = (int)(want < 4 ? 4 : (want > 0x7fffffffull ? 0x7fffffffull : want));
+  }
+  int nsub_total = 0;
+  for (int x = tid; x < carry; x += kScanThreads) {
+    const int s = find_segment(seg_prefix, nseg, x);
+    const int steps = G * tile_cost(g, s, x - seg_prefix[s], 1);
+    const int nsub = steps == 0 ? 1 : (int)(((long long)steps + smax - 1) / smax);
+    nsub_total += nsub;
+    for (int i = 0; i < nsub; ++i) {
+      const int c = (int)((long long)steps * (i + 1) / nsub - (long long)steps * i / nsub);
+      atomicAdd(&hist[min(c, kBuckets - 1)], 1);
+    }
+  }
+  int n_all;
+  block_excl_scan(nsub_total, &n_all);
+  if (n_all > item_cap) {
+    if (tid == 0) {
+      record_status(status, kStatusDeviceArgs);
+      *n_items = 0;
+    }
+    return;
+  }
+  int tot;
+  const int rb = kBuckets - 1 - tid;
+  const int ex = block_excl_scan(hist[rb], &tot);
+  start[rb] = ex;
+  hist[rb] = 0;
+  __syncthreads();
+  for (int x = tid; x < carry; x += kScanThreads) {
+    const int s = find_segment(seg_prefix, nseg, x);
+    const int t = x - seg_prefix[s];
+    const int steps = G * tile_cost(g, s, t, 1);
+    const int nsub = steps == 0 ? 1 : (int)(((long long)steps + smax - 1) / smax);
+    for (int i = 0; i < nsub; ++i) {
+      const int a = (int)((long long)steps * i / nsub), e = (int)((long long)steps * (i + 1) / nsub);
+      const int b = min(e - a, kBuckets - 1);
+      items[start[b] + atomicAdd(&hist[b], 1)] = make_int4(s, t, a, e);
+    }
+  }
+  if (tid == 0) *n_items = n_all;
+}
+
 __global__ void fwd_tail_kernel(SegInfo g, __nv_bfloat16* out, int64_t o_sb, int64_t o_ss, int64_t o_sh, float* lse,
                                 int64_t l_sb, int64_t l_sh, int Hq, int Dv) {
   const int nseg = seg_count(g);
@@ -229,19 +332,22 @@ __global__ void __launch_bounds__(kScanThreads) build_segments_kernel(const int3
   }
 }
 
+// One warp per query row: a padding row (id 0) gets out = 0 on every head and
+// lse = -inf; other rows cost one id read.
 __global__ void pad_fixup_kernel(__nv_bfloat16* out, float* lse, const int32_t* qids, int B, int Lq, int Hq, int Dv,
                                  int64_t o_sb, int64_t o_ss, int64_t o_sh, int64_t l_sb, int64_t l_sh) {
+  const int lane = threadIdx.x & 31;
+  const int64_t rows = (int64_t)B * Lq;
+  const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x / 32);
   const int groups = Dv / 8;
-  const int64_t total = (int64_t)B * Lq * Hq * groups;
-  for (int64_t x = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; x < total; x += (int64_t)gridDim.x * blockDim.x) {
-    const int gidx = (int)(x % groups);
-    const int64_t rh = x / groups;
-    const int h = (int)(rh % Hq);
-    const int64_t f = rh / Hq;
+  for (int64_t f = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) / 32; f < rows; f += nwarps) {
     if (qids[f] != 0) continue;
     const int b = (int)(f / Lq), s = (int)(f - (int64_t)b * Lq);
-    reinterpret_cast<uint4*>(out + b * o_sb + (int64_t)s * o_ss + h * o_sh)[gidx] = make_uint4(0, 0, 0, 0);
-    if (gidx == 0) lse[b * l_sb + h * l_sh + s] = -CUDART_INF_F;
+    for (int x = lane; x < Hq * groups; x += 32) {
+      const int h = x / groups, gidx = x - h * groups;
+      reinterpret_cast<uint4*>(out + b * o_sb + (int64_t)s * o_ss + h * o_sh)[gidx] = make_uint4(0, 0, 0, 0);
+    }
+    for (int h = lane; h < Hq; h += 32) lse[b * l_sb + h * l_sh + s] = -CUDART_INF_F;
   }
 }
 
@@ -282,43 +388,59 @@ __global__ void lse_merge_kernel(const __nv_bfloat16* o1, const float* l1, const
   }
 }
 
-// One warp per (row, head): Delta = sum_d dO * O in fp32. Then grid-stride
-// zeroing of the dQ accumulator and of dK / dV rows no segment covers.
+// Delta = sum_d dO * O in fp32, by groups of min(32, Dv/8) lanes per
+// (row, head); then grid-stride zeroing of the fp32 accumulators. When dK/dV
+// are written directly (no accumulators), rows no segment covers are zeroed.
 __global__ void bwd_pre_kernel(SegInfo g, const __nv_bfloat16* dout, const __nv_bfloat16* out, int64_t o_sb,
                                int64_t o_ss, int64_t o_sh, float* delta, float* dq_acc, int Hq, int Dqk, int Dv,
-                               __nv_bfloat16* dk, __nv_bfloat16* dv, int64_t k_sb, int64_t k_ss, int64_t k_sh,
-                               int64_t v_sb, int64_t v_ss, int64_t v_sh, int Hkv) {
+                               float* dk_acc, float* dv_acc, __nv_bfloat16* dk, __nv_bfloat16* dv, int64_t k_sb,
+                               int64_t k_ss, int64_t k_sh, int64_t v_sb, int64_t v_ss, int64_t v_sh, int Hkv) {
   const int64_t rows = (int64_t)g.B * g.Sq;
+  const int lanes = min(32, Dv / 8);
   const int lane = threadIdx.x & 31;
+  const int sub = lane % lanes, grp = lane / lanes, per_warp = 32 / lanes;
   const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x / 32);
-  for (int64_t wrk = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) / 32; wrk < rows * Hq; wrk += nwarps) {
-    const int h = (int)(wrk % Hq);
-    const int64_t f = wrk / Hq;
-    const int b = (int)(f / g.Sq), s = (int)(f - (int64_t)b * g.Sq);
-    const int64_t off = b * o_sb + (int64_t)s * o_ss + h * o_sh;
+  for (int64_t base = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) / 32 * per_warp; base < rows * Hq;
+       base += nwarps * per_warp) {
+    const int64_t wrk = base + grp;
     float acc = 0.f;
-    for (int d = lane * 8; d < Dv; d += 256) {
-      uint4 ug = *reinterpret_cast<const uint4*>(dout + off + d);
-      uint4 uo = *reinterpret_cast<const uint4*>(out + off + d);
-      const __nv_bfloat162* pg = reinterpret_cast<const __nv_bfloat162*>(&ug);
-      const __nv_bfloat162* po = reinterpret_cast<const __nv_bfloat162*>(&uo);
+    int64_t f = 0;
+    int h = 0;
+    if (wrk < rows * Hq) {
+      h = (int)(wrk % Hq);
+      f = wrk / Hq;
+      const int b = (int)(f / g.Sq), s = (int)(f - (int64_t)b * g.Sq);
+      const int64_t off = b * o_sb + (int64_t)s * o_ss + h * o_sh;
+      for (int d = sub * 8; d < Dv; d += lanes * 8) {
+        uint4 ug = *reinterpret_cast<const uint4*>(dout + off + d);
+        uint4 uo = *reinterpret_cast<const uint4*>(out + off + d);
+        const __nv_bfloat162* pg = reinterpret_cast<const __nv_bfloat162*>(&ug);
+        const __nv_bfloat162* po = reinterpret_cast<const __nv_bfloat162*>(&uo);
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        float2 a = __bfloat1622float2(pg[j]), c = __bfloat1622float2(po[j]);
-        acc = fmaf(a.x, c.x, acc);
-        acc = fmaf(a.y, c.y, acc);
+        for (int j = 0; j < 4; ++j) {
+          float2 x = __bfloat1622float2(pg[j]), y = __bfloat1622float2(po[j]);
+          acc = fmaf(x.x, y.x, acc);
+          acc = fmaf(x.y, y.y, acc);
+        }
       }
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    if (lane == 0) delta[(int64_t)h * rows + f] = acc;
+    for (int o = lanes / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (sub == 0 && wrk < rows * Hq) delta[(int64_t)h * rows + f] = acc;
   }
   const int64_t tid = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
   const int64_t nthr = (int64_t)gridDim.x * blockDim.x;
+  const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
   const int64_t n4 = rows * Hq * Dqk / 4;
-  for (int64_t x = tid; x < n4; x += nthr) reinterpret_cast<float4*>(dq_acc)[x] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int64_t x = tid; x < n4; x += nthr) reinterpret_cast<float4*>(dq_acc)[x] = z4;
+  const int64_t krows_all = (int64_t)g.B * g.Sk;
+  if (dk_acc) {
+    const int64_t nk4 = krows_all * Hkv * Dqk / 4, nv4 = krows_all * Hkv * Dv / 4;
+    for (int64_t x = tid; x < nk4; x += nthr) reinterpret_cast<float4*>(dk_acc)[x] = z4;
+    for (int64_t x = tid; x < nv4; x += nthr) reinterpret_cast<float4*>(dv_acc)[x] = z4;
+    return;
+  }
   const int first = cu_k_at(g, seg_count(g));
-  const int64_t krows = (int64_t)g.B * g.Sk - first;
+  const int64_t krows = krows_all - first;
   if (krows > 0) {
     const int gk = Dqk / 8, gv = Dv / 8;
     const int64_t nk = krows * Hkv * (gk + gv);
@@ -336,21 +458,39 @@ __global__ void bwd_pre_kernel(SegInfo g, const __nv_bfloat16* dout, const __nv_
   }
 }
 
-__global__ void dq_convert_kernel(const float* dq_acc, __nv_bfloat16* dq, int B, int Sq, int Hq, int Dqk,
-                                  int64_t q_sb, int64_t q_ss, int64_t q_sh, float scale) {
-  const int groups = Dqk / 8;
-  const int64_t total = (int64_t)B * Sq * Hq * groups;
+// bf16 out = scale * fp32 accumulator ([rows][H][D], packed) in the tensor's own layout.
+__device__ __forceinline__ void convert_rows(const float* acc, __nv_bfloat16* dst, int64_t x, int Sr, int H, int D,
+                                             int64_t sb, int64_t ss, int64_t sh, float scale) {
+  const int groups = D / 8;
+  const int gidx = (int)(x % groups);
+  const int64_t rh = x / groups;
+  const int h = (int)(rh % H);
+  const int64_t f = rh / H;
+  const int b = (int)(f / Sr), s = (int)(f - (int64_t)b * Sr);
+  const float4 a = reinterpret_cast<const float4*>(acc + rh * D)[2 * gidx];
+  const float4 c = reinterpret_cast<const float4*>(acc + rh * D)[2 * gidx + 1];
+  reinterpret_cast<uint4*>(dst + b * sb + (int64_t)s * ss + h * sh)[gidx] =
+      make_uint4(pack_bf16x2(a.x * scale, a.y * scale), pack_bf16x2(a.z * scale, a.w * scale),
+                 pack_bf16x2(c.x * scale, c.y * scale), pack_bf16x2(c.z * scale, c.w * scale));
+}
+
+// dQ = scale * dQacc, and (when accumulated) dK = scale * dKacc, dV = dVacc.
+__global__ void bwd_convert_kernel(const float* dq_acc, __nv_bfloat16* dq, int64_t nq, int Sq, int Hq, int Dqk,
+                                   int64_t q_sb, int64_t q_ss, int64_t q_sh, const float* dk_acc, __nv_bfloat16* dk,
+                                   const float* dv_acc, __nv_bfloat16* dv, int64_t nk, int Sk, int Hkv, int Dv,
+                                   int64_t k_sb, int64_t k_ss, int64_t k_sh, int64_t v_sb, int64_t v_ss, int64_t v_sh,
+                                   float scale) {
+  const int64_t nk_dk = dk_acc ? nk * Hkv * (Dqk / 8) : 0;
+  const int64_t nk_dv = dk_acc ? nk * Hkv * (Dv / 8) : 0;
+  const int64_t nq_all = nq * Hq * (Dqk / 8);
+  const int64_t total = nq_all + nk_dk + nk_dv;
   for (int64_t x = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; x < total; x += (int64_t)gridDim.x * blockDim.x) {
-    const int gidx = (int)(x % groups);
-    const int64_t rh = x / groups;
-    const int h = (int)(rh % Hq);
-    const int64_t f = rh / Hq;
-    const int b = (int)(f / Sq), s = (int)(f - (int64_t)b * Sq);
-    const float4 a = reinterpret_cast<const float4*>(dq_acc + rh * Dqk)[2 * gidx];
-    const float4 c = reinterpret_cast<const float4*>(dq_acc + rh * Dqk)[2 * gidx + 1];
-    reinterpret_cast<uint4*>(dq + b * q_sb + (int64_t)s * q_ss + h * q_sh)[gidx] =
-        make_uint4(pack_bf16x2(a.x * scale, a.y * scale), pack_bf16x2(a.z * scale, a.w * scale),
-                   pack_bf16x2(c.x * scale, c.y * scale), pack_bf16x2(c.z * scale, c.w * scale));
+    if (x < nq_all)
+      convert_rows(dq_acc, dq, x, Sq, Hq, Dqk, q_sb, q_ss, q_sh, scale);
+    else if (x < nq_all + nk_dk)
+      convert_rows(dk_acc, dk, x - nq_all, Sk, Hkv, Dqk, k_sb, k_ss, k_sh, scale);
+    else
+      convert_rows(dv_acc, dv, x - nq_all - nk_dk, Sk, Hkv, Dv, v_sb, v_ss, v_sh, 1.f);
   }
 }
 
@@ -366,6 +506,13 @@ int grid_for(int64_t work, int threads) {
 cudaError_t launch_schedule(const SegInfo& g, int over_keys, int2* items, int* n_items, int* seg_prefix, int item_cap,
                             int* status, cudaStream_t st) {
   schedule_kernel<<<1, kScanThreads, 0, st>>>(g, over_keys, items, n_items, seg_prefix, item_cap, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_schedule(const SegInfo& g, int G, int Hkv, int split_target, int4* items, int* n_items,
+                                int* seg_prefix, int item_cap, int* status, cudaStream_t st) {
+  bwd_schedule_kernel<<<1, kScanThreads, 0, st>>>(g, G, Hkv, split_target, items, n_items, seg_prefix, item_cap,
+                                                  status);
   return cudaGetLastError();
 }
 
@@ -385,8 +532,8 @@ cudaError_t launch_build_segments(const int32_t* ids, int B, int Sk, int Lq, int
 
 cudaError_t launch_pad_fixup(__nv_bfloat16* out, float* lse, const int32_t* qids, int B, int Lq, int Hq, int Dv,
                              int64_t o_sb, int64_t o_ss, int64_t o_sh, int64_t l_sb, int64_t l_sh, cudaStream_t st) {
-  pad_fixup_kernel<<<grid_for((int64_t)B * Lq * Hq * (Dv / 8), 256), 256, 0, st>>>(out, lse, qids, B, Lq, Hq, Dv, o_sb,
-                                                                                  o_ss, o_sh, l_sb, l_sh);
+  pad_fixup_kernel<<<grid_for((int64_t)B * Lq * 32, 256), 256, 0, st>>>(out, lse, qids, B, Lq, Hq, Dv, o_sb, o_ss,
+                                                                        o_sh, l_sb, l_sh);
   return cudaGetLastError();
 }
 
@@ -398,17 +545,27 @@ cudaError_t launch_lse_merge(const __nv_bfloat16* o1, const float* l1, const __n
 
 cudaError_t launch_bwd_pre(const SegInfo& g, const __nv_bfloat16* dout, const __nv_bfloat16* out, int64_t o_sb,
                            int64_t o_ss, int64_t o_sh, float* delta, float* dq_acc, int Hq, int Dqk, int Dv,
-                           __nv_bfloat16* dk, __nv_bfloat16* dv, int64_t k_sb, int64_t k_ss, int64_t k_sh,
-                           int64_t v_sb, int64_t v_ss, int64_t v_sh, int Hkv, cudaStream_t st) {
-  bwd_pre_kernel<<<grid_for((int64_t)g.B * g.Sq * Hq * 32, 256), 256, 0, st>>>(
-      g, dout, out, o_sb, o_ss, o_sh, delta, dq_acc, Hq, Dqk, Dv, dk, dv, k_sb, k_ss, k_sh, v_sb, v_ss, v_sh, Hkv);
+                           float* dk_acc, float* dv_acc, __nv_bfloat16* dk, __nv_bfloat16* dv, int64_t k_sb,
+                           int64_t k_ss, int64_t k_sh, int64_t v_sb, int64_t v_ss, int64_t v_sh, int Hkv,
+                           cudaStream_t st) {
+  const int64_t work = (int64_t)g.B * g.Sq * Hq * Dqk / 4 + (int64_t)g.B * g.Sk * Hkv * (Dqk + Dv) / 4;
+  bwd_pre_kernel<<<grid_for(work, 256), 256, 0, st>>>(g, dout, out, o_sb, o_ss, o_sh, delta, dq_acc, Hq, Dqk, Dv,
+                                                       dk_acc, dv_acc, dk, dv, k_sb, k_ss, k_sh, v_sb, v_ss, v_sh,
+                                                       Hkv);
   return cudaGetLastError();
 }
 
-cudaError_t launch_dq_convert(const float* dq_acc, __nv_bfloat16* dq, int B, int Sq, int Hq, int Dqk, int64_t q_sb,
-                              int64_t q_ss, int64_t q_sh, float scale, cudaStream_t st) {
-  dq_convert_kernel<<<grid_for((int64_t)B * Sq * Hq * (Dqk / 8), 256), 256, 0, st>>>(dq_acc, dq, B, Sq, Hq, Dqk, q_sb,
-                                                                                    q_ss, q_sh, scale);
+cudaError_t launch_bwd_convert(const float* dq_acc, __nv_bfloat16* dq, bool have_q, int B, int Sq, int Hq, int Dqk,
+                               int64_t q_sb, int64_t q_ss, int64_t q_sh, const float* dk_acc, __nv_bfloat16* dk,
+                               const float* dv_acc, __nv_bfloat16* dv, int Sk, int Hkv, int Dv, int64_t k_sb,
+                               int64_t k_ss, int64_t k_sh, int64_t v_sb, int64_t v_ss, int64_t v_sh, float scale,
+                               cudaStream_t st) {
+  const int64_t nq = have_q ? (int64_t)B * Sq : 0, nk = (int64_t)B * Sk;
+  const int64_t work = nq * Hq * (Dqk / 8) + (dk_acc ? nk * Hkv * ((Dqk + Dv) / 8) : 0);
+  if (work == 0) return cudaSuccess;
+  bwd_convert_kernel<<<grid_for(work, 256), 256, 0, st>>>(dq_acc, dq, nq, Sq, Hq, Dqk, q_sb, q_ss, q_sh, dk_acc, dk,
+                                                          dv_acc, dv, nk, Sk, Hkv, Dv, k_sb, k_ss, k_sh, v_sb, v_ss,
+                                                          v_sh, scale);
   return cudaGetLastError();
 }
 

@@ -35,6 +35,7 @@ namespace psf {
 struct BwdParams {
   CUtensorMap tm_q, tm_k, tm_v, tm_do;  // bf16 (d, s, h, b) views, box (64, 128)
   CUtensorMap tm_dq;                    // fp32 dQ accumulator [rows][Hq][Dqk], box (32, 32)
+  CUtensorMap tm_dk, tm_dv;             // fp32 dK / dV accumulators [rows][Hkv][D], box (32, 32)
   SegInfo seg;
   const float* lse;
   int64_t l_sb, l_sh;
@@ -46,7 +47,7 @@ struct BwdParams {
   int64_t v_sb, v_ss, v_sh;
   int Hq, Hkv;
   float scale, scale_log2;
-  const int2* items;  // (segment, key tile), heaviest first
+  const int4* items;  // (segment, key tile, first step, end step), heaviest first
   const int* n_items;
   int* status;
   uint64_t limit_ns;
@@ -77,19 +78,24 @@ struct BwdCfg {
   static_assert(DUAL || (DQK == 192 && DV == 128), "single-region plan is laid out for (192, 128)");
 };
 
+// One work unit: a key tile of one KV head and a range [k0, k1) of its steps.
+// Step k is query head hk * G + k / nqt and query tile qt0 + k % nqt.
 struct BwdItem {
   int s, kt, hk;
   int cq0, ck0, m, n;
   int qt0, nqt;  // query tiles [qt0, qt0 + nqt) see this key tile
+  int k0, k1;
 };
 
 __device__ __forceinline__ BwdItem bwd_decode(const BwdParams& p, int w) {
   BwdItem t;
   const int item = w / p.Hkv;
   t.hk = w - item * p.Hkv;
-  const int2 it = p.items[item];
+  const int4 it = p.items[item];
   t.s = it.x;
   t.kt = it.y;
+  t.k0 = it.z;
+  t.k1 = it.w;
   t.cq0 = cu_q_at(p.seg, t.s);
   t.ck0 = cu_k_at(p.seg, t.s);
   t.m = cu_q_at(p.seg, t.s + 1) - t.cq0;
@@ -158,7 +164,7 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_kernel(const __grid_constant_
       bool ok = true;
       for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
         const BwdItem t = bwd_decode(p, w);
-        if (t.nqt == 0) continue;
+        if (t.k1 == t.k0) continue;
         if (!wait_bar(&kv_empty, (nz & 1) ^ 1, ctl)) break;
         mbar_arrive_expect_tx(&kv_full, (C::KCH + C::VCH) * kChunkBytes);
         const int fk = t.ck0 + t.kt * kBN, bk = fk / p.seg.Sk, sk = fk - bk * p.seg.Sk;
@@ -167,20 +173,19 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_kernel(const __grid_constant_
         for (int c = 0; c < C::VCH; ++c)
           tma_load_4d(smem + C::V_OFF + c * kChunkBytes, &p.tm_v, &kv_full, c * 64, sk, t.hk, bk);
         ++nz;
-        for (int h = t.hk * G; h < (t.hk + 1) * G && ok; ++h) {
-          for (int qt = t.qt0; qt < t.qt0 + t.nqt; ++qt) {
-            if (!wait_bar(&q_empty, (gstep & 1) ^ 1, ctl)) {
-              ok = false;
-              break;
-            }
-            mbar_arrive_expect_tx(&q_full, (C::KCH + C::VCH) * kChunkBytes);
-            const int fq = t.cq0 + qt * kBM, bq = fq / p.seg.Sq, sq = fq - bq * p.seg.Sq;
-            for (int c = 0; c < C::KCH; ++c)
-              tma_load_4d(smem + C::Q_OFF + c * kChunkBytes, &p.tm_q, &q_full, c * 64, sq, h, bq);
-            for (int c = 0; c < C::VCH; ++c)
-              tma_load_4d(smem + C::DO_OFF + c * kChunkBytes, &p.tm_do, &q_full, c * 64, sq, h, bq);
-            ++gstep;
+        for (int k = t.k0; k < t.k1; ++k) {
+          const int h = t.hk * G + k / t.nqt, qt = t.qt0 + k % t.nqt;
+          if (!wait_bar(&q_empty, (gstep & 1) ^ 1, ctl)) {
+            ok = false;
+            break;
           }
+          mbar_arrive_expect_tx(&q_full, (C::KCH + C::VCH) * kChunkBytes);
+          const int fq = t.cq0 + qt * kBM, bq = fq / p.seg.Sq, sq = fq - bq * p.seg.Sq;
+          for (int c = 0; c < C::KCH; ++c)
+            tma_load_4d(smem + C::Q_OFF + c * kChunkBytes, &p.tm_q, &q_full, c * 64, sq, h, bq);
+          for (int c = 0; c < C::VCH; ++c)
+            tma_load_4d(smem + C::DO_OFF + c * kChunkBytes, &p.tm_do, &q_full, c * 64, sq, h, bq);
+          ++gstep;
         }
       }
       if (nz > 0) wait_bar_drain(&kv_full, (nz - 1) & 1, p.limit_ns);
@@ -199,12 +204,11 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_kernel(const __grid_constant_
       bool ok = true;
       for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
         const BwdItem t = bwd_decode(p, w);
-        if (t.nqt == 0) continue;
+        if (t.k1 == t.k0) continue;
         if (!wait_bar(&kv_full, nz & 1, ctl)) break;
         if (nz > 0 && !wait_bar(&acc_free, (nz - 1) & 1, ctl)) break;
         tc_fence_after();
-        const int nsteps = G * t.nqt;
-        for (int k = 0; k < nsteps && ok; ++k, ++gstep) {
+        for (int k = t.k0; k < t.k1 && ok; ++k, ++gstep) {
           if (!wait_bar(&q_full, gstep & 1, ctl)) {
             ok = false;
             break;
@@ -242,7 +246,7 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_kernel(const __grid_constant_
                      sdesc_sw128(do_a + c * kChunkBytes + kk * 32, 16, 1024), id_sq, (c | kk) != 0);
           }
           mma_commit(&dp_full);
-          const uint32_t first = (k == 0) ? 1u : 0u;
+          const uint32_t first = (k == t.k0) ? 1u : 0u;
           if (!C::DUAL) {
             // P^T is already in shared memory: dV can start while dS is computed.
 #pragma unroll
@@ -301,7 +305,7 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_kernel(const __grid_constant_
       const int fk = t.ck0 + j, bk = fk / p.seg.Sk, sk = fk - bk * p.seg.Sk;
       __nv_bfloat16* dk_row = p.dk + bk * p.k_sb + (int64_t)sk * p.k_ss + t.hk * p.k_sh;
       __nv_bfloat16* dv_row = p.dv + bk * p.v_sb + (int64_t)sk * p.v_ss + t.hk * p.v_sh;
-      if (t.nqt == 0) {
+      if (t.k1 == t.k0) {
         if (valid) {
           for (int c = 0; c < DQK / 8; ++c) reinterpret_cast<uint4*>(dk_row)[c] = make_uint4(0, 0, 0, 0);
           for (int c = 0; c < DV / 8; ++c) reinterpret_cast<uint4*>(dv_row)[c] = make_uint4(0, 0, 0, 0);
@@ -309,9 +313,10 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_kernel(const __grid_constant_
         continue;
       }
       const int delta = t.n - t.m;
-      for (int h = t.hk * G; h < (t.hk + 1) * G && ok; ++h) {
-        for (int qt = t.qt0; qt < t.qt0 + t.nqt; ++qt, ++gstep) {
-          const int i0 = qt * kBM;
+      {
+        for (int k = t.k0; k < t.k1; ++k, ++gstep) {
+          const int h = t.hk * G + k / t.nqt;
+          const int i0 = (t.qt0 + k % t.nqt) * kBM;
           // Per-key visible query columns [q_lo, q_hi) of this tile.
           int q_lo = p.seg.causal ? j - delta - i0 : -0x40000000;
           int q_hi = t.m - i0;
@@ -492,9 +497,10 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_kernel(const __grid_constant_
     bool ok = true;
     for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
       const BwdItem t = bwd_decode(p, w);
-      if (t.nqt == 0) continue;
-      for (int h = t.hk * G; h < (t.hk + 1) * G && ok; ++h) {
-        for (int qt = t.qt0; qt < t.qt0 + t.nqt; ++qt, ++gstep) {
+      if (t.k1 == t.k0) continue;
+      {
+        for (int k = t.k0; k < t.k1; ++k, ++gstep) {
+          const int h = t.hk * G + k / t.nqt, qt = t.qt0 + k % t.nqt;
           if (!wait_bar(&dq_full, gstep & 1, ctl)) {
             ok = false;
             break;

@@ -12,13 +12,18 @@
 //          dQ = dS K then lands in X (the MMAs run in issue order, so dQ
 //          overwrites P^T only after dV has read it).
 //   SMEM   K, V resident per key tile; Q double-buffered; dO single-buffered
-//          but released right after dV, its last reader, so the next tile's
-//          dO loads while dK and dQ run; dS^T (bf16, 128-byte swizzled) read
-//          K-major by dK and M-major by dQ; the dQ read-out stages its fp32
-//          boxes in the dS^T buffer once the dQ MMA has consumed it.
+//          but released right after dV, its last reader; dS^T (bf16, 128-byte
+//          swizzled) read K-major by dK and M-major by dQ; the dQ read-out
+//          stages its fp32 boxes in the dS^T buffer once the dQ MMA has
+//          consumed it; a separate 16 KB area stages the dK/dV epilogue.
+//   Work   a unit is a key tile of one KV head and a range of its (query head,
+//          query tile) steps; the scheduler cuts heavy key tiles into several
+//          ranges so that the SMs finish together. dV and dK accumulate in
+//          TMEM across the range (all query heads of the GQA group when the
+//          range covers them) and are added into fp32 accumulators with TMA
+//          reduce-add; a convert kernel writes the bf16 results.
 //   Warps  0 TMA producer, 1 MMA issuer, 2 TMEM allocator, 4-7 compute
-//          (thread = key row: P, dS, and the dK/dV epilogue), 8-11 dQ read-out
-//          (TMA reduce-add of 32 x 32 fp32 boxes into the global accumulator).
+//          (thread = key row: P, dS, then the dK/dV epilogue), 8-11 dQ read-out.
 // The compute warps prefetch the next step's lse and Delta into registers.
 #pragma once
 
@@ -37,8 +42,9 @@ struct BwdDualCfg {
   static constexpr int Q_OFF = V_OFF + VCH * kChunkBytes;  // two slots
   static constexpr int Q_SLOT = KCH * kChunkBytes;
   static constexpr int DO_OFF = Q_OFF + 2 * Q_SLOT;
-  static constexpr int DS_OFF = DO_OFF + VCH * kChunkBytes;  // dS^T; later the dQ staging (4 warps x 2 x 4 KB)
-  static constexpr int ROWV_OFF = DS_OFF + 2 * kChunkBytes;
+  static constexpr int DS_OFF = DO_OFF + VCH * kChunkBytes;  // dS^T; then the dQ staging (4 warps x 2 x 4 KB)
+  static constexpr int EPI_OFF = DS_OFF + 2 * kChunkBytes;   // dK/dV staging (4 warps x 4 KB)
+  static constexpr int ROWV_OFF = EPI_OFF + 4 * 4096;
   static constexpr int SMEM_BYTES = ROWV_OFF + 2 * 4 * 128 * 4 + 1024;
   static constexpr int T_DV = 0;
   static constexpr int T_DK = DV;
@@ -53,8 +59,8 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_dual_kernel(const __grid_cons
   using C = BwdDualCfg<DQK, DV>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  float* lse_s = reinterpret_cast<float*>(smem + C::ROWV_OFF);  // [4 warps][128]
-  float* dl_s = lse_s + 4 * 128;
+  float* nlse_s = reinterpret_cast<float*>(smem + C::ROWV_OFF);  // [4 warps][128]: -lse * log2(e)
+  float* ndl_s = nlse_s + 4 * 128;                                // [4 warps][128]: -Delta
 
   __shared__ uint64_t kv_full, kv_empty, q_full[2], q_empty[2], do_full, do_empty, s_full, dp_full, ds_full,
       ds_free, dq_full, dq_free, stg_free, acc_done, acc_free, drain;
@@ -108,7 +114,7 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_dual_kernel(const __grid_cons
       bool ok = true;
       for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
         const BwdItem t = bwd_decode(p, w);
-        if (t.nqt == 0) continue;
+        if (t.k1 == t.k0) continue;
         if (!wait_bar(&kv_empty, (nz & 1) ^ 1, ctl)) break;
         mbar_arrive_expect_tx(&kv_full, (C::KCH + C::VCH) * kChunkBytes);
         const int fk = t.ck0 + t.kt * kBN, bk = fk / p.seg.Sk, sk = fk - bk * p.seg.Sk;
@@ -117,26 +123,24 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_dual_kernel(const __grid_cons
         for (int c = 0; c < C::VCH; ++c)
           tma_load_4d(smem + C::V_OFF + c * kChunkBytes, &p.tm_v, &kv_full, c * 64, sk, t.hk, bk);
         ++nz;
-        for (int h = t.hk * G; h < (t.hk + 1) * G && ok; ++h) {
-          for (int qt = t.qt0; qt < t.qt0 + t.nqt; ++qt, ++gstep) {
-            const int fq = t.cq0 + qt * kBM, bq = fq / p.seg.Sq, sq = fq - bq * p.seg.Sq;
-            const int qs = gstep & 1;
-            if (!wait_bar(&q_empty[qs], ((gstep >> 1) & 1) ^ 1, ctl)) {
-              ok = false;
-              break;
-            }
-            mbar_arrive_expect_tx(&q_full[qs], C::KCH * kChunkBytes);
-            for (int c = 0; c < C::KCH; ++c)
-              tma_load_4d(smem + C::Q_OFF + qs * C::Q_SLOT + c * kChunkBytes, &p.tm_q, &q_full[qs], c * 64, sq, h,
-                          bq);
-            if (!wait_bar(&do_empty, (gstep & 1) ^ 1, ctl)) {
-              ok = false;
-              break;
-            }
-            mbar_arrive_expect_tx(&do_full, C::VCH * kChunkBytes);
-            for (int c = 0; c < C::VCH; ++c)
-              tma_load_4d(smem + C::DO_OFF + c * kChunkBytes, &p.tm_do, &do_full, c * 64, sq, h, bq);
+        for (int k = t.k0; k < t.k1; ++k, ++gstep) {
+          const int h = t.hk * G + k / t.nqt, qt = t.qt0 + k % t.nqt;
+          const int fq = t.cq0 + qt * kBM, bq = fq / p.seg.Sq, sq = fq - bq * p.seg.Sq;
+          const int qs = gstep & 1;
+          if (!wait_bar(&q_empty[qs], ((gstep >> 1) & 1) ^ 1, ctl)) {
+            ok = false;
+            break;
           }
+          mbar_arrive_expect_tx(&q_full[qs], C::KCH * kChunkBytes);
+          for (int c = 0; c < C::KCH; ++c)
+            tma_load_4d(smem + C::Q_OFF + qs * C::Q_SLOT + c * kChunkBytes, &p.tm_q, &q_full[qs], c * 64, sq, h, bq);
+          if (!wait_bar(&do_empty, (gstep & 1) ^ 1, ctl)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&do_full, C::VCH * kChunkBytes);
+          for (int c = 0; c < C::VCH; ++c)
+            tma_load_4d(smem + C::DO_OFF + c * kChunkBytes, &p.tm_do, &do_full, c * 64, sq, h, bq);
         }
       }
       if (nz > 0) wait_bar_drain(&kv_full, (nz - 1) & 1, p.limit_ns);
@@ -156,12 +160,11 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_dual_kernel(const __grid_cons
       bool ok = true;
       for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
         const BwdItem t = bwd_decode(p, w);
-        if (t.nqt == 0) continue;
+        if (t.k1 == t.k0) continue;
         if (!wait_bar(&kv_full, nz & 1, ctl)) break;
         if (nz > 0 && !wait_bar(&acc_free, (nz - 1) & 1, ctl)) break;
         tc_fence_after();
-        const int nsteps = G * t.nqt;
-        for (int k = 0; k < nsteps && ok; ++k, ++gstep) {
+        for (int k = t.k0; k < t.k1 && ok; ++k, ++gstep) {
           const int qs = gstep & 1;
           const uint32_t q_a = q_a0 + qs * C::Q_SLOT;
           const uint32_t rx = tmem + ((gstep & 1) ? C::T_B : C::T_A);
@@ -195,7 +198,7 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_dual_kernel(const __grid_cons
             break;
           }
           tc_fence_after();
-          const uint32_t first = (k == 0) ? 1u : 0u;
+          const uint32_t first = (k == t.k0) ? 1u : 0u;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
             mma_ts(tmem + C::T_DV, rx + kk * 8, sdesc_sw128(do_a + kk * 2048, kChunkBytes, 1024), id_dv,
@@ -226,63 +229,52 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_dual_kernel(const __grid_cons
     const int wq = warp - 4;
     const int r = threadIdx.x - 128;  // key row within the tile
     const uint32_t lane_base = (uint32_t)(32 * wq) << 16;
-    float* my_lse = lse_s + wq * 128;
-    float* my_dl = dl_s + wq * 128;
+    float* my_nlse = nlse_s + wq * 128;
+    float* my_ndl = ndl_s + wq * 128;
     uint8_t* ds_s = smem + C::DS_OFF;
+    uint8_t* epi = smem + C::EPI_OFF + wq * 4096;
     const float sl2 = p.scale_log2;
+    const float2 sl2x2 = make_float2(sl2, sl2), one2 = make_float2(1.f, 1.f), zero2 = make_float2(0.f, 0.f);
     uint32_t nz = 0, gstep = 0;
     bool ok = true;
-    // lse * log2(e) (+inf where the row carries no probability) and Delta of
-    // 4 query columns per lane for one step.
-    auto fetch_rows = [&](const BwdItem& t, int h, int i0, float (&lv)[4], float (&dv)[4]) {
+    // -lse * log2(e) (-inf where the row carries no probability, so P = 0)
+    // and -Delta of 4 query columns per lane for one step.
+    auto fetch_rows = [&](const BwdItem& t, int k, float (&lv)[4], float (&dv)[4]) {
+      const int h = t.hk * G + k / t.nqt, i0 = (t.qt0 + k % t.nqt) * kBM;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int qc = lane * 4 + e;
         const int f = t.cq0 + i0 + qc;
-        lv[e] = CUDART_INF_F;
+        lv[e] = -CUDART_INF_F;
         dv[e] = 0.f;
         if (i0 + qc < t.m && f < p.q_rows) {
           const int bq = f / p.seg.Sq, sq = f - bq * p.seg.Sq;
           const float x = p.lse[bq * p.l_sb + h * p.l_sh + sq];
-          lv[e] = x == -CUDART_INF_F ? CUDART_INF_F : x * 1.4426950408889634f;
-          dv[e] = p.delta[(int64_t)h * p.q_rows + f];
+          lv[e] = x == -CUDART_INF_F ? -CUDART_INF_F : -x * 1.4426950408889634f;
+          dv[e] = -p.delta[(int64_t)h * p.q_rows + f];
         }
       }
     };
     for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
       const BwdItem t = bwd_decode(p, w);
+      if (t.k1 == t.k0) continue;
       const int j = t.kt * kBN + r;  // segment-local key index
       const bool valid = j < t.n;
-      const int fk = t.ck0 + j, bk = fk / p.seg.Sk, sk = fk - bk * p.seg.Sk;
-      __nv_bfloat16* dk_row = p.dk + bk * p.k_sb + (int64_t)sk * p.k_ss + t.hk * p.k_sh;
-      __nv_bfloat16* dv_row = p.dv + bk * p.v_sb + (int64_t)sk * p.v_ss + t.hk * p.v_sh;
-      if (t.nqt == 0) {
-        if (valid) {
-          for (int c = 0; c < DQK / 8; ++c) reinterpret_cast<uint4*>(dk_row)[c] = make_uint4(0, 0, 0, 0);
-          for (int c = 0; c < DV / 8; ++c) reinterpret_cast<uint4*>(dv_row)[c] = make_uint4(0, 0, 0, 0);
-        }
-        continue;
-      }
       const int delta = t.n - t.m;
-      const int nsteps = G * t.nqt;
       float nlv[4], ndv[4];
-      fetch_rows(t, t.hk * G, t.qt0 * kBM, nlv, ndv);
-      for (int k = 0; k < nsteps && ok; ++k, ++gstep) {
-        const int h = t.hk * G + k / t.nqt;
+      fetch_rows(t, t.k0, nlv, ndv);
+      for (int k = t.k0; k < t.k1; ++k, ++gstep) {
         const int i0 = (t.qt0 + k % t.nqt) * kBM;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          my_lse[lane * 4 + e] = nlv[e];
-          my_dl[lane * 4 + e] = ndv[e];
-        }
+        *reinterpret_cast<float4*>(my_nlse + lane * 4) = make_float4(nlv[0], nlv[1], nlv[2], nlv[3]);
+        *reinterpret_cast<float4*>(my_ndl + lane * 4) = make_float4(ndv[0], ndv[1], ndv[2], ndv[3]);
         __syncwarp();
-        if (k + 1 < nsteps) fetch_rows(t, t.hk * G + (k + 1) / t.nqt, (t.qt0 + (k + 1) % t.nqt) * kBM, nlv, ndv);
+        if (k + 1 < t.k1) fetch_rows(t, k + 1, nlv, ndv);
         // Per-key visible query columns [q_lo, q_hi) of this tile.
         int q_lo = p.seg.causal ? j - delta - i0 : -0x40000000;
         int q_hi = t.m - i0;
         if (p.seg.window > 0) q_hi = min(q_hi, j - delta + p.seg.window - i0);
         if (!valid) q_lo = q_hi = 0;
-        const bool masked = q_lo > 0 || q_hi < kBM;
+        const bool masked = __any_sync(0xffffffffu, q_lo > 0 || q_hi < kBM);
         if (!wait_bar(&s_full, gstep & 1, ctl) || !wait_bar(&dp_full, gstep & 1, ctl)) {
           ok = false;
           break;
@@ -297,22 +289,29 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_dual_kernel(const __grid_cons
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           uint32_t sv[32], pv[32];
-          tmem_ld32(rx + c * 32, sv);
-          tmem_ld32(ry + c * 32, pv);
+          tmem_ld32x2(rx + c * 32, ry + c * 32, sv, pv);
           uint32_t pk[16], dk2[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            float pr[2], dr[2];
+          for (int e4 = 0; e4 < 8; ++e4) {
+            const float4 nl = *reinterpret_cast<const float4*>(my_nlse + c * 32 + e4 * 4);
+            const float4 nd = *reinterpret_cast<const float4*>(my_ndl + c * 32 + e4 * 4);
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              const int qc = c * 32 + 2 * e + u;
-              float pe = ex2_approx(fmaf(__uint_as_float(sv[2 * e + u]), sl2, -my_lse[qc]));
-              if (masked && (qc < q_lo || qc >= q_hi)) pe = 0.f;
-              pr[u] = pe;
-              dr[u] = pe * (__uint_as_float(pv[2 * e + u]) - my_dl[qc]);
+            for (int hf = 0; hf < 2; ++hf) {
+              const int e = e4 * 2 + hf;
+              const float2 nl2 = hf ? make_float2(nl.z, nl.w) : make_float2(nl.x, nl.y);
+              const float2 nd2 = hf ? make_float2(nd.z, nd.w) : make_float2(nd.x, nd.y);
+              const float2 x = fma2(make_float2(__uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1])), sl2x2, nl2);
+              float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
+              if (masked) {
+                const int qc = c * 32 + 2 * e;
+                if (qc < q_lo || qc >= q_hi) p0 = 0.f;
+                if (qc + 1 < q_lo || qc + 1 >= q_hi) p1 = 0.f;
+              }
+              const float2 dd = fma2(make_float2(__uint_as_float(pv[2 * e]), __uint_as_float(pv[2 * e + 1])), one2, nd2);
+              const float2 ds = fma2(make_float2(p0, p1), dd, zero2);
+              pk[e] = pack_bf16x2(p0, p1);
+              dk2[e] = pack_bf16x2(ds.x, ds.y);
             }
-            pk[e] = pack_bf16x2(pr[0], pr[1]);
-            dk2[e] = pack_bf16x2(dr[0], dr[1]);
           }
           // P^T (bf16) over the S^T columns already read: chunk c -> columns [16c, 16c + 16).
           tmem_st16(rx + c * 16, pk);
@@ -328,43 +327,37 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_dual_kernel(const __grid_cons
         if (lane == 0) mbar_arrive(&ds_full);
       }
       if (!ok) break;
-      // dK / dV epilogue for this key tile.
+      // Epilogue: add this range's dV and dK (scale applied by the convert) into
+      // the fp32 accumulators, 32 x 32 boxes per warp.
       if (!wait_bar(&acc_done, nz & 1, ctl)) break;
       tc_fence_after();
+      const int fk = t.ck0 + t.kt * kBN + 32 * wq, bk = fk / p.seg.Sk, sk = fk - bk * p.seg.Sk;
 #pragma unroll 1
-      for (int c = 0; c < DV / 32; ++c) {
+      for (int c = 0; c < (DV + DQK) / 32; ++c) {
+        const bool is_v = c < DV / 32;
         uint32_t a[32];
-        tmem_ld32(tmem + lane_base + C::T_DV + c * 32, a);
-        if (valid) {
-          uint4* dst = reinterpret_cast<uint4*>(dv_row + c * 32);
+        tmem_ld32(tmem + lane_base + (is_v ? C::T_DV + c * 32 : C::T_DK + (c - DV / 32) * 32), a);
+        if (c == (DV + DQK) / 32 - 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acc_free);
+        }
+        if (lane == 0) bulk_wait_group_read0();
+        __syncwarp();
 #pragma unroll
-          for (int u = 0; u < 4; ++u)
-            dst[u] = make_uint4(pack_bf16x2(__uint_as_float(a[8 * u]), __uint_as_float(a[8 * u + 1])),
-                                pack_bf16x2(__uint_as_float(a[8 * u + 2]), __uint_as_float(a[8 * u + 3])),
-                                pack_bf16x2(__uint_as_float(a[8 * u + 4]), __uint_as_float(a[8 * u + 5])),
-                                pack_bf16x2(__uint_as_float(a[8 * u + 6]), __uint_as_float(a[8 * u + 7])));
+        for (int u = 0; u < 8; ++u)
+          *reinterpret_cast<uint4*>(epi + sw128_offset(lane, u)) =
+              make_uint4(a[4 * u], a[4 * u + 1], a[4 * u + 2], a[4 * u + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_reduce_add_4d(is_v ? &p.tm_dv : &p.tm_dk, epi, (is_v ? c : c - DV / 32) * 32, sk, t.hk, bk);
+          bulk_commit_group();
         }
       }
-      const float sc = p.scale;
-#pragma unroll 1
-      for (int c = 0; c < DQK / 32; ++c) {
-        uint32_t a[32];
-        tmem_ld32(tmem + lane_base + C::T_DK + c * 32, a);
-        if (valid) {
-          uint4* dst = reinterpret_cast<uint4*>(dk_row + c * 32);
-#pragma unroll
-          for (int u = 0; u < 4; ++u)
-            dst[u] = make_uint4(pack_bf16x2(__uint_as_float(a[8 * u]) * sc, __uint_as_float(a[8 * u + 1]) * sc),
-                                pack_bf16x2(__uint_as_float(a[8 * u + 2]) * sc, __uint_as_float(a[8 * u + 3]) * sc),
-                                pack_bf16x2(__uint_as_float(a[8 * u + 4]) * sc, __uint_as_float(a[8 * u + 5]) * sc),
-                                pack_bf16x2(__uint_as_float(a[8 * u + 6]) * sc, __uint_as_float(a[8 * u + 7]) * sc));
-        }
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_free);
       ++nz;
     }
+    if (lane == 0) bulk_wait_group0();
   } else if (warp >= 8) {
     // ------------------------------------------------------------ dQ read-out
     const int wq = warp - 8;
@@ -374,47 +367,45 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_dual_kernel(const __grid_cons
     bool ok = true;
     for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
       const BwdItem t = bwd_decode(p, w);
-      if (t.nqt == 0) continue;
-      for (int h = t.hk * G; h < (t.hk + 1) * G && ok; ++h) {
-        for (int qt = t.qt0; qt < t.qt0 + t.nqt; ++qt, ++gstep) {
-          if (!wait_bar(&dq_full, gstep & 1, ctl)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t rq = tmem + lane_base + ((gstep & 1) ? C::T_B : C::T_A);
-          const int fq = t.cq0 + qt * kBM + 32 * wq, bq = fq / p.seg.Sq, sq = fq - bq * p.seg.Sq;
-#pragma unroll 1
-          for (int c = 0; c < DQK / 32; ++c) {
-            uint32_t a[32];
-            tmem_ld32(rq + c * 32, a);
-            if (c == DQK / 32 - 1) {
-              // Every TMEM read of this step is done: the region can take the next dP.
-              tc_fence_before();
-              __syncwarp();
-              if (lane == 0) mbar_arrive(&dq_free);
-            }
-            uint8_t* box = stg + (c & 1) * 4096;
-            if (c >= 2) {
-              if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-              __syncwarp();
-            }
-#pragma unroll
-            for (int u = 0; u < 8; ++u)
-              *reinterpret_cast<uint4*>(box + sw128_offset(lane, u)) =
-                  make_uint4(a[4 * u], a[4 * u + 1], a[4 * u + 2], a[4 * u + 3]);
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-              tma_reduce_add_4d(&p.tm_dq, box, c * 32, sq, h, bq);
-              bulk_commit_group();
-            }
-          }
-          // The staging boxes live in the dS^T buffer: free them for the next dS^T.
-          if (lane == 0) bulk_wait_group_read0();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&stg_free);
+      if (t.k1 == t.k0) continue;
+      for (int k = t.k0; k < t.k1; ++k, ++gstep) {
+        const int h = t.hk * G + k / t.nqt, qt = t.qt0 + k % t.nqt;
+        if (!wait_bar(&dq_full, gstep & 1, ctl)) {
+          ok = false;
+          break;
         }
+        tc_fence_after();
+        const uint32_t rq = tmem + lane_base + ((gstep & 1) ? C::T_B : C::T_A);
+        const int fq = t.cq0 + qt * kBM + 32 * wq, bq = fq / p.seg.Sq, sq = fq - bq * p.seg.Sq;
+        uint32_t a[DQK / 32][32];
+#pragma unroll
+        for (int c = 0; c < DQK / 32; c += 2) tmem_ld32x2(rq + c * 32, rq + (c + 1) * 32, a[c], a[c + 1]);
+        // Every TMEM read of this step is done: the region can take the next dP.
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&dq_free);
+#pragma unroll
+        for (int c = 0; c < DQK / 32; ++c) {
+          uint8_t* box = stg + (c & 1) * 4096;
+          if (c >= 2) {
+            if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+            __syncwarp();
+          }
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            *reinterpret_cast<uint4*>(box + sw128_offset(lane, u)) =
+                make_uint4(a[c][4 * u], a[c][4 * u + 1], a[c][4 * u + 2], a[c][4 * u + 3]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_reduce_add_4d(&p.tm_dq, box, c * 32, sq, h, bq);
+            bulk_commit_group();
+          }
+        }
+        // The staging boxes live in the dS^T buffer: free them for the next dS^T.
+        if (lane == 0) bulk_wait_group_read0();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&stg_free);
       }
     }
     if (lane == 0) bulk_wait_group0();

@@ -114,10 +114,11 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_wide_kernel(const __grid_cons
       for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
         int part;
         const BwdItem t = decode(w, part);
-        if (t.nqt == 0) continue;
+        if (t.k1 == t.k0) continue;
         const int fk = t.ck0 + t.kt * kBN, bk = fk / p.seg.Sk, sk = fk - bk * p.seg.Sk;
-        for (int h = t.hk * G; h < (t.hk + 1) * G && ok; ++h) {
-          for (int qt = t.qt0; qt < t.qt0 + t.nqt && ok; ++qt) {
+        {
+          for (int k = t.k0; k < t.k1 && ok; ++k) {
+            const int h = t.hk * G + k / t.nqt, qt = t.qt0 + k % t.nqt;
             const int fq = t.cq0 + qt * kBM, bq = fq / p.seg.Sq, sq = fq - bq * p.seg.Sq;
             for (int c = 0; c < C::NCH && ok; ++c) {
               ok = load(&p.tm_k, c * 64, sk, t.hk, bk) && load(&p.tm_q, c * 64, sq, h, bq);
@@ -157,10 +158,9 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_wide_kernel(const __grid_cons
       for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
         int part;
         const BwdItem t = decode(w, part);
-        if (t.nqt == 0) continue;
+        if (t.k1 == t.k0) continue;
         if (nz > 0 && !wait_bar(&acc_free, (nz - 1) & 1, ctl)) break;
-        const int nsteps = G * t.nqt;
-        for (int k = 0; k < nsteps && ok; ++k, ++gstep) {
+        for (int k = t.k0; k < t.k1 && ok; ++k, ++gstep) {
           if (gstep > 0 && !wait_bar(&dq_free, (gstep - 1) & 1, ctl)) {
             ok = false;
             break;
@@ -203,7 +203,7 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_wide_kernel(const __grid_cons
             break;
           }
           tc_fence_after();
-          const uint32_t first = (k == 0) ? 1u : 0u;
+          const uint32_t first = (k == t.k0) ? 1u : 0u;
           // dV_part += P^T dO_part (two 64-column halves)
           for (int hh = 0; hh < 2 && ok; ++hh) {
             uint32_t da;
@@ -265,7 +265,7 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_wide_kernel(const __grid_cons
       const int fk = t.ck0 + j, bk = fk / p.seg.Sk, sk = fk - bk * p.seg.Sk;
       __nv_bfloat16* dk_row = p.dk + bk * p.k_sb + (int64_t)sk * p.k_ss + t.hk * p.k_sh + part * 128;
       __nv_bfloat16* dv_row = p.dv + bk * p.v_sb + (int64_t)sk * p.v_ss + t.hk * p.v_sh + part * 128;
-      if (t.nqt == 0) {
+      if (t.k1 == t.k0) {
         if (valid) {
           for (int c = 0; c < 16; ++c) {
             reinterpret_cast<uint4*>(dk_row)[c] = make_uint4(0, 0, 0, 0);
@@ -275,9 +275,10 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_wide_kernel(const __grid_cons
         continue;
       }
       const int delta = t.n - t.m;
-      for (int h = t.hk * G; h < (t.hk + 1) * G && ok; ++h) {
-        for (int qt = t.qt0; qt < t.qt0 + t.nqt; ++qt, ++gstep) {
-          const int i0 = qt * kBM;
+      {
+        for (int k = t.k0; k < t.k1; ++k, ++gstep) {
+          const int h = t.hk * G + k / t.nqt;
+          const int i0 = (t.qt0 + k % t.nqt) * kBM;
           int q_lo = p.seg.causal ? j - delta - i0 : -0x40000000;
           int q_hi = t.m - i0;
           if (p.seg.window > 0) q_hi = min(q_hi, j - delta + p.seg.window - i0);
@@ -378,9 +379,10 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_wide_kernel(const __grid_cons
     for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
       int part;
       const BwdItem t = decode(w, part);
-      if (t.nqt == 0) continue;
-      for (int h = t.hk * G; h < (t.hk + 1) * G && ok; ++h) {
-        for (int qt = t.qt0; qt < t.qt0 + t.nqt; ++qt, ++gstep) {
+      if (t.k1 == t.k0) continue;
+      {
+        for (int k = t.k0; k < t.k1; ++k, ++gstep) {
+          const int h = t.hk * G + k / t.nqt, qt = t.qt0 + k % t.nqt;
           if (!wait_bar(&dq_full, gstep & 1, ctl)) {
             ok = false;
             break;

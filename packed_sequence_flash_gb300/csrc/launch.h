@@ -15,6 +15,10 @@ struct BwdParams;
 // (over_keys = 1) of every segment; validates the segment arrays.
 cudaError_t launch_schedule(const SegInfo& g, int over_keys, int2* items, int* n_items, int* seg_prefix,
                             int item_cap, int* status, cudaStream_t st);
+// Backward work list: key tiles split into (first step, end step) sub-ranges
+// when split_target > 0; items are int4 (segment, key tile, first, end).
+cudaError_t launch_bwd_schedule(const SegInfo& g, int G, int Hkv, int split_target, int4* items, int* n_items,
+                                int* seg_prefix, int item_cap, int* status, cudaStream_t st);
 // out = 0 and lse = -inf for query rows at or past cu_q[nseg].
 cudaError_t launch_fwd_tail(const SegInfo& g, __nv_bfloat16* out, int64_t o_sb, int64_t o_ss, int64_t o_sh, float* lse,
                             int64_t l_sb, int64_t l_sh, int Hq, int Dv, cudaStream_t st);
@@ -29,14 +33,19 @@ cudaError_t launch_pad_fixup(__nv_bfloat16* out, float* lse, const int32_t* qids
                              int64_t o_sb, int64_t o_ss, int64_t o_sh, int64_t l_sb, int64_t l_sh, cudaStream_t st);
 cudaError_t launch_lse_merge(const __nv_bfloat16* o1, const float* l1, const __nv_bfloat16* o2, const float* l2,
                              float* of, __nv_bfloat16* ob, float* l, int T, int H, int D, cudaStream_t st);
-// Delta = rowsum(dO * O) (fp32, [Hq][rows]); zero the fp32 dQ accumulator; zero
-// dK / dV rows at or past cu_k[nseg].
+// Delta = rowsum(dO * O) (fp32, [Hq][rows]); zero the fp32 accumulators
+// (dK/dV ones when given; otherwise dK / dV rows at or past cu_k[nseg]).
 cudaError_t launch_bwd_pre(const SegInfo& g, const __nv_bfloat16* dout, const __nv_bfloat16* out, int64_t o_sb,
                            int64_t o_ss, int64_t o_sh, float* delta, float* dq_acc, int Hq, int Dqk, int Dv,
-                           __nv_bfloat16* dk, __nv_bfloat16* dv, int64_t k_sb, int64_t k_ss, int64_t k_sh,
-                           int64_t v_sb, int64_t v_ss, int64_t v_sh, int Hkv, cudaStream_t st);
-// dQ = scale * dQacc in bf16 with q's layout.
-cudaError_t launch_dq_convert(const float* dq_acc, __nv_bfloat16* dq, int B, int Sq, int Hq, int Dqk, int64_t q_sb,
-                              int64_t q_ss, int64_t q_sh, float scale, cudaStream_t st);
+                           float* dk_acc, float* dv_acc, __nv_bfloat16* dk, __nv_bfloat16* dv, int64_t k_sb,
+                           int64_t k_ss, int64_t k_sh, int64_t v_sb, int64_t v_ss, int64_t v_sh, int Hkv,
+                           cudaStream_t st);
+// dQ = scale * dQacc (bf16, q's layout); with accumulators also dK = scale *
+// dKacc and dV = dVacc.
+cudaError_t launch_bwd_convert(const float* dq_acc, __nv_bfloat16* dq, bool have_q, int B, int Sq, int Hq, int Dqk,
+                               int64_t q_sb, int64_t q_ss, int64_t q_sh, const float* dk_acc, __nv_bfloat16* dk,
+                               const float* dv_acc, __nv_bfloat16* dv, int Sk, int Hkv, int Dv, int64_t k_sb,
+                               int64_t k_ss, int64_t k_sh, int64_t v_sb, int64_t v_ss, int64_t v_sh, float scale,
+                               cudaStream_t st);
 
 }  // namespace psf

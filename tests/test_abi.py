@@ -46,9 +46,9 @@ def test_workspace_size_queries_need_no_gpu():
 
     lib = _lib.load()
     a = lib.psf_attn_fwd_workspace_size(8192, 11)
-    b = lib.psf_attn_bwd_workspace_size(8192, 8192, 11, 16, 128)
+    b = lib.psf_attn_bwd_workspace_size(8192, 8192, 11, 16, 4, 128, 128)
     assert a >= 256 + 8 * (8192 // 128)
-    assert b >= 4 * 8192 * 16 * 128 + 4 * 16 * 8192
+    assert b >= 4 * 8192 * 16 * 128 + 4 * 16 * 8192 + 4 * 8192 * 4 * 256
     assert lib.psf_attn_fwd_workspace_size(-1, 0) == 0
 
 
