@@ -265,35 +265,64 @@ def our_arm(args):
     if psf.device_status() != 0:
         raise RuntimeError("device status after warm-up is not OK")
 
-    # ---- device-timed steps (inputs resident in HBM)
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    stops = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    sampler = ClockSampler(dev.index) if rank == 0 else None
-    time.sleep(0.3)
+    # ---- eager steps: per-step time and the main kernels' own launch times
+    def timed(run_one, n):
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        stops = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        for i in range(n):
+            flush.zero_()
+            starts[i].record()
+            run_one()
+            stops[i].record()
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in zip(starts, stops)]
+
+    run_step = lambda: step(q, k, v, do, ids, qids)
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
-    t0 = time.time()
     lib.psf_kernel_timing(1)
-    for i in range(args.steps):
-        flush.zero_()
-        starts[i].record()
-        step(q, k, v, do, ids, qids)
-        stops[i].record()
-    torch.cuda.synchronize()
+    eager_steps = timed(run_step, args.steps)
     lib.psf_kernel_timing(0)
-    t1 = time.time()
-    if dist:
-        dist.barrier()
-    clocks = sampler.summary(t0, t1) if sampler else None
-    per_step = [a.elapsed_time(b) for a, b in zip(starts, stops)]
-    ms = statistics.mean(per_step)
     kt = {}
     for kind, name in ((0, "fwd"), (1, "bwd")):
         tot = ctypes_double()
         n = ctypes_int()
         _lib.check(lib.psf_kernel_times_ms(kind, tot, n))
         kt[name] = (tot.value, n.value)
+    if psf.device_status() != 0:
+        raise RuntimeError("device status after the eager steps is not OK")
+
+    # ---- the step replayed as one CUDA graph (same kernels, no launch gaps)
+    graph, graph_note = None, None
+    try:
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            run_step()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            run_step()
+        graph.replay()
+        torch.cuda.synchronize()
+        if psf.device_status() != 0:
+            raise RuntimeError("device status after a graph replay is not OK")
+    except Exception as exc:  # capture unsupported here: report the eager timing instead
+        graph, graph_note = None, f"graph capture failed: {type(exc).__name__}: {exc}"[:200]
+    sampler = ClockSampler(dev.index) if rank == 0 else None
+    time.sleep(0.3)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    per_step = timed(graph.replay, args.steps) if graph is not None else timed(run_step, args.steps)
+    t1 = time.time()
+    if dist:
+        dist.barrier()
+    clocks = sampler.summary(t0, t1) if sampler else None
+    ms = statistics.mean(per_step)
     if psf.device_status() != 0:
         raise RuntimeError("device status after the timed steps is not OK")
     ms_max = ms
@@ -369,6 +398,8 @@ def our_arm(args):
         "fwd_tflops": f_fwd / (fwd_ms * 1e-3) / 1e12 if fwd_ms > 0 else None,
         "bwd_tflops": f_bwd / (bwd_ms * 1e-3) / 1e12 if bwd_ms > 0 else None,
         "step_ms_spread": {"min": min(per_step), "median": statistics.median(per_step), "max": max(per_step)},
+        "timing": ("each step replayed as one captured CUDA graph" if graph is not None else graph_note),
+        "ms_per_step_eager": statistics.mean(eager_steps),
         "roofline": roofline, "roofline_other": dict(roof[other], kernel=other),
         "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms},

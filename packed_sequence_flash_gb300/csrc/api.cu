@@ -10,7 +10,7 @@
 #include <string>
 #include <vector>
 
-#include "../../include/psf.h"
+#include "psf.h"
 #include "bwd.cuh"
 #include "fwd.cuh"
 #include "launch.h"

@@ -12,6 +12,9 @@ namespace {
 
 constexpr int kScanThreads = 1024;
 constexpr int kBuckets = 1024;
+// Per-segment tile prefixes live in shared memory when they fit (the common
+// case); the workspace copy is used beyond that.
+constexpr int kSmemPrefix = 6144;
 
 // Exclusive block-wide prefix sum over kScanThreads threads; *total gets the sum.
 __device__ int block_excl_scan(int v, int* total) {
@@ -86,6 +89,8 @@ __global__ void __launch_bounds__(kScanThreads) schedule_kernel(SegInfo g, int o
   __shared__ int bad;
   const int tid = threadIdx.x;
   const int nseg = seg_count(g);
+  __shared__ int prefix_smem[kSmemPrefix];
+  int* pref = nseg + 1 <= kSmemPrefix ? prefix_smem : seg_prefix;
   const int max_q = g.dev_meta ? g.dev_meta[1] : g.max_q;
   const int max_k = g.dev_meta ? g.dev_meta[2] : g.max_k;
   const int Tq = g.B * g.Sq, Tk = g.B * g.Sk;
@@ -108,10 +113,10 @@ __global__ void __launch_bounds__(kScanThreads) schedule_kernel(SegInfo g, int o
     }
     int tot;
     const int ex = block_excl_scan(cnt, &tot);
-    if (s < nseg) seg_prefix[s] = carry + ex;
+    if (s < nseg) pref[s] = carry + ex;
     carry += tot;
   }
-  if (tid == 0) seg_prefix[nseg] = carry;
+  if (tid == 0) pref[nseg] = carry;
   __syncthreads();
   if (bad || carry > item_cap) {
     if (tid == 0) {
@@ -121,8 +126,8 @@ __global__ void __launch_bounds__(kScanThreads) schedule_kernel(SegInfo g, int o
     return;
   }
   for (int x = tid; x < carry; x += kScanThreads) {
-    const int s = find_segment(seg_prefix, nseg, x);
-    const int c = tile_cost(g, s, x - seg_prefix[s], over_keys);
+    const int s = find_segment(pref, nseg, x);
+    const int c = tile_cost(g, s, x - pref[s], over_keys);
     atomicAdd(&hist[min(c, kBuckets - 1)], 1);
   }
   __syncthreads();
@@ -134,8 +139,8 @@ __global__ void __launch_bounds__(kScanThreads) schedule_kernel(SegInfo g, int o
   hist[rb] = 0;
   __syncthreads();
   for (int x = tid; x < carry; x += kScanThreads) {
-    const int s = find_segment(seg_prefix, nseg, x);
-    const int t = x - seg_prefix[s];
+    const int s = find_segment(pref, nseg, x);
+    const int t = x - pref[s];
     const int b = min(tile_cost(g, s, t, over_keys), kBuckets - 1);
     const int pos = start[b] + atomicAdd(&hist[b], 1);
     items[pos] = make_int2(s, t);
@@ -156,6 +161,8 @@ __global__ void __launch_bounds__(kScanThreads) bwd_schedule_kernel(SegInfo g, i
   __shared__ unsigned long long total_steps;
   const int tid = threadIdx.x;
   const int nseg = seg_count(g);
+  __shared__ int prefix_smem[kSmemPrefix];
+  int* pref = nseg + 1 <= kSmemPrefix ? prefix_smem : seg_prefix;
   const int max_q = g.dev_meta ? g.dev_meta[1] : g.max_q;
   const int max_k = g.dev_meta ? g.dev_meta[2] : g.max_k;
   const int Tq = g.B * g.Sq, Tk = g.B * g.Sk;
@@ -181,10 +188,10 @@ __global__ void __launch_bounds__(kScanThreads) bwd_schedule_kernel(SegInfo g, i
     }
     int tot;
     const int ex = block_excl_scan(cnt, &tot);
-    if (s < nseg) seg_prefix[s] = carry + ex;
+    if (s < nseg) pref[s] = carry + ex;
     carry += tot;
   }
-  if (tid == 0) seg_prefix[nseg] = carry;
+  if (tid == 0) pref[nseg] = carry;
   __syncthreads();
   if (bad) {
     if (tid == 0) {
@@ -195,8 +202,8 @@ __global__ void __launch_bounds__(kScanThreads) bwd_schedule_kernel(SegInfo g, i
   }
   unsigned long long mine = 0;
   for (int x = tid; x < carry; x += kScanThreads) {
-    const int s = find_segment(seg_prefix, nseg, x);
-    mine += (unsigned long long)G * tile_cost(g, s, x - seg_prefix[s], 1);
+    const int s = find_segment(pref, nseg, x);
+    mine += (unsigned long long)G * tile_cost(g, s, x - pref[s], 1);
   }
   atomicAdd(&total_steps, mine);
   __syncthreads();
@@ -207,8 +214,8 @@ __global__ void __launch_bounds__(kScanThreads) bwd_schedule_kernel(SegInfo g, i
   }
   int nsub_total = 0;
   for (int x = tid; x < carry; x += kScanThreads) {
-    const int s = find_segment(seg_prefix, nseg, x);
-    const int steps = G * tile_cost(g, s, x - seg_prefix[s], 1);
+    const int s = find_segment(pref, nseg, x);
+    const int steps = G * tile_cost(g, s, x - pref[s], 1);
     const int nsub = steps == 0 ? 1 : (int)(((long long)steps + smax - 1) / smax);
     nsub_total += nsub;
     for (int i = 0; i < nsub; ++i) {
@@ -232,8 +239,8 @@ __global__ void __launch_bounds__(kScanThreads) bwd_schedule_kernel(SegInfo g, i
   hist[rb] = 0;
   __syncthreads();
   for (int x = tid; x < carry; x += kScanThreads) {
-    const int s = find_segment(seg_prefix, nseg, x);
-    const int t = x - seg_prefix[s];
+    const int s = find_segment(pref, nseg, x);
+    const int t = x - pref[s];
     const int steps = G * tile_cost(g, s, t, 1);
     const int nsub = steps == 0 ? 1 : (int)(((long long)steps + smax - 1) / smax);
     for (int i = 0; i < nsub; ++i) {

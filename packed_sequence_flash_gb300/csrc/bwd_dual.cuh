@@ -6,16 +6,21 @@
 // Same arithmetic as bwd.cuh, laid out for head dims up to 128 so that every
 // operand stream overlaps the tensor core:
 //   TMEM   dV [0, Dv) | dK [Dv, Dv + Dqk) | region A [256, 384) | region B [384, 512)
-//          Step g writes S^T into one region (X) and dP^T into the other (Y);
-//          the roles swap every step. P^T (bf16) is written back over the
-//          first 64 columns of X and feeds dV += P^T dO as the TMEM operand;
-//          dQ = dS K then lands in X (the MMAs run in issue order, so dQ
-//          overwrites P^T only after dV has read it).
+//          A holds S^T, then P^T (bf16, first 64 columns) as the TMEM operand of
+//          dV += P^T dO; B holds dP^T, then dQ = dS K.
+//   Order  per step g the MMA warp issues dP(g) -> B, dV(g) once P^T is
+//          written, then, as soon as dS^T(g) is in shared memory, S(g+1) -> A
+//          ahead of dK(g) and dQ(g) -> B, so the next step's element-wise pass
+//          runs while the tensor core finishes this one.
 //   SMEM   K, V resident per key tile; Q double-buffered; dO single-buffered
 //          but released right after dV, its last reader; dS^T (bf16, 128-byte
-//          swizzled) read K-major by dK and M-major by dQ; the dQ read-out
-//          stages its fp32 boxes in the dS^T buffer once the dQ MMA has
-//          consumed it; a separate 16 KB area stages the dK/dV epilogue.
+//          swizzled) read K-major by dK and M-major by dQ; a 16 KB area stages
+//          the dQ read-out's fp32 boxes; the dK/dV epilogue stages in the dS^T
+//          buffer, which the compute warps own between steps.
+//   Steps  the compute warps make two passes: P^T (stored to A as packed
+//          bf16), then dS^T from dP^T and the stored P^T. TMEM reads run one
+//          32-column chunk ahead of the arithmetic; S(g+1) is issued only after
+//          dS^T(g), so the second pass can still read P^T(g) from A.
 //   Work   a unit is a key tile of one KV head and a range of its (query head,
 //          query tile) steps; the scheduler cuts heavy key tiles into several
 //          ranges so that the SMs finish together. dV and dK accumulate in
@@ -42,9 +47,9 @@ struct BwdDualCfg {
   static constexpr int Q_OFF = V_OFF + VCH * kChunkBytes;  // two slots
   static constexpr int Q_SLOT = KCH * kChunkBytes;
   static constexpr int DO_OFF = Q_OFF + 2 * Q_SLOT;
-  static constexpr int DS_OFF = DO_OFF + VCH * kChunkBytes;  // dS^T; then the dQ staging (4 warps x 2 x 4 KB)
-  static constexpr int EPI_OFF = DS_OFF + 2 * kChunkBytes;   // dK/dV staging (4 warps x 4 KB)
-  static constexpr int ROWV_OFF = EPI_OFF + 4 * 4096;
+  static constexpr int DS_OFF = DO_OFF + VCH * kChunkBytes;  // dS^T; the dK/dV epilogue stages here (4 x 8 KB)
+  static constexpr int STG_OFF = DS_OFF + 2 * kChunkBytes;   // dQ read-out staging (4 warps x 4 KB)
+  static constexpr int ROWV_OFF = STG_OFF + 4 * 4096;
   static constexpr int SMEM_BYTES = ROWV_OFF + 2 * 4 * 128 * 4 + 1024;
   static constexpr int T_DV = 0;
   static constexpr int T_DK = DV;
@@ -62,8 +67,8 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_dual_kernel(const __grid_cons
   float* nlse_s = reinterpret_cast<float*>(smem + C::ROWV_OFF);  // [4 warps][128]: -lse * log2(e)
   float* ndl_s = nlse_s + 4 * 128;                                // [4 warps][128]: -Delta
 
-  __shared__ uint64_t kv_full, kv_empty, q_full[2], q_empty[2], do_full, do_empty, s_full, dp_full, ds_full,
-      ds_free, dq_full, dq_free, stg_free, acc_done, acc_free, drain;
+  __shared__ uint64_t kv_full, kv_empty, q_full[2], q_empty[2], do_full, do_empty, s_full, dp_full, p_full,
+      ds_full, ds_free, dq_full, dq_free, acc_done, acc_free, drain;
   __shared__ uint32_t tmem_base_smem;
   __shared__ int abort_flag;
 
@@ -79,11 +84,11 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_dual_kernel(const __grid_cons
     mbar_init(&do_empty, 1);
     mbar_init(&s_full, 1);
     mbar_init(&dp_full, 1);
+    mbar_init(&p_full, 4);
     mbar_init(&ds_full, 4);
     mbar_init(&ds_free, 1);
     mbar_init(&dq_full, 1);
     mbar_init(&dq_free, 4);
-    mbar_init(&stg_free, 4);
     mbar_init(&acc_done, 1);
     mbar_init(&acc_free, 4);
     mbar_init(&drain, 1);
@@ -156,6 +161,7 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_dual_kernel(const __grid_cons
       constexpr uint32_t id_dq = idesc_bf16_f32(128, DQK, 1, 1);  // dQ  = dS K
       const uint32_t k_a = sbase + C::K_OFF, v_a = sbase + C::V_OFF, q_a0 = sbase + C::Q_OFF;
       const uint32_t do_a = sbase + C::DO_OFF, ds_a = sbase + C::DS_OFF;
+      const uint32_t ra = tmem + C::T_A, rb = tmem + C::T_B;
       uint32_t nz = 0, gstep = 0;
       bool ok = true;
       for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
@@ -164,23 +170,22 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_dual_kernel(const __grid_cons
         if (!wait_bar(&kv_full, nz & 1, ctl)) break;
         if (nz > 0 && !wait_bar(&acc_free, (nz - 1) & 1, ctl)) break;
         tc_fence_after();
-        for (int k = t.k0; k < t.k1 && ok; ++k, ++gstep) {
+        // S of the range's first step; later ones are issued inside the loop.
+        {
           const int qs = gstep & 1;
-          const uint32_t q_a = q_a0 + qs * C::Q_SLOT;
-          const uint32_t rx = tmem + ((gstep & 1) ? C::T_B : C::T_A);
-          const uint32_t ry = tmem + ((gstep & 1) ? C::T_A : C::T_B);
-          if (!wait_bar(&q_full[qs], (gstep >> 1) & 1, ctl)) {
-            ok = false;
-            break;
-          }
+          if (!wait_bar(&q_full[qs], (gstep >> 1) & 1, ctl)) break;
           tc_fence_after();
           for (int c = 0; c < C::KCH; ++c) {
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              mma_ss(rx, sdesc_sw128(k_a + c * kChunkBytes + kk * 32, 16, 1024),
-                     sdesc_sw128(q_a + c * kChunkBytes + kk * 32, 16, 1024), id_sq, (c | kk) != 0);
+              mma_ss(ra, sdesc_sw128(k_a + c * kChunkBytes + kk * 32, 16, 1024),
+                     sdesc_sw128(q_a0 + qs * C::Q_SLOT + c * kChunkBytes + kk * 32, 16, 1024), id_sq, (c | kk) != 0);
           }
           mma_commit(&s_full);
+        }
+        for (int k = t.k0; k < t.k1 && ok; ++k, ++gstep) {
+          const int qs = gstep & 1;
+          const uint32_t q_a = q_a0 + qs * C::Q_SLOT;
           if (!wait_bar(&do_full, gstep & 1, ctl) || (gstep > 0 && !wait_bar(&dq_free, (gstep - 1) & 1, ctl))) {
             ok = false;
             break;
@@ -189,11 +194,11 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_dual_kernel(const __grid_cons
           for (int c = 0; c < C::VCH; ++c) {
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              mma_ss(ry, sdesc_sw128(v_a + c * kChunkBytes + kk * 32, 16, 1024),
+              mma_ss(rb, sdesc_sw128(v_a + c * kChunkBytes + kk * 32, 16, 1024),
                      sdesc_sw128(do_a + c * kChunkBytes + kk * 32, 16, 1024), id_sq, (c | kk) != 0);
           }
           mma_commit(&dp_full);
-          if (!wait_bar(&ds_full, gstep & 1, ctl)) {
+          if (!wait_bar(&p_full, gstep & 1, ctl)) {
             ok = false;
             break;
           }
@@ -201,9 +206,31 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_dual_kernel(const __grid_cons
           const uint32_t first = (k == t.k0) ? 1u : 0u;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            mma_ts(tmem + C::T_DV, rx + kk * 8, sdesc_sw128(do_a + kk * 2048, kChunkBytes, 1024), id_dv,
+            mma_ts(tmem + C::T_DV, ra + kk * 8, sdesc_sw128(do_a + kk * 2048, kChunkBytes, 1024), id_dv,
                    !(first && kk == 0));
           mma_commit(&do_empty);
+          if (!wait_bar(&ds_full, gstep & 1, ctl)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (k + 1 < t.k1) {
+            // Next step's S into A: P^T(g) there has been read by dV(g), issued before.
+            const int qn = (gstep + 1) & 1;
+            if (!wait_bar(&q_full[qn], ((gstep + 1) >> 1) & 1, ctl)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            for (int c = 0; c < C::KCH; ++c) {
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                mma_ss(ra, sdesc_sw128(k_a + c * kChunkBytes + kk * 32, 16, 1024),
+                       sdesc_sw128(q_a0 + qn * C::Q_SLOT + c * kChunkBytes + kk * 32, 16, 1024), id_sq,
+                       (c | kk) != 0);
+            }
+            mma_commit(&s_full);
+          }
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
             mma_ss(tmem + C::T_DK, sdesc_sw128(ds_a + (kk >> 2) * kChunkBytes + (kk & 3) * 32, 16, 1024),
@@ -211,7 +238,7 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_dual_kernel(const __grid_cons
           mma_commit(&q_empty[qs]);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            mma_ss(rx, sdesc_sw128(ds_a + kk * 2048, kChunkBytes, 1024), sdesc_sw128(k_a + kk * 2048, kChunkBytes, 1024),
+            mma_ss(rb, sdesc_sw128(ds_a + kk * 2048, kChunkBytes, 1024), sdesc_sw128(k_a + kk * 2048, kChunkBytes, 1024),
                    id_dq, kk > 0);
           mma_commit(&dq_full);
           mma_commit(&ds_free);
@@ -232,7 +259,7 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_dual_kernel(const __grid_cons
     float* my_nlse = nlse_s + wq * 128;
     float* my_ndl = ndl_s + wq * 128;
     uint8_t* ds_s = smem + C::DS_OFF;
-    uint8_t* epi = smem + C::EPI_OFF + wq * 4096;
+    uint8_t* epi = smem + C::DS_OFF + wq * 8192;  // two 4 KB boxes per warp, used between steps
     const float sl2 = p.scale_log2;
     const float2 sl2x2 = make_float2(sl2, sl2), one2 = make_float2(1.f, 1.f), zero2 = make_float2(0.f, 0.f);
     uint32_t nz = 0, gstep = 0;
@@ -275,51 +302,92 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_dual_kernel(const __grid_cons
         if (p.seg.window > 0) q_hi = min(q_hi, j - delta + p.seg.window - i0);
         if (!valid) q_lo = q_hi = 0;
         const bool masked = __any_sync(0xffffffffu, q_lo > 0 || q_hi < kBM);
-        if (!wait_bar(&s_full, gstep & 1, ctl) || !wait_bar(&dp_full, gstep & 1, ctl)) {
-          ok = false;
-          break;
-        }
-        if (gstep > 0 && (!wait_bar(&ds_free, (gstep - 1) & 1, ctl) || !wait_bar(&stg_free, (gstep - 1) & 1, ctl))) {
+        if (!wait_bar(&s_full, gstep & 1, ctl)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t rx = tmem + lane_base + ((gstep & 1) ? C::T_B : C::T_A);
-        const uint32_t ry = tmem + lane_base + ((gstep & 1) ? C::T_A : C::T_B);
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          uint32_t sv[32], pv[32];
-          tmem_ld32x2(rx + c * 32, ry + c * 32, sv, pv);
-          uint32_t pk[16], dk2[16];
+        const uint32_t ra = tmem + lane_base + C::T_A, rb = tmem + lane_base + C::T_B;
+        // Pass 1: P^T = exp2(S^T * scale * log2 e - lse * log2 e) as packed bf16
+        // over the S^T columns already read (chunk c -> A[16c, 16c + 16)).
+        {
+          uint32_t sa[32], sb[32];
+          tmem_ld32_async(ra, sa);
 #pragma unroll
-          for (int e4 = 0; e4 < 8; ++e4) {
-            const float4 nl = *reinterpret_cast<const float4*>(my_nlse + c * 32 + e4 * 4);
-            const float4 nd = *reinterpret_cast<const float4*>(my_ndl + c * 32 + e4 * 4);
+          for (int c = 0; c < 4; ++c) {
+            uint32_t(&cur)[32] = (c & 1) ? sb : sa;
+            uint32_t(&nxt)[32] = (c & 1) ? sa : sb;
+            tmem_wait_ld32(cur);
+            if (c + 1 < 4) tmem_ld32_async(ra + (c + 1) * 32, nxt);
+            uint32_t pk[16];
 #pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-              const int e = e4 * 2 + hf;
-              const float2 nl2 = hf ? make_float2(nl.z, nl.w) : make_float2(nl.x, nl.y);
-              const float2 nd2 = hf ? make_float2(nd.z, nd.w) : make_float2(nd.x, nd.y);
-              const float2 x = fma2(make_float2(__uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1])), sl2x2, nl2);
-              float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
-              if (masked) {
-                const int qc = c * 32 + 2 * e;
-                if (qc < q_lo || qc >= q_hi) p0 = 0.f;
-                if (qc + 1 < q_lo || qc + 1 >= q_hi) p1 = 0.f;
+            for (int e4 = 0; e4 < 8; ++e4) {
+              const float4 nl = *reinterpret_cast<const float4*>(my_nlse + c * 32 + e4 * 4);
+#pragma unroll
+              for (int hf = 0; hf < 2; ++hf) {
+                const int e = e4 * 2 + hf;
+                const float2 nl2 = hf ? make_float2(nl.z, nl.w) : make_float2(nl.x, nl.y);
+                const float2 x =
+                    fma2(make_float2(__uint_as_float(cur[2 * e]), __uint_as_float(cur[2 * e + 1])), sl2x2, nl2);
+                float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
+                if (masked) {
+                  const int qc = c * 32 + 2 * e;
+                  if (qc < q_lo || qc >= q_hi) p0 = 0.f;
+                  if (qc + 1 < q_lo || qc + 1 >= q_hi) p1 = 0.f;
+                }
+                pk[e] = pack_bf16x2(p0, p1);
               }
-              const float2 dd = fma2(make_float2(__uint_as_float(pv[2 * e]), __uint_as_float(pv[2 * e + 1])), one2, nd2);
-              const float2 ds = fma2(make_float2(p0, p1), dd, zero2);
-              pk[e] = pack_bf16x2(p0, p1);
-              dk2[e] = pack_bf16x2(ds.x, ds.y);
             }
+            // Columns [16c, 16c + 16) of S^T were read with chunk c / 2.
+            tmem_st16_async(ra + c * 16, pk);
           }
-          // P^T (bf16) over the S^T columns already read: chunk c -> columns [16c, 16c + 16).
-          tmem_st16(rx + c * 16, pk);
-          const int chunk = c >> 1, g0 = (c & 1) * 4;
+          tmem_wait_st();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_full);
+        // Pass 2: dS^T = P^T (dP^T - Delta) into shared memory (bf16, swizzled).
+        if (!wait_bar(&dp_full, gstep & 1, ctl) || (gstep > 0 && !wait_bar(&ds_free, (gstep - 1) & 1, ctl))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        {
+          uint32_t da[32], db[32], pa[16], pb[16];
+          tmem_ld32_async(rb, da);
+          tmem_ld16_async(ra, pa);
 #pragma unroll
-          for (int u = 0; u < 4; ++u)
-            *reinterpret_cast<uint4*>(ds_s + chunk * kChunkBytes + sw128_offset(r, g0 + u)) =
-                make_uint4(dk2[4 * u], dk2[4 * u + 1], dk2[4 * u + 2], dk2[4 * u + 3]);
+          for (int c = 0; c < 4; ++c) {
+            uint32_t(&dcur)[32] = (c & 1) ? db : da;
+            uint32_t(&dnxt)[32] = (c & 1) ? da : db;
+            uint32_t(&pcur)[16] = (c & 1) ? pb : pa;
+            uint32_t(&pnxt)[16] = (c & 1) ? pa : pb;
+            tmem_wait_ld32_16(dcur, pcur);
+            if (c + 1 < 4) {
+              tmem_ld32_async(rb + (c + 1) * 32, dnxt);
+              tmem_ld16_async(ra + (c + 1) * 16, pnxt);
+            }
+            uint32_t dk2[16];
+#pragma unroll
+            for (int e4 = 0; e4 < 8; ++e4) {
+              const float4 nd = *reinterpret_cast<const float4*>(my_ndl + c * 32 + e4 * 4);
+#pragma unroll
+              for (int hf = 0; hf < 2; ++hf) {
+                const int e = e4 * 2 + hf;
+                const float2 nd2 = hf ? make_float2(nd.z, nd.w) : make_float2(nd.x, nd.y);
+                const float2 pf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pcur[e]));
+                const float2 dd =
+                    fma2(make_float2(__uint_as_float(dcur[2 * e]), __uint_as_float(dcur[2 * e + 1])), one2, nd2);
+                const float2 ds = fma2(pf, dd, zero2);
+                dk2[e] = pack_bf16x2(ds.x, ds.y);
+              }
+            }
+            const int chunk = c >> 1, g0 = (c & 1) * 4;
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              *reinterpret_cast<uint4*>(ds_s + chunk * kChunkBytes + sw128_offset(r, g0 + u)) =
+                  make_uint4(dk2[4 * u], dk2[4 * u + 1], dk2[4 * u + 2], dk2[4 * u + 3]);
+          }
         }
         fence_proxy_async_smem();
         tc_fence_before();
@@ -342,19 +410,25 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_dual_kernel(const __grid_cons
           __syncwarp();
           if (lane == 0) mbar_arrive(&acc_free);
         }
-        if (lane == 0) bulk_wait_group_read0();
-        __syncwarp();
+        uint8_t* box = epi + (c & 1) * 4096;
+        if (c >= 2) {
+          if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+          __syncwarp();
+        }
 #pragma unroll
         for (int u = 0; u < 8; ++u)
-          *reinterpret_cast<uint4*>(epi + sw128_offset(lane, u)) =
+          *reinterpret_cast<uint4*>(box + sw128_offset(lane, u)) =
               make_uint4(a[4 * u], a[4 * u + 1], a[4 * u + 2], a[4 * u + 3]);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          tma_reduce_add_4d(is_v ? &p.tm_dv : &p.tm_dk, epi, (is_v ? c : c - DV / 32) * 32, sk, t.hk, bk);
+          tma_reduce_add_4d(is_v ? &p.tm_dv : &p.tm_dk, box, (is_v ? c : c - DV / 32) * 32, sk, t.hk, bk);
           bulk_commit_group();
         }
       }
+      // The boxes sit in the dS^T buffer: drain them before the next dS^T.
+      if (lane == 0) bulk_wait_group_read0();
+      __syncwarp();
       ++nz;
     }
     if (lane == 0) bulk_wait_group0();
@@ -362,7 +436,7 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_dual_kernel(const __grid_cons
     // ------------------------------------------------------------ dQ read-out
     const int wq = warp - 8;
     const uint32_t lane_base = (uint32_t)(32 * wq) << 16;
-    uint8_t* stg = smem + C::DS_OFF + wq * 8192;  // two 4 KB boxes per warp
+    uint8_t* box = smem + C::STG_OFF + wq * 4096;
     uint32_t gstep = 0;
     bool ok = true;
     for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
@@ -375,7 +449,7 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_dual_kernel(const __grid_cons
           break;
         }
         tc_fence_after();
-        const uint32_t rq = tmem + lane_base + ((gstep & 1) ? C::T_B : C::T_A);
+        const uint32_t rq = tmem + lane_base + C::T_B;
         const int fq = t.cq0 + qt * kBM + 32 * wq, bq = fq / p.seg.Sq, sq = fq - bq * p.seg.Sq;
         uint32_t a[DQK / 32][32];
 #pragma unroll
@@ -386,11 +460,8 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_dual_kernel(const __grid_cons
         if (lane == 0) mbar_arrive(&dq_free);
 #pragma unroll
         for (int c = 0; c < DQK / 32; ++c) {
-          uint8_t* box = stg + (c & 1) * 4096;
-          if (c >= 2) {
-            if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-            __syncwarp();
-          }
+          if (lane == 0) bulk_wait_group_read0();
+          __syncwarp();
 #pragma unroll
           for (int u = 0; u < 8; ++u)
             *reinterpret_cast<uint4*>(box + sw128_offset(lane, u)) =
@@ -402,10 +473,6 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_dual_kernel(const __grid_cons
             bulk_commit_group();
           }
         }
-        // The staging boxes live in the dS^T buffer: free them for the next dS^T.
-        if (lane == 0) bulk_wait_group_read0();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&stg_free);
       }
     }
     if (lane == 0) bulk_wait_group0();

@@ -70,8 +70,8 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, const C
   uint64_t t0 = globaltimer_ns();
   while (true) {
 #pragma unroll 1
-    for (int i = 0; i < 128; ++i)
-      if (mbar_test(bar, parity)) return true;
+    for (int i = 0; i < 16; ++i)
+      if (mbar_test_sleep(bar, parity, 20000)) return true;
     if (*c.abort_flag) return false;
     if (globaltimer_ns() - t0 > c.limit_ns) {
       atomicCAS(c.status, 0, kStatusTimeout);

@@ -47,6 +47,21 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Like mbar_test, but a thread whose phase is not yet complete may be
+// suspended by the hardware for up to `suspend_ns` (woken early when the phase
+// completes), so waiting warps stop competing for issue slots.
+__device__ __forceinline__ bool mbar_test_sleep(uint64_t* bar, uint32_t parity, uint32_t suspend_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(suspend_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
@@ -155,6 +170,68 @@ __device__ __forceinline__ void tmem_ld32x2(uint32_t taddr_a, uint32_t taddr_b, 
       : PSF_R8(a, 0), PSF_R8(a, 8), PSF_R8(a, 16), PSF_R8(a, 24), PSF_R8(b, 0), PSF_R8(b, 8), PSF_R8(b, 16),
         PSF_R8(b, 24)
       : "r"(taddr_a), "r"(taddr_b)
+      : "memory");
+}
+// Asynchronous 16-column load without a wait: the registers are valid only
+// after tmem_wait_ld16 on the same array, which names them as in/out operands
+// so the compiler cannot read them earlier.
+__device__ __forceinline__ void tmem_ld16_async(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : PSF_R8(r, 0), PSF_R8(r, 8)
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld8_async(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : PSF_R8(r, 0)
+               : "r"(taddr)
+               : "memory");
+}
+#define PSF_RW8(a, o) "+r"(a[o + 0]), "+r"(a[o + 1]), "+r"(a[o + 2]), "+r"(a[o + 3]), "+r"(a[o + 4]), \
+                      "+r"(a[o + 5]), "+r"(a[o + 6]), "+r"(a[o + 7])
+__device__ __forceinline__ void tmem_ld32_async(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : PSF_R8(r, 0), PSF_R8(r, 8), PSF_R8(r, 16), PSF_R8(r, 24)
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld16(uint32_t (&r)[16]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" : PSF_RW8(r, 0), PSF_RW8(r, 8) : : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld16_8(uint32_t (&r)[16], uint32_t (&q)[8]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" : PSF_RW8(r, 0), PSF_RW8(r, 8), PSF_RW8(q, 0) : : "memory");
+}
+// Asynchronous 16-column store; tmem_wait_st completes all of this thread's stores.
+__device__ __forceinline__ void tmem_st16_async(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      PSF_W8(r, 0), PSF_W8(r, 8)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_ld32(uint32_t (&r)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : PSF_RW8(r, 0), PSF_RW8(r, 8), PSF_RW8(r, 16), PSF_RW8(r, 24)
+               :
+               : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld32_16(uint32_t (&r)[32], uint32_t (&q)[16]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : PSF_RW8(r, 0), PSF_RW8(r, 8), PSF_RW8(r, 16), PSF_RW8(r, 24), PSF_RW8(q, 0), PSF_RW8(q, 8)
+               :
+               : "memory");
+}
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};\n\t"
+      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+      PSF_W8(r, 0)
       : "memory");
 }
 // Warp-collective store of 32 columns; waits until the store is done.
