@@ -281,13 +281,13 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, void* out, float*
   p.scale_log2 = scale * 1.4426950408889634f;
   p.items = w.items;
   p.n_items = w.n_items;
+  p.work_next = w.n_items + 1;
   p.status = dev->status;
   p.limit_ns = g_wait_limit_ns;
   const int64_t max_work = (int64_t)w.item_cap * Hq * p.dv_parts;
-  const int grid = (int)(max_work < dev->sms ? max_work : dev->sms);
   TimedLaunch tl;
   const bool timed = timing_begin(0, st, &tl);
-  e = launch_fwd(p, Dqk, Dv / p.dv_parts, grid, st);
+  e = launch_fwd(p, Dqk, Dv / p.dv_parts, dev->sms, max_work, st);
   if (timed) timing_end(&tl, st);
   if (e != cudaSuccess) return cuda_fail(e, "forward launch");
   return PSF_OK;

@@ -1,5 +1,6 @@
-// fwd.cu -- instantiations and launcher of the attention forward kernel.
+// fwd.cu -- instantiations and launcher of the attention forward kernels.
 #include "fwd.cuh"
+#include "fwd_duo.cuh"
 #include "launch.h"
 
 namespace psf {
@@ -13,19 +14,33 @@ cudaError_t run(const FwdParams& p, int grid, cudaStream_t st) {
   attn_fwd_kernel<DQK, DVC><<<grid, 256, smem, st>>>(p);
   return cudaGetLastError();
 }
+template <int D>
+cudaError_t run_duo(const FwdParams& p, int grid, cudaStream_t st) {
+  const int smem = FwdDuoCfg<D>::SMEM_BYTES;
+  cudaError_t e = cudaFuncSetAttribute(attn_fwd_duo_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  attn_fwd_duo_kernel<D><<<grid, 192, smem, st>>>(p);
+  return cudaGetLastError();
+}
 }  // namespace
 
 int fwd_smem_bytes(int dqk, int dvc) {
-  if (dqk == 64 && dvc == 64) return FwdCfg<64, 64>::SMEM_BYTES;
-  if (dqk == 128 && dvc == 128) return FwdCfg<128, 128>::SMEM_BYTES;
+  if (dqk == 64 && dvc == 64) return FwdDuoCfg<64>::SMEM_BYTES;
+  if (dqk == 128 && dvc == 128) return FwdDuoCfg<128>::SMEM_BYTES;
   if (dqk == 192 && dvc == 128) return FwdCfg<192, 128>::SMEM_BYTES;
   if (dqk == 512 && dvc == 256) return FwdCfg<512, 256>::SMEM_BYTES;
   return -1;
 }
 
-cudaError_t launch_fwd(const FwdParams& p, int dqk, int dvc, int grid, cudaStream_t st) {
-  if (dqk == 64 && dvc == 64) return run<64, 64>(p, grid, st);
-  if (dqk == 128 && dvc == 128) return run<128, 128>(p, grid, st);
+// Head dims 64 and 128 run two CTAs per SM (attn_fwd_duo_kernel); the wider
+// ones one CTA per SM.
+cudaError_t launch_fwd(const FwdParams& p, int dqk, int dvc, int sms, int64_t max_work, cudaStream_t st) {
+  const bool duo = (dqk == 64 && dvc == 64) || (dqk == 128 && dvc == 128);
+  const int64_t cap = (int64_t)sms * (duo ? 2 : 1);
+  const int grid = (int)(max_work < cap ? max_work : cap);
+  if (grid <= 0) return cudaSuccess;
+  if (dqk == 64 && dvc == 64) return run_duo<64>(p, grid, st);
+  if (dqk == 128 && dvc == 128) return run_duo<128>(p, grid, st);
   if (dqk == 192 && dvc == 128) return run<192, 128>(p, grid, st);
   if (dqk == 512 && dvc == 256) return run<512, 256>(p, grid, st);
   return cudaErrorInvalidValue;

@@ -45,6 +45,7 @@ struct FwdParams {
   float scale_log2;
   const int2* items;  // (segment, q tile), heaviest first
   const int* n_items;
+  int* work_next;  // zeroed by the schedule kernel; kernels that take work dynamically count on it
   int* status;
   uint64_t limit_ns;
 };

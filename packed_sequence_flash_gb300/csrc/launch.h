@@ -12,7 +12,8 @@ struct FwdParams;
 struct BwdParams;
 
 // Heaviest-first work list over query tiles (over_keys = 0) or key tiles
-// (over_keys = 1) of every segment; validates the segment arrays.
+// (over_keys = 1) of every segment; validates the segment arrays. Also zeroes
+// n_items[1], the counter of kernels that take work items dynamically.
 cudaError_t launch_schedule(const SegInfo& g, int over_keys, int2* items, int* n_items, int* seg_prefix,
                             int item_cap, int* status, cudaStream_t st);
 // Backward work list: key tiles split into (first step, end step) sub-ranges
@@ -22,7 +23,8 @@ cudaError_t launch_bwd_schedule(const SegInfo& g, int G, int Hkv, int split_targ
 // out = 0 and lse = -inf for query rows at or past cu_q[nseg].
 cudaError_t launch_fwd_tail(const SegInfo& g, __nv_bfloat16* out, int64_t o_sb, int64_t o_ss, int64_t o_sh, float* lse,
                             int64_t l_sb, int64_t l_sh, int Hq, int Dv, cudaStream_t st);
-cudaError_t launch_fwd(const FwdParams& p, int dqk, int dvc, int grid, cudaStream_t st);
+// Grid: one CTA per SM (two for head dims 64 and 128), at most max_work.
+cudaError_t launch_fwd(const FwdParams& p, int dqk, int dvc, int sms, int64_t max_work, cudaStream_t st);
 cudaError_t launch_bwd(const BwdParams& p, int dqk, int dv, int sms, int item_cap, cudaStream_t st);
 int fwd_smem_bytes(int dqk, int dvc);
 int bwd_smem_bytes(int dqk, int dv);
