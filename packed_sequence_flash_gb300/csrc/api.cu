@@ -375,6 +375,7 @@ int attn_bwd_impl(const void* dout, const void* q, const void* k, const void* v,
     p.scale_log2 = scale * 1.4426950408889634f;
     p.items = w.items;
     p.n_items = w.n_items;
+    p.work_next = w.n_items + 1;
     p.status = dev->status;
     p.limit_ns = g_wait_limit_ns;
     TimedLaunch tl;

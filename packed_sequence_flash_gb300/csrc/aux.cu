@@ -168,6 +168,7 @@ __global__ void __launch_bounds__(kScanThreads) bwd_schedule_kernel(SegInfo g, i
   const int max_k = g.dev_meta ? g.dev_meta[2] : g.max_k;
   const int Tq = g.B * g.Sq, Tk = g.B * g.Sk;
   hist[tid] = 0;
+  if (tid == 0) n_items[1] = 0;  // work counter of kernels that take items dynamically
   if (tid == 0) {
     bad = (g.cu_q && nseg >= 0 && (g.cu_q[0] != 0 || g.cu_k[0] != 0)) ? 1 : 0;
     total_steps = 0;

@@ -49,6 +49,7 @@ struct BwdParams {
   float scale, scale_log2;
   const int4* items;  // (segment, key tile, first step, end step), heaviest first
   const int* n_items;
+  int* work_next;  // zeroed by the schedule kernel; kernels that take work dynamically count on it
   int* status;
   uint64_t limit_ns;
 };

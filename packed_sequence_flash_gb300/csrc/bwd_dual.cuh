@@ -29,6 +29,10 @@
 //          reduce-add; a convert kernel writes the bf16 results.
 //   Warps  0 TMA producer, 1 MMA issuer, 2 TMEM allocator, 4-7 compute
 //          (thread = key row: P, dS, then the dK/dV epilogue), 8-11 dQ read-out.
+//   Work   a CTA starts on unit blockIdx.x of the heaviest-first list, then takes
+//          the next untaken unit from a global counter; the producer passes each
+//          unit's index to the other warps through a two-entry ring in shared
+//          memory (-1 = no more work).
 // The compute warps prefetch the next step's lse and Delta into registers.
 #pragma once
 
@@ -68,7 +72,8 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_dual_kernel(const __grid_cons
   float* ndl_s = nlse_s + 4 * 128;                                // [4 warps][128]: -Delta
 
   __shared__ uint64_t kv_full, kv_empty, q_full[2], q_empty[2], do_full, do_empty, s_full, dp_full, p_full,
-      ds_full, ds_free, dq_full, dq_free, acc_done, acc_free, drain;
+      ds_full, ds_free, dq_full, dq_free, acc_done, acc_free, drain, work_full[2], work_empty[2];
+  __shared__ int work_slot[2];
   __shared__ uint32_t tmem_base_smem;
   __shared__ int abort_flag;
 
@@ -92,6 +97,10 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_dual_kernel(const __grid_cons
     mbar_init(&acc_done, 1);
     mbar_init(&acc_free, 4);
     mbar_init(&drain, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&work_full[i], 1);
+      mbar_init(&work_empty[i], 9);  // the MMA thread, four compute and four dQ warps
+    }
     abort_flag = 0;
     fence_mbar_init();
   }
@@ -107,6 +116,20 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_dual_kernel(const __grid_cons
   const int total = (*p.n_items) * p.Hkv;
   const int G = p.Hq / p.Hkv;
   const uint32_t sbase = smem_u32(smem);
+  // Next work item for the MMA, compute and dQ warps (-1: none left, or abort).
+  uint32_t nwork = 0;
+  auto next_work = [&](bool& ok) -> int {
+    const int ws = nwork & 1;
+    if (!wait_bar(&work_full[ws], (nwork >> 1) & 1, ctl)) {
+      ok = false;
+      return -1;
+    }
+    const int w = work_slot[ws];
+    __syncwarp(__activemask());
+    if (lane == 0) mbar_arrive(&work_empty[ws]);
+    ++nwork;
+    return w;
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -117,8 +140,17 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_dual_kernel(const __grid_cons
       tma_prefetch_desc(&p.tm_do);
       uint32_t nz = 0, gstep = 0;
       bool ok = true;
-      for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+      int w = blockIdx.x;
+      while (ok) {
+        if (w >= total) w = -1;
+        const int ws = nwork & 1;
+        if (!wait_bar(&work_empty[ws], ((nwork >> 1) & 1) ^ 1, ctl)) break;
+        work_slot[ws] = w;
+        mbar_arrive(&work_full[ws]);
+        ++nwork;
+        if (w < 0) break;
         const BwdItem t = bwd_decode(p, w);
+        w = gridDim.x + atomicAdd(p.work_next, 1);
         if (t.k1 == t.k0) continue;
         if (!wait_bar(&kv_empty, (nz & 1) ^ 1, ctl)) break;
         mbar_arrive_expect_tx(&kv_full, (C::KCH + C::VCH) * kChunkBytes);
@@ -164,7 +196,9 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_dual_kernel(const __grid_cons
       const uint32_t ra = tmem + C::T_A, rb = tmem + C::T_B;
       uint32_t nz = 0, gstep = 0;
       bool ok = true;
-      for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+      while (ok) {
+        const int w = next_work(ok);
+        if (w < 0) break;
         const BwdItem t = bwd_decode(p, w);
         if (t.k1 == t.k0) continue;
         if (!wait_bar(&kv_full, nz & 1, ctl)) break;
@@ -282,7 +316,9 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_dual_kernel(const __grid_cons
         }
       }
     };
-    for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+    while (ok) {
+      const int w = next_work(ok);
+      if (w < 0) break;
       const BwdItem t = bwd_decode(p, w);
       if (t.k1 == t.k0) continue;
       const int j = t.kt * kBN + r;  // segment-local key index
@@ -310,7 +346,8 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_dual_kernel(const __grid_cons
         const uint32_t ra = tmem + lane_base + C::T_A, rb = tmem + lane_base + C::T_B;
         // Pass 1: P^T = exp2(S^T * scale * log2 e - lse * log2 e) as packed bf16
         // over the S^T columns already read (chunk c -> A[16c, 16c + 16)).
-        {
+        auto pass1 = [&](auto tag) {
+          constexpr bool MASK = decltype(tag)::value;
           uint32_t sa[32], sb[32];
           tmem_ld32_async(ra, sa);
 #pragma unroll
@@ -330,10 +367,10 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_dual_kernel(const __grid_cons
                 const float2 x =
                     fma2(make_float2(__uint_as_float(cur[2 * e]), __uint_as_float(cur[2 * e + 1])), sl2x2, nl2);
                 float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
-                if (masked) {
+                if constexpr (MASK) {
                   const int qc = c * 32 + 2 * e;
-                  if (qc < q_lo || qc >= q_hi) p0 = 0.f;
-                  if (qc + 1 < q_lo || qc + 1 >= q_hi) p1 = 0.f;
+                  p0 = (qc < q_lo || qc >= q_hi) ? 0.f : p0;
+                  p1 = (qc + 1 < q_lo || qc + 1 >= q_hi) ? 0.f : p1;
                 }
                 pk[e] = pack_bf16x2(p0, p1);
               }
@@ -342,7 +379,11 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_dual_kernel(const __grid_cons
             tmem_st16_async(ra + c * 16, pk);
           }
           tmem_wait_st();
-        }
+        };
+        if (masked)
+          pass1(MaskTag<true>{});
+        else
+          pass1(MaskTag<false>{});
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&p_full);
@@ -439,7 +480,9 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_dual_kernel(const __grid_cons
     uint8_t* box = smem + C::STG_OFF + wq * 4096;
     uint32_t gstep = 0;
     bool ok = true;
-    for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+    while (ok) {
+      const int w = next_work(ok);
+      if (w < 0) break;
       const BwdItem t = bwd_decode(p, w);
       if (t.k1 == t.k0) continue;
       for (int k = t.k0; k < t.k1; ++k, ++gstep) {

@@ -55,6 +55,14 @@ __device__ __forceinline__ void q_range_for_kv_tile(int m, int n, int j0, int ca
 }
 __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
+// Compile-time flag for element passes that exist in a masked and an unmasked
+// form (mask arithmetic inside the common, unmasked loop costs throughput even
+// when it never fires).
+template <bool B>
+struct MaskTag {
+  static constexpr bool value = B;
+};
+
 // Pipeline control: every wait is bounded. A wait that runs out records
 // kStatusTimeout, raises the CTA-wide abort flag and returns false; the other
 // roles notice the flag at their next wait and wind down, so the CTA always

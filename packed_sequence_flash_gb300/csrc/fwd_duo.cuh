@@ -60,11 +60,6 @@ struct FwdDuoCfg {
   static_assert(3 * (SMEM_BYTES + 1024) > 233472, "at most two CTAs per SM");
 };
 
-template <bool B>
-struct MaskTag {
-  static constexpr bool value = B;
-};
-
 template <int D>
 __global__ void __launch_bounds__(192, 2) attn_fwd_duo_kernel(const __grid_constant__ FwdParams p) {
   using C = FwdDuoCfg<D>;
