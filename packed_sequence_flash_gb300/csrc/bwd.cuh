@@ -314,9 +314,27 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_kernel(const __grid_constant_
         continue;
       }
       const int delta = t.n - t.m;
+      // lse and Delta of 4 query columns per lane, loaded one step ahead and
+      // left in flight until the step stages them (-inf / 0 outside the segment).
+      auto fetch_rows = [&](int k, float (&lv)[4], float (&dv)[4]) {
+        const int h = t.hk * G + k / t.nqt, i0 = (t.qt0 + k % t.nqt) * kBM;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int qc = lane * 4 + e;
+          const int f = t.cq0 + i0 + qc;
+          const bool in = i0 + qc < t.m && f < p.q_rows;
+          const int fs = in ? f : 0;
+          const int bq = fs / p.seg.Sq, sq = fs - bq * p.seg.Sq;
+          lv[e] = -CUDART_INF_F;
+          dv[e] = 0.f;
+          ldg_pred_f32(lv[e], p.lse + bq * p.l_sb + h * p.l_sh + sq, in);
+          ldg_pred_f32(dv[e], p.delta + (int64_t)h * p.q_rows + fs, in);
+        }
+      };
+      float rlv[4], rdv[4];
+      fetch_rows(t.k0, rlv, rdv);
       {
         for (int k = t.k0; k < t.k1; ++k, ++gstep) {
-          const int h = t.hk * G + k / t.nqt;
           const int i0 = (t.qt0 + k % t.nqt) * kBM;
           // Per-key visible query columns [q_lo, q_hi) of this tile.
           int q_lo = p.seg.causal ? j - delta - i0 : -0x40000000;
@@ -324,21 +342,14 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_kernel(const __grid_constant_
           if (p.seg.window > 0) q_hi = min(q_hi, j - delta + p.seg.window - i0);
           if (!valid) q_lo = q_hi = 0;
           const bool masked = q_lo > 0 || q_hi < kBM;
-          // Stage lse * log2(e) (+inf for rows without mass) and Delta for this tile.
+          // lse * log2(e) (+inf for rows without mass) and Delta for this step.
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int qc = lane * 4 + e;
-            const int f = t.cq0 + i0 + qc;
-            float lv = CUDART_INF_F, dv = 0.f;
-            if (i0 + qc < t.m && f < p.q_rows) {
-              const int bq = f / p.seg.Sq, sq = f - bq * p.seg.Sq;
-              const float x = p.lse[bq * p.l_sb + h * p.l_sh + sq];
-              lv = x == -CUDART_INF_F ? CUDART_INF_F : x * 1.4426950408889634f;
-              dv = p.delta[(int64_t)h * p.q_rows + f];
-            }
-            my_lse[qc] = lv;
-            my_dl[qc] = dv;
+            my_lse[qc] = rlv[e] == -CUDART_INF_F ? CUDART_INF_F : rlv[e] * 1.4426950408889634f;
+            my_dl[qc] = rdv[e];
           }
+          if (k + 1 < t.k1) fetch_rows(k + 1, rlv, rdv);
           __syncwarp();
           if (!wait_bar(&s_full, gstep & 1, ctl)) {
             ok = false;

@@ -33,7 +33,8 @@
 //          the next untaken unit from a global counter; the producer passes each
 //          unit's index to the other warps through a two-entry ring in shared
 //          memory (-1 = no more work).
-// The compute warps prefetch the next step's lse and Delta into registers.
+// The compute warps load the next step's lse and Delta one step ahead and
+// leave the loads in flight until the step begins.
 #pragma once
 
 #include <math_constants.h>
@@ -298,24 +299,25 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_dual_kernel(const __grid_cons
     const float2 sl2x2 = make_float2(sl2, sl2), one2 = make_float2(1.f, 1.f), zero2 = make_float2(0.f, 0.f);
     uint32_t nz = 0, gstep = 0;
     bool ok = true;
-    // -lse * log2(e) (-inf where the row carries no probability, so P = 0)
-    // and -Delta of 4 query columns per lane for one step.
+    // lse and Delta of 4 query columns per lane for one step, loaded one step
+    // ahead and left in flight (-inf / 0 for rows outside the segment).
     auto fetch_rows = [&](const BwdItem& t, int k, float (&lv)[4], float (&dv)[4]) {
       const int h = t.hk * G + k / t.nqt, i0 = (t.qt0 + k % t.nqt) * kBM;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int qc = lane * 4 + e;
         const int f = t.cq0 + i0 + qc;
+        const bool in = i0 + qc < t.m && f < p.q_rows;
+        const int fs = in ? f : 0;
+        const int bq = fs / p.seg.Sq, sq = fs - bq * p.seg.Sq;
         lv[e] = -CUDART_INF_F;
         dv[e] = 0.f;
-        if (i0 + qc < t.m && f < p.q_rows) {
-          const int bq = f / p.seg.Sq, sq = f - bq * p.seg.Sq;
-          const float x = p.lse[bq * p.l_sb + h * p.l_sh + sq];
-          lv[e] = x == -CUDART_INF_F ? -CUDART_INF_F : -x * 1.4426950408889634f;
-          dv[e] = -p.delta[(int64_t)h * p.q_rows + f];
-        }
+        ldg_pred_f32(lv[e], p.lse + bq * p.l_sb + h * p.l_sh + sq, in);
+        ldg_pred_f32(dv[e], p.delta + (int64_t)h * p.q_rows + fs, in);
       }
     };
+    // -lse * log2(e) (-inf where the row carries no probability, so P = 0).
+    auto neg_lse2 = [](float x) { return x == -CUDART_INF_F ? -CUDART_INF_F : -x * 1.4426950408889634f; };
     while (ok) {
       const int w = next_work(ok);
       if (w < 0) break;
@@ -328,8 +330,9 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_dual_kernel(const __grid_cons
       fetch_rows(t, t.k0, nlv, ndv);
       for (int k = t.k0; k < t.k1; ++k, ++gstep) {
         const int i0 = (t.qt0 + k % t.nqt) * kBM;
-        *reinterpret_cast<float4*>(my_nlse + lane * 4) = make_float4(nlv[0], nlv[1], nlv[2], nlv[3]);
-        *reinterpret_cast<float4*>(my_ndl + lane * 4) = make_float4(ndv[0], ndv[1], ndv[2], ndv[3]);
+        *reinterpret_cast<float4*>(my_nlse + lane * 4) =
+            make_float4(neg_lse2(nlv[0]), neg_lse2(nlv[1]), neg_lse2(nlv[2]), neg_lse2(nlv[3]));
+        *reinterpret_cast<float4*>(my_ndl + lane * 4) = make_float4(-ndv[0], -ndv[1], -ndv[2], -ndv[3]);
         __syncwarp();
         if (k + 1 < t.k1) fetch_rows(t, k + 1, nlv, ndv);
         // Per-key visible query columns [q_lo, q_hi) of this tile.

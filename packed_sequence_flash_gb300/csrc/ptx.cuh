@@ -290,6 +290,19 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   return d;
 }
 
+// ---------------------------------------------------------------- global loads
+// x = *ptr when pred, else x keeps its value. The load is left in flight: the
+// thread stalls only where x is next read, so a load issued one pipeline step
+// ahead hides its latency.
+__device__ __forceinline__ void ldg_pred_f32(float& x, const float* ptr, bool pred) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %2, 0;\n\t"
+      "@p ld.global.nc.f32 %0, [%1];\n\t}"
+      : "+f"(x)
+      : "l"(ptr), "r"((int)pred));
+}
+
 // ---------------------------------------------------------------- math
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
