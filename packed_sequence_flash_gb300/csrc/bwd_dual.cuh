@@ -10,8 +10,9 @@
 //          dV += P^T dO; B holds dP^T, then dQ = dS K.
 //   Order  per step g the MMA warp issues dP(g) -> B, dV(g) once P^T is
 //          written, then, as soon as dS^T(g) is in shared memory, S(g+1) -> A
-//          ahead of dK(g) and dQ(g) -> B, so the next step's element-wise pass
-//          runs while the tensor core finishes this one.
+//          ahead of dQ(g) -> B and dK(g), so the next step's element-wise pass
+//          runs while the tensor core finishes this one, and the dQ read-out
+//          (which frees B for dP(g+1)) overlaps the dK MMAs.
 //   SMEM   K, V resident per key tile; Q double-buffered; dO single-buffered
 //          but released right after dV, its last reader; dS^T (bf16, 128-byte
 //          swizzled) read K-major by dK and M-major by dQ; a 16 KB area stages
@@ -266,16 +267,18 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_dual_kernel(const __grid_cons
             }
             mma_commit(&s_full);
           }
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_ss(tmem + C::T_DK, sdesc_sw128(ds_a + (kk >> 2) * kChunkBytes + (kk & 3) * 32, 16, 1024),
-                   sdesc_sw128(q_a + kk * 2048, kChunkBytes, 1024), id_dk, !(first && kk == 0));
-          mma_commit(&q_empty[qs]);
+          // dQ before dK: its read-out, which frees region B for the next dP,
+          // then overlaps the dK MMAs.
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
             mma_ss(rb, sdesc_sw128(ds_a + kk * 2048, kChunkBytes, 1024), sdesc_sw128(k_a + kk * 2048, kChunkBytes, 1024),
                    id_dq, kk > 0);
           mma_commit(&dq_full);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ss(tmem + C::T_DK, sdesc_sw128(ds_a + (kk >> 2) * kChunkBytes + (kk & 3) * 32, 16, 1024),
+                   sdesc_sw128(q_a + kk * 2048, kChunkBytes, 1024), id_dk, !(first && kk == 0));
+          mma_commit(&q_empty[qs]);
           mma_commit(&ds_free);
         }
         if (!ok) break;
