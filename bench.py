@@ -43,18 +43,39 @@ UNIT = "TFLOP/s"
 FALLBACK_BF16_TFLOPS = 1900.0
 FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 256 << 20
-# dram__bytes_read.sum + dram__bytes_write.sum per launch of the backward main
-# kernel from one ncu capture, keyed by a hash of the kernel sources it was
-# taken on; reported as null once the sources change.
-NCU_TRAFFIC = {}  # filled in once a capture of the current sources exists
+# dram__bytes_read.sum + dram__bytes_write.sum per launch of a main kernel from
+# one ncu capture: kernel -> (hash of the kernel's sources when captured, bytes).
+# Reported as null once the sources change.
+NCU_TRAFFIC = {}
+
+# Sources each main kernel is compiled from (for the hash above).
+KERNEL_SOURCES = {
+    "attn_fwd_duo_kernel": ("fwd.cuh", "fwd_duo.cuh", "common.cuh", "ptx.cuh"),
+    "attn_fwd_kernel": ("fwd.cuh", "common.cuh", "ptx.cuh"),
+    "attn_bwd_dual_kernel": ("bwd.cuh", "bwd_dual.cuh", "common.cuh", "ptx.cuh"),
+    "attn_bwd_kernel": ("bwd.cuh", "common.cuh", "ptx.cuh"),
+    "attn_bwd_wide_kernel": ("bwd.cuh", "bwd_wide.cuh", "common.cuh", "ptx.cuh"),
+}
 
 
-def kernel_source_hash(files=("bwd.cuh", "common.cuh", "ptx.cuh")) -> str:
+def kernel_source_hash(kernel: str) -> str:
     h = hashlib.sha256()
-    for f in files:
+    for f in KERNEL_SOURCES[kernel]:
         with open(os.path.join(ROOT, "packed_sequence_flash_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
+
+
+def main_kernels(dqk: int, dv: int) -> tuple[str, str]:
+    """Names of the forward and backward kernels the library runs for these head dims."""
+    fwd = "attn_fwd_duo_kernel" if dqk == dv and dqk in (64, 128) else "attn_fwd_kernel"
+    if dqk <= 128 and dv <= 128:
+        bwd = "attn_bwd_dual_kernel"
+    elif dqk == 512 and dv == 512:
+        bwd = "attn_bwd_wide_kernel"
+    else:
+        bwd = "attn_bwd_kernel"
+    return fwd, bwd
 
 
 def visible_pairs(doc_ids: np.ndarray, q0: int, Lq: int, window=None) -> int:
@@ -376,16 +397,17 @@ def our_arm(args):
     fwd_ms = kt["fwd"][0] / max(kt["fwd"][1], 1)
     bwd_ms = kt["bwd"][0] / max(kt["bwd"][1], 1)
     roof = {}
-    for name, kms, kfl in (("attn_fwd_kernel", fwd_ms, f_fwd), ("attn_bwd_kernel", bwd_ms, f_bwd)):
+    fwd_name, bwd_name = main_kernels(w.q.shape[-1], w.v.shape[-1])
+    for name, kms, kfl in ((fwd_name, fwd_ms, f_fwd), (bwd_name, bwd_ms, f_bwd)):
         ach = kfl / (kms * 1e-3) / 1e12 if kms > 0 else 0.0
         roof[name] = {"bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s",
                       "frac": ach / peak, "ms_per_launch": kms,
                       "peak_source": f"bf16 dense burst, {'of measured' if src == 'measured' else 'of fallback'}"}
-    dominant = "attn_bwd_kernel" if bwd_ms >= fwd_ms else "attn_fwd_kernel"
+    dominant = bwd_name if bwd_ms >= fwd_ms else fwd_name
     roofline = dict(roof[dominant])
     roofline["kernel"] = dominant
-    h = kernel_source_hash()
-    roofline["traffic"] = NCU_TRAFFIC.get(h) if dominant == "attn_bwd_kernel" else None
+    cap = NCU_TRAFFIC.get(dominant)
+    roofline["traffic"] = cap[1] if cap and cap[0] == kernel_source_hash(dominant) else None
     other = [n for n in roof if n != dominant][0]
 
     value = world * flops / (ms_max * 1e-3) / 1e12
