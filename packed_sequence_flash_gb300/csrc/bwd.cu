@@ -14,7 +14,7 @@ cudaError_t run_dual(const BwdParams& p, int grid, cudaStream_t st) {
   cudaError_t e =
       cudaFuncSetAttribute(attn_bwd_dual_kernel<DQK, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  attn_bwd_dual_kernel<DQK, DV><<<grid, 384, smem, st>>>(p);
+  attn_bwd_dual_kernel<DQK, DV><<<grid, 512, smem, st>>>(p);
   return cudaGetLastError();
 }
 template <int D>

@@ -53,10 +53,10 @@ struct BwdDualCfg {
   static constexpr int Q_OFF = V_OFF + VCH * kChunkBytes;  // two slots
   static constexpr int Q_SLOT = KCH * kChunkBytes;
   static constexpr int DO_OFF = Q_OFF + 2 * Q_SLOT;
-  static constexpr int DS_OFF = DO_OFF + VCH * kChunkBytes;  // dS^T; the dK/dV epilogue stages here (4 x 8 KB)
+  static constexpr int DS_OFF = DO_OFF + VCH * kChunkBytes;  // dS^T; the dK/dV epilogue stages here (8 x 4 KB)
   static constexpr int STG_OFF = DS_OFF + 2 * kChunkBytes;   // dQ read-out staging (4 warps x 4 KB)
   static constexpr int ROWV_OFF = STG_OFF + 4 * 4096;
-  static constexpr int SMEM_BYTES = ROWV_OFF + 2 * 4 * 128 * 4 + 1024;
+  static constexpr int SMEM_BYTES = ROWV_OFF + 2 * 8 * 64 * 4 + 1024;
   static constexpr int T_DV = 0;
   static constexpr int T_DK = DV;
   static constexpr int T_A = 256;
@@ -66,12 +66,12 @@ struct BwdDualCfg {
 };
 
 template <int DQK, int DV>
-__global__ void __launch_bounds__(384, 1) attn_bwd_dual_kernel(const __grid_constant__ BwdParams p) {
+__global__ void __launch_bounds__(512, 1) attn_bwd_dual_kernel(const __grid_constant__ BwdParams p) {
   using C = BwdDualCfg<DQK, DV>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  float* nlse_s = reinterpret_cast<float*>(smem + C::ROWV_OFF);  // [4 warps][128]: -lse * log2(e)
-  float* ndl_s = nlse_s + 4 * 128;                                // [4 warps][128]: -Delta
+  float* nlse_s = reinterpret_cast<float*>(smem + C::ROWV_OFF);  // [8 compute warps][64]: -lse * log2(e)
+  float* ndl_s = nlse_s + 8 * 64;                                 // [8 compute warps][64]: -Delta
 
   __shared__ uint64_t kv_full, kv_empty, q_full[2], q_empty[2], do_full, do_empty, s_full, dp_full, p_full,
       ds_full, ds_free, dq_full, dq_free, acc_done, acc_free, drain, work_full[2], work_empty[2];
@@ -91,17 +91,17 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_dual_kernel(const __grid_cons
     mbar_init(&do_empty, 1);
     mbar_init(&s_full, 1);
     mbar_init(&dp_full, 1);
-    mbar_init(&p_full, 4);
-    mbar_init(&ds_full, 4);
+    mbar_init(&p_full, 8);
+    mbar_init(&ds_full, 8);
     mbar_init(&ds_free, 1);
     mbar_init(&dq_full, 1);
     mbar_init(&dq_free, 4);
     mbar_init(&acc_done, 1);
-    mbar_init(&acc_free, 4);
+    mbar_init(&acc_free, 8);
     mbar_init(&drain, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&work_full[i], 1);
-      mbar_init(&work_empty[i], 9);  // the MMA thread, four compute and four dQ warps
+      mbar_init(&work_empty[i], 13);  // the MMA thread, eight compute and four dQ warps
     }
     abort_flag = 0;
     fence_mbar_init();
@@ -242,7 +242,7 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_dual_kernel(const __grid_cons
           const uint32_t first = (k == t.k0) ? 1u : 0u;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            mma_ts(tmem + C::T_DV, ra + kk * 8, sdesc_sw128(do_a + kk * 2048, kChunkBytes, 1024), id_dv,
+            mma_ts(tmem + C::T_DV, ra + kk * 8 + (kk >= 4 ? 32 : 0), sdesc_sw128(do_a + kk * 2048, kChunkBytes, 1024), id_dv,
                    !(first && kk == 0));
           mma_commit(&do_empty);
           if (!wait_bar(&ds_full, gstep & 1, ctl)) {
@@ -289,26 +289,31 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_dual_kernel(const __grid_cons
       mma_commit(&drain);
       wait_bar_drain(&drain, 0, p.limit_ns);
     }
-  } else if (warp >= 4 && warp < 8) {
-    // ------------------------------------------------------------ compute warpgroup
-    const int wq = warp - 4;
-    const int r = threadIdx.x - 128;  // key row within the tile
+  } else if (warp >= 4 && (warp < 8 || warp >= 12)) {
+    // ------------------------------------------------------------ compute warpgroups
+    // Warps 4-7 take query columns [0, 64) of every step, warps 12-15 columns
+    // [64, 128); thread = key row in both.
+    const int half = warp >= 12 ? 1 : 0;
+    const int wq = warp & 3;
+    const int cb = half * 64;                       // first query column of this half
+    const uint32_t pofs = half ? 64 : 0;            // where this half's P^T sits in A
+    const int r = 32 * wq + lane;                   // key row within the tile
     const uint32_t lane_base = (uint32_t)(32 * wq) << 16;
-    float* my_nlse = nlse_s + wq * 128;
-    float* my_ndl = ndl_s + wq * 128;
-    uint8_t* ds_s = smem + C::DS_OFF;
-    uint8_t* epi = smem + C::DS_OFF + wq * 8192;  // two 4 KB boxes per warp, used between steps
+    float* my_nlse = nlse_s + (half * 4 + wq) * 64;
+    float* my_ndl = ndl_s + (half * 4 + wq) * 64;
+    uint8_t* ds_s = smem + C::DS_OFF + half * kChunkBytes;
+    uint8_t* epi = smem + C::DS_OFF + (half * 4 + wq) * 4096;  // one 4 KB box per warp, used between units
     const float sl2 = p.scale_log2;
     const float2 sl2x2 = make_float2(sl2, sl2), one2 = make_float2(1.f, 1.f), zero2 = make_float2(0.f, 0.f);
     uint32_t nz = 0, gstep = 0;
     bool ok = true;
-    // lse and Delta of 4 query columns per lane for one step, loaded one step
-    // ahead and left in flight (-inf / 0 for rows outside the segment).
-    auto fetch_rows = [&](const BwdItem& t, int k, float (&lv)[4], float (&dv)[4]) {
+    // lse and Delta of 2 of this half's query columns per lane for one step,
+    // loaded one step ahead and left in flight (-inf / 0 outside the segment).
+    auto fetch_rows = [&](const BwdItem& t, int k, float (&lv)[2], float (&dv)[2]) {
       const int h = t.hk * G + k / t.nqt, i0 = (t.qt0 + k % t.nqt) * kBM;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int qc = lane * 4 + e;
+      for (int e = 0; e < 2; ++e) {
+        const int qc = cb + lane * 2 + e;
         const int f = t.cq0 + i0 + qc;
         const bool in = i0 + qc < t.m && f < p.q_rows;
         const int fs = in ? f : 0;
@@ -329,39 +334,41 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_dual_kernel(const __grid_cons
       const int j = t.kt * kBN + r;  // segment-local key index
       const bool valid = j < t.n;
       const int delta = t.n - t.m;
-      float nlv[4], ndv[4];
+      float nlv[2], ndv[2];
       fetch_rows(t, t.k0, nlv, ndv);
       for (int k = t.k0; k < t.k1; ++k, ++gstep) {
         const int i0 = (t.qt0 + k % t.nqt) * kBM;
-        *reinterpret_cast<float4*>(my_nlse + lane * 4) =
-            make_float4(neg_lse2(nlv[0]), neg_lse2(nlv[1]), neg_lse2(nlv[2]), neg_lse2(nlv[3]));
-        *reinterpret_cast<float4*>(my_ndl + lane * 4) = make_float4(-ndv[0], -ndv[1], -ndv[2], -ndv[3]);
+        *reinterpret_cast<float2*>(my_nlse + lane * 2) = make_float2(neg_lse2(nlv[0]), neg_lse2(nlv[1]));
+        *reinterpret_cast<float2*>(my_ndl + lane * 2) = make_float2(-ndv[0], -ndv[1]);
         __syncwarp();
         if (k + 1 < t.k1) fetch_rows(t, k + 1, nlv, ndv);
-        // Per-key visible query columns [q_lo, q_hi) of this tile.
+        // Per-key visible query columns [q_lo, q_hi) of this tile, relative to
+        // this half's first column.
         int q_lo = p.seg.causal ? j - delta - i0 : -0x40000000;
         int q_hi = t.m - i0;
         if (p.seg.window > 0) q_hi = min(q_hi, j - delta + p.seg.window - i0);
         if (!valid) q_lo = q_hi = 0;
-        const bool masked = __any_sync(0xffffffffu, q_lo > 0 || q_hi < kBM);
+        q_lo -= cb;
+        q_hi -= cb;
+        const bool masked = __any_sync(0xffffffffu, q_lo > 0 || q_hi < 64);
         if (!wait_bar(&s_full, gstep & 1, ctl)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t ra = tmem + lane_base + C::T_A, rb = tmem + lane_base + C::T_B;
-        // Pass 1: P^T = exp2(S^T * scale * log2 e - lse * log2 e) as packed bf16
-        // over the S^T columns already read (chunk c -> A[16c, 16c + 16)).
+        // Pass 1: P^T = exp2(S^T * scale * log2 e - lse * log2 e) as packed bf16;
+        // chunk c of this half's S^T columns -> A[pofs + 16c, pofs + 16c + 16),
+        // columns this half has already read.
         auto pass1 = [&](auto tag) {
           constexpr bool MASK = decltype(tag)::value;
           uint32_t sa[32], sb[32];
-          tmem_ld32_async(ra, sa);
+          tmem_ld32_async(ra + cb, sa);
+          tmem_ld32_async(ra + cb + 32, sb);
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t(&cur)[32] = (c & 1) ? sb : sa;
-            uint32_t(&nxt)[32] = (c & 1) ? sa : sb;
+          for (int c = 0; c < 2; ++c) {
+            uint32_t(&cur)[32] = c ? sb : sa;
             tmem_wait_ld32(cur);
-            if (c + 1 < 4) tmem_ld32_async(ra + (c + 1) * 32, nxt);
             uint32_t pk[16];
 #pragma unroll
             for (int e4 = 0; e4 < 8; ++e4) {
@@ -381,8 +388,7 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_dual_kernel(const __grid_cons
                 pk[e] = pack_bf16x2(p0, p1);
               }
             }
-            // Columns [16c, 16c + 16) of S^T were read with chunk c / 2.
-            tmem_st16_async(ra + c * 16, pk);
+            tmem_st16_async(ra + pofs + c * 16, pk);
           }
           tmem_wait_st();
         };
@@ -393,31 +399,33 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_dual_kernel(const __grid_cons
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&p_full);
-        // Pass 2: dS^T = P^T (dP^T - Delta) into shared memory (bf16, swizzled).
+        // Pass 2: dS^T = P^T (dP^T - Delta) into this half's 64 columns of the
+        // dS^T buffer (bf16, 128-byte swizzled).
         if (!wait_bar(&dp_full, gstep & 1, ctl) || (gstep > 0 && !wait_bar(&ds_free, (gstep - 1) & 1, ctl))) {
           ok = false;
           break;
         }
         tc_fence_after();
         {
-          uint32_t da[32], db[32], pa[16], pb[16];
-          tmem_ld32_async(rb, da);
-          tmem_ld16_async(ra, pa);
+          // Four 16-column pieces, the next one's TMEM loads in flight.
+          uint32_t da[16], db[16], pa[8], pb[8];
+          tmem_ld16_async(rb + cb, da);
+          tmem_ld8_async(ra + pofs, pa);
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
-            uint32_t(&dcur)[32] = (c & 1) ? db : da;
-            uint32_t(&dnxt)[32] = (c & 1) ? da : db;
-            uint32_t(&pcur)[16] = (c & 1) ? pb : pa;
-            uint32_t(&pnxt)[16] = (c & 1) ? pa : pb;
-            tmem_wait_ld32_16(dcur, pcur);
+            uint32_t(&dcur)[16] = (c & 1) ? db : da;
+            uint32_t(&dnxt)[16] = (c & 1) ? da : db;
+            uint32_t(&pcur)[8] = (c & 1) ? pb : pa;
+            uint32_t(&pnxt)[8] = (c & 1) ? pa : pb;
+            tmem_wait_ld16_8(dcur, pcur);
             if (c + 1 < 4) {
-              tmem_ld32_async(rb + (c + 1) * 32, dnxt);
-              tmem_ld16_async(ra + (c + 1) * 16, pnxt);
+              tmem_ld16_async(rb + cb + (c + 1) * 16, dnxt);
+              tmem_ld8_async(ra + pofs + (c + 1) * 8, pnxt);
             }
-            uint32_t dk2[16];
+            uint32_t dk2[8];
 #pragma unroll
-            for (int e4 = 0; e4 < 8; ++e4) {
-              const float4 nd = *reinterpret_cast<const float4*>(my_ndl + c * 32 + e4 * 4);
+            for (int e4 = 0; e4 < 4; ++e4) {
+              const float4 nd = *reinterpret_cast<const float4*>(my_ndl + c * 16 + e4 * 4);
 #pragma unroll
               for (int hf = 0; hf < 2; ++hf) {
                 const int e = e4 * 2 + hf;
@@ -429,10 +437,9 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_dual_kernel(const __grid_cons
                 dk2[e] = pack_bf16x2(ds.x, ds.y);
               }
             }
-            const int chunk = c >> 1, g0 = (c & 1) * 4;
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
-              *reinterpret_cast<uint4*>(ds_s + chunk * kChunkBytes + sw128_offset(r, g0 + u)) =
+            for (int u = 0; u < 2; ++u)
+              *reinterpret_cast<uint4*>(ds_s + sw128_offset(r, c * 2 + u)) =
                   make_uint4(dk2[4 * u], dk2[4 * u + 1], dk2[4 * u + 2], dk2[4 * u + 3]);
           }
         }
@@ -442,34 +449,34 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_dual_kernel(const __grid_cons
         if (lane == 0) mbar_arrive(&ds_full);
       }
       if (!ok) break;
-      // Epilogue: add this range's dV and dK (scale applied by the convert) into
-      // the fp32 accumulators, 32 x 32 boxes per warp.
+      // Epilogue: add this range's dV (warps 4-7) or dK (warps 12-15), scale
+      // applied by the convert, into the fp32 accumulators in 32 x 32 boxes.
       if (!wait_bar(&acc_done, nz & 1, ctl)) break;
       tc_fence_after();
       const int fk = t.ck0 + t.kt * kBN + 32 * wq, bk = fk / p.seg.Sk, sk = fk - bk * p.seg.Sk;
+      constexpr int NCV = DV / 32, NCK = DQK / 32;
+      const int nc = half ? NCK : NCV;
 #pragma unroll 1
-      for (int c = 0; c < (DV + DQK) / 32; ++c) {
-        const bool is_v = c < DV / 32;
+      for (int c = 0; c < nc; ++c) {
         uint32_t a[32];
-        tmem_ld32(tmem + lane_base + (is_v ? C::T_DV + c * 32 : C::T_DK + (c - DV / 32) * 32), a);
-        if (c == (DV + DQK) / 32 - 1) {
+        tmem_ld32(tmem + lane_base + (half ? C::T_DK : C::T_DV) + c * 32, a);
+        if (c == nc - 1) {
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&acc_free);
         }
-        uint8_t* box = epi + (c & 1) * 4096;
-        if (c >= 2) {
-          if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+        if (c >= 1) {
+          if (lane == 0) bulk_wait_group_read0();
           __syncwarp();
         }
 #pragma unroll
         for (int u = 0; u < 8; ++u)
-          *reinterpret_cast<uint4*>(box + sw128_offset(lane, u)) =
+          *reinterpret_cast<uint4*>(epi + sw128_offset(lane, u)) =
               make_uint4(a[4 * u], a[4 * u + 1], a[4 * u + 2], a[4 * u + 3]);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          tma_reduce_add_4d(is_v ? &p.tm_dv : &p.tm_dk, box, (is_v ? c : c - DV / 32) * 32, sk, t.hk, bk);
+          tma_reduce_add_4d(half ? &p.tm_dk : &p.tm_dv, epi, c * 32, sk, t.hk, bk);
           bulk_commit_group();
         }
       }
@@ -479,7 +486,7 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_dual_kernel(const __grid_cons
       ++nz;
     }
     if (lane == 0) bulk_wait_group0();
-  } else if (warp >= 8) {
+  } else if (warp >= 8 && warp < 12) {
     // ------------------------------------------------------------ dQ read-out
     const int wq = warp - 8;
     const uint32_t lane_base = (uint32_t)(32 * wq) << 16;
@@ -500,26 +507,30 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_dual_kernel(const __grid_cons
         tc_fence_after();
         const uint32_t rq = tmem + lane_base + C::T_B;
         const int fq = t.cq0 + qt * kBM + 32 * wq, bq = fq / p.seg.Sq, sq = fq - bq * p.seg.Sq;
-        uint32_t a[DQK / 32][32];
 #pragma unroll
-        for (int c = 0; c < DQK / 32; c += 2) tmem_ld32x2(rq + c * 32, rq + (c + 1) * 32, a[c], a[c + 1]);
-        // Every TMEM read of this step is done: the region can take the next dP.
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&dq_free);
+        for (int rnd = 0; rnd < DQK / 64; ++rnd) {
+          uint32_t a[2][32];
+          tmem_ld32x2(rq + rnd * 64, rq + rnd * 64 + 32, a[0], a[1]);
+          if (rnd == DQK / 64 - 1) {
+            // Every TMEM read of this step is done: the region can take the next dP.
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&dq_free);
+          }
 #pragma unroll
-        for (int c = 0; c < DQK / 32; ++c) {
-          if (lane == 0) bulk_wait_group_read0();
-          __syncwarp();
+          for (int c = 0; c < 2; ++c) {
+            if (lane == 0) bulk_wait_group_read0();
+            __syncwarp();
 #pragma unroll
-          for (int u = 0; u < 8; ++u)
-            *reinterpret_cast<uint4*>(box + sw128_offset(lane, u)) =
-                make_uint4(a[c][4 * u], a[c][4 * u + 1], a[c][4 * u + 2], a[c][4 * u + 3]);
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            tma_reduce_add_4d(&p.tm_dq, box, c * 32, sq, h, bq);
-            bulk_commit_group();
+            for (int u = 0; u < 8; ++u)
+              *reinterpret_cast<uint4*>(box + sw128_offset(lane, u)) =
+                  make_uint4(a[c][4 * u], a[c][4 * u + 1], a[c][4 * u + 2], a[c][4 * u + 3]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_reduce_add_4d(&p.tm_dq, box, (rnd * 2 + c) * 32, sq, h, bq);
+              bulk_commit_group();
+            }
           }
         }
       }
