@@ -6,8 +6,9 @@
 // Same arithmetic as bwd.cuh, laid out for head dims up to 128 so that every
 // operand stream overlaps the tensor core:
 //   TMEM   dV [0, Dv) | dK [Dv, Dv + Dqk) | region A [256, 384) | region B [384, 512)
-//          A holds S^T, then P^T (bf16, first 64 columns) as the TMEM operand of
-//          dV += P^T dO; B holds dP^T, then dQ = dS K.
+//          A holds S^T, then P^T (bf16; query columns 0-63 at A[0, 32),
+//          64-127 at A[64, 96)) as the TMEM operand of dV += P^T dO; B holds
+//          dP^T (two N = 64 halves), then dQ = dS K.
 //   Order  per step g the MMA warp issues dP(g) -> B, dV(g) once P^T is
 //          written, then, as soon as dS^T(g) is in shared memory, S(g+1) -> A
 //          ahead of dQ(g) -> B and dK(g), so the next step's element-wise pass
@@ -73,8 +74,8 @@ __global__ void __launch_bounds__(512, 1) attn_bwd_dual_kernel(const __grid_cons
   float* nlse_s = reinterpret_cast<float*>(smem + C::ROWV_OFF);  // [8 compute warps][64]: -lse * log2(e)
   float* ndl_s = nlse_s + 8 * 64;                                 // [8 compute warps][64]: -Delta
 
-  __shared__ uint64_t kv_full, kv_empty, q_full[2], q_empty[2], do_full, do_empty, s_full, dp_full, p_full,
-      ds_full, ds_free, dq_full, dq_free, acc_done, acc_free, drain, work_full[2], work_empty[2];
+  __shared__ uint64_t kv_full, kv_empty, q_full[2], q_empty[2], do_full, do_empty, s_full, dp_full[2], p_full,
+      ds_full, ds_free, dq_full, dq_free[2], acc_done, acc_free, drain, work_full[2], work_empty[2];
   __shared__ int work_slot[2];
   __shared__ uint32_t tmem_base_smem;
   __shared__ int abort_flag;
@@ -90,12 +91,14 @@ __global__ void __launch_bounds__(512, 1) attn_bwd_dual_kernel(const __grid_cons
     mbar_init(&do_full, 1);
     mbar_init(&do_empty, 1);
     mbar_init(&s_full, 1);
-    mbar_init(&dp_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&dp_full[i], 1);
+      mbar_init(&dq_free[i], 4);
+    }
     mbar_init(&p_full, 8);
     mbar_init(&ds_full, 8);
     mbar_init(&ds_free, 1);
     mbar_init(&dq_full, 1);
-    mbar_init(&dq_free, 4);
     mbar_init(&acc_done, 1);
     mbar_init(&acc_free, 8);
     mbar_init(&drain, 1);
@@ -189,7 +192,8 @@ __global__ void __launch_bounds__(512, 1) attn_bwd_dual_kernel(const __grid_cons
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t id_sq = idesc_bf16_f32(128, 128, 0, 0);  // S^T = K Q^T, dP^T = V dO^T
+      constexpr uint32_t id_sq = idesc_bf16_f32(128, 128, 0, 0);  // S^T = K Q^T
+      constexpr uint32_t id_dp = idesc_bf16_f32(128, 64, 0, 0);   // one half of dP^T = V dO^T
       constexpr uint32_t id_dv = idesc_bf16_f32(128, DV, 0, 1);   // dV += P^T (TMEM) dO
       constexpr uint32_t id_dk = idesc_bf16_f32(128, DQK, 0, 1);  // dK += dS^T Q
       constexpr uint32_t id_dq = idesc_bf16_f32(128, DQK, 1, 1);  // dQ  = dS K
@@ -222,18 +226,28 @@ __global__ void __launch_bounds__(512, 1) attn_bwd_dual_kernel(const __grid_cons
         for (int k = t.k0; k < t.k1 && ok; ++k, ++gstep) {
           const int qs = gstep & 1;
           const uint32_t q_a = q_a0 + qs * C::Q_SLOT;
-          if (!wait_bar(&do_full, gstep & 1, ctl) || (gstep > 0 && !wait_bar(&dq_free, (gstep - 1) & 1, ctl))) {
+          // dP^T in two N = 64 halves (query rows 0-63, 64-127), each issued
+          // as soon as the dQ read-out has freed its columns of B; each
+          // compute warpgroup waits only for its own half.
+          if (!wait_bar(&do_full, gstep & 1, ctl)) {
             ok = false;
             break;
           }
-          tc_fence_after();
-          for (int c = 0; c < C::VCH; ++c) {
+          for (int hh = 0; hh < 2 && ok; ++hh) {
+            if (gstep > 0 && (hh == 0 || DQK > 64) && !wait_bar(&dq_free[hh], (gstep - 1) & 1, ctl)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            for (int c = 0; c < C::VCH; ++c) {
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_ss(rb, sdesc_sw128(v_a + c * kChunkBytes + kk * 32, 16, 1024),
-                     sdesc_sw128(do_a + c * kChunkBytes + kk * 32, 16, 1024), id_sq, (c | kk) != 0);
+              for (int kk = 0; kk < 4; ++kk)
+                mma_ss(rb + hh * 64, sdesc_sw128(v_a + c * kChunkBytes + kk * 32, 16, 1024),
+                       sdesc_sw128(do_a + c * kChunkBytes + hh * 8192 + kk * 32, 16, 1024), id_dp, (c | kk) != 0);
+            }
+            mma_commit(&dp_full[hh]);
           }
-          mma_commit(&dp_full);
+          if (!ok) break;
           if (!wait_bar(&p_full, gstep & 1, ctl)) {
             ok = false;
             break;
@@ -401,7 +415,7 @@ __global__ void __launch_bounds__(512, 1) attn_bwd_dual_kernel(const __grid_cons
         if (lane == 0) mbar_arrive(&p_full);
         // Pass 2: dS^T = P^T (dP^T - Delta) into this half's 64 columns of the
         // dS^T buffer (bf16, 128-byte swizzled).
-        if (!wait_bar(&dp_full, gstep & 1, ctl) || (gstep > 0 && !wait_bar(&ds_free, (gstep - 1) & 1, ctl))) {
+        if (!wait_bar(&dp_full[half], gstep & 1, ctl) || (gstep > 0 && !wait_bar(&ds_free, (gstep - 1) & 1, ctl))) {
           ok = false;
           break;
         }
@@ -511,12 +525,10 @@ __global__ void __launch_bounds__(512, 1) attn_bwd_dual_kernel(const __grid_cons
         for (int rnd = 0; rnd < DQK / 64; ++rnd) {
           uint32_t a[2][32];
           tmem_ld32x2(rq + rnd * 64, rq + rnd * 64 + 32, a[0], a[1]);
-          if (rnd == DQK / 64 - 1) {
-            // Every TMEM read of this step is done: the region can take the next dP.
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&dq_free);
-          }
+          // These 64 columns of B are read: they can take the next dP half.
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&dq_free[rnd]);
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
             if (lane == 0) bulk_wait_group_read0();
