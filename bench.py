@@ -425,7 +425,7 @@ def our_arm(args):
         "roofline": roofline, "roofline_other": dict(roof[other], kernel=other),
         "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms},
-        "gpu_launches": 9 * args.steps,
+        "gpu_launches": 7 * args.steps,
         "clocks": clocks,
     }
     if world == 1 and not args.no_cpu:

@@ -252,13 +252,12 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, void* out, float*
   FwdWorkspace w;
   fwd_ws_layout(q_rows, nseg, &w, ws);
   SegInfo g{cu_q, cu_k, dev_meta, nseg, max_q, max_k, B, Sq, Sk, causal ? 1 : 0, window > 0 ? (int)window : 0};
-  cudaError_t e = launch_schedule(g, 0, w.items, w.n_items, w.seg_prefix, w.item_cap, dev->status, st);
-  if (e != cudaSuccess) return cuda_fail(e, "schedule launch");
   const View vq = tensor_view(layout, Sq, Hq, Dqk), vk = tensor_view(layout, Sk, Hkv, Dqk);
   const View vv = tensor_view(layout, Sk, Hkv, Dv), vo = tensor_view(layout, Sq, Hq, Dv);
   const View vl = lse_view(layout, Sq, Hq);
-  e = launch_fwd_tail(g, static_cast<__nv_bfloat16*>(out), vo.sb, vo.ss, vo.sh, lse, vl.sb, vl.sh, Hq, Dv, st);
-  if (e != cudaSuccess) return cuda_fail(e, "tail launch");
+  cudaError_t e = launch_fwd_prep(g, w.items, w.n_items, w.seg_prefix, w.item_cap, dev->status,
+                                  static_cast<__nv_bfloat16*>(out), vo.sb, vo.ss, vo.sh, lse, vl.sb, vl.sh, Hq, Dv, st);
+  if (e != cudaSuccess) return cuda_fail(e, "forward preparation launch");
 
   FwdParams p;
   memset(&p, 0, sizeof(p));
@@ -327,14 +326,12 @@ int attn_bwd_impl(const void* dout, const void* q, const void* k, const void* v,
   const View vq = tensor_view(layout, Sq, Hq, Dqk), vk = tensor_view(layout, Sk, Hkv, Dqk);
   const View vv = tensor_view(layout, Sk, Hkv, Dv), vo = tensor_view(layout, Sq, Hq, Dv);
   const View vl = lse_view(layout, Sq, Hq);
-  cudaError_t e = launch_bwd_schedule(g, Hq / Hkv, Hkv, accumulate ? kSplitPerSm * dev->sms : 0, w.items,
-                                      w.n_items, w.seg_prefix, w.item_cap, dev->status, st);
-  if (e != cudaSuccess) return cuda_fail(e, "schedule launch");
-  e = launch_bwd_pre(g, static_cast<const __nv_bfloat16*>(dout), static_cast<const __nv_bfloat16*>(out), vo.sb,
-                     vo.ss, vo.sh, w.delta, w.dq_acc, Hq, Dqk, Dv, accumulate ? w.dk_acc : nullptr,
-                     accumulate ? w.dv_acc : nullptr, static_cast<__nv_bfloat16*>(dk),
-                     static_cast<__nv_bfloat16*>(dv), vk.sb, vk.ss, vk.sh, vv.sb, vv.ss, vv.sh, Hkv, st);
-  if (e != cudaSuccess) return cuda_fail(e, "preprocess launch");
+  cudaError_t e = launch_bwd_prep(
+      g, Hq / Hkv, Hkv, accumulate ? kSplitPerSm * dev->sms : 0, w.items, w.n_items, w.seg_prefix, w.item_cap,
+      dev->status, static_cast<const __nv_bfloat16*>(dout), static_cast<const __nv_bfloat16*>(out), vo.sb, vo.ss,
+      vo.sh, w.delta, w.dq_acc, Hq, Dqk, Dv, accumulate ? w.dk_acc : nullptr, accumulate ? w.dv_acc : nullptr,
+      static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(dv), vk.sb, vk.ss, vk.sh, vv.sb, vv.ss, vv.sh, st);
+  if (e != cudaSuccess) return cuda_fail(e, "backward preparation launch");
 
   if (k_rows > 0) {
     BwdParams p;

@@ -82,7 +82,8 @@ __device__ int tile_cost(const SegInfo& g, int s, int t, int over_keys) {
   return hi > lo ? ceil_div(hi, kBN) - lo / kBN : 0;
 }
 
-__global__ void __launch_bounds__(kScanThreads) schedule_kernel(SegInfo g, int over_keys, int2* items, int* n_items,
+// Runs in one 1024-thread block (block 0 of fwd_prep_kernel).
+__device__ void schedule_body(SegInfo g, int over_keys, int2* items, int* n_items,
                                                                 int* seg_prefix, int item_cap, int* status) {
   __shared__ int hist[kBuckets];
   __shared__ int start[kBuckets];
@@ -153,7 +154,8 @@ __global__ void __launch_bounds__(kScanThreads) schedule_kernel(SegInfo g, int o
 // (query head, query tile) steps when it holds more than its share of the
 // total (split_target > 0: aim at split_target sub-items' worth of steps),
 // heaviest first. Items are (segment, key tile, first step, end step).
-__global__ void __launch_bounds__(kScanThreads) bwd_schedule_kernel(SegInfo g, int G, int Hkv, int split_target,
+// Runs in one 1024-thread block (block 0 of bwd_prep_kernel).
+__device__ void bwd_schedule_body(SegInfo g, int G, int Hkv, int split_target,
                                                                     int4* items, int* n_items, int* seg_prefix,
                                                                     int item_cap, int* status) {
   __shared__ int hist[kBuckets];
@@ -254,15 +256,16 @@ __global__ void __launch_bounds__(kScanThreads) bwd_schedule_kernel(SegInfo g, i
   if (tid == 0) *n_items = n_all;
 }
 
-__global__ void fwd_tail_kernel(SegInfo g, __nv_bfloat16* out, int64_t o_sb, int64_t o_ss, int64_t o_sh, float* lse,
-                                int64_t l_sb, int64_t l_sh, int Hq, int Dv) {
+// out = 0, lse = -inf for query rows at or past cu_q[nseg]; blocks bid of nblk.
+__device__ void fwd_tail_body(SegInfo g, __nv_bfloat16* out, int64_t o_sb, int64_t o_ss, int64_t o_sh, float* lse,
+                              int64_t l_sb, int64_t l_sh, int Hq, int Dv, int bid, int nblk) {
   const int nseg = seg_count(g);
   const int first = cu_q_at(g, nseg);
   const int64_t rows = (int64_t)g.B * g.Sq - first;
   if (rows <= 0) return;
   const int groups = Dv / 8;
   const int64_t total = rows * Hq * groups;
-  for (int64_t x = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; x < total; x += (int64_t)gridDim.x * blockDim.x) {
+  for (int64_t x = bid * (int64_t)blockDim.x + threadIdx.x; x < total; x += (int64_t)nblk * blockDim.x) {
     const int gidx = (int)(x % groups);
     const int64_t rh = x / groups;
     const int h = (int)(rh % Hq);
@@ -400,16 +403,18 @@ __global__ void lse_merge_kernel(const __nv_bfloat16* o1, const float* l1, const
 // Delta = sum_d dO * O in fp32, by groups of min(32, Dv/8) lanes per
 // (row, head); then grid-stride zeroing of the fp32 accumulators. When dK/dV
 // are written directly (no accumulators), rows no segment covers are zeroed.
-__global__ void bwd_pre_kernel(SegInfo g, const __nv_bfloat16* dout, const __nv_bfloat16* out, int64_t o_sb,
-                               int64_t o_ss, int64_t o_sh, float* delta, float* dq_acc, int Hq, int Dqk, int Dv,
-                               float* dk_acc, float* dv_acc, __nv_bfloat16* dk, __nv_bfloat16* dv, int64_t k_sb,
-                               int64_t k_ss, int64_t k_sh, int64_t v_sb, int64_t v_ss, int64_t v_sh, int Hkv) {
+// Delta = rowsum(dO * O) and the zeroed accumulators; blocks bid of nblk.
+__device__ void bwd_pre_body(SegInfo g, const __nv_bfloat16* dout, const __nv_bfloat16* out, int64_t o_sb,
+                             int64_t o_ss, int64_t o_sh, float* delta, float* dq_acc, int Hq, int Dqk, int Dv,
+                             float* dk_acc, float* dv_acc, __nv_bfloat16* dk, __nv_bfloat16* dv, int64_t k_sb,
+                             int64_t k_ss, int64_t k_sh, int64_t v_sb, int64_t v_ss, int64_t v_sh, int Hkv, int bid,
+                             int nblk) {
   const int64_t rows = (int64_t)g.B * g.Sq;
   const int lanes = min(32, Dv / 8);
   const int lane = threadIdx.x & 31;
   const int sub = lane % lanes, grp = lane / lanes, per_warp = 32 / lanes;
-  const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x / 32);
-  for (int64_t base = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) / 32 * per_warp; base < rows * Hq;
+  const int64_t nwarps = (int64_t)nblk * (blockDim.x / 32);
+  for (int64_t base = (bid * (int64_t)blockDim.x + threadIdx.x) / 32 * per_warp; base < rows * Hq;
        base += nwarps * per_warp) {
     const int64_t wrk = base + grp;
     float acc = 0.f;
@@ -436,8 +441,8 @@ __global__ void bwd_pre_kernel(SegInfo g, const __nv_bfloat16* dout, const __nv_
     for (int o = lanes / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
     if (sub == 0 && wrk < rows * Hq) delta[(int64_t)h * rows + f] = acc;
   }
-  const int64_t tid = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
-  const int64_t nthr = (int64_t)gridDim.x * blockDim.x;
+  const int64_t tid = bid * (int64_t)blockDim.x + threadIdx.x;
+  const int64_t nthr = (int64_t)nblk * blockDim.x;
   const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
   const int64_t n4 = rows * Hq * Dqk / 4;
   for (int64_t x = tid; x < n4; x += nthr) reinterpret_cast<float4*>(dq_acc)[x] = z4;
@@ -503,6 +508,34 @@ __global__ void bwd_convert_kernel(const float* dq_acc, __nv_bfloat16* dq, int64
   }
 }
 
+// Forward preparation: block 0 builds the heaviest-first tile list while the
+// other blocks fill uncovered query rows, so the list's latency-bound build
+// overlaps the fill and costs no launch of its own.
+__global__ void __launch_bounds__(kScanThreads) fwd_prep_kernel(SegInfo g, int2* items, int* n_items, int* seg_prefix,
+                                                                int item_cap, int* status, __nv_bfloat16* out,
+                                                                int64_t o_sb, int64_t o_ss, int64_t o_sh, float* lse,
+                                                                int64_t l_sb, int64_t l_sh, int Hq, int Dv) {
+  if (blockIdx.x == 0)
+    schedule_body(g, 0, items, n_items, seg_prefix, item_cap, status);
+  else
+    fwd_tail_body(g, out, o_sb, o_ss, o_sh, lse, l_sb, l_sh, Hq, Dv, blockIdx.x - 1, gridDim.x - 1);
+}
+
+// Backward preparation: block 0 builds the work list while the other blocks
+// compute Delta and zero the accumulators (HBM-bound), hiding the list's
+// latency behind that traffic.
+__global__ void __launch_bounds__(kScanThreads) bwd_prep_kernel(
+    SegInfo g, int G, int Hkv, int split_target, int4* items, int* n_items, int* seg_prefix, int item_cap, int* status,
+    const __nv_bfloat16* dout, const __nv_bfloat16* out, int64_t o_sb, int64_t o_ss, int64_t o_sh, float* delta,
+    float* dq_acc, int Hq, int Dqk, int Dv, float* dk_acc, float* dv_acc, __nv_bfloat16* dk, __nv_bfloat16* dv,
+    int64_t k_sb, int64_t k_ss, int64_t k_sh, int64_t v_sb, int64_t v_ss, int64_t v_sh) {
+  if (blockIdx.x == 0)
+    bwd_schedule_body(g, G, Hkv, split_target, items, n_items, seg_prefix, item_cap, status);
+  else
+    bwd_pre_body(g, dout, out, o_sb, o_ss, o_sh, delta, dq_acc, Hq, Dqk, Dv, dk_acc, dv_acc, dk, dv, k_sb, k_ss, k_sh,
+                 v_sb, v_ss, v_sh, Hkv, blockIdx.x - 1, gridDim.x - 1);
+}
+
 int grid_for(int64_t work, int threads) {
   int64_t g = (work + threads - 1) / threads;
   if (g < 1) g = 1;
@@ -512,26 +545,16 @@ int grid_for(int64_t work, int threads) {
 
 }  // namespace
 
-cudaError_t launch_schedule(const SegInfo& g, int over_keys, int2* items, int* n_items, int* seg_prefix, int item_cap,
-                            int* status, cudaStream_t st) {
-  schedule_kernel<<<1, kScanThreads, 0, st>>>(g, over_keys, items, n_items, seg_prefix, item_cap, status);
+cudaError_t launch_fwd_prep(const SegInfo& g, int2* items, int* n_items, int* seg_prefix, int item_cap, int* status,
+                            __nv_bfloat16* out, int64_t o_sb, int64_t o_ss, int64_t o_sh, float* lse, int64_t l_sb,
+                            int64_t l_sh, int Hq, int Dv, cudaStream_t st) {
+  // The fill usually has no rows at all (the builder covers every token); a
+  // few blocks with a grid-stride loop cover the rest.
+  const int fill = min(grid_for((int64_t)g.B * g.Sq * Hq * (Dv / 8), kScanThreads), 2 * 152);
+  fwd_prep_kernel<<<1 + fill, kScanThreads, 0, st>>>(g, items, n_items, seg_prefix, item_cap, status, out, o_sb, o_ss,
+                                                     o_sh, lse, l_sb, l_sh, Hq, Dv);
   return cudaGetLastError();
 }
-
-cudaError_t launch_bwd_schedule(const SegInfo& g, int G, int Hkv, int split_target, int4* items, int* n_items,
-                                int* seg_prefix, int item_cap, int* status, cudaStream_t st) {
-  bwd_schedule_kernel<<<1, kScanThreads, 0, st>>>(g, G, Hkv, split_target, items, n_items, seg_prefix, item_cap,
-                                                  status);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_fwd_tail(const SegInfo& g, __nv_bfloat16* out, int64_t o_sb, int64_t o_ss, int64_t o_sh, float* lse,
-                            int64_t l_sb, int64_t l_sh, int Hq, int Dv, cudaStream_t st) {
-  fwd_tail_kernel<<<grid_for((int64_t)g.B * g.Sq * Hq * (Dv / 8), 256), 256, 0, st>>>(g, out, o_sb, o_ss, o_sh, lse,
-                                                                                     l_sb, l_sh, Hq, Dv);
-  return cudaGetLastError();
-}
-
 cudaError_t launch_build_segments(const int32_t* ids, int B, int Sk, int Lq, int q0, int32_t* cu_q, int32_t* cu_k,
                                   int capacity, int32_t* meta, uint8_t* seg_is_pad, int* status, cudaStream_t st) {
   build_segments_kernel<<<1, kScanThreads, 0, st>>>(ids, B, Sk, Lq, q0, cu_q, cu_k, capacity, meta, seg_is_pad,
@@ -552,18 +575,19 @@ cudaError_t launch_lse_merge(const __nv_bfloat16* o1, const float* l1, const __n
   return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_pre(const SegInfo& g, const __nv_bfloat16* dout, const __nv_bfloat16* out, int64_t o_sb,
-                           int64_t o_ss, int64_t o_sh, float* delta, float* dq_acc, int Hq, int Dqk, int Dv,
-                           float* dk_acc, float* dv_acc, __nv_bfloat16* dk, __nv_bfloat16* dv, int64_t k_sb,
-                           int64_t k_ss, int64_t k_sh, int64_t v_sb, int64_t v_ss, int64_t v_sh, int Hkv,
-                           cudaStream_t st) {
+cudaError_t launch_bwd_prep(const SegInfo& g, int G, int Hkv, int split_target, int4* items, int* n_items,
+                            int* seg_prefix, int item_cap, int* status, const __nv_bfloat16* dout,
+                            const __nv_bfloat16* out, int64_t o_sb, int64_t o_ss, int64_t o_sh, float* delta,
+                            float* dq_acc, int Hq, int Dqk, int Dv, float* dk_acc, float* dv_acc, __nv_bfloat16* dk,
+                            __nv_bfloat16* dv, int64_t k_sb, int64_t k_ss, int64_t k_sh, int64_t v_sb, int64_t v_ss,
+                            int64_t v_sh, cudaStream_t st) {
   const int64_t work = (int64_t)g.B * g.Sq * Hq * Dqk / 4 + (int64_t)g.B * g.Sk * Hkv * (Dqk + Dv) / 4;
-  bwd_pre_kernel<<<grid_for(work, 256), 256, 0, st>>>(g, dout, out, o_sb, o_ss, o_sh, delta, dq_acc, Hq, Dqk, Dv,
-                                                       dk_acc, dv_acc, dk, dv, k_sb, k_ss, k_sh, v_sb, v_ss, v_sh,
-                                                       Hkv);
+  const int fill = min(grid_for(work, kScanThreads), 2 * 152);
+  bwd_prep_kernel<<<1 + fill, kScanThreads, 0, st>>>(g, G, Hkv, split_target, items, n_items, seg_prefix, item_cap,
+                                                     status, dout, out, o_sb, o_ss, o_sh, delta, dq_acc, Hq, Dqk, Dv,
+                                                     dk_acc, dv_acc, dk, dv, k_sb, k_ss, k_sh, v_sb, v_ss, v_sh);
   return cudaGetLastError();
 }
-
 cudaError_t launch_bwd_convert(const float* dq_acc, __nv_bfloat16* dq, bool have_q, int B, int Sq, int Hq, int Dqk,
                                int64_t q_sb, int64_t q_ss, int64_t q_sh, const float* dk_acc, __nv_bfloat16* dk,
                                const float* dv_acc, __nv_bfloat16* dv, int Sk, int Hkv, int Dv, int64_t k_sb,

@@ -11,18 +11,25 @@ namespace psf {
 struct FwdParams;
 struct BwdParams;
 
-// Heaviest-first work list over query tiles (over_keys = 0) or key tiles
-// (over_keys = 1) of every segment; validates the segment arrays. Also zeroes
-// n_items[1], the counter of kernels that take work items dynamically.
-cudaError_t launch_schedule(const SegInfo& g, int over_keys, int2* items, int* n_items, int* seg_prefix,
-                            int item_cap, int* status, cudaStream_t st);
-// Backward work list: key tiles split into (first step, end step) sub-ranges
-// when split_target > 0; items are int4 (segment, key tile, first, end).
-cudaError_t launch_bwd_schedule(const SegInfo& g, int G, int Hkv, int split_target, int4* items, int* n_items,
-                                int* seg_prefix, int item_cap, int* status, cudaStream_t st);
-// out = 0 and lse = -inf for query rows at or past cu_q[nseg].
-cudaError_t launch_fwd_tail(const SegInfo& g, __nv_bfloat16* out, int64_t o_sb, int64_t o_ss, int64_t o_sh, float* lse,
-                            int64_t l_sb, int64_t l_sh, int Hq, int Dv, cudaStream_t st);
+// Forward preparation in one launch: the heaviest-first list of (segment, query
+// tile) items (validating the segment arrays; n_items[1] is zeroed as the
+// counter of kernels that take items dynamically), and out = 0 / lse = -inf for
+// query rows at or past cu_q[nseg].
+cudaError_t launch_fwd_prep(const SegInfo& g, int2* items, int* n_items, int* seg_prefix, int item_cap, int* status,
+                            __nv_bfloat16* out, int64_t o_sb, int64_t o_ss, int64_t o_sh, float* lse, int64_t l_sb,
+                            int64_t l_sh, int Hq, int Dv, cudaStream_t st);
+// Backward preparation in one launch: the work list of key tiles, split into
+// (first step, end step) sub-ranges when split_target > 0 (items are int4
+// (segment, key tile, first, end); n_items[1] zeroed as above); Delta =
+// rowsum(dO * O) (fp32, [Hq][rows]); the zeroed dQ accumulator, and either the
+// zeroed dK/dV accumulators (when given) or zeroed dK / dV rows at or past
+// cu_k[nseg].
+cudaError_t launch_bwd_prep(const SegInfo& g, int G, int Hkv, int split_target, int4* items, int* n_items,
+                            int* seg_prefix, int item_cap, int* status, const __nv_bfloat16* dout,
+                            const __nv_bfloat16* out, int64_t o_sb, int64_t o_ss, int64_t o_sh, float* delta,
+                            float* dq_acc, int Hq, int Dqk, int Dv, float* dk_acc, float* dv_acc, __nv_bfloat16* dk,
+                            __nv_bfloat16* dv, int64_t k_sb, int64_t k_ss, int64_t k_sh, int64_t v_sb, int64_t v_ss,
+                            int64_t v_sh, cudaStream_t st);
 // Grid: one CTA per SM (two for head dims 64 and 128), at most max_work.
 cudaError_t launch_fwd(const FwdParams& p, int dqk, int dvc, int sms, int64_t max_work, cudaStream_t st);
 cudaError_t launch_bwd(const BwdParams& p, int dqk, int dv, int sms, int item_cap, cudaStream_t st);
@@ -35,13 +42,6 @@ cudaError_t launch_pad_fixup(__nv_bfloat16* out, float* lse, const int32_t* qids
                              int64_t o_sb, int64_t o_ss, int64_t o_sh, int64_t l_sb, int64_t l_sh, cudaStream_t st);
 cudaError_t launch_lse_merge(const __nv_bfloat16* o1, const float* l1, const __nv_bfloat16* o2, const float* l2,
                              float* of, __nv_bfloat16* ob, float* l, int T, int H, int D, cudaStream_t st);
-// Delta = rowsum(dO * O) (fp32, [Hq][rows]); zero the fp32 accumulators
-// (dK/dV ones when given; otherwise dK / dV rows at or past cu_k[nseg]).
-cudaError_t launch_bwd_pre(const SegInfo& g, const __nv_bfloat16* dout, const __nv_bfloat16* out, int64_t o_sb,
-                           int64_t o_ss, int64_t o_sh, float* delta, float* dq_acc, int Hq, int Dqk, int Dv,
-                           float* dk_acc, float* dv_acc, __nv_bfloat16* dk, __nv_bfloat16* dv, int64_t k_sb,
-                           int64_t k_ss, int64_t k_sh, int64_t v_sb, int64_t v_ss, int64_t v_sh, int Hkv,
-                           cudaStream_t st);
 // dQ = scale * dQacc (bf16, q's layout); with accumulators also dK = scale *
 // dKacc and dV = dVacc.
 cudaError_t launch_bwd_convert(const float* dq_acc, __nv_bfloat16* dq, bool have_q, int B, int Sq, int Hq, int Dqk,
