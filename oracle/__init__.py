@@ -63,6 +63,8 @@ def _load():
             lib.oracle_build_segments.argtypes = [P, I, I, I, I, P, P, I, P, P]
             lib.oracle_build_segments.restype = I
             lib.oracle_lse_merge.argtypes = [P, P, P, P, P, P, I, I, I]
+            lib.oracle_build_cross_segments.argtypes = [P, I, I, I, I, I, I, P, P, P, P]
+            lib.oracle_build_cross_segments.restype = I
             lib.oracle_lse_merge.restype = None
             _lib = lib
     return _lib
@@ -252,6 +254,57 @@ def build_segments(doc_ids, q_length, q_global_start):
     if n < 0:
         raise ValueError("oracle_build_segments: capacity exceeded")
     return cu_q[: n + 1].copy(), cu_k[: n + 1].copy(), int(mq[0]), int(mk[0])
+
+
+def build_cross_segments(doc_ids, q_start, q_length, k_start, k_length):
+    """Cross-chunk segments of the shard [q_start, q_start + q_length) against
+    the earlier key chunk [k_start, k_start + k_length) of every row of
+    doc_ids [B, S] -> (cu_q, cu_k, max_q, max_k)."""
+    lib = _load()
+    doc_ids = _i32(doc_ids)
+    if doc_ids.ndim == 1:
+        doc_ids = doc_ids[None, :]
+    B, S = doc_ids.shape
+    cu_q = np.zeros(3 * B + 1, dtype=np.int32)
+    cu_k = np.zeros(3 * B + 1, dtype=np.int32)
+    mq = np.zeros(1, dtype=np.int32)
+    mk = np.zeros(1, dtype=np.int32)
+    n = lib.oracle_build_cross_segments(_ptr(doc_ids), B, S, int(q_start), int(q_length), int(k_start),
+                                        int(k_length), _ptr(cu_q), _ptr(cu_k), _ptr(mq), _ptr(mk))
+    if n < 0:
+        raise ValueError("oracle_build_cross_segments: the key chunk must lie before the query shard")
+    return cu_q, cu_k, int(mq[0]), int(mk[0])
+
+
+def live_rows(cu_q, cu_k):
+    """Query rows of the segments that have at least one key (numpy int array)."""
+    cu_q, cu_k = np.asarray(cu_q), np.asarray(cu_k)
+    rows = [np.arange(cu_q[s], cu_q[s + 1]) for s in range(len(cu_q) - 1) if cu_k[s + 1] > cu_k[s]]
+    return np.concatenate(rows).astype(np.int64) if rows else np.zeros(0, np.int64)
+
+
+def lse_merge_live_rows(o_acc, l_acc, o_new, l_new, cu_q, cu_k):
+    """Running result (o_acc [T,H,D], l_acc [H,T]) merged with one chunk's
+    (o_new, l_new) on the query rows of the chunk's segments with keys; the
+    other rows keep the running values. Returns new fp64 arrays.
+    [cp_attention page, the in-place live-row merge]"""
+    o = _f64(o_acc).copy()
+    l = _f64(l_acc).copy()
+    rows = live_rows(cu_q, cu_k)
+    if rows.size:
+        om, lm = lse_merge(o[rows], l[:, rows], _f64(o_new)[rows], _f64(l_new)[:, rows])
+        o[rows] = om
+        l[:, rows] = lm
+    return o, l
+
+
+def grad_add_live_rows(dst, src, cu_q, cu_k):
+    """dst + src on the query rows of the segments with keys, dst elsewhere
+    (fp64). [cp_attention page, the in-place grad scatter-add]"""
+    out = _f64(dst).copy()
+    rows = live_rows(cu_q, cu_k)
+    out[rows] += _f64(src)[rows]
+    return out
 
 
 def lse_merge(o1, l1, o2, l2):

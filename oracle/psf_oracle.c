@@ -51,6 +51,19 @@
  *    a row with both inputs -inf stays 0 with lse -inf.
  *      [nemo_automodel.components.models.gemma4_moe.cp_attention, the
  *       "-inf-safe online-softmax merge" docstring]
+ *  - cross-chunk segment builder: a query shard [q0, q0 + Lq) and an earlier
+ *    key chunk [k0, k0 + Lk) (k0 + Lk <= q0) of every batch row; a document
+ *    (a maximal run of one nonzero id) present in both pairs its shard queries
+ *    with its chunk keys as one segment, which the chunk runs without a causal
+ *    mask (every chunk key precedes every shard query). Since runs are
+ *    contiguous, only the run holding position q0 can reach back into the chunk.
+ *    Each row gives three segments in the packed shard / chunk rows:
+ *    (no queries x the chunk keys before that run), (the run's shard queries x
+ *    its chunk keys), (the other shard queries x no keys); the middle one is
+ *    empty when no document is shared.
+ *      [nemo_automodel.components.models.gemma4_moe.cp_attention,
+ *       `_build_packed_ring_segments`: "for each doc present in both", paired
+ *       query and key tokens, cu_q[i] pairing cu_k[i]]
  *
  * Layouts: q [Tq, Hq, Dqk], k [Tk, Hkv, Dqk], v [Tk, Hkv, Dv], out [Tq, Hq, Dv],
  * lse [Hq, Tq], all row-major and contiguous, double precision.
@@ -541,4 +554,45 @@ void oracle_lse_merge(const double *o1, const double *l1, const double *o2, cons
             for (int d = 0; d < D; ++d) od[d] = wa * x[d] + wb * y[d];
         }
     }
+}
+
+/*
+ * Cross-chunk segments of a query shard against an earlier key chunk (see the
+ * header). Writes cu_q / cu_k (3 B + 1 entries each) over the packed shard rows
+ * (b * Lq + p - q0) and chunk rows (b * Lk + j - k0); returns 3 B, or -1 when
+ * the chunk does not lie before the shard.
+ */
+int oracle_build_cross_segments(const int32_t *doc_ids, int B, int S, int q0, int Lq, int k0, int Lk,
+                                int32_t *cu_q, int32_t *cu_k, int32_t *max_q, int32_t *max_k) {
+    if (q0 < 0 || Lq < 0 || k0 < 0 || Lk < 0 || k0 + Lk > q0 || q0 + Lq > S) return -1;
+    int mq = 0, mk = 0, n = 0;
+    cu_q[0] = 0;
+    cu_k[0] = 0;
+    for (int b = 0; b < B; ++b) {
+        const int32_t *ids = doc_ids + (size_t)b * S;
+        int nq = 0, ks = k0 + Lk; /* shared run: queries [q0, q0 + nq), keys [ks, k0 + Lk) */
+        if (Lq > 0 && Lk > 0 && ids[q0] != 0) {
+            int d = ids[q0];
+            int s0 = q0;
+            while (s0 > 0 && ids[s0 - 1] == d) --s0;
+            int e = q0;
+            while (e < S && ids[e] == d) ++e;
+            if (s0 < k0 + Lk) {
+                ks = s0 > k0 ? s0 : k0;
+                nq = (e < q0 + Lq ? e : q0 + Lq) - q0;
+            }
+        }
+        const int qn[3] = {0, nq, Lq - nq};
+        const int kn[3] = {ks - k0, k0 + Lk - ks, 0};
+        for (int i = 0; i < 3; ++i) {
+            cu_q[n + 1] = cu_q[n] + qn[i];
+            cu_k[n + 1] = cu_k[n] + kn[i];
+            if (qn[i] > mq) mq = qn[i];
+            if (kn[i] > mk) mk = kn[i];
+            ++n;
+        }
+    }
+    *max_q = mq;
+    *max_k = mk;
+    return n;
 }

@@ -10,7 +10,10 @@ Sources of truth used here (never the oracle's own formula retyped):
   * invariants (GQA = repeated-KV MHA, chunked results merged by lse = full result,
     document mode = segment mode over the builder's segments, zero-query segments
     contribute nothing, pad rows zero);
-  * hand-derived segment lists and brute-force pair visibility for the builder.
+  * hand-derived segment lists and brute-force pair visibility for the builders
+    (doc ids -> segments, and the cross-chunk builder of a query shard against an
+    earlier key chunk), and the cross-chunk decomposition (live-row merge, live-row
+    gradient add) against document mode on the unsplit problem.
 """
 import json
 import math
@@ -400,3 +403,104 @@ def test_builder_brute_force_visibility_and_tiling(seed):
                 if same_run and j <= p:
                     doc_vis[b * Lq + i, b * S + j] = True
     np.testing.assert_array_equal(seg_vis, doc_vis)
+
+
+# ---------------------------------------------------------------------------
+# cross-chunk pins (the one-device core of the ring decomposition)
+
+def test_cross_builder_golden_examples():
+    with open(os.path.join(GOLDEN, "cross_examples.json")) as fh:
+        cases = json.load(fh)["cases"]
+    for c in cases:
+        cu_q, cu_k, mq, mk = oracle.build_cross_segments(c["doc_ids"], c["q_start"], c["q_length"], c["k_start"],
+                                                         c["k_length"])
+        assert cu_q.tolist() == c["cu_q"], c
+        assert cu_k.tolist() == c["cu_k"], c
+        assert (mq, mk) == (c["max_q"], c["max_k"]), c
+
+
+def test_cross_builder_rejects_chunk_after_shard_start():
+    with pytest.raises(ValueError):
+        oracle.build_cross_segments([[1, 1, 1, 1]], 2, 2, 1, 2)
+
+
+@pytest.mark.parametrize("seed", range(25))
+def test_cross_builder_brute_force_pairs_and_tiling(seed):
+    r = np.random.default_rng(seed)
+    B, S = int(r.integers(1, 4)), int(r.integers(2, 24))
+    ids = _random_doc_ids(B, S, 300 + seed, pad_prob=0.25)
+    q0 = int(r.integers(1, S))
+    Lq = int(r.integers(0, S - q0 + 1))
+    k0 = int(r.integers(0, q0))
+    Lk = int(r.integers(0, q0 - k0 + 1))
+    cu_q, cu_k, mq, mk = oracle.build_cross_segments(ids, q0, Lq, k0, Lk)
+    nq, nk = np.diff(cu_q), np.diff(cu_k)
+    assert len(nq) == 3 * B and cu_q[-1] == B * Lq and cu_k[-1] == B * Lk
+    assert np.all(nq >= 0) and np.all(nk >= 0)
+    assert mq == nq.max() and mk == nk.max()
+    # every segment lies inside its own batch row of the shard and the chunk
+    for s in range(3 * B):
+        b = s // 3
+        assert b * Lq <= cu_q[s] <= cu_q[s + 1] <= (b + 1) * Lq
+        assert b * Lk <= cu_k[s] <= cu_k[s + 1] <= (b + 1) * Lk
+    # non-causal pairs of the segments = same nonzero run across shard and chunk
+    seg_vis = np.zeros((B * Lq, B * Lk), bool)
+    for s in range(3 * B):
+        seg_vis[cu_q[s]:cu_q[s + 1], cu_k[s]:cu_k[s + 1]] = True
+    doc_vis = np.zeros_like(seg_vis)
+    for b in range(B):
+        for i in range(Lq):
+            p = q0 + i
+            for jj in range(Lk):
+                j = k0 + jj
+                run = ids[b, j:p + 1]
+                if ids[b, p] != 0 and np.all(run == ids[b, p]):
+                    doc_vis[b * Lq + i, b * Lk + jj] = True
+    np.testing.assert_array_equal(seg_vis, doc_vis)
+
+
+def _pad_fix(out, lse, qids):
+    out = out.copy()
+    lse = lse.copy()
+    pad = np.asarray(qids).reshape(-1) == 0
+    out[pad] = 0.0
+    lse[:, pad] = -np.inf
+    return out, lse
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_cross_chunk_decomposition_equals_document_mode(seed):
+    # shard [q0, S) of one row: its own keys causally (segments from the
+    # builder on the shard's sub-map) plus the earlier keys [0, q0) through the
+    # cross segments (non-causal); the live-row merge, the pad fixup, each
+    # chunk's backward fed the merged out/lse and the live-row gradient add
+    # must give the document-mode result of the unsplit problem.
+    r = np.random.default_rng(seed)
+    S, Hq, Hkv, D = 40, 2, 1, 8
+    ids = _random_doc_ids(1, S, 500 + seed, pad_prob=0.15)
+    q0 = int(r.integers(8, 32))
+    Lq = S - q0
+    q, k, v, do = rnd(Lq, Hq, D), rnd(S, Hkv, D), rnd(S, Hkv, D), rnd(Lq, Hq, D)
+    scale = 0.4
+    cq1, ck1, _, _ = oracle.build_segments(ids[:, q0:], Lq, 0)
+    cq2, ck2, _, _ = oracle.build_cross_segments(ids, q0, Lq, 0, q0)
+    o1, l1 = oracle.attn_fwd_segments(q, k[q0:], v[q0:], cq1, ck1, scale, True)
+    o2, l2 = oracle.attn_fwd_segments(q, k[:q0], v[:q0], cq2, ck2, scale, False)
+    om, lm = oracle.lse_merge_live_rows(o1, l1, o2, l2, cq2, ck2)
+    om, lm = _pad_fix(om, lm, ids[:, q0:])
+    ref_o, ref_l = oracle.attn_fwd_document(q, k, v, ids, q0, scale, None)
+    np.testing.assert_allclose(om, ref_o, atol=1e-12)
+    np.testing.assert_array_equal(np.isneginf(lm), np.isneginf(ref_l))
+    fin = np.isfinite(ref_l)
+    np.testing.assert_allclose(lm[fin], ref_l[fin], atol=1e-12)
+    dq1, dk1, dv1 = oracle.attn_bwd_segments(do, q, k[q0:], v[q0:], om, lm, cq1, ck1, scale, True)
+    dq2, dk2, dv2 = oracle.attn_bwd_segments(do, q, k[:q0], v[:q0], om, lm, cq2, ck2, scale, False)
+    dq = oracle.grad_add_live_rows(dq1, dq2, cq2, ck2)
+    rq, rk, rv = oracle.attn_bwd_document(do, q, k, v, ref_o, ref_l, ids, q0, scale, None)
+    np.testing.assert_allclose(dq, rq, atol=1e-10)
+    np.testing.assert_allclose(np.concatenate([dk2, dk1]), rk, atol=1e-10)
+    np.testing.assert_allclose(np.concatenate([dv2, dv1]), rv, atol=1e-10)
+    # rows outside the cross chunk's live segments kept the local result
+    live = oracle.live_rows(cq2, ck2)
+    other = np.setdiff1d(np.arange(Lq), live)
+    np.testing.assert_array_equal(dq[other], dq1[other])
