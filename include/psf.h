@@ -232,6 +232,61 @@ int psf_pad_fixup(void* out, float* lse, const int32_t* q_doc_ids, int layout, i
 int psf_lse_merge(const void* o1, const float* l1, const void* o2, const float* l2, float* o_f32, void* o_bf16,
                   float* l, int T, int H, int D, void* stream);
 
+/*
+ * Cross-chunk segments of a query shard against an earlier key chunk, on the
+ * GPU (the one-device core of the ring decomposition).
+ *                           [cp_attention page, `_build_packed_ring_segments`:
+ *                            for each document present in both the query shard
+ *                            and the KV chunk, its query tokens are paired with
+ *                            its key tokens as one segment, cu_q[i] pairing
+ *                            cu_k[i]; the chunk before the shard runs without a
+ *                            causal mask]
+ *  kv_doc_ids: int32 [B, S] document ids (1-based, 0 = padding, no document).
+ *  The shard is [q_start, q_start + q_length) and the chunk
+ *  [k_start, k_start + k_length) of every row, with the chunk before the shard
+ *  (k_start + k_length <= q_start); the shard's queries and the chunk's keys are
+ *  packed row-major as B * q_length and B * k_length rows. Since documents are
+ *  contiguous runs, only the run holding position q_start can be shared. Each
+ *  row gives three segments: (no queries x the chunk keys before the shared
+ *  run), (the run's shard queries x its chunk keys), (the remaining shard
+ *  queries x no keys); with nothing shared the middle one is empty.
+ *  Outputs: cu_q, cu_k int32 [3 B + 1]; dev_meta int32[3] = {3 B, max_q, max_k}.
+ *  Run the chunk with psf_attn_varlen_fwd/bwd, causal = 0: shard queries outside
+ *  the shared run get out = 0, lse = -inf, dq = 0.
+ *  Errors: PSF_EINVAL when the chunk does not lie before the shard.
+ */
+int psf_build_cross_segments(const int32_t* kv_doc_ids, int B, int S, int q_start, int q_length, int k_start,
+                             int k_length, int32_t* cu_q, int32_t* cu_k, int32_t* dev_meta, void* stream);
+
+/*
+ * Merge one key chunk's result into a running result, in place, on the query
+ * rows that took part in the chunk.
+ *                           [cp_attention page, the in-place live-row merge of
+ *                            a varlen chunk into the running accumulators at its
+ *                            rows only, with the online-softmax merge]
+ *  Live rows: the query rows of segments (cu_q, cu_k) that have at least one
+ *  key. On those rows l = logaddexp(l_acc, l_new) and o = o_run exp(l_acc - l)
+ *  + o_new exp(l_new - l) (both -inf gives o = 0, l = -inf); other rows are not
+ *  touched. Running output: o_acc fp32 [T, H, D] (nullable) and/or o_run bf16
+ *  [T, H, D] (nullable), read from o_acc when given, written to both; l_acc fp32
+ *  [H, T] in place. o_new bf16 [T, H, D], l_new fp32 [H, T].
+ *  Segments: nseg (or dev_meta[0], capped at nseg, when dev_meta is given).
+ */
+int psf_lse_merge_live_rows(float* o_acc, void* o_run, float* l_acc, const void* o_new, const float* l_new,
+                            const int32_t* cu_q, const int32_t* cu_k, const int32_t* dev_meta, int nseg, int T, int H,
+                            int D, void* stream);
+
+/*
+ * Add one key chunk's query gradient into the running one on the query rows
+ * that took part in the chunk.
+ *                           [cp_attention page, the in-place grad scatter-add
+ *                            of a chunk's packed gradient into the full one]
+ *  dst += src on the live rows of (cu_q, cu_k) (as in psf_lse_merge_live_rows),
+ *  bf16 [T, H, D] both, added in fp32 and rounded once; other rows untouched.
+ */
+int psf_grad_add_live_rows(void* dst, const void* src, const int32_t* cu_q, const int32_t* cu_k,
+                           const int32_t* dev_meta, int nseg, int T, int H, int D, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -40,6 +40,9 @@ SIGNATURES = {
     "psf_build_doc_segments": (I, [P, I, I, I, I, P, P, I, P, P, P]),
     "psf_pad_fixup": (I, [P, P, P, I, I, I, I, I, P]),
     "psf_lse_merge": (I, [P, P, P, P, P, P, P, I, I, I, P]),
+    "psf_build_cross_segments": (I, [P, I, I, I, I, I, I, P, P, P, P]),
+    "psf_lse_merge_live_rows": (I, [P, P, P, P, P, P, P, P, I, I, I, I, P]),
+    "psf_grad_add_live_rows": (I, [P, P, P, P, P, I, I, I, I, P]),
 }
 
 PSF_LAYOUT_THD = 0

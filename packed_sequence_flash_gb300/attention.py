@@ -236,6 +236,53 @@ def lse_merge(o1, l1, o2, l2, want_f32=True, want_bf16=False):
     return of, ob, l
 
 
+def build_cross_segments(kv_doc_ids, q_start, q_length, k_start, k_length):
+    """Segments of the shard [q_start, q_start + q_length) against the earlier
+    key chunk [k_start, k_start + k_length) of every row of kv_doc_ids [B, S]
+    (device int32) -> (cu_q, cu_k, dev_meta), 3 segments per row; run the chunk
+    with causal=False."""
+    _i32(kv_doc_ids, "kv_doc_ids")
+    if kv_doc_ids.dim() == 1:
+        kv_doc_ids = kv_doc_ids[None]
+    B, S = kv_doc_ids.shape
+    dev = kv_doc_ids.device
+    cu_q = torch.empty(3 * B + 1, dtype=torch.int32, device=dev)
+    cu_k = torch.empty(3 * B + 1, dtype=torch.int32, device=dev)
+    meta = torch.empty(3, dtype=torch.int32, device=dev)
+    rc = _lib.load().psf_build_cross_segments(_ptr(kv_doc_ids), B, S, int(q_start), int(q_length), int(k_start),
+                                              int(k_length), _ptr(cu_q), _ptr(cu_k), _ptr(meta), _stream())
+    check(rc)
+    return cu_q, cu_k, meta
+
+
+def lse_merge_live_rows(o_run, l_acc, o_new, l_new, cu_q, cu_k, dev_meta=None, o_acc=None):
+    """In place: merge (o_new, l_new) into the running (o_run / o_acc, l_acc) on
+    the query rows of the segments that have keys. o_run bf16 [T,H,D] (may be
+    None when o_acc, fp32 [T,H,D], holds the running output), l_acc fp32 [H,T]."""
+    _need(o_new, "o_new", torch.bfloat16)
+    for t, n in ((l_acc, "l_acc"), (l_new, "l_new")):
+        _need(t, n, torch.float32)
+    if o_run is not None:
+        _need(o_run, "o_run", torch.bfloat16)
+    if o_acc is not None:
+        _need(o_acc, "o_acc", torch.float32)
+    T, H, D = o_new.shape
+    rc = _lib.load().psf_lse_merge_live_rows(_ptr(o_acc), _ptr(o_run), _ptr(l_acc), _ptr(o_new), _ptr(l_new),
+                                             _ptr(cu_q), _ptr(cu_k), _ptr(dev_meta), cu_q.numel() - 1, T, H, D,
+                                             _stream())
+    check(rc)
+
+
+def grad_add_live_rows(dst, src, cu_q, cu_k, dev_meta=None):
+    """In place: dst += src (bf16 [T,H,D]) on the query rows of the segments that have keys."""
+    _need(dst, "dst", torch.bfloat16)
+    _need(src, "src", torch.bfloat16)
+    T, H, D = dst.shape
+    rc = _lib.load().psf_grad_add_live_rows(_ptr(dst), _ptr(src), _ptr(cu_q), _ptr(cu_k), _ptr(dev_meta),
+                                            cu_q.numel() - 1, T, H, D, _stream())
+    check(rc)
+
+
 # ---------------------------------------------------------------------------
 # document-causal composition [fa4 page, document_causal_fa4_attention]
 

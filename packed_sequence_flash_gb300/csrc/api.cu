@@ -585,4 +585,50 @@ int psf_lse_merge(const void* o1, const float* l1, const void* o2, const float* 
   return e == cudaSuccess ? PSF_OK : cuda_fail(e, "merge launch");
 }
 
+int psf_build_cross_segments(const int32_t* kv_doc_ids, int B, int S, int q_start, int q_length, int k_start,
+                             int k_length, int32_t* cu_q, int32_t* cu_k, int32_t* dev_meta, void* stream) {
+  if (B < 1 || S < 0 || q_start < 0 || q_length < 0 || k_start < 0 || k_length < 0 ||
+      (int64_t)q_start + q_length > S || (int64_t)k_start + k_length > q_start)
+    return fail(PSF_EINVAL, "need 0 <= k_start <= k_start + k_length <= q_start <= q_start + q_length <= S");
+  if ((int64_t)B * 3 + 1 > 0x7fffffff || (int64_t)B * (S + 1) > 0x7fffffff) return fail(PSF_EINVAL, "too many rows");
+  if (!cu_q || !cu_k || !dev_meta || (S > 0 && !kv_doc_ids)) return fail(PSF_EINVAL, "null pointer");
+  DeviceInfo* dev = nullptr;
+  int rc = device_info(&dev);
+  if (rc) return rc;
+  cudaError_t e = launch_cross_segments(kv_doc_ids, B, S, q_start, q_length, k_start, k_length, cu_q, cu_k, dev_meta,
+                                        static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PSF_OK : cuda_fail(e, "cross builder launch");
+}
+
+int psf_lse_merge_live_rows(float* o_acc, void* o_run, float* l_acc, const void* o_new, const float* l_new,
+                            const int32_t* cu_q, const int32_t* cu_k, const int32_t* dev_meta, int nseg, int T, int H,
+                            int D, void* stream) {
+  if (T < 0 || H < 1 || D < 8 || D % 8 || nseg < 0) return fail(PSF_EINVAL, "bad sizes");
+  if (T == 0 || nseg == 0) return PSF_OK;
+  if ((!o_acc && !o_run) || !l_acc || !o_new || !l_new || !cu_q || !cu_k) return fail(PSF_EINVAL, "null pointer");
+  if ((o_acc && !aligned16(o_acc)) || (o_run && !aligned16(o_run)) || !aligned16(o_new))
+    return fail(PSF_EINVAL, "unaligned pointer");
+  DeviceInfo* dev = nullptr;
+  int rc = device_info(&dev);
+  if (rc) return rc;
+  cudaError_t e = launch_lse_merge_live(o_acc, static_cast<__nv_bfloat16*>(o_run), l_acc,
+                                        static_cast<const __nv_bfloat16*>(o_new), l_new, cu_q, cu_k, dev_meta, nseg, T,
+                                        H, D, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PSF_OK : cuda_fail(e, "live-row merge launch");
+}
+
+int psf_grad_add_live_rows(void* dst, const void* src, const int32_t* cu_q, const int32_t* cu_k,
+                           const int32_t* dev_meta, int nseg, int T, int H, int D, void* stream) {
+  if (T < 0 || H < 1 || D < 8 || D % 8 || nseg < 0) return fail(PSF_EINVAL, "bad sizes");
+  if (T == 0 || nseg == 0) return PSF_OK;
+  if (!dst || !src || !cu_q || !cu_k) return fail(PSF_EINVAL, "null pointer");
+  if (!aligned16(dst) || !aligned16(src)) return fail(PSF_EINVAL, "unaligned pointer");
+  DeviceInfo* dev = nullptr;
+  int rc = device_info(&dev);
+  if (rc) return rc;
+  cudaError_t e = launch_grad_add_live(static_cast<__nv_bfloat16*>(dst), static_cast<const __nv_bfloat16*>(src), cu_q,
+                                       cu_k, dev_meta, nseg, T, H, D, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PSF_OK : cuda_fail(e, "live-row gradient add launch");
+}
+
 }  // extern "C"

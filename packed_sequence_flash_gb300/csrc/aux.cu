@@ -508,6 +508,157 @@ __global__ void bwd_convert_kernel(const float* dq_acc, __nv_bfloat16* dq, int64
   }
 }
 
+// Cross-chunk segments of a query shard [q0, q0 + Lq) against an earlier key
+// chunk [k0, k0 + Lk) of every row: block b handles row b. Runs are contiguous,
+// so only the run holding position q0 can reach back into the chunk; the block
+// finds where that run starts inside the chunk (the last position in [k0, q0)
+// with another id, plus one) and where it ends inside the shard.
+// dev_meta must hold zeros on entry (the launcher clears it).
+__global__ void __launch_bounds__(kScanThreads) cross_segments_kernel(const int32_t* ids, int B, int S, int q0, int Lq,
+                                                                      int k0, int Lk, int32_t* cu_q, int32_t* cu_k,
+                                                                      int32_t* dev_meta) {
+  const int b = blockIdx.x, tid = threadIdx.x;
+  const int32_t* row = ids + (size_t)b * S;
+  int nq = 0, ks = k0 + Lk;  // shared run: shard queries [q0, q0 + nq), chunk keys [ks, k0 + Lk)
+  if (Lq > 0 && Lk > 0) {
+    const int d = row[q0];
+    if (d != 0) {
+      int last = k0 - 1;
+      for (int p = k0 + tid; p < q0; p += blockDim.x)
+        if (row[p] != d) last = max(last, p);
+      last = block_max(last);
+      if (last + 1 < k0 + Lk) {
+        ks = last + 1;
+        int first = -(q0 + Lq);  // block_max of the negated first position with another id
+        for (int p = q0 + tid; p < q0 + Lq; p += blockDim.x)
+          if (row[p] != d) first = max(first, -p);
+        nq = -block_max(first) - q0;
+      }
+    }
+  }
+  if (tid == 0) {
+    const int qb = b * Lq, kb = b * Lk;
+    cu_q[3 * b + 1] = qb;
+    cu_q[3 * b + 2] = qb + nq;
+    cu_q[3 * b + 3] = qb + Lq;
+    cu_k[3 * b + 1] = kb + (ks - k0);
+    cu_k[3 * b + 2] = kb + Lk;
+    cu_k[3 * b + 3] = kb + Lk;
+    if (b == 0) {
+      cu_q[0] = 0;
+      cu_k[0] = 0;
+      dev_meta[0] = 3 * B;
+    }
+    atomicMax(&dev_meta[1], max(nq, Lq - nq));
+    atomicMax(&dev_meta[2], max(ks - k0, k0 + Lk - ks));
+  }
+}
+
+// Segment holding row t (cu_q[s] <= t < cu_q[s + 1]) if it has keys, else -1.
+__device__ __forceinline__ int live_segment(const int32_t* cu_q, const int32_t* cu_k, int nseg, int t) {
+  int lo = 0, hi = nseg - 1;  // largest s in [0, nseg) with cu_q[s] <= t
+  if (nseg <= 0 || __ldg(cu_q) > t) return -1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(cu_q + mid) <= t)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  if (t >= __ldg(cu_q + lo + 1)) return -1;
+  return __ldg(cu_k + lo + 1) > __ldg(cu_k + lo) ? lo : -1;
+}
+
+// In-place merge of one chunk's (o_new, l_new) into the running result on the
+// query rows of the chunk's segments with keys; a warp per (row, head). The
+// running output is read from o_acc (fp32) when given, else from o_run (bf16);
+// both are written when given.
+__global__ void lse_merge_live_kernel(float* o_acc, __nv_bfloat16* o_run, float* l_acc, const __nv_bfloat16* o_new,
+                                      const float* l_new, const int32_t* cu_q, const int32_t* cu_k,
+                                      const int32_t* dev_meta, int nseg_cap, int T, int H, int D) {
+  const int nseg = dev_meta ? min(dev_meta[0], nseg_cap) : nseg_cap;
+  const int lane = threadIdx.x & 31;
+  const int64_t nw = (int64_t)gridDim.x * (blockDim.x / 32);
+  for (int64_t w = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) / 32; w < (int64_t)T * H; w += nw) {
+    const int t = (int)(w / H), h = (int)(w - (int64_t)t * H);
+    if (live_segment(cu_q, cu_k, nseg, t) < 0) continue;
+    const float a = l_acc[(int64_t)h * T + t], c = l_new[(int64_t)h * T + t];
+    const float m = fmaxf(a, c);
+    const float l = m == -CUDART_INF_F ? -CUDART_INF_F : m + logf(expf(a - m) + expf(c - m));
+    const float wa = l == -CUDART_INF_F ? 0.f : expf(a - l), wc = l == -CUDART_INF_F ? 0.f : expf(c - l);
+    const int64_t off = ((int64_t)t * H + h) * D;
+    for (int d = lane * 8; d < D; d += 256) {
+      float x[8];
+      if (o_acc) {
+        const float4 u0 = *reinterpret_cast<const float4*>(o_acc + off + d);
+        const float4 u1 = *reinterpret_cast<const float4*>(o_acc + off + d + 4);
+        x[0] = u0.x; x[1] = u0.y; x[2] = u0.z; x[3] = u0.w; x[4] = u1.x; x[5] = u1.y; x[6] = u1.z; x[7] = u1.w;
+      } else {
+        const uint4 u = *reinterpret_cast<const uint4*>(o_run + off + d);
+        const __nv_bfloat162* pr = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float2 f = __bfloat1622float2(pr[j]);
+          x[2 * j] = f.x;
+          x[2 * j + 1] = f.y;
+        }
+      }
+      const uint4 un = *reinterpret_cast<const uint4*>(o_new + off + d);
+      const __nv_bfloat162* pn = reinterpret_cast<const __nv_bfloat162*>(&un);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float2 f = __bfloat1622float2(pn[j]);
+        x[2 * j] = wa * x[2 * j] + wc * f.x;
+        x[2 * j + 1] = wa * x[2 * j + 1] + wc * f.y;
+      }
+      if (o_acc) {
+        *reinterpret_cast<float4*>(o_acc + off + d) = make_float4(x[0], x[1], x[2], x[3]);
+        *reinterpret_cast<float4*>(o_acc + off + d + 4) = make_float4(x[4], x[5], x[6], x[7]);
+      }
+      if (o_run) {
+        uint4 r;
+        uint32_t* rp = reinterpret_cast<uint32_t*>(&r);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          __nv_bfloat162 v2 = __floats2bfloat162_rn(x[2 * j], x[2 * j + 1]);
+          rp[j] = *reinterpret_cast<uint32_t*>(&v2);
+        }
+        *reinterpret_cast<uint4*>(o_run + off + d) = r;
+      }
+    }
+    if (lane == 0) l_acc[(int64_t)h * T + t] = l;
+  }
+}
+
+// dst += src (bf16, added in fp32, rounded once) on the query rows of the
+// segments with keys; a warp per (row, head).
+__global__ void grad_add_live_kernel(__nv_bfloat16* dst, const __nv_bfloat16* src, const int32_t* cu_q,
+                                     const int32_t* cu_k, const int32_t* dev_meta, int nseg_cap, int T, int H, int D) {
+  const int nseg = dev_meta ? min(dev_meta[0], nseg_cap) : nseg_cap;
+  const int lane = threadIdx.x & 31;
+  const int64_t nw = (int64_t)gridDim.x * (blockDim.x / 32);
+  for (int64_t w = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) / 32; w < (int64_t)T * H; w += nw) {
+    const int t = (int)(w / H);
+    if (live_segment(cu_q, cu_k, nseg, t) < 0) continue;
+    const int64_t off = w * D;
+    for (int d = lane * 8; d < D; d += 256) {
+      const uint4 ua = *reinterpret_cast<const uint4*>(dst + off + d);
+      const uint4 ub = *reinterpret_cast<const uint4*>(src + off + d);
+      const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&ua);
+      const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&ub);
+      uint4 r;
+      uint32_t* rp = reinterpret_cast<uint32_t*>(&r);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float2 fa = __bfloat1622float2(pa[j]), fb = __bfloat1622float2(pb[j]);
+        __nv_bfloat162 v2 = __floats2bfloat162_rn(fa.x + fb.x, fa.y + fb.y);
+        rp[j] = *reinterpret_cast<uint32_t*>(&v2);
+      }
+      *reinterpret_cast<uint4*>(dst + off + d) = r;
+    }
+  }
+}
+
 // Forward preparation: block 0 builds the heaviest-first tile list while the
 // other blocks fill uncovered query rows, so the list's latency-bound build
 // overlaps the fill and costs no launch of its own.
@@ -586,6 +737,27 @@ cudaError_t launch_bwd_prep(const SegInfo& g, int G, int Hkv, int split_target, 
   bwd_prep_kernel<<<1 + fill, kScanThreads, 0, st>>>(g, G, Hkv, split_target, items, n_items, seg_prefix, item_cap,
                                                      status, dout, out, o_sb, o_ss, o_sh, delta, dq_acc, Hq, Dqk, Dv,
                                                      dk_acc, dv_acc, dk, dv, k_sb, k_ss, k_sh, v_sb, v_ss, v_sh);
+  return cudaGetLastError();
+}
+cudaError_t launch_cross_segments(const int32_t* ids, int B, int S, int q0, int Lq, int k0, int Lk, int32_t* cu_q,
+                                  int32_t* cu_k, int32_t* dev_meta, cudaStream_t st) {
+  cudaError_t e = cudaMemsetAsync(dev_meta, 0, 3 * sizeof(int32_t), st);
+  if (e != cudaSuccess) return e;
+  cross_segments_kernel<<<B, kScanThreads, 0, st>>>(ids, B, S, q0, Lq, k0, Lk, cu_q, cu_k, dev_meta);
+  return cudaGetLastError();
+}
+cudaError_t launch_lse_merge_live(float* o_acc, __nv_bfloat16* o_run, float* l_acc, const __nv_bfloat16* o_new,
+                                  const float* l_new, const int32_t* cu_q, const int32_t* cu_k, const int32_t* dev_meta,
+                                  int nseg, int T, int H, int D, cudaStream_t st) {
+  lse_merge_live_kernel<<<grid_for((int64_t)T * H * 32, 256), 256, 0, st>>>(o_acc, o_run, l_acc, o_new, l_new, cu_q,
+                                                                            cu_k, dev_meta, nseg, T, H, D);
+  return cudaGetLastError();
+}
+cudaError_t launch_grad_add_live(__nv_bfloat16* dst, const __nv_bfloat16* src, const int32_t* cu_q,
+                                 const int32_t* cu_k, const int32_t* dev_meta, int nseg, int T, int H, int D,
+                                 cudaStream_t st) {
+  grad_add_live_kernel<<<grid_for((int64_t)T * H * 32, 256), 256, 0, st>>>(dst, src, cu_q, cu_k, dev_meta, nseg, T,
+                                                                           H, D);
   return cudaGetLastError();
 }
 cudaError_t launch_bwd_convert(const float* dq_acc, __nv_bfloat16* dq, bool have_q, int B, int Sq, int Hq, int Dqk,

@@ -42,6 +42,18 @@ cudaError_t launch_pad_fixup(__nv_bfloat16* out, float* lse, const int32_t* qids
                              int64_t o_sb, int64_t o_ss, int64_t o_sh, int64_t l_sb, int64_t l_sh, cudaStream_t st);
 cudaError_t launch_lse_merge(const __nv_bfloat16* o1, const float* l1, const __nv_bfloat16* o2, const float* l2,
                              float* of, __nv_bfloat16* ob, float* l, int T, int H, int D, cudaStream_t st);
+// Cross-chunk segments (3 per row) of the shard [q0, q0 + Lq) against the
+// earlier key chunk [k0, k0 + Lk); dev_meta = {3 B, max_q, max_k}.
+cudaError_t launch_cross_segments(const int32_t* ids, int B, int S, int q0, int Lq, int k0, int Lk, int32_t* cu_q,
+                                  int32_t* cu_k, int32_t* dev_meta, cudaStream_t st);
+// Live-row merge and gradient add over the query rows of segments with keys
+// (segment count from dev_meta when given, capped at nseg).
+cudaError_t launch_lse_merge_live(float* o_acc, __nv_bfloat16* o_run, float* l_acc, const __nv_bfloat16* o_new,
+                                  const float* l_new, const int32_t* cu_q, const int32_t* cu_k, const int32_t* dev_meta,
+                                  int nseg, int T, int H, int D, cudaStream_t st);
+cudaError_t launch_grad_add_live(__nv_bfloat16* dst, const __nv_bfloat16* src, const int32_t* cu_q,
+                                 const int32_t* cu_k, const int32_t* dev_meta, int nseg, int T, int H, int D,
+                                 cudaStream_t st);
 // dQ = scale * dQacc (bf16, q's layout); with accumulators also dK = scale *
 // dKacc and dV = dVacc.
 cudaError_t launch_bwd_convert(const float* dq_acc, __nv_bfloat16* dq, bool have_q, int B, int Sq, int Hq, int Dqk,

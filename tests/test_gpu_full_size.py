@@ -5,11 +5,12 @@ rows one key at a time).
 
 Workload 5 also runs the cross-chunk decomposition of the cp_attention page on
 one GPU: the query shard 32768..65535 attends its own key chunk causally
-(through the builder) and the earlier key chunk non-causally (the document that
-straddles the chunk edge, as one segment between zero-query and zero-key
-segments); the two partial results are merged by lse, and each chunk's
-backward is fed the merged out/lse. The sum is compared with the oracle's
-unsplit document-causal result for that shard.
+(through the builder) and the earlier key chunk non-causally (through the
+cross-chunk builder: the document that straddles the chunk edge, as one segment
+between zero-query and zero-key segments); the cross result is merged into the
+local one on its live rows, each chunk's backward is fed the merged out/lse, and
+the cross chunk's dQ is added on its live rows. The result is compared with the
+oracle's unsplit document-causal result for that shard.
 """
 import numpy as np
 import pytest
@@ -105,26 +106,6 @@ def test_workload3_dense_d512_full_size():
         _check_grad_rows(grads[2][b].permute(1, 0, 2), dv_o, k_rows, "dv")
 
 
-def _cross_segments(ids_row, split, Lq):
-    """Segments of the non-causal cross chunk: queries [split, split + Lq) of the
-    row against keys [0, split); only the run that straddles the split shares a
-    document with both sides."""
-    a = split - 1
-    doc = ids_row[split]
-    if doc == 0 or ids_row[a] != doc:
-        return np.array([0, 0, Lq], np.int32), np.array([0, split, split], np.int32)
-    start = a
-    while start > 0 and ids_row[start - 1] == doc:
-        start -= 1
-    end = split
-    while end < split + Lq and ids_row[end] == doc:
-        end += 1
-    nq = end - split
-    cu_q = np.array([0, 0, nq, Lq], np.int32)
-    cu_k = np.array([0, start, split, split], np.int32)
-    return cu_q, cu_k
-
-
 def _cheap_key_rows(lengths, offset=0, per_doc=2):
     """Keys whose visible query sets are short (the last tokens of every
     document, all tokens of the shortest one), so the oracle's per-key dK/dV
@@ -187,24 +168,29 @@ def test_workload5_cross_chunk_merge():
     # local chunk: keys split..S, causal, through the builder
     ids_local = torch.from_numpy(np.ascontiguousarray(w.doc_ids[:, split:])).to(dev)
     out1, lse1, seg1 = psf.document_causal_attention(q, k[split:], v[split:], ids_local, ids_local, 0, w.scale)
-    # cross chunk: keys 0..split, non-causal, the straddling document only
-    cu_q2, cu_k2 = _cross_segments(ids_row, split, Lq)
-    cq2, ck2 = torch.from_numpy(cu_q2).to(dev), torch.from_numpy(cu_k2).to(dev)
-    mq2, mk2 = int(np.diff(cu_q2).max()), int(np.diff(cu_k2).max())
-    out2, lse2 = psf.attn_varlen_fwd(q, k[:split], v[:split], cq2, ck2, mq2, mk2, w.scale, False)
-    _, out_m, lse_m = psf.lse_merge(out1, lse1, out2, lse2, want_f32=False, want_bf16=True)
+    # cross chunk: keys 0..split, non-causal, through the cross-chunk builder
+    ids = torch.from_numpy(w.doc_ids).to(dev)
+    cq2, ck2, meta2 = psf.build_cross_segments(ids, split, Lq, 0, split)
+    cu_q2, cu_k2, mq2, mk2 = oracle.build_cross_segments(w.doc_ids, split, Lq, 0, split)
+    np.testing.assert_array_equal(cq2.cpu().numpy(), cu_q2)
+    np.testing.assert_array_equal(ck2.cpu().numpy(), cu_k2)
+    out2, lse2 = psf.attn_varlen_fwd(q, k[:split], v[:split], cq2, ck2, -1, -1, w.scale, False, dev_meta=meta2)
+    # the local result is the running one; merge the cross chunk in on its live rows
+    out_m, lse_m = out1.clone(), lse1.clone()
+    psf.lse_merge_live_rows(out_m, lse_m, out2, lse2, cq2, ck2, dev_meta=meta2)
     # each chunk's backward is fed the merged out/lse
     dq1, dk1, dv1 = psf.document_causal_attention_backward(do, q, k[split:], v[split:], out_m, lse_m, seg1,
                                                            w.scale)
-    dq2, dk2, dv2 = psf.attn_varlen_bwd(do, q, k[:split], v[:split], out_m, lse_m, cq2, ck2, mq2, mk2, w.scale,
-                                        False)
+    dq2, dk2, dv2 = psf.attn_varlen_bwd(do, q, k[:split], v[:split], out_m, lse_m, cq2, ck2, -1, -1, w.scale,
+                                        False, dev_meta=meta2)
+    dq = dq1.clone()
+    psf.grad_add_live_rows(dq, dq2, cq2, ck2, dev_meta=meta2)
     assert psf.device_status() == 0
-    dq = dq1.float() + dq2.float()
     dk = torch.cat([dk2, dk1])
     dv = torch.cat([dv2, dv1])
     # against the oracle's unsplit result for the shard, on sampled query rows
     # and on keys with short query sets
-    strad = int(cu_q2[2]) if len(cu_q2) == 4 else 0
+    strad = int(cu_q2[2])
     q_rows = _rows(Lq, 64, 5, must=[0, Lq - 1, strad - 1, strad])
     out_o, lse_o = oracle.attn_fwd_document(q_sh, w.k, w.v, w.doc_ids, split, w.scale, None, rows=q_rows)
     _check_fwd_rows(out_m, lse_m, out_o, lse_o, q_rows)
@@ -218,7 +204,6 @@ def test_workload5_cross_chunk_merge():
     _check_grad_rows(dk, dk_o, k_rows, "dk")
     _check_grad_rows(dv, dv_o, k_rows, "dv")
     # the decomposition as a whole against the unsplit path on every row
-    ids = torch.from_numpy(w.doc_ids).to(dev)
     qids = ids[:, split:].contiguous()
     out_u, lse_u, seg_u = psf.document_causal_attention(q, k, v, qids, ids, split, w.scale)
     gu = psf.document_causal_attention_backward(do, q, k, v, out_u, lse_u, seg_u, w.scale)

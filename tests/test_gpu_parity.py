@@ -11,7 +11,7 @@ import torch
 import oracle
 import packed_sequence_flash_gb300 as psf
 from packed_sequence_flash_gb300 import inputs
-from gpu_helpers import assert_fwd, assert_grads, cuda, doc_case
+from gpu_helpers import assert_fwd, assert_grads, cuda, doc_case, np64
 
 pytestmark = pytest.mark.gpu
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
@@ -199,3 +199,108 @@ def test_lse_merge_matches_oracle_and_neg_inf_rows():
     fin = np.isfinite(l_ref)
     assert np.max(np.abs(lg[fin] - l_ref[fin])) < 1e-5
     assert not np.isnan(of.cpu().numpy()).any()
+
+
+# ---------------------------------------------------------------- cross-chunk pieces
+
+def _build_cross_gpu(ids, q0, Lq, k0, Lk):
+    ids_t = torch.as_tensor(np.asarray(ids, np.int32)).to("cuda")
+    cu_q, cu_k, meta = psf.build_cross_segments(ids_t, q0, Lq, k0, Lk)
+    m = meta.cpu().tolist()
+    return cu_q.cpu().numpy(), cu_k.cpu().numpy(), m
+
+
+def test_cross_builder_golden_examples_bit_exact():
+    with open(os.path.join(GOLDEN, "cross_examples.json")) as fh:
+        cases = json.load(fh)["cases"]
+    for c in cases:
+        cu_q, cu_k, m = _build_cross_gpu(c["doc_ids"], c["q_start"], c["q_length"], c["k_start"], c["k_length"])
+        assert cu_q.tolist() == c["cu_q"] and cu_k.tolist() == c["cu_k"], c
+        assert m == [len(c["cu_q"]) - 1, c["max_q"], c["max_k"]], c
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_cross_builder_random_maps_bit_exact(seed):
+    r = np.random.default_rng(seed)
+    B = int(r.integers(1, 4))
+    S = int(r.integers(2, 40000))
+    ids = np.zeros((B, S), np.int32)
+    for b in range(B):
+        pos, d = 0, 1
+        while pos < S:
+            n = int(r.integers(1, 6000))
+            ids[b, pos:pos + n] = 0 if r.random() < 0.2 else d
+            d += 1
+            pos += n
+    q0 = int(r.integers(1, S))
+    Lq = int(r.integers(0, S - q0 + 1))
+    k0 = int(r.integers(0, q0))
+    Lk = int(r.integers(0, q0 - k0 + 1))
+    cu_q, cu_k, m = _build_cross_gpu(ids, q0, Lq, k0, Lk)
+    ref = oracle.build_cross_segments(ids, q0, Lq, k0, Lk)
+    np.testing.assert_array_equal(cu_q, ref[0])
+    np.testing.assert_array_equal(cu_k, ref[1])
+    assert m == [3 * B, ref[2], ref[3]]
+
+
+def test_cross_builder_rejects_chunk_after_shard():
+    ids = torch.ones(1, 16, dtype=torch.int32, device="cuda")
+    with pytest.raises(ValueError):
+        psf.build_cross_segments(ids, 4, 8, 2, 4)
+
+
+def _live_case(seed, H=3, D=64):
+    """30 segments with 0-59 query rows each; about a third have no keys."""
+    r = np.random.default_rng(seed)
+    nq = r.integers(0, 60, size=30)
+    cu_q = np.concatenate([[0], np.cumsum(nq)]).astype(np.int32)
+    nk = r.integers(0, 3, size=30) * r.integers(1, 50, size=30)
+    cu_k = np.concatenate([[0], np.cumsum(nk)]).astype(np.int32)
+    T = int(cu_q[-1])
+    o_run = inputs.randn_bf16((T, H, D), seed * 3 + 1)
+    o_new = inputs.randn_bf16((T, H, D), seed * 3 + 2)
+    l_acc = torch.from_numpy(r.standard_normal((H, T)).astype(np.float32))
+    l_new = torch.from_numpy(r.standard_normal((H, T)).astype(np.float32))
+    l_acc[:, : T // 10] = -np.inf
+    l_new[:, T // 20: T // 7] = -np.inf
+    return cu_q, cu_k, o_run, l_acc, o_new, l_new
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_lse_merge_live_rows_matches_oracle(seed):
+    cu_q, cu_k, o_run, l_acc, o_new, l_new = _live_case(seed)
+    o_ref, l_ref = oracle.lse_merge_live_rows(o_run, l_acc, o_new, l_new, cu_q, cu_k)
+    cq, ck = torch.from_numpy(cu_q).cuda(), torch.from_numpy(cu_k).cuda()
+    # running output held in bf16, merged in place
+    ob, lb = cuda(o_run).clone(), cuda(l_acc).clone()
+    psf.lse_merge_live_rows(ob, lb, cuda(o_new), cuda(l_new), cq, ck)
+    # running output held in fp32 (and mirrored to bf16)
+    of, lf, ob2 = cuda(o_run).float().clone(), cuda(l_acc).clone(), cuda(o_run).clone()
+    psf.lse_merge_live_rows(ob2, lf, cuda(o_new), cuda(l_new), cq, ck, o_acc=of)
+    assert psf.device_status() == 0
+    live = oracle.live_rows(cu_q, cu_k)
+    other = np.setdiff1d(np.arange(o_run.shape[0]), live)
+    for o, l in ((ob, lb), (of, lf), (ob2, lf)):
+        og, lg = np64(o), np64(l)
+        assert not np.isnan(og).any() and not np.isnan(lg).any()
+        assert np.max(np.abs(og - o_ref)) < 2e-2
+        assert np.array_equal(np.isneginf(lg), np.isneginf(l_ref))
+        fin = np.isfinite(l_ref)
+        assert np.max(np.abs(lg[fin] - l_ref[fin])) < 1e-5
+    # rows outside the live segments are untouched, bit for bit
+    np.testing.assert_array_equal(ob.cpu()[other].view(torch.int16).numpy(), o_run[other].view(torch.int16).numpy())
+    np.testing.assert_array_equal(np64(lb)[:, other], np64(l_acc)[:, other])
+    assert np.max(np.abs(np64(of) - o_ref)) < 1e-5
+
+
+def test_grad_add_live_rows_matches_oracle():
+    cu_q, cu_k, a, _, b, _ = _live_case(5, H=4, D=128)
+    ref = oracle.grad_add_live_rows(a, b, cu_q, cu_k)
+    dst = cuda(a).clone()
+    psf.grad_add_live_rows(dst, cuda(b), torch.from_numpy(cu_q).cuda(), torch.from_numpy(cu_k).cuda())
+    assert psf.device_status() == 0
+    got = np64(dst)
+    # one bf16 rounding of the fp32 sum
+    assert np.max(np.abs(got - ref) / np.maximum(np.abs(ref), 1e-3)) < 8e-3
+    other = np.setdiff1d(np.arange(a.shape[0]), oracle.live_rows(cu_q, cu_k))
+    np.testing.assert_array_equal(dst.cpu()[other].view(torch.int16).numpy(), a[other].view(torch.int16).numpy())
