@@ -270,6 +270,9 @@ def our_arm(args):
     lib = _lib.load()
 
     w = inputs.config(args.config, args.seed + rank)
+    if args.dtype == "fp16":
+        # the same draws held as fp16 (fp16 storage and fp16 tensor-core inputs)
+        w.q, w.k, w.v, w.dout = (t.to(torch.float16) for t in (w.q, w.k, w.v, w.dout))
     pairs, f_fwd, f_bwd = workload_flops(w)
     flops = f_fwd + f_bwd
     Lq = w.q.shape[0]
@@ -417,7 +420,7 @@ def our_arm(args):
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "impl": "ours",
+        "vs_baseline": None, "dtype": args.dtype, "data": "synthetic", "impl": "ours",
         "config": dict(config_dict(w, args, pairs, len(w.extra["lengths"])),
                        parallelism=f"replicas{world}" if world > 1 else "single GPU"),
         "fwd_tflops": f_fwd / (fwd_ms * 1e-3) / 1e12 if fwd_ms > 0 else None,
@@ -459,6 +462,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", type=int, default=2, help="workload number (2 = the headline workload)")
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--dtype", choices=["bf16", "fp16"], default="bf16",
+                    help="16-bit type of q, k, v, dO and the outputs (the headline is bf16)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -19,8 +19,8 @@
  *  - Kernel-side faults in the caller's data (bad segment arrays) and pipeline
  *    waits that ran out are recorded in a per-device status word that
  *    psf_device_status() returns after synchronising the device.
- *  - dtype: bf16 inputs and outputs (`out`, `dq`, `dk`, `dv`); lse and the
- *    row-dot Delta are fp32.
+ *  - dtype: bf16 or fp16 inputs and outputs (`out`, `dq`, `dk`, `dv`), chosen
+ *    per call by a PSF_DTYPE_* argument; lse and the row-dot Delta are fp32.
  *  - Head dims (Dqk, Dv) supported: (64,64), (128,128), (192,128), (512,512).
  *  - GQA: Hq % Hkv == 0; query head h uses KV head h / (Hq / Hkv).
  *  - Causal masks are aligned to the bottom-right corner of each segment
@@ -55,6 +55,15 @@ extern "C" {
 /* Tensor layouts accepted by the varlen calls. */
 #define PSF_LAYOUT_THD 0  /* packed [T, H, D]; lse [H, T]                                */
 #define PSF_LAYOUT_BHSD 1 /* batched [B, H, S, D]; lse [B, H, S]; rows are b * S + s     */
+
+/*
+ * Element type of the 16-bit tensors of a call (q, k, v, out, dout, dq, dk, dv,
+ * merge operands); one type per call. lse, Delta and every accumulator stay
+ * fp32.                     [ffpa_attention page, module docstring: the op
+ *                            takes bf16 and fp16 inputs]
+ */
+#define PSF_DTYPE_BF16 0
+#define PSF_DTYPE_F16 1
 
 /* Message for the last failing call on this thread (never NULL). */
 const char* psf_last_error(void);
@@ -113,7 +122,7 @@ size_t psf_attn_bwd_workspace_size(int64_t total_q_rows, int64_t total_k_rows, i
  */
 int psf_attn_varlen_fwd(const void* q, const void* k, const void* v, void* out, float* lse, const int32_t* cu_q,
                         const int32_t* cu_k, const int32_t* dev_meta, int nseg, int max_q, int max_k, int layout,
-                        int B, int Sq, int Sk, int Hq, int Hkv, int Dqk, int Dv, float scale, int causal,
+                        int dtype, int B, int Sq, int Sk, int Hq, int Hkv, int Dqk, int Dv, float scale, int causal,
                         int32_t window_left, void* workspace, size_t ws_bytes, void* stream);
 
 /*
@@ -141,8 +150,8 @@ int psf_attn_varlen_fwd(const void* q, const void* k, const void* v, void* out, 
 #define PSF_NOALLOC_MAX_SEGMENTS 65536
 int psf_attn_varlen_fwd_noalloc(const void* q, const void* k, const void* v, void* out, float* lse,
                                 const int32_t* cu_q, const int32_t* cu_k, const int32_t* dev_meta, int nseg,
-                                int max_q, int max_k, int layout, int B, int Sq, int Sk, int Hq, int Hkv, int Dqk,
-                                int Dv, float scale, int causal, int32_t window_left, void* stream);
+                                int max_q, int max_k, int layout, int dtype, int B, int Sq, int Sk, int Hq, int Hkv,
+                                int Dqk, int Dv, float scale, int causal, int32_t window_left, void* stream);
 
 /*
  * Varlen backward from caller-supplied out / lse.
@@ -159,8 +168,8 @@ int psf_attn_varlen_fwd_noalloc(const void* q, const void* k, const void* v, voi
  */
 int psf_attn_varlen_bwd(const void* dout, const void* q, const void* k, const void* v, const void* out,
                         const float* lse, void* dq, void* dk, void* dv, const int32_t* cu_q, const int32_t* cu_k,
-                        const int32_t* dev_meta, int nseg, int max_q, int max_k, int layout, int B, int Sq, int Sk,
-                        int Hq, int Hkv, int Dqk, int Dv, float scale, int causal, int32_t window_left,
+                        const int32_t* dev_meta, int nseg, int max_q, int max_k, int layout, int dtype, int B, int Sq,
+                        int Sk, int Hq, int Hkv, int Dqk, int Dv, float scale, int causal, int32_t window_left,
                         void* workspace, size_t ws_bytes, void* stream);
 
 /*
@@ -174,7 +183,7 @@ int psf_attn_varlen_bwd(const void* dout, const void* q, const void* k, const vo
  *  workspace: psf_attn_fwd_workspace_size(B * Nq, B) bytes.
  */
 int psf_attn_dense_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq, int Hkv,
-                       int Nq, int Nk, int Dqk, int Dv, float scale, int causal, int32_t window_left,
+                       int Nq, int Nk, int Dqk, int Dv, int dtype, float scale, int causal, int32_t window_left,
                        void* workspace, size_t ws_bytes, void* stream);
 
 /*
@@ -184,7 +193,7 @@ int psf_attn_dense_fwd(const void* q, const void* k, const void* v, void* out, f
  */
 int psf_attn_dense_bwd(const void* dout, const void* q, const void* k, const void* v, const void* out,
                        const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Nq, int Nk,
-                       int Dqk, int Dv, float scale, int causal, int32_t window_left, void* workspace,
+                       int Dqk, int Dv, int dtype, float scale, int causal, int32_t window_left, void* workspace,
                        size_t ws_bytes, void* stream);
 
 /*
@@ -225,12 +234,12 @@ int psf_pad_fixup(void* out, float* lse, const int32_t* q_doc_ids, int layout, i
  *                           [cp_attention page, "-inf-safe online-softmax merge"]
  *  l = logaddexp(l1, l2); o = o1 * exp(l1 - l) + o2 * exp(l2 - l), in fp32. A
  *  row with both inputs -inf gives o = 0, l = -inf (never NaN).
- *  o1, o2: bf16 [T, H, D]; l1, l2: fp32 [H, T] (PSF_LAYOUT_THD only).
- *  Outputs: o_f32 (nullable) fp32 [T,H,D], o_bf16 (nullable) bf16 [T,H,D],
+ *  o1, o2: dtype [T, H, D]; l1, l2: fp32 [H, T] (PSF_LAYOUT_THD only).
+ *  Outputs: o_f32 (nullable) fp32 [T,H,D], o_bf16 (nullable) dtype [T,H,D],
  *  l fp32 [H,T]. Outputs may alias neither input.
  */
 int psf_lse_merge(const void* o1, const float* l1, const void* o2, const float* l2, float* o_f32, void* o_bf16,
-                  float* l, int T, int H, int D, void* stream);
+                  float* l, int T, int H, int D, int dtype, void* stream);
 
 /*
  * Cross-chunk segments of a query shard against an earlier key chunk, on the
@@ -267,14 +276,14 @@ int psf_build_cross_segments(const int32_t* kv_doc_ids, int B, int S, int q_star
  *  Live rows: the query rows of segments (cu_q, cu_k) that have at least one
  *  key. On those rows l = logaddexp(l_acc, l_new) and o = o_run exp(l_acc - l)
  *  + o_new exp(l_new - l) (both -inf gives o = 0, l = -inf); other rows are not
- *  touched. Running output: o_acc fp32 [T, H, D] (nullable) and/or o_run bf16
+ *  touched. Running output: o_acc fp32 [T, H, D] (nullable) and/or o_run dtype
  *  [T, H, D] (nullable), read from o_acc when given, written to both; l_acc fp32
- *  [H, T] in place. o_new bf16 [T, H, D], l_new fp32 [H, T].
+ *  [H, T] in place. o_new dtype [T, H, D], l_new fp32 [H, T].
  *  Segments: nseg (or dev_meta[0], capped at nseg, when dev_meta is given).
  */
 int psf_lse_merge_live_rows(float* o_acc, void* o_run, float* l_acc, const void* o_new, const float* l_new,
                             const int32_t* cu_q, const int32_t* cu_k, const int32_t* dev_meta, int nseg, int T, int H,
-                            int D, void* stream);
+                            int D, int dtype, void* stream);
 
 /*
  * Add one key chunk's query gradient into the running one on the query rows
@@ -282,10 +291,10 @@ int psf_lse_merge_live_rows(float* o_acc, void* o_run, float* l_acc, const void*
  *                           [cp_attention page, the in-place grad scatter-add
  *                            of a chunk's packed gradient into the full one]
  *  dst += src on the live rows of (cu_q, cu_k) (as in psf_lse_merge_live_rows),
- *  bf16 [T, H, D] both, added in fp32 and rounded once; other rows untouched.
+ *  dtype [T, H, D] both, added in fp32 and rounded once; other rows untouched.
  */
 int psf_grad_add_live_rows(void* dst, const void* src, const int32_t* cu_q, const int32_t* cu_k,
-                           const int32_t* dev_meta, int nseg, int T, int H, int D, void* stream);
+                           const int32_t* dev_meta, int nseg, int T, int H, int D, int dtype, void* stream);
 
 #ifdef __cplusplus
 }

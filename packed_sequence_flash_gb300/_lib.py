@@ -31,22 +31,24 @@ SIGNATURES = {
     "psf_kernel_times_ms": (I, [I, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int)]),
     "psf_attn_fwd_workspace_size": (SZ, [I64, I]),
     "psf_attn_bwd_workspace_size": (SZ, [I64, I64, I, I, I, I, I]),
-    "psf_attn_varlen_fwd": (I, [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, I, I, F, I, I32, P, SZ, P]),
-    "psf_attn_varlen_fwd_noalloc": (I, [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, I, I, F, I, I32, P]),
-    "psf_attn_varlen_bwd": (I, [P, P, P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, I, I, F, I, I32,
+    "psf_attn_varlen_fwd": (I, [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, I, I, I, F, I, I32, P, SZ, P]),
+    "psf_attn_varlen_fwd_noalloc": (I, [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, I, I, I, F, I, I32, P]),
+    "psf_attn_varlen_bwd": (I, [P, P, P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, I, I, I, F, I, I32,
                                 P, SZ, P]),
-    "psf_attn_dense_fwd": (I, [P, P, P, P, P, I, I, I, I, I, I, I, F, I, I32, P, SZ, P]),
-    "psf_attn_dense_bwd": (I, [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, I, I32, P, SZ, P]),
+    "psf_attn_dense_fwd": (I, [P, P, P, P, P, I, I, I, I, I, I, I, I, F, I, I32, P, SZ, P]),
+    "psf_attn_dense_bwd": (I, [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, F, I, I32, P, SZ, P]),
     "psf_build_doc_segments": (I, [P, I, I, I, I, P, P, I, P, P, P]),
     "psf_pad_fixup": (I, [P, P, P, I, I, I, I, I, P]),
-    "psf_lse_merge": (I, [P, P, P, P, P, P, P, I, I, I, P]),
+    "psf_lse_merge": (I, [P, P, P, P, P, P, P, I, I, I, I, P]),
     "psf_build_cross_segments": (I, [P, I, I, I, I, I, I, P, P, P, P]),
-    "psf_lse_merge_live_rows": (I, [P, P, P, P, P, P, P, P, I, I, I, I, P]),
-    "psf_grad_add_live_rows": (I, [P, P, P, P, P, I, I, I, I, P]),
+    "psf_lse_merge_live_rows": (I, [P, P, P, P, P, P, P, P, I, I, I, I, I, P]),
+    "psf_grad_add_live_rows": (I, [P, P, P, P, P, I, I, I, I, I, P]),
 }
 
 PSF_LAYOUT_THD = 0
 PSF_LAYOUT_BHSD = 1
+PSF_DTYPE_BF16 = 0
+PSF_DTYPE_F16 = 1
 ERRORS = {-1: "PSF_EINVAL", -2: "PSF_EUNSUPPORTED", -3: "PSF_ECUDA", -4: "PSF_EDEVICE_ARGS",
           -5: "PSF_ETIMEOUT", -6: "PSF_EWORKSPACE"}
 

@@ -18,7 +18,7 @@ from __future__ import annotations
 import torch
 
 from . import _lib
-from ._lib import PSF_LAYOUT_BHSD, PSF_LAYOUT_THD, check
+from ._lib import PSF_DTYPE_BF16, PSF_DTYPE_F16, PSF_LAYOUT_BHSD, PSF_LAYOUT_THD, check
 
 NO_WINDOW = -(2 ** 31)  # the pages' "no window" sentinel
 
@@ -35,6 +35,19 @@ def _window(window) -> int:
     if window is None:
         return NO_WINDOW
     return int(window)
+
+
+_DTYPES = {torch.bfloat16: PSF_DTYPE_BF16, torch.float16: PSF_DTYPE_F16}
+
+
+def _dtype_code(tensors):
+    """PSF_DTYPE_* of a call's 16-bit tensors ((tensor, name) pairs), which must share one type."""
+    t0, n0 = tensors[0]
+    if t0.dtype not in _DTYPES:
+        raise ValueError(f"{n0} must be bfloat16 or float16, got {t0.dtype}")
+    for t, n in tensors:
+        _need(t, n, t0.dtype)
+    return _DTYPES[t0.dtype]
 
 
 def _need(t, name, dtype=None):
@@ -94,9 +107,9 @@ def _varlen_dims(q, k, v, layout):
 
 def attn_varlen_fwd(q, k, v, cu_q, cu_k, max_q, max_k, scale, causal, window=None, dev_meta=None,
                     layout="thd", out=None, lse=None, workspace=None):
-    """Packed varlen forward -> (out, lse). cu_q/cu_k int32 [nseg+1] on the device."""
-    for t, n in ((q, "q"), (k, "k"), (v, "v")):
-        _need(t, n, torch.bfloat16)
+    """Packed varlen forward -> (out, lse). cu_q/cu_k int32 [nseg+1] on the device.
+    q, k, v: bf16 or fp16 (one type); out has their type, lse is fp32."""
+    dt = _dtype_code([(q, "q"), (k, "k"), (v, "v")])
     _i32(cu_q, "cu_q")
     _i32(cu_k, "cu_k")
     lay, B, Sq, Sk, Hq, Hkv, Dqk, Dv = _varlen_dims(q, k, v, layout)
@@ -109,17 +122,16 @@ def attn_varlen_fwd(q, k, v, cu_q, cu_k, max_q, max_k, scale, causal, window=Non
         workspace = _workspace(fwd_workspace_size(B * Sq, nseg), q.device)
     rc = _lib.load().psf_attn_varlen_fwd(
         _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(cu_q), _ptr(cu_k), _ptr(dev_meta), nseg,
-        int(max_q), int(max_k), lay, B, Sq, Sk, Hq, Hkv, Dqk, Dv, float(scale), int(bool(causal)), _window(window),
-        _ptr(workspace), workspace.numel(), _stream())
+        int(max_q), int(max_k), lay, dt, B, Sq, Sk, Hq, Hkv, Dqk, Dv, float(scale), int(bool(causal)),
+        _window(window), _ptr(workspace), workspace.numel(), _stream())
     check(rc)
     return out, lse
 
 
 def attn_varlen_bwd(dout, q, k, v, out, lse, cu_q, cu_k, max_q, max_k, scale, causal, window=None,
                     dev_meta=None, layout="thd", workspace=None):
-    """Packed varlen backward from caller-supplied out/lse -> (dq, dk, dv)."""
-    for t, n in ((dout, "dout"), (q, "q"), (k, "k"), (v, "v"), (out, "out")):
-        _need(t, n, torch.bfloat16)
+    """Packed varlen backward from caller-supplied out/lse -> (dq, dk, dv) in the inputs' type."""
+    dt = _dtype_code([(dout, "dout"), (q, "q"), (k, "k"), (v, "v"), (out, "out")])
     _need(lse, "lse", torch.float32)
     _i32(cu_q, "cu_q")
     _i32(cu_k, "cu_k")
@@ -132,7 +144,7 @@ def attn_varlen_bwd(dout, q, k, v, out, lse, cu_q, cu_k, max_q, max_k, scale, ca
         workspace = _workspace(bwd_workspace_size(B * Sq, B * Sk, nseg, Hq, Hkv, Dqk, Dv), q.device)
     rc = _lib.load().psf_attn_varlen_bwd(
         _ptr(dout), _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(cu_q),
-        _ptr(cu_k), _ptr(dev_meta), nseg, int(max_q), int(max_k), lay, B, Sq, Sk, Hq, Hkv, Dqk, Dv, float(scale),
+        _ptr(cu_k), _ptr(dev_meta), nseg, int(max_q), int(max_k), lay, dt, B, Sq, Sk, Hq, Hkv, Dqk, Dv, float(scale),
         int(bool(causal)), _window(window), _ptr(workspace), workspace.numel(), _stream())
     check(rc)
     return dq, dk, dv
@@ -142,9 +154,8 @@ def attn_varlen_bwd(dout, q, k, v, out, lse, cu_q, cu_k, max_q, max_k, scale, ca
 # dense [B, H, N, D]
 
 def attn_dense_fwd(q, k, v, scale, causal, window=None, workspace=None):
-    """Dense forward -> (out [B,Hq,Nq,Dv], lse [B,Hq,Nq] fp32)."""
-    for t, n in ((q, "q"), (k, "k"), (v, "v")):
-        _need(t, n, torch.bfloat16)
+    """Dense forward -> (out [B,Hq,Nq,Dv] in the inputs' type, lse [B,Hq,Nq] fp32)."""
+    dt = _dtype_code([(q, "q"), (k, "k"), (v, "v")])
     B, Hq, Nq, Dqk = q.shape
     Hkv, Nk = k.shape[1], k.shape[2]
     Dv = v.shape[3]
@@ -153,7 +164,7 @@ def attn_dense_fwd(q, k, v, scale, causal, window=None, workspace=None):
     if workspace is None:
         workspace = _workspace(fwd_workspace_size(B * Nq, B), q.device)
     rc = _lib.load().psf_attn_dense_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, Nq, Nk, Dqk,
-                                        Dv, float(scale), int(bool(causal)), _window(window), _ptr(workspace),
+                                        Dv, dt, float(scale), int(bool(causal)), _window(window), _ptr(workspace),
                                         workspace.numel(), _stream())
     check(rc)
     return out, lse
@@ -161,8 +172,7 @@ def attn_dense_fwd(q, k, v, scale, causal, window=None, workspace=None):
 
 def attn_dense_bwd(dout, q, k, v, out, lse, scale, causal, window=None, workspace=None):
     """Dense backward -> (dq, dk, dv) in [B,H,N,D], dk/dv at Hkv heads."""
-    for t, n in ((dout, "dout"), (q, "q"), (k, "k"), (v, "v"), (out, "out")):
-        _need(t, n, torch.bfloat16)
+    dt = _dtype_code([(dout, "dout"), (q, "q"), (k, "k"), (v, "v"), (out, "out")])
     _need(lse, "lse", torch.float32)
     B, Hq, Nq, Dqk = q.shape
     Hkv, Nk = k.shape[1], k.shape[2]
@@ -171,7 +181,7 @@ def attn_dense_bwd(dout, q, k, v, out, lse, scale, causal, window=None, workspac
     if workspace is None:
         workspace = _workspace(bwd_workspace_size(B * Nq, B * Nk, B, Hq, Hkv, Dqk, Dv), q.device)
     rc = _lib.load().psf_attn_dense_bwd(_ptr(dout), _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dq),
-                                        _ptr(dk), _ptr(dv), B, Hq, Hkv, Nq, Nk, Dqk, Dv, float(scale),
+                                        _ptr(dk), _ptr(dv), B, Hq, Hkv, Nq, Nk, Dqk, Dv, dt, float(scale),
                                         int(bool(causal)), _window(window), _ptr(workspace), workspace.numel(),
                                         _stream())
     check(rc)
@@ -206,7 +216,7 @@ def build_doc_segments(kv_doc_ids, q_length, q_global_start, capacity=None, want
 
 def pad_fixup(out, lse, q_doc_ids, layout="thd"):
     """In place: rows with query doc id 0 get out = 0 and lse = -inf."""
-    _need(out, "out", torch.bfloat16)
+    _dtype_code([(out, "out")])
     _need(lse, "lse", torch.float32)
     _i32(q_doc_ids, "q_doc_ids")
     if layout == "thd":
@@ -222,16 +232,15 @@ def pad_fixup(out, lse, q_doc_ids, layout="thd"):
 
 def lse_merge(o1, l1, o2, l2, want_f32=True, want_bf16=False):
     """Merge two partial results over disjoint keys: o [T,H,D] bf16, l [H,T] fp32."""
-    for t, n in ((o1, "o1"), (o2, "o2")):
-        _need(t, n, torch.bfloat16)
+    dt = _dtype_code([(o1, "o1"), (o2, "o2")])
     for t, n in ((l1, "l1"), (l2, "l2")):
         _need(t, n, torch.float32)
     T, H, D = o1.shape
     of = torch.empty(T, H, D, dtype=torch.float32, device=o1.device) if want_f32 else None
-    ob = torch.empty(T, H, D, dtype=torch.bfloat16, device=o1.device) if want_bf16 else None
+    ob = torch.empty(T, H, D, dtype=o1.dtype, device=o1.device) if want_bf16 else None
     l = torch.empty(H, T, dtype=torch.float32, device=o1.device)
     rc = _lib.load().psf_lse_merge(_ptr(o1), _ptr(l1), _ptr(o2), _ptr(l2), _ptr(of), _ptr(ob), _ptr(l), T, H, D,
-                                   _stream())
+                                   dt, _stream())
     check(rc)
     return of, ob, l
 
@@ -259,27 +268,24 @@ def lse_merge_live_rows(o_run, l_acc, o_new, l_new, cu_q, cu_k, dev_meta=None, o
     """In place: merge (o_new, l_new) into the running (o_run / o_acc, l_acc) on
     the query rows of the segments that have keys. o_run bf16 [T,H,D] (may be
     None when o_acc, fp32 [T,H,D], holds the running output), l_acc fp32 [H,T]."""
-    _need(o_new, "o_new", torch.bfloat16)
+    dt = _dtype_code([(o_new, "o_new")] + ([(o_run, "o_run")] if o_run is not None else []))
     for t, n in ((l_acc, "l_acc"), (l_new, "l_new")):
         _need(t, n, torch.float32)
-    if o_run is not None:
-        _need(o_run, "o_run", torch.bfloat16)
     if o_acc is not None:
         _need(o_acc, "o_acc", torch.float32)
     T, H, D = o_new.shape
     rc = _lib.load().psf_lse_merge_live_rows(_ptr(o_acc), _ptr(o_run), _ptr(l_acc), _ptr(o_new), _ptr(l_new),
-                                             _ptr(cu_q), _ptr(cu_k), _ptr(dev_meta), cu_q.numel() - 1, T, H, D,
+                                             _ptr(cu_q), _ptr(cu_k), _ptr(dev_meta), cu_q.numel() - 1, T, H, D, dt,
                                              _stream())
     check(rc)
 
 
 def grad_add_live_rows(dst, src, cu_q, cu_k, dev_meta=None):
     """In place: dst += src (bf16 [T,H,D]) on the query rows of the segments that have keys."""
-    _need(dst, "dst", torch.bfloat16)
-    _need(src, "src", torch.bfloat16)
+    dt = _dtype_code([(dst, "dst"), (src, "src")])
     T, H, D = dst.shape
     rc = _lib.load().psf_grad_add_live_rows(_ptr(dst), _ptr(src), _ptr(cu_q), _ptr(cu_k), _ptr(dev_meta),
-                                            cu_q.numel() - 1, T, H, D, _stream())
+                                            cu_q.numel() - 1, T, H, D, dt, _stream())
     check(rc)
 
 

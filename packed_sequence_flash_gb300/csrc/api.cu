@@ -224,19 +224,27 @@ int check_common(int layout, int B, int Sq, int Sk, int Hq, int Hkv, int Dqk, in
   return PSF_OK;
 }
 
-int make_bf16_map(CUtensorMap* m, const void* base, int D, int S, int H, int B, const View& v, int box_d) {
-  int rc = make_tmap_4d(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, D, S, H, B, v.ss, v.sh, v.sb, box_d, kBM,
-                        CU_TENSOR_MAP_SWIZZLE_128B);
+int check_dtype(int dtype) {
+  if (dtype != PSF_DTYPE_BF16 && dtype != PSF_DTYPE_F16) return fail(PSF_EINVAL, "unknown dtype %d", dtype);
+  return PSF_OK;
+}
+
+// TMA view of a 16-bit (bf16 or fp16) tensor.
+int make_map16(CUtensorMap* m, const void* base, int D, int S, int H, int B, const View& v, int box_d, int dtype) {
+  int rc = make_tmap_4d(m, dtype == PSF_DTYPE_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                        2, base, D, S, H, B, v.ss, v.sh, v.sb, box_d, kBM, CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc) return fail(PSF_ECUDA, "cuTensorMapEncodeTiled failed (%d) for a [%d,%d,%d,%d] view", rc, B, H, S, D);
   return PSF_OK;
 }
 
 int attn_fwd_impl(const void* q, const void* k, const void* v, void* out, float* lse, const int32_t* cu_q,
-                  const int32_t* cu_k, const int32_t* dev_meta, int nseg, int max_q, int max_k, int layout, int B,
+                  const int32_t* cu_k, const int32_t* dev_meta, int nseg, int max_q, int max_k, int layout, int dtype,
+                  int B,
                   int Sq, int Sk, int Hq, int Hkv, int Dqk, int Dv, float scale, int causal, int32_t window, void* ws,
                   size_t ws_bytes, void* stream) {
   int rc = check_common(layout, B, Sq, Sk, Hq, Hkv, Dqk, Dv, scale, window, nseg);
   if (rc) return rc;
+  if ((rc = check_dtype(dtype))) return rc;
   const int64_t q_rows = (int64_t)B * Sq, k_rows = (int64_t)B * Sk;
   if (q_rows == 0) return PSF_OK;
   if (!q || !out || !lse || (k_rows > 0 && (!k || !v))) return fail(PSF_EINVAL, "null tensor pointer");
@@ -256,18 +264,18 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, void* out, float*
   const View vv = tensor_view(layout, Sk, Hkv, Dv), vo = tensor_view(layout, Sq, Hq, Dv);
   const View vl = lse_view(layout, Sq, Hq);
   cudaError_t e = launch_fwd_prep(g, w.items, w.n_items, w.seg_prefix, w.item_cap, dev->status,
-                                  static_cast<__nv_bfloat16*>(out), vo.sb, vo.ss, vo.sh, lse, vl.sb, vl.sh, Hq, Dv, st);
+                                  out, vo.sb, vo.ss, vo.sh, lse, vl.sb, vl.sh, Hq, Dv, st);
   if (e != cudaSuccess) return cuda_fail(e, "forward preparation launch");
 
   FwdParams p;
   memset(&p, 0, sizeof(p));
-  if ((rc = make_bf16_map(&p.tm_q, q, Dqk, Sq, Hq, B, vq, 64))) return rc;
+  if ((rc = make_map16(&p.tm_q, q, Dqk, Sq, Hq, B, vq, 64, dtype))) return rc;
   if (k_rows > 0) {
-    if ((rc = make_bf16_map(&p.tm_k, k, Dqk, Sk, Hkv, B, vk, 64))) return rc;
-    if ((rc = make_bf16_map(&p.tm_v, v, Dv, Sk, Hkv, B, vv, 64))) return rc;
+    if ((rc = make_map16(&p.tm_k, k, Dqk, Sk, Hkv, B, vk, 64, dtype))) return rc;
+    if ((rc = make_map16(&p.tm_v, v, Dv, Sk, Hkv, B, vv, 64, dtype))) return rc;
   }
   p.seg = g;
-  p.out = static_cast<__nv_bfloat16*>(out);
+  p.out = out;
   p.o_sb = vo.sb;
   p.o_ss = vo.ss;
   p.o_sh = vo.sh;
@@ -286,7 +294,7 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, void* out, float*
   const int64_t max_work = (int64_t)w.item_cap * Hq * p.dv_parts;
   TimedLaunch tl;
   const bool timed = timing_begin(0, st, &tl);
-  e = launch_fwd(p, Dqk, Dv / p.dv_parts, dev->sms, max_work, st);
+  e = launch_fwd(p, Dqk, Dv / p.dv_parts, dev->sms, max_work, dtype == PSF_DTYPE_F16, st);
   if (timed) timing_end(&tl, st);
   if (e != cudaSuccess) return cuda_fail(e, "forward launch");
   return PSF_OK;
@@ -294,10 +302,12 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, void* out, float*
 
 int attn_bwd_impl(const void* dout, const void* q, const void* k, const void* v, const void* out, const float* lse,
                   void* dq, void* dk, void* dv, const int32_t* cu_q, const int32_t* cu_k, const int32_t* dev_meta,
-                  int nseg, int max_q, int max_k, int layout, int B, int Sq, int Sk, int Hq, int Hkv, int Dqk, int Dv,
-                  float scale, int causal, int32_t window, void* ws, size_t ws_bytes, void* stream) {
+                  int nseg, int max_q, int max_k, int layout, int dtype, int B, int Sq, int Sk, int Hq, int Hkv,
+                  int Dqk, int Dv, float scale, int causal, int32_t window, void* ws, size_t ws_bytes, void* stream) {
   int rc = check_common(layout, B, Sq, Sk, Hq, Hkv, Dqk, Dv, scale, window, nseg);
   if (rc) return rc;
+  if ((rc = check_dtype(dtype))) return rc;
+  const int f16 = dtype == PSF_DTYPE_F16;
   if (bwd_smem_bytes(Dqk, Dv) < 0)
     return fail(PSF_EUNSUPPORTED, "backward for (Dqk=%d, Dv=%d) is not built", Dqk, Dv);
   const int64_t q_rows = (int64_t)B * Sq, k_rows = (int64_t)B * Sk;
@@ -328,17 +338,17 @@ int attn_bwd_impl(const void* dout, const void* q, const void* k, const void* v,
   const View vl = lse_view(layout, Sq, Hq);
   cudaError_t e = launch_bwd_prep(
       g, Hq / Hkv, Hkv, accumulate ? kSplitPerSm * dev->sms : 0, w.items, w.n_items, w.seg_prefix, w.item_cap,
-      dev->status, static_cast<const __nv_bfloat16*>(dout), static_cast<const __nv_bfloat16*>(out), vo.sb, vo.ss,
+      dev->status, dout, out, vo.sb, vo.ss,
       vo.sh, w.delta, w.dq_acc, Hq, Dqk, Dv, accumulate ? w.dk_acc : nullptr, accumulate ? w.dv_acc : nullptr,
-      static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(dv), vk.sb, vk.ss, vk.sh, vv.sb, vv.ss, vv.sh, st);
+      dk, dv, vk.sb, vk.ss, vk.sh, vv.sb, vv.ss, vv.sh, f16, st);
   if (e != cudaSuccess) return cuda_fail(e, "backward preparation launch");
 
   if (k_rows > 0) {
     BwdParams p;
     memset(&p, 0, sizeof(p));
     if (q_rows > 0) {
-      if ((rc = make_bf16_map(&p.tm_q, q, Dqk, Sq, Hq, B, vq, 64))) return rc;
-      if ((rc = make_bf16_map(&p.tm_do, dout, Dv, Sq, Hq, B, vo, 64))) return rc;
+      if ((rc = make_map16(&p.tm_q, q, Dqk, Sq, Hq, B, vq, 64, dtype))) return rc;
+      if ((rc = make_map16(&p.tm_do, dout, Dv, Sq, Hq, B, vo, 64, dtype))) return rc;
       int r2 = make_tmap_4d(&p.tm_dq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, w.dq_acc, Dqk, Sq, Hq, B, (int64_t)Hq * Dqk,
                             Dqk, (int64_t)Sq * Hq * Dqk, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B);
       if (r2) return fail(PSF_ECUDA, "cuTensorMapEncodeTiled failed (%d) for the dQ accumulator", r2);
@@ -350,19 +360,19 @@ int attn_bwd_impl(const void* dout, const void* q, const void* k, const void* v,
                          Dv, (int64_t)Sk * Hkv * Dv, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B);
       if (r2) return fail(PSF_ECUDA, "cuTensorMapEncodeTiled failed for the dK/dV accumulators");
     }
-    if ((rc = make_bf16_map(&p.tm_k, k, Dqk, Sk, Hkv, B, vk, 64))) return rc;
-    if ((rc = make_bf16_map(&p.tm_v, v, Dv, Sk, Hkv, B, vv, 64))) return rc;
+    if ((rc = make_map16(&p.tm_k, k, Dqk, Sk, Hkv, B, vk, 64, dtype))) return rc;
+    if ((rc = make_map16(&p.tm_v, v, Dv, Sk, Hkv, B, vv, 64, dtype))) return rc;
     p.seg = g;
     p.lse = lse;
     p.l_sb = vl.sb;
     p.l_sh = vl.sh;
     p.delta = w.delta;
     p.q_rows = (int)q_rows;
-    p.dk = static_cast<__nv_bfloat16*>(dk);
+    p.dk = dk;
     p.k_sb = vk.sb;
     p.k_ss = vk.ss;
     p.k_sh = vk.sh;
-    p.dv = static_cast<__nv_bfloat16*>(dv);
+    p.dv = dv;
     p.v_sb = vv.sb;
     p.v_ss = vv.ss;
     p.v_sh = vv.sh;
@@ -377,14 +387,13 @@ int attn_bwd_impl(const void* dout, const void* q, const void* k, const void* v,
     p.limit_ns = g_wait_limit_ns;
     TimedLaunch tl;
     const bool timed = timing_begin(1, st, &tl);
-    e = launch_bwd(p, Dqk, Dv, dev->sms, w.item_cap, st);
+    e = launch_bwd(p, Dqk, Dv, dev->sms, w.item_cap, f16, st);
     if (timed) timing_end(&tl, st);
     if (e != cudaSuccess) return cuda_fail(e, "backward launch");
   }
-  e = launch_bwd_convert(w.dq_acc, static_cast<__nv_bfloat16*>(dq), q_rows > 0, B, Sq, Hq, Dqk, vq.sb, vq.ss, vq.sh,
-                         accumulate ? w.dk_acc : nullptr, static_cast<__nv_bfloat16*>(dk),
-                         accumulate ? w.dv_acc : nullptr, static_cast<__nv_bfloat16*>(dv), Sk, Hkv, Dv, vk.sb, vk.ss,
-                         vk.sh, vv.sb, vv.ss, vv.sh, scale, st);
+  e = launch_bwd_convert(w.dq_acc, dq, q_rows > 0, B, Sq, Hq, Dqk, vq.sb, vq.ss, vq.sh, accumulate ? w.dk_acc : nullptr,
+                         dk, accumulate ? w.dv_acc : nullptr, dv, Sk, Hkv, Dv, vk.sb, vk.ss, vk.sh, vv.sb, vv.ss,
+                         vv.sh, scale, f16, st);
   if (e != cudaSuccess) return cuda_fail(e, "convert launch");
   return PSF_OK;
 }
@@ -486,17 +495,17 @@ size_t psf_attn_bwd_workspace_size(int64_t total_q_rows, int64_t total_k_rows, i
 
 int psf_attn_varlen_fwd(const void* q, const void* k, const void* v, void* out, float* lse, const int32_t* cu_q,
                         const int32_t* cu_k, const int32_t* dev_meta, int nseg, int max_q, int max_k, int layout,
-                        int B, int Sq, int Sk, int Hq, int Hkv, int Dqk, int Dv, float scale, int causal,
+                        int dtype, int B, int Sq, int Sk, int Hq, int Hkv, int Dqk, int Dv, float scale, int causal,
                         int32_t window_left, void* workspace, size_t ws_bytes, void* stream) {
   if (!cu_q || !cu_k) return fail(PSF_EINVAL, "varlen calls need cu_q and cu_k");
-  return attn_fwd_impl(q, k, v, out, lse, cu_q, cu_k, dev_meta, nseg, max_q, max_k, layout, B, Sq, Sk, Hq, Hkv, Dqk,
-                       Dv, scale, causal, window_left, workspace, ws_bytes, stream);
+  return attn_fwd_impl(q, k, v, out, lse, cu_q, cu_k, dev_meta, nseg, max_q, max_k, layout, dtype, B, Sq, Sk, Hq, Hkv,
+                       Dqk, Dv, scale, causal, window_left, workspace, ws_bytes, stream);
 }
 
 int psf_attn_varlen_fwd_noalloc(const void* q, const void* k, const void* v, void* out, float* lse,
                                 const int32_t* cu_q, const int32_t* cu_k, const int32_t* dev_meta, int nseg,
-                                int max_q, int max_k, int layout, int B, int Sq, int Sk, int Hq, int Hkv, int Dqk,
-                                int Dv, float scale, int causal, int32_t window_left, void* stream) {
+                                int max_q, int max_k, int layout, int dtype, int B, int Sq, int Sk, int Hq, int Hkv,
+                                int Dqk, int Dv, float scale, int causal, int32_t window_left, void* stream) {
   if (!cu_q || !cu_k) return fail(PSF_EINVAL, "varlen calls need cu_q and cu_k");
   if (B < 1 || Sq < 0 || nseg < 0) return fail(PSF_EINVAL, "bad sizes B=%d Sq=%d nseg=%d", B, Sq, nseg);
   if ((int64_t)B * Sq > PSF_NOALLOC_MAX_Q_ROWS)
@@ -508,33 +517,33 @@ int psf_attn_varlen_fwd_noalloc(const void* q, const void* k, const void* v, voi
   void* scratch = nullptr;
   int rc = noalloc_scratch(&scratch);
   if (rc) return rc;
-  return attn_fwd_impl(q, k, v, out, lse, cu_q, cu_k, dev_meta, nseg, max_q, max_k, layout, B, Sq, Sk, Hq, Hkv, Dqk,
-                       Dv, scale, causal, window_left, scratch, kNoAllocScratchBytes, stream);
+  return attn_fwd_impl(q, k, v, out, lse, cu_q, cu_k, dev_meta, nseg, max_q, max_k, layout, dtype, B, Sq, Sk, Hq, Hkv,
+                       Dqk, Dv, scale, causal, window_left, scratch, kNoAllocScratchBytes, stream);
 }
 
 int psf_attn_varlen_bwd(const void* dout, const void* q, const void* k, const void* v, const void* out,
                         const float* lse, void* dq, void* dk, void* dv, const int32_t* cu_q, const int32_t* cu_k,
-                        const int32_t* dev_meta, int nseg, int max_q, int max_k, int layout, int B, int Sq, int Sk,
-                        int Hq, int Hkv, int Dqk, int Dv, float scale, int causal, int32_t window_left,
+                        const int32_t* dev_meta, int nseg, int max_q, int max_k, int layout, int dtype, int B, int Sq,
+                        int Sk, int Hq, int Hkv, int Dqk, int Dv, float scale, int causal, int32_t window_left,
                         void* workspace, size_t ws_bytes, void* stream) {
   if (!cu_q || !cu_k) return fail(PSF_EINVAL, "varlen calls need cu_q and cu_k");
-  return attn_bwd_impl(dout, q, k, v, out, lse, dq, dk, dv, cu_q, cu_k, dev_meta, nseg, max_q, max_k, layout, B, Sq,
-                       Sk, Hq, Hkv, Dqk, Dv, scale, causal, window_left, workspace, ws_bytes, stream);
+  return attn_bwd_impl(dout, q, k, v, out, lse, dq, dk, dv, cu_q, cu_k, dev_meta, nseg, max_q, max_k, layout, dtype, B,
+                       Sq, Sk, Hq, Hkv, Dqk, Dv, scale, causal, window_left, workspace, ws_bytes, stream);
 }
 
 int psf_attn_dense_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq, int Hkv,
-                       int Nq, int Nk, int Dqk, int Dv, float scale, int causal, int32_t window_left,
+                       int Nq, int Nk, int Dqk, int Dv, int dtype, float scale, int causal, int32_t window_left,
                        void* workspace, size_t ws_bytes, void* stream) {
-  return attn_fwd_impl(q, k, v, out, lse, nullptr, nullptr, nullptr, B, Nq, Nk, PSF_LAYOUT_BHSD, B, Nq, Nk, Hq, Hkv,
-                       Dqk, Dv, scale, causal, window_left, workspace, ws_bytes, stream);
+  return attn_fwd_impl(q, k, v, out, lse, nullptr, nullptr, nullptr, B, Nq, Nk, PSF_LAYOUT_BHSD, dtype, B, Nq, Nk, Hq,
+                       Hkv, Dqk, Dv, scale, causal, window_left, workspace, ws_bytes, stream);
 }
 
 int psf_attn_dense_bwd(const void* dout, const void* q, const void* k, const void* v, const void* out,
                        const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Nq, int Nk,
-                       int Dqk, int Dv, float scale, int causal, int32_t window_left, void* workspace,
+                       int Dqk, int Dv, int dtype, float scale, int causal, int32_t window_left, void* workspace,
                        size_t ws_bytes, void* stream) {
-  return attn_bwd_impl(dout, q, k, v, out, lse, dq, dk, dv, nullptr, nullptr, nullptr, B, Nq, Nk, PSF_LAYOUT_BHSD, B,
-                       Nq, Nk, Hq, Hkv, Dqk, Dv, scale, causal, window_left, workspace, ws_bytes, stream);
+  return attn_bwd_impl(dout, q, k, v, out, lse, dq, dk, dv, nullptr, nullptr, nullptr, B, Nq, Nk, PSF_LAYOUT_BHSD,
+                       dtype, B, Nq, Nk, Hq, Hkv, Dqk, Dv, scale, causal, window_left, workspace, ws_bytes, stream);
 }
 
 int psf_build_doc_segments(const int32_t* kv_doc_ids, int B, int Sk, int q_length, int q_global_start,
@@ -564,14 +573,15 @@ int psf_pad_fixup(void* out, float* lse, const int32_t* q_doc_ids, int layout, i
   int rc = device_info(&dev);
   if (rc) return rc;
   const View vo = tensor_view(layout, Lq, Hq, Dv), vl = lse_view(layout, Lq, Hq);
-  cudaError_t e = launch_pad_fixup(static_cast<__nv_bfloat16*>(out), lse, q_doc_ids, B, Lq, Hq, Dv, vo.sb, vo.ss,
+  cudaError_t e = launch_pad_fixup(out, lse, q_doc_ids, B, Lq, Hq, Dv, vo.sb, vo.ss,
                                    vo.sh, vl.sb, vl.sh, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PSF_OK : cuda_fail(e, "pad fixup launch");
 }
 
 int psf_lse_merge(const void* o1, const float* l1, const void* o2, const float* l2, float* o_f32, void* o_bf16,
-                  float* l, int T, int H, int D, void* stream) {
+                  float* l, int T, int H, int D, int dtype, void* stream) {
   if (T < 0 || H < 1 || D < 8 || D % 8) return fail(PSF_EINVAL, "bad sizes");
+  if (int rc0 = check_dtype(dtype)) return rc0;
   if (T == 0) return PSF_OK;
   if (!o1 || !o2 || !l1 || !l2 || !l || (!o_f32 && !o_bf16)) return fail(PSF_EINVAL, "null pointer");
   if (!aligned16(o1) || !aligned16(o2) || (o_f32 && !aligned16(o_f32)) || (o_bf16 && !aligned16(o_bf16)))
@@ -579,8 +589,7 @@ int psf_lse_merge(const void* o1, const float* l1, const void* o2, const float* 
   DeviceInfo* dev = nullptr;
   int rc = device_info(&dev);
   if (rc) return rc;
-  cudaError_t e = launch_lse_merge(static_cast<const __nv_bfloat16*>(o1), l1, static_cast<const __nv_bfloat16*>(o2),
-                                   l2, o_f32, static_cast<__nv_bfloat16*>(o_bf16), l, T, H, D,
+  cudaError_t e = launch_lse_merge(o1, l1, o2, l2, o_f32, o_bf16, l, T, H, D, dtype == PSF_DTYPE_F16,
                                    static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PSF_OK : cuda_fail(e, "merge launch");
 }
@@ -602,8 +611,9 @@ int psf_build_cross_segments(const int32_t* kv_doc_ids, int B, int S, int q_star
 
 int psf_lse_merge_live_rows(float* o_acc, void* o_run, float* l_acc, const void* o_new, const float* l_new,
                             const int32_t* cu_q, const int32_t* cu_k, const int32_t* dev_meta, int nseg, int T, int H,
-                            int D, void* stream) {
+                            int D, int dtype, void* stream) {
   if (T < 0 || H < 1 || D < 8 || D % 8 || nseg < 0) return fail(PSF_EINVAL, "bad sizes");
+  if (int rc0 = check_dtype(dtype)) return rc0;
   if (T == 0 || nseg == 0) return PSF_OK;
   if ((!o_acc && !o_run) || !l_acc || !o_new || !l_new || !cu_q || !cu_k) return fail(PSF_EINVAL, "null pointer");
   if ((o_acc && !aligned16(o_acc)) || (o_run && !aligned16(o_run)) || !aligned16(o_new))
@@ -611,23 +621,23 @@ int psf_lse_merge_live_rows(float* o_acc, void* o_run, float* l_acc, const void*
   DeviceInfo* dev = nullptr;
   int rc = device_info(&dev);
   if (rc) return rc;
-  cudaError_t e = launch_lse_merge_live(o_acc, static_cast<__nv_bfloat16*>(o_run), l_acc,
-                                        static_cast<const __nv_bfloat16*>(o_new), l_new, cu_q, cu_k, dev_meta, nseg, T,
-                                        H, D, static_cast<cudaStream_t>(stream));
+  cudaError_t e = launch_lse_merge_live(o_acc, o_run, l_acc, o_new, l_new, cu_q, cu_k, dev_meta, nseg, T, H, D,
+                                        dtype == PSF_DTYPE_F16, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PSF_OK : cuda_fail(e, "live-row merge launch");
 }
 
 int psf_grad_add_live_rows(void* dst, const void* src, const int32_t* cu_q, const int32_t* cu_k,
-                           const int32_t* dev_meta, int nseg, int T, int H, int D, void* stream) {
+                           const int32_t* dev_meta, int nseg, int T, int H, int D, int dtype, void* stream) {
   if (T < 0 || H < 1 || D < 8 || D % 8 || nseg < 0) return fail(PSF_EINVAL, "bad sizes");
+  if (int rc0 = check_dtype(dtype)) return rc0;
   if (T == 0 || nseg == 0) return PSF_OK;
   if (!dst || !src || !cu_q || !cu_k) return fail(PSF_EINVAL, "null pointer");
   if (!aligned16(dst) || !aligned16(src)) return fail(PSF_EINVAL, "unaligned pointer");
   DeviceInfo* dev = nullptr;
   int rc = device_info(&dev);
   if (rc) return rc;
-  cudaError_t e = launch_grad_add_live(static_cast<__nv_bfloat16*>(dst), static_cast<const __nv_bfloat16*>(src), cu_q,
-                                       cu_k, dev_meta, nseg, T, H, D, static_cast<cudaStream_t>(stream));
+  cudaError_t e = launch_grad_add_live(dst, src, cu_q, cu_k, dev_meta, nseg, T, H, D, dtype == PSF_DTYPE_F16,
+                                       static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PSF_OK : cuda_fail(e, "live-row gradient add launch");
 }
 

@@ -257,7 +257,7 @@ __device__ void bwd_schedule_body(SegInfo g, int G, int Hkv, int split_target,
 }
 
 // out = 0, lse = -inf for query rows at or past cu_q[nseg]; blocks bid of nblk.
-__device__ void fwd_tail_body(SegInfo g, __nv_bfloat16* out, int64_t o_sb, int64_t o_ss, int64_t o_sh, float* lse,
+__device__ void fwd_tail_body(SegInfo g, uint16_t* out, int64_t o_sb, int64_t o_ss, int64_t o_sh, float* lse,
                               int64_t l_sb, int64_t l_sh, int Hq, int Dv, int bid, int nblk) {
   const int nseg = seg_count(g);
   const int first = cu_q_at(g, nseg);
@@ -346,7 +346,7 @@ __global__ void __launch_bounds__(kScanThreads) build_segments_kernel(const int3
 
 // One warp per query row: a padding row (id 0) gets out = 0 on every head and
 // lse = -inf; other rows cost one id read.
-__global__ void pad_fixup_kernel(__nv_bfloat16* out, float* lse, const int32_t* qids, int B, int Lq, int Hq, int Dv,
+__global__ void pad_fixup_kernel(uint16_t* out, float* lse, const int32_t* qids, int B, int Lq, int Hq, int Dv,
                                  int64_t o_sb, int64_t o_ss, int64_t o_sh, int64_t l_sb, int64_t l_sh) {
   const int lane = threadIdx.x & 31;
   const int64_t rows = (int64_t)B * Lq;
@@ -363,8 +363,9 @@ __global__ void pad_fixup_kernel(__nv_bfloat16* out, float* lse, const int32_t* 
   }
 }
 
-__global__ void lse_merge_kernel(const __nv_bfloat16* o1, const float* l1, const __nv_bfloat16* o2, const float* l2,
-                                 float* of, __nv_bfloat16* ob, float* l, int T, int H, int D) {
+template <typename E>
+__global__ void lse_merge_kernel(const E* o1, const float* l1, const E* o2, const float* l2, float* of, E* ob,
+                                 float* l, int T, int H, int D) {
   const int groups = D / 8;
   const int64_t total = (int64_t)T * H * groups;
   for (int64_t x = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; x < total; x += (int64_t)gridDim.x * blockDim.x) {
@@ -380,12 +381,12 @@ __global__ void lse_merge_kernel(const __nv_bfloat16* o1, const float* l1, const
     const int64_t off = th * D + gidx * 8;
     uint4 ua = *reinterpret_cast<const uint4*>(o1 + off);
     uint4 uc = *reinterpret_cast<const uint4*>(o2 + off);
-    const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&ua);
-    const __nv_bfloat162* pc = reinterpret_cast<const __nv_bfloat162*>(&uc);
+    const uint32_t* pa = reinterpret_cast<const uint32_t*>(&ua);
+    const uint32_t* pc = reinterpret_cast<const uint32_t*>(&uc);
     float r[8];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      float2 fa = __bfloat1622float2(pa[j]), fc = __bfloat1622float2(pc[j]);
+      const float2 fa = unpack2<E>(pa[j]), fc = unpack2<E>(pc[j]);
       r[2 * j] = wa * fa.x + wc * fc.x;
       r[2 * j + 1] = wa * fa.y + wc * fc.y;
     }
@@ -395,7 +396,7 @@ __global__ void lse_merge_kernel(const __nv_bfloat16* o1, const float* l1, const
     }
     if (ob)
       *reinterpret_cast<uint4*>(ob + off) =
-          make_uint4(pack_bf16x2(r[0], r[1]), pack_bf16x2(r[2], r[3]), pack_bf16x2(r[4], r[5]), pack_bf16x2(r[6], r[7]));
+          make_uint4(pack2<E>(r[0], r[1]), pack2<E>(r[2], r[3]), pack2<E>(r[4], r[5]), pack2<E>(r[6], r[7]));
     if (gidx == 0) l[(int64_t)h * T + t] = lm;
   }
 }
@@ -404,9 +405,10 @@ __global__ void lse_merge_kernel(const __nv_bfloat16* o1, const float* l1, const
 // (row, head); then grid-stride zeroing of the fp32 accumulators. When dK/dV
 // are written directly (no accumulators), rows no segment covers are zeroed.
 // Delta = rowsum(dO * O) and the zeroed accumulators; blocks bid of nblk.
-__device__ void bwd_pre_body(SegInfo g, const __nv_bfloat16* dout, const __nv_bfloat16* out, int64_t o_sb,
+template <typename E>
+__device__ void bwd_pre_body(SegInfo g, const E* dout, const E* out, int64_t o_sb,
                              int64_t o_ss, int64_t o_sh, float* delta, float* dq_acc, int Hq, int Dqk, int Dv,
-                             float* dk_acc, float* dv_acc, __nv_bfloat16* dk, __nv_bfloat16* dv, int64_t k_sb,
+                             float* dk_acc, float* dv_acc, uint16_t* dk, uint16_t* dv, int64_t k_sb,
                              int64_t k_ss, int64_t k_sh, int64_t v_sb, int64_t v_ss, int64_t v_sh, int Hkv, int bid,
                              int nblk) {
   const int64_t rows = (int64_t)g.B * g.Sq;
@@ -428,11 +430,11 @@ __device__ void bwd_pre_body(SegInfo g, const __nv_bfloat16* dout, const __nv_bf
       for (int d = sub * 8; d < Dv; d += lanes * 8) {
         uint4 ug = *reinterpret_cast<const uint4*>(dout + off + d);
         uint4 uo = *reinterpret_cast<const uint4*>(out + off + d);
-        const __nv_bfloat162* pg = reinterpret_cast<const __nv_bfloat162*>(&ug);
-        const __nv_bfloat162* po = reinterpret_cast<const __nv_bfloat162*>(&uo);
+        const uint32_t* pg = reinterpret_cast<const uint32_t*>(&ug);
+        const uint32_t* po = reinterpret_cast<const uint32_t*>(&uo);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          float2 x = __bfloat1622float2(pg[j]), y = __bfloat1622float2(po[j]);
+          const float2 x = unpack2<E>(pg[j]), y = unpack2<E>(po[j]);
           acc = fmaf(x.x, y.x, acc);
           acc = fmaf(x.y, y.y, acc);
         }
@@ -473,7 +475,8 @@ __device__ void bwd_pre_body(SegInfo g, const __nv_bfloat16* dout, const __nv_bf
 }
 
 // bf16 out = scale * fp32 accumulator ([rows][H][D], packed) in the tensor's own layout.
-__device__ __forceinline__ void convert_rows(const float* acc, __nv_bfloat16* dst, int64_t x, int Sr, int H, int D,
+template <typename E>
+__device__ __forceinline__ void convert_rows(const float* acc, E* dst, int64_t x, int Sr, int H, int D,
                                              int64_t sb, int64_t ss, int64_t sh, float scale) {
   const int groups = D / 8;
   const int gidx = (int)(x % groups);
@@ -484,14 +487,15 @@ __device__ __forceinline__ void convert_rows(const float* acc, __nv_bfloat16* ds
   const float4 a = reinterpret_cast<const float4*>(acc + rh * D)[2 * gidx];
   const float4 c = reinterpret_cast<const float4*>(acc + rh * D)[2 * gidx + 1];
   reinterpret_cast<uint4*>(dst + b * sb + (int64_t)s * ss + h * sh)[gidx] =
-      make_uint4(pack_bf16x2(a.x * scale, a.y * scale), pack_bf16x2(a.z * scale, a.w * scale),
-                 pack_bf16x2(c.x * scale, c.y * scale), pack_bf16x2(c.z * scale, c.w * scale));
+      make_uint4(pack2<E>(a.x * scale, a.y * scale), pack2<E>(a.z * scale, a.w * scale),
+                 pack2<E>(c.x * scale, c.y * scale), pack2<E>(c.z * scale, c.w * scale));
 }
 
 // dQ = scale * dQacc, and (when accumulated) dK = scale * dKacc, dV = dVacc.
-__global__ void bwd_convert_kernel(const float* dq_acc, __nv_bfloat16* dq, int64_t nq, int Sq, int Hq, int Dqk,
-                                   int64_t q_sb, int64_t q_ss, int64_t q_sh, const float* dk_acc, __nv_bfloat16* dk,
-                                   const float* dv_acc, __nv_bfloat16* dv, int64_t nk, int Sk, int Hkv, int Dv,
+template <typename E>
+__global__ void bwd_convert_kernel(const float* dq_acc, E* dq, int64_t nq, int Sq, int Hq, int Dqk,
+                                   int64_t q_sb, int64_t q_ss, int64_t q_sh, const float* dk_acc, E* dk,
+                                   const float* dv_acc, E* dv, int64_t nk, int Sk, int Hkv, int Dv,
                                    int64_t k_sb, int64_t k_ss, int64_t k_sh, int64_t v_sb, int64_t v_ss, int64_t v_sh,
                                    float scale) {
   const int64_t nk_dk = dk_acc ? nk * Hkv * (Dqk / 8) : 0;
@@ -573,7 +577,8 @@ __device__ __forceinline__ int live_segment(const int32_t* cu_q, const int32_t* 
 // query rows of the chunk's segments with keys; a warp per (row, head). The
 // running output is read from o_acc (fp32) when given, else from o_run (bf16);
 // both are written when given.
-__global__ void lse_merge_live_kernel(float* o_acc, __nv_bfloat16* o_run, float* l_acc, const __nv_bfloat16* o_new,
+template <typename E>
+__global__ void lse_merge_live_kernel(float* o_acc, E* o_run, float* l_acc, const E* o_new,
                                       const float* l_new, const int32_t* cu_q, const int32_t* cu_k,
                                       const int32_t* dev_meta, int nseg_cap, int T, int H, int D) {
   const int nseg = dev_meta ? min(dev_meta[0], nseg_cap) : nseg_cap;
@@ -595,19 +600,19 @@ __global__ void lse_merge_live_kernel(float* o_acc, __nv_bfloat16* o_run, float*
         x[0] = u0.x; x[1] = u0.y; x[2] = u0.z; x[3] = u0.w; x[4] = u1.x; x[5] = u1.y; x[6] = u1.z; x[7] = u1.w;
       } else {
         const uint4 u = *reinterpret_cast<const uint4*>(o_run + off + d);
-        const __nv_bfloat162* pr = reinterpret_cast<const __nv_bfloat162*>(&u);
+        const uint32_t* pr = reinterpret_cast<const uint32_t*>(&u);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          const float2 f = __bfloat1622float2(pr[j]);
+          const float2 f = unpack2<E>(pr[j]);
           x[2 * j] = f.x;
           x[2 * j + 1] = f.y;
         }
       }
       const uint4 un = *reinterpret_cast<const uint4*>(o_new + off + d);
-      const __nv_bfloat162* pn = reinterpret_cast<const __nv_bfloat162*>(&un);
+      const uint32_t* pn = reinterpret_cast<const uint32_t*>(&un);
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const float2 f = __bfloat1622float2(pn[j]);
+        const float2 f = unpack2<E>(pn[j]);
         x[2 * j] = wa * x[2 * j] + wc * f.x;
         x[2 * j + 1] = wa * x[2 * j + 1] + wc * f.y;
       }
@@ -619,10 +624,7 @@ __global__ void lse_merge_live_kernel(float* o_acc, __nv_bfloat16* o_run, float*
         uint4 r;
         uint32_t* rp = reinterpret_cast<uint32_t*>(&r);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          __nv_bfloat162 v2 = __floats2bfloat162_rn(x[2 * j], x[2 * j + 1]);
-          rp[j] = *reinterpret_cast<uint32_t*>(&v2);
-        }
+        for (int j = 0; j < 4; ++j) rp[j] = pack2<E>(x[2 * j], x[2 * j + 1]);
         *reinterpret_cast<uint4*>(o_run + off + d) = r;
       }
     }
@@ -632,7 +634,8 @@ __global__ void lse_merge_live_kernel(float* o_acc, __nv_bfloat16* o_run, float*
 
 // dst += src (bf16, added in fp32, rounded once) on the query rows of the
 // segments with keys; a warp per (row, head).
-__global__ void grad_add_live_kernel(__nv_bfloat16* dst, const __nv_bfloat16* src, const int32_t* cu_q,
+template <typename E>
+__global__ void grad_add_live_kernel(E* dst, const E* src, const int32_t* cu_q,
                                      const int32_t* cu_k, const int32_t* dev_meta, int nseg_cap, int T, int H, int D) {
   const int nseg = dev_meta ? min(dev_meta[0], nseg_cap) : nseg_cap;
   const int lane = threadIdx.x & 31;
@@ -644,15 +647,14 @@ __global__ void grad_add_live_kernel(__nv_bfloat16* dst, const __nv_bfloat16* sr
     for (int d = lane * 8; d < D; d += 256) {
       const uint4 ua = *reinterpret_cast<const uint4*>(dst + off + d);
       const uint4 ub = *reinterpret_cast<const uint4*>(src + off + d);
-      const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&ua);
-      const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&ub);
+      const uint32_t* pa = reinterpret_cast<const uint32_t*>(&ua);
+      const uint32_t* pb = reinterpret_cast<const uint32_t*>(&ub);
       uint4 r;
       uint32_t* rp = reinterpret_cast<uint32_t*>(&r);
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const float2 fa = __bfloat1622float2(pa[j]), fb = __bfloat1622float2(pb[j]);
-        __nv_bfloat162 v2 = __floats2bfloat162_rn(fa.x + fb.x, fa.y + fb.y);
-        rp[j] = *reinterpret_cast<uint32_t*>(&v2);
+        const float2 fa = unpack2<E>(pa[j]), fb = unpack2<E>(pb[j]);
+        rp[j] = pack2<E>(fa.x + fb.x, fa.y + fb.y);
       }
       *reinterpret_cast<uint4*>(dst + off + d) = r;
     }
@@ -663,7 +665,7 @@ __global__ void grad_add_live_kernel(__nv_bfloat16* dst, const __nv_bfloat16* sr
 // other blocks fill uncovered query rows, so the list's latency-bound build
 // overlaps the fill and costs no launch of its own.
 __global__ void __launch_bounds__(kScanThreads) fwd_prep_kernel(SegInfo g, int2* items, int* n_items, int* seg_prefix,
-                                                                int item_cap, int* status, __nv_bfloat16* out,
+                                                                int item_cap, int* status, uint16_t* out,
                                                                 int64_t o_sb, int64_t o_ss, int64_t o_sh, float* lse,
                                                                 int64_t l_sb, int64_t l_sh, int Hq, int Dv) {
   if (blockIdx.x == 0)
@@ -675,10 +677,11 @@ __global__ void __launch_bounds__(kScanThreads) fwd_prep_kernel(SegInfo g, int2*
 // Backward preparation: block 0 builds the work list while the other blocks
 // compute Delta and zero the accumulators (HBM-bound), hiding the list's
 // latency behind that traffic.
+template <typename E>
 __global__ void __launch_bounds__(kScanThreads) bwd_prep_kernel(
     SegInfo g, int G, int Hkv, int split_target, int4* items, int* n_items, int* seg_prefix, int item_cap, int* status,
-    const __nv_bfloat16* dout, const __nv_bfloat16* out, int64_t o_sb, int64_t o_ss, int64_t o_sh, float* delta,
-    float* dq_acc, int Hq, int Dqk, int Dv, float* dk_acc, float* dv_acc, __nv_bfloat16* dk, __nv_bfloat16* dv,
+    const E* dout, const E* out, int64_t o_sb, int64_t o_ss, int64_t o_sh, float* delta,
+    float* dq_acc, int Hq, int Dqk, int Dv, float* dk_acc, float* dv_acc, uint16_t* dk, uint16_t* dv,
     int64_t k_sb, int64_t k_ss, int64_t k_sh, int64_t v_sb, int64_t v_ss, int64_t v_sh) {
   if (blockIdx.x == 0)
     bwd_schedule_body(g, G, Hkv, split_target, items, n_items, seg_prefix, item_cap, status);
@@ -697,13 +700,14 @@ int grid_for(int64_t work, int threads) {
 }  // namespace
 
 cudaError_t launch_fwd_prep(const SegInfo& g, int2* items, int* n_items, int* seg_prefix, int item_cap, int* status,
-                            __nv_bfloat16* out, int64_t o_sb, int64_t o_ss, int64_t o_sh, float* lse, int64_t l_sb,
+                            void* out, int64_t o_sb, int64_t o_ss, int64_t o_sh, float* lse, int64_t l_sb,
                             int64_t l_sh, int Hq, int Dv, cudaStream_t st) {
   // The fill usually has no rows at all (the builder covers every token); a
   // few blocks with a grid-stride loop cover the rest.
   const int fill = min(grid_for((int64_t)g.B * g.Sq * Hq * (Dv / 8), kScanThreads), 2 * 152);
-  fwd_prep_kernel<<<1 + fill, kScanThreads, 0, st>>>(g, items, n_items, seg_prefix, item_cap, status, out, o_sb, o_ss,
-                                                     o_sh, lse, l_sb, l_sh, Hq, Dv);
+  fwd_prep_kernel<<<1 + fill, kScanThreads, 0, st>>>(g, items, n_items, seg_prefix, item_cap, status,
+                                                     static_cast<uint16_t*>(out), o_sb, o_ss, o_sh, lse, l_sb, l_sh,
+                                                     Hq, Dv);
   return cudaGetLastError();
 }
 cudaError_t launch_build_segments(const int32_t* ids, int B, int Sk, int Lq, int q0, int32_t* cu_q, int32_t* cu_k,
@@ -713,30 +717,45 @@ cudaError_t launch_build_segments(const int32_t* ids, int B, int Sk, int Lq, int
   return cudaGetLastError();
 }
 
-cudaError_t launch_pad_fixup(__nv_bfloat16* out, float* lse, const int32_t* qids, int B, int Lq, int Hq, int Dv,
+cudaError_t launch_pad_fixup(void* out, float* lse, const int32_t* qids, int B, int Lq, int Hq, int Dv,
                              int64_t o_sb, int64_t o_ss, int64_t o_sh, int64_t l_sb, int64_t l_sh, cudaStream_t st) {
-  pad_fixup_kernel<<<grid_for((int64_t)B * Lq * 32, 256), 256, 0, st>>>(out, lse, qids, B, Lq, Hq, Dv, o_sb, o_ss,
+  pad_fixup_kernel<<<grid_for((int64_t)B * Lq * 32, 256), 256, 0, st>>>(static_cast<uint16_t*>(out), lse, qids, B, Lq, Hq, Dv, o_sb, o_ss,
                                                                         o_sh, l_sb, l_sh);
   return cudaGetLastError();
 }
 
-cudaError_t launch_lse_merge(const __nv_bfloat16* o1, const float* l1, const __nv_bfloat16* o2, const float* l2,
-                             float* of, __nv_bfloat16* ob, float* l, int T, int H, int D, cudaStream_t st) {
-  lse_merge_kernel<<<grid_for((int64_t)T * H * (D / 8), 256), 256, 0, st>>>(o1, l1, o2, l2, of, ob, l, T, H, D);
+cudaError_t launch_lse_merge(const void* o1, const float* l1, const void* o2, const float* l2, float* of, void* ob,
+                             float* l, int T, int H, int D, int f16, cudaStream_t st) {
+  const int grid = grid_for((int64_t)T * H * (D / 8), 256);
+  if (f16)
+    lse_merge_kernel<__half><<<grid, 256, 0, st>>>(static_cast<const __half*>(o1), l1, static_cast<const __half*>(o2),
+                                                   l2, of, static_cast<__half*>(ob), l, T, H, D);
+  else
+    lse_merge_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(o1), l1,
+                                                          static_cast<const __nv_bfloat16*>(o2), l2, of,
+                                                          static_cast<__nv_bfloat16*>(ob), l, T, H, D);
   return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_prep(const SegInfo& g, int G, int Hkv, int split_target, int4* items, int* n_items,
-                            int* seg_prefix, int item_cap, int* status, const __nv_bfloat16* dout,
-                            const __nv_bfloat16* out, int64_t o_sb, int64_t o_ss, int64_t o_sh, float* delta,
-                            float* dq_acc, int Hq, int Dqk, int Dv, float* dk_acc, float* dv_acc, __nv_bfloat16* dk,
-                            __nv_bfloat16* dv, int64_t k_sb, int64_t k_ss, int64_t k_sh, int64_t v_sb, int64_t v_ss,
-                            int64_t v_sh, cudaStream_t st) {
+                            int* seg_prefix, int item_cap, int* status, const void* dout, const void* out, int64_t o_sb,
+                            int64_t o_ss, int64_t o_sh, float* delta, float* dq_acc, int Hq, int Dqk, int Dv,
+                            float* dk_acc, float* dv_acc, void* dk, void* dv, int64_t k_sb, int64_t k_ss, int64_t k_sh,
+                            int64_t v_sb, int64_t v_ss, int64_t v_sh, int f16, cudaStream_t st) {
   const int64_t work = (int64_t)g.B * g.Sq * Hq * Dqk / 4 + (int64_t)g.B * g.Sk * Hkv * (Dqk + Dv) / 4;
   const int fill = min(grid_for(work, kScanThreads), 2 * 152);
-  bwd_prep_kernel<<<1 + fill, kScanThreads, 0, st>>>(g, G, Hkv, split_target, items, n_items, seg_prefix, item_cap,
-                                                     status, dout, out, o_sb, o_ss, o_sh, delta, dq_acc, Hq, Dqk, Dv,
-                                                     dk_acc, dv_acc, dk, dv, k_sb, k_ss, k_sh, v_sb, v_ss, v_sh);
+  uint16_t* dk16 = static_cast<uint16_t*>(dk);
+  uint16_t* dv16 = static_cast<uint16_t*>(dv);
+  if (f16)
+    bwd_prep_kernel<__half><<<1 + fill, kScanThreads, 0, st>>>(
+        g, G, Hkv, split_target, items, n_items, seg_prefix, item_cap, status, static_cast<const __half*>(dout),
+        static_cast<const __half*>(out), o_sb, o_ss, o_sh, delta, dq_acc, Hq, Dqk, Dv, dk_acc, dv_acc, dk16, dv16,
+        k_sb, k_ss, k_sh, v_sb, v_ss, v_sh);
+  else
+    bwd_prep_kernel<__nv_bfloat16><<<1 + fill, kScanThreads, 0, st>>>(
+        g, G, Hkv, split_target, items, n_items, seg_prefix, item_cap, status,
+        static_cast<const __nv_bfloat16*>(dout), static_cast<const __nv_bfloat16*>(out), o_sb, o_ss, o_sh, delta,
+        dq_acc, Hq, Dqk, Dv, dk_acc, dv_acc, dk16, dv16, k_sb, k_ss, k_sh, v_sb, v_ss, v_sh);
   return cudaGetLastError();
 }
 cudaError_t launch_cross_segments(const int32_t* ids, int B, int S, int q0, int Lq, int k0, int Lk, int32_t* cu_q,
@@ -746,31 +765,49 @@ cudaError_t launch_cross_segments(const int32_t* ids, int B, int S, int q0, int 
   cross_segments_kernel<<<B, kScanThreads, 0, st>>>(ids, B, S, q0, Lq, k0, Lk, cu_q, cu_k, dev_meta);
   return cudaGetLastError();
 }
-cudaError_t launch_lse_merge_live(float* o_acc, __nv_bfloat16* o_run, float* l_acc, const __nv_bfloat16* o_new,
-                                  const float* l_new, const int32_t* cu_q, const int32_t* cu_k, const int32_t* dev_meta,
-                                  int nseg, int T, int H, int D, cudaStream_t st) {
-  lse_merge_live_kernel<<<grid_for((int64_t)T * H * 32, 256), 256, 0, st>>>(o_acc, o_run, l_acc, o_new, l_new, cu_q,
-                                                                            cu_k, dev_meta, nseg, T, H, D);
+cudaError_t launch_lse_merge_live(float* o_acc, void* o_run, float* l_acc, const void* o_new, const float* l_new,
+                                  const int32_t* cu_q, const int32_t* cu_k, const int32_t* dev_meta, int nseg, int T,
+                                  int H, int D, int f16, cudaStream_t st) {
+  const int grid = grid_for((int64_t)T * H * 32, 256);
+  if (f16)
+    lse_merge_live_kernel<__half><<<grid, 256, 0, st>>>(o_acc, static_cast<__half*>(o_run), l_acc,
+                                                        static_cast<const __half*>(o_new), l_new, cu_q, cu_k, dev_meta,
+                                                        nseg, T, H, D);
+  else
+    lse_merge_live_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(o_acc, static_cast<__nv_bfloat16*>(o_run), l_acc,
+                                                               static_cast<const __nv_bfloat16*>(o_new), l_new, cu_q,
+                                                               cu_k, dev_meta, nseg, T, H, D);
   return cudaGetLastError();
 }
-cudaError_t launch_grad_add_live(__nv_bfloat16* dst, const __nv_bfloat16* src, const int32_t* cu_q,
-                                 const int32_t* cu_k, const int32_t* dev_meta, int nseg, int T, int H, int D,
-                                 cudaStream_t st) {
-  grad_add_live_kernel<<<grid_for((int64_t)T * H * 32, 256), 256, 0, st>>>(dst, src, cu_q, cu_k, dev_meta, nseg, T,
-                                                                           H, D);
+cudaError_t launch_grad_add_live(void* dst, const void* src, const int32_t* cu_q, const int32_t* cu_k,
+                                 const int32_t* dev_meta, int nseg, int T, int H, int D, int f16, cudaStream_t st) {
+  const int grid = grid_for((int64_t)T * H * 32, 256);
+  if (f16)
+    grad_add_live_kernel<__half><<<grid, 256, 0, st>>>(static_cast<__half*>(dst), static_cast<const __half*>(src), cu_q,
+                                                       cu_k, dev_meta, nseg, T, H, D);
+  else
+    grad_add_live_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(static_cast<__nv_bfloat16*>(dst),
+                                                              static_cast<const __nv_bfloat16*>(src), cu_q, cu_k,
+                                                              dev_meta, nseg, T, H, D);
   return cudaGetLastError();
 }
-cudaError_t launch_bwd_convert(const float* dq_acc, __nv_bfloat16* dq, bool have_q, int B, int Sq, int Hq, int Dqk,
-                               int64_t q_sb, int64_t q_ss, int64_t q_sh, const float* dk_acc, __nv_bfloat16* dk,
-                               const float* dv_acc, __nv_bfloat16* dv, int Sk, int Hkv, int Dv, int64_t k_sb,
-                               int64_t k_ss, int64_t k_sh, int64_t v_sb, int64_t v_ss, int64_t v_sh, float scale,
+cudaError_t launch_bwd_convert(const float* dq_acc, void* dq, bool have_q, int B, int Sq, int Hq, int Dqk,
+                               int64_t q_sb, int64_t q_ss, int64_t q_sh, const float* dk_acc, void* dk,
+                               const float* dv_acc, void* dv, int Sk, int Hkv, int Dv, int64_t k_sb, int64_t k_ss,
+                               int64_t k_sh, int64_t v_sb, int64_t v_ss, int64_t v_sh, float scale, int f16,
                                cudaStream_t st) {
   const int64_t nq = have_q ? (int64_t)B * Sq : 0, nk = (int64_t)B * Sk;
   const int64_t work = nq * Hq * (Dqk / 8) + (dk_acc ? nk * Hkv * ((Dqk + Dv) / 8) : 0);
   if (work == 0) return cudaSuccess;
-  bwd_convert_kernel<<<grid_for(work, 256), 256, 0, st>>>(dq_acc, dq, nq, Sq, Hq, Dqk, q_sb, q_ss, q_sh, dk_acc, dk,
-                                                          dv_acc, dv, nk, Sk, Hkv, Dv, k_sb, k_ss, k_sh, v_sb, v_ss,
-                                                          v_sh, scale);
+  if (f16)
+    bwd_convert_kernel<__half><<<grid_for(work, 256), 256, 0, st>>>(
+        dq_acc, static_cast<__half*>(dq), nq, Sq, Hq, Dqk, q_sb, q_ss, q_sh, dk_acc, static_cast<__half*>(dk), dv_acc,
+        static_cast<__half*>(dv), nk, Sk, Hkv, Dv, k_sb, k_ss, k_sh, v_sb, v_ss, v_sh, scale);
+  else
+    bwd_convert_kernel<__nv_bfloat16><<<grid_for(work, 256), 256, 0, st>>>(
+        dq_acc, static_cast<__nv_bfloat16*>(dq), nq, Sq, Hq, Dqk, q_sb, q_ss, q_sh, dk_acc,
+        static_cast<__nv_bfloat16*>(dk), dv_acc, static_cast<__nv_bfloat16*>(dv), nk, Sk, Hkv, Dv, k_sb, k_ss, k_sh,
+        v_sb, v_ss, v_sh, scale);
   return cudaGetLastError();
 }
 

@@ -41,9 +41,9 @@ struct BwdParams {
   int64_t l_sb, l_sh;
   const float* delta;  // [Hq][q_rows]
   int q_rows;
-  __nv_bfloat16* dk;
+  void* dk;  // T
   int64_t k_sb, k_ss, k_sh;
-  __nv_bfloat16* dv;
+  void* dv;  // T
   int64_t v_sb, v_ss, v_sh;
   int Hq, Hkv;
   float scale, scale_log2;
@@ -108,7 +108,7 @@ __device__ __forceinline__ BwdItem bwd_decode(const BwdParams& p, int w) {
   return t;
 }
 
-template <int DQK, int DV>
+template <typename T, int DQK, int DV>
 __global__ void __launch_bounds__(384, 1) attn_bwd_kernel(const __grid_constant__ BwdParams p) {
   using C = BwdCfg<DQK, DV>;
   extern __shared__ uint8_t smem_raw[];
@@ -195,10 +195,10 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_kernel(const __grid_constant_
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t id_sq = idesc_bf16_f32(128, 128, 0, 0);  // S^T, dP^T
-      constexpr uint32_t id_dv = idesc_bf16_f32(128, DV, 0, 1);   // dV += P^T dO
-      constexpr uint32_t id_dk = idesc_bf16_f32(128, DQK, 0, 1);  // dK += dS^T Q
-      constexpr uint32_t id_dq = idesc_bf16_f32(128, DQK, 1, 1);  // dQ = dS K
+      constexpr uint32_t id_sq = idesc_f32acc<T>(128, 128, 0, 0);  // S^T, dP^T
+      constexpr uint32_t id_dv = idesc_f32acc<T>(128, DV, 0, 1);   // dV += P^T dO
+      constexpr uint32_t id_dk = idesc_f32acc<T>(128, DQK, 0, 1);  // dK += dS^T Q
+      constexpr uint32_t id_dq = idesc_f32acc<T>(128, DQK, 1, 1);  // dQ = dS K
       const uint32_t k_a = sbase + C::K_OFF, v_a = sbase + C::V_OFF, q_a = sbase + C::Q_OFF;
       const uint32_t do_a = sbase + C::DO_OFF, pt_a = sbase + C::PT_OFF, ds_a = sbase + C::DS_OFF;
       uint32_t nz = 0, gstep = 0;
@@ -304,8 +304,8 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_kernel(const __grid_constant_
       const int j = t.kt * kBN + r;  // segment-local key index
       const bool valid = j < t.n;
       const int fk = t.ck0 + j, bk = fk / p.seg.Sk, sk = fk - bk * p.seg.Sk;
-      __nv_bfloat16* dk_row = p.dk + bk * p.k_sb + (int64_t)sk * p.k_ss + t.hk * p.k_sh;
-      __nv_bfloat16* dv_row = p.dv + bk * p.v_sb + (int64_t)sk * p.v_ss + t.hk * p.v_sh;
+      T* dk_row = static_cast<T*>(p.dk) + bk * p.k_sb + (int64_t)sk * p.k_ss + t.hk * p.k_sh;
+      T* dv_row = static_cast<T*>(p.dv) + bk * p.v_sb + (int64_t)sk * p.v_ss + t.hk * p.v_sh;
       if (t.k1 == t.k0) {
         if (valid) {
           for (int c = 0; c < DQK / 8; ++c) reinterpret_cast<uint4*>(dk_row)[c] = make_uint4(0, 0, 0, 0);
@@ -385,8 +385,8 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_kernel(const __grid_constant_
                   pr[u] = pe;
                   dr[u] = pe * (__uint_as_float(pv[2 * e + u]) - my_dl[qc]);
                 }
-                pk[e] = pack_bf16x2(pr[0], pr[1]);
-                dk2[e] = pack_bf16x2(dr[0], dr[1]);
+                pk[e] = pack2<T>(pr[0], pr[1]);
+                dk2[e] = pack2<T>(dr[0], dr[1]);
               }
               const int chunk = c >> 1, g0 = (c & 1) * 4;
 #pragma unroll
@@ -413,7 +413,7 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_kernel(const __grid_constant_
                   if (masked && (qc < q_lo || qc >= q_hi)) pe = 0.f;
                   pr[u] = pe;
                 }
-                pk[e] = pack_bf16x2(pr[0], pr[1]);
+                pk[e] = pack2<T>(pr[0], pr[1]);
               }
               const int chunk = c >> 1, g0 = (c & 1) * 4;
 #pragma unroll
@@ -443,10 +443,9 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_kernel(const __grid_constant_
 #pragma unroll
                 for (int e2 = 0; e2 < 4; ++e2) {
                   const int e = 4 * u + e2;
-                  __nv_bfloat162 b2 = *reinterpret_cast<const __nv_bfloat162*>(&pw[e2]);
-                  float2 pf = __bfloat1622float2(b2);
+                  float2 pf = unpack2<T>(pw[e2]);
                   const int qc = c * 32 + 2 * e;
-                  dk2[e] = pack_bf16x2(pf.x * (__uint_as_float(pv[2 * e]) - my_dl[qc]),
+                  dk2[e] = pack2<T>(pf.x * (__uint_as_float(pv[2 * e]) - my_dl[qc]),
                                        pf.y * (__uint_as_float(pv[2 * e + 1]) - my_dl[qc + 1]));
                 }
               }
@@ -474,10 +473,10 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_kernel(const __grid_constant_
           uint4* dst = reinterpret_cast<uint4*>(dv_row + c * 32);
 #pragma unroll
           for (int u = 0; u < 4; ++u)
-            dst[u] = make_uint4(pack_bf16x2(__uint_as_float(a[8 * u]), __uint_as_float(a[8 * u + 1])),
-                                pack_bf16x2(__uint_as_float(a[8 * u + 2]), __uint_as_float(a[8 * u + 3])),
-                                pack_bf16x2(__uint_as_float(a[8 * u + 4]), __uint_as_float(a[8 * u + 5])),
-                                pack_bf16x2(__uint_as_float(a[8 * u + 6]), __uint_as_float(a[8 * u + 7])));
+            dst[u] = make_uint4(pack2<T>(__uint_as_float(a[8 * u]), __uint_as_float(a[8 * u + 1])),
+                                pack2<T>(__uint_as_float(a[8 * u + 2]), __uint_as_float(a[8 * u + 3])),
+                                pack2<T>(__uint_as_float(a[8 * u + 4]), __uint_as_float(a[8 * u + 5])),
+                                pack2<T>(__uint_as_float(a[8 * u + 6]), __uint_as_float(a[8 * u + 7])));
         }
       }
       const float sc = p.scale;
@@ -489,10 +488,10 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_kernel(const __grid_constant_
           uint4* dst = reinterpret_cast<uint4*>(dk_row + c * 32);
 #pragma unroll
           for (int u = 0; u < 4; ++u)
-            dst[u] = make_uint4(pack_bf16x2(__uint_as_float(a[8 * u]) * sc, __uint_as_float(a[8 * u + 1]) * sc),
-                                pack_bf16x2(__uint_as_float(a[8 * u + 2]) * sc, __uint_as_float(a[8 * u + 3]) * sc),
-                                pack_bf16x2(__uint_as_float(a[8 * u + 4]) * sc, __uint_as_float(a[8 * u + 5]) * sc),
-                                pack_bf16x2(__uint_as_float(a[8 * u + 6]) * sc, __uint_as_float(a[8 * u + 7]) * sc));
+            dst[u] = make_uint4(pack2<T>(__uint_as_float(a[8 * u]) * sc, __uint_as_float(a[8 * u + 1]) * sc),
+                                pack2<T>(__uint_as_float(a[8 * u + 2]) * sc, __uint_as_float(a[8 * u + 3]) * sc),
+                                pack2<T>(__uint_as_float(a[8 * u + 4]) * sc, __uint_as_float(a[8 * u + 5]) * sc),
+                                pack2<T>(__uint_as_float(a[8 * u + 6]) * sc, __uint_as_float(a[8 * u + 7]) * sc));
         }
       }
       tc_fence_before();

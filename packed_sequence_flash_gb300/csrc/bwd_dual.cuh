@@ -66,7 +66,7 @@ struct BwdDualCfg {
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
 
-template <int DQK, int DV>
+template <typename T, int DQK, int DV>
 __global__ void __launch_bounds__(512, 1) attn_bwd_dual_kernel(const __grid_constant__ BwdParams p) {
   using C = BwdDualCfg<DQK, DV>;
   extern __shared__ uint8_t smem_raw[];
@@ -192,11 +192,11 @@ __global__ void __launch_bounds__(512, 1) attn_bwd_dual_kernel(const __grid_cons
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t id_sq = idesc_bf16_f32(128, 128, 0, 0);  // S^T = K Q^T
-      constexpr uint32_t id_dp = idesc_bf16_f32(128, 64, 0, 0);   // one half of dP^T = V dO^T
-      constexpr uint32_t id_dv = idesc_bf16_f32(128, DV, 0, 1);   // dV += P^T (TMEM) dO
-      constexpr uint32_t id_dk = idesc_bf16_f32(128, DQK, 0, 1);  // dK += dS^T Q
-      constexpr uint32_t id_dq = idesc_bf16_f32(128, DQK, 1, 1);  // dQ  = dS K
+      constexpr uint32_t id_sq = idesc_f32acc<T>(128, 128, 0, 0);  // S^T = K Q^T
+      constexpr uint32_t id_dp = idesc_f32acc<T>(128, 64, 0, 0);   // one half of dP^T = V dO^T
+      constexpr uint32_t id_dv = idesc_f32acc<T>(128, DV, 0, 1);   // dV += P^T (TMEM) dO
+      constexpr uint32_t id_dk = idesc_f32acc<T>(128, DQK, 0, 1);  // dK += dS^T Q
+      constexpr uint32_t id_dq = idesc_f32acc<T>(128, DQK, 1, 1);  // dQ  = dS K
       const uint32_t k_a = sbase + C::K_OFF, v_a = sbase + C::V_OFF, q_a0 = sbase + C::Q_OFF;
       const uint32_t do_a = sbase + C::DO_OFF, ds_a = sbase + C::DS_OFF;
       const uint32_t ra = tmem + C::T_A, rb = tmem + C::T_B;
@@ -399,7 +399,7 @@ __global__ void __launch_bounds__(512, 1) attn_bwd_dual_kernel(const __grid_cons
                   p0 = (qc < q_lo || qc >= q_hi) ? 0.f : p0;
                   p1 = (qc + 1 < q_lo || qc + 1 >= q_hi) ? 0.f : p1;
                 }
-                pk[e] = pack_bf16x2(p0, p1);
+                pk[e] = pack2<T>(p0, p1);
               }
             }
             tmem_st16_async(ra + pofs + c * 16, pk);
@@ -444,11 +444,11 @@ __global__ void __launch_bounds__(512, 1) attn_bwd_dual_kernel(const __grid_cons
               for (int hf = 0; hf < 2; ++hf) {
                 const int e = e4 * 2 + hf;
                 const float2 nd2 = hf ? make_float2(nd.z, nd.w) : make_float2(nd.x, nd.y);
-                const float2 pf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pcur[e]));
+                const float2 pf = unpack2<T>(pcur[e]);
                 const float2 dd =
                     fma2(make_float2(__uint_as_float(dcur[2 * e]), __uint_as_float(dcur[2 * e + 1])), one2, nd2);
                 const float2 ds = fma2(pf, dd, zero2);
-                dk2[e] = pack_bf16x2(ds.x, ds.y);
+                dk2[e] = pack2<T>(ds.x, ds.y);
               }
             }
 #pragma unroll

@@ -40,7 +40,7 @@ struct BwdWideCfg {
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
 
-template <int D>
+template <typename T, int D>
 __global__ void __launch_bounds__(384, 1) attn_bwd_wide_kernel(const __grid_constant__ BwdParams p) {
   using C = BwdWideCfg<D>;
   constexpr int NST = C::NST;
@@ -138,9 +138,9 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_wide_kernel(const __grid_cons
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t id_sq = idesc_bf16_f32(128, 128, 0, 0);
-      constexpr uint32_t id_part64 = idesc_bf16_f32(128, 64, 0, 1);  // dV, dK parts: B MN-major, N = 64
-      constexpr uint32_t id_dq64 = idesc_bf16_f32(128, 64, 1, 1);         // dQ part: A (dS) M-major
+      constexpr uint32_t id_sq = idesc_f32acc<T>(128, 128, 0, 0);
+      constexpr uint32_t id_part64 = idesc_f32acc<T>(128, 64, 0, 1);  // dV, dK parts: B MN-major, N = 64
+      constexpr uint32_t id_dq64 = idesc_f32acc<T>(128, 64, 1, 1);         // dQ part: A (dS) M-major
       const uint32_t ring = sbase + C::RING_OFF, pt_a = sbase + C::PT_OFF, ds_a = sbase + C::DS_OFF;
       uint32_t it = 0, nz = 0, gstep = 0;
       bool ok = true;
@@ -263,8 +263,8 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_wide_kernel(const __grid_cons
       const int j = t.kt * kBN + r;
       const bool valid = j < t.n;
       const int fk = t.ck0 + j, bk = fk / p.seg.Sk, sk = fk - bk * p.seg.Sk;
-      __nv_bfloat16* dk_row = p.dk + bk * p.k_sb + (int64_t)sk * p.k_ss + t.hk * p.k_sh + part * 128;
-      __nv_bfloat16* dv_row = p.dv + bk * p.v_sb + (int64_t)sk * p.v_ss + t.hk * p.v_sh + part * 128;
+      T* dk_row = static_cast<T*>(p.dk) + bk * p.k_sb + (int64_t)sk * p.k_ss + t.hk * p.k_sh + part * 128;
+      T* dv_row = static_cast<T*>(p.dv) + bk * p.v_sb + (int64_t)sk * p.v_ss + t.hk * p.v_sh + part * 128;
       if (t.k1 == t.k0) {
         if (valid) {
           for (int c = 0; c < 16; ++c) {
@@ -334,8 +334,8 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_wide_kernel(const __grid_cons
                 pr[u] = pe;
                 dr[u] = pe * (__uint_as_float(pv[2 * e + u]) - my_dl[qc]);
               }
-              pk[e] = pack_bf16x2(pr[0], pr[1]);
-              dk2[e] = pack_bf16x2(dr[0], dr[1]);
+              pk[e] = pack2<T>(pr[0], pr[1]);
+              dk2[e] = pack2<T>(dr[0], dr[1]);
             }
             const int chunk = c >> 1, g0 = (c & 1) * 4;
 #pragma unroll
@@ -365,14 +365,14 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_wide_kernel(const __grid_cons
           uint4* dk_dst = reinterpret_cast<uint4*>(dk_row + c * 32);
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            dv_dst[u] = make_uint4(pack_bf16x2(__uint_as_float(a[8 * u]), __uint_as_float(a[8 * u + 1])),
-                                   pack_bf16x2(__uint_as_float(a[8 * u + 2]), __uint_as_float(a[8 * u + 3])),
-                                   pack_bf16x2(__uint_as_float(a[8 * u + 4]), __uint_as_float(a[8 * u + 5])),
-                                   pack_bf16x2(__uint_as_float(a[8 * u + 6]), __uint_as_float(a[8 * u + 7])));
-            dk_dst[u] = make_uint4(pack_bf16x2(__uint_as_float(b[8 * u]) * sc, __uint_as_float(b[8 * u + 1]) * sc),
-                                   pack_bf16x2(__uint_as_float(b[8 * u + 2]) * sc, __uint_as_float(b[8 * u + 3]) * sc),
-                                   pack_bf16x2(__uint_as_float(b[8 * u + 4]) * sc, __uint_as_float(b[8 * u + 5]) * sc),
-                                   pack_bf16x2(__uint_as_float(b[8 * u + 6]) * sc, __uint_as_float(b[8 * u + 7]) * sc));
+            dv_dst[u] = make_uint4(pack2<T>(__uint_as_float(a[8 * u]), __uint_as_float(a[8 * u + 1])),
+                                   pack2<T>(__uint_as_float(a[8 * u + 2]), __uint_as_float(a[8 * u + 3])),
+                                   pack2<T>(__uint_as_float(a[8 * u + 4]), __uint_as_float(a[8 * u + 5])),
+                                   pack2<T>(__uint_as_float(a[8 * u + 6]), __uint_as_float(a[8 * u + 7])));
+            dk_dst[u] = make_uint4(pack2<T>(__uint_as_float(b[8 * u]) * sc, __uint_as_float(b[8 * u + 1]) * sc),
+                                   pack2<T>(__uint_as_float(b[8 * u + 2]) * sc, __uint_as_float(b[8 * u + 3]) * sc),
+                                   pack2<T>(__uint_as_float(b[8 * u + 4]) * sc, __uint_as_float(b[8 * u + 5]) * sc),
+                                   pack2<T>(__uint_as_float(b[8 * u + 6]) * sc, __uint_as_float(b[8 * u + 7]) * sc));
           }
         }
       }

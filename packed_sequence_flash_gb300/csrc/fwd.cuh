@@ -36,7 +36,7 @@ namespace psf {
 struct FwdParams {
   CUtensorMap tm_q, tm_k, tm_v;  // (d, s, h, b) views, box (64, 128), 128B swizzle, bf16
   SegInfo seg;
-  __nv_bfloat16* out;
+  void* out;  // T (bf16 or fp16), the inputs' type
   int64_t o_sb, o_ss, o_sh;  // element strides of out (batch, row, head)
   float* lse;
   int64_t l_sb, l_sh;  // element strides of lse (batch, head); rows are contiguous
@@ -89,7 +89,7 @@ __device__ __forceinline__ FwdTile fwd_decode(const FwdParams& p, int w) {
   return t;
 }
 
-template <int DQK, int DVC>
+template <typename T, int DQK, int DVC>
 __global__ void __launch_bounds__(256, 1) attn_fwd_kernel(const __grid_constant__ FwdParams p) {
   using C = FwdCfg<DQK, DVC>;
   constexpr int NST = C::NST, NQB = C::NQB;
@@ -186,8 +186,8 @@ __global__ void __launch_bounds__(256, 1) attn_fwd_kernel(const __grid_constant_
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, 0, 0);
-      constexpr uint32_t idesc_pv = idesc_bf16_f32(128, 64, 0, 1);
+      constexpr uint32_t idesc_qk = idesc_f32acc<T>(128, 128, 0, 0);
+      constexpr uint32_t idesc_pv = idesc_f32acc<T>(128, 64, 0, 1);
       uint32_t qcnt = 0, kvit = 0, scnt = 0, pcnt = 0, ntile = 0;
       bool ok = true;
       for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
@@ -276,7 +276,7 @@ __global__ void __launch_bounds__(256, 1) attn_fwd_kernel(const __grid_constant_
       const int fq = t.cq0 + i;
       const int bq = fq / p.seg.Sq;
       const int sq = fq - bq * p.seg.Sq;
-      __nv_bfloat16* orow = p.out + bq * p.o_sb + (int64_t)sq * p.o_ss + t.h * p.o_sh + t.part * DVC;
+      T* orow = static_cast<T*>(p.out) + bq * p.o_sb + (int64_t)sq * p.o_ss + t.h * p.o_sh + t.part * DVC;
       float* lrow = p.lse + bq * p.l_sb + t.h * p.l_sh + sq;
       if (t.nk == 0) {
         if (valid) {
@@ -333,7 +333,7 @@ __global__ void __launch_bounds__(256, 1) attn_fwd_kernel(const __grid_constant_
           const float e0 = ex2_approx(x.x), e1 = ex2_approx(x.y);
           r8[(2 * j) & 7] += e0;
           r8[(2 * j + 1) & 7] += e1;
-          pa[j] = pack_bf16x2(e0, e1);
+          pa[j] = pack2<T>(e0, e1);
         }
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
@@ -341,7 +341,7 @@ __global__ void __launch_bounds__(256, 1) attn_fwd_kernel(const __grid_constant_
           const float e0 = ex2_approx(x.x), e1 = ex2_approx(x.y);
           r8[(2 * j) & 7] += e0;
           r8[(2 * j + 1) & 7] += e1;
-          pb2[j] = pack_bf16x2(e0, e1);
+          pb2[j] = pack2<T>(e0, e1);
         }
         const float rs = ((r8[0] + r8[1]) + (r8[2] + r8[3])) + ((r8[4] + r8[5]) + (r8[6] + r8[7]));
         if (jj > 0) {
@@ -386,7 +386,7 @@ __global__ void __launch_bounds__(256, 1) attn_fwd_kernel(const __grid_constant_
           uint32_t pk[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j)
-            pk[j] = pack_bf16x2(__uint_as_float(r[2 * j]) * inv, __uint_as_float(r[2 * j + 1]) * inv);
+            pk[j] = pack2<T>(__uint_as_float(r[2 * j]) * inv, __uint_as_float(r[2 * j + 1]) * inv);
           uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
           for (int j = 0; j < 4; ++j) dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);

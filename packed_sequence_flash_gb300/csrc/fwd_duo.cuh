@@ -60,7 +60,7 @@ struct FwdDuoCfg {
   static_assert(3 * (SMEM_BYTES + 1024) > 233472, "at most two CTAs per SM");
 };
 
-template <int D>
+template <typename T, int D>
 __global__ void __launch_bounds__(192, 2) attn_fwd_duo_kernel(const __grid_constant__ FwdParams p) {
   using C = FwdDuoCfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -168,8 +168,8 @@ __global__ void __launch_bounds__(192, 2) attn_fwd_duo_kernel(const __grid_const
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t id_qk = idesc_bf16_f32(128, 128, 0, 0);
-      constexpr uint32_t id_pv = idesc_bf16_f32(128, D, 0, 1);
+      constexpr uint32_t id_qk = idesc_f32acc<T>(128, 128, 0, 0);
+      constexpr uint32_t id_pv = idesc_f32acc<T>(128, D, 0, 1);
       const uint32_t q_a = smem_u32(smem + C::Q_OFF), slot_a = smem_u32(smem + C::SLOT_OFF);
       uint32_t qcnt = 0, it = 0, kv = 0, ntile = 0;
       bool ok = true;
@@ -251,7 +251,7 @@ __global__ void __launch_bounds__(192, 2) attn_fwd_duo_kernel(const __grid_const
       const int fq = t.cq0 + i;
       const int bq = fq / p.seg.Sq;
       const int sq = fq - bq * p.seg.Sq;
-      __nv_bfloat16* orow = p.out + bq * p.o_sb + (int64_t)sq * p.o_ss + t.h * p.o_sh;
+      T* orow = static_cast<T*>(p.out) + bq * p.o_sb + (int64_t)sq * p.o_ss + t.h * p.o_sh;
       float* lrow = p.lse + bq * p.l_sb + t.h * p.l_sh + sq;
       if (t.nk == 0) {
         if (valid) {
@@ -341,7 +341,7 @@ __global__ void __launch_bounds__(192, 2) attn_fwd_duo_kernel(const __grid_const
               const float e0 = ex2_approx(x.x), e1 = ex2_approx(x.y);
               r8[(2 * e) & 7] += e0;
               r8[(2 * e + 1) & 7] += e1;
-              pk[e] = pack_bf16x2(e0, e1);
+              pk[e] = pack2<T>(e0, e1);
             }
             tmem_st16_async(ts + c * 16, pk);
           }
@@ -368,7 +368,7 @@ __global__ void __launch_bounds__(192, 2) attn_fwd_duo_kernel(const __grid_const
           uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e)
-            pk[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * inv, __uint_as_float(r[2 * e + 1]) * inv);
+            pk[e] = pack2<T>(__uint_as_float(r[2 * e]) * inv, __uint_as_float(r[2 * e + 1]) * inv);
           uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
           for (int e = 0; e < 4; ++e) dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);

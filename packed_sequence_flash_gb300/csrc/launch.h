@@ -16,7 +16,7 @@ struct BwdParams;
 // counter of kernels that take items dynamically), and out = 0 / lse = -inf for
 // query rows at or past cu_q[nseg].
 cudaError_t launch_fwd_prep(const SegInfo& g, int2* items, int* n_items, int* seg_prefix, int item_cap, int* status,
-                            __nv_bfloat16* out, int64_t o_sb, int64_t o_ss, int64_t o_sh, float* lse, int64_t l_sb,
+                            void* out, int64_t o_sb, int64_t o_ss, int64_t o_sh, float* lse, int64_t l_sb,
                             int64_t l_sh, int Hq, int Dv, cudaStream_t st);
 // Backward preparation in one launch: the work list of key tiles, split into
 // (first step, end step) sub-ranges when split_target > 0 (items are int4
@@ -25,41 +25,40 @@ cudaError_t launch_fwd_prep(const SegInfo& g, int2* items, int* n_items, int* se
 // zeroed dK/dV accumulators (when given) or zeroed dK / dV rows at or past
 // cu_k[nseg].
 cudaError_t launch_bwd_prep(const SegInfo& g, int G, int Hkv, int split_target, int4* items, int* n_items,
-                            int* seg_prefix, int item_cap, int* status, const __nv_bfloat16* dout,
-                            const __nv_bfloat16* out, int64_t o_sb, int64_t o_ss, int64_t o_sh, float* delta,
-                            float* dq_acc, int Hq, int Dqk, int Dv, float* dk_acc, float* dv_acc, __nv_bfloat16* dk,
-                            __nv_bfloat16* dv, int64_t k_sb, int64_t k_ss, int64_t k_sh, int64_t v_sb, int64_t v_ss,
-                            int64_t v_sh, cudaStream_t st);
+                            int* seg_prefix, int item_cap, int* status, const void* dout, const void* out, int64_t o_sb,
+                            int64_t o_ss, int64_t o_sh, float* delta, float* dq_acc, int Hq, int Dqk, int Dv,
+                            float* dk_acc, float* dv_acc, void* dk, void* dv, int64_t k_sb, int64_t k_ss, int64_t k_sh,
+                            int64_t v_sb, int64_t v_ss, int64_t v_sh, int f16, cudaStream_t st);
 // Grid: one CTA per SM (two for head dims 64 and 128), at most max_work.
-cudaError_t launch_fwd(const FwdParams& p, int dqk, int dvc, int sms, int64_t max_work, cudaStream_t st);
-cudaError_t launch_bwd(const BwdParams& p, int dqk, int dv, int sms, int item_cap, cudaStream_t st);
+// f16 selects fp16 inputs and outputs (else bf16).
+cudaError_t launch_fwd(const FwdParams& p, int dqk, int dvc, int sms, int64_t max_work, int f16, cudaStream_t st);
+cudaError_t launch_bwd(const BwdParams& p, int dqk, int dv, int sms, int item_cap, int f16, cudaStream_t st);
 int fwd_smem_bytes(int dqk, int dvc);
 int bwd_smem_bytes(int dqk, int dv);
 
 cudaError_t launch_build_segments(const int32_t* ids, int B, int Sk, int Lq, int q0, int32_t* cu_q, int32_t* cu_k,
                                   int capacity, int32_t* meta, uint8_t* seg_is_pad, int* status, cudaStream_t st);
-cudaError_t launch_pad_fixup(__nv_bfloat16* out, float* lse, const int32_t* qids, int B, int Lq, int Hq, int Dv,
+cudaError_t launch_pad_fixup(void* out, float* lse, const int32_t* qids, int B, int Lq, int Hq, int Dv,
                              int64_t o_sb, int64_t o_ss, int64_t o_sh, int64_t l_sb, int64_t l_sh, cudaStream_t st);
-cudaError_t launch_lse_merge(const __nv_bfloat16* o1, const float* l1, const __nv_bfloat16* o2, const float* l2,
-                             float* of, __nv_bfloat16* ob, float* l, int T, int H, int D, cudaStream_t st);
+cudaError_t launch_lse_merge(const void* o1, const float* l1, const void* o2, const float* l2, float* of, void* ob,
+                             float* l, int T, int H, int D, int f16, cudaStream_t st);
 // Cross-chunk segments (3 per row) of the shard [q0, q0 + Lq) against the
 // earlier key chunk [k0, k0 + Lk); dev_meta = {3 B, max_q, max_k}.
 cudaError_t launch_cross_segments(const int32_t* ids, int B, int S, int q0, int Lq, int k0, int Lk, int32_t* cu_q,
                                   int32_t* cu_k, int32_t* dev_meta, cudaStream_t st);
 // Live-row merge and gradient add over the query rows of segments with keys
 // (segment count from dev_meta when given, capped at nseg).
-cudaError_t launch_lse_merge_live(float* o_acc, __nv_bfloat16* o_run, float* l_acc, const __nv_bfloat16* o_new,
-                                  const float* l_new, const int32_t* cu_q, const int32_t* cu_k, const int32_t* dev_meta,
-                                  int nseg, int T, int H, int D, cudaStream_t st);
-cudaError_t launch_grad_add_live(__nv_bfloat16* dst, const __nv_bfloat16* src, const int32_t* cu_q,
-                                 const int32_t* cu_k, const int32_t* dev_meta, int nseg, int T, int H, int D,
-                                 cudaStream_t st);
+cudaError_t launch_lse_merge_live(float* o_acc, void* o_run, float* l_acc, const void* o_new, const float* l_new,
+                                  const int32_t* cu_q, const int32_t* cu_k, const int32_t* dev_meta, int nseg, int T,
+                                  int H, int D, int f16, cudaStream_t st);
+cudaError_t launch_grad_add_live(void* dst, const void* src, const int32_t* cu_q, const int32_t* cu_k,
+                                 const int32_t* dev_meta, int nseg, int T, int H, int D, int f16, cudaStream_t st);
 // dQ = scale * dQacc (bf16, q's layout); with accumulators also dK = scale *
 // dKacc and dV = dVacc.
-cudaError_t launch_bwd_convert(const float* dq_acc, __nv_bfloat16* dq, bool have_q, int B, int Sq, int Hq, int Dqk,
-                               int64_t q_sb, int64_t q_ss, int64_t q_sh, const float* dk_acc, __nv_bfloat16* dk,
-                               const float* dv_acc, __nv_bfloat16* dv, int Sk, int Hkv, int Dv, int64_t k_sb,
-                               int64_t k_ss, int64_t k_sh, int64_t v_sb, int64_t v_ss, int64_t v_sh, float scale,
+cudaError_t launch_bwd_convert(const float* dq_acc, void* dq, bool have_q, int B, int Sq, int Hq, int Dqk,
+                               int64_t q_sb, int64_t q_ss, int64_t q_sh, const float* dk_acc, void* dk,
+                               const float* dv_acc, void* dv, int Sk, int Hkv, int Dv, int64_t k_sb, int64_t k_ss,
+                               int64_t k_sh, int64_t v_sb, int64_t v_ss, int64_t v_sh, float scale, int f16,
                                cudaStream_t st);
 
 }  // namespace psf

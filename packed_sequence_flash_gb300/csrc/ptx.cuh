@@ -6,6 +6,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 namespace psf {
@@ -262,13 +263,52 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
       : "memory");
 }
 
+// ---------------------------------------------------------------- 16-bit operand types
+// The kernels take bf16 or fp16 inputs (one type per call): T is __nv_bfloat16
+// or __half. kFmt is the A/B format code of tcgen05.mma kind::f16.
+template <typename T>
+struct Elem16;
+template <>
+struct Elem16<__nv_bfloat16> {
+  static constexpr uint32_t kFmt = 1;
+};
+template <>
+struct Elem16<__half> {
+  static constexpr uint32_t kFmt = 0;
+};
+// Two floats -> a packed pair of T (round to nearest even), low half first.
+template <typename T>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi);
+template <>
+__device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+template <>
+__device__ __forceinline__ uint32_t pack2<__half>(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+// A packed pair of T -> two floats.
+template <typename T>
+__device__ __forceinline__ float2 unpack2(uint32_t u);
+template <>
+__device__ __forceinline__ float2 unpack2<__nv_bfloat16>(uint32_t u) {
+  return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u));
+}
+template <>
+__device__ __forceinline__ float2 unpack2<__half>(uint32_t u) {
+  return __half22float2(*reinterpret_cast<const __half2*>(&u));
+}
+
 // ---------------------------------------------------------------- descriptors
-// Instruction descriptor, kind::f16 with bf16 inputs and an fp32 accumulator.
-// a_mn / b_mn select MN-major (1) instead of K-major (0) operands.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn, int b_mn) {
+// Instruction descriptor, kind::f16 with T (bf16 or fp16) inputs and an fp32
+// accumulator. a_mn / b_mn select MN-major (1) instead of K-major (0) operands.
+template <typename T>
+__host__ __device__ constexpr uint32_t idesc_f32acc(int M, int N, int a_mn, int b_mn) {
   return (1u << 4)                      // D format: f32
-         | (1u << 7)                    // A format: bf16
-         | (1u << 10)                   // B format: bf16
+         | (Elem16<T>::kFmt << 7)       // A format
+         | (Elem16<T>::kFmt << 10)      // B format
          | ((uint32_t)a_mn << 15)       // A major
          | ((uint32_t)b_mn << 16)       // B major
          | ((uint32_t)(N >> 3) << 17)   // N / 8
@@ -317,10 +357,6 @@ __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
       : "l"(*reinterpret_cast<uint64_t*>(&a)), "l"(*reinterpret_cast<uint64_t*>(&b)),
         "l"(*reinterpret_cast<uint64_t*>(&c)));
   return *reinterpret_cast<float2*>(&d);
-}
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&v);
 }
 
 }  // namespace psf

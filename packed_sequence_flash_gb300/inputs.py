@@ -65,12 +65,17 @@ def doc_ids_from_lengths(lengths: list[int], total: int) -> np.ndarray:
     return ids
 
 
-def randn_bf16(shape, seed: int, factor: float = 1.0) -> torch.Tensor:
+def randn16(shape, seed: int, factor: float = 1.0, dtype=torch.bfloat16) -> torch.Tensor:
+    """Seeded N(0, 1) * factor in fp32, rounded to a 16-bit type (bf16 or fp16, RNE)."""
     g = torch.Generator().manual_seed(int(seed))
     x = torch.randn(*shape, generator=g, dtype=torch.float32)
     if factor != 1.0:
         x = x * factor
-    return x.to(torch.bfloat16)
+    return x.to(dtype)
+
+
+def randn_bf16(shape, seed: int, factor: float = 1.0) -> torch.Tensor:
+    return randn16(shape, seed, factor, torch.bfloat16)
 
 
 @dataclass

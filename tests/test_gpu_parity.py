@@ -86,22 +86,25 @@ def _rand_segments(r, nseg, max_len, allow_empty=True):
     return cu_q, cu_k
 
 
-def _varlen_case(seed, Dqk, Dv, Hq, Hkv, causal, window, nseg=5, max_len=400, tail_q=0, tail_k=0):
+def _varlen_case(seed, Dqk, Dv, Hq, Hkv, causal, window, nseg=5, max_len=400, tail_q=0, tail_k=0,
+                 dtype=torch.bfloat16):
     r = np.random.default_rng(seed)
     cu_q, cu_k = _rand_segments(r, nseg, max_len)
     Tq, Tk = int(cu_q[-1]) + tail_q, int(cu_k[-1]) + tail_k
-    q = inputs.randn_bf16((Tq, Hq, Dqk), seed * 7 + 1)
-    k = inputs.randn_bf16((Tk, Hkv, Dqk), seed * 7 + 2)
-    v = inputs.randn_bf16((Tk, Hkv, Dv), seed * 7 + 3)
-    do = inputs.randn_bf16((Tq, Hq, Dv), seed * 7 + 4)
+    q = inputs.randn16((Tq, Hq, Dqk), seed * 7 + 1, dtype=dtype)
+    k = inputs.randn16((Tk, Hkv, Dqk), seed * 7 + 2, dtype=dtype)
+    v = inputs.randn16((Tk, Hkv, Dv), seed * 7 + 3, dtype=dtype)
+    do = inputs.randn16((Tq, Hq, Dv), seed * 7 + 4, dtype=dtype)
     scale = 1.0 / np.sqrt(Dqk)
     cq, ck = torch.from_numpy(cu_q).cuda(), torch.from_numpy(cu_k).cuda()
     mq, mk = int(np.diff(cu_q).max()), int(np.diff(cu_k).max())
     out, lse = psf.attn_varlen_fwd(cuda(q), cuda(k), cuda(v), cq, ck, mq, mk, scale, causal, window)
+    assert out.dtype == dtype
     out_o, lse_o = oracle.attn_fwd_segments(q, k, v, cu_q, cu_k, scale, causal, window)
     assert_fwd(out, lse, out_o, lse_o)
     grads = psf.attn_varlen_bwd(cuda(do), cuda(q), cuda(k), cuda(v), out, lse, cq, ck, mq, mk, scale, causal,
                                 window)
+    assert all(g.dtype == dtype for g in grads)
     ref = oracle.attn_bwd_segments(do, q, k, v, out_o, lse_o, cu_q, cu_k, scale, causal, window)
     assert_grads(grads, ref)
     assert psf.device_status() == 0
@@ -141,8 +144,9 @@ def test_document_causal_d64_window_one():
 
 # ---------------------------------------------------------------- dense
 
-def _dense_case(B, Hq, Hkv, Nq, Nk, Dqk, Dv, causal, window=None, seed=0, factor=1.0):
+def _dense_case(B, Hq, Hkv, Nq, Nk, Dqk, Dv, causal, window=None, seed=0, factor=1.0, dtype=torch.bfloat16):
     w = inputs.dense_workload(B, Hq, Hkv, Nq, Nk, Dqk, Dv, seed, factor=factor, causal=causal)
+    w.q, w.k, w.v, w.dout = (t.to(dtype) for t in (w.q, w.k, w.v, w.dout))
     q, k, v, do = (cuda(t) for t in (w.q, w.k, w.v, w.dout))
     out, lse = psf.attn_dense_fwd(q, k, v, w.scale, causal, window)
     out_o, lse_o = oracle.attn_fwd_dense(w.q, w.k, w.v, w.scale, causal, window)
@@ -304,3 +308,48 @@ def test_grad_add_live_rows_matches_oracle():
     assert np.max(np.abs(got - ref) / np.maximum(np.abs(ref), 1e-3)) < 8e-3
     other = np.setdiff1d(np.arange(a.shape[0]), oracle.live_rows(cu_q, cu_k))
     np.testing.assert_array_equal(dst.cpu()[other].view(torch.int16).numpy(), a[other].view(torch.int16).numpy())
+
+
+# ---------------------------------------------------------------- fp16 inputs
+
+@pytest.mark.parametrize("dims", [(64, 64), (128, 128), (192, 128)])
+@pytest.mark.parametrize("causal,window", [(True, None), (False, 150)])
+def test_varlen_fwd_bwd_fp16_matches_oracle(dims, causal, window):
+    _varlen_case(13, dims[0], dims[1], 4, 2, causal, window, dtype=torch.float16)
+
+
+def test_dense_d512_fp16_forward_backward():
+    _dense_case(1, 4, 2, 260, 260, 512, 512, True, seed=4, factor=0.5, dtype=torch.float16)
+
+
+def test_document_causal_fp16():
+    w = inputs.small_document_workload(900, 4, 2, 128, 128, 5, max_len=350, pad_tail=61)
+    w.q, w.k, w.v, w.dout = (t.to(torch.float16) for t in (w.q, w.k, w.v, w.dout))
+    doc_case(w)
+
+
+def test_lse_merge_and_live_rows_fp16():
+    cu_q, cu_k, o_run, l_acc, o_new, l_new = _live_case(7)
+    o_run, o_new = o_run.to(torch.float16), o_new.to(torch.float16)
+    _, ob, l = psf.lse_merge(cuda(o_run), cuda(l_acc), cuda(o_new), cuda(l_new), want_f32=False, want_bf16=True)
+    assert ob.dtype == torch.float16
+    o_ref, l_ref = oracle.lse_merge(o_run, l_acc, o_new, l_new)
+    assert np.max(np.abs(np64(ob) - o_ref)) < 5e-3
+    run, lr = cuda(o_run).clone(), cuda(l_acc).clone()
+    cq, ck = torch.from_numpy(cu_q).cuda(), torch.from_numpy(cu_k).cuda()
+    psf.lse_merge_live_rows(run, lr, cuda(o_new), cuda(l_new), cq, ck)
+    o_lv, _ = oracle.lse_merge_live_rows(o_run, l_acc, o_new, l_new, cu_q, cu_k)
+    assert np.max(np.abs(np64(run) - o_lv)) < 5e-3
+    dst = cuda(o_run).clone()
+    psf.grad_add_live_rows(dst, cuda(o_new), cq, ck)
+    ref = oracle.grad_add_live_rows(o_run, o_new, cu_q, cu_k)
+    assert np.max(np.abs(np64(dst) - ref)) < 1e-2
+    assert psf.device_status() == 0
+
+
+def test_mixed_dtypes_are_rejected():
+    q = torch.zeros(128, 2, 64, dtype=torch.float16, device="cuda")
+    k = torch.zeros(128, 1, 64, dtype=torch.bfloat16, device="cuda")
+    cu = torch.tensor([0, 128], dtype=torch.int32, device="cuda")
+    with pytest.raises(ValueError):
+        psf.attn_varlen_fwd(q, k, k, cu, cu, 128, 128, 0.125, True)

@@ -43,7 +43,7 @@ def _call(lib, noalloc, q, k, v, cu_q, cu_k, mq, mk, window):
     lse = torch.full((Hq, Tq), float("nan"), dtype=torch.float32, device="cuda")
     stream = torch.cuda.current_stream().cuda_stream
     common = [q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), cu_q.data_ptr(),
-              cu_k.data_ptr(), None, nseg, mq, mk, 0, 1, Tq, Tk, Hq, Hkv, D, D, 1.0 / np.sqrt(D), 1, window]
+              cu_k.data_ptr(), None, nseg, mq, mk, 0, 0, 1, Tq, Tk, Hq, Hkv, D, D, 1.0 / np.sqrt(D), 1, window]
     if noalloc:
         rc = lib.psf_attn_varlen_fwd_noalloc(*common, stream)
         ws = None
@@ -79,10 +79,10 @@ def test_noalloc_forward_rejects_sizes_beyond_its_limit():
     lib = _lib.load()
     q, k, v, cu_q, cu_k, mq, mk = _case(3)
     rc = lib.psf_attn_varlen_fwd_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), q.data_ptr(), q.data_ptr(),
-                                         cu_q.data_ptr(), cu_k.data_ptr(), None, 65537, mq, mk, 0, 1, q.shape[0],
+                                         cu_q.data_ptr(), cu_k.data_ptr(), None, 65537, mq, mk, 0, 0, 1, q.shape[0],
                                          k.shape[0], 4, 2, 128, 128, 0.1, 1, -1, None)
     assert rc == -1 and b"segments" in lib.psf_last_error()
     rc = lib.psf_attn_varlen_fwd_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), q.data_ptr(), q.data_ptr(),
-                                         cu_q.data_ptr(), cu_k.data_ptr(), None, 6, mq, mk, 1, 2, 1 << 20, 16, 4, 2,
+                                         cu_q.data_ptr(), cu_k.data_ptr(), None, 6, mq, mk, 1, 0, 2, 1 << 20, 16, 4, 2,
                                          128, 128, 0.1, 1, -1, None)
     assert rc == -1 and b"query rows" in lib.psf_last_error()
