@@ -358,36 +358,67 @@ def our_arm(args):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms_max = float(t.item())
 
-    # ---- end to end through the public API: pinned host inputs in, results out
+    # ---- end to end through the public API: every step copies its inputs in
+    # from pinned host memory and its results (out, lse, dq, dk, dv) back out.
+    # The steps are pipelined the way a data loader feeds a GPU: step i+1's
+    # inputs upload on one copy stream and step i-1's results download on
+    # another while step i computes (device inputs double-buffered). No L2
+    # flush here: each step's inputs arrive fresh from the host.
     hq, hk, hv, hd = (t.pin_memory() for t in (w.q, w.k, w.v, w.dout))
     hids = torch.from_numpy(np.ascontiguousarray(w.doc_ids)).pin_memory()
-    dq_, dk_, dv_, dd_ = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v), torch.empty_like(do)
-    di_ = torch.empty_like(ids)
-    res_host = None
-    e2e_steps = max(3, min(args.steps, 50))
-    e_start = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
-    e_stop = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
-    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hd, hids))
+    host_in = (hq, hk, hv, hd, hids)
+    comp_s = torch.cuda.current_stream()
+    h2d_s, d2h_s = torch.cuda.Stream(), torch.cuda.Stream()
+    nbuf = 2
+    dev_in = [tuple(torch.empty_like(t) for t in (q, k, v, do, ids)) for _ in range(nbuf)]
+    in_ready = [torch.cuda.Event() for _ in range(nbuf)]
+    in_free = [torch.cuda.Event() for _ in range(nbuf)]
+    out_ready = [torch.cuda.Event() for _ in range(nbuf)]
+    host_out = [None] * nbuf
+    keep = [None] * nbuf
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
     d2h = 0
-    for i in range(e2e_steps + 1):
-        flush.zero_()
-        rec = i > 0
-        if rec:
-            e_start[i - 1].record()
-        for dst, src in ((dq_, hq), (dk_, hk), (dv_, hv), (dd_, hd), (di_, hids)):
-            dst.copy_(src, non_blocking=True)
+
+    def e2e_step(i):
+        nonlocal d2h
+        b = i % nbuf
+        with torch.cuda.stream(h2d_s):
+            h2d_s.wait_event(in_free[b])
+            for dst, src in zip(dev_in[b], host_in):
+                dst.copy_(src, non_blocking=True)
+            in_ready[b].record(h2d_s)
+        comp_s.wait_event(in_ready[b])
+        dq_, dk_, dv_, dd_, di_ = dev_in[b]
         qi_ = di_[:, w.q_global_start:w.q_global_start + Lq].contiguous()
         out, lse, grads = step(dq_, dk_, dv_, dd_, di_, qi_)
+        in_free[b].record(comp_s)
+        out_ready[b].record(comp_s)
         results = (out, lse) + tuple(grads)
-        if res_host is None:
-            res_host = [torch.empty(r.shape, dtype=r.dtype, pin_memory=True) for r in results]
+        if host_out[b] is None:
+            host_out[b] = [torch.empty(r.shape, dtype=r.dtype, pin_memory=True) for r in results]
             d2h = sum(r.numel() * r.element_size() for r in results)
-        for hdst, r in zip(res_host, results):
-            hdst.copy_(r, non_blocking=True)
-        if rec:
-            e_stop[i - 1].record()
+        with torch.cuda.stream(d2h_s):
+            d2h_s.wait_event(out_ready[b])
+            for hdst, r in zip(host_out[b], results):
+                r.record_stream(d2h_s)
+                hdst.copy_(r, non_blocking=True)
+        keep[b] = results
+
+    for i in range(nbuf):  # warm the pipeline (pinned buffers, allocator)
+        e2e_step(i)
     torch.cuda.synchronize()
-    e2e_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(e_start, e_stop))
+    e2e_steps = max(3, min(args.steps, 50))
+    e_start, e_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e_start.record(comp_s)
+    h2d_s.wait_event(e_start)
+    for i in range(e2e_steps):
+        e2e_step(i)
+    d2h_done = torch.cuda.Event()
+    d2h_done.record(d2h_s)
+    comp_s.wait_event(d2h_done)
+    e_stop.record(comp_s)
+    torch.cuda.synchronize()
+    e2e_ms = e_start.elapsed_time(e_stop) / e2e_steps
     if dist:
         t = torch.tensor([e2e_ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -430,7 +461,8 @@ def our_arm(args):
         "ms_per_step_eager": statistics.mean(eager_steps),
         "roofline": roofline, "roofline_other": dict(roof[other], kernel=other),
         "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
-                "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms},
+                "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms,
+                "timing": "steps pipelined: uploads and downloads overlap neighbouring steps' compute"},
         "gpu_launches": 7 * args.steps,
         "clocks": clocks,
     }
