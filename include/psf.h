@@ -278,7 +278,8 @@ int psf_build_cross_segments(const int32_t* kv_doc_ids, int B, int S, int q_star
  *  + o_new exp(l_new - l) (both -inf gives o = 0, l = -inf); other rows are not
  *  touched. Running output: o_acc fp32 [T, H, D] (nullable) and/or o_run dtype
  *  [T, H, D] (nullable), read from o_acc when given, written to both; l_acc fp32
- *  [H, T] in place. o_new dtype [T, H, D], l_new fp32 [H, T].
+ *  [H, T] in place. o_new dtype [T, H, D], l_new fp32 [H, T]. No two of o_acc,
+ *  o_run, o_new alias one another, nor l_acc and l_new.
  *  Segments: nseg (or dev_meta[0], capped at nseg, when dev_meta is given).
  */
 int psf_lse_merge_live_rows(float* o_acc, void* o_run, float* l_acc, const void* o_new, const float* l_new,
@@ -292,6 +293,7 @@ int psf_lse_merge_live_rows(float* o_acc, void* o_run, float* l_acc, const void*
  *                            of a chunk's packed gradient into the full one]
  *  dst += src on the live rows of (cu_q, cu_k) (as in psf_lse_merge_live_rows),
  *  dtype [T, H, D] both, added in fp32 and rounded once; other rows untouched.
+ *  dst and src do not alias.
  */
 int psf_grad_add_live_rows(void* dst, const void* src, const int32_t* cu_q, const int32_t* cu_k,
                            const int32_t* dev_meta, int nseg, int T, int H, int D, int dtype, void* stream);

@@ -527,15 +527,34 @@ __global__ void __launch_bounds__(kScanThreads) cross_segments_kernel(const int3
   if (Lq > 0 && Lk > 0) {
     const int d = row[q0];
     if (d != 0) {
+      // Eight loads in flight per thread and pass.
       int last = k0 - 1;
-      for (int p = k0 + tid; p < q0; p += blockDim.x)
-        if (row[p] != d) last = max(last, p);
+      for (int p0 = k0 + tid; p0 < q0; p0 += 8 * blockDim.x) {
+        int v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int p = p0 + u * blockDim.x;
+          v[u] = p < q0 ? row[p] : d;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          if (v[u] != d) last = max(last, p0 + u * (int)blockDim.x);
+      }
       last = block_max(last);
       if (last + 1 < k0 + Lk) {
         ks = last + 1;
         int first = -(q0 + Lq);  // block_max of the negated first position with another id
-        for (int p = q0 + tid; p < q0 + Lq; p += blockDim.x)
-          if (row[p] != d) first = max(first, -p);
+        for (int p0 = q0 + tid; p0 < q0 + Lq; p0 += 8 * blockDim.x) {
+          int v[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int p = p0 + u * blockDim.x;
+            v[u] = p < q0 + Lq ? row[p] : d;
+          }
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            if (v[u] != d) first = max(first, -(p0 + u * (int)blockDim.x));
+        }
         nq = -block_max(first) - q0;
       }
     }
@@ -574,89 +593,133 @@ __device__ __forceinline__ int live_segment(const int32_t* cu_q, const int32_t* 
 }
 
 // In-place merge of one chunk's (o_new, l_new) into the running result on the
-// query rows of the chunk's segments with keys; a warp per (row, head). The
-// running output is read from o_acc (fp32) when given, else from o_run (bf16);
-// both are written when given.
-template <typename E>
-__global__ void lse_merge_live_kernel(float* o_acc, E* o_run, float* l_acc, const E* o_new,
-                                      const float* l_new, const int32_t* cu_q, const int32_t* cu_k,
-                                      const int32_t* dev_meta, int nseg_cap, int T, int H, int D) {
+// query rows of the chunk's segments with keys. A warp takes one row at a time
+// (one segment lookup per row) and its heads 32 at a time: lane i merges the
+// lse of head hb + i, which only it reads and writes, then the warp streams the
+// heads' 8-element pieces, four (two with kAcc) per lane in flight, each
+// taking its weights from the head's lane by shuffle. kAcc: the running output is read from o_acc
+// (fp32) and written to it and to o_run when given; otherwise it is read from
+// and written to o_run (E).
+template <typename E, bool kAcc>
+__global__ void __launch_bounds__(256, 4)
+    lse_merge_live_kernel(float* __restrict__ o_acc, E* __restrict__ o_run, float* __restrict__ l_acc,
+                          const E* __restrict__ o_new, const float* __restrict__ l_new, const int32_t* cu_q,
+                          const int32_t* cu_k, const int32_t* dev_meta, int nseg_cap, int T, int H, int D) {
+  constexpr int U = kAcc ? 2 : 4;
   const int nseg = dev_meta ? min(dev_meta[0], nseg_cap) : nseg_cap;
+  const int G = D / 8;  // pieces per head
   const int lane = threadIdx.x & 31;
-  const int64_t nw = (int64_t)gridDim.x * (blockDim.x / 32);
-  for (int64_t w = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) / 32; w < (int64_t)T * H; w += nw) {
-    const int t = (int)(w / H), h = (int)(w - (int64_t)t * H);
+  const int nw = gridDim.x * (blockDim.x / 32);
+  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) / 32; t < T; t += nw) {
     if (live_segment(cu_q, cu_k, nseg, t) < 0) continue;
-    const float a = l_acc[(int64_t)h * T + t], c = l_new[(int64_t)h * T + t];
-    const float m = fmaxf(a, c);
-    const float l = m == -CUDART_INF_F ? -CUDART_INF_F : m + logf(expf(a - m) + expf(c - m));
-    const float wa = l == -CUDART_INF_F ? 0.f : expf(a - l), wc = l == -CUDART_INF_F ? 0.f : expf(c - l);
-    const int64_t off = ((int64_t)t * H + h) * D;
-    for (int d = lane * 8; d < D; d += 256) {
-      float x[8];
-      if (o_acc) {
-        const float4 u0 = *reinterpret_cast<const float4*>(o_acc + off + d);
-        const float4 u1 = *reinterpret_cast<const float4*>(o_acc + off + d + 4);
-        x[0] = u0.x; x[1] = u0.y; x[2] = u0.z; x[3] = u0.w; x[4] = u1.x; x[5] = u1.y; x[6] = u1.z; x[7] = u1.w;
-      } else {
-        const uint4 u = *reinterpret_cast<const uint4*>(o_run + off + d);
-        const uint32_t* pr = reinterpret_cast<const uint32_t*>(&u);
+    for (int hb = 0; hb < H; hb += 32) {
+      const int h = hb + lane;
+      float wa = 0.f, wc = 0.f;
+      if (h < H) {
+        const float a = l_acc[(int64_t)h * T + t], c = l_new[(int64_t)h * T + t];
+        const float m = fmaxf(a, c);
+        const float l = m == -CUDART_INF_F ? -CUDART_INF_F : m + logf(expf(a - m) + expf(c - m));
+        if (l != -CUDART_INF_F) {
+          wa = expf(a - l);
+          wc = expf(c - l);
+        }
+        l_acc[(int64_t)h * T + t] = l;
+      }
+      const int n = min(32, H - hb) * G;
+      const int64_t base = ((int64_t)t * H + hb) * D;
+      for (int k0 = 0; k0 < n; k0 += 32 * U) {  // the same trip count on every lane
+        const int i0 = k0 + lane;
+        uint4 un[U], ur[U];
+        float4 fa[U][2];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float2 f = unpack2<E>(pr[j]);
-          x[2 * j] = f.x;
-          x[2 * j + 1] = f.y;
+        for (int u = 0; u < U; ++u) {
+          const int i = i0 + 32 * u;
+          if (i >= n) continue;
+          const int64_t off = base + (int64_t)i * 8;
+          if constexpr (kAcc) {
+            fa[u][0] = reinterpret_cast<const float4*>(o_acc + off)[0];
+            fa[u][1] = reinterpret_cast<const float4*>(o_acc + off)[1];
+          } else {
+            ur[u] = *reinterpret_cast<const uint4*>(o_run + off);
+          }
+          un[u] = *reinterpret_cast<const uint4*>(o_new + off);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int i = i0 + 32 * u;
+          const int src = min(i, n - 1) / G;  // every lane takes part in the shuffles
+          const float w_a = __shfl_sync(0xffffffffu, wa, src), w_c = __shfl_sync(0xffffffffu, wc, src);
+          if (i >= n) continue;
+          const int64_t off = base + (int64_t)i * 8;
+          float x8[8];
+          if constexpr (kAcc) {
+            x8[0] = fa[u][0].x; x8[1] = fa[u][0].y; x8[2] = fa[u][0].z; x8[3] = fa[u][0].w;
+            x8[4] = fa[u][1].x; x8[5] = fa[u][1].y; x8[6] = fa[u][1].z; x8[7] = fa[u][1].w;
+          } else {
+            const uint32_t* pr = reinterpret_cast<const uint32_t*>(&ur[u]);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const float2 f = unpack2<E>(pr[j]);
+              x8[2 * j] = f.x;
+              x8[2 * j + 1] = f.y;
+            }
+          }
+          const uint32_t* pn = reinterpret_cast<const uint32_t*>(&un[u]);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float2 f = unpack2<E>(pn[j]);
+            x8[2 * j] = w_a * x8[2 * j] + w_c * f.x;
+            x8[2 * j + 1] = w_a * x8[2 * j + 1] + w_c * f.y;
+          }
+          if constexpr (kAcc) {
+            reinterpret_cast<float4*>(o_acc + off)[0] = make_float4(x8[0], x8[1], x8[2], x8[3]);
+            reinterpret_cast<float4*>(o_acc + off)[1] = make_float4(x8[4], x8[5], x8[6], x8[7]);
+          }
+          if (!kAcc || o_run)
+            *reinterpret_cast<uint4*>(o_run + off) =
+                make_uint4(pack2<E>(x8[0], x8[1]), pack2<E>(x8[2], x8[3]), pack2<E>(x8[4], x8[5]), pack2<E>(x8[6], x8[7]));
         }
       }
-      const uint4 un = *reinterpret_cast<const uint4*>(o_new + off + d);
-      const uint32_t* pn = reinterpret_cast<const uint32_t*>(&un);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float2 f = unpack2<E>(pn[j]);
-        x[2 * j] = wa * x[2 * j] + wc * f.x;
-        x[2 * j + 1] = wa * x[2 * j + 1] + wc * f.y;
-      }
-      if (o_acc) {
-        *reinterpret_cast<float4*>(o_acc + off + d) = make_float4(x[0], x[1], x[2], x[3]);
-        *reinterpret_cast<float4*>(o_acc + off + d + 4) = make_float4(x[4], x[5], x[6], x[7]);
-      }
-      if (o_run) {
-        uint4 r;
-        uint32_t* rp = reinterpret_cast<uint32_t*>(&r);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) rp[j] = pack2<E>(x[2 * j], x[2 * j + 1]);
-        *reinterpret_cast<uint4*>(o_run + off + d) = r;
-      }
     }
-    if (lane == 0) l_acc[(int64_t)h * T + t] = l;
   }
 }
 
-// dst += src (bf16, added in fp32, rounded once) on the query rows of the
-// segments with keys; a warp per (row, head).
+// dst += src (E, added in fp32, rounded once) on the query rows of the
+// segments with keys. A warp takes one row at a time (one segment lookup per
+// row) and walks its H*D/8 16-byte pieces with four pieces per lane in flight.
 template <typename E>
-__global__ void grad_add_live_kernel(E* dst, const E* src, const int32_t* cu_q,
+__global__ void grad_add_live_kernel(E* __restrict__ dst, const E* __restrict__ src, const int32_t* cu_q,
                                      const int32_t* cu_k, const int32_t* dev_meta, int nseg_cap, int T, int H, int D) {
   const int nseg = dev_meta ? min(dev_meta[0], nseg_cap) : nseg_cap;
+  const int per_row = H * (D / 8);
   const int lane = threadIdx.x & 31;
-  const int64_t nw = (int64_t)gridDim.x * (blockDim.x / 32);
-  for (int64_t w = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) / 32; w < (int64_t)T * H; w += nw) {
-    const int t = (int)(w / H);
+  const int nw = gridDim.x * (blockDim.x / 32);
+  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) / 32; t < T; t += nw) {
     if (live_segment(cu_q, cu_k, nseg, t) < 0) continue;
-    const int64_t off = w * D;
-    for (int d = lane * 8; d < D; d += 256) {
-      const uint4 ua = *reinterpret_cast<const uint4*>(dst + off + d);
-      const uint4 ub = *reinterpret_cast<const uint4*>(src + off + d);
-      const uint32_t* pa = reinterpret_cast<const uint32_t*>(&ua);
-      const uint32_t* pb = reinterpret_cast<const uint32_t*>(&ub);
-      uint4 r;
-      uint32_t* rp = reinterpret_cast<uint32_t*>(&r);
+    uint4* a = reinterpret_cast<uint4*>(dst) + (int64_t)t * per_row;
+    const uint4* b = reinterpret_cast<const uint4*>(src) + (int64_t)t * per_row;
+    for (int i0 = lane; i0 < per_row; i0 += 128) {
+      uint4 ua[4], ub[4];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float2 fa = unpack2<E>(pa[j]), fb = unpack2<E>(pb[j]);
-        rp[j] = pack2<E>(fa.x + fb.x, fa.y + fb.y);
-      }
-      *reinterpret_cast<uint4*>(dst + off + d) = r;
+      for (int u = 0; u < 4; ++u)
+        if (i0 + 32 * u < per_row) {
+          ua[u] = a[i0 + 32 * u];
+          ub[u] = b[i0 + 32 * u];
+        }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (i0 + 32 * u < per_row) {
+          const uint32_t* pa = reinterpret_cast<const uint32_t*>(&ua[u]);
+          const uint32_t* pb = reinterpret_cast<const uint32_t*>(&ub[u]);
+          uint4 r;
+          uint32_t* rp = reinterpret_cast<uint32_t*>(&r);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float2 fa = unpack2<E>(pa[j]), fb = unpack2<E>(pb[j]);
+            rp[j] = pack2<E>(fa.x + fb.x, fa.y + fb.y);
+          }
+          a[i0 + 32 * u] = r;
+        }
     }
   }
 }
@@ -768,20 +831,26 @@ cudaError_t launch_cross_segments(const int32_t* ids, int B, int S, int q0, int 
 cudaError_t launch_lse_merge_live(float* o_acc, void* o_run, float* l_acc, const void* o_new, const float* l_new,
                                   const int32_t* cu_q, const int32_t* cu_k, const int32_t* dev_meta, int nseg, int T,
                                   int H, int D, int f16, cudaStream_t st) {
-  const int grid = grid_for((int64_t)T * H * 32, 256);
-  if (f16)
-    lse_merge_live_kernel<__half><<<grid, 256, 0, st>>>(o_acc, static_cast<__half*>(o_run), l_acc,
-                                                        static_cast<const __half*>(o_new), l_new, cu_q, cu_k, dev_meta,
-                                                        nseg, T, H, D);
-  else
-    lse_merge_live_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(o_acc, static_cast<__nv_bfloat16*>(o_run), l_acc,
-                                                               static_cast<const __nv_bfloat16*>(o_new), l_new, cu_q,
-                                                               cu_k, dev_meta, nseg, T, H, D);
+  const int grid = grid_for((int64_t)T * 32, 256);
+  auto go = [&](auto kern, auto* run, auto* onew) {
+    kern<<<grid, 256, 0, st>>>(o_acc, run, l_acc, onew, l_new, cu_q, cu_k, dev_meta, nseg, T, H, D);
+  };
+  if (f16) {
+    __half* run = static_cast<__half*>(o_run);
+    const __half* onew = static_cast<const __half*>(o_new);
+    if (o_acc) go(lse_merge_live_kernel<__half, true>, run, onew);
+    else go(lse_merge_live_kernel<__half, false>, run, onew);
+  } else {
+    __nv_bfloat16* run = static_cast<__nv_bfloat16*>(o_run);
+    const __nv_bfloat16* onew = static_cast<const __nv_bfloat16*>(o_new);
+    if (o_acc) go(lse_merge_live_kernel<__nv_bfloat16, true>, run, onew);
+    else go(lse_merge_live_kernel<__nv_bfloat16, false>, run, onew);
+  }
   return cudaGetLastError();
 }
 cudaError_t launch_grad_add_live(void* dst, const void* src, const int32_t* cu_q, const int32_t* cu_k,
                                  const int32_t* dev_meta, int nseg, int T, int H, int D, int f16, cudaStream_t st) {
-  const int grid = grid_for((int64_t)T * H * 32, 256);
+  const int grid = grid_for((int64_t)T * 32, 256);
   if (f16)
     grad_add_live_kernel<__half><<<grid, 256, 0, st>>>(static_cast<__half*>(dst), static_cast<const __half*>(src), cu_q,
                                                        cu_k, dev_meta, nseg, T, H, D);
