@@ -405,6 +405,7 @@ __global__ void lse_merge_kernel(const E* o1, const float* l1, const E* o2, cons
 // (row, head); then grid-stride zeroing of the fp32 accumulators. When dK/dV
 // are written directly (no accumulators), rows no segment covers are zeroed.
 // Delta = rowsum(dO * O) and the zeroed accumulators; blocks bid of nblk.
+constexpr int kDeltaUnroll = 2;
 template <typename E>
 __device__ void bwd_pre_body(SegInfo g, const E* dout, const E* out, int64_t o_sb,
                              int64_t o_ss, int64_t o_sh, float* delta, float* dq_acc, int Hq, int Dqk, int Dv,
@@ -416,32 +417,51 @@ __device__ void bwd_pre_body(SegInfo g, const E* dout, const E* out, int64_t o_s
   const int lane = threadIdx.x & 31;
   const int sub = lane % lanes, grp = lane / lanes, per_warp = 32 / lanes;
   const int64_t nwarps = (int64_t)nblk * (blockDim.x / 32);
-  for (int64_t base = (bid * (int64_t)blockDim.x + threadIdx.x) / 32 * per_warp; base < rows * Hq;
-       base += nwarps * per_warp) {
-    const int64_t wrk = base + grp;
-    float acc = 0.f;
-    int64_t f = 0;
-    int h = 0;
-    if (wrk < rows * Hq) {
-      h = (int)(wrk % Hq);
-      f = wrk / Hq;
-      const int b = (int)(f / g.Sq), s = (int)(f - (int64_t)b * g.Sq);
-      const int64_t off = b * o_sb + (int64_t)s * o_ss + h * o_sh;
-      for (int d = sub * 8; d < Dv; d += lanes * 8) {
-        uint4 ug = *reinterpret_cast<const uint4*>(dout + off + d);
-        uint4 uo = *reinterpret_cast<const uint4*>(out + off + d);
-        const uint32_t* pg = reinterpret_cast<const uint32_t*>(&ug);
-        const uint32_t* po = reinterpret_cast<const uint32_t*>(&uo);
+  const int64_t n = rows * Hq, stride = nwarps * per_warp;
+  // kDeltaUnroll (row, head) pairs per lane group and pass, all loads issued together.
+  constexpr int U = kDeltaUnroll;
+  for (int64_t base = (bid * (int64_t)blockDim.x + threadIdx.x) / 32 * per_warp; base < n; base += stride * U) {
+    float acc[U];
+    int64_t off[U];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float2 x = unpack2<E>(pg[j]), y = unpack2<E>(po[j]);
-          acc = fmaf(x.x, y.x, acc);
-          acc = fmaf(x.y, y.y, acc);
+    for (int u = 0; u < U; ++u) {
+      acc[u] = 0.f;
+      const int64_t wrk = base + u * stride + grp;
+      const int64_t f = wrk / Hq;
+      const int h = (int)(wrk - f * Hq);
+      const int b = (int)(f / g.Sq), s = (int)(f - (int64_t)b * g.Sq);
+      off[u] = wrk < n && grp < per_warp ? b * o_sb + (int64_t)s * o_ss + h * o_sh : -1;
+    }
+    for (int d = sub * 8; d < Dv; d += lanes * 8) {
+      uint4 ug[U], uo[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        if (off[u] >= 0) {
+          ug[u] = *reinterpret_cast<const uint4*>(dout + off[u] + d);
+          uo[u] = *reinterpret_cast<const uint4*>(out + off[u] + d);
         }
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        if (off[u] >= 0) {
+          const uint32_t* pg = reinterpret_cast<const uint32_t*>(&ug[u]);
+          const uint32_t* po = reinterpret_cast<const uint32_t*>(&uo[u]);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float2 x = unpack2<E>(pg[j]), y = unpack2<E>(po[j]);
+            acc[u] = fmaf(x.x, y.x, acc[u]);
+            acc[u] = fmaf(x.y, y.y, acc[u]);
+          }
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      for (int o = lanes / 2; o > 0; o >>= 1) acc[u] += __shfl_xor_sync(0xffffffffu, acc[u], o);
+      const int64_t wrk = base + u * stride + grp;
+      if (sub == 0 && off[u] >= 0) {
+        const int64_t f = wrk / Hq;
+        delta[(int64_t)(wrk - f * Hq) * rows + f] = acc[u];
       }
     }
-    for (int o = lanes / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    if (sub == 0 && wrk < rows * Hq) delta[(int64_t)h * rows + f] = acc;
   }
   const int64_t tid = bid * (int64_t)blockDim.x + threadIdx.x;
   const int64_t nthr = (int64_t)nblk * blockDim.x;
@@ -474,41 +494,56 @@ __device__ void bwd_pre_body(SegInfo g, const E* dout, const E* out, int64_t o_s
   }
 }
 
-// bf16 out = scale * fp32 accumulator ([rows][H][D], packed) in the tensor's own layout.
+// E out = scale * fp32 accumulator ([rows][H][D], packed) in the tensor's own
+// layout, for packed row f of a warp: the row's H*D/8 pieces, four per lane in
+// flight.
 template <typename E>
-__device__ __forceinline__ void convert_rows(const float* acc, E* dst, int64_t x, int Sr, int H, int D,
-                                             int64_t sb, int64_t ss, int64_t sh, float scale) {
-  const int groups = D / 8;
-  const int gidx = (int)(x % groups);
-  const int64_t rh = x / groups;
-  const int h = (int)(rh % H);
-  const int64_t f = rh / H;
+__device__ __forceinline__ void convert_row(const float* __restrict__ acc, E* __restrict__ dst, int64_t f, int Sr,
+                                            int H, int D, int64_t sb, int64_t ss, int64_t sh, float scale) {
+  const int G = D / 8, n = H * G, lane = threadIdx.x & 31;
   const int b = (int)(f / Sr), s = (int)(f - (int64_t)b * Sr);
-  const float4 a = reinterpret_cast<const float4*>(acc + rh * D)[2 * gidx];
-  const float4 c = reinterpret_cast<const float4*>(acc + rh * D)[2 * gidx + 1];
-  reinterpret_cast<uint4*>(dst + b * sb + (int64_t)s * ss + h * sh)[gidx] =
-      make_uint4(pack2<E>(a.x * scale, a.y * scale), pack2<E>(a.z * scale, a.w * scale),
-                 pack2<E>(c.x * scale, c.y * scale), pack2<E>(c.z * scale, c.w * scale));
+  const float4* src = reinterpret_cast<const float4*>(acc + f * H * D);
+  E* row = dst + b * sb + (int64_t)s * ss;
+  for (int i0 = lane; i0 < n; i0 += 128) {
+    float4 a[4], c[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (i0 + 32 * u < n) {
+        a[u] = src[2 * (i0 + 32 * u)];
+        c[u] = src[2 * (i0 + 32 * u) + 1];
+      }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = i0 + 32 * u;
+      if (i >= n) continue;
+      const int h = i / G, gi = i - h * G;
+      reinterpret_cast<uint4*>(row + h * sh)[gi] =
+          make_uint4(pack2<E>(a[u].x * scale, a[u].y * scale), pack2<E>(a[u].z * scale, a[u].w * scale),
+                     pack2<E>(c[u].x * scale, c[u].y * scale), pack2<E>(c[u].z * scale, c[u].w * scale));
+    }
+  }
 }
 
-// dQ = scale * dQacc, and (when accumulated) dK = scale * dKacc, dV = dVacc.
+// dQ = scale * dQacc, and (when accumulated) dK = scale * dKacc, dV = dVacc;
+// a warp per packed row of dQ, then of dK, then of dV.
 template <typename E>
-__global__ void bwd_convert_kernel(const float* dq_acc, E* dq, int64_t nq, int Sq, int Hq, int Dqk,
+__global__ void __launch_bounds__(256, 4) bwd_convert_kernel(const float* dq_acc, E* dq, int64_t nq, int Sq, int Hq, int Dqk,
                                    int64_t q_sb, int64_t q_ss, int64_t q_sh, const float* dk_acc, E* dk,
                                    const float* dv_acc, E* dv, int64_t nk, int Sk, int Hkv, int Dv,
                                    int64_t k_sb, int64_t k_ss, int64_t k_sh, int64_t v_sb, int64_t v_ss, int64_t v_sh,
                                    float scale) {
-  const int64_t nk_dk = dk_acc ? nk * Hkv * (Dqk / 8) : 0;
-  const int64_t nk_dv = dk_acc ? nk * Hkv * (Dv / 8) : 0;
-  const int64_t nq_all = nq * Hq * (Dqk / 8);
-  const int64_t total = nq_all + nk_dk + nk_dv;
-  for (int64_t x = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; x < total; x += (int64_t)gridDim.x * blockDim.x) {
-    if (x < nq_all)
-      convert_rows(dq_acc, dq, x, Sq, Hq, Dqk, q_sb, q_ss, q_sh, scale);
-    else if (x < nq_all + nk_dk)
-      convert_rows(dk_acc, dk, x - nq_all, Sk, Hkv, Dqk, k_sb, k_ss, k_sh, scale);
-    else
-      convert_rows(dv_acc, dv, x - nq_all - nk_dk, Sk, Hkv, Dv, v_sb, v_ss, v_sh, 1.f);
+  const int64_t nkr = dk_acc ? nk : 0;
+  const int64_t total = nq + 2 * nkr;
+  const int64_t nw = (int64_t)gridDim.x * (blockDim.x / 32);
+  for (int64_t r = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) / 32; r < total; r += nw) {
+    const bool is_q = r < nq, is_k = !is_q && r < nq + nkr;
+    const float* acc = is_q ? dq_acc : is_k ? dk_acc : dv_acc;
+    E* dst = is_q ? dq : is_k ? dk : dv;
+    const int64_t f = is_q ? r : is_k ? r - nq : r - nq - nkr;
+    const int Sr = is_q ? Sq : Sk, H = is_q ? Hq : Hkv, D = is_q || is_k ? Dqk : Dv;
+    const int64_t sb = is_q ? q_sb : is_k ? k_sb : v_sb, ss = is_q ? q_ss : is_k ? k_ss : v_ss;
+    const int64_t sh = is_q ? q_sh : is_k ? k_sh : v_sh;
+    convert_row(acc, dst, f, Sr, H, D, sb, ss, sh, is_q || is_k ? scale : 1.f);
   }
 }
 
@@ -805,8 +840,10 @@ cudaError_t launch_bwd_prep(const SegInfo& g, int G, int Hkv, int split_target, 
                             int64_t o_ss, int64_t o_sh, float* delta, float* dq_acc, int Hq, int Dqk, int Dv,
                             float* dk_acc, float* dv_acc, void* dk, void* dv, int64_t k_sb, int64_t k_ss, int64_t k_sh,
                             int64_t v_sb, int64_t v_ss, int64_t v_sh, int f16, cudaStream_t st) {
+  // One 1024-thread block per SM fits (the schedule block's registers and
+  // shared memory), so the fill takes one wave beside it.
   const int64_t work = (int64_t)g.B * g.Sq * Hq * Dqk / 4 + (int64_t)g.B * g.Sk * Hkv * (Dqk + Dv) / 4;
-  const int fill = min(grid_for(work, kScanThreads), 2 * 152);
+  const int fill = min(grid_for(work, kScanThreads), 152 - 1);
   uint16_t* dk16 = static_cast<uint16_t*>(dk);
   uint16_t* dv16 = static_cast<uint16_t*>(dv);
   if (f16)
@@ -866,8 +903,9 @@ cudaError_t launch_bwd_convert(const float* dq_acc, void* dq, bool have_q, int B
                                int64_t k_sh, int64_t v_sb, int64_t v_ss, int64_t v_sh, float scale, int f16,
                                cudaStream_t st) {
   const int64_t nq = have_q ? (int64_t)B * Sq : 0, nk = (int64_t)B * Sk;
-  const int64_t work = nq * Hq * (Dqk / 8) + (dk_acc ? nk * Hkv * ((Dqk + Dv) / 8) : 0);
-  if (work == 0) return cudaSuccess;
+  const int64_t rows = nq + (dk_acc ? 2 * nk : 0);
+  if (rows == 0) return cudaSuccess;
+  const int64_t work = rows * 32;  // a warp per row
   if (f16)
     bwd_convert_kernel<__half><<<grid_for(work, 256), 256, 0, st>>>(
         dq_acc, static_cast<__half*>(dq), nq, Sq, Hq, Dqk, q_sb, q_ss, q_sh, dk_acc, static_cast<__half*>(dk), dv_acc,
