@@ -17,7 +17,7 @@
 //   PV    one N = D MMA chain over a whole V tile: the B operand is MN-major and
 //         its 64-column chunks are reached through the leading-byte offset.
 //   warps 0-3  softmax, thread t = query row t (TMEM lane t). Pass 1 reads S
-//              and takes the row maximum; pass 2 re-reads S, writes P over the
+//              and takes the row maximum (three-input max); pass 2 re-reads S, writes P over the
 //              S columns it has already read and sums the row. The running
 //              maximum is raised only when it grows by more than 2^8, and only
 //              then is O rescaled (the final division by the row sum cancels
@@ -200,21 +200,23 @@ __global__ void __launch_bounds__(192, 2) attn_fwd_duo_kernel(const __grid_const
           mma_commit(&s_full);
           if (jj == t.nk - 1) mma_commit(&q_empty);
           // O (+)= P V_j once the softmax has written P (and, on a tile's first
-          // key tile, once the previous tile's epilogue has read O).
-          if (!wait_bar(&p_full, kv & 1, ctl)) {
-            ok = false;
-            break;
-          }
-          ++kv;
-          if (jj == 0 && ntile > 0 && !wait_bar(&o_free, (ntile - 1) & 1, ctl)) {
-            ok = false;
-            break;
-          }
+          // key tile, once the previous tile's epilogue has read O). V_j is
+          // waited for first: it lands while the softmax runs, so the wait on
+          // P is the last step before the PV issue.
           sl = it & 1;
           if (!wait_bar(&slot_full[sl], (it >> 1) & 1, ctl)) {
             ok = false;
             break;
           }
+          if (jj == 0 && ntile > 0 && !wait_bar(&o_free, (ntile - 1) & 1, ctl)) {
+            ok = false;
+            break;
+          }
+          if (!wait_bar(&p_full, kv & 1, ctl)) {
+            ok = false;
+            break;
+          }
+          ++kv;
           tc_fence_after();
           const uint32_t v_a = slot_a + sl * C::TILE_BYTES;
 #pragma unroll
@@ -239,7 +241,7 @@ __global__ void __launch_bounds__(192, 2) attn_fwd_duo_kernel(const __grid_const
     const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
     const uint32_t ts = tmem + lane_base + C::T_S, to = tmem + lane_base + C::T_O;
     const float sl2 = p.scale_log2;
-    const float2 sl2x2 = make_float2(sl2, sl2);
+    const float2 sl2x2 = make_float2(sl2, sl2), zero2 = make_float2(0.f, 0.f);
     uint32_t kv = 0, ntile = 0;
     bool ok = true;
     while (ok) {
@@ -292,10 +294,13 @@ __global__ void __launch_bounds__(192, 2) attn_fwd_duo_kernel(const __grid_const
             if (c + 1 < 4) tmem_ld32_async(ts + (c + 1) * 32, nxt);
             const int lo = lo_c - c * 32, hi = hi_c - c * 32;
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              float x = __uint_as_float(cur[e]);
-              if constexpr (MASK) x = (e < lo || e >= hi) ? -CUDART_INF_F : x;
-              m8[e & 7] = fmaxf(m8[e & 7], x);
+            for (int e = 0; e < 32; e += 2) {
+              float x0 = __uint_as_float(cur[e]), x1 = __uint_as_float(cur[e + 1]);
+              if constexpr (MASK) {
+                x0 = (e < lo || e >= hi) ? -CUDART_INF_F : x0;
+                x1 = (e + 1 < lo || e + 1 >= hi) ? -CUDART_INF_F : x1;
+              }
+              m8[(e >> 1) & 7] = fmax3(m8[(e >> 1) & 7], x0, x1);
             }
           }
           return fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
@@ -319,7 +324,7 @@ __global__ void __launch_bounds__(192, 2) attn_fwd_duo_kernel(const __grid_const
         // columns already read (chunk c -> columns [16c, 16c + 16)), and the row sum.
         auto pass2 = [&](auto tag) -> float {
           constexpr bool MASK = decltype(tag)::value;
-          float r8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+          float2 r4[4] = {zero2, zero2, zero2, zero2};
           const float2 nbase = make_float2(-base, -base);
           uint32_t a[32], b[32];
           tmem_ld32_async(ts, a);
@@ -338,15 +343,15 @@ __global__ void __launch_bounds__(192, 2) attn_fwd_duo_kernel(const __grid_const
                 x.x = (2 * e < lo || 2 * e >= hi) ? -CUDART_INF_F : x.x;
                 x.y = (2 * e + 1 < lo || 2 * e + 1 >= hi) ? -CUDART_INF_F : x.y;
               }
-              const float e0 = ex2_approx(x.x), e1 = ex2_approx(x.y);
-              r8[(2 * e) & 7] += e0;
-              r8[(2 * e + 1) & 7] += e1;
-              pk[e] = pack2<T>(e0, e1);
+              const float2 ex = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+              r4[e & 3] = add2(r4[e & 3], ex);
+              pk[e] = pack2<T>(ex.x, ex.y);
             }
             tmem_st16_async(ts + c * 16, pk);
           }
           tmem_wait_st();
-          return ((r8[0] + r8[1]) + (r8[2] + r8[3])) + ((r8[4] + r8[5]) + (r8[6] + r8[7]));
+          const float2 r2 = add2(add2(r4[0], r4[1]), add2(r4[2], r4[3]));
+          return r2.x + r2.y;
         };
         const float rs = masked ? pass2(MaskTag<true>{}) : pass2(MaskTag<false>{});
         tc_fence_before();
