@@ -16,9 +16,9 @@
 //         (D / 64 chunks of 128 rows x 64 columns, 128-byte swizzled each).
 //   PV    one N = D MMA chain over a whole V tile: the B operand is MN-major and
 //         its 64-column chunks are reached through the leading-byte offset.
-//   warps 0-3  softmax, thread t = query row t (TMEM lane t). Pass 1 reads S
-//              and takes the row maximum (three-input max); pass 2 re-reads S, writes P over the
-//              S columns it has already read and sums the row. The running
+//   warps 0-3  softmax, thread t = query row t (TMEM lane t). One pass per
+//              key tile: the row of S into registers, its maximum, then P
+//              written over S's first columns and the row sum. The running
 //              maximum is raised only when it grows by more than 2^8, and only
 //              then is O rescaled (the final division by the row sum cancels
 //              any common factor). The tile's epilogue divides O by the sum and
@@ -278,71 +278,60 @@ __global__ void __launch_bounds__(192, 2) attn_fwd_duo_kernel(const __grid_const
         }
         ++kv;
         tc_fence_after();
-        // Pass 1: row maximum (eight independent chains).
-        auto pass1 = [&](auto tag) -> float {
+        // One pass over the row: the 128 S columns into registers (four loads,
+        // one wait), masked columns set to -inf, the row maximum, then
+        // P = 2^(S * scale * log2 e - base) as packed T over S's first 64
+        // columns and the row sum.
+        float m_new = m_used, alpha = 1.f;
+        auto softmax_tile = [&](auto tag) -> float {
           constexpr bool MASK = decltype(tag)::value;
+          uint32_t s0[32], s1[32], s2[32], s3[32];
+          tmem_ld32_async(ts, s0);
+          tmem_ld32_async(ts + 32, s1);
+          tmem_ld32_async(ts + 64, s2);
+          tmem_ld32_async(ts + 96, s3);
+          tmem_wait_ld32(s0);
+          tmem_wait_ld32(s1);
+          tmem_wait_ld32(s2);
+          tmem_wait_ld32(s3);
+          auto chunk = [&](int c) -> uint32_t(&)[32] { return c == 0 ? s0 : c == 1 ? s1 : c == 2 ? s2 : s3; };
+          if constexpr (MASK) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              uint32_t(&cur)[32] = chunk(c);
+#pragma unroll
+              for (int e = 0; e < 32; ++e)
+                if (c * 32 + e < lo_c || c * 32 + e >= hi_c) cur[e] = 0xff800000u;  // -inf
+            }
+          }
           float m8[8];
 #pragma unroll
           for (int u = 0; u < 8; ++u) m8[u] = -CUDART_INF_F;
-          uint32_t a[32], b[32];
-          tmem_ld32_async(ts, a);
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
-            uint32_t(&cur)[32] = (c & 1) ? b : a;
-            uint32_t(&nxt)[32] = (c & 1) ? a : b;
-            tmem_wait_ld32(cur);
-            if (c + 1 < 4) tmem_ld32_async(ts + (c + 1) * 32, nxt);
-            const int lo = lo_c - c * 32, hi = hi_c - c * 32;
+            uint32_t(&cur)[32] = chunk(c);
 #pragma unroll
-            for (int e = 0; e < 32; e += 2) {
-              float x0 = __uint_as_float(cur[e]), x1 = __uint_as_float(cur[e + 1]);
-              if constexpr (MASK) {
-                x0 = (e < lo || e >= hi) ? -CUDART_INF_F : x0;
-                x1 = (e + 1 < lo || e + 1 >= hi) ? -CUDART_INF_F : x1;
-              }
-              m8[(e >> 1) & 7] = fmax3(m8[(e >> 1) & 7], x0, x1);
+            for (int e = 0; e < 32; e += 4) {
+              const int u = ((c * 32 + e) >> 2) & 7;
+              m8[u] = fmax3(m8[u], __uint_as_float(cur[e]), __uint_as_float(cur[e + 1]));
+              m8[u] = fmax3(m8[u], __uint_as_float(cur[e + 2]), __uint_as_float(cur[e + 3]));
             }
           }
-          return fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
-        };
-        const float mx = (masked ? pass1(MaskTag<true>{}) : pass1(MaskTag<false>{})) * sl2;
-        const float m_new = (mx > m_used + 8.f) ? mx : m_used;
-        const float alpha = (m_new == m_used) ? 1.f : ex2_approx(m_used - m_new);
-        const float base = (m_new == -CUDART_INF_F) ? 0.f : m_new;
-        // O holds PV_{jj-1} already (see the header); rescale it if the maximum moved.
-        if (jj > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t r[32];
-            tmem_ld32(to + c * 32, r);
-#pragma unroll
-            for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-            tmem_st32(to + c * 32, r);
-          }
-        }
-        // Pass 2: P = 2^(S * scale * log2 e - base) as packed bf16 over the S
-        // columns already read (chunk c -> columns [16c, 16c + 16)), and the row sum.
-        auto pass2 = [&](auto tag) -> float {
-          constexpr bool MASK = decltype(tag)::value;
-          float2 r4[4] = {zero2, zero2, zero2, zero2};
+          const float mx =
+              fmaxf(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], fmax3(m8[5], m8[6], m8[7]))) * sl2;
+          m_new = (mx > m_used + 8.f) ? mx : m_used;
+          alpha = (m_new == m_used) ? 1.f : ex2_approx(m_used - m_new);
+          const float base = (m_new == -CUDART_INF_F) ? 0.f : m_new;
           const float2 nbase = make_float2(-base, -base);
-          uint32_t a[32], b[32];
-          tmem_ld32_async(ts, a);
+          float2 r4[4] = {zero2, zero2, zero2, zero2};
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
-            uint32_t(&cur)[32] = (c & 1) ? b : a;
-            uint32_t(&nxt)[32] = (c & 1) ? a : b;
-            tmem_wait_ld32(cur);
-            if (c + 1 < 4) tmem_ld32_async(ts + (c + 1) * 32, nxt);
-            const int lo = lo_c - c * 32, hi = hi_c - c * 32;
+            uint32_t(&cur)[32] = chunk(c);
             uint32_t pk[16];
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
-              float2 x = fma2(make_float2(__uint_as_float(cur[2 * e]), __uint_as_float(cur[2 * e + 1])), sl2x2, nbase);
-              if constexpr (MASK) {
-                x.x = (2 * e < lo || 2 * e >= hi) ? -CUDART_INF_F : x.x;
-                x.y = (2 * e + 1 < lo || 2 * e + 1 >= hi) ? -CUDART_INF_F : x.y;
-              }
+              const float2 x =
+                  fma2(make_float2(__uint_as_float(cur[2 * e]), __uint_as_float(cur[2 * e + 1])), sl2x2, nbase);
               const float2 ex = make_float2(ex2_approx(x.x), ex2_approx(x.y));
               r4[e & 3] = add2(r4[e & 3], ex);
               pk[e] = pack2<T>(ex.x, ex.y);
@@ -353,7 +342,19 @@ __global__ void __launch_bounds__(192, 2) attn_fwd_duo_kernel(const __grid_const
           const float2 r2 = add2(add2(r4[0], r4[1]), add2(r4[2], r4[3]));
           return r2.x + r2.y;
         };
-        const float rs = masked ? pass2(MaskTag<true>{}) : pass2(MaskTag<false>{});
+        const float rs = masked ? softmax_tile(MaskTag<true>{}) : softmax_tile(MaskTag<false>{});
+        // O holds PV_{jj-1} already (see the header); rescale it if the maximum
+        // moved, before PV_jj is released.
+        if (jj > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld32(to + c * 32, r);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+            tmem_st32(to + c * 32, r);
+          }
+        }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&p_full);
