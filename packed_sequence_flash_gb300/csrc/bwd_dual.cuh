@@ -32,9 +32,10 @@
 //   Warps  0 TMA producer, 1 MMA issuer, 2 TMEM allocator, 4-7 compute
 //          (thread = key row: P, dS, then the dK/dV epilogue), 8-11 dQ read-out.
 //   Work   a CTA starts on unit blockIdx.x of the heaviest-first list, then takes
-//          the next untaken unit from a global counter; the producer passes each
-//          unit's index to the other warps through a two-entry ring in shared
-//          memory (-1 = no more work).
+//          the next untaken unit from a global counter; the producer decodes
+//          each unit while the previous one's first step loads and passes its
+//          index and decoded unit to the other warps through a two-entry ring
+//          in shared memory (-1 = no more work).
 // The compute warps load the next step's lse and Delta one step ahead and
 // leave the loads in flight until the step begins.
 #pragma once
@@ -77,6 +78,7 @@ __global__ void __launch_bounds__(512, 1) attn_bwd_dual_kernel(const __grid_cons
   __shared__ uint64_t kv_full, kv_empty, q_full[2], q_empty[2], do_full, do_empty, s_full, dp_full[2], p_full,
       ds_full, ds_free, dq_full, dq_free[2], acc_done, acc_free, drain, work_full[2], work_empty[2];
   __shared__ int work_slot[2];
+  __shared__ BwdItem work_tile[2];
   __shared__ uint32_t tmem_base_smem;
   __shared__ int abort_flag;
 
@@ -121,15 +123,17 @@ __global__ void __launch_bounds__(512, 1) attn_bwd_dual_kernel(const __grid_cons
   const int total = (*p.n_items) * p.Hkv;
   const int G = p.Hq / p.Hkv;
   const uint32_t sbase = smem_u32(smem);
-  // Next work item for the MMA, compute and dQ warps (-1: none left, or abort).
+  // Next work item for the MMA, compute and dQ warps (-1: none left, or
+  // abort), with its decoded unit.
   uint32_t nwork = 0;
-  auto next_work = [&](bool& ok) -> int {
+  auto next_work = [&](bool& ok, BwdItem& t) -> int {
     const int ws = nwork & 1;
     if (!wait_bar(&work_full[ws], (nwork >> 1) & 1, ctl)) {
       ok = false;
       return -1;
     }
     const int w = work_slot[ws];
+    t = work_tile[ws];
     __syncwarp(__activemask());
     if (lane == 0) mbar_arrive(&work_empty[ws]);
     ++nwork;
@@ -145,45 +149,59 @@ __global__ void __launch_bounds__(512, 1) attn_bwd_dual_kernel(const __grid_cons
       tma_prefetch_desc(&p.tm_do);
       uint32_t nz = 0, gstep = 0;
       bool ok = true;
+      // Each unit is decoded (two dependent global reads) while the previous
+      // one's first step loads, and published decoded.
       int w = blockIdx.x;
+      BwdItem tw{};
+      if (w < total) tw = bwd_decode(p, w);
       while (ok) {
         if (w >= total) w = -1;
         const int ws = nwork & 1;
         if (!wait_bar(&work_empty[ws], ((nwork >> 1) & 1) ^ 1, ctl)) break;
         work_slot[ws] = w;
+        work_tile[ws] = tw;
         mbar_arrive(&work_full[ws]);
         ++nwork;
         if (w < 0) break;
-        const BwdItem t = bwd_decode(p, w);
-        w = gridDim.x + atomicAdd(p.work_next, 1);
-        if (t.k1 == t.k0) continue;
-        if (!wait_bar(&kv_empty, (nz & 1) ^ 1, ctl)) break;
-        mbar_arrive_expect_tx(&kv_full, (C::KCH + C::VCH) * kChunkBytes);
-        const int fk = t.ck0 + t.kt * kBN, bk = fk / p.seg.Sk, sk = fk - bk * p.seg.Sk;
-        for (int c = 0; c < C::KCH; ++c)
-          tma_load_4d(smem + C::K_OFF + c * kChunkBytes, &p.tm_k, &kv_full, c * 64, sk, t.hk, bk);
-        for (int c = 0; c < C::VCH; ++c)
-          tma_load_4d(smem + C::V_OFF + c * kChunkBytes, &p.tm_v, &kv_full, c * 64, sk, t.hk, bk);
-        ++nz;
-        for (int k = t.k0; k < t.k1; ++k, ++gstep) {
-          const int h = t.hk * G + k / t.nqt, qt = t.qt0 + k % t.nqt;
-          const int fq = t.cq0 + qt * kBM, bq = fq / p.seg.Sq, sq = fq - bq * p.seg.Sq;
-          const int qs = gstep & 1;
-          if (!wait_bar(&q_empty[qs], ((gstep >> 1) & 1) ^ 1, ctl)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(&q_full[qs], C::KCH * kChunkBytes);
+        const BwdItem t = tw;
+        const int wn = gridDim.x + atomicAdd(p.work_next, 1);
+        bool decoded = false;
+        if (t.k1 > t.k0) {
+          if (!wait_bar(&kv_empty, (nz & 1) ^ 1, ctl)) break;
+          mbar_arrive_expect_tx(&kv_full, (C::KCH + C::VCH) * kChunkBytes);
+          const int fk = t.ck0 + t.kt * kBN, bk = fk / p.seg.Sk, sk = fk - bk * p.seg.Sk;
           for (int c = 0; c < C::KCH; ++c)
-            tma_load_4d(smem + C::Q_OFF + qs * C::Q_SLOT + c * kChunkBytes, &p.tm_q, &q_full[qs], c * 64, sq, h, bq);
-          if (!wait_bar(&do_empty, (gstep & 1) ^ 1, ctl)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(&do_full, C::VCH * kChunkBytes);
+            tma_load_4d(smem + C::K_OFF + c * kChunkBytes, &p.tm_k, &kv_full, c * 64, sk, t.hk, bk);
           for (int c = 0; c < C::VCH; ++c)
-            tma_load_4d(smem + C::DO_OFF + c * kChunkBytes, &p.tm_do, &do_full, c * 64, sq, h, bq);
+            tma_load_4d(smem + C::V_OFF + c * kChunkBytes, &p.tm_v, &kv_full, c * 64, sk, t.hk, bk);
+          ++nz;
+          for (int k = t.k0; k < t.k1; ++k, ++gstep) {
+            const int h = t.hk * G + k / t.nqt, qt = t.qt0 + k % t.nqt;
+            const int fq = t.cq0 + qt * kBM, bq = fq / p.seg.Sq, sq = fq - bq * p.seg.Sq;
+            const int qs = gstep & 1;
+            if (!wait_bar(&q_empty[qs], ((gstep >> 1) & 1) ^ 1, ctl)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&q_full[qs], C::KCH * kChunkBytes);
+            for (int c = 0; c < C::KCH; ++c)
+              tma_load_4d(smem + C::Q_OFF + qs * C::Q_SLOT + c * kChunkBytes, &p.tm_q, &q_full[qs], c * 64, sq, h, bq);
+            if (!wait_bar(&do_empty, (gstep & 1) ^ 1, ctl)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&do_full, C::VCH * kChunkBytes);
+            for (int c = 0; c < C::VCH; ++c)
+              tma_load_4d(smem + C::DO_OFF + c * kChunkBytes, &p.tm_do, &do_full, c * 64, sq, h, bq);
+            if (k == t.k0 && wn < total) {
+              tw = bwd_decode(p, wn);
+              decoded = true;
+            }
+          }
         }
+        if (!ok) break;
+        if (!decoded && wn < total) tw = bwd_decode(p, wn);
+        w = wn;
       }
       if (nz > 0) wait_bar_drain(&kv_full, (nz - 1) & 1, p.limit_ns);
       for (uint32_t i = gstep > 2 ? gstep - 2 : 0; i < gstep; ++i) wait_bar_drain(&q_full[i & 1], (i >> 1) & 1, p.limit_ns);
@@ -203,9 +221,9 @@ __global__ void __launch_bounds__(512, 1) attn_bwd_dual_kernel(const __grid_cons
       uint32_t nz = 0, gstep = 0;
       bool ok = true;
       while (ok) {
-        const int w = next_work(ok);
+        BwdItem t;
+        const int w = next_work(ok, t);
         if (w < 0) break;
-        const BwdItem t = bwd_decode(p, w);
         if (t.k1 == t.k0) continue;
         if (!wait_bar(&kv_full, nz & 1, ctl)) break;
         if (nz > 0 && !wait_bar(&acc_free, (nz - 1) & 1, ctl)) break;
@@ -341,9 +359,9 @@ __global__ void __launch_bounds__(512, 1) attn_bwd_dual_kernel(const __grid_cons
     // -lse * log2(e) (-inf where the row carries no probability, so P = 0).
     auto neg_lse2 = [](float x) { return x == -CUDART_INF_F ? -CUDART_INF_F : -x * 1.4426950408889634f; };
     while (ok) {
-      const int w = next_work(ok);
+      BwdItem t;
+      const int w = next_work(ok, t);
       if (w < 0) break;
-      const BwdItem t = bwd_decode(p, w);
       if (t.k1 == t.k0) continue;
       const int j = t.kt * kBN + r;  // segment-local key index
       const bool valid = j < t.n;
@@ -508,9 +526,9 @@ __global__ void __launch_bounds__(512, 1) attn_bwd_dual_kernel(const __grid_cons
     uint32_t gstep = 0;
     bool ok = true;
     while (ok) {
-      const int w = next_work(ok);
+      BwdItem t;
+      const int w = next_work(ok, t);
       if (w < 0) break;
-      const BwdItem t = bwd_decode(p, w);
       if (t.k1 == t.k0) continue;
       for (int k = t.k0; k < t.k1; ++k, ++gstep) {
         const int h = t.hk * G + k / t.nqt, qt = t.qt0 + k % t.nqt;

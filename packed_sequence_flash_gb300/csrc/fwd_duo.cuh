@@ -30,9 +30,10 @@
 // S_j is ready.
 // Work: each CTA starts on work item blockIdx.x of the heaviest-first list and
 // then takes the next untaken item from a global counter, so SMs that finish
-// early pick up the remaining items. The producer takes the item and passes
-// its index to the MMA and softmax warps through a two-entry ring in shared
-// memory (-1 = no more work).
+// early pick up the remaining items. The producer takes the item, decodes it
+// while the previous item's tiles load, and passes index and decoded tile to
+// the MMA and softmax warps through a two-entry ring in shared memory (-1 = no
+// more work).
 // Both softmax passes exist in two forms: one for tiles that cross a mask edge
 // and one, free of any mask arithmetic, for the rest.
 #pragma once
@@ -69,6 +70,7 @@ __global__ void __launch_bounds__(192, 2) attn_fwd_duo_kernel(const __grid_const
   __shared__ uint64_t q_full, q_empty, slot_full[2], slot_empty[2], s_full, p_full, pv_done, o_free, drain;
   __shared__ uint64_t work_full[2], work_empty[2];
   __shared__ int work_slot[2];
+  __shared__ FwdTile work_tile[2];
   __shared__ uint32_t tmem_base_smem;
   __shared__ int abort_flag;
 
@@ -103,15 +105,17 @@ __global__ void __launch_bounds__(192, 2) attn_fwd_duo_kernel(const __grid_const
   const Ctl ctl{p.status, p.limit_ns, &abort_flag};
   const int total = (*p.n_items) * p.Hq;
   const int G = p.Hq / p.Hkv;
-  // Next work item for the MMA and softmax warps (-1: none left, or abort).
+  // Next work item for the MMA and softmax warps (-1: none left, or abort),
+  // with its decoded tile.
   uint32_t nwork = 0;
-  auto next_work = [&](bool& ok) -> int {
+  auto next_work = [&](bool& ok, FwdTile& t) -> int {
     const int ws = nwork & 1;
     if (!wait_bar(&work_full[ws], (nwork >> 1) & 1, ctl)) {
       ok = false;
       return -1;
     }
     const int w = work_slot[ws];
+    t = work_tile[ws];
     __syncwarp(__activemask());
     if (lane == 0) mbar_arrive(&work_empty[ws]);
     ++nwork;
@@ -136,30 +140,43 @@ __global__ void __launch_bounds__(192, 2) attn_fwd_duo_kernel(const __grid_const
         ++it;
         return true;
       };
+      // Each item is decoded (two dependent global reads) while the previous
+      // one's tiles are still being loaded, and published decoded.
       int w = blockIdx.x;
+      FwdTile tw{};
+      if (w < total) tw = fwd_decode(p, w);
       while (true) {
         if (w >= total) w = -1;
         const int ws = nwork & 1;
         if (!wait_bar(&work_empty[ws], ((nwork >> 1) & 1) ^ 1, ctl)) break;
         work_slot[ws] = w;
+        work_tile[ws] = tw;
         mbar_arrive(&work_full[ws]);
         ++nwork;
         if (w < 0) break;
-        const FwdTile t = fwd_decode(p, w);
-        w = gridDim.x + atomicAdd(p.work_next, 1);
-        if (t.nk == 0) continue;
-        if (!wait_bar(&q_empty, (qcnt & 1) ^ 1, ctl)) break;
-        mbar_arrive_expect_tx(&q_full, C::TILE_BYTES);
-        const int fq = t.cq0 + t.qt * kBM, bq = fq / p.seg.Sq;
-        for (int c = 0; c < C::CH; ++c)
-          tma_load_4d(smem + C::Q_OFF + c * kChunkBytes, &p.tm_q, &q_full, c * 64, fq - bq * p.seg.Sq, t.h, bq);
-        ++qcnt;
-        const int hk = t.h / G;
-        for (int jj = 0; jj < t.nk && ok; ++jj) {
-          const int fk = t.ck0 + (t.kv_t0 + jj) * kBN, bk = fk / p.seg.Sk, sk = fk - bk * p.seg.Sk;
-          ok = load_tile(&p.tm_k, sk, hk, bk) && load_tile(&p.tm_v, sk, hk, bk);
+        const FwdTile t = tw;
+        const int wn = gridDim.x + atomicAdd(p.work_next, 1);
+        bool decoded = false;
+        if (t.nk > 0) {
+          if (!wait_bar(&q_empty, (qcnt & 1) ^ 1, ctl)) break;
+          mbar_arrive_expect_tx(&q_full, C::TILE_BYTES);
+          const int fq = t.cq0 + t.qt * kBM, bq = fq / p.seg.Sq;
+          for (int c = 0; c < C::CH; ++c)
+            tma_load_4d(smem + C::Q_OFF + c * kChunkBytes, &p.tm_q, &q_full, c * 64, fq - bq * p.seg.Sq, t.h, bq);
+          ++qcnt;
+          const int hk = t.h / G;
+          for (int jj = 0; jj < t.nk && ok; ++jj) {
+            const int fk = t.ck0 + (t.kv_t0 + jj) * kBN, bk = fk / p.seg.Sk, sk = fk - bk * p.seg.Sk;
+            ok = load_tile(&p.tm_k, sk, hk, bk) && load_tile(&p.tm_v, sk, hk, bk);
+            if (jj == 0 && wn < total) {
+              tw = fwd_decode(p, wn);
+              decoded = true;
+            }
+          }
+          if (!ok) break;
         }
-        if (!ok) break;
+        if (!decoded && wn < total) tw = fwd_decode(p, wn);
+        w = wn;
       }
       // Wind down: no copy may still be landing in shared memory.
       for (uint32_t i = it > 2u ? it - 2 : 0; i < it; ++i) wait_bar_drain(&slot_full[i & 1], (i >> 1) & 1, p.limit_ns);
@@ -174,9 +191,9 @@ __global__ void __launch_bounds__(192, 2) attn_fwd_duo_kernel(const __grid_const
       uint32_t qcnt = 0, it = 0, kv = 0, ntile = 0;
       bool ok = true;
       while (ok) {
-        const int w = next_work(ok);
+        FwdTile t;
+        const int w = next_work(ok, t);
         if (w < 0) break;
-        const FwdTile t = fwd_decode(p, w);
         if (t.nk == 0) continue;
         if (!wait_bar(&q_full, qcnt & 1, ctl)) break;
         tc_fence_after();
@@ -245,9 +262,9 @@ __global__ void __launch_bounds__(192, 2) attn_fwd_duo_kernel(const __grid_const
     uint32_t kv = 0, ntile = 0;
     bool ok = true;
     while (ok) {
-      const int w = next_work(ok);
+      FwdTile t;
+      const int w = next_work(ok, t);
       if (w < 0) break;
-      const FwdTile t = fwd_decode(p, w);
       const int i = t.qt * kBM + row;  // segment-local query index
       const bool valid = i < t.m;
       const int fq = t.cq0 + i;
