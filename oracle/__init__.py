@@ -60,7 +60,7 @@ def _load():
                                             P, P, P, P, P, P, I, I, I, I, I, I, D,
                                             P, I, P, I, P, P, P, I]
             lib.oracle_attn_bwd.restype = I
-            lib.oracle_build_segments.argtypes = [P, I, I, I, I, P, P, I, P, P]
+            lib.oracle_build_segments.argtypes = [P, I, I, I, I, P, P, I, P, P, I]
             lib.oracle_build_segments.restype = I
             lib.oracle_lse_merge.argtypes = [P, P, P, P, P, P, I, I, I]
             lib.oracle_build_cross_segments.argtypes = [P, I, I, I, I, I, I, P, P, P, P]
@@ -237,20 +237,22 @@ def attn_bwd_dense(dout, q, k, v, out, lse, scale, causal, window=None, nthreads
 # ---------------------------------------------------------------------------
 # segment builder and merge
 
-def build_segments(doc_ids, q_length, q_global_start):
-    """Doc ids [B, Sk] -> (cu_q, cu_k, max_q, max_k) as numpy int32 arrays and ints."""
+def build_segments(doc_ids, q_length, q_global_start, skip_pad=False):
+    """Doc ids [B, Sk] -> (cu_q, cu_k, max_q, max_k) as numpy int32 arrays and ints.
+    skip_pad: every padding piece becomes (its queries, no keys) then (no
+    queries, its keys)."""
     lib = _load()
     doc_ids = _i32(doc_ids)
     if doc_ids.ndim == 1:
         doc_ids = doc_ids[None, :]
     B, Sk = doc_ids.shape
-    cap = 2 * B * Sk + 2
+    cap = 2 * B * (Sk + 1) + 2
     cu_q = np.zeros(cap + 1, dtype=np.int32)
     cu_k = np.zeros(cap + 1, dtype=np.int32)
     mq = np.zeros(1, dtype=np.int32)
     mk = np.zeros(1, dtype=np.int32)
     n = lib.oracle_build_segments(_ptr(doc_ids), B, Sk, int(q_length), int(q_global_start),
-                                  _ptr(cu_q), _ptr(cu_k), cap, _ptr(mq), _ptr(mk))
+                                  _ptr(cu_q), _ptr(cu_k), cap, _ptr(mq), _ptr(mk), 1 if skip_pad else 0)
     if n < 0:
         raise ValueError("oracle_build_segments: capacity exceeded")
     return cu_q[: n + 1].copy(), cu_k[: n + 1].copy(), int(mq[0]), int(mk[0])

@@ -493,9 +493,15 @@ int oracle_attn_bwd(int mode, int causal, int window, const int32_t *cu_q, const
  * Segment builder. doc_ids [B, Sk]; the query shard is [q0, q0 + Lq) of every
  * row. Writes cu_q/cu_k (capacity + 1 entries each) and returns the number of
  * segments, or -1 when capacity is too small.
+ * skip_pad != 0: a piece of a padding run (id 0) becomes two segments, its
+ * queries with no keys and then its keys with no queries, so no padding query
+ * attends anything (out 0, lse -inf, the value padding queries must get) and
+ * the key segments still tile the keys.
+ *   [fa4 page, `document_causal_fa4_attention`: padding queries are zero;
+ *    cp_attention page, `_build_packed_ring_segments`: pad query rows zeroed]
  */
 int oracle_build_segments(const int32_t *doc_ids, int B, int Sk, int Lq, int q0, int32_t *cu_q,
-                          int32_t *cu_k, int capacity, int32_t *max_q, int32_t *max_k) {
+                          int32_t *cu_k, int capacity, int32_t *max_q, int32_t *max_k, int skip_pad) {
     int q_end = q0 + Lq;
     int nseg = 0;
     int mq = 0, mk = 0;
@@ -519,11 +525,21 @@ int oracle_build_segments(const int32_t *doc_ids, int B, int Sk, int Lq, int q0,
                 int hi = pe < q_end ? pe : q_end;
                 int nq = hi > lo ? hi - lo : 0;
                 int nk = pe - pa;
+                if (nq > mq) mq = nq;
+                if (nk > mk) mk = nk;
+                if (skip_pad && ids[a] == 0) {
+                    if (nseg + 2 > capacity) return -1;
+                    cu_q[nseg + 1] = cu_q[nseg] + nq; /* the queries, no keys */
+                    cu_k[nseg + 1] = cu_k[nseg];
+                    ++nseg;
+                    cu_q[nseg + 1] = cu_q[nseg]; /* the keys, no queries */
+                    cu_k[nseg + 1] = cu_k[nseg] + nk;
+                    ++nseg;
+                    continue;
+                }
                 if (nseg >= capacity) return -1;
                 cu_q[nseg + 1] = cu_q[nseg] + nq;
                 cu_k[nseg + 1] = cu_k[nseg] + nk;
-                if (nq > mq) mq = nq;
-                if (nk > mk) mk = nk;
                 ++nseg;
             }
             a = e;

@@ -405,6 +405,83 @@ def test_builder_brute_force_visibility_and_tiling(seed):
     np.testing.assert_array_equal(seg_vis, doc_vis)
 
 
+def test_builder_skip_pad_golden_examples():
+    with open(os.path.join(GOLDEN, "builder_skip_pad_examples.json")) as fh:
+        cases = json.load(fh)["cases"]
+    for c in cases:
+        cu_q, cu_k, mq, mk = oracle.build_segments(c["doc_ids"], c["q_length"], c["q_global_start"], skip_pad=True)
+        assert cu_q.tolist() == c["cu_q"], c
+        assert cu_k.tolist() == c["cu_k"], c
+        assert (mq, mk) == (c["max_q"], c["max_k"]), c
+
+
+@pytest.mark.parametrize("seed", range(25))
+def test_builder_skip_pad_brute_force(seed):
+    # padding queries sit in segments without keys, padding keys in segments
+    # without queries, and every other pair is the doc-id predicate
+    r = np.random.default_rng(seed)
+    B, S = int(r.integers(1, 4)), int(r.integers(1, 20))
+    ids = _random_doc_ids(B, S, 700 + seed, pad_prob=0.35)
+    q0 = int(r.integers(0, S))
+    Lq = int(r.integers(0, S - q0 + 1))
+    cu_q, cu_k, mq, mk = oracle.build_segments(ids, Lq, q0, skip_pad=True)
+    nq, nk = np.diff(cu_q), np.diff(cu_k)
+    assert cu_q[0] == 0 and cu_k[0] == 0 and cu_q[-1] == B * Lq and cu_k[-1] == B * S
+    assert np.all(nq >= 0) and np.all(nk >= 0)
+    assert mq == (nq.max() if len(nq) else 0) and mk == (nk.max() if len(nk) else 0)
+    qid = ids[:, q0:q0 + Lq].reshape(-1)
+    kid = ids.reshape(-1)
+    for s in range(len(nq)):
+        if (qid[cu_q[s]:cu_q[s + 1]] == 0).any():
+            assert nk[s] == 0 and (qid[cu_q[s]:cu_q[s + 1]] == 0).all()
+        if (kid[cu_k[s]:cu_k[s + 1]] == 0).any():
+            assert nq[s] == 0 and (kid[cu_k[s]:cu_k[s + 1]] == 0).all()
+    seg_vis = np.zeros((B * Lq, B * S), bool)
+    for s in range(len(nq)):
+        d = nk[s] - nq[s]
+        for i in range(nq[s]):
+            for j in range(nk[s]):
+                if j <= i + d:
+                    seg_vis[cu_q[s] + i, cu_k[s] + j] = True
+    doc_vis = np.zeros_like(seg_vis)
+    for b in range(B):
+        for i in range(Lq):
+            p = q0 + i
+            if ids[b, p] == 0:
+                continue
+            for j in range(p + 1):
+                if np.all(ids[b, j:p + 1] == ids[b, p]):
+                    doc_vis[b * Lq + i, b * S + j] = True
+    np.testing.assert_array_equal(seg_vis, doc_vis)
+
+
+@pytest.mark.parametrize("seed,window", [(0, None), (1, None), (2, 3), (3, 5)])
+def test_skip_pad_segments_equal_document_mode(seed, window):
+    # the skip-pad segments run through the plain segment oracle, with no pad
+    # fixup afterwards, reproduce the document-mode result (forward and
+    # backward) including the padding rows' zero output and -inf lse
+    r = np.random.default_rng(seed)
+    B, S, Hq, Hkv, D = 2, 24, 2, 1, 8
+    ids = _random_doc_ids(B, S, 900 + seed, pad_prob=0.3)
+    q0 = int(r.integers(0, 12))
+    Lq = int(r.integers(1, S - q0 + 1))
+    q, do = rnd(B * Lq, Hq, D), rnd(B * Lq, Hq, D)
+    k, v = rnd(B * S, Hkv, D), rnd(B * S, Hkv, D)
+    scale = 0.35
+    cu_q, cu_k, _, _ = oracle.build_segments(ids, Lq, q0, skip_pad=True)
+    o, l = oracle.attn_fwd_segments(q, k, v, cu_q, cu_k, scale, True, window)
+    ro, rl = oracle.attn_fwd_document(q, k, v, ids, q0, scale, window)
+    np.testing.assert_allclose(o, ro, atol=1e-12)
+    np.testing.assert_array_equal(np.isneginf(l), np.isneginf(rl))
+    fin = np.isfinite(rl)
+    np.testing.assert_allclose(l[fin], rl[fin], atol=1e-12)
+    assert (ids[:, q0:q0 + Lq].reshape(-1) == 0).sum() == 0 or np.isneginf(rl).any()
+    g = oracle.attn_bwd_segments(do, q, k, v, o, l, cu_q, cu_k, scale, True, window)
+    rg = oracle.attn_bwd_document(do, q, k, v, ro, rl, ids, q0, scale, window)
+    for a, b in zip(g, rg):
+        np.testing.assert_allclose(a, b, atol=1e-10)
+
+
 # ---------------------------------------------------------------------------
 # cross-chunk pins (the one-device core of the ring decomposition)
 
