@@ -210,13 +210,23 @@ int psf_attn_dense_bwd(const void* dout, const void* q, const void* k, const voi
  *  Outputs: cu_q, cu_k (int32, capacity + 1 entries each, prefix sums),
  *  dev_meta int32[3] = {nseg, max_q, max_k}, and seg_is_pad (nullable, uint8
  *  [capacity]: 1 for a segment cut from a padding run).
- *  capacity: room in cu_q / cu_k; B * Sk + B always suffices. Too small a
- *  capacity is a PSF_EDEVICE_ARGS device status (dev_meta[0] is then 0).
+ *  flags: 0, or PSF_SEGMENTS_SKIP_PAD: every piece cut from a padding run is
+ *  written as two segments, its queries with no keys, then its keys with no
+ *  queries. The attention then gives padding queries out = 0 and lse = -inf by
+ *  itself (no psf_pad_fixup needed) and computes no padding-vs-padding pairs;
+ *  dK/dV of padding keys come out 0. Any other bit is PSF_EINVAL.
+ *                           [fa4 page, `document_causal_fa4_attention`: padding
+ *                            queries are zero; cp_attention page,
+ *                            `_build_packed_ring_segments`: pad query rows zeroed]
+ *  capacity: room in cu_q / cu_k; B * Sk + B always suffices without flags,
+ *  2 * (B * Sk + B) with PSF_SEGMENTS_SKIP_PAD. Too small a capacity is a
+ *  PSF_EDEVICE_ARGS device status (dev_meta[0] is then 0).
  *  Requires 0 <= q_global_start, q_global_start + q_length <= Sk.
  */
+#define PSF_SEGMENTS_SKIP_PAD 1
 int psf_build_doc_segments(const int32_t* kv_doc_ids, int B, int Sk, int q_length, int q_global_start,
                            int32_t* cu_q, int32_t* cu_k, int capacity, int32_t* dev_meta, uint8_t* seg_is_pad,
-                           void* stream);
+                           int flags, void* stream);
 
 /*
  * Zero the padding queries of a document-causal result: rows whose query

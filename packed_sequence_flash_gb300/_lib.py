@@ -37,7 +37,7 @@ SIGNATURES = {
                                 P, SZ, P]),
     "psf_attn_dense_fwd": (I, [P, P, P, P, P, I, I, I, I, I, I, I, I, F, I, I32, P, SZ, P]),
     "psf_attn_dense_bwd": (I, [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, F, I, I32, P, SZ, P]),
-    "psf_build_doc_segments": (I, [P, I, I, I, I, P, P, I, P, P, P]),
+    "psf_build_doc_segments": (I, [P, I, I, I, I, P, P, I, P, P, I, P]),
     "psf_pad_fixup": (I, [P, P, P, I, I, I, I, I, P]),
     "psf_lse_merge": (I, [P, P, P, P, P, P, P, I, I, I, I, P]),
     "psf_build_cross_segments": (I, [P, I, I, I, I, I, I, P, P, P, P]),
@@ -49,6 +49,7 @@ PSF_LAYOUT_THD = 0
 PSF_LAYOUT_BHSD = 1
 PSF_DTYPE_BF16 = 0
 PSF_DTYPE_F16 = 1
+PSF_SEGMENTS_SKIP_PAD = 1
 ERRORS = {-1: "PSF_EINVAL", -2: "PSF_EUNSUPPORTED", -3: "PSF_ECUDA", -4: "PSF_EDEVICE_ARGS",
           -5: "PSF_ETIMEOUT", -6: "PSF_EWORKSPACE"}
 

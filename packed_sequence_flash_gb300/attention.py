@@ -18,7 +18,7 @@ from __future__ import annotations
 import torch
 
 from . import _lib
-from ._lib import PSF_DTYPE_BF16, PSF_DTYPE_F16, PSF_LAYOUT_BHSD, PSF_LAYOUT_THD, check
+from ._lib import PSF_DTYPE_BF16, PSF_DTYPE_F16, PSF_LAYOUT_BHSD, PSF_LAYOUT_THD, PSF_SEGMENTS_SKIP_PAD, check
 
 NO_WINDOW = -(2 ** 31)  # the pages' "no window" sentinel
 
@@ -191,25 +191,28 @@ def attn_dense_bwd(dout, q, k, v, out, lse, scale, causal, window=None, workspac
 # ---------------------------------------------------------------------------
 # segment builder, pad fixup, merge
 
-def build_doc_segments(kv_doc_ids, q_length, q_global_start, capacity=None, want_pad_flags=False):
+def build_doc_segments(kv_doc_ids, q_length, q_global_start, capacity=None, want_pad_flags=False, skip_pad=False):
     """Doc ids [B, Sk] int32 (device) -> (cu_q, cu_k, dev_meta, seg_is_pad).
 
     dev_meta = int32 [nseg, max_q, max_k] on the device; cu arrays hold
     capacity + 1 entries of which the first nseg + 1 are meaningful.
+    skip_pad: padding pieces become (their queries, no keys) + (no queries,
+    their keys), so the attention itself zeroes padding queries.
     """
     _i32(kv_doc_ids, "kv_doc_ids")
     if kv_doc_ids.dim() == 1:
         kv_doc_ids = kv_doc_ids[None]
     B, Sk = kv_doc_ids.shape
     if capacity is None:
-        capacity = B * Sk + B
+        capacity = (B * Sk + B) * (2 if skip_pad else 1)
     dev = kv_doc_ids.device
     cu_q = torch.empty(capacity + 1, dtype=torch.int32, device=dev)
     cu_k = torch.empty(capacity + 1, dtype=torch.int32, device=dev)
     meta = torch.empty(3, dtype=torch.int32, device=dev)
     pad = torch.empty(max(capacity, 1), dtype=torch.uint8, device=dev) if want_pad_flags else None
     rc = _lib.load().psf_build_doc_segments(_ptr(kv_doc_ids), B, Sk, int(q_length), int(q_global_start),
-                                            _ptr(cu_q), _ptr(cu_k), int(capacity), _ptr(meta), _ptr(pad), _stream())
+                                            _ptr(cu_q), _ptr(cu_k), int(capacity), _ptr(meta), _ptr(pad),
+                                            PSF_SEGMENTS_SKIP_PAD if skip_pad else 0, _stream())
     check(rc)
     return cu_q, cu_k, meta, pad
 
@@ -292,7 +295,7 @@ def grad_add_live_rows(dst, src, cu_q, cu_k, dev_meta=None):
 # ---------------------------------------------------------------------------
 # document-causal composition [fa4 page, document_causal_fa4_attention]
 
-def document_causal_attention(q, k, v, q_doc_ids, kv_doc_ids, q_global_start, scale, window=None):
+def document_causal_attention(q, k, v, q_doc_ids, kv_doc_ids, q_global_start, scale, window=None, skip_pad=True):
     """Causal per-document attention of a local query shard against global keys.
 
     q [B, Hq, Lq, Dqk], k [B, Hkv, Sk, Dqk], v [B, Hkv, Sk, Dv] (or packed
@@ -300,6 +303,10 @@ def document_causal_attention(q, k, v, q_doc_ids, kv_doc_ids, q_global_start, sc
     int32, 1-based, 0 = padding. Returns (out, lse, segments) where padding
     queries are zero with lse -inf, and segments = (cu_q, cu_k, dev_meta) for
     the backward. No host synchronisation: the segment count stays on the device.
+    skip_pad (default): padding runs get segments without keys for their
+    queries, so the attention writes their zero rows itself and computes no
+    padding pairs; False runs padding runs as ordinary segments and zeroes
+    the padding queries afterwards with pad_fixup (q_doc_ids is read only then).
     """
     layout = "thd" if q.dim() == 3 else "bhsd"
     if kv_doc_ids.dim() == 1:
@@ -307,10 +314,10 @@ def document_causal_attention(q, k, v, q_doc_ids, kv_doc_ids, q_global_start, sc
     if q_doc_ids.dim() == 1:
         q_doc_ids = q_doc_ids[None]
     Lq = q.shape[0] if layout == "thd" else q.shape[2]
-    cu_q, cu_k, meta, _ = build_doc_segments(kv_doc_ids, Lq, q_global_start)
-    cap = cu_q.numel() - 1
+    cu_q, cu_k, meta, _ = build_doc_segments(kv_doc_ids, Lq, q_global_start, skip_pad=skip_pad)
     out, lse = attn_varlen_fwd(q, k, v, cu_q, cu_k, -1, -1, scale, True, window, dev_meta=meta, layout=layout)
-    pad_fixup(out, lse, q_doc_ids, layout)
+    if not skip_pad:
+        pad_fixup(out, lse, q_doc_ids, layout)
     return out, lse, (cu_q, cu_k, meta)
 
 

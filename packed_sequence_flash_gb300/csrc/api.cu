@@ -548,7 +548,8 @@ int psf_attn_dense_bwd(const void* dout, const void* q, const void* k, const voi
 
 int psf_build_doc_segments(const int32_t* kv_doc_ids, int B, int Sk, int q_length, int q_global_start,
                            int32_t* cu_q, int32_t* cu_k, int capacity, int32_t* dev_meta, uint8_t* seg_is_pad,
-                           void* stream) {
+                           int flags, void* stream) {
+  if (flags & ~PSF_SEGMENTS_SKIP_PAD) return fail(PSF_EINVAL, "unknown builder flags 0x%x", flags);
   if (B < 1 || Sk < 0 || q_length < 0 || q_global_start < 0 || (int64_t)q_global_start + q_length > Sk)
     return fail(PSF_EINVAL, "need B >= 1 and 0 <= q_global_start <= q_global_start + q_length <= Sk");
   if ((int64_t)B * (Sk + 1) > 0x7fffffff) return fail(PSF_EINVAL, "too many rows");
@@ -558,7 +559,8 @@ int psf_build_doc_segments(const int32_t* kv_doc_ids, int B, int Sk, int q_lengt
   int rc = device_info(&dev);
   if (rc) return rc;
   cudaError_t e = launch_build_segments(kv_doc_ids, B, Sk, q_length, q_global_start, cu_q, cu_k, capacity, dev_meta,
-                                        seg_is_pad, dev->status, static_cast<cudaStream_t>(stream));
+                                        seg_is_pad, (flags & PSF_SEGMENTS_SKIP_PAD) ? 1 : 0, dev->status,
+                                        static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PSF_OK : cuda_fail(e, "builder launch");
 }
 

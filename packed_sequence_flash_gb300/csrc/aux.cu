@@ -282,7 +282,7 @@ constexpr int kBuildPer = 8;
 __global__ void __launch_bounds__(kScanThreads) build_segments_kernel(const int32_t* ids, int B, int Sk, int Lq,
                                                                       int q0, int32_t* cu_q, int32_t* cu_k,
                                                                       int capacity, int32_t* meta, uint8_t* is_pad,
-                                                                      int* status) {
+                                                                      int skip_pad, int* status) {
   const int tid = threadIdx.x;
   const int q_end = q0 + Lq;
   int offset = 0;
@@ -297,7 +297,7 @@ __global__ void __launch_bounds__(kScanThreads) build_segments_kernel(const int3
         const int j = j0 + e;
         if (j < Sk && (j == 0 || j == q_end || row[j] != row[j - 1])) {
           flags |= 1u << e;
-          ++cnt;
+          cnt += (skip_pad && row[j] == 0) ? 2 : 1;
         }
       }
       int tot;
@@ -306,12 +306,24 @@ __global__ void __launch_bounds__(kScanThreads) build_segments_kernel(const int3
       for (int e = 0; e < kBuildPer; ++e) {
         if (flags & (1u << e)) {
           const int j = j0 + e;
+          const bool pad = row[j] == 0;
           if (idx < capacity) {
             cu_k[idx] = b * Sk + j;
             cu_q[idx] = b * Lq + min(max(j - q0, 0), Lq);
-            if (is_pad) is_pad[idx] = row[j] == 0 ? 1 : 0;
+            if (is_pad) is_pad[idx] = pad ? 1 : 0;
           }
           ++idx;
+          // Padding skip: the piece's queries got no keys above; its keys
+          // start a second segment with no queries, whose query offset is the
+          // next boundary's (filled in below, -1 until then).
+          if (skip_pad && pad) {
+            if (idx < capacity) {
+              cu_k[idx] = b * Sk + j;
+              cu_q[idx] = -1;
+              if (is_pad) is_pad[idx] = 1;
+            }
+            ++idx;
+          }
         }
       }
       offset += tot;
@@ -330,6 +342,12 @@ __global__ void __launch_bounds__(kScanThreads) build_segments_kernel(const int3
     cu_k[nseg] = B * Sk;
   }
   __syncthreads();
+  if (skip_pad) {
+    // A -1 is always followed by a real boundary (or the end), never another -1.
+    for (int i = tid; i < nseg; i += kScanThreads)
+      if (cu_q[i] < 0) cu_q[i] = cu_q[i + 1];
+    __syncthreads();
+  }
   int mq = 0, mk = 0;
   for (int i = tid; i < nseg; i += kScanThreads) {
     mq = max(mq, cu_q[i + 1] - cu_q[i]);
@@ -809,9 +827,10 @@ cudaError_t launch_fwd_prep(const SegInfo& g, int2* items, int* n_items, int* se
   return cudaGetLastError();
 }
 cudaError_t launch_build_segments(const int32_t* ids, int B, int Sk, int Lq, int q0, int32_t* cu_q, int32_t* cu_k,
-                                  int capacity, int32_t* meta, uint8_t* seg_is_pad, int* status, cudaStream_t st) {
+                                  int capacity, int32_t* meta, uint8_t* seg_is_pad, int skip_pad, int* status,
+                                  cudaStream_t st) {
   build_segments_kernel<<<1, kScanThreads, 0, st>>>(ids, B, Sk, Lq, q0, cu_q, cu_k, capacity, meta, seg_is_pad,
-                                                    status);
+                                                    skip_pad, status);
   return cudaGetLastError();
 }
 

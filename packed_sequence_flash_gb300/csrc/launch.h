@@ -37,7 +37,8 @@ int fwd_smem_bytes(int dqk, int dvc);
 int bwd_smem_bytes(int dqk, int dv);
 
 cudaError_t launch_build_segments(const int32_t* ids, int B, int Sk, int Lq, int q0, int32_t* cu_q, int32_t* cu_k,
-                                  int capacity, int32_t* meta, uint8_t* seg_is_pad, int* status, cudaStream_t st);
+                                  int capacity, int32_t* meta, uint8_t* seg_is_pad, int skip_pad, int* status,
+                                  cudaStream_t st);
 cudaError_t launch_pad_fixup(void* out, float* lse, const int32_t* qids, int B, int Lq, int Hq, int Dv,
                              int64_t o_sb, int64_t o_ss, int64_t o_sh, int64_t l_sb, int64_t l_sh, cudaStream_t st);
 cudaError_t launch_lse_merge(const void* o1, const float* l1, const void* o2, const float* l2, float* of, void* ob,

@@ -64,13 +64,14 @@ def assert_grads(got, ref, names=("dq", "dk", "dv"), rows=None):
     return errs
 
 
-def doc_case(w, window=None, check_bwd=True):
+def doc_case(w, window=None, check_bwd=True, skip_pad=True):
     """Run a packed single-row document workload through both paths."""
     q, k, v, do = (cuda(t) for t in (w.q, w.k, w.v, w.dout))
     ids = torch.from_numpy(w.doc_ids).to("cuda")
     Lq = w.q.shape[0]
     qids = ids[:, w.q_global_start:w.q_global_start + Lq].contiguous()
-    out, lse, seg = psf.document_causal_attention(q, k, v, qids, ids, w.q_global_start, w.scale, window)
+    out, lse, seg = psf.document_causal_attention(q, k, v, qids, ids, w.q_global_start, w.scale, window,
+                                                  skip_pad=skip_pad)
     out_o, lse_o = oracle.attn_fwd_document(w.q, w.k, w.v, w.doc_ids, w.q_global_start, w.scale, window)
     assert_fwd(out, lse, out_o, lse_o)
     res = {}

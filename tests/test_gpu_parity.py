@@ -17,9 +17,9 @@ pytestmark = pytest.mark.gpu
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
 
-def _build_gpu(ids, Lq, q0):
+def _build_gpu(ids, Lq, q0, skip_pad=False):
     ids_t = torch.as_tensor(np.asarray(ids, np.int32)).to("cuda")
-    cu_q, cu_k, meta, pad = psf.build_doc_segments(ids_t, Lq, q0, want_pad_flags=True)
+    cu_q, cu_k, meta, pad = psf.build_doc_segments(ids_t, Lq, q0, want_pad_flags=True, skip_pad=skip_pad)
     m = meta.cpu().tolist()
     n = m[0]
     return cu_q[: n + 1].cpu().numpy(), cu_k[: n + 1].cpu().numpy(), m[1], m[2], pad[:n].cpu().numpy()
@@ -58,6 +58,76 @@ def test_builder_random_maps_bit_exact(seed):
     assert (got[2], got[3]) == (ref[2], ref[3])
     starts = ref[1][:-1]
     np.testing.assert_array_equal(got[4], (ids.reshape(-1)[starts] == 0).astype(np.uint8))
+
+
+def test_builder_skip_pad_golden_examples_bit_exact():
+    with open(os.path.join(GOLDEN, "builder_skip_pad_examples.json")) as fh:
+        cases = json.load(fh)["cases"]
+    for c in cases:
+        cu_q, cu_k, mq, mk, pad = _build_gpu(c["doc_ids"], c["q_length"], c["q_global_start"], skip_pad=True)
+        assert cu_q.tolist() == c["cu_q"] and cu_k.tolist() == c["cu_k"], c
+        assert (mq, mk) == (c["max_q"], c["max_k"])
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_builder_skip_pad_random_maps_bit_exact(seed):
+    r = np.random.default_rng(50 + seed)
+    B = int(r.integers(1, 4))
+    S = int(r.integers(1, 20000))
+    ids = np.zeros((B, S), np.int32)
+    for b in range(B):
+        pos, d = 0, 1
+        while pos < S:
+            n = int(r.integers(1, 3000 if seed % 2 else 40))
+            ids[b, pos:pos + n] = 0 if r.random() < 0.3 else d
+            d += 1
+            pos += n
+    q0 = int(r.integers(0, S))
+    Lq = int(r.integers(0, S - q0 + 1))
+    got = _build_gpu(ids, Lq, q0, skip_pad=True)
+    ref = oracle.build_segments(ids, Lq, q0, skip_pad=True)
+    np.testing.assert_array_equal(got[0], ref[0])
+    np.testing.assert_array_equal(got[1], ref[1])
+    assert (got[2], got[3]) == (ref[2], ref[3])
+    # a padding flag on both segments of every padding piece
+    kid = ids.reshape(-1)
+    nk = np.diff(ref[1])
+    first_key = np.where(nk > 0, ref[1][:-1], -1)
+    for s_ in range(len(nk)):
+        if first_key[s_] >= 0:
+            assert got[4][s_] == (kid[first_key[s_]] == 0)
+
+
+def test_document_path_skip_pad_equals_pad_fixup_path():
+    # the two ways of zeroing padding queries give the same forward (bitwise:
+    # every non-padding row runs the same tiles) and the same gradients
+    w = inputs.config(2, seed=1)
+    q, k, v, do = (cuda(t) for t in (w.q, w.k, w.v, w.dout))
+    ids = torch.from_numpy(w.doc_ids).to("cuda")
+    res = []
+    for skip in (True, False):
+        out, lse, seg = psf.document_causal_attention(q, k, v, ids, ids, 0, w.scale, None, skip_pad=skip)
+        g = psf.document_causal_attention_backward(do, q, k, v, out, lse, seg, w.scale)
+        res.append((out, lse, g))
+    assert torch.equal(res[0][0], res[1][0])
+    assert torch.equal(res[0][1], res[1][1])
+    for a, b in zip(res[0][2], res[1][2]):
+        e = float(torch.linalg.norm(a.float() - b.float()) / torch.linalg.norm(b.float()))
+        assert e <= 1e-3, e
+    pad_rows = (ids[0] == 0).nonzero().flatten()
+    assert pad_rows.numel() > 0
+    assert float(res[0][0][pad_rows].abs().max()) == 0.0
+    assert bool(torch.isneginf(res[0][1][:, pad_rows]).all())
+
+
+def test_builder_rejects_unknown_flags():
+    ids = torch.ones(1, 8, dtype=torch.int32, device="cuda")
+    cu = torch.empty(20, dtype=torch.int32, device="cuda")
+    meta = torch.empty(3, dtype=torch.int32, device="cuda")
+    from packed_sequence_flash_gb300 import _lib
+    rc = _lib.load().psf_build_doc_segments(ids.data_ptr(), 1, 8, 8, 0, cu.data_ptr(), cu.data_ptr(), 19,
+                                            meta.data_ptr(), None, 2, None)
+    assert rc == -1  # PSF_EINVAL
 
 
 @pytest.mark.parametrize("cfg", [2, 4, 5])
@@ -126,9 +196,15 @@ def test_varlen_many_small_and_empty_segments():
 
 # ---------------------------------------------------------------- document-causal composition
 
-@pytest.mark.parametrize("seed", [0, 1])
-def test_document_causal_small_rows(seed):
+@pytest.mark.parametrize("seed,skip_pad", [(0, True), (1, True), (1, False)])
+def test_document_causal_small_rows(seed, skip_pad):
     w = inputs.small_document_workload(900, 4, 2, 128, 128, seed, max_len=350, pad_tail=61)
+    doc_case(w, skip_pad=skip_pad)
+
+
+def test_document_causal_d512_padding_skip():
+    # the wide kernels' zero-key (padding query) and zero-query (padding key) units
+    w = inputs.small_document_workload(600, 2, 1, 512, 512, 6, max_len=200, pad_tail=45)
     doc_case(w)
 
 
@@ -182,7 +258,7 @@ def test_varlen_d512_window_noncausal():
 
 def test_pad_fixup_zeroes_pad_rows():
     w = inputs.small_document_workload(400, 2, 2, 64, 64, 4, max_len=100, pad_tail=50)
-    doc_case(w, check_bwd=False)
+    doc_case(w, check_bwd=False, skip_pad=False)
 
 
 def test_lse_merge_matches_oracle_and_neg_inf_rows():
