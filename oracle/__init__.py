@@ -278,6 +278,47 @@ def build_cross_segments(doc_ids, q_start, q_length, k_start, k_length):
     return cu_q, cu_k, int(mq[0]), int(mk[0])
 
 
+def row_is_single_document(ids_row):
+    """Exactly one document with no padding: every position holds the same id > 0.
+    [cp_attention page, the row predicate behind the dense_cross flag of
+    `_build_packed_ring_segments`]"""
+    ids_row = [int(x) for x in np.asarray(ids_row).reshape(-1)]
+    return len(ids_row) > 0 and ids_row[0] > 0 and all(x == ids_row[0] for x in ids_row)
+
+
+def row_is_document_prefix(ids_row):
+    """The real (> 0) tokens are one document forming a contiguous prefix and the
+    padding, if any, is a trailing suffix (an all-padding row qualifies).
+    [cp_attention page, the row predicate behind the dense_local flag]"""
+    ids_row = [int(x) for x in np.asarray(ids_row).reshape(-1)]
+    k = 0
+    while k < len(ids_row) and ids_row[k] != 0:
+        k += 1
+    return len(set(ids_row[:k])) <= 1 and all(x == 0 for x in ids_row[k:])
+
+
+def chunk_dense_flags(doc_ids, q_start, q_length, k_start, k_length):
+    """(local, cross): whether the key chunk [k_start, k_start + k_length) may run
+    through the dense kernel for the query shard [q_start, q_start + q_length)
+    of every row of doc_ids [B, S], in the local role (causal; the chunk ends
+    where the shard ends and contains it; every row's chunk a document prefix)
+    or the cross role (non-causal; the chunk before the shard; every row's
+    [k_start, q_start) one document without padding that the shard starts with
+    and holds alone, padding only as its suffix).
+    [cp_attention page, `_build_packed_ring_segments` dense flags,
+    `_chunk_dense_eligible`]"""
+    ids = np.asarray(doc_ids)
+    if ids.ndim == 1:
+        ids = ids[None]
+    q_end, k_end = q_start + q_length, k_start + k_length
+    local = q_length > 0 and k_start <= q_start and k_end == q_end and all(
+        row_is_document_prefix(row[k_start:k_end]) for row in ids)
+    cross = q_length > 0 and k_length > 0 and k_end <= q_start and all(
+        row_is_single_document(row[k_start:q_start]) and row[q_start] == row[k_start]
+        and row_is_document_prefix(row[q_start:q_end]) for row in ids)
+    return bool(local), bool(cross)
+
+
 def live_rows(cu_q, cu_k):
     """Query rows of the segments that have at least one key (numpy int array)."""
     cu_q, cu_k = np.asarray(cu_q), np.asarray(cu_k)

@@ -483,6 +483,101 @@ def test_skip_pad_segments_equal_document_mode(seed, window):
 
 
 # ---------------------------------------------------------------------------
+# dense-kernel eligibility of a ring chunk (routing)
+
+def test_dense_route_golden_examples():
+    with open(os.path.join(GOLDEN, "dense_route_examples.json")) as fh:
+        g = json.load(fh)
+    for r in g["rows"]:
+        assert oracle.row_is_single_document(r["ids"]) == r["single"], r
+        assert oracle.row_is_document_prefix(r["ids"]) == r["prefix"], r
+    for c in g["chunks"]:
+        got = oracle.chunk_dense_flags(c["doc_ids"], c["q_start"], c["q_length"], c["k_start"], c["k_length"])
+        assert got == (c["local"], c["cross"]), c
+
+
+def _bhsd(x, B, N):
+    # packed [B*N, H, D] -> [B, H, N, D]
+    return x.reshape(B, N, x.shape[1], x.shape[2]).transpose(0, 2, 1, 3)
+
+
+def _packed(x):
+    # [B, H, N, D] -> packed [B*N, H, D]
+    B, H, N, D = x.shape
+    return x.transpose(0, 2, 1, 3).reshape(B * N, H, D)
+
+
+def _dense_route(q, k, v, do, qids, scale, causal, window=None):
+    """Dense oracle on [B,H,N,D], padding query rows zeroed after, backward fed the fixed out/lse."""
+    o, l = oracle.attn_fwd_dense(q, k, v, scale, causal, window)
+    pad = np.asarray(qids) == 0  # [B, Lq]
+    o = o.copy()
+    l = l.copy()
+    o[pad[:, None, :, None].repeat(o.shape[1], 1).repeat(o.shape[3], 3)] = 0.0
+    l[pad[:, None, :].repeat(l.shape[1], 1)] = -np.inf
+    g = oracle.attn_bwd_dense(do, q, k, v, o, l, scale, causal, window)
+    return o, l, g
+
+
+@pytest.mark.parametrize("seed,window", [(0, None), (1, None), (2, 4)])
+def test_dense_local_route_equals_document_mode(seed, window):
+    r = np.random.default_rng(seed)
+    B, S, Hq, Hkv, D = 3, 20, 2, 1, 8
+    ids = np.zeros((B, S), np.int32)
+    for b in range(B):
+        ids[b, :int(r.integers(0, S + 1))] = b + 1  # one document prefix, padding suffix
+    q0 = int(r.integers(0, S))
+    Lq = S - q0
+    k0 = int(r.integers(0, q0 + 1))
+    Lk = S - k0
+    assert oracle.chunk_dense_flags(ids, q0, Lq, k0, Lk)[0]
+    q, do = rnd(B, Hq, Lq, D), rnd(B, Hq, Lq, D)
+    k, v = rnd(B, Hkv, Lk, D), rnd(B, Hkv, Lk, D)
+    scale = 0.4
+    o, l, g = _dense_route(q, k, v, do, ids[:, q0:], scale, True, window)
+    ids_chunk = ids[:, k0:]
+    ro, rl = oracle.attn_fwd_document(_packed(q), _packed(k), _packed(v), ids_chunk, q0 - k0, scale, window)
+    np.testing.assert_allclose(_packed(o), ro, atol=1e-12)
+    np.testing.assert_array_equal(np.isneginf(l.transpose(1, 0, 2).reshape(Hq, -1)), np.isneginf(rl))
+    rg = oracle.attn_bwd_document(_packed(do), _packed(q), _packed(k), _packed(v), ro, rl, ids_chunk, q0 - k0,
+                                  scale, window)
+    for a, b in zip(g, rg):
+        np.testing.assert_allclose(_packed(a), b, atol=1e-10)
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_dense_cross_route_equals_cross_segments(seed):
+    r = np.random.default_rng(20 + seed)
+    B, S, Hq, Hkv, D = 2, 24, 2, 1, 8
+    q0 = int(r.integers(4, 16))
+    Lq = S - q0
+    ids = np.zeros((B, S), np.int32)
+    for b in range(B):
+        ids[b, :q0 + int(r.integers(1, Lq + 1))] = b + 3  # the document crosses into the shard, then padding
+    k0 = int(r.integers(0, q0))
+    Lk = int(r.integers(1, q0 - k0 + 1))
+    assert oracle.chunk_dense_flags(ids, q0, Lq, k0, Lk)[1]
+    q, do = rnd(B, Hq, Lq, D), rnd(B, Hq, Lq, D)
+    k, v = rnd(B, Hkv, Lk, D), rnd(B, Hkv, Lk, D)
+    scale = 0.4
+    o, l, g = _dense_route(q, k, v, do, ids[:, q0:], scale, False)
+    cu_q, cu_k, _, _ = oracle.build_cross_segments(ids, q0, Lq, k0, Lk)
+    ro, rl = oracle.attn_fwd_segments(_packed(q), _packed(k), _packed(v), cu_q, cu_k, scale, False)
+    np.testing.assert_allclose(_packed(o), ro, atol=1e-12)
+    np.testing.assert_array_equal(np.isneginf(l.transpose(1, 0, 2).reshape(Hq, -1)), np.isneginf(rl))
+    rg = oracle.attn_bwd_segments(_packed(do), _packed(q), _packed(k), _packed(v), ro, rl, cu_q, cu_k, scale, False)
+    for a, b in zip(g, rg):
+        np.testing.assert_allclose(_packed(a), b, atol=1e-10)
+
+
+def test_dense_route_flags_off_for_two_documents():
+    ids = np.array([[1, 1, 1, 2, 2, 2, 2, 2]], np.int32)
+    assert oracle.chunk_dense_flags(ids, 4, 4, 4, 4) == (True, False)    # chunk = shard = document 2 alone
+    assert oracle.chunk_dense_flags(ids, 2, 6, 2, 6) == (False, False)   # the chunk holds 1 and 2
+    assert oracle.chunk_dense_flags(ids, 4, 4, 0, 2) == (False, False)   # cross: [0, 4) holds 1 and 2
+
+
+# ---------------------------------------------------------------------------
 # cross-chunk pins (the one-device core of the ring decomposition)
 
 def test_cross_builder_golden_examples():
