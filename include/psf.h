@@ -229,6 +229,32 @@ int psf_build_doc_segments(const int32_t* kv_doc_ids, int B, int Sk, int q_lengt
                            int flags, void* stream);
 
 /*
+ * Dense-kernel eligibility of one ring chunk, on the GPU.
+ *                           [cp_attention page, `_build_packed_ring_segments`
+ *                            (the dense_local / dense_cross flags and pad_rows)
+ *                            and `_chunk_dense_eligible`; the row predicates
+ *                            "exactly one document with no padding" and "real
+ *                            tokens are one document forming a contiguous
+ *                            prefix, padding a trailing suffix"]
+ *  kv_doc_ids: int32 [B, S] (1-based ids, 0 = padding); the query shard is
+ *  [q_start, q_start + q_length) and the key chunk [k_start, k_start + k_length)
+ *  of every row. Writes flags, a device int32[2], 1 = eligible:
+ *   flags[0] (local role, causal): the chunk ends where the shard ends and
+ *     contains it, and in every row the chunk's real tokens are one document
+ *     forming a prefix (padding only as a suffix; an all-padding row counts).
+ *     psf_attn_dense_fwd/bwd (causal) on the raw [B, H, N, D] shard and chunk,
+ *     then psf_pad_fixup on the shard's ids, give the document-causal result.
+ *   flags[1] (cross role, non-causal): the chunk lies before the shard, in
+ *     every row [k_start, q_start) is one document d > 0 without padding, and
+ *     the shard starts with d and holds no other document (padding only as a
+ *     suffix). The non-causal dense kernels, then psf_pad_fixup, give the
+ *     result of the psf_build_cross_segments segments.
+ *  Errors: PSF_EINVAL when the shard or the chunk leaves the row.
+ */
+int psf_chunk_dense_flags(const int32_t* kv_doc_ids, int B, int S, int q_start, int q_length, int k_start,
+                          int k_length, int32_t* flags, void* stream);
+
+/*
  * Zero the padding queries of a document-causal result: rows whose query
  * document id is 0 get out = 0 and lse = -inf.
  *                           [fa4 page, `document_causal_fa4_attention`:

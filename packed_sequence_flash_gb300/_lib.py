@@ -38,6 +38,7 @@ SIGNATURES = {
     "psf_attn_dense_fwd": (I, [P, P, P, P, P, I, I, I, I, I, I, I, I, F, I, I32, P, SZ, P]),
     "psf_attn_dense_bwd": (I, [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, F, I, I32, P, SZ, P]),
     "psf_build_doc_segments": (I, [P, I, I, I, I, P, P, I, P, P, I, P]),
+    "psf_chunk_dense_flags": (I, [P, I, I, I, I, I, I, P, P]),
     "psf_pad_fixup": (I, [P, P, P, I, I, I, I, I, P]),
     "psf_lse_merge": (I, [P, P, P, P, P, P, P, I, I, I, I, P]),
     "psf_build_cross_segments": (I, [P, I, I, I, I, I, I, P, P, P, P]),

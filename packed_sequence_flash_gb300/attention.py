@@ -217,6 +217,64 @@ def build_doc_segments(kv_doc_ids, q_length, q_global_start, capacity=None, want
     return cu_q, cu_k, meta, pad
 
 
+def chunk_dense_eligible(kv_doc_ids, q_start, q_length, k_start, k_length):
+    """(local, cross) dense-kernel eligibility of the key chunk
+    [k_start, k_start + k_length) for the query shard [q_start, q_start + q_length)
+    of every row of kv_doc_ids [B, S] (device int32): see psf_chunk_dense_flags.
+    Reads the two flags back to the host (one synchronisation)."""
+    _i32(kv_doc_ids, "kv_doc_ids")
+    if kv_doc_ids.dim() == 1:
+        kv_doc_ids = kv_doc_ids[None]
+    B, S = kv_doc_ids.shape
+    flags = torch.empty(2, dtype=torch.int32, device=kv_doc_ids.device)
+    check(_lib.load().psf_chunk_dense_flags(_ptr(kv_doc_ids), B, S, int(q_start), int(q_length), int(k_start),
+                                            int(k_length), _ptr(flags), _stream()))
+    f = flags.tolist()
+    return bool(f[0]), bool(f[1])
+
+
+def chunk_attention(q, k, v, kv_doc_ids, q_start, k_start, scale, causal, window=None, dense=None):
+    """One chunk of the ring decomposition on one device: the query shard
+    [q_start, q_start + Lq) of every row, q [B, Hq, Lq, Dqk], against the key
+    chunk [k_start, k_start + Lk), k [B, Hkv, Lk, Dqk] / v [B, Hkv, Lk, Dv], with
+    kv_doc_ids [B, S] the whole rows' ids.
+
+    causal=True is the local role (the chunk ends where the shard ends; the
+    document-causal mask, optional left window); causal=False the cross role
+    (the chunk before the shard, no mask inside the shared document).
+    dense=None routes by chunk_dense_eligible (one host read); True / False
+    force the dense kernels (then pad_fixup) or the segment path.
+    Returns (out, lse, plan); plan feeds chunk_attention_backward.
+    """
+    if not causal and window is not None:
+        raise ValueError("a cross chunk runs without a window")
+    B, Hq, Lq, _ = q.shape
+    Lk = k.shape[2]
+    if dense is None:
+        local, cross = chunk_dense_eligible(kv_doc_ids, q_start, Lq, k_start, Lk)
+        dense = local if causal else cross
+    if dense:
+        out, lse = attn_dense_fwd(q, k, v, scale, causal, window)
+        pad_fixup(out, lse, kv_doc_ids[:, q_start:q_start + Lq].contiguous(), "bhsd")
+        return out, lse, ("dense", causal, window)
+    if causal:
+        ids_chunk = kv_doc_ids[:, k_start:k_start + Lk].contiguous()
+        cu_q, cu_k, meta, _ = build_doc_segments(ids_chunk, Lq, q_start - k_start, skip_pad=True)
+    else:
+        cu_q, cu_k, meta = build_cross_segments(kv_doc_ids, q_start, Lq, k_start, Lk)
+    out, lse = attn_varlen_fwd(q, k, v, cu_q, cu_k, -1, -1, scale, causal, window, dev_meta=meta, layout="bhsd")
+    return out, lse, ("segments", causal, window, cu_q, cu_k, meta)
+
+
+def chunk_attention_backward(dout, q, k, v, out, lse, plan, scale):
+    """Backward of chunk_attention from the (possibly merged) out/lse -> (dq, dk, dv)."""
+    if plan[0] == "dense":
+        return attn_dense_bwd(dout, q, k, v, out, lse, scale, plan[1], plan[2])
+    _, causal, window, cu_q, cu_k, meta = plan
+    return attn_varlen_bwd(dout, q, k, v, out, lse, cu_q, cu_k, -1, -1, scale, causal, window, dev_meta=meta,
+                           layout="bhsd")
+
+
 def pad_fixup(out, lse, q_doc_ids, layout="thd"):
     """In place: rows with query doc id 0 get out = 0 and lse = -inf."""
     _dtype_code([(out, "out")])

@@ -564,6 +564,20 @@ int psf_build_doc_segments(const int32_t* kv_doc_ids, int B, int Sk, int q_lengt
   return e == cudaSuccess ? PSF_OK : cuda_fail(e, "builder launch");
 }
 
+int psf_chunk_dense_flags(const int32_t* kv_doc_ids, int B, int S, int q_start, int q_length, int k_start,
+                          int k_length, int32_t* flags, void* stream) {
+  if (B < 1 || S < 1 || q_start < 0 || q_length < 0 || k_start < 0 || k_length < 0 ||
+      (int64_t)q_start + q_length > S || (int64_t)k_start + k_length > S)
+    return fail(PSF_EINVAL, "shard and chunk must lie inside the row");
+  if (!kv_doc_ids || !flags) return fail(PSF_EINVAL, "null pointer");
+  DeviceInfo* dev = nullptr;
+  int rc = device_info(&dev);
+  if (rc) return rc;
+  cudaError_t e = launch_chunk_dense_flags(kv_doc_ids, B, S, q_start, q_length, k_start, k_length, flags,
+                                           static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PSF_OK : cuda_fail(e, "dense-eligibility launch");
+}
+
 int psf_pad_fixup(void* out, float* lse, const int32_t* q_doc_ids, int layout, int B, int Lq, int Hq, int Dv,
                   void* stream) {
   if (layout != PSF_LAYOUT_THD && layout != PSF_LAYOUT_BHSD) return fail(PSF_EINVAL, "unknown layout");

@@ -362,6 +362,48 @@ __global__ void __launch_bounds__(kScanThreads) build_segments_kernel(const int3
   }
 }
 
+// Dense-kernel eligibility of one ring chunk over all rows (one block):
+//   local: the chunk [k0, k0 + Lk) ends where the shard [q0, q0 + Lq) ends and
+//     contains it, and in every row the chunk's real tokens are one document
+//     forming a prefix (no position p > k0 inside the chunk starts a non-zero
+//     run);
+//   cross: the chunk lies before the shard, in every row [k0, q0) is one
+//     document d > 0 without padding and the shard starts with d and holds no
+//     other non-zero run.
+// flags[0] = local, flags[1] = cross (1 eligible, 0 not).
+__global__ void __launch_bounds__(kScanThreads) chunk_dense_flags_kernel(const int32_t* ids, int B, int S, int q0,
+                                                                         int Lq, int k0, int Lk, int32_t* flags) {
+  const int tid = threadIdx.x;
+  const int q_end = q0 + Lq, k_end = k0 + Lk;
+  bool local = Lq > 0 && k0 <= q0 && k_end == q_end;
+  bool cross = Lq > 0 && Lk > 0 && k_end <= q0;
+  for (int b = 0; b < B && (local || cross); ++b) {
+    const int32_t* row = ids + (size_t)b * S;
+    int bad_local = 0, bad_cross = 0;
+    if (local)
+      for (int p = k0 + 1 + tid; p < k_end; p += kScanThreads) {
+        const int32_t x = row[p];
+        if (x != 0 && x != row[p - 1]) bad_local = 1;
+      }
+    if (cross) {
+      const int32_t d = row[k0];
+      if (tid == 0 && (d <= 0 || row[q0] != d)) bad_cross = 1;
+      for (int p = k0 + 1 + tid; p < q0; p += kScanThreads)
+        if (row[p] != d) bad_cross = 1;
+      for (int p = q0 + 1 + tid; p < q_end; p += kScanThreads) {
+        const int32_t x = row[p];
+        if (x != 0 && x != row[p - 1]) bad_cross = 1;
+      }
+    }
+    if (__syncthreads_or(bad_local)) local = false;
+    if (__syncthreads_or(bad_cross)) cross = false;
+  }
+  if (tid == 0) {
+    flags[0] = local ? 1 : 0;
+    flags[1] = cross ? 1 : 0;
+  }
+}
+
 // One warp per query row: a padding row (id 0) gets out = 0 on every head and
 // lse = -inf; other rows cost one id read.
 __global__ void pad_fixup_kernel(uint16_t* out, float* lse, const int32_t* qids, int B, int Lq, int Hq, int Dv,
@@ -834,6 +876,11 @@ cudaError_t launch_build_segments(const int32_t* ids, int B, int Sk, int Lq, int
   return cudaGetLastError();
 }
 
+cudaError_t launch_chunk_dense_flags(const int32_t* ids, int B, int S, int q0, int Lq, int k0, int Lk, int32_t* flags,
+                                     cudaStream_t st) {
+  chunk_dense_flags_kernel<<<1, kScanThreads, 0, st>>>(ids, B, S, q0, Lq, k0, Lk, flags);
+  return cudaGetLastError();
+}
 cudaError_t launch_pad_fixup(void* out, float* lse, const int32_t* qids, int B, int Lq, int Hq, int Dv,
                              int64_t o_sb, int64_t o_ss, int64_t o_sh, int64_t l_sb, int64_t l_sh, cudaStream_t st) {
   pad_fixup_kernel<<<grid_for((int64_t)B * Lq * 32, 256), 256, 0, st>>>(static_cast<uint16_t*>(out), lse, qids, B, Lq, Hq, Dv, o_sb, o_ss,

@@ -36,6 +36,8 @@ cudaError_t launch_bwd(const BwdParams& p, int dqk, int dv, int sms, int item_ca
 int fwd_smem_bytes(int dqk, int dvc);
 int bwd_smem_bytes(int dqk, int dv);
 
+cudaError_t launch_chunk_dense_flags(const int32_t* ids, int B, int S, int q0, int Lq, int k0, int Lk, int32_t* flags,
+                                     cudaStream_t st);
 cudaError_t launch_build_segments(const int32_t* ids, int B, int Sk, int Lq, int q0, int32_t* cu_q, int32_t* cu_k,
                                   int capacity, int32_t* meta, uint8_t* seg_is_pad, int skip_pad, int* status,
                                   cudaStream_t st);

@@ -429,3 +429,100 @@ def test_mixed_dtypes_are_rejected():
     cu = torch.tensor([0, 128], dtype=torch.int32, device="cuda")
     with pytest.raises(ValueError):
         psf.attn_varlen_fwd(q, k, k, cu, cu, 128, 128, 0.125, True)
+
+
+# ---------------------------------------------------------------- dense routing of ring chunks
+
+def test_chunk_dense_flags_golden_bit_exact():
+    with open(os.path.join(GOLDEN, "dense_route_examples.json")) as fh:
+        chunks = json.load(fh)["chunks"]
+    for c in chunks:
+        ids = torch.as_tensor(np.asarray(c["doc_ids"], np.int32)).to("cuda")
+        got = psf.chunk_dense_eligible(ids, c["q_start"], c["q_length"], c["k_start"], c["k_length"])
+        assert got == (c["local"], c["cross"]), c
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_chunk_dense_flags_random_bit_exact(seed):
+    r = np.random.default_rng(70 + seed)
+    B, S = int(r.integers(1, 4)), int(r.integers(2, 5000))
+    ids = np.zeros((B, S), np.int32)
+    for b in range(B):
+        kind = int(r.integers(0, 3))
+        if kind == 0:    # one document then padding
+            ids[b, :int(r.integers(0, S + 1))] = 5
+        elif kind == 1:  # one document
+            ids[b] = 7
+        else:            # several documents
+            pos, d = 0, 1
+            while pos < S:
+                n = int(r.integers(1, S // 2 + 2))
+                ids[b, pos:pos + n] = 0 if r.random() < 0.2 else d
+                d += 1
+                pos += n
+    q0 = int(r.integers(1, S))
+    Lq = S - q0 if seed % 2 else int(r.integers(1, S - q0 + 1))
+    for k0, Lk in ((q0, Lq), (0, q0 + Lq), (0, q0), (int(r.integers(0, q0)), 1)):
+        want = oracle.chunk_dense_flags(ids, q0, Lq, k0, Lk)
+        got = psf.chunk_dense_eligible(torch.from_numpy(ids).cuda(), q0, Lq, k0, Lk)
+        assert got == want, (k0, Lk)
+
+
+def _chunk_case(role, seed, D=128, window=None):
+    r = np.random.default_rng(seed)
+    B, S, Hq, Hkv = 2, 700, 4, 2
+    q0 = int(r.integers(200, 400))
+    Lq = S - q0
+    ids = np.zeros((B, S), np.int32)
+    for b in range(B):
+        ids[b, :q0 + int(r.integers(1, Lq + 1))] = b + 2
+    if role == "local":  # the chunk ends where the shard ends
+        k0 = int(r.integers(0, q0))
+        Lk = S - k0
+    else:  # the chunk lies before the shard, inside the shared document
+        k0 = int(r.integers(0, q0 // 2))
+        Lk = int(r.integers(1, q0 - k0 + 1))
+    causal = role == "local"
+    q = inputs.randn16((B, Hq, Lq, D), 10 * seed + 1)
+    k = inputs.randn16((B, Hkv, Lk, D), 10 * seed + 2)
+    v = inputs.randn16((B, Hkv, Lk, D), 10 * seed + 3)
+    do = inputs.randn16((B, Hq, Lq, D), 10 * seed + 4)
+    idt = torch.from_numpy(ids).cuda()
+    res = {}
+    for dense in (None, False):
+        out, lse, plan = psf.chunk_attention(cuda(q), cuda(k), cuda(v), idt, q0, k0, 1.0 / np.sqrt(D), causal,
+                                             window, dense=dense)
+        grads = psf.chunk_attention_backward(cuda(do), cuda(q), cuda(k), cuda(v), out, lse, plan, 1.0 / np.sqrt(D))
+        res[dense] = (out, lse, grads, plan[0])
+    assert res[None][3] == "dense" and res[False][3] == "segments"
+    # the oracle: document mode over the chunk (local) or the cross segments
+    pk = lambda x: np64(x).transpose(0, 2, 1, 3).reshape(-1, x.shape[1], x.shape[3])
+    if causal:
+        ro, rl = oracle.attn_fwd_document(pk(q), pk(k), pk(v), ids[:, k0:], q0 - k0, 1.0 / np.sqrt(D), window)
+        rg = oracle.attn_bwd_document(pk(do), pk(q), pk(k), pk(v), ro, rl, ids[:, k0:], q0 - k0, 1.0 / np.sqrt(D),
+                                      window)
+    else:
+        cu_q, cu_k, _, _ = oracle.build_cross_segments(ids, q0, Lq, k0, Lk)
+        ro, rl = oracle.attn_fwd_segments(pk(q), pk(k), pk(v), cu_q, cu_k, 1.0 / np.sqrt(D), False)
+        rg = oracle.attn_bwd_segments(pk(do), pk(q), pk(k), pk(v), ro, rl, cu_q, cu_k, 1.0 / np.sqrt(D), False)
+    for dense in (None, False):
+        out, lse, grads, _ = res[dense]
+        o_p = out.permute(0, 2, 1, 3).reshape(-1, Hq, D)
+        l_p = lse.permute(1, 0, 2).reshape(Hq, -1)
+        assert_fwd(o_p, l_p, ro, rl)
+        assert_grads(tuple(g.permute(0, 2, 1, 3).reshape(-1, g.shape[1], g.shape[3]) for g in grads), rg)
+    assert psf.device_status() == 0
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_chunk_attention_local_dense_route_matches_oracle(seed):
+    _chunk_case("local", seed)
+
+
+def test_chunk_attention_local_dense_route_window():
+    _chunk_case("local", 5, D=64, window=90)
+
+
+@pytest.mark.parametrize("seed", [2, 3])
+def test_chunk_attention_cross_dense_route_matches_oracle(seed):
+    _chunk_case("cross", seed)
