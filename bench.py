@@ -213,7 +213,8 @@ def config_dict(w, args, pairs, n_docs):
     return {"workload": w.name, "tokens": int(w.k.shape[0]), "q_tokens": int(w.q.shape[0]),
             "q_global_start": int(w.q_global_start), "Hq": int(w.q.shape[1]), "Hkv": int(w.k.shape[1]),
             "Dqk": int(w.q.shape[2]), "Dv": int(w.v.shape[2]), "window": w.window, "documents": n_docs,
-            "visible_pairs_x_heads": int(pairs), "seed": args.seed, "l2": "flushed between steps (256 MiB write)"}
+            "visible_pairs_x_heads": int(pairs), "seed": args.seed, "l2": "flushed between steps (256 MiB write)",
+            "pack_gqa": bool(getattr(args, "pack_gqa", False))}
 
 
 # ---------------------------------------------------------------------------
@@ -283,7 +284,8 @@ def our_arm(args):
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
     def step(qq, kk, vv, dd, ii, qi):
-        out, lse, seg = psf.document_causal_attention(qq, kk, vv, qi, ii, w.q_global_start, w.scale, w.window)
+        out, lse, seg = psf.document_causal_attention(qq, kk, vv, qi, ii, w.q_global_start, w.scale, w.window,
+                                                      pack_gqa=args.pack_gqa)
         grads = psf.document_causal_attention_backward(dd, qq, kk, vv, out, lse, seg, w.scale, w.window)
         return out, lse, grads
 
@@ -498,6 +500,8 @@ def main():
     ap.add_argument("--dtype", choices=["bf16", "fp16"], default="bf16",
                     help="16-bit type of q, k, v, dO and the outputs (the headline is bf16)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--pack-gqa", action="store_true",
+                    help="forward with a KV head's query heads packed into one tile (for short documents, --config 6)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -118,12 +118,21 @@ size_t psf_attn_bwd_workspace_size(int64_t total_q_rows, int64_t total_k_rows, i
  *  from it on the device and `nseg` is only the capacity of cu_q/cu_k.
  *  max_q / max_k: the longest segment lengths (ignored when dev_meta is given);
  *  a longer segment is a PSF_EDEVICE_ARGS device status.
- *  workspace: psf_attn_fwd_workspace_size(Tq, nseg) bytes.
+ *  flags: 0, or PSF_FWD_PACK_GQA: the G = Hq / Hkv query heads of a KV head
+ *  share one 128-row tile (128 / G rows of each), so short segments fill the
+ *  tile and K/V are loaded once for all G heads. Same results; it applies to
+ *  head dims (64, 64) and (128, 128) with G in 2..16 dividing 128, and other
+ *  shapes run one head per tile.
+ *                           [ffpa_attention page, `_ffpa_varlen_fwd`: the
+ *                            pack-GQA sentinel the pages fix off]
+ *  Any other bit is PSF_EINVAL.
+ *  workspace: psf_attn_fwd_workspace_size(Tq, nseg) bytes (enough for either flag).
  */
+#define PSF_FWD_PACK_GQA 1
 int psf_attn_varlen_fwd(const void* q, const void* k, const void* v, void* out, float* lse, const int32_t* cu_q,
                         const int32_t* cu_k, const int32_t* dev_meta, int nseg, int max_q, int max_k, int layout,
                         int dtype, int B, int Sq, int Sk, int Hq, int Hkv, int Dqk, int Dv, float scale, int causal,
-                        int32_t window_left, void* workspace, size_t ws_bytes, void* stream);
+                        int32_t window_left, int flags, void* workspace, size_t ws_bytes, void* stream);
 
 /*
  * Varlen forward that allocates nothing and takes no workspace.
@@ -133,7 +142,8 @@ int psf_attn_varlen_fwd(const void* q, const void* k, const void* v, void* out, 
  *  device memory up front and hand out nothing afterwards, plugin hosts that
  *  own every allocation, or code that must not touch the allocator while a
  *  step runs. This entry point behaves like psf_attn_varlen_fwd (same
- *  arguments minus workspace / ws_bytes, same results) but keeps its tile
+ *  arguments minus flags, workspace and ws_bytes, one query head per tile,
+ *  same results) but keeps its tile
  *  schedule in a fixed array in the library's device memory (852,736 bytes,
  *  held on every GPU that loads the library until the process exits).
  *  Limits: B * Sq <= PSF_NOALLOC_MAX_Q_ROWS and nseg <= PSF_NOALLOC_MAX_SEGMENTS;
@@ -180,11 +190,12 @@ int psf_attn_varlen_bwd(const void* dout, const void* q, const void* k, const vo
  *                            fa4 page, `causal_fa4_attention`]
  *  q [B,Hq,Nq,Dqk], k [B,Hkv,Nk,Dqk], v [B,Hkv,Nk,Dv], out [B,Hq,Nq,Dv],
  *  lse [B,Hq,Nq]. Causal is bottom-right aligned when Nq != Nk.
+ *  flags: as for psf_attn_varlen_fwd (0 or PSF_FWD_PACK_GQA).
  *  workspace: psf_attn_fwd_workspace_size(B * Nq, B) bytes.
  */
 int psf_attn_dense_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq, int Hkv,
                        int Nq, int Nk, int Dqk, int Dv, int dtype, float scale, int causal, int32_t window_left,
-                       void* workspace, size_t ws_bytes, void* stream);
+                       int flags, void* workspace, size_t ws_bytes, void* stream);
 
 /*
  * Dense backward.           [ffpa_attention page, `_ffpa_dense_bwd`: returns

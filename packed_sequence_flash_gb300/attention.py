@@ -18,7 +18,8 @@ from __future__ import annotations
 import torch
 
 from . import _lib
-from ._lib import PSF_DTYPE_BF16, PSF_DTYPE_F16, PSF_LAYOUT_BHSD, PSF_LAYOUT_THD, PSF_SEGMENTS_SKIP_PAD, check
+from ._lib import (PSF_DTYPE_BF16, PSF_DTYPE_F16, PSF_FWD_PACK_GQA, PSF_LAYOUT_BHSD, PSF_LAYOUT_THD,
+                   PSF_SEGMENTS_SKIP_PAD, check)
 
 NO_WINDOW = -(2 ** 31)  # the pages' "no window" sentinel
 
@@ -106,9 +107,11 @@ def _varlen_dims(q, k, v, layout):
 
 
 def attn_varlen_fwd(q, k, v, cu_q, cu_k, max_q, max_k, scale, causal, window=None, dev_meta=None,
-                    layout="thd", out=None, lse=None, workspace=None):
+                    layout="thd", out=None, lse=None, workspace=None, pack_gqa=False):
     """Packed varlen forward -> (out, lse). cu_q/cu_k int32 [nseg+1] on the device.
-    q, k, v: bf16 or fp16 (one type); out has their type, lse is fp32."""
+    q, k, v: bf16 or fp16 (one type); out has their type, lse is fp32.
+    pack_gqa: the query heads of a KV head share one tile (same results; for
+    short segments)."""
     dt = _dtype_code([(q, "q"), (k, "k"), (v, "v")])
     _i32(cu_q, "cu_q")
     _i32(cu_k, "cu_k")
@@ -123,7 +126,7 @@ def attn_varlen_fwd(q, k, v, cu_q, cu_k, max_q, max_k, scale, causal, window=Non
     rc = _lib.load().psf_attn_varlen_fwd(
         _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(cu_q), _ptr(cu_k), _ptr(dev_meta), nseg,
         int(max_q), int(max_k), lay, dt, B, Sq, Sk, Hq, Hkv, Dqk, Dv, float(scale), int(bool(causal)),
-        _window(window), _ptr(workspace), workspace.numel(), _stream())
+        _window(window), PSF_FWD_PACK_GQA if pack_gqa else 0, _ptr(workspace), workspace.numel(), _stream())
     check(rc)
     return out, lse
 
@@ -153,7 +156,7 @@ def attn_varlen_bwd(dout, q, k, v, out, lse, cu_q, cu_k, max_q, max_k, scale, ca
 # ---------------------------------------------------------------------------
 # dense [B, H, N, D]
 
-def attn_dense_fwd(q, k, v, scale, causal, window=None, workspace=None):
+def attn_dense_fwd(q, k, v, scale, causal, window=None, workspace=None, pack_gqa=False):
     """Dense forward -> (out [B,Hq,Nq,Dv] in the inputs' type, lse [B,Hq,Nq] fp32)."""
     dt = _dtype_code([(q, "q"), (k, "k"), (v, "v")])
     B, Hq, Nq, Dqk = q.shape
@@ -164,8 +167,9 @@ def attn_dense_fwd(q, k, v, scale, causal, window=None, workspace=None):
     if workspace is None:
         workspace = _workspace(fwd_workspace_size(B * Nq, B), q.device)
     rc = _lib.load().psf_attn_dense_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, Nq, Nk, Dqk,
-                                        Dv, dt, float(scale), int(bool(causal)), _window(window), _ptr(workspace),
-                                        workspace.numel(), _stream())
+                                        Dv, dt, float(scale), int(bool(causal)), _window(window),
+                                        PSF_FWD_PACK_GQA if pack_gqa else 0, _ptr(workspace), workspace.numel(),
+                                        _stream())
     check(rc)
     return out, lse
 
@@ -353,7 +357,8 @@ def grad_add_live_rows(dst, src, cu_q, cu_k, dev_meta=None):
 # ---------------------------------------------------------------------------
 # document-causal composition [fa4 page, document_causal_fa4_attention]
 
-def document_causal_attention(q, k, v, q_doc_ids, kv_doc_ids, q_global_start, scale, window=None, skip_pad=True):
+def document_causal_attention(q, k, v, q_doc_ids, kv_doc_ids, q_global_start, scale, window=None, skip_pad=True,
+                              pack_gqa=False):
     """Causal per-document attention of a local query shard against global keys.
 
     q [B, Hq, Lq, Dqk], k [B, Hkv, Sk, Dqk], v [B, Hkv, Sk, Dv] (or packed
@@ -365,6 +370,8 @@ def document_causal_attention(q, k, v, q_doc_ids, kv_doc_ids, q_global_start, sc
     queries, so the attention writes their zero rows itself and computes no
     padding pairs; False runs padding runs as ordinary segments and zeroes
     the padding queries afterwards with pad_fixup (q_doc_ids is read only then).
+    pack_gqa: the forward packs a KV head's query heads into one tile (short
+    documents).
     """
     layout = "thd" if q.dim() == 3 else "bhsd"
     if kv_doc_ids.dim() == 1:
@@ -373,7 +380,8 @@ def document_causal_attention(q, k, v, q_doc_ids, kv_doc_ids, q_global_start, sc
         q_doc_ids = q_doc_ids[None]
     Lq = q.shape[0] if layout == "thd" else q.shape[2]
     cu_q, cu_k, meta, _ = build_doc_segments(kv_doc_ids, Lq, q_global_start, skip_pad=skip_pad)
-    out, lse = attn_varlen_fwd(q, k, v, cu_q, cu_k, -1, -1, scale, True, window, dev_meta=meta, layout=layout)
+    out, lse = attn_varlen_fwd(q, k, v, cu_q, cu_k, -1, -1, scale, True, window, dev_meta=meta, layout=layout,
+                               pack_gqa=pack_gqa)
     if not skip_pad:
         pad_fixup(out, lse, q_doc_ids, layout)
     return out, lse, (cu_q, cu_k, meta)

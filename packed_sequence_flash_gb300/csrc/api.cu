@@ -145,8 +145,9 @@ struct FwdWorkspace {
   int2* items;
   int item_cap;
 };
-size_t fwd_ws_layout(int64_t rows, int nseg, FwdWorkspace* w, void* base) {
-  const int64_t cap = (rows + kBM - 1) / kBM + nseg + 1;
+// qrows: query rows per tile (kBM, or fewer when query heads share a tile).
+size_t fwd_ws_layout(int64_t rows, int nseg, FwdWorkspace* w, void* base, int qrows = kBM) {
+  const int64_t cap = (rows + qrows - 1) / qrows + nseg + 1;
   size_t off = 256;
   size_t prefix_off = off;
   off += align256(sizeof(int) * (size_t)(nseg + 2));
@@ -206,6 +207,7 @@ size_t bwd_ws_layout(int64_t q_rows, int64_t k_rows, int nseg, int Hq, int Hkv, 
 }
 // The workspace size query must not depend on the device; size it for the
 // largest SM count this library targets.
+constexpr int kMinPackedRows = kBM / 16;  // tile rows with 16 query heads packed into one tile
 constexpr int kMaxSms = 160;
 
 int check_common(int layout, int B, int Sq, int Sk, int Hq, int Hkv, int Dqk, int Dv, float scale, int32_t window,
@@ -229,10 +231,11 @@ int check_dtype(int dtype) {
   return PSF_OK;
 }
 
-// TMA view of a 16-bit (bf16 or fp16) tensor.
-int make_map16(CUtensorMap* m, const void* base, int D, int S, int H, int B, const View& v, int box_d, int dtype) {
+// TMA view of a 16-bit (bf16 or fp16) tensor; a box is box_d x box_s rows x box_h heads.
+int make_map16(CUtensorMap* m, const void* base, int D, int S, int H, int B, const View& v, int box_d, int dtype,
+               int box_s = kBM, int box_h = 1) {
   int rc = make_tmap_4d(m, dtype == PSF_DTYPE_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                        2, base, D, S, H, B, v.ss, v.sh, v.sb, box_d, kBM, CU_TENSOR_MAP_SWIZZLE_128B);
+                        2, base, D, S, H, B, v.ss, v.sh, v.sb, box_d, box_s, CU_TENSOR_MAP_SWIZZLE_128B, box_h);
   if (rc) return fail(PSF_ECUDA, "cuTensorMapEncodeTiled failed (%d) for a [%d,%d,%d,%d] view", rc, B, H, S, D);
   return PSF_OK;
 }
@@ -241,25 +244,35 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, void* out, float*
                   const int32_t* cu_k, const int32_t* dev_meta, int nseg, int max_q, int max_k, int layout, int dtype,
                   int B,
                   int Sq, int Sk, int Hq, int Hkv, int Dqk, int Dv, float scale, int causal, int32_t window, void* ws,
-                  size_t ws_bytes, void* stream) {
+                  size_t ws_bytes, void* stream, int flags = 0) {
   int rc = check_common(layout, B, Sq, Sk, Hq, Hkv, Dqk, Dv, scale, window, nseg);
   if (rc) return rc;
   if ((rc = check_dtype(dtype))) return rc;
+  if (flags & ~PSF_FWD_PACK_GQA) return fail(PSF_EINVAL, "unknown forward flags 0x%x", flags);
+  // Packed query heads: the G = Hq / Hkv heads of a KV head share one tile of
+  // 128 / G rows each (the two-CTA kernel, head dims 64 and 128, G in 2..16
+  // dividing 128); other shapes run one head per tile, with the same result.
+  const int G = Hq / Hkv;
+  const int pack = ((flags & PSF_FWD_PACK_GQA) && G > 1 && G <= 16 && kBM % G == 0 && Dqk == Dv &&
+                    (Dqk == 64 || Dqk == 128))
+                       ? G
+                       : 1;
+  const int qrows = kBM / pack;
   const int64_t q_rows = (int64_t)B * Sq, k_rows = (int64_t)B * Sk;
   if (q_rows == 0) return PSF_OK;
   if (!q || !out || !lse || (k_rows > 0 && (!k || !v))) return fail(PSF_EINVAL, "null tensor pointer");
   if (!aligned16(q) || !aligned16(out) || (k_rows > 0 && (!aligned16(k) || !aligned16(v))))
     return fail(PSF_EINVAL, "tensor base pointers must be 16-byte aligned");
   if ((cu_q == nullptr) != (cu_k == nullptr)) return fail(PSF_EINVAL, "cu_q and cu_k must both be given");
-  const size_t need = fwd_ws_layout(q_rows, nseg, nullptr, nullptr);
+  const size_t need = fwd_ws_layout(q_rows, nseg, nullptr, nullptr, qrows);
   if (!ws || ws_bytes < need) return fail(PSF_EWORKSPACE, "forward workspace needs %zu bytes (got %zu)", need, ws_bytes);
   DeviceInfo* dev = nullptr;
   if ((rc = device_info(&dev))) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
   FwdWorkspace w;
-  fwd_ws_layout(q_rows, nseg, &w, ws);
-  SegInfo g{cu_q, cu_k, dev_meta, nseg, max_q, max_k, B, Sq, Sk, causal ? 1 : 0, window > 0 ? (int)window : 0};
+  fwd_ws_layout(q_rows, nseg, &w, ws, qrows);
+  SegInfo g{cu_q, cu_k, dev_meta, nseg, max_q, max_k, B, Sq, Sk, causal ? 1 : 0, window > 0 ? (int)window : 0, qrows};
   const View vq = tensor_view(layout, Sq, Hq, Dqk), vk = tensor_view(layout, Sk, Hkv, Dqk);
   const View vv = tensor_view(layout, Sk, Hkv, Dv), vo = tensor_view(layout, Sq, Hq, Dv);
   const View vl = lse_view(layout, Sq, Hq);
@@ -269,7 +282,7 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, void* out, float*
 
   FwdParams p;
   memset(&p, 0, sizeof(p));
-  if ((rc = make_map16(&p.tm_q, q, Dqk, Sq, Hq, B, vq, 64, dtype))) return rc;
+  if ((rc = make_map16(&p.tm_q, q, Dqk, Sq, Hq, B, vq, 64, dtype, qrows, pack))) return rc;
   if (k_rows > 0) {
     if ((rc = make_map16(&p.tm_k, k, Dqk, Sk, Hkv, B, vk, 64, dtype))) return rc;
     if ((rc = make_map16(&p.tm_v, v, Dv, Sk, Hkv, B, vv, 64, dtype))) return rc;
@@ -284,6 +297,7 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, void* out, float*
   p.l_sh = vl.sh;
   p.Hq = Hq;
   p.Hkv = Hkv;
+  p.pack = pack;
   p.dv_parts = Dv == 512 ? 2 : 1;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.items = w.items;
@@ -291,7 +305,7 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, void* out, float*
   p.work_next = w.n_items + 1;
   p.status = dev->status;
   p.limit_ns = g_wait_limit_ns;
-  const int64_t max_work = (int64_t)w.item_cap * Hq * p.dv_parts;
+  const int64_t max_work = (int64_t)w.item_cap * (Hq / pack) * p.dv_parts;
   TimedLaunch tl;
   const bool timed = timing_begin(0, st, &tl);
   e = launch_fwd(p, Dqk, Dv / p.dv_parts, dev->sms, max_work, dtype == PSF_DTYPE_F16, st);
@@ -484,7 +498,8 @@ int psf_kernel_times_ms(int kind, double* total_ms, int* launches) {
 
 size_t psf_attn_fwd_workspace_size(int64_t total_q_rows, int nseg) {
   if (total_q_rows < 0 || nseg < 0) return 0;
-  return fwd_ws_layout(total_q_rows, nseg, nullptr, nullptr);
+  // Large enough for the shortest tiles (packed query heads, up to kBM / 8 = 16 heads).
+  return fwd_ws_layout(total_q_rows, nseg, nullptr, nullptr, kMinPackedRows);
 }
 
 size_t psf_attn_bwd_workspace_size(int64_t total_q_rows, int64_t total_k_rows, int nseg, int Hq, int Hkv, int Dqk,
@@ -496,10 +511,10 @@ size_t psf_attn_bwd_workspace_size(int64_t total_q_rows, int64_t total_k_rows, i
 int psf_attn_varlen_fwd(const void* q, const void* k, const void* v, void* out, float* lse, const int32_t* cu_q,
                         const int32_t* cu_k, const int32_t* dev_meta, int nseg, int max_q, int max_k, int layout,
                         int dtype, int B, int Sq, int Sk, int Hq, int Hkv, int Dqk, int Dv, float scale, int causal,
-                        int32_t window_left, void* workspace, size_t ws_bytes, void* stream) {
+                        int32_t window_left, int flags, void* workspace, size_t ws_bytes, void* stream) {
   if (!cu_q || !cu_k) return fail(PSF_EINVAL, "varlen calls need cu_q and cu_k");
   return attn_fwd_impl(q, k, v, out, lse, cu_q, cu_k, dev_meta, nseg, max_q, max_k, layout, dtype, B, Sq, Sk, Hq, Hkv,
-                       Dqk, Dv, scale, causal, window_left, workspace, ws_bytes, stream);
+                       Dqk, Dv, scale, causal, window_left, workspace, ws_bytes, stream, flags);
 }
 
 int psf_attn_varlen_fwd_noalloc(const void* q, const void* k, const void* v, void* out, float* lse,
@@ -533,9 +548,9 @@ int psf_attn_varlen_bwd(const void* dout, const void* q, const void* k, const vo
 
 int psf_attn_dense_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq, int Hkv,
                        int Nq, int Nk, int Dqk, int Dv, int dtype, float scale, int causal, int32_t window_left,
-                       void* workspace, size_t ws_bytes, void* stream) {
+                       int flags, void* workspace, size_t ws_bytes, void* stream) {
   return attn_fwd_impl(q, k, v, out, lse, nullptr, nullptr, nullptr, B, Nq, Nk, PSF_LAYOUT_BHSD, dtype, B, Nq, Nk, Hq,
-                       Hkv, Dqk, Dv, scale, causal, window_left, workspace, ws_bytes, stream);
+                       Hkv, Dqk, Dv, scale, causal, window_left, workspace, ws_bytes, stream, flags);
 }
 
 int psf_attn_dense_bwd(const void* dout, const void* q, const void* k, const void* v, const void* out,

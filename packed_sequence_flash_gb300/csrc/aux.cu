@@ -78,7 +78,7 @@ __device__ int tile_cost(const SegInfo& g, int s, int t, int over_keys) {
     q_range_for_kv_tile(m, n, t * kBN, g.causal, g.window, lo, hi);
     return hi > lo ? ceil_div(hi, kBM) - lo / kBM : 0;
   }
-  kv_range_for_q_tile(m, n, t * kBM, g.causal, g.window, lo, hi);
+  kv_range_for_q_tile(m, n, t * g.qrows, g.causal, g.window, lo, hi, g.qrows);
   return hi > lo ? ceil_div(hi, kBN) - lo / kBN : 0;
 }
 
@@ -111,7 +111,7 @@ __device__ void schedule_body(SegInfo g, int over_keys, int2* items, int* n_item
       if (ok && g.B > 1)
         ok = (m == 0 || q0 / g.Sq == (q1 - 1) / g.Sq) && (n == 0 || k0 / g.Sk == (k1 - 1) / g.Sk);
       if (!ok) bad = 1;
-      else cnt = over_keys ? ceil_div(n, kBN) : ceil_div(m, kBM);
+      else cnt = over_keys ? ceil_div(n, kBN) : ceil_div(m, g.qrows);
     }
     int tot;
     const int ex = block_excl_scan(cnt, &tot);

@@ -27,6 +27,7 @@ struct SegInfo {
   int B, Sq, Sk;            // batches and rows per batch of the q / k tensors
   int causal;
   int window;               // > 0: left window counting the current token
+  int qrows = kBM;          // query rows per forward tile (fewer when query heads are packed into one tile)
 };
 
 __device__ __forceinline__ int seg_count(const SegInfo& g) {
@@ -37,9 +38,10 @@ __device__ __forceinline__ int seg_count(const SegInfo& g) {
 __device__ __forceinline__ int cu_q_at(const SegInfo& g, int s) { return g.cu_q ? g.cu_q[s] : s * g.Sq; }
 __device__ __forceinline__ int cu_k_at(const SegInfo& g, int s) { return g.cu_k ? g.cu_k[s] : s * g.Sk; }
 
-// Keys [lo, hi) (segment-local) that some query of rows [i0, i0 + kBM) can see.
-__device__ __forceinline__ void kv_range_for_q_tile(int m, int n, int i0, int causal, int window, int& lo, int& hi) {
-  int i1 = min(i0 + kBM, m);
+// Keys [lo, hi) (segment-local) that some query of rows [i0, i0 + rows) can see.
+__device__ __forceinline__ void kv_range_for_q_tile(int m, int n, int i0, int causal, int window, int& lo, int& hi,
+                                                    int rows = kBM) {
+  int i1 = min(i0 + rows, m);
   int delta = n - m;
   hi = causal ? min(n, i1 + delta) : n;
   lo = window > 0 ? max(0, i0 + delta - window + 1) : 0;

@@ -41,6 +41,7 @@ struct FwdParams {
   float* lse;
   int64_t l_sb, l_sh;  // element strides of lse (batch, head); rows are contiguous
   int Hq, Hkv;
+  int pack;      // query heads per tile: 1, or Hq / Hkv when a KV head's query heads share one tile
   int dv_parts;  // value-dim slices computed by separate tiles (each DVC wide)
   float scale_log2;
   const int2* items;  // (segment, q tile), heaviest first
@@ -63,18 +64,19 @@ struct FwdCfg {
 };
 
 struct FwdTile {
-  int s, qt, h, part;
+  int s, qt, h, part;  // h: the tile's first query head
   int cq0, ck0, m, n;
   int kv_t0, nk;
 };
 
 __device__ __forceinline__ FwdTile fwd_decode(const FwdParams& p, int w) {
   FwdTile t;
-  const int hp = p.Hq * p.dv_parts;
+  const int hp = (p.Hq / p.pack) * p.dv_parts;
   int item = w / hp;
   int r = w - item * hp;
-  t.h = r / p.dv_parts;
-  t.part = r - t.h * p.dv_parts;
+  const int hg = r / p.dv_parts;
+  t.part = r - hg * p.dv_parts;
+  t.h = hg * p.pack;
   int2 it = p.items[item];
   t.s = it.x;
   t.qt = it.y;
@@ -83,7 +85,7 @@ __device__ __forceinline__ FwdTile fwd_decode(const FwdParams& p, int w) {
   t.m = cu_q_at(p.seg, t.s + 1) - t.cq0;
   t.n = cu_k_at(p.seg, t.s + 1) - t.ck0;
   int lo, hi;
-  kv_range_for_q_tile(t.m, t.n, t.qt * kBM, p.seg.causal, p.seg.window, lo, hi);
+  kv_range_for_q_tile(t.m, t.n, t.qt * p.seg.qrows, p.seg.causal, p.seg.window, lo, hi, p.seg.qrows);
   t.kv_t0 = lo / kBN;
   t.nk = hi > lo ? ceil_div(hi, kBN) - t.kv_t0 : 0;
   return t;
@@ -132,7 +134,7 @@ __global__ void __launch_bounds__(256, 1) attn_fwd_kernel(const __grid_constant_
   tc_fence_after();
   const uint32_t tmem = tmem_base_smem;
   const Ctl ctl{p.status, p.limit_ns, &abort_flag};
-  const int total = (*p.n_items) * p.Hq * p.dv_parts;
+  const int total = (*p.n_items) * (p.Hq / p.pack) * p.dv_parts;  // p.pack is 1 for this kernel
   const int G = p.Hq / p.Hkv;
 
   if (warp == 0) {

@@ -12,6 +12,9 @@
 // strictly in that order, so a single S buffer suffices.
 //   TMEM  256 columns per CTA: S, then P (bf16 over S's first 64 columns)
 //         [0, 128) | O [128, 128 + D)
+//   Pack  with p.pack = G = Hq / Hkv > 1 the 128-row tile holds the G query
+//         heads of one KV head, 128 / G rows each (one TMA box of 128/G rows x G
+//         heads), so short segments fill the tile and K/V load once for all G.
 //   SMEM  the Q tile and two tile slots that K_j and V_j pass through in turn
 //         (D / 64 chunks of 128 rows x 64 columns, 128-byte swizzled each).
 //   PV    one N = D MMA chain over a whole V tile: the B operand is MN-major and
@@ -103,7 +106,7 @@ __global__ void __launch_bounds__(192, 2) attn_fwd_duo_kernel(const __grid_const
   tc_fence_after();
   const uint32_t tmem = tmem_base_smem;
   const Ctl ctl{p.status, p.limit_ns, &abort_flag};
-  const int total = (*p.n_items) * p.Hq;
+  const int total = (*p.n_items) * (p.Hq / p.pack);
   const int G = p.Hq / p.Hkv;
   // Next work item for the MMA and softmax warps (-1: none left, or abort),
   // with its decoded tile.
@@ -160,7 +163,7 @@ __global__ void __launch_bounds__(192, 2) attn_fwd_duo_kernel(const __grid_const
         if (t.nk > 0) {
           if (!wait_bar(&q_empty, (qcnt & 1) ^ 1, ctl)) break;
           mbar_arrive_expect_tx(&q_full, C::TILE_BYTES);
-          const int fq = t.cq0 + t.qt * kBM, bq = fq / p.seg.Sq;
+          const int fq = t.cq0 + t.qt * p.seg.qrows, bq = fq / p.seg.Sq;
           for (int c = 0; c < C::CH; ++c)
             tma_load_4d(smem + C::Q_OFF + c * kChunkBytes, &p.tm_q, &q_full, c * 64, fq - bq * p.seg.Sq, t.h, bq);
           ++qcnt;
@@ -265,13 +268,17 @@ __global__ void __launch_bounds__(192, 2) attn_fwd_duo_kernel(const __grid_const
       FwdTile t;
       const int w = next_work(ok, t);
       if (w < 0) break;
-      const int i = t.qt * kBM + row;  // segment-local query index
+      // TMEM lane / tile row -> (query head, segment-local query index): the
+      // tile holds p.pack query heads of qrows rows each, head-major.
+      const int qrows = p.seg.qrows;
+      const int i = t.qt * qrows + row % qrows;
+      const int h = t.h + row / qrows;
       const bool valid = i < t.m;
       const int fq = t.cq0 + i;
       const int bq = fq / p.seg.Sq;
       const int sq = fq - bq * p.seg.Sq;
-      T* orow = static_cast<T*>(p.out) + bq * p.o_sb + (int64_t)sq * p.o_ss + t.h * p.o_sh;
-      float* lrow = p.lse + bq * p.l_sb + t.h * p.l_sh + sq;
+      T* orow = static_cast<T*>(p.out) + bq * p.o_sb + (int64_t)sq * p.o_ss + h * p.o_sh;
+      float* lrow = p.lse + bq * p.l_sb + h * p.l_sh + sq;
       if (t.nk == 0) {
         if (valid) {
           const uint4 z = make_uint4(0, 0, 0, 0);

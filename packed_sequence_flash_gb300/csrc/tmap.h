@@ -32,7 +32,7 @@ inline EncodeTiledFn encode_tiled_fn() {
 // Returns 0 on success.
 inline int make_tmap_4d(CUtensorMap* map, CUtensorMapDataType dtype, int elem_bytes, const void* base,
                         int64_t D, int64_t S, int64_t H, int64_t B, int64_t stride_s, int64_t stride_h,
-                        int64_t stride_b, int box_d, int box_s, CUtensorMapSwizzle swz) {
+                        int64_t stride_b, int box_d, int box_s, CUtensorMapSwizzle swz, int box_h = 1) {
   EncodeTiledFn fn = encode_tiled_fn();
   if (!fn) return -1;
   cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)(S > 0 ? S : 1), (cuuint64_t)(H > 0 ? H : 1),
@@ -48,7 +48,7 @@ inline int make_tmap_4d(CUtensorMap* map, CUtensorMapDataType dtype, int elem_by
     }
     if (strides[i] == 0 || (strides[i] % 16) != 0) return -2;
   }
-  cuuint32_t box[4] = {(cuuint32_t)box_d, (cuuint32_t)box_s, 1, 1};
+  cuuint32_t box[4] = {(cuuint32_t)box_d, (cuuint32_t)box_s, (cuuint32_t)box_h, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = fn(map, dtype, 4, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                   swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);

@@ -31,7 +31,8 @@ def doc_lengths(kind: str, total: int, seed: int) -> list[int]:
       * ``"uniform64_2048"``: integers uniform in [64, 2048];
       * ``"lognormal1024"``: lognormal with median 1024 and sigma 1.0, rounded,
         clipped to [32, 8192];
-      * ``"pareto256"``: floor(256 * (1 - U) ** (-1 / 1.2)), clipped to [256, 32768].
+      * ``"pareto256"``: floor(256 * (1 - U) ** (-1 / 1.2)), clipped to [256, 32768];
+      * ``"uniform16_64"``: integers uniform in [16, 64] (short documents).
     """
     rng = np.random.default_rng(seed)
     out: list[int] = []
@@ -42,6 +43,8 @@ def doc_lengths(kind: str, total: int, seed: int) -> list[int]:
         elif kind == "lognormal1024":
             n = int(round(float(rng.lognormal(mean=math.log(1024.0), sigma=1.0))))
             n = min(max(n, 32), 8192)
+        elif kind == "uniform16_64":
+            n = int(rng.integers(16, 65))
         elif kind == "pareto256":
             u = float(rng.random())
             n = int(math.floor(256.0 * (1.0 - u) ** (-1.0 / 1.2)))
@@ -139,7 +142,9 @@ def config(n: int, seed: int = 0) -> Workload:
     3. dense causal, B=2, Hq=8, Hkv=2, N=4096, D=512, inputs times 0.5;
     4. 16384-token row, lognormal lengths (median 1024), queries 8192..16383, Dqk=192, Dv=128,
        Hq=Hkv=16;
-    5. 65536 tokens, Pareto(1.2) lengths in [256, 32768], Hq=32, Hkv=8, D=128, left window 4096.
+    5. 65536 tokens, Pareto(1.2) lengths in [256, 32768], Hq=32, Hkv=8, D=128, left window 4096;
+    6. short documents: 65536 tokens, lengths uniform in [16, 64], Hq=32, Hkv=8, D=128 (the
+       workload that packing a KV head's query heads into one tile is for).
     """
     if n == 1:
         return dense_workload(1, 2, 1, 128, 128, 64, 64, seed, name="cfg1_dense_causal_n128_d64")
@@ -155,6 +160,9 @@ def config(n: int, seed: int = 0) -> Workload:
     if n == 5:
         return document_workload("pareto256", 65536, 32, 8, 128, 128, seed, window=4096,
                                  name="cfg5_doc_causal_t65536_w4096")
+    if n == 6:
+        return document_workload("uniform16_64", 65536, 32, 8, 128, 128, seed,
+                                 name="short_docs_t65536_len16_64_d128")
     raise ValueError(f"no workload {n}")
 
 

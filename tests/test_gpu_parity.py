@@ -526,3 +526,59 @@ def test_chunk_attention_local_dense_route_window():
 @pytest.mark.parametrize("seed", [2, 3])
 def test_chunk_attention_cross_dense_route_matches_oracle(seed):
     _chunk_case("cross", seed)
+
+
+# ---------------------------------------------------------------- packed query heads (pack-GQA forward)
+
+@pytest.mark.parametrize("D,G,causal,window", [(128, 4, True, None), (128, 2, False, None), (64, 8, True, 37),
+                                               (128, 16, True, None), (64, 4, False, 21)])
+def test_varlen_fwd_pack_gqa_matches_unpacked_and_oracle(D, G, causal, window):
+    # many short segments (and a few long ones, and empty ones) with the query
+    # heads of a KV head packed into one tile
+    r = np.random.default_rng(100 + G + D)
+    lens_q = [int(x) for x in r.integers(0, 40, 60)] + [300, 129, 0, 1]
+    lens_k = [lq + int(r.integers(0, 20)) if causal else int(r.integers(0, 60)) for lq in lens_q]
+    cu_q = np.concatenate([[0], np.cumsum(lens_q)]).astype(np.int32)
+    cu_k = np.concatenate([[0], np.cumsum(lens_k)]).astype(np.int32)
+    Hkv = 2
+    Hq = G * Hkv
+    Tq, Tk = int(cu_q[-1]) + 5, int(cu_k[-1])
+    q = inputs.randn16((Tq, Hq, D), G * 31 + 1)
+    k = inputs.randn16((Tk, Hkv, D), G * 31 + 2)
+    v = inputs.randn16((Tk, Hkv, D), G * 31 + 3)
+    scale = 1.0 / np.sqrt(D)
+    cq, ck = torch.from_numpy(cu_q).cuda(), torch.from_numpy(cu_k).cuda()
+    mq, mk = max(lens_q), max(lens_k)
+    out_p, lse_p = psf.attn_varlen_fwd(cuda(q), cuda(k), cuda(v), cq, ck, mq, mk, scale, causal, window,
+                                       pack_gqa=True)
+    out_u, lse_u = psf.attn_varlen_fwd(cuda(q), cuda(k), cuda(v), cq, ck, mq, mk, scale, causal, window)
+    out_o, lse_o = oracle.attn_fwd_segments(q, k, v, cu_q, cu_k, scale, causal, window)
+    assert_fwd(out_p, lse_p, out_o, lse_o)
+    assert float((out_p.float() - out_u.float()).abs().max()) <= 1e-2
+    fin = torch.isfinite(lse_u)
+    assert torch.equal(fin, torch.isfinite(lse_p))
+    assert float((lse_p[fin] - lse_u[fin]).abs().max()) <= 1e-4
+    assert psf.device_status() == 0
+
+
+def test_document_causal_pack_gqa_with_backward():
+    w = inputs.small_document_workload(1500, 8, 2, 128, 128, 7, max_len=90, pad_tail=40)
+    q, k, v, do = (cuda(t) for t in (w.q, w.k, w.v, w.dout))
+    ids = torch.from_numpy(w.doc_ids).to("cuda")
+    out, lse, seg = psf.document_causal_attention(q, k, v, ids, ids, 0, w.scale, None, pack_gqa=True)
+    out_o, lse_o = oracle.attn_fwd_document(w.q, w.k, w.v, w.doc_ids, 0, w.scale, None)
+    assert_fwd(out, lse, out_o, lse_o)
+    grads = psf.document_causal_attention_backward(do, q, k, v, out, lse, seg, w.scale)
+    ref = oracle.attn_bwd_document(w.dout, w.q, w.k, w.v, out_o, lse_o, w.doc_ids, 0, w.scale, None)
+    assert_grads(grads, ref)
+    assert psf.device_status() == 0
+
+
+def test_dense_fwd_pack_gqa_matches_oracle():
+    q = inputs.randn16((2, 8, 100, 64), 501)
+    k = inputs.randn16((2, 2, 160, 64), 502)
+    v = inputs.randn16((2, 2, 160, 64), 503)
+    out, lse = psf.attn_dense_fwd(cuda(q), cuda(k), cuda(v), 0.125, True, pack_gqa=True)
+    out_o, lse_o = oracle.attn_fwd_dense(q, k, v, 0.125, True)
+    assert_fwd(out.reshape(-1, 64), lse.reshape(-1), out_o.reshape(-1, 64), lse_o.reshape(-1))
+    assert psf.device_status() == 0
