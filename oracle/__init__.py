@@ -54,10 +54,10 @@ def _load():
             I = ctypes.c_int
             D = ctypes.c_double
             lib.oracle_attn_fwd.argtypes = [I, I, I, P, P, I, P, I, I, I, I,
-                                            P, P, P, I, I, I, I, I, I, D, P, I, P, P, I]
+                                            P, P, P, I, I, I, I, I, I, D, D, P, I, P, P, I]
             lib.oracle_attn_fwd.restype = I
             lib.oracle_attn_bwd.argtypes = [I, I, I, P, P, I, P, I, I, I, I,
-                                            P, P, P, P, P, P, I, I, I, I, I, I, D,
+                                            P, P, P, P, P, P, I, I, I, I, I, I, D, D,
                                             P, I, P, I, P, P, P, I]
             lib.oracle_attn_bwd.restype = I
             lib.oracle_build_segments.argtypes = [P, I, I, I, I, P, P, I, P, P, I]
@@ -114,8 +114,12 @@ def _mask_args(mode, causal, window, cu_q, cu_k, doc_ids, B, Sk, Lq, q0):
 # ---------------------------------------------------------------------------
 # forward
 
+def _softcap(softcap) -> float:
+    return float(softcap) if softcap is not None and softcap > 0 else 0.0
+
+
 def _fwd(mode, q, k, v, scale, causal, window, cu_q=None, cu_k=None, doc_ids=None, B=0, Sk=0,
-         Lq=0, q0=0, rows=None, nthreads=None):
+         Lq=0, q0=0, rows=None, nthreads=None, softcap=None):
     lib = _load()
     q, k, v = _f64(q), _f64(k), _f64(v)
     Tq, Hq, Dqk = q.shape
@@ -126,21 +130,22 @@ def _fwd(mode, q, k, v, scale, causal, window, cu_q=None, cu_k=None, doc_ids=Non
     rows = _i32(rows)
     rc = lib.oracle_attn_fwd(*_mask_args(mode, causal, window, cu_q, cu_k, doc_ids, B, Sk, Lq, q0),
                              _ptr(q), _ptr(k), _ptr(v), Tq, Tk, Hq, Hkv, Dqk, Dv, float(scale),
-                             _ptr(rows), 0 if rows is None else len(rows), _ptr(out), _ptr(lse),
+                             _softcap(softcap), _ptr(rows), 0 if rows is None else len(rows), _ptr(out), _ptr(lse),
                              nthreads or default_threads())
     if rc != 0:
         raise ValueError(f"oracle_attn_fwd failed ({rc})")
     return out, lse
 
 
-def attn_fwd_segments(q, k, v, cu_q, cu_k, scale, causal, window=None, rows=None, nthreads=None):
-    """Packed forward: q [Tq,Hq,Dqk], k [Tk,Hkv,Dqk], v [Tk,Hkv,Dv] -> out [Tq,Hq,Dv], lse [Hq,Tq]."""
+def attn_fwd_segments(q, k, v, cu_q, cu_k, scale, causal, window=None, rows=None, nthreads=None, softcap=None):
+    """Packed forward: q [Tq,Hq,Dqk], k [Tk,Hkv,Dqk], v [Tk,Hkv,Dv] -> out [Tq,Hq,Dv], lse [Hq,Tq].
+    softcap > 0 caps each logit as softcap * tanh(logit / softcap)."""
     return _fwd(MODE_SEGMENTS, q, k, v, scale, causal, window, cu_q=_i32(cu_q), cu_k=_i32(cu_k),
-                rows=rows, nthreads=nthreads)
+                rows=rows, nthreads=nthreads, softcap=softcap)
 
 
 def attn_fwd_document(q, k, v, doc_ids, q_global_start, scale, window=None, rows=None,
-                      nthreads=None):
+                      nthreads=None, softcap=None):
     """Document-causal forward with the mask materialised from doc ids.
 
     q [B*Lq, Hq, Dqk] (batch-major rows), k/v [B*Sk, Hkv, D]; doc_ids [B, Sk].
@@ -149,10 +154,10 @@ def attn_fwd_document(q, k, v, doc_ids, q_global_start, scale, window=None, rows
     B, Sk = doc_ids.shape
     Lq = q.shape[0] // B
     return _fwd(MODE_DOCUMENT, q, k, v, scale, True, window, doc_ids=doc_ids, B=B, Sk=Sk, Lq=Lq,
-                q0=int(q_global_start), rows=rows, nthreads=nthreads)
+                q0=int(q_global_start), rows=rows, nthreads=nthreads, softcap=softcap)
 
 
-def attn_fwd_dense(q, k, v, scale, causal, window=None, nthreads=None):
+def attn_fwd_dense(q, k, v, scale, causal, window=None, nthreads=None, softcap=None):
     """Dense forward on [B,H,N,D]: out [B,Hq,Nq,Dv], lse [B,Hq,Nq]; causal is bottom-right."""
     q, k, v = _f64(q), _f64(k), _f64(v)
     B, Hq, Nq, Dqk = q.shape
@@ -162,7 +167,8 @@ def attn_fwd_dense(q, k, v, scale, causal, window=None, nthreads=None):
     vp = v.transpose(0, 2, 1, 3).reshape(B * Nk, v.shape[1], v.shape[3])
     cu_q = np.arange(B + 1, dtype=np.int32) * Nq
     cu_k = np.arange(B + 1, dtype=np.int32) * Nk
-    out, lse = attn_fwd_segments(qp, kp, vp, cu_q, cu_k, scale, causal, window, nthreads=nthreads)
+    out, lse = attn_fwd_segments(qp, kp, vp, cu_q, cu_k, scale, causal, window, nthreads=nthreads,
+                                 softcap=softcap)
     out = out.reshape(B, Nq, Hq, -1).transpose(0, 2, 1, 3)
     lse = lse.reshape(Hq, B, Nq).transpose(1, 0, 2)
     return np.ascontiguousarray(out), np.ascontiguousarray(lse)
@@ -173,7 +179,7 @@ def attn_fwd_dense(q, k, v, scale, causal, window=None, nthreads=None):
 
 def _bwd(mode, dout, q, k, v, out, lse, scale, causal, window, cu_q=None, cu_k=None, doc_ids=None,
          B=0, Sk=0, Lq=0, q0=0, q_rows=None, k_rows=None, want_dq=True, want_dkdv=True,
-         nthreads=None):
+         nthreads=None, softcap=None):
     lib = _load()
     dout, q, k, v, out, lse = (_f64(x) for x in (dout, q, k, v, out, lse))
     Tq, Hq, Dqk = q.shape
@@ -185,7 +191,7 @@ def _bwd(mode, dout, q, k, v, out, lse, scale, causal, window, cu_q=None, cu_k=N
     q_rows, k_rows = _i32(q_rows), _i32(k_rows)
     rc = lib.oracle_attn_bwd(*_mask_args(mode, causal, window, cu_q, cu_k, doc_ids, B, Sk, Lq, q0),
                              _ptr(dout), _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), Tq, Tk,
-                             Hq, Hkv, Dqk, Dv, float(scale), _ptr(q_rows),
+                             Hq, Hkv, Dqk, Dv, float(scale), _softcap(softcap), _ptr(q_rows),
                              0 if q_rows is None else len(q_rows), _ptr(k_rows),
                              0 if k_rows is None else len(k_rows), _ptr(dq), _ptr(dk), _ptr(dv),
                              nthreads or default_threads())
@@ -195,24 +201,24 @@ def _bwd(mode, dout, q, k, v, out, lse, scale, causal, window, cu_q=None, cu_k=N
 
 
 def attn_bwd_segments(dout, q, k, v, out, lse, cu_q, cu_k, scale, causal, window=None, q_rows=None,
-                      k_rows=None, want_dq=True, want_dkdv=True, nthreads=None):
+                      k_rows=None, want_dq=True, want_dkdv=True, nthreads=None, softcap=None):
     """Packed backward from caller-supplied out [Tq,Hq,Dv] / lse [Hq,Tq] -> dq, dk, dv."""
     return _bwd(MODE_SEGMENTS, dout, q, k, v, out, lse, scale, causal, window, cu_q=_i32(cu_q),
                 cu_k=_i32(cu_k), q_rows=q_rows, k_rows=k_rows, want_dq=want_dq,
-                want_dkdv=want_dkdv, nthreads=nthreads)
+                want_dkdv=want_dkdv, nthreads=nthreads, softcap=softcap)
 
 
 def attn_bwd_document(dout, q, k, v, out, lse, doc_ids, q_global_start, scale, window=None,
-                      q_rows=None, k_rows=None, want_dq=True, want_dkdv=True, nthreads=None):
+                      q_rows=None, k_rows=None, want_dq=True, want_dkdv=True, nthreads=None, softcap=None):
     doc_ids = _i32(doc_ids)
     B, Sk = doc_ids.shape
     Lq = q.shape[0] // B
     return _bwd(MODE_DOCUMENT, dout, q, k, v, out, lse, scale, True, window, doc_ids=doc_ids, B=B,
                 Sk=Sk, Lq=Lq, q0=int(q_global_start), q_rows=q_rows, k_rows=k_rows,
-                want_dq=want_dq, want_dkdv=want_dkdv, nthreads=nthreads)
+                want_dq=want_dq, want_dkdv=want_dkdv, nthreads=nthreads, softcap=softcap)
 
 
-def attn_bwd_dense(dout, q, k, v, out, lse, scale, causal, window=None, nthreads=None):
+def attn_bwd_dense(dout, q, k, v, out, lse, scale, causal, window=None, nthreads=None, softcap=None):
     """Dense backward on [B,H,N,D] with lse [B,Hq,Nq]; returns dq, dk, dv in [B,H,N,D]."""
     dout, q, k, v, out, lse = (_f64(x) for x in (dout, q, k, v, out, lse))
     B, Hq, Nq, Dqk = q.shape
@@ -226,7 +232,7 @@ def attn_bwd_dense(dout, q, k, v, out, lse, scale, causal, window=None, nthreads
     cu_q = np.arange(B + 1, dtype=np.int32) * Nq
     cu_k = np.arange(B + 1, dtype=np.int32) * Nk
     dq, dk, dv = attn_bwd_segments(pack(dout), pack(q), pack(k), pack(v), pack(out), lse_p, cu_q,
-                                   cu_k, scale, causal, window, nthreads=nthreads)
+                                   cu_k, scale, causal, window, nthreads=nthreads, softcap=softcap)
 
     def unpack(x, N, H, D):
         return np.ascontiguousarray(x.reshape(B, N, H, D).transpose(0, 2, 1, 3))

@@ -30,6 +30,10 @@
  *      [nemo_automodel.components.attention.fa4, `document_causal_fa4_attention`
  *       ("padding queries are zero") and module docstring bullet 2 ("query at
  *       global position p sees keys of its document up to p")]
+ *  - softcap c > 0 (off by default): each logit z = scale * q . k becomes
+ *    c * tanh(z / c) before the mask and the softmax, and the backward carries
+ *    the factor 1 - tanh(z / c)^2 into dS.
+ *      [ffpa_attention page, `ffpa_attention_forward` softcap argument]
  *  - attention backward from the caller-supplied out and lse:
  *      Delta_i = dO_i . out_i,  P_ij = exp(scale q_i.k_j - lse_i) (0 when
  *      lse_i = -inf), dP_ij = dO_i . v_j, dS_ij = P_ij (dP_ij - Delta_i),
@@ -96,6 +100,7 @@ typedef struct {
     double *o_out, *lse_out, *dq, *dk, *dv, *delta;
     int Tq, Tk, Hq, Hkv, Dqk, Dv;
     double scale;
+    double softcap; /* > 0: logits capped as softcap * tanh(z / softcap); 0: off */
     const visibility *vis;
     const int32_t *rows; /* rows (or key rows) to evaluate */
     int nrows;
@@ -237,6 +242,27 @@ static void parallel_rows(const problem *pb, int nthreads, void (*fn)(const prob
     free(ws);
 }
 
+/* ---- logits ------------------------------------------------------------- */
+
+/*
+ * The logit of a (query, key) pair from q . k: z = scale * q . k, or with a
+ * softcap c > 0, c * tanh(z / c), applied before the mask and the softmax.
+ *   [ffpa_attention page, `ffpa_attention_forward` (softcap argument; the
+ *    eager attention it falls back to for softcap caps the scaled scores as
+ *    softcap * tanh(scores / softcap))]
+ */
+static double logit(const problem *pb, double qk) {
+    double z = pb->scale * qk;
+    return pb->softcap > 0.0 ? pb->softcap * tanh(z / pb->softcap) : z;
+}
+
+/* d logit / dz: 1 - tanh(z / c)^2 with a softcap, else 1. */
+static double logit_slope(const problem *pb, double qk) {
+    if (!(pb->softcap > 0.0)) return 1.0;
+    double t = tanh(pb->scale * qk / pb->softcap);
+    return 1.0 - t * t;
+}
+
 /* ---- forward ------------------------------------------------------------ */
 
 static void fwd_rows(const problem *pb, int begin, int end) {
@@ -260,7 +286,7 @@ static void fwd_rows(const problem *pb, int begin, int end) {
             double zmax = -INFINITY;
             for (int c = 0; c < nvis; ++c) {
                 const double *kj = pb->k + ((size_t)idx[c] * pb->Hkv + hk) * pb->Dqk;
-                z[c] = pb->scale * dot(qi, kj, pb->Dqk);
+                z[c] = logit(pb, dot(qi, kj, pb->Dqk));
                 if (z[c] > zmax) zmax = z[c];
             }
             double sum = 0.0;
@@ -310,8 +336,9 @@ static void dq_rows(const problem *pb, int begin, int end) {
             for (int c = 0; c < nvis; ++c) {
                 const double *kj = pb->k + ((size_t)idx[c] * pb->Hkv + hk) * pb->Dqk;
                 const double *vj = pb->v + ((size_t)idx[c] * pb->Hkv + hk) * pb->Dv;
-                double p = exp(pb->scale * dot(qi, kj, pb->Dqk) - lse);
-                double ds = p * (dot(gi, vj, pb->Dv) - delta);
+                double qk = dot(qi, kj, pb->Dqk);
+                double p = exp(logit(pb, qk) - lse);
+                double ds = p * (dot(gi, vj, pb->Dv) - delta) * logit_slope(pb, qk);
                 for (int d = 0; d < pb->Dqk; ++d) dq[d] += pb->scale * ds * kj[d];
             }
         }
@@ -340,8 +367,9 @@ static void dkdv_rows(const problem *pb, int begin, int end) {
                     if (lse == -INFINITY) continue;
                     const double *qi = pb->q + ((size_t)r * pb->Hq + h) * pb->Dqk;
                     const double *gi = pb->dout + ((size_t)r * pb->Hq + h) * pb->Dv;
-                    double p = exp(pb->scale * dot(qi, kj, pb->Dqk) - lse);
-                    double ds = p * (dot(gi, vj, pb->Dv) - pb->delta[(size_t)h * pb->Tq + r]);
+                    double qk = dot(qi, kj, pb->Dqk);
+                    double p = exp(logit(pb, qk) - lse);
+                    double ds = p * (dot(gi, vj, pb->Dv) - pb->delta[(size_t)h * pb->Tq + r]) * logit_slope(pb, qk);
                     for (int d = 0; d < pb->Dv; ++d) dv[d] += p * gi[d];
                     for (int d = 0; d < pb->Dqk; ++d) dk[d] += pb->scale * ds * qi[d];
                 }
@@ -387,7 +415,7 @@ static visibility make_visibility(int mode, int causal, int window, const int32_
 int oracle_attn_fwd(int mode, int causal, int window, const int32_t *cu_q, const int32_t *cu_k,
                     int nseg, const int32_t *doc_ids, int B, int Sk, int Lq, int q0,
                     const double *q, const double *k, const double *v, int Tq, int Tk, int Hq,
-                    int Hkv, int Dqk, int Dv, double scale, const int32_t *rows, int nrows,
+                    int Hkv, int Dqk, int Dv, double scale, double softcap, const int32_t *rows, int nrows,
                     double *out, double *lse, int nthreads) {
     if (Hkv <= 0 || Hq % Hkv != 0) return -1;
     visibility vz = make_visibility(mode, causal, window, cu_q, cu_k, nseg, doc_ids, B, Sk, Lq, q0);
@@ -412,6 +440,7 @@ int oracle_attn_fwd(int mode, int causal, int window, const int32_t *cu_q, const
     pb.Dqk = Dqk;
     pb.Dv = Dv;
     pb.scale = scale;
+    pb.softcap = softcap;
     pb.vis = &vz;
     pb.rows = rows;
     pb.nrows = nrows;
@@ -430,7 +459,7 @@ int oracle_attn_bwd(int mode, int causal, int window, const int32_t *cu_q, const
                     int nseg, const int32_t *doc_ids, int B, int Sk, int Lq, int q0,
                     const double *dout, const double *q, const double *k, const double *v,
                     const double *out, const double *lse, int Tq, int Tk, int Hq, int Hkv, int Dqk,
-                    int Dv, double scale, const int32_t *q_rows, int nq_rows, const int32_t *k_rows,
+                    int Dv, double scale, double softcap, const int32_t *q_rows, int nq_rows, const int32_t *k_rows,
                     int nk_rows, double *dq, double *dk, double *dv, int nthreads) {
     if (Hkv <= 0 || Hq % Hkv != 0) return -1;
     visibility vz = make_visibility(mode, causal, window, cu_q, cu_k, nseg, doc_ids, B, Sk, Lq, q0);
@@ -450,6 +479,7 @@ int oracle_attn_bwd(int mode, int causal, int window, const int32_t *cu_q, const
     pb.Dqk = Dqk;
     pb.Dv = Dv;
     pb.scale = scale;
+    pb.softcap = softcap;
     pb.vis = &vz;
     pb.delta = (double *)malloc(sizeof(double) * (size_t)Hq * (size_t)(Tq > 0 ? Tq : 1));
     int32_t *every_q = all_rows(Tq);

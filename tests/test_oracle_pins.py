@@ -676,3 +676,74 @@ def test_cross_chunk_decomposition_equals_document_mode(seed):
     live = oracle.live_rows(cq2, ck2)
     other = np.setdiff1d(np.arange(Lq), live)
     np.testing.assert_array_equal(dq[other], dq1[other])
+
+
+# ---------------------------------------------------------------------------
+# softcap pins
+
+def _segments_case(seed, Tq_lens, Tk_lens, Hq=2, Hkv=1, D=6):
+    r = np.random.default_rng(seed)
+    cu_q = np.concatenate([[0], np.cumsum(Tq_lens)]).astype(np.int32)
+    cu_k = np.concatenate([[0], np.cumsum(Tk_lens)]).astype(np.int32)
+    Tq, Tk = int(cu_q[-1]), int(cu_k[-1])
+    return (cu_q, cu_k, r.standard_normal((Tq, Hq, D)), r.standard_normal((Tk, Hkv, D)),
+            r.standard_normal((Tk, Hkv, D)), r.standard_normal((Tq, Hq, D)))
+
+
+def test_softcap_huge_cap_is_the_plain_attention():
+    cu_q, cu_k, q, k, v, do = _segments_case(1, [5, 9, 3], [7, 9, 6])
+    o0, l0 = oracle.attn_fwd_segments(q, k, v, cu_q, cu_k, 0.7, True)
+    o1, l1 = oracle.attn_fwd_segments(q, k, v, cu_q, cu_k, 0.7, True, softcap=1e7)
+    np.testing.assert_allclose(o1, o0, atol=1e-9)
+    np.testing.assert_allclose(l1, l0, atol=1e-9)
+    g0 = oracle.attn_bwd_segments(do, q, k, v, o0, l0, cu_q, cu_k, 0.7, True)
+    g1 = oracle.attn_bwd_segments(do, q, k, v, o1, l1, cu_q, cu_k, 0.7, True, softcap=1e7)
+    for a, b in zip(g1, g0):
+        np.testing.assert_allclose(a, b, atol=1e-8)
+
+
+def test_softcap_single_key_rows_closed_form():
+    # one visible key: out = v exactly and lse = c * tanh(scale * q.k / c)
+    cu_q, cu_k, q, k, v, _ = _segments_case(2, [1, 1], [1, 1], Hq=1)
+    c, scale = 3.0, 2.5
+    o, l = oracle.attn_fwd_segments(q, k, v, cu_q, cu_k, scale, True, softcap=c)
+    for row in range(2):
+        np.testing.assert_allclose(o[row, 0], v[row, 0], atol=1e-14)
+        z = scale * float(q[row, 0] @ k[row, 0])
+        assert abs(l[0, row] - c * np.tanh(z / c)) < 1e-14
+
+
+def test_softcap_bounds_every_logit():
+    # all capped logits lie in (-c, c), so log n - c < lse < log n + c for a row
+    # seeing n keys, however large the raw scores
+    cu_q, cu_k, q, k, v, _ = _segments_case(3, [6, 4], [6, 11], Hq=2)
+    c = 1.5
+    _, l = oracle.attn_fwd_segments(q * 40, k * 40, v, cu_q, cu_k, 1.0, False, softcap=c)
+    n = np.repeat(np.diff(cu_k), np.diff(cu_q))
+    assert np.all(l < np.log(n)[None, :] + c) and np.all(l > np.log(n)[None, :] - c)
+
+
+@pytest.mark.parametrize("causal,window", [(True, None), (False, 3)])
+def test_softcap_gradients_match_finite_differences(causal, window):
+    # d/dx of L = sum(dO * out) by central differences against the analytic
+    # backward (which carries the 1 - tanh^2 factor of the cap)
+    cu_q, cu_k, q, k, v, do = _segments_case(4, [4, 3], [5, 3], Hq=2, Hkv=1, D=3)
+    c, scale = 1.2, 0.9
+
+    def loss(q_, k_, v_):
+        o, _ = oracle.attn_fwd_segments(q_, k_, v_, cu_q, cu_k, scale, causal, window, softcap=c, nthreads=1)
+        return float((o * do).sum())
+
+    o, l = oracle.attn_fwd_segments(q, k, v, cu_q, cu_k, scale, causal, window, softcap=c)
+    dq, dk, dv = oracle.attn_bwd_segments(do, q, k, v, o, l, cu_q, cu_k, scale, causal, window, softcap=c)
+    eps = 1e-6
+    for x, g in ((q, dq), (k, dk), (v, dv)):
+        num = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += eps
+            xm[idx] -= eps
+            args_p = [xp if y is x else y for y in (q, k, v)]
+            args_m = [xm if y is x else y for y in (q, k, v)]
+            num[idx] = (loss(*args_p) - loss(*args_m)) / (2 * eps)
+        np.testing.assert_allclose(g, num, atol=2e-7)
