@@ -118,6 +118,12 @@ size_t psf_attn_bwd_workspace_size(int64_t total_q_rows, int64_t total_k_rows, i
  *  from it on the device and `nseg` is only the capacity of cu_q/cu_k.
  *  max_q / max_k: the longest segment lengths (ignored when dev_meta is given);
  *  a longer segment is a PSF_EDEVICE_ARGS device status.
+ *  softcap: 0 (off), or c > 0: every logit z = scale * q . k becomes
+ *  c * tanh(z / c) before the mask and the softmax (lse is over the capped
+ *  logits). Negative or non-finite values are PSF_EINVAL.
+ *                           [ffpa_attention page, `ffpa_attention_forward`
+ *                            softcap argument; the eager attention the page
+ *                            falls back to for it caps the scaled scores so]
  *  flags: 0, or PSF_FWD_PACK_GQA: the G = Hq / Hkv query heads of a KV head
  *  share one 128-row tile (128 / G rows of each), so short segments fill the
  *  tile and K/V are loaded once for all G heads. Same results; it applies to
@@ -132,7 +138,7 @@ size_t psf_attn_bwd_workspace_size(int64_t total_q_rows, int64_t total_k_rows, i
 int psf_attn_varlen_fwd(const void* q, const void* k, const void* v, void* out, float* lse, const int32_t* cu_q,
                         const int32_t* cu_k, const int32_t* dev_meta, int nseg, int max_q, int max_k, int layout,
                         int dtype, int B, int Sq, int Sk, int Hq, int Hkv, int Dqk, int Dv, float scale, int causal,
-                        int32_t window_left, int flags, void* workspace, size_t ws_bytes, void* stream);
+                        int32_t window_left, float softcap, int flags, void* workspace, size_t ws_bytes, void* stream);
 
 /*
  * Varlen forward that allocates nothing and takes no workspace.
@@ -142,8 +148,8 @@ int psf_attn_varlen_fwd(const void* q, const void* k, const void* v, void* out, 
  *  device memory up front and hand out nothing afterwards, plugin hosts that
  *  own every allocation, or code that must not touch the allocator while a
  *  step runs. This entry point behaves like psf_attn_varlen_fwd (same
- *  arguments minus flags, workspace and ws_bytes, one query head per tile,
- *  same results) but keeps its tile
+ *  arguments minus softcap, flags, workspace and ws_bytes: no softcap, one
+ *  query head per tile, same results) but keeps its tile
  *  schedule in a fixed array in the library's device memory (852,736 bytes,
  *  held on every GPU that loads the library until the process exits).
  *  Limits: B * Sq <= PSF_NOALLOC_MAX_Q_ROWS and nseg <= PSF_NOALLOC_MAX_SEGMENTS;
@@ -172,6 +178,7 @@ int psf_attn_varlen_fwd_noalloc(const void* q, const void* k, const void* v, voi
  *  the Hq / Hkv query heads sharing a KV head are summed on chip).
  *  Keys that no query sees get dk = dv = 0; query rows outside every segment
  *  get dq = 0.
+ *  softcap: the forward's (0 = off); with c > 0, dS carries 1 - tanh^2(z / c).
  *  workspace: psf_attn_bwd_workspace_size(Tq, Tk, nseg, Hq, Hkv, Dqk, Dv) bytes
  *  (holds the fp32 dQ, dK and dV accumulators, Delta = rowsum(dO * out) and the
  *  tile schedule).
@@ -180,7 +187,7 @@ int psf_attn_varlen_bwd(const void* dout, const void* q, const void* k, const vo
                         const float* lse, void* dq, void* dk, void* dv, const int32_t* cu_q, const int32_t* cu_k,
                         const int32_t* dev_meta, int nseg, int max_q, int max_k, int layout, int dtype, int B, int Sq,
                         int Sk, int Hq, int Hkv, int Dqk, int Dv, float scale, int causal, int32_t window_left,
-                        void* workspace, size_t ws_bytes, void* stream);
+                        float softcap, void* workspace, size_t ws_bytes, void* stream);
 
 /*
  * Dense forward on SDPA-layout tensors.
@@ -190,12 +197,12 @@ int psf_attn_varlen_bwd(const void* dout, const void* q, const void* k, const vo
  *                            fa4 page, `causal_fa4_attention`]
  *  q [B,Hq,Nq,Dqk], k [B,Hkv,Nk,Dqk], v [B,Hkv,Nk,Dv], out [B,Hq,Nq,Dv],
  *  lse [B,Hq,Nq]. Causal is bottom-right aligned when Nq != Nk.
- *  flags: as for psf_attn_varlen_fwd (0 or PSF_FWD_PACK_GQA).
+ *  softcap, flags: as for psf_attn_varlen_fwd.
  *  workspace: psf_attn_fwd_workspace_size(B * Nq, B) bytes.
  */
 int psf_attn_dense_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq, int Hkv,
                        int Nq, int Nk, int Dqk, int Dv, int dtype, float scale, int causal, int32_t window_left,
-                       int flags, void* workspace, size_t ws_bytes, void* stream);
+                       float softcap, int flags, void* workspace, size_t ws_bytes, void* stream);
 
 /*
  * Dense backward.           [ffpa_attention page, `_ffpa_dense_bwd`: returns
@@ -204,8 +211,8 @@ int psf_attn_dense_fwd(const void* q, const void* k, const void* v, void* out, f
  */
 int psf_attn_dense_bwd(const void* dout, const void* q, const void* k, const void* v, const void* out,
                        const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Nq, int Nk,
-                       int Dqk, int Dv, int dtype, float scale, int causal, int32_t window_left, void* workspace,
-                       size_t ws_bytes, void* stream);
+                       int Dqk, int Dv, int dtype, float scale, int causal, int32_t window_left, float softcap,
+                       void* workspace, size_t ws_bytes, void* stream);
 
 /*
  * Doc ids -> varlen segments, on the GPU.

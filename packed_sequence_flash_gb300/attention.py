@@ -106,12 +106,16 @@ def _varlen_dims(q, k, v, layout):
     return PSF_LAYOUT_BHSD, B, Sq, Sk, Hq, Hkv, Dqk, v.shape[3]
 
 
+def _cap(softcap):
+    return float(softcap) if softcap else 0.0
+
+
 def attn_varlen_fwd(q, k, v, cu_q, cu_k, max_q, max_k, scale, causal, window=None, dev_meta=None,
-                    layout="thd", out=None, lse=None, workspace=None, pack_gqa=False):
+                    layout="thd", out=None, lse=None, workspace=None, pack_gqa=False, softcap=None):
     """Packed varlen forward -> (out, lse). cu_q/cu_k int32 [nseg+1] on the device.
     q, k, v: bf16 or fp16 (one type); out has their type, lse is fp32.
     pack_gqa: the query heads of a KV head share one tile (same results; for
-    short segments)."""
+    short segments). softcap > 0 caps each logit as softcap * tanh(logit / softcap)."""
     dt = _dtype_code([(q, "q"), (k, "k"), (v, "v")])
     _i32(cu_q, "cu_q")
     _i32(cu_k, "cu_k")
@@ -126,13 +130,14 @@ def attn_varlen_fwd(q, k, v, cu_q, cu_k, max_q, max_k, scale, causal, window=Non
     rc = _lib.load().psf_attn_varlen_fwd(
         _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(cu_q), _ptr(cu_k), _ptr(dev_meta), nseg,
         int(max_q), int(max_k), lay, dt, B, Sq, Sk, Hq, Hkv, Dqk, Dv, float(scale), int(bool(causal)),
-        _window(window), PSF_FWD_PACK_GQA if pack_gqa else 0, _ptr(workspace), workspace.numel(), _stream())
+        _window(window), _cap(softcap), PSF_FWD_PACK_GQA if pack_gqa else 0, _ptr(workspace), workspace.numel(),
+        _stream())
     check(rc)
     return out, lse
 
 
 def attn_varlen_bwd(dout, q, k, v, out, lse, cu_q, cu_k, max_q, max_k, scale, causal, window=None,
-                    dev_meta=None, layout="thd", workspace=None):
+                    dev_meta=None, layout="thd", workspace=None, softcap=None):
     """Packed varlen backward from caller-supplied out/lse -> (dq, dk, dv) in the inputs' type."""
     dt = _dtype_code([(dout, "dout"), (q, "q"), (k, "k"), (v, "v"), (out, "out")])
     _need(lse, "lse", torch.float32)
@@ -148,7 +153,7 @@ def attn_varlen_bwd(dout, q, k, v, out, lse, cu_q, cu_k, max_q, max_k, scale, ca
     rc = _lib.load().psf_attn_varlen_bwd(
         _ptr(dout), _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(cu_q),
         _ptr(cu_k), _ptr(dev_meta), nseg, int(max_q), int(max_k), lay, dt, B, Sq, Sk, Hq, Hkv, Dqk, Dv, float(scale),
-        int(bool(causal)), _window(window), _ptr(workspace), workspace.numel(), _stream())
+        int(bool(causal)), _window(window), _cap(softcap), _ptr(workspace), workspace.numel(), _stream())
     check(rc)
     return dq, dk, dv
 
@@ -156,7 +161,7 @@ def attn_varlen_bwd(dout, q, k, v, out, lse, cu_q, cu_k, max_q, max_k, scale, ca
 # ---------------------------------------------------------------------------
 # dense [B, H, N, D]
 
-def attn_dense_fwd(q, k, v, scale, causal, window=None, workspace=None, pack_gqa=False):
+def attn_dense_fwd(q, k, v, scale, causal, window=None, workspace=None, pack_gqa=False, softcap=None):
     """Dense forward -> (out [B,Hq,Nq,Dv] in the inputs' type, lse [B,Hq,Nq] fp32)."""
     dt = _dtype_code([(q, "q"), (k, "k"), (v, "v")])
     B, Hq, Nq, Dqk = q.shape
@@ -167,14 +172,14 @@ def attn_dense_fwd(q, k, v, scale, causal, window=None, workspace=None, pack_gqa
     if workspace is None:
         workspace = _workspace(fwd_workspace_size(B * Nq, B), q.device)
     rc = _lib.load().psf_attn_dense_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, Nq, Nk, Dqk,
-                                        Dv, dt, float(scale), int(bool(causal)), _window(window),
+                                        Dv, dt, float(scale), int(bool(causal)), _window(window), _cap(softcap),
                                         PSF_FWD_PACK_GQA if pack_gqa else 0, _ptr(workspace), workspace.numel(),
                                         _stream())
     check(rc)
     return out, lse
 
 
-def attn_dense_bwd(dout, q, k, v, out, lse, scale, causal, window=None, workspace=None):
+def attn_dense_bwd(dout, q, k, v, out, lse, scale, causal, window=None, workspace=None, softcap=None):
     """Dense backward -> (dq, dk, dv) in [B,H,N,D], dk/dv at Hkv heads."""
     dt = _dtype_code([(dout, "dout"), (q, "q"), (k, "k"), (v, "v"), (out, "out")])
     _need(lse, "lse", torch.float32)
@@ -186,8 +191,8 @@ def attn_dense_bwd(dout, q, k, v, out, lse, scale, causal, window=None, workspac
         workspace = _workspace(bwd_workspace_size(B * Nq, B * Nk, B, Hq, Hkv, Dqk, Dv), q.device)
     rc = _lib.load().psf_attn_dense_bwd(_ptr(dout), _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dq),
                                         _ptr(dk), _ptr(dv), B, Hq, Hkv, Nq, Nk, Dqk, Dv, dt, float(scale),
-                                        int(bool(causal)), _window(window), _ptr(workspace), workspace.numel(),
-                                        _stream())
+                                        int(bool(causal)), _window(window), _cap(softcap), _ptr(workspace),
+                                        workspace.numel(), _stream())
     check(rc)
     return dq, dk, dv
 
@@ -237,7 +242,7 @@ def chunk_dense_eligible(kv_doc_ids, q_start, q_length, k_start, k_length):
     return bool(f[0]), bool(f[1])
 
 
-def chunk_attention(q, k, v, kv_doc_ids, q_start, k_start, scale, causal, window=None, dense=None):
+def chunk_attention(q, k, v, kv_doc_ids, q_start, k_start, scale, causal, window=None, dense=None, softcap=None):
     """One chunk of the ring decomposition on one device: the query shard
     [q_start, q_start + Lq) of every row, q [B, Hq, Lq, Dqk], against the key
     chunk [k_start, k_start + Lk), k [B, Hkv, Lk, Dqk] / v [B, Hkv, Lk, Dv], with
@@ -247,7 +252,8 @@ def chunk_attention(q, k, v, kv_doc_ids, q_start, k_start, scale, causal, window
     document-causal mask, optional left window); causal=False the cross role
     (the chunk before the shard, no mask inside the shared document).
     dense=None routes by chunk_dense_eligible (one host read); True / False
-    force the dense kernels (then pad_fixup) or the segment path.
+    force the dense kernels (then pad_fixup) or the segment path. softcap > 0
+    caps the logits (the backward takes it from the plan).
     Returns (out, lse, plan); plan feeds chunk_attention_backward.
     """
     if not causal and window is not None:
@@ -258,25 +264,26 @@ def chunk_attention(q, k, v, kv_doc_ids, q_start, k_start, scale, causal, window
         local, cross = chunk_dense_eligible(kv_doc_ids, q_start, Lq, k_start, Lk)
         dense = local if causal else cross
     if dense:
-        out, lse = attn_dense_fwd(q, k, v, scale, causal, window)
+        out, lse = attn_dense_fwd(q, k, v, scale, causal, window, softcap=softcap)
         pad_fixup(out, lse, kv_doc_ids[:, q_start:q_start + Lq].contiguous(), "bhsd")
-        return out, lse, ("dense", causal, window)
+        return out, lse, ("dense", causal, window, softcap)
     if causal:
         ids_chunk = kv_doc_ids[:, k_start:k_start + Lk].contiguous()
         cu_q, cu_k, meta, _ = build_doc_segments(ids_chunk, Lq, q_start - k_start, skip_pad=True)
     else:
         cu_q, cu_k, meta = build_cross_segments(kv_doc_ids, q_start, Lq, k_start, Lk)
-    out, lse = attn_varlen_fwd(q, k, v, cu_q, cu_k, -1, -1, scale, causal, window, dev_meta=meta, layout="bhsd")
-    return out, lse, ("segments", causal, window, cu_q, cu_k, meta)
+    out, lse = attn_varlen_fwd(q, k, v, cu_q, cu_k, -1, -1, scale, causal, window, dev_meta=meta, layout="bhsd",
+                               softcap=softcap)
+    return out, lse, ("segments", causal, window, softcap, cu_q, cu_k, meta)
 
 
 def chunk_attention_backward(dout, q, k, v, out, lse, plan, scale):
     """Backward of chunk_attention from the (possibly merged) out/lse -> (dq, dk, dv)."""
     if plan[0] == "dense":
-        return attn_dense_bwd(dout, q, k, v, out, lse, scale, plan[1], plan[2])
-    _, causal, window, cu_q, cu_k, meta = plan
+        return attn_dense_bwd(dout, q, k, v, out, lse, scale, plan[1], plan[2], softcap=plan[3])
+    _, causal, window, softcap, cu_q, cu_k, meta = plan
     return attn_varlen_bwd(dout, q, k, v, out, lse, cu_q, cu_k, -1, -1, scale, causal, window, dev_meta=meta,
-                           layout="bhsd")
+                           layout="bhsd", softcap=softcap)
 
 
 def pad_fixup(out, lse, q_doc_ids, layout="thd"):
@@ -358,7 +365,7 @@ def grad_add_live_rows(dst, src, cu_q, cu_k, dev_meta=None):
 # document-causal composition [fa4 page, document_causal_fa4_attention]
 
 def document_causal_attention(q, k, v, q_doc_ids, kv_doc_ids, q_global_start, scale, window=None, skip_pad=True,
-                              pack_gqa=False):
+                              pack_gqa=False, softcap=None):
     """Causal per-document attention of a local query shard against global keys.
 
     q [B, Hq, Lq, Dqk], k [B, Hkv, Sk, Dqk], v [B, Hkv, Sk, Dv] (or packed
@@ -371,7 +378,7 @@ def document_causal_attention(q, k, v, q_doc_ids, kv_doc_ids, q_global_start, sc
     padding pairs; False runs padding runs as ordinary segments and zeroes
     the padding queries afterwards with pad_fixup (q_doc_ids is read only then).
     pack_gqa: the forward packs a KV head's query heads into one tile (short
-    documents).
+    documents). softcap > 0 caps the logits (pass the same value to the backward).
     """
     layout = "thd" if q.dim() == 3 else "bhsd"
     if kv_doc_ids.dim() == 1:
@@ -381,15 +388,15 @@ def document_causal_attention(q, k, v, q_doc_ids, kv_doc_ids, q_global_start, sc
     Lq = q.shape[0] if layout == "thd" else q.shape[2]
     cu_q, cu_k, meta, _ = build_doc_segments(kv_doc_ids, Lq, q_global_start, skip_pad=skip_pad)
     out, lse = attn_varlen_fwd(q, k, v, cu_q, cu_k, -1, -1, scale, True, window, dev_meta=meta, layout=layout,
-                               pack_gqa=pack_gqa)
+                               pack_gqa=pack_gqa, softcap=softcap)
     if not skip_pad:
         pad_fixup(out, lse, q_doc_ids, layout)
     return out, lse, (cu_q, cu_k, meta)
 
 
-def document_causal_attention_backward(dout, q, k, v, out, lse, segments, scale, window=None):
+def document_causal_attention_backward(dout, q, k, v, out, lse, segments, scale, window=None, softcap=None):
     """Backward of document_causal_attention from its out/lse -> (dq, dk, dv)."""
     layout = "thd" if q.dim() == 3 else "bhsd"
     cu_q, cu_k, meta = segments
     return attn_varlen_bwd(dout, q, k, v, out, lse, cu_q, cu_k, -1, -1, scale, True, window, dev_meta=meta,
-                           layout=layout)
+                           layout=layout, softcap=softcap)

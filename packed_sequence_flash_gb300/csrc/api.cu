@@ -226,6 +226,11 @@ int check_common(int layout, int B, int Sq, int Sk, int Hq, int Hkv, int Dqk, in
   return PSF_OK;
 }
 
+int check_softcap(float softcap) {
+  if (!(softcap >= 0.f) || !isfinite(softcap)) return fail(PSF_EINVAL, "softcap must be finite and >= 0 (got %g)", (double)softcap);
+  return PSF_OK;
+}
+
 int check_dtype(int dtype) {
   if (dtype != PSF_DTYPE_BF16 && dtype != PSF_DTYPE_F16) return fail(PSF_EINVAL, "unknown dtype %d", dtype);
   return PSF_OK;
@@ -244,9 +249,10 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, void* out, float*
                   const int32_t* cu_k, const int32_t* dev_meta, int nseg, int max_q, int max_k, int layout, int dtype,
                   int B,
                   int Sq, int Sk, int Hq, int Hkv, int Dqk, int Dv, float scale, int causal, int32_t window, void* ws,
-                  size_t ws_bytes, void* stream, int flags = 0) {
+                  size_t ws_bytes, void* stream, int flags = 0, float softcap = 0.f) {
   int rc = check_common(layout, B, Sq, Sk, Hq, Hkv, Dqk, Dv, scale, window, nseg);
   if (rc) return rc;
+  if ((rc = check_softcap(softcap))) return rc;
   if ((rc = check_dtype(dtype))) return rc;
   if (flags & ~PSF_FWD_PACK_GQA) return fail(PSF_EINVAL, "unknown forward flags 0x%x", flags);
   // Packed query heads: the G = Hq / Hkv heads of a KV head share one tile of
@@ -300,6 +306,7 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, void* out, float*
   p.pack = pack;
   p.dv_parts = Dv == 512 ? 2 : 1;
   p.scale_log2 = scale * 1.4426950408889634f;
+  p.softcap = softcap;
   p.items = w.items;
   p.n_items = w.n_items;
   p.work_next = w.n_items + 1;
@@ -317,9 +324,11 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, void* out, float*
 int attn_bwd_impl(const void* dout, const void* q, const void* k, const void* v, const void* out, const float* lse,
                   void* dq, void* dk, void* dv, const int32_t* cu_q, const int32_t* cu_k, const int32_t* dev_meta,
                   int nseg, int max_q, int max_k, int layout, int dtype, int B, int Sq, int Sk, int Hq, int Hkv,
-                  int Dqk, int Dv, float scale, int causal, int32_t window, void* ws, size_t ws_bytes, void* stream) {
+                  int Dqk, int Dv, float scale, int causal, int32_t window, void* ws, size_t ws_bytes, void* stream,
+                  float softcap = 0.f) {
   int rc = check_common(layout, B, Sq, Sk, Hq, Hkv, Dqk, Dv, scale, window, nseg);
   if (rc) return rc;
+  if ((rc = check_softcap(softcap))) return rc;
   if ((rc = check_dtype(dtype))) return rc;
   const int f16 = dtype == PSF_DTYPE_F16;
   if (bwd_smem_bytes(Dqk, Dv) < 0)
@@ -394,6 +403,7 @@ int attn_bwd_impl(const void* dout, const void* q, const void* k, const void* v,
     p.Hkv = Hkv;
     p.scale = scale;
     p.scale_log2 = scale * 1.4426950408889634f;
+    p.softcap = softcap;
     p.items = w.items;
     p.n_items = w.n_items;
     p.work_next = w.n_items + 1;
@@ -511,10 +521,10 @@ size_t psf_attn_bwd_workspace_size(int64_t total_q_rows, int64_t total_k_rows, i
 int psf_attn_varlen_fwd(const void* q, const void* k, const void* v, void* out, float* lse, const int32_t* cu_q,
                         const int32_t* cu_k, const int32_t* dev_meta, int nseg, int max_q, int max_k, int layout,
                         int dtype, int B, int Sq, int Sk, int Hq, int Hkv, int Dqk, int Dv, float scale, int causal,
-                        int32_t window_left, int flags, void* workspace, size_t ws_bytes, void* stream) {
+                        int32_t window_left, float softcap, int flags, void* workspace, size_t ws_bytes, void* stream) {
   if (!cu_q || !cu_k) return fail(PSF_EINVAL, "varlen calls need cu_q and cu_k");
   return attn_fwd_impl(q, k, v, out, lse, cu_q, cu_k, dev_meta, nseg, max_q, max_k, layout, dtype, B, Sq, Sk, Hq, Hkv,
-                       Dqk, Dv, scale, causal, window_left, workspace, ws_bytes, stream, flags);
+                       Dqk, Dv, scale, causal, window_left, workspace, ws_bytes, stream, flags, softcap);
 }
 
 int psf_attn_varlen_fwd_noalloc(const void* q, const void* k, const void* v, void* out, float* lse,
@@ -540,25 +550,26 @@ int psf_attn_varlen_bwd(const void* dout, const void* q, const void* k, const vo
                         const float* lse, void* dq, void* dk, void* dv, const int32_t* cu_q, const int32_t* cu_k,
                         const int32_t* dev_meta, int nseg, int max_q, int max_k, int layout, int dtype, int B, int Sq,
                         int Sk, int Hq, int Hkv, int Dqk, int Dv, float scale, int causal, int32_t window_left,
-                        void* workspace, size_t ws_bytes, void* stream) {
+                        float softcap, void* workspace, size_t ws_bytes, void* stream) {
   if (!cu_q || !cu_k) return fail(PSF_EINVAL, "varlen calls need cu_q and cu_k");
   return attn_bwd_impl(dout, q, k, v, out, lse, dq, dk, dv, cu_q, cu_k, dev_meta, nseg, max_q, max_k, layout, dtype, B,
-                       Sq, Sk, Hq, Hkv, Dqk, Dv, scale, causal, window_left, workspace, ws_bytes, stream);
+                       Sq, Sk, Hq, Hkv, Dqk, Dv, scale, causal, window_left, workspace, ws_bytes, stream, softcap);
 }
 
 int psf_attn_dense_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq, int Hkv,
                        int Nq, int Nk, int Dqk, int Dv, int dtype, float scale, int causal, int32_t window_left,
-                       int flags, void* workspace, size_t ws_bytes, void* stream) {
+                       float softcap, int flags, void* workspace, size_t ws_bytes, void* stream) {
   return attn_fwd_impl(q, k, v, out, lse, nullptr, nullptr, nullptr, B, Nq, Nk, PSF_LAYOUT_BHSD, dtype, B, Nq, Nk, Hq,
-                       Hkv, Dqk, Dv, scale, causal, window_left, workspace, ws_bytes, stream, flags);
+                       Hkv, Dqk, Dv, scale, causal, window_left, workspace, ws_bytes, stream, flags, softcap);
 }
 
 int psf_attn_dense_bwd(const void* dout, const void* q, const void* k, const void* v, const void* out,
                        const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Nq, int Nk,
-                       int Dqk, int Dv, int dtype, float scale, int causal, int32_t window_left, void* workspace,
-                       size_t ws_bytes, void* stream) {
+                       int Dqk, int Dv, int dtype, float scale, int causal, int32_t window_left, float softcap,
+                       void* workspace, size_t ws_bytes, void* stream) {
   return attn_bwd_impl(dout, q, k, v, out, lse, dq, dk, dv, nullptr, nullptr, nullptr, B, Nq, Nk, PSF_LAYOUT_BHSD,
-                       dtype, B, Nq, Nk, Hq, Hkv, Dqk, Dv, scale, causal, window_left, workspace, ws_bytes, stream);
+                       dtype, B, Nq, Nk, Hq, Hkv, Dqk, Dv, scale, causal, window_left, workspace, ws_bytes, stream,
+                       softcap);
 }
 
 int psf_build_doc_segments(const int32_t* kv_doc_ids, int B, int Sk, int q_length, int q_global_start,

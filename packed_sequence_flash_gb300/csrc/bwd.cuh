@@ -47,6 +47,7 @@ struct BwdParams {
   int64_t v_sb, v_ss, v_sh;
   int Hq, Hkv;
   float scale, scale_log2;
+  float softcap;  // > 0: logits capped as softcap * tanh(logit / softcap) (the CAP kernels)
   const int4* items;  // (segment, key tile, first step, end step), heaviest first
   const int* n_items;
   int* work_next;  // zeroed by the schedule kernel; kernels that take work dynamically count on it
@@ -75,6 +76,8 @@ struct BwdCfg {
   static constexpr int T_DK = DUAL ? DV : 128;
   static constexpr int T_A = DUAL ? 256 : 320;
   static constexpr int T_B = DUAL ? 384 : 320;
+  // Single-region plan with a softcap: P^T (1 - tanh^2), packed, between the passes.
+  static constexpr int T_PF = 448;
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
   static_assert(DUAL || (DQK == 192 && DV == 128), "single-region plan is laid out for (192, 128)");
 };
@@ -108,7 +111,8 @@ __device__ __forceinline__ BwdItem bwd_decode(const BwdParams& p, int w) {
   return t;
 }
 
-template <typename T, int DQK, int DV>
+// CAP: logits softcapped (p.softcap > 0); dS carries the cap's 1 - tanh^2.
+template <typename T, int DQK, int DV, bool CAP>
 __global__ void __launch_bounds__(384, 1) attn_bwd_kernel(const __grid_constant__ BwdParams p) {
   using C = BwdCfg<DQK, DV>;
   extern __shared__ uint8_t smem_raw[];
@@ -297,6 +301,21 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_kernel(const __grid_constant_
     uint8_t* pt_s = smem + C::PT_OFF;
     uint8_t* ds_s = smem + C::DS_OFF;
     const float sl2 = p.scale_log2;
+    const float cap_c2 = CAP ? p.softcap * 1.4426950408889634f : 0.f;
+    const float cap_k1 = CAP ? 2.f * sl2 / p.softcap : 0.f, cap_ic2 = CAP ? 1.f / cap_c2 : 0.f;
+    // P (and, with CAP, the factor 1 - tanh^2 of the capped logit) of score s
+    // for a row whose lse (log2 units) is l2.
+    auto prob = [&](float s, float l2, float& fac) -> float {
+      if constexpr (CAP) {
+        const float y = softcap_log2(s, cap_k1, cap_c2);
+        const float tt = y * cap_ic2;
+        fac = fmaf(-tt, tt, 1.f);
+        return ex2_approx(y - l2);
+      } else {
+        fac = 1.f;
+        return ex2_approx(fmaf(s, sl2, -l2));
+      }
+    };
     uint32_t nz = 0, gstep = 0;
     bool ok = true;
     for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
@@ -380,10 +399,11 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_kernel(const __grid_constant_
 #pragma unroll
                 for (int u = 0; u < 2; ++u) {
                   const int qc = c * 32 + 2 * e + u;
-                  float pe = ex2_approx(fmaf(__uint_as_float(sv[2 * e + u]), sl2, -my_lse[qc]));
+                  float fe;
+                  float pe = prob(__uint_as_float(sv[2 * e + u]), my_lse[qc], fe);
                   if (masked && (qc < q_lo || qc >= q_hi)) pe = 0.f;
                   pr[u] = pe;
-                  dr[u] = pe * (__uint_as_float(pv[2 * e + u]) - my_dl[qc]);
+                  dr[u] = pe * fe * (__uint_as_float(pv[2 * e + u]) - my_dl[qc]);
                 }
                 pk[e] = pack2<T>(pr[0], pr[1]);
                 dk2[e] = pack2<T>(dr[0], dr[1]);
@@ -402,24 +422,31 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_kernel(const __grid_constant_
             for (int c = 0; c < 4; ++c) {
               uint32_t sv[32];
               tmem_ld32(rs + c * 32, sv);
-              uint32_t pk[16];
+              uint32_t pk[16], pfk[16];
 #pragma unroll
               for (int e = 0; e < 16; ++e) {
-                float pr[2];
+                float pr[2], pf[2];
 #pragma unroll
                 for (int u = 0; u < 2; ++u) {
                   const int qc = c * 32 + 2 * e + u;
-                  float pe = ex2_approx(fmaf(__uint_as_float(sv[2 * e + u]), sl2, -my_lse[qc]));
+                  float fe;
+                  float pe = prob(__uint_as_float(sv[2 * e + u]), my_lse[qc], fe);
                   if (masked && (qc < q_lo || qc >= q_hi)) pe = 0.f;
                   pr[u] = pe;
+                  pf[u] = pe * fe;
                 }
                 pk[e] = pack2<T>(pr[0], pr[1]);
+                if constexpr (CAP) pfk[e] = pack2<T>(pf[0], pf[1]);
               }
               const int chunk = c >> 1, g0 = (c & 1) * 4;
 #pragma unroll
-              for (int u = 0; u < 4; ++u)
-                *reinterpret_cast<uint4*>(pt_s + chunk * kChunkBytes + sw128_offset(r, g0 + u)) =
-                    make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+              for (int u = 0; u < 4; ++u) {
+                const uint32_t off = chunk * kChunkBytes + sw128_offset(r, g0 + u);
+                *reinterpret_cast<uint4*>(pt_s + off) = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+              }
+              // With CAP, P^T (1 - tanh^2) waits in TMEM (the dS^T buffer is
+              // P^T's own in this plan) for the second pass.
+              if constexpr (CAP) tmem_st16(tmem + lane_base + C::T_PF + c * 16, pfk);
             }
             fence_proxy_async_smem();
             tc_fence_before();
@@ -435,10 +462,12 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_kernel(const __grid_constant_
               uint32_t pv[32];
               tmem_ld32(rp + c * 32, pv);
               const int chunk = c >> 1, g0 = (c & 1) * 4;
-              uint32_t dk2[16];
+              uint32_t dk2[16], pfw[16];
+              if constexpr (CAP) tmem_ld16(tmem + lane_base + C::T_PF + c * 16, pfw);
 #pragma unroll
               for (int u = 0; u < 4; ++u) {
-                const uint4 pp = *reinterpret_cast<const uint4*>(pt_s + chunk * kChunkBytes + sw128_offset(r, g0 + u));
+                const uint4 pp = CAP ? make_uint4(pfw[4 * u], pfw[4 * u + 1], pfw[4 * u + 2], pfw[4 * u + 3])
+                                     : *reinterpret_cast<const uint4*>(pt_s + chunk * kChunkBytes + sw128_offset(r, g0 + u));
                 const uint32_t pw[4] = {pp.x, pp.y, pp.z, pp.w};
 #pragma unroll
                 for (int e2 = 0; e2 < 4; ++e2) {

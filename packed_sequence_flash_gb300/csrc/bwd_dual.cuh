@@ -67,7 +67,11 @@ struct BwdDualCfg {
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
 
-template <typename T, int DQK, int DV>
+// CAP: logits softcapped (p.softcap > 0). Pass 1 then also writes
+// P (1 - tanh^2) of the capped logit, packed, into the other 32 columns of
+// its half of region A (S^T columns it has already read and dV never reads),
+// and pass 2 takes dS^T from those instead of from P^T.
+template <typename T, int DQK, int DV, bool CAP>
 __global__ void __launch_bounds__(512, 1) attn_bwd_dual_kernel(const __grid_constant__ BwdParams p) {
   using C = BwdDualCfg<DQK, DV>;
   extern __shared__ uint8_t smem_raw[];
@@ -337,6 +341,8 @@ __global__ void __launch_bounds__(512, 1) attn_bwd_dual_kernel(const __grid_cons
     uint8_t* epi = smem + C::DS_OFF + (half * 4 + wq) * 4096;  // one 4 KB box per warp, used between units
     const float sl2 = p.scale_log2;
     const float2 sl2x2 = make_float2(sl2, sl2), one2 = make_float2(1.f, 1.f), zero2 = make_float2(0.f, 0.f);
+    const float cap_c2 = CAP ? p.softcap * 1.4426950408889634f : 0.f;
+    const float cap_k1 = CAP ? 2.f * sl2 / p.softcap : 0.f, cap_ic2 = CAP ? 1.f / cap_c2 : 0.f;
     uint32_t nz = 0, gstep = 0;
     bool ok = true;
     // lse and Delta of 2 of this half's query columns per lane for one step,
@@ -401,7 +407,7 @@ __global__ void __launch_bounds__(512, 1) attn_bwd_dual_kernel(const __grid_cons
           for (int c = 0; c < 2; ++c) {
             uint32_t(&cur)[32] = c ? sb : sa;
             tmem_wait_ld32(cur);
-            uint32_t pk[16];
+            uint32_t pk[16], pfk[16];
 #pragma unroll
             for (int e4 = 0; e4 < 8; ++e4) {
               const float4 nl = *reinterpret_cast<const float4*>(my_nlse + c * 32 + e4 * 4);
@@ -409,8 +415,16 @@ __global__ void __launch_bounds__(512, 1) attn_bwd_dual_kernel(const __grid_cons
               for (int hf = 0; hf < 2; ++hf) {
                 const int e = e4 * 2 + hf;
                 const float2 nl2 = hf ? make_float2(nl.z, nl.w) : make_float2(nl.x, nl.y);
-                const float2 x =
-                    fma2(make_float2(__uint_as_float(cur[2 * e]), __uint_as_float(cur[2 * e + 1])), sl2x2, nl2);
+                float2 x, fac = one2;
+                if constexpr (CAP) {
+                  const float2 y = make_float2(softcap_log2(__uint_as_float(cur[2 * e]), cap_k1, cap_c2),
+                                               softcap_log2(__uint_as_float(cur[2 * e + 1]), cap_k1, cap_c2));
+                  x = fma2(y, one2, nl2);
+                  const float2 tt = make_float2(y.x * cap_ic2, y.y * cap_ic2);
+                  fac = make_float2(fmaf(-tt.x, tt.x, 1.f), fmaf(-tt.y, tt.y, 1.f));
+                } else {
+                  x = fma2(make_float2(__uint_as_float(cur[2 * e]), __uint_as_float(cur[2 * e + 1])), sl2x2, nl2);
+                }
                 float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
                 if constexpr (MASK) {
                   const int qc = c * 32 + 2 * e;
@@ -418,9 +432,11 @@ __global__ void __launch_bounds__(512, 1) attn_bwd_dual_kernel(const __grid_cons
                   p1 = (qc + 1 < q_lo || qc + 1 >= q_hi) ? 0.f : p1;
                 }
                 pk[e] = pack2<T>(p0, p1);
+                if constexpr (CAP) pfk[e] = pack2<T>(p0 * fac.x, p1 * fac.y);
               }
             }
             tmem_st16_async(ra + pofs + c * 16, pk);
+            if constexpr (CAP) tmem_st16_async(ra + pofs + 32 + c * 16, pfk);
           }
           tmem_wait_st();
         };
@@ -442,7 +458,8 @@ __global__ void __launch_bounds__(512, 1) attn_bwd_dual_kernel(const __grid_cons
           // Four 16-column pieces, the next one's TMEM loads in flight.
           uint32_t da[16], db[16], pa[8], pb[8];
           tmem_ld16_async(rb + cb, da);
-          tmem_ld8_async(ra + pofs, pa);
+          constexpr uint32_t kPsrc = CAP ? 32 : 0;  // P^T, or P^T (1 - tanh^2) with a cap
+          tmem_ld8_async(ra + pofs + kPsrc, pa);
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             uint32_t(&dcur)[16] = (c & 1) ? db : da;
@@ -452,7 +469,7 @@ __global__ void __launch_bounds__(512, 1) attn_bwd_dual_kernel(const __grid_cons
             tmem_wait_ld16_8(dcur, pcur);
             if (c + 1 < 4) {
               tmem_ld16_async(rb + cb + (c + 1) * 16, dnxt);
-              tmem_ld8_async(ra + pofs + (c + 1) * 8, pnxt);
+              tmem_ld8_async(ra + pofs + kPsrc + (c + 1) * 8, pnxt);
             }
             uint32_t dk2[8];
 #pragma unroll

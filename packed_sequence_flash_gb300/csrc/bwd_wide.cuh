@@ -40,7 +40,8 @@ struct BwdWideCfg {
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
 
-template <typename T, int D>
+// CAP: logits softcapped (p.softcap > 0); dS carries the cap's 1 - tanh^2.
+template <typename T, int D, bool CAP>
 __global__ void __launch_bounds__(384, 1) attn_bwd_wide_kernel(const __grid_constant__ BwdParams p) {
   using C = BwdWideCfg<D>;
   constexpr int NST = C::NST;
@@ -255,6 +256,8 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_wide_kernel(const __grid_cons
     uint8_t* pt_s = smem + C::PT_OFF;
     uint8_t* ds_s = smem + C::DS_OFF;
     const float sl2 = p.scale_log2;
+    const float cap_c2 = CAP ? p.softcap * 1.4426950408889634f : 0.f;
+    const float cap_k1 = CAP ? 2.f * sl2 / p.softcap : 0.f, cap_ic2 = CAP ? 1.f / cap_c2 : 0.f;
     uint32_t nz = 0, gstep = 0;
     bool ok = true;
     for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
@@ -329,10 +332,18 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_wide_kernel(const __grid_cons
 #pragma unroll
               for (int u = 0; u < 2; ++u) {
                 const int qc = c * 32 + 2 * e + u;
-                float pe = ex2_approx(fmaf(__uint_as_float(sv[2 * e + u]), sl2, -my_lse[qc]));
+                float pe, fe = 1.f;
+                if constexpr (CAP) {
+                  const float y = softcap_log2(__uint_as_float(sv[2 * e + u]), cap_k1, cap_c2);
+                  const float tt = y * cap_ic2;
+                  fe = fmaf(-tt, tt, 1.f);
+                  pe = ex2_approx(y - my_lse[qc]);
+                } else {
+                  pe = ex2_approx(fmaf(__uint_as_float(sv[2 * e + u]), sl2, -my_lse[qc]));
+                }
                 if (masked && (qc < q_lo || qc >= q_hi)) pe = 0.f;
                 pr[u] = pe;
-                dr[u] = pe * (__uint_as_float(pv[2 * e + u]) - my_dl[qc]);
+                dr[u] = pe * fe * (__uint_as_float(pv[2 * e + u]) - my_dl[qc]);
               }
               pk[e] = pack2<T>(pr[0], pr[1]);
               dk2[e] = pack2<T>(dr[0], dr[1]);

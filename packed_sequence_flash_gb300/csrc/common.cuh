@@ -2,6 +2,7 @@
 // arithmetic shared by the attention kernels.
 #pragma once
 
+#include <math_constants.h>
 #include <stdint.h>
 
 #include "ptx.cuh"
@@ -56,6 +57,16 @@ __device__ __forceinline__ void q_range_for_kv_tile(int m, int n, int j0, int ca
   if (hi < lo) hi = lo;
 }
 __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// Softcapped logit in log2 units, c * log2(e) * tanh(scale * s / c), for a raw
+// score s = q . k, from tanh(u) = 1 - 2 / (e^(2u) + 1) with k1 = 2 * scale *
+// log2(e) / c and c2 = c * log2(e) (the saturated ends come out as +-c2 exactly).
+// A masked score (-inf) stays -inf.
+__device__ __forceinline__ float softcap_log2(float s, float k1, float c2) {
+  const float e = ex2_approx(s * k1);
+  const float y = fmaf(rcp_approx(e + 1.f), -2.f * c2, c2);
+  return s == -CUDART_INF_F ? -CUDART_INF_F : y;
+}
 
 // Compile-time flag for element passes that exist in a masked and an unmasked
 // form (mask arithmetic inside the common, unmasked loop costs throughput even

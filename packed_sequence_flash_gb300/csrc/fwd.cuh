@@ -44,6 +44,7 @@ struct FwdParams {
   int pack;      // query heads per tile: 1, or Hq / Hkv when a KV head's query heads share one tile
   int dv_parts;  // value-dim slices computed by separate tiles (each DVC wide)
   float scale_log2;
+  float softcap;      // > 0: logits capped as softcap * tanh(logit / softcap) (the CAP kernels)
   const int2* items;  // (segment, q tile), heaviest first
   const int* n_items;
   int* work_next;  // zeroed by the schedule kernel; kernels that take work dynamically count on it
@@ -91,7 +92,9 @@ __device__ __forceinline__ FwdTile fwd_decode(const FwdParams& p, int w) {
   return t;
 }
 
-template <typename T, int DQK, int DVC>
+// CAP: logits softcapped (p.softcap > 0), applied to the score registers in
+// place before the row maximum.
+template <typename T, int DQK, int DVC, bool CAP>
 __global__ void __launch_bounds__(256, 1) attn_fwd_kernel(const __grid_constant__ FwdParams p) {
   using C = FwdCfg<DQK, DVC>;
   constexpr int NST = C::NST, NQB = C::NQB;
@@ -314,6 +317,12 @@ __global__ void __launch_bounds__(256, 1) attn_fwd_kernel(const __grid_constant_
 #pragma unroll
           for (int j = 0; j < 128; ++j) s[j] = (j < lo_c || j >= hi_c) ? -CUDART_INF_F : s[j];
         }
+        if constexpr (CAP) {
+          // capped logits in log2 units; the multiplier below becomes 1
+          const float k1 = 2.f * sl2 / p.softcap, c2 = p.softcap * 1.4426950408889634f;
+#pragma unroll
+          for (int j = 0; j < 128; ++j) s[j] = softcap_log2(s[j], k1, c2);
+        }
         // Row maximum with eight independent chains (one warp per SM
         // sub-partition: latency, not throughput, bounds a single chain).
         float m8[8];
@@ -322,13 +331,13 @@ __global__ void __launch_bounds__(256, 1) attn_fwd_kernel(const __grid_constant_
 #pragma unroll
         for (int j = 8; j < 128; ++j) m8[j & 7] = fmaxf(m8[j & 7], s[j]);
         float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
-        mx *= sl2;
+        if constexpr (!CAP) mx *= sl2;
         const float m_new = (mx > m_used + 8.f) ? mx : m_used;
         const float alpha = (m_new == m_used) ? 1.f : ex2_approx(m_used - m_new);
         const float base = (m_new == -CUDART_INF_F) ? 0.f : m_new;
         float r8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         uint32_t pa[32], pb2[32];
-        const float2 sl2x2 = make_float2(sl2, sl2), nbase = make_float2(-base, -base);
+        const float2 sl2x2 = CAP ? make_float2(1.f, 1.f) : make_float2(sl2, sl2), nbase = make_float2(-base, -base);
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
           const float2 x = fma2(make_float2(s[2 * j], s[2 * j + 1]), sl2x2, nbase);

@@ -64,7 +64,9 @@ struct FwdDuoCfg {
   static_assert(3 * (SMEM_BYTES + 1024) > 233472, "at most two CTAs per SM");
 };
 
-template <typename T, int D>
+// CAP: logits softcapped (p.softcap > 0), applied to the score registers in
+// place before the row maximum.
+template <typename T, int D, bool CAP>
 __global__ void __launch_bounds__(192, 2) attn_fwd_duo_kernel(const __grid_constant__ FwdParams p) {
   using C = FwdDuoCfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -261,7 +263,11 @@ __global__ void __launch_bounds__(192, 2) attn_fwd_duo_kernel(const __grid_const
     const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
     const uint32_t ts = tmem + lane_base + C::T_S, to = tmem + lane_base + C::T_O;
     const float sl2 = p.scale_log2;
-    const float2 sl2x2 = make_float2(sl2, sl2), zero2 = make_float2(0.f, 0.f);
+    const float2 zero2 = make_float2(0.f, 0.f);
+    // With CAP the score registers hold capped logits in log2 units already.
+    const float mul = CAP ? 1.f : sl2;
+    const float2 mul2 = make_float2(mul, mul);
+    const float cap_k1 = CAP ? 2.f * sl2 / p.softcap : 0.f, cap_c2 = CAP ? p.softcap * 1.4426950408889634f : 0.f;
     uint32_t kv = 0, ntile = 0;
     bool ok = true;
     while (ok) {
@@ -328,6 +334,14 @@ __global__ void __launch_bounds__(192, 2) attn_fwd_duo_kernel(const __grid_const
                 if (c * 32 + e < lo_c || c * 32 + e >= hi_c) cur[e] = 0xff800000u;  // -inf
             }
           }
+          if constexpr (CAP) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              uint32_t(&cur)[32] = chunk(c);
+#pragma unroll
+              for (int e = 0; e < 32; ++e) cur[e] = __float_as_uint(softcap_log2(__uint_as_float(cur[e]), cap_k1, cap_c2));
+            }
+          }
           float m8[8];
 #pragma unroll
           for (int u = 0; u < 8; ++u) m8[u] = -CUDART_INF_F;
@@ -342,7 +356,7 @@ __global__ void __launch_bounds__(192, 2) attn_fwd_duo_kernel(const __grid_const
             }
           }
           const float mx =
-              fmaxf(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], fmax3(m8[5], m8[6], m8[7]))) * sl2;
+              fmaxf(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], fmax3(m8[5], m8[6], m8[7]))) * mul;
           m_new = (mx > m_used + 8.f) ? mx : m_used;
           alpha = (m_new == m_used) ? 1.f : ex2_approx(m_used - m_new);
           const float base = (m_new == -CUDART_INF_F) ? 0.f : m_new;
@@ -355,7 +369,7 @@ __global__ void __launch_bounds__(192, 2) attn_fwd_duo_kernel(const __grid_const
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
               const float2 x =
-                  fma2(make_float2(__uint_as_float(cur[2 * e]), __uint_as_float(cur[2 * e + 1])), sl2x2, nbase);
+                  fma2(make_float2(__uint_as_float(cur[2 * e]), __uint_as_float(cur[2 * e + 1])), mul2, nbase);
               const float2 ex = make_float2(ex2_approx(x.x), ex2_approx(x.y));
               r4[e & 3] = add2(r4[e & 3], ex);
               pk[e] = pack2<T>(ex.x, ex.y);

@@ -32,7 +32,11 @@ cudaError_t launch_bwd_prep(const SegInfo& g, int G, int Hkv, int split_target, 
 // Grid: one CTA per SM (two for head dims 64 and 128), at most max_work.
 // f16 selects fp16 inputs and outputs (else bf16).
 cudaError_t launch_fwd(const FwdParams& p, int dqk, int dvc, int sms, int64_t max_work, int f16, cudaStream_t st);
+// The softcapped kernels (fwd_cap.cu); launch_fwd calls it when p.softcap > 0.
+cudaError_t launch_fwd_capped(const FwdParams& p, int dqk, int dvc, int grid, int f16, cudaStream_t st);
 cudaError_t launch_bwd(const BwdParams& p, int dqk, int dv, int sms, int item_cap, int f16, cudaStream_t st);
+// The softcapped kernels (bwd_cap.cu); launch_bwd calls it when p.softcap > 0.
+cudaError_t launch_bwd_capped(const BwdParams& p, int dqk, int dv, int grid, int f16, cudaStream_t st);
 int fwd_smem_bytes(int dqk, int dvc);
 int bwd_smem_bytes(int dqk, int dv);
 

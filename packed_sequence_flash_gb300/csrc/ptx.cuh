@@ -349,6 +349,12 @@ __device__ __forceinline__ float ex2_approx(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+// Approximate reciprocal (one SFU instruction).
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 // Largest of three floats in one instruction.
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;

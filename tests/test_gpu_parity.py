@@ -157,25 +157,25 @@ def _rand_segments(r, nseg, max_len, allow_empty=True):
 
 
 def _varlen_case(seed, Dqk, Dv, Hq, Hkv, causal, window, nseg=5, max_len=400, tail_q=0, tail_k=0,
-                 dtype=torch.bfloat16):
+                 dtype=torch.bfloat16, softcap=None, factor=1.0):
     r = np.random.default_rng(seed)
     cu_q, cu_k = _rand_segments(r, nseg, max_len)
     Tq, Tk = int(cu_q[-1]) + tail_q, int(cu_k[-1]) + tail_k
-    q = inputs.randn16((Tq, Hq, Dqk), seed * 7 + 1, dtype=dtype)
-    k = inputs.randn16((Tk, Hkv, Dqk), seed * 7 + 2, dtype=dtype)
+    q = inputs.randn16((Tq, Hq, Dqk), seed * 7 + 1, factor, dtype=dtype)
+    k = inputs.randn16((Tk, Hkv, Dqk), seed * 7 + 2, factor, dtype=dtype)
     v = inputs.randn16((Tk, Hkv, Dv), seed * 7 + 3, dtype=dtype)
     do = inputs.randn16((Tq, Hq, Dv), seed * 7 + 4, dtype=dtype)
     scale = 1.0 / np.sqrt(Dqk)
     cq, ck = torch.from_numpy(cu_q).cuda(), torch.from_numpy(cu_k).cuda()
     mq, mk = int(np.diff(cu_q).max()), int(np.diff(cu_k).max())
-    out, lse = psf.attn_varlen_fwd(cuda(q), cuda(k), cuda(v), cq, ck, mq, mk, scale, causal, window)
+    out, lse = psf.attn_varlen_fwd(cuda(q), cuda(k), cuda(v), cq, ck, mq, mk, scale, causal, window, softcap=softcap)
     assert out.dtype == dtype
-    out_o, lse_o = oracle.attn_fwd_segments(q, k, v, cu_q, cu_k, scale, causal, window)
+    out_o, lse_o = oracle.attn_fwd_segments(q, k, v, cu_q, cu_k, scale, causal, window, softcap=softcap)
     assert_fwd(out, lse, out_o, lse_o)
     grads = psf.attn_varlen_bwd(cuda(do), cuda(q), cuda(k), cuda(v), out, lse, cq, ck, mq, mk, scale, causal,
-                                window)
+                                window, softcap=softcap)
     assert all(g.dtype == dtype for g in grads)
-    ref = oracle.attn_bwd_segments(do, q, k, v, out_o, lse_o, cu_q, cu_k, scale, causal, window)
+    ref = oracle.attn_bwd_segments(do, q, k, v, out_o, lse_o, cu_q, cu_k, scale, causal, window, softcap=softcap)
     assert_grads(grads, ref)
     assert psf.device_status() == 0
 
@@ -220,15 +220,16 @@ def test_document_causal_d64_window_one():
 
 # ---------------------------------------------------------------- dense
 
-def _dense_case(B, Hq, Hkv, Nq, Nk, Dqk, Dv, causal, window=None, seed=0, factor=1.0, dtype=torch.bfloat16):
+def _dense_case(B, Hq, Hkv, Nq, Nk, Dqk, Dv, causal, window=None, seed=0, factor=1.0, dtype=torch.bfloat16,
+                softcap=None):
     w = inputs.dense_workload(B, Hq, Hkv, Nq, Nk, Dqk, Dv, seed, factor=factor, causal=causal)
     w.q, w.k, w.v, w.dout = (t.to(dtype) for t in (w.q, w.k, w.v, w.dout))
     q, k, v, do = (cuda(t) for t in (w.q, w.k, w.v, w.dout))
-    out, lse = psf.attn_dense_fwd(q, k, v, w.scale, causal, window)
-    out_o, lse_o = oracle.attn_fwd_dense(w.q, w.k, w.v, w.scale, causal, window)
+    out, lse = psf.attn_dense_fwd(q, k, v, w.scale, causal, window, softcap=softcap)
+    out_o, lse_o = oracle.attn_fwd_dense(w.q, w.k, w.v, w.scale, causal, window, softcap=softcap)
     assert_fwd(out, lse, out_o, lse_o)
-    grads = psf.attn_dense_bwd(do, q, k, v, out, lse, w.scale, causal, window)
-    ref = oracle.attn_bwd_dense(w.dout, w.q, w.k, w.v, out_o, lse_o, w.scale, causal, window)
+    grads = psf.attn_dense_bwd(do, q, k, v, out, lse, w.scale, causal, window, softcap=softcap)
+    ref = oracle.attn_bwd_dense(w.dout, w.q, w.k, w.v, out_o, lse_o, w.scale, causal, window, softcap=softcap)
     assert_grads(grads, ref)
     assert psf.device_status() == 0
 
@@ -582,3 +583,42 @@ def test_dense_fwd_pack_gqa_matches_oracle():
     out_o, lse_o = oracle.attn_fwd_dense(q, k, v, 0.125, True)
     assert_fwd(out.reshape(-1, 64), lse.reshape(-1), out_o.reshape(-1, 64), lse_o.reshape(-1))
     assert psf.device_status() == 0
+
+
+# ---------------------------------------------------------------- logit softcap
+
+@pytest.mark.parametrize("dims", [(64, 64), (128, 128), (192, 128)])
+@pytest.mark.parametrize("causal,window,cap", [(True, None, 1.5), (False, None, 4.0), (True, 97, 30.0)])
+def test_varlen_softcap_matches_oracle(dims, causal, window, cap):
+    # inputs scaled up so that the cap bends the logits
+    _varlen_case(21, dims[0], dims[1], 4, 2, causal, window, factor=2.0, softcap=cap)
+
+
+def test_dense_d512_softcap_forward_backward():
+    _dense_case(1, 4, 2, 300, 300, 512, 512, True, seed=9, factor=1.0, softcap=2.0)
+
+
+def test_varlen_softcap_fp16_and_gqa():
+    _varlen_case(23, 128, 128, 8, 2, True, None, nseg=6, max_len=300, dtype=torch.float16, factor=2.0,
+                 softcap=3.0)
+
+
+def test_document_causal_softcap():
+    w = inputs.small_document_workload(900, 4, 2, 128, 128, 8, max_len=350, pad_tail=61)
+    q, k, v, do = (cuda(t) for t in (w.q, w.k, w.v, w.dout))
+    ids = torch.from_numpy(w.doc_ids).to("cuda")
+    out, lse, seg = psf.document_causal_attention(q, k, v, ids, ids, 0, w.scale, None, softcap=2.5)
+    out_o, lse_o = oracle.attn_fwd_document(w.q, w.k, w.v, w.doc_ids, 0, w.scale, None, softcap=2.5)
+    assert_fwd(out, lse, out_o, lse_o)
+    grads = psf.document_causal_attention_backward(do, q, k, v, out, lse, seg, w.scale, softcap=2.5)
+    ref = oracle.attn_bwd_document(w.dout, w.q, w.k, w.v, out_o, lse_o, w.doc_ids, 0, w.scale, None, softcap=2.5)
+    assert_grads(grads, ref)
+    assert psf.device_status() == 0
+
+
+def test_softcap_rejects_negative():
+    q = torch.zeros(8, 2, 64, dtype=torch.bfloat16, device="cuda")
+    k = torch.zeros(8, 1, 64, dtype=torch.bfloat16, device="cuda")
+    cu = torch.tensor([0, 8], dtype=torch.int32, device="cuda")
+    with pytest.raises(psf.PSFError):
+        psf.attn_varlen_fwd(q, k, k, cu, cu, 8, 8, 0.125, True, softcap=-1.0)

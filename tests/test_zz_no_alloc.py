@@ -49,7 +49,7 @@ def _call(lib, noalloc, q, k, v, cu_q, cu_k, mq, mk, window):
         ws = None
     else:
         ws = torch.empty(lib.psf_attn_fwd_workspace_size(Tq, nseg), dtype=torch.uint8, device="cuda")
-        rc = lib.psf_attn_varlen_fwd(*common, 0, ws.data_ptr(), ws.numel(), stream)
+        rc = lib.psf_attn_varlen_fwd(*common, 0.0, 0, ws.data_ptr(), ws.numel(), stream)
     assert rc == 0, lib.psf_last_error()
     torch.cuda.synchronize()
     return out, lse
