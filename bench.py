@@ -181,14 +181,14 @@ def cpu_sample_workload(w, frac=0.25, offset_docs=0):
     return sub, i - offset_docs
 
 
-def run_oracle(sub, nthreads):
+def run_oracle(sub, nthreads, softcap=None):
     import oracle
 
     t = time.perf_counter()
     out, lse = oracle.attn_fwd_document(sub.q, sub.k, sub.v, sub.doc_ids, 0, sub.scale, sub.window,
-                                        nthreads=nthreads)
+                                        nthreads=nthreads, softcap=softcap)
     oracle.attn_bwd_document(sub.dout, sub.q, sub.k, sub.v, out, lse, sub.doc_ids, 0, sub.scale, sub.window,
-                             nthreads=nthreads)
+                             nthreads=nthreads, softcap=softcap)
     return time.perf_counter() - t
 
 
@@ -199,11 +199,11 @@ def cores():
         return os.cpu_count() or 1
 
 
-def cpu_baseline(w):
+def cpu_baseline(w, softcap=None):
     sub, ndocs = cpu_sample_workload(w, 1.0)
     _, f, b = workload_flops(sub)
     c = cores()
-    secs = run_oracle(sub, c)
+    secs = run_oracle(sub, c, softcap)
     return {"value": (f + b) / secs / 1e12, "unit": UNIT, "cores": c, "kind": "oracle",
             "sample": f"fp64 oracle fwd+bwd on all {ndocs} documents of the step ({sub.q.shape[0]} tokens, "
                       f"{(f + b) / 1e9:.1f} GFLOP), once, {secs:.1f} s"}
@@ -214,7 +214,7 @@ def config_dict(w, args, pairs, n_docs):
             "q_global_start": int(w.q_global_start), "Hq": int(w.q.shape[1]), "Hkv": int(w.k.shape[1]),
             "Dqk": int(w.q.shape[2]), "Dv": int(w.v.shape[2]), "window": w.window, "documents": n_docs,
             "visible_pairs_x_heads": int(pairs), "seed": args.seed, "l2": "flushed between steps (256 MiB write)",
-            "pack_gqa": bool(getattr(args, "pack_gqa", False))}
+            "pack_gqa": bool(getattr(args, "pack_gqa", False)), "softcap": getattr(args, "softcap", None)}
 
 
 # ---------------------------------------------------------------------------
@@ -232,7 +232,7 @@ def reference_arm(args):
     for s in range(args.warmup + args.steps):
         sub, nd = cpu_sample_workload(w, 0.06, offset_docs=s % max(ndocs_total - 1, 1))
         _, f, b = workload_flops(sub)
-        secs = run_oracle(sub, c)
+        secs = run_oracle(sub, c, args.softcap)
         if s >= args.warmup:
             total_f += f + b
             total_s += secs
@@ -285,8 +285,9 @@ def our_arm(args):
 
     def step(qq, kk, vv, dd, ii, qi):
         out, lse, seg = psf.document_causal_attention(qq, kk, vv, qi, ii, w.q_global_start, w.scale, w.window,
-                                                      pack_gqa=args.pack_gqa)
-        grads = psf.document_causal_attention_backward(dd, qq, kk, vv, out, lse, seg, w.scale, w.window)
+                                                      pack_gqa=args.pack_gqa, softcap=args.softcap)
+        grads = psf.document_causal_attention_backward(dd, qq, kk, vv, out, lse, seg, w.scale, w.window,
+                                                       softcap=args.softcap)
         return out, lse, grads
 
     for _ in range(args.warmup):
@@ -470,7 +471,7 @@ def our_arm(args):
         "clocks": clocks,
     }
     if world == 1 and not args.no_cpu:
-        line["cpu_baseline"] = cpu_baseline(w)
+        line["cpu_baseline"] = cpu_baseline(w, args.softcap)
     print(json.dumps(line))
     if dist:
         dist.destroy_process_group()
@@ -500,6 +501,8 @@ def main():
     ap.add_argument("--dtype", choices=["bf16", "fp16"], default="bf16",
                     help="16-bit type of q, k, v, dO and the outputs (the headline is bf16)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--softcap", type=float, default=None,
+                    help="cap the logits as softcap * tanh(logit / softcap) (off by default)")
     ap.add_argument("--pack-gqa", action="store_true",
                     help="forward with a KV head's query heads packed into one tile (for short documents, --config 6)")
     args = ap.parse_args()
