@@ -287,7 +287,7 @@ def our_arm(args):
         out, lse, seg = psf.document_causal_attention(qq, kk, vv, qi, ii, w.q_global_start, w.scale, w.window,
                                                       pack_gqa=args.pack_gqa, softcap=args.softcap)
         grads = psf.document_causal_attention_backward(dd, qq, kk, vv, out, lse, seg, w.scale, w.window,
-                                                       softcap=args.softcap)
+                                                       softcap=args.softcap, pack_gqa=args.pack_gqa)
         return out, lse, grads
 
     for _ in range(args.warmup):
@@ -504,7 +504,8 @@ def main():
     ap.add_argument("--softcap", type=float, default=None,
                     help="cap the logits as softcap * tanh(logit / softcap) (off by default)")
     ap.add_argument("--pack-gqa", action="store_true",
-                    help="forward with a KV head's query heads packed into one tile (for short documents, --config 6)")
+                    help="forward and backward with a KV head's query heads packed into one tile (for short "
+                         "documents, --config 6)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

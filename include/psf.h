@@ -179,6 +179,10 @@ int psf_attn_varlen_fwd_noalloc(const void* q, const void* k, const void* v, voi
  *  Keys that no query sees get dk = dv = 0; query rows outside every segment
  *  get dq = 0.
  *  softcap: the forward's (0 = off); with c > 0, dS carries 1 - tanh^2(z / c).
+ *  flags: 0, or PSF_BWD_PACK_GQA: each step takes the G = Hq / Hkv query heads
+ *  of its KV head, 128 / G rows each (head dims up to 128 with G = 2 or 4 and
+ *  no softcap; other calls take one head per step). Same results; for short segments,
+ *  where one head's rows fill little of a 128-row step. Other bits: PSF_EINVAL.
  *  workspace: psf_attn_bwd_workspace_size(Tq, Tk, nseg, Hq, Hkv, Dqk, Dv) bytes
  *  (holds the fp32 dQ, dK and dV accumulators, Delta = rowsum(dO * out) and the
  *  tile schedule).
@@ -187,7 +191,8 @@ int psf_attn_varlen_bwd(const void* dout, const void* q, const void* k, const vo
                         const float* lse, void* dq, void* dk, void* dv, const int32_t* cu_q, const int32_t* cu_k,
                         const int32_t* dev_meta, int nseg, int max_q, int max_k, int layout, int dtype, int B, int Sq,
                         int Sk, int Hq, int Hkv, int Dqk, int Dv, float scale, int causal, int32_t window_left,
-                        float softcap, void* workspace, size_t ws_bytes, void* stream);
+                        float softcap, int flags, void* workspace, size_t ws_bytes, void* stream);
+#define PSF_BWD_PACK_GQA 1
 
 /*
  * Dense forward on SDPA-layout tensors.
@@ -207,12 +212,13 @@ int psf_attn_dense_fwd(const void* q, const void* k, const void* v, void* out, f
 /*
  * Dense backward.           [ffpa_attention page, `_ffpa_dense_bwd`: returns
  *                            (dq, dk, dv) in [B,H,N,D], dK/dV reduced to Hkv]
+ *  softcap, flags: as for psf_attn_varlen_bwd.
  *  workspace: psf_attn_bwd_workspace_size(B * Nq, B * Nk, B, Hq, Hkv, Dqk, Dv) bytes.
  */
 int psf_attn_dense_bwd(const void* dout, const void* q, const void* k, const void* v, const void* out,
                        const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Nq, int Nk,
                        int Dqk, int Dv, int dtype, float scale, int causal, int32_t window_left, float softcap,
-                       void* workspace, size_t ws_bytes, void* stream);
+                       int flags, void* workspace, size_t ws_bytes, void* stream);
 
 /*
  * Doc ids -> varlen segments, on the GPU.

@@ -34,9 +34,9 @@ SIGNATURES = {
     "psf_attn_varlen_fwd": (I, [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, I, I, I, F, I, I32, F, I, P, SZ, P]),
     "psf_attn_varlen_fwd_noalloc": (I, [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, I, I, I, F, I, I32, P]),
     "psf_attn_varlen_bwd": (I, [P, P, P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, I, I, I, F, I, I32,
-                                F, P, SZ, P]),
+                                F, I, P, SZ, P]),
     "psf_attn_dense_fwd": (I, [P, P, P, P, P, I, I, I, I, I, I, I, I, F, I, I32, F, I, P, SZ, P]),
-    "psf_attn_dense_bwd": (I, [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, F, I, I32, F, P, SZ, P]),
+    "psf_attn_dense_bwd": (I, [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, F, I, I32, F, I, P, SZ, P]),
     "psf_build_doc_segments": (I, [P, I, I, I, I, P, P, I, P, P, I, P]),
     "psf_chunk_dense_flags": (I, [P, I, I, I, I, I, I, P, P]),
     "psf_pad_fixup": (I, [P, P, P, I, I, I, I, I, P]),
@@ -52,6 +52,7 @@ PSF_DTYPE_BF16 = 0
 PSF_DTYPE_F16 = 1
 PSF_SEGMENTS_SKIP_PAD = 1
 PSF_FWD_PACK_GQA = 1
+PSF_BWD_PACK_GQA = 1
 ERRORS = {-1: "PSF_EINVAL", -2: "PSF_EUNSUPPORTED", -3: "PSF_ECUDA", -4: "PSF_EDEVICE_ARGS",
           -5: "PSF_ETIMEOUT", -6: "PSF_EWORKSPACE"}
 

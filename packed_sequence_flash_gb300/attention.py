@@ -18,7 +18,7 @@ from __future__ import annotations
 import torch
 
 from . import _lib
-from ._lib import (PSF_DTYPE_BF16, PSF_DTYPE_F16, PSF_FWD_PACK_GQA, PSF_LAYOUT_BHSD, PSF_LAYOUT_THD,
+from ._lib import (PSF_BWD_PACK_GQA, PSF_DTYPE_BF16, PSF_DTYPE_F16, PSF_FWD_PACK_GQA, PSF_LAYOUT_BHSD, PSF_LAYOUT_THD,
                    PSF_SEGMENTS_SKIP_PAD, check)
 
 NO_WINDOW = -(2 ** 31)  # the pages' "no window" sentinel
@@ -137,8 +137,9 @@ def attn_varlen_fwd(q, k, v, cu_q, cu_k, max_q, max_k, scale, causal, window=Non
 
 
 def attn_varlen_bwd(dout, q, k, v, out, lse, cu_q, cu_k, max_q, max_k, scale, causal, window=None,
-                    dev_meta=None, layout="thd", workspace=None, softcap=None):
-    """Packed varlen backward from caller-supplied out/lse -> (dq, dk, dv) in the inputs' type."""
+                    dev_meta=None, layout="thd", workspace=None, softcap=None, pack_gqa=False):
+    """Packed varlen backward from caller-supplied out/lse -> (dq, dk, dv) in the inputs' type.
+    pack_gqa: each step takes a KV head's query heads together (same results)."""
     dt = _dtype_code([(dout, "dout"), (q, "q"), (k, "k"), (v, "v"), (out, "out")])
     _need(lse, "lse", torch.float32)
     _i32(cu_q, "cu_q")
@@ -153,7 +154,8 @@ def attn_varlen_bwd(dout, q, k, v, out, lse, cu_q, cu_k, max_q, max_k, scale, ca
     rc = _lib.load().psf_attn_varlen_bwd(
         _ptr(dout), _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(cu_q),
         _ptr(cu_k), _ptr(dev_meta), nseg, int(max_q), int(max_k), lay, dt, B, Sq, Sk, Hq, Hkv, Dqk, Dv, float(scale),
-        int(bool(causal)), _window(window), _cap(softcap), _ptr(workspace), workspace.numel(), _stream())
+        int(bool(causal)), _window(window), _cap(softcap), PSF_BWD_PACK_GQA if pack_gqa else 0, _ptr(workspace),
+        workspace.numel(), _stream())
     check(rc)
     return dq, dk, dv
 
@@ -179,7 +181,8 @@ def attn_dense_fwd(q, k, v, scale, causal, window=None, workspace=None, pack_gqa
     return out, lse
 
 
-def attn_dense_bwd(dout, q, k, v, out, lse, scale, causal, window=None, workspace=None, softcap=None):
+def attn_dense_bwd(dout, q, k, v, out, lse, scale, causal, window=None, workspace=None, softcap=None,
+                   pack_gqa=False):
     """Dense backward -> (dq, dk, dv) in [B,H,N,D], dk/dv at Hkv heads."""
     dt = _dtype_code([(dout, "dout"), (q, "q"), (k, "k"), (v, "v"), (out, "out")])
     _need(lse, "lse", torch.float32)
@@ -191,8 +194,9 @@ def attn_dense_bwd(dout, q, k, v, out, lse, scale, causal, window=None, workspac
         workspace = _workspace(bwd_workspace_size(B * Nq, B * Nk, B, Hq, Hkv, Dqk, Dv), q.device)
     rc = _lib.load().psf_attn_dense_bwd(_ptr(dout), _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dq),
                                         _ptr(dk), _ptr(dv), B, Hq, Hkv, Nq, Nk, Dqk, Dv, dt, float(scale),
-                                        int(bool(causal)), _window(window), _cap(softcap), _ptr(workspace),
-                                        workspace.numel(), _stream())
+                                        int(bool(causal)), _window(window), _cap(softcap),
+                                        PSF_BWD_PACK_GQA if pack_gqa else 0, _ptr(workspace), workspace.numel(),
+                                        _stream())
     check(rc)
     return dq, dk, dv
 
@@ -394,9 +398,10 @@ def document_causal_attention(q, k, v, q_doc_ids, kv_doc_ids, q_global_start, sc
     return out, lse, (cu_q, cu_k, meta)
 
 
-def document_causal_attention_backward(dout, q, k, v, out, lse, segments, scale, window=None, softcap=None):
+def document_causal_attention_backward(dout, q, k, v, out, lse, segments, scale, window=None, softcap=None,
+                                       pack_gqa=False):
     """Backward of document_causal_attention from its out/lse -> (dq, dk, dv)."""
     layout = "thd" if q.dim() == 3 else "bhsd"
     cu_q, cu_k, meta = segments
     return attn_varlen_bwd(dout, q, k, v, out, lse, cu_q, cu_k, -1, -1, scale, True, window, dev_meta=meta,
-                           layout=layout, softcap=softcap)
+                           layout=layout, softcap=softcap, pack_gqa=pack_gqa)

@@ -18,7 +18,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libpsf.so")
 ROOT = os.path.dirname(HERE)
 INCLUDE = os.path.join(ROOT, "include")
-SOURCES = ["api.cu", "fwd.cu", "fwd_cap.cu", "bwd.cu", "bwd_cap.cu", "aux.cu"]
+SOURCES = ["api.cu", "fwd.cu", "fwd_cap.cu", "bwd.cu", "bwd_cap.cu", "bwd_pack.cu", "aux.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I", CSRC, "-I", INCLUDE]

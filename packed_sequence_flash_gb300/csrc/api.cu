@@ -325,10 +325,11 @@ int attn_bwd_impl(const void* dout, const void* q, const void* k, const void* v,
                   void* dq, void* dk, void* dv, const int32_t* cu_q, const int32_t* cu_k, const int32_t* dev_meta,
                   int nseg, int max_q, int max_k, int layout, int dtype, int B, int Sq, int Sk, int Hq, int Hkv,
                   int Dqk, int Dv, float scale, int causal, int32_t window, void* ws, size_t ws_bytes, void* stream,
-                  float softcap = 0.f) {
+                  float softcap = 0.f, int flags = 0) {
   int rc = check_common(layout, B, Sq, Sk, Hq, Hkv, Dqk, Dv, scale, window, nseg);
   if (rc) return rc;
   if ((rc = check_softcap(softcap))) return rc;
+  if (flags & ~PSF_BWD_PACK_GQA) return fail(PSF_EINVAL, "unknown backward flags 0x%x", flags);
   if ((rc = check_dtype(dtype))) return rc;
   const int f16 = dtype == PSF_DTYPE_F16;
   if (bwd_smem_bytes(Dqk, Dv) < 0)
@@ -353,9 +354,16 @@ int attn_bwd_impl(const void* dout, const void* q, const void* k, const void* v,
   // Head dims up to 128 run the kernel that adds dK/dV partial sums into fp32
   // accumulators, which lets heavy key tiles be split across SMs.
   const bool accumulate = Dqk <= 128 && Dv <= 128;
+  // Packed query heads: a step of the head-dim-<=-128 kernel takes the G = Hq / Hkv
+  // query heads of its KV head, 128 / G rows each (G in {2, 4}, so that a dQ
+  // read-out box of 32 rows stays inside one head; no softcap); other calls
+  // take one head per step, with the same results.
+  const int G = Hq / Hkv;
+  const int pack = ((flags & PSF_BWD_PACK_GQA) && accumulate && (G == 2 || G == 4) && softcap == 0.f) ? G : 1;
+  const int qrows = kBM / pack;
   BwdWorkspace w;
   bwd_ws_layout(q_rows, k_rows, nseg, Hq, Hkv, Dqk, Dv, dev->sms, &w, ws);
-  SegInfo g{cu_q, cu_k, dev_meta, nseg, max_q, max_k, B, Sq, Sk, causal ? 1 : 0, window > 0 ? (int)window : 0};
+  SegInfo g{cu_q, cu_k, dev_meta, nseg, max_q, max_k, B, Sq, Sk, causal ? 1 : 0, window > 0 ? (int)window : 0, qrows};
   const View vq = tensor_view(layout, Sq, Hq, Dqk), vk = tensor_view(layout, Sk, Hkv, Dqk);
   const View vv = tensor_view(layout, Sk, Hkv, Dv), vo = tensor_view(layout, Sq, Hq, Dv);
   const View vl = lse_view(layout, Sq, Hq);
@@ -370,8 +378,8 @@ int attn_bwd_impl(const void* dout, const void* q, const void* k, const void* v,
     BwdParams p;
     memset(&p, 0, sizeof(p));
     if (q_rows > 0) {
-      if ((rc = make_map16(&p.tm_q, q, Dqk, Sq, Hq, B, vq, 64, dtype))) return rc;
-      if ((rc = make_map16(&p.tm_do, dout, Dv, Sq, Hq, B, vo, 64, dtype))) return rc;
+      if ((rc = make_map16(&p.tm_q, q, Dqk, Sq, Hq, B, vq, 64, dtype, qrows, pack))) return rc;
+      if ((rc = make_map16(&p.tm_do, dout, Dv, Sq, Hq, B, vo, 64, dtype, qrows, pack))) return rc;
       int r2 = make_tmap_4d(&p.tm_dq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, w.dq_acc, Dqk, Sq, Hq, B, (int64_t)Hq * Dqk,
                             Dqk, (int64_t)Sq * Hq * Dqk, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B);
       if (r2) return fail(PSF_ECUDA, "cuTensorMapEncodeTiled failed (%d) for the dQ accumulator", r2);
@@ -404,6 +412,7 @@ int attn_bwd_impl(const void* dout, const void* q, const void* k, const void* v,
     p.scale = scale;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.softcap = softcap;
+    p.pack = pack;
     p.items = w.items;
     p.n_items = w.n_items;
     p.work_next = w.n_items + 1;
@@ -550,10 +559,11 @@ int psf_attn_varlen_bwd(const void* dout, const void* q, const void* k, const vo
                         const float* lse, void* dq, void* dk, void* dv, const int32_t* cu_q, const int32_t* cu_k,
                         const int32_t* dev_meta, int nseg, int max_q, int max_k, int layout, int dtype, int B, int Sq,
                         int Sk, int Hq, int Hkv, int Dqk, int Dv, float scale, int causal, int32_t window_left,
-                        float softcap, void* workspace, size_t ws_bytes, void* stream) {
+                        float softcap, int flags, void* workspace, size_t ws_bytes, void* stream) {
   if (!cu_q || !cu_k) return fail(PSF_EINVAL, "varlen calls need cu_q and cu_k");
   return attn_bwd_impl(dout, q, k, v, out, lse, dq, dk, dv, cu_q, cu_k, dev_meta, nseg, max_q, max_k, layout, dtype, B,
-                       Sq, Sk, Hq, Hkv, Dqk, Dv, scale, causal, window_left, workspace, ws_bytes, stream, softcap);
+                       Sq, Sk, Hq, Hkv, Dqk, Dv, scale, causal, window_left, workspace, ws_bytes, stream, softcap,
+                       flags);
 }
 
 int psf_attn_dense_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq, int Hkv,
@@ -566,10 +576,10 @@ int psf_attn_dense_fwd(const void* q, const void* k, const void* v, void* out, f
 int psf_attn_dense_bwd(const void* dout, const void* q, const void* k, const void* v, const void* out,
                        const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Nq, int Nk,
                        int Dqk, int Dv, int dtype, float scale, int causal, int32_t window_left, float softcap,
-                       void* workspace, size_t ws_bytes, void* stream) {
+                       int flags, void* workspace, size_t ws_bytes, void* stream) {
   return attn_bwd_impl(dout, q, k, v, out, lse, dq, dk, dv, nullptr, nullptr, nullptr, B, Nq, Nk, PSF_LAYOUT_BHSD,
                        dtype, B, Nq, Nk, Hq, Hkv, Dqk, Dv, scale, causal, window_left, workspace, ws_bytes, stream,
-                       softcap);
+                       softcap, flags);
 }
 
 int psf_build_doc_segments(const int32_t* kv_doc_ids, int B, int Sk, int q_length, int q_global_start,

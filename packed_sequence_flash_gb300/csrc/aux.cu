@@ -76,7 +76,7 @@ __device__ int tile_cost(const SegInfo& g, int s, int t, int over_keys) {
   int lo, hi;
   if (over_keys) {
     q_range_for_kv_tile(m, n, t * kBN, g.causal, g.window, lo, hi);
-    return hi > lo ? ceil_div(hi, kBM) - lo / kBM : 0;
+    return hi > lo ? ceil_div(hi, g.qrows) - lo / g.qrows : 0;
   }
   kv_range_for_q_tile(m, n, t * g.qrows, g.causal, g.window, lo, hi, g.qrows);
   return hi > lo ? ceil_div(hi, kBN) - lo / kBN : 0;
@@ -169,6 +169,9 @@ __device__ void bwd_schedule_body(SegInfo g, int G, int Hkv, int split_target,
   const int max_q = g.dev_meta ? g.dev_meta[1] : g.max_q;
   const int max_k = g.dev_meta ? g.dev_meta[2] : g.max_k;
   const int Tq = g.B * g.Sq, Tk = g.B * g.Sk;
+  // Steps of a key tile: (query head groups) x (query tiles); a group is one
+  // head, or kBM / qrows heads packed into one tile.
+  const int Gs = G / (kBM / g.qrows);
   hist[tid] = 0;
   if (tid == 0) n_items[1] = 0;  // work counter of kernels that take items dynamically
   if (tid == 0) {
@@ -207,7 +210,7 @@ __device__ void bwd_schedule_body(SegInfo g, int G, int Hkv, int split_target,
   unsigned long long mine = 0;
   for (int x = tid; x < carry; x += kScanThreads) {
     const int s = find_segment(pref, nseg, x);
-    mine += (unsigned long long)G * tile_cost(g, s, x - pref[s], 1);
+    mine += (unsigned long long)Gs * tile_cost(g, s, x - pref[s], 1);
   }
   atomicAdd(&total_steps, mine);
   __syncthreads();
@@ -219,7 +222,7 @@ __device__ void bwd_schedule_body(SegInfo g, int G, int Hkv, int split_target,
   int nsub_total = 0;
   for (int x = tid; x < carry; x += kScanThreads) {
     const int s = find_segment(pref, nseg, x);
-    const int steps = G * tile_cost(g, s, x - pref[s], 1);
+    const int steps = Gs * tile_cost(g, s, x - pref[s], 1);
     const int nsub = steps == 0 ? 1 : (int)(((long long)steps + smax - 1) / smax);
     nsub_total += nsub;
     for (int i = 0; i < nsub; ++i) {
@@ -245,7 +248,7 @@ __device__ void bwd_schedule_body(SegInfo g, int G, int Hkv, int split_target,
   for (int x = tid; x < carry; x += kScanThreads) {
     const int s = find_segment(pref, nseg, x);
     const int t = x - pref[s];
-    const int steps = G * tile_cost(g, s, t, 1);
+    const int steps = Gs * tile_cost(g, s, t, 1);
     const int nsub = steps == 0 ? 1 : (int)(((long long)steps + smax - 1) / smax);
     for (int i = 0; i < nsub; ++i) {
       const int a = (int)((long long)steps * i / nsub), e = (int)((long long)steps * (i + 1) / nsub);

@@ -18,6 +18,7 @@ cudaError_t launch_bwd(const BwdParams& p, int dqk, int dv, int sms, int item_ca
   const int64_t units = (int64_t)item_cap * p.Hkv * (dqk == 512 ? BwdWideCfg<512>::NP : 1);
   const int grid = (int)(units < sms ? units : sms);
   if (grid <= 0) return cudaSuccess;
+  if (p.pack > 1) return launch_bwd_packed(p, dqk, dv, grid, f16, st);
   if (p.softcap > 0.f) return launch_bwd_capped(p, dqk, dv, grid, f16, st);
   return bwd_run::launch_grid<false>(p, dqk, dv, grid, f16, st);
 }

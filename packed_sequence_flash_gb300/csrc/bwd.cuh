@@ -47,6 +47,7 @@ struct BwdParams {
   int64_t v_sb, v_ss, v_sh;
   int Hq, Hkv;
   float scale, scale_log2;
+  int pack;       // query heads per step: 1, or Hq / Hkv when a KV head's query heads share one tile
   float softcap;  // > 0: logits capped as softcap * tanh(logit / softcap) (the CAP kernels)
   const int4* items;  // (segment, key tile, first step, end step), heaviest first
   const int* n_items;
@@ -87,7 +88,7 @@ struct BwdCfg {
 struct BwdItem {
   int s, kt, hk;
   int cq0, ck0, m, n;
-  int qt0, nqt;  // query tiles [qt0, qt0 + nqt) see this key tile
+  int qt0, nqt;  // query tiles [qt0, qt0 + nqt) (of p.seg.qrows rows) see this key tile
   int k0, k1;
 };
 
@@ -106,8 +107,8 @@ __device__ __forceinline__ BwdItem bwd_decode(const BwdParams& p, int w) {
   t.n = cu_k_at(p.seg, t.s + 1) - t.ck0;
   int lo, hi;
   q_range_for_kv_tile(t.m, t.n, t.kt * kBN, p.seg.causal, p.seg.window, lo, hi);
-  t.qt0 = lo / kBM;
-  t.nqt = hi > lo ? ceil_div(hi, kBM) - t.qt0 : 0;
+  t.qt0 = lo / p.seg.qrows;
+  t.nqt = hi > lo ? ceil_div(hi, p.seg.qrows) - t.qt0 : 0;
   return t;
 }
 

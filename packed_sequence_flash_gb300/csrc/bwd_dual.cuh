@@ -71,7 +71,9 @@ struct BwdDualCfg {
 // P (1 - tanh^2) of the capped logit, packed, into the other 32 columns of
 // its half of region A (S^T columns it has already read and dV never reads),
 // and pass 2 takes dS^T from those instead of from P^T.
-template <typename T, int DQK, int DV, bool CAP>
+// PACK: a step takes the p.pack query heads of its KV head (p.seg.qrows rows
+// each); without it one head of 128 rows, with compile-time tile arithmetic.
+template <typename T, int DQK, int DV, bool CAP, bool PACK>
 __global__ void __launch_bounds__(512, 1) attn_bwd_dual_kernel(const __grid_constant__ BwdParams p) {
   using C = BwdDualCfg<DQK, DV>;
   extern __shared__ uint8_t smem_raw[];
@@ -126,6 +128,8 @@ __global__ void __launch_bounds__(512, 1) attn_bwd_dual_kernel(const __grid_cons
   const Ctl ctl{p.status, p.limit_ns, &abort_flag};
   const int total = (*p.n_items) * p.Hkv;
   const int G = p.Hq / p.Hkv;
+  const int hpack = PACK ? p.pack : 1;        // query heads per step
+  const int qrows = PACK ? p.seg.qrows : kBM;  // rows of each of them
   const uint32_t sbase = smem_u32(smem);
   // Next work item for the MMA, compute and dQ warps (-1: none left, or
   // abort), with its decoded unit.
@@ -180,8 +184,9 @@ __global__ void __launch_bounds__(512, 1) attn_bwd_dual_kernel(const __grid_cons
             tma_load_4d(smem + C::V_OFF + c * kChunkBytes, &p.tm_v, &kv_full, c * 64, sk, t.hk, bk);
           ++nz;
           for (int k = t.k0; k < t.k1; ++k, ++gstep) {
-            const int h = t.hk * G + k / t.nqt, qt = t.qt0 + k % t.nqt;
-            const int fq = t.cq0 + qt * kBM, bq = fq / p.seg.Sq, sq = fq - bq * p.seg.Sq;
+            // the step's first query head (p.pack heads per step) and query tile
+            const int h = t.hk * G + (k / t.nqt) * hpack, qt = t.qt0 + k % t.nqt;
+            const int fq = t.cq0 + qt * qrows, bq = fq / p.seg.Sq, sq = fq - bq * p.seg.Sq;
             const int qs = gstep & 1;
             if (!wait_bar(&q_empty[qs], ((gstep >> 1) & 1) ^ 1, ctl)) {
               ok = false;
@@ -343,17 +348,21 @@ __global__ void __launch_bounds__(512, 1) attn_bwd_dual_kernel(const __grid_cons
     const float2 sl2x2 = make_float2(sl2, sl2), one2 = make_float2(1.f, 1.f), zero2 = make_float2(0.f, 0.f);
     const float cap_c2 = CAP ? p.softcap * 1.4426950408889634f : 0.f;
     const float cap_k1 = CAP ? 2.f * sl2 / p.softcap : 0.f, cap_ic2 = CAP ? 1.f / cap_c2 : 0.f;
+    // Query column qc of a step is row i0 + (qc & rmask) of query head
+    // h0 + qc / qrows (qrows = 128 unless a KV head's query heads share a tile).
+    const int rmask = qrows - 1, qshift = PACK ? 31 - __clz(qrows) : 7;  // qrows is a power of two
     uint32_t nz = 0, gstep = 0;
     bool ok = true;
     // lse and Delta of 2 of this half's query columns per lane for one step,
     // loaded one step ahead and left in flight (-inf / 0 outside the segment).
     auto fetch_rows = [&](const BwdItem& t, int k, float (&lv)[2], float (&dv)[2]) {
-      const int h = t.hk * G + k / t.nqt, i0 = (t.qt0 + k % t.nqt) * kBM;
+      const int h0 = t.hk * G + (k / t.nqt) * hpack, i0 = (t.qt0 + k % t.nqt) * qrows;
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const int qc = cb + lane * 2 + e;
-        const int f = t.cq0 + i0 + qc;
-        const bool in = i0 + qc < t.m && f < p.q_rows;
+        const int h = h0 + (qc >> qshift), ri = qc & rmask;
+        const int f = t.cq0 + i0 + ri;
+        const bool in = i0 + ri < t.m && f < p.q_rows;
         const int fs = in ? f : 0;
         const int bq = fs / p.seg.Sq, sq = fs - bq * p.seg.Sq;
         lv[e] = -CUDART_INF_F;
@@ -375,20 +384,20 @@ __global__ void __launch_bounds__(512, 1) attn_bwd_dual_kernel(const __grid_cons
       float nlv[2], ndv[2];
       fetch_rows(t, t.k0, nlv, ndv);
       for (int k = t.k0; k < t.k1; ++k, ++gstep) {
-        const int i0 = (t.qt0 + k % t.nqt) * kBM;
+        const int i0 = (t.qt0 + k % t.nqt) * qrows;
         *reinterpret_cast<float2*>(my_nlse + lane * 2) = make_float2(neg_lse2(nlv[0]), neg_lse2(nlv[1]));
         *reinterpret_cast<float2*>(my_ndl + lane * 2) = make_float2(-ndv[0], -ndv[1]);
         __syncwarp();
         if (k + 1 < t.k1) fetch_rows(t, k + 1, nlv, ndv);
-        // Per-key visible query columns [q_lo, q_hi) of this tile, relative to
-        // this half's first column.
+        // Per-key visible query rows [q_lo, q_hi) of the tile, relative to i0
+        // (the same rows in every head block of a packed tile); this half's
+        // columns cover rows [rstart, rend) of each of its head blocks.
         int q_lo = p.seg.causal ? j - delta - i0 : -0x40000000;
         int q_hi = t.m - i0;
         if (p.seg.window > 0) q_hi = min(q_hi, j - delta + p.seg.window - i0);
         if (!valid) q_lo = q_hi = 0;
-        q_lo -= cb;
-        q_hi -= cb;
-        const bool masked = __any_sync(0xffffffffu, q_lo > 0 || q_hi < 64);
+        const int rstart = cb & rmask, rend = rstart + min(64, qrows);
+        const bool masked = __any_sync(0xffffffffu, q_lo > rstart || q_hi < rend);
         if (!wait_bar(&s_full, gstep & 1, ctl)) {
           ok = false;
           break;
@@ -427,9 +436,9 @@ __global__ void __launch_bounds__(512, 1) attn_bwd_dual_kernel(const __grid_cons
                 }
                 float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
                 if constexpr (MASK) {
-                  const int qc = c * 32 + 2 * e;
-                  p0 = (qc < q_lo || qc >= q_hi) ? 0.f : p0;
-                  p1 = (qc + 1 < q_lo || qc + 1 >= q_hi) ? 0.f : p1;
+                  const int rc = (cb + c * 32 + 2 * e) & rmask;  // row of the column pair's first column
+                  p0 = (rc < q_lo || rc >= q_hi) ? 0.f : p0;
+                  p1 = (rc + 1 < q_lo || rc + 1 >= q_hi) ? 0.f : p1;
                 }
                 pk[e] = pack2<T>(p0, p1);
                 if constexpr (CAP) pfk[e] = pack2<T>(p0 * fac.x, p1 * fac.y);
@@ -548,14 +557,15 @@ __global__ void __launch_bounds__(512, 1) attn_bwd_dual_kernel(const __grid_cons
       if (w < 0) break;
       if (t.k1 == t.k0) continue;
       for (int k = t.k0; k < t.k1; ++k, ++gstep) {
-        const int h = t.hk * G + k / t.nqt, qt = t.qt0 + k % t.nqt;
+        // this warp's 32 rows lie in one head block (packing keeps qrows >= 32)
+        const int h = t.hk * G + (k / t.nqt) * hpack + (32 * wq) / qrows, qt = t.qt0 + k % t.nqt;
         if (!wait_bar(&dq_full, gstep & 1, ctl)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t rq = tmem + lane_base + C::T_B;
-        const int fq = t.cq0 + qt * kBM + 32 * wq, bq = fq / p.seg.Sq, sq = fq - bq * p.seg.Sq;
+        const int fq = t.cq0 + qt * qrows + ((32 * wq) & (qrows - 1)), bq = fq / p.seg.Sq, sq = fq - bq * p.seg.Sq;
 #pragma unroll
         for (int rnd = 0; rnd < DQK / 64; ++rnd) {
           uint32_t a[2][32];

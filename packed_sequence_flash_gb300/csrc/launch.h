@@ -37,6 +37,8 @@ cudaError_t launch_fwd_capped(const FwdParams& p, int dqk, int dvc, int grid, in
 cudaError_t launch_bwd(const BwdParams& p, int dqk, int dv, int sms, int item_cap, int f16, cudaStream_t st);
 // The softcapped kernels (bwd_cap.cu); launch_bwd calls it when p.softcap > 0.
 cudaError_t launch_bwd_capped(const BwdParams& p, int dqk, int dv, int grid, int f16, cudaStream_t st);
+// Packed query heads (bwd_pack.cu); launch_bwd calls it when p.pack > 1.
+cudaError_t launch_bwd_packed(const BwdParams& p, int dqk, int dv, int grid, int f16, cudaStream_t st);
 int fwd_smem_bytes(int dqk, int dvc);
 int bwd_smem_bytes(int dqk, int dv);
 

@@ -569,8 +569,40 @@ def test_document_causal_pack_gqa_with_backward():
     out, lse, seg = psf.document_causal_attention(q, k, v, ids, ids, 0, w.scale, None, pack_gqa=True)
     out_o, lse_o = oracle.attn_fwd_document(w.q, w.k, w.v, w.doc_ids, 0, w.scale, None)
     assert_fwd(out, lse, out_o, lse_o)
-    grads = psf.document_causal_attention_backward(do, q, k, v, out, lse, seg, w.scale)
+    grads = psf.document_causal_attention_backward(do, q, k, v, out, lse, seg, w.scale, pack_gqa=True)
     ref = oracle.attn_bwd_document(w.dout, w.q, w.k, w.v, out_o, lse_o, w.doc_ids, 0, w.scale, None)
+    assert_grads(grads, ref)
+    assert psf.device_status() == 0
+
+
+@pytest.mark.parametrize("D,G,causal,window,cap", [(128, 4, True, None, None), (64, 2, False, None, None),
+                                                   (128, 2, True, 45, None), (64, 4, True, None, 2.0),
+                                                   (128, 8, True, None, None)])
+def test_varlen_bwd_pack_gqa_matches_oracle(D, G, causal, window, cap):
+    # short and long segments, empty ones, uncovered tail rows; G = 8 asks for
+    # packing that the backward does not do (same results either way)
+    r = np.random.default_rng(300 + G + D)
+    lens_q = [int(x) for x in r.integers(0, 50, 30)] + [260, 0, 3]
+    lens_k = [lq + int(r.integers(0, 20)) if causal else int(r.integers(1, 70)) for lq in lens_q]
+    cu_q = np.concatenate([[0], np.cumsum(lens_q)]).astype(np.int32)
+    cu_k = np.concatenate([[0], np.cumsum(lens_k)]).astype(np.int32)
+    Hkv = 2
+    Hq = G * Hkv
+    Tq, Tk = int(cu_q[-1]) + 7, int(cu_k[-1])
+    q = inputs.randn16((Tq, Hq, D), G * 41 + 1)
+    k = inputs.randn16((Tk, Hkv, D), G * 41 + 2)
+    v = inputs.randn16((Tk, Hkv, D), G * 41 + 3)
+    do = inputs.randn16((Tq, Hq, D), G * 41 + 4)
+    scale = 1.0 / np.sqrt(D)
+    cq, ck = torch.from_numpy(cu_q).cuda(), torch.from_numpy(cu_k).cuda()
+    mq, mk = max(lens_q), max(lens_k)
+    out, lse = psf.attn_varlen_fwd(cuda(q), cuda(k), cuda(v), cq, ck, mq, mk, scale, causal, window, softcap=cap,
+                                   pack_gqa=True)
+    out_o, lse_o = oracle.attn_fwd_segments(q, k, v, cu_q, cu_k, scale, causal, window, softcap=cap)
+    assert_fwd(out, lse, out_o, lse_o)
+    grads = psf.attn_varlen_bwd(cuda(do), cuda(q), cuda(k), cuda(v), out, lse, cq, ck, mq, mk, scale, causal,
+                                window, softcap=cap, pack_gqa=True)
+    ref = oracle.attn_bwd_segments(do, q, k, v, out_o, lse_o, cu_q, cu_k, scale, causal, window, softcap=cap)
     assert_grads(grads, ref)
     assert psf.device_status() == 0
 
