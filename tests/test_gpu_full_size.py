@@ -1,5 +1,6 @@
-"""Full-size parity: the five workloads at their stated sizes, run through the
-same calls the benchmark times, checked against the oracle on sampled rows
+"""Full-size parity: the five workloads at their stated sizes (and the
+short-document workload with packed query heads), run through the same calls
+the benchmark times, checked against the oracle on sampled rows
 (the oracle evaluates forward rows and dQ rows one query at a time and dK/dV
 rows one key at a time).
 
@@ -50,27 +51,31 @@ def _check_grad_rows(g, ref, rows, name):
     assert e <= GRAD_TOL, f"{name} relative Frobenius error {e:.3e} on sampled rows"
 
 
-def _doc_full(cfg, n_rows=192):
+def _doc_full(cfg, n_rows=192, softcap=None, pack_gqa=False):
     w = inputs.config(cfg, seed=0)
     dev = "cuda"
     q, k, v, do = (t.to(dev) for t in (w.q, w.k, w.v, w.dout))
     ids = torch.from_numpy(w.doc_ids).to(dev)
     Lq = w.q.shape[0]
     qids = ids[:, w.q_global_start:w.q_global_start + Lq].contiguous()
-    out, lse, seg = psf.document_causal_attention(q, k, v, qids, ids, w.q_global_start, w.scale, w.window)
-    grads = psf.document_causal_attention_backward(do, q, k, v, out, lse, seg, w.scale, w.window)
+    out, lse, seg = psf.document_causal_attention(q, k, v, qids, ids, w.q_global_start, w.scale, w.window,
+                                                  softcap=softcap, pack_gqa=pack_gqa)
+    grads = psf.document_causal_attention_backward(do, q, k, v, out, lse, seg, w.scale, w.window, softcap=softcap,
+                                                   pack_gqa=pack_gqa)
     assert psf.device_status() == 0
     # sample rows, always including document edges and the shard edges
     starts = np.cumsum([0] + w.extra["lengths"])
     q_rows = _rows(Lq, n_rows, 1, must=[0, Lq - 1] + [s - w.q_global_start for s in starts])
     k_rows = _rows(w.k.shape[0], n_rows, 2, must=[0, w.k.shape[0] - 1] + list(starts[:-1]) + list(starts[1:] - 1))
     out_o, lse_o = oracle.attn_fwd_document(w.q, w.k, w.v, w.doc_ids, w.q_global_start, w.scale, w.window,
-                                            rows=q_rows)
+                                            rows=q_rows, softcap=softcap)
     _check_fwd_rows(out, lse, out_o, lse_o, q_rows)
     # the oracle backward needs the oracle's out/lse on every query row a sampled key sees
-    out_all, lse_all = oracle.attn_fwd_document(w.q, w.k, w.v, w.doc_ids, w.q_global_start, w.scale, w.window)
+    out_all, lse_all = oracle.attn_fwd_document(w.q, w.k, w.v, w.doc_ids, w.q_global_start, w.scale, w.window,
+                                                softcap=softcap)
     dq_o, dk_o, dv_o = oracle.attn_bwd_document(w.dout, w.q, w.k, w.v, out_all, lse_all, w.doc_ids,
-                                                w.q_global_start, w.scale, w.window, q_rows=q_rows, k_rows=k_rows)
+                                                w.q_global_start, w.scale, w.window, q_rows=q_rows, k_rows=k_rows,
+                                                softcap=softcap)
     _check_grad_rows(grads[0], dq_o, q_rows, "dq")
     _check_grad_rows(grads[1], dk_o, k_rows, "dk")
     _check_grad_rows(grads[2], dv_o, k_rows, "dv")
@@ -82,6 +87,16 @@ def test_workload2_full_size():
 
 def test_workload4_full_size_shard_unequal_dims():
     _doc_full(4)
+
+
+def test_workload2_full_size_softcap():
+    _doc_full(2, softcap=30.0)
+
+
+def test_short_documents_full_size_pack_gqa():
+    # 65536 tokens of 16-64 token documents, the query heads of each KV head
+    # packed into one tile in the forward and one step in the backward
+    _doc_full(6, n_rows=256, pack_gqa=True)
 
 
 def test_workload3_dense_d512_full_size():
