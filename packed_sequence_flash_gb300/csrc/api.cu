@@ -238,9 +238,9 @@ int check_dtype(int dtype) {
 
 // TMA view of a 16-bit (bf16 or fp16) tensor; a box is box_d x box_s rows x box_h heads.
 int make_map16(CUtensorMap* m, const void* base, int D, int S, int H, int B, const View& v, int box_d, int dtype,
-               int box_s = kBM, int box_h = 1) {
+               int box_s = kBM, int box_h = 1, CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
   int rc = make_tmap_4d(m, dtype == PSF_DTYPE_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                        2, base, D, S, H, B, v.ss, v.sh, v.sb, box_d, box_s, CU_TENSOR_MAP_SWIZZLE_128B, box_h);
+                        2, base, D, S, H, B, v.ss, v.sh, v.sb, box_d, box_s, swz, box_h);
   if (rc) return fail(PSF_ECUDA, "cuTensorMapEncodeTiled failed (%d) for a [%d,%d,%d,%d] view", rc, B, H, S, D);
   return PSF_OK;
 }
@@ -289,6 +289,10 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, void* out, float*
   FwdParams p;
   memset(&p, 0, sizeof(p));
   if ((rc = make_map16(&p.tm_q, q, Dqk, Sq, Hq, B, vq, 64, dtype, qrows, pack))) return rc;
+  // The two-CTA kernel (head dims 64, 128) stores out in 32 x 32 boxes.
+  if (Dqk == Dv && (Dv == 64 || Dv == 128) &&
+      (rc = make_map16(&p.tm_o, out, Dv, Sq, Hq, B, vo, 32, dtype, 32, 1, CU_TENSOR_MAP_SWIZZLE_64B)))
+    return rc;
   if (k_rows > 0) {
     if ((rc = make_map16(&p.tm_k, k, Dqk, Sk, Hkv, B, vk, 64, dtype))) return rc;
     if ((rc = make_map16(&p.tm_v, v, Dv, Sk, Hkv, B, vv, 64, dtype))) return rc;

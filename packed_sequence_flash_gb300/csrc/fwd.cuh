@@ -35,6 +35,7 @@ namespace psf {
 
 struct FwdParams {
   CUtensorMap tm_q, tm_k, tm_v;  // (d, s, h, b) views, box (64, 128), 128B swizzle, bf16
+  CUtensorMap tm_o;              // out, box (32, 32), 64B swizzle (the two-CTA kernel's epilogue stores)
   SegInfo seg;
   void* out;  // T (bf16 or fp16), the inputs' type
   int64_t o_sb, o_ss, o_sh;  // element strides of out (batch, row, head)

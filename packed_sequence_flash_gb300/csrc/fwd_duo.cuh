@@ -53,7 +53,8 @@ struct FwdDuoCfg {
   static constexpr int TILE_BYTES = CH * kChunkBytes;
   static constexpr int Q_OFF = 0;
   static constexpr int SLOT_OFF = TILE_BYTES;  // two slots
-  static constexpr int SMEM_USED = 3 * TILE_BYTES + 1024;
+  static constexpr int STG_OFF = 3 * TILE_BYTES;  // epilogue staging: 4 softmax warps x (32 rows x 64 B)
+  static constexpr int SMEM_USED = STG_OFF + 4 * 2048 + 1024;
   // Never more than two CTAs per SM: a third could not allocate its TMEM.
   static constexpr int SMEM_BYTES = SMEM_USED > 80 * 1024 ? SMEM_USED : 80 * 1024;
   static constexpr int T_S = 0;
@@ -404,15 +405,36 @@ __global__ void __launch_bounds__(192, 2) attn_fwd_duo_kernel(const __grid_const
       ++ntile;
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
+      // A warp whose 32 rows are all real rows of one head (all valid, and
+      // qrows >= 32) stores them as 32 x 32 boxes: each row's 64 bytes into a
+      // 64-byte-swizzled staging buffer, then one TMA store per box. Other
+      // warps (a segment's last tile, heads packed 8 or 16 to a tile) store
+      // their valid rows directly.
+      const bool boxed = qrows >= 32 && __all_sync(0xffffffffu, valid);
+      uint8_t* stg = smem + C::STG_OFF + warp * 2048;
+      const int s_box = __shfl_sync(0xffffffffu, sq, 0), b_box = __shfl_sync(0xffffffffu, bq, 0);
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t r[32];
         tmem_ld32(to + c * 32, r);
-        if (valid) {
-          uint32_t pk[16];
+        uint32_t pk[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e)
-            pk[e] = pack2<T>(__uint_as_float(r[2 * e]) * inv, __uint_as_float(r[2 * e + 1]) * inv);
+        for (int e = 0; e < 16; ++e)
+          pk[e] = pack2<T>(__uint_as_float(r[2 * e]) * inv, __uint_as_float(r[2 * e + 1]) * inv);
+        if (boxed) {
+          if (lane == 0) bulk_wait_group_read0();  // the buffer's previous box has been read
+          __syncwarp();
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            *reinterpret_cast<uint4*>(stg + lane * 64 + ((q ^ ((lane >> 1) & 3)) << 4)) =
+                make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_4d(&p.tm_o, stg, c * 32, s_box, h, b_box);
+            bulk_commit_group();
+          }
+        } else if (valid) {
           uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
           for (int e = 0; e < 4; ++e) dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
@@ -423,6 +445,8 @@ __global__ void __launch_bounds__(192, 2) attn_fwd_duo_kernel(const __grid_const
       __syncwarp();
       if (lane == 0) mbar_arrive(&o_free);
     }
+    // Every box this warp stored has been written out before the CTA exits.
+    if (lane == 0) bulk_wait_group0();
   }
   tc_fence_before();
   __syncthreads();
