@@ -77,7 +77,7 @@ int device_info(DeviceInfo** out) {
     d.ready = true;
   }
   if (!(d.major == 10 && d.minor == 3))
-    return fail(PSF_EUNSUPPORTED, "device compute capability %d.%d; this build targets sm_103a", d.major, d.minor);
+    return fail(PSF_EUNSUPPORTED, "device compute capability %d.%d; the library is compiled for sm_103a", d.major, d.minor);
   *out = &d;
   return PSF_OK;
 }
