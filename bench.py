@@ -219,9 +219,34 @@ def config_dict(w, args, pairs, n_docs):
 
 # ---------------------------------------------------------------------------
 
+# ---------------------------------------------------------------------------
+# ranks: one replica per GPU, no collective on the data path
+
+def replica_seed(seed: int, rank: int) -> int:
+    """Each rank runs its own replica of the workload, drawn with its own seed."""
+    return seed + rank
+
+
+def max_over_ranks(x: float, dist=None, device=None) -> float:
+    """The largest of the ranks' values, on every rank (the timing rule: a
+    step takes as long as the slowest replica)."""
+    if dist is None:
+        return x
+    import torch
+
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_value(world: int, flops_per_replica: float, ms_max: float) -> float:
+    """Whole-job TFLOP/s: every replica's work over the slowest replica's time."""
+    return world * flops_per_replica / (ms_max * 1e-3) / 1e12
+
+
 def reference_arm(args):
     rank = int(os.environ.get("RANK", "0"))
-    if rank != 0:
+    if rank != 0:  # the oracle runs once, on rank 0; other ranks exit without work
         return 0
     w = inputs.config(args.config, args.seed)
     pairs, _, _ = workload_flops(w)
@@ -271,7 +296,7 @@ def our_arm(args):
     dev = torch.device("cuda", torch.cuda.current_device())
     lib = _lib.load()
 
-    w = inputs.config(args.config, args.seed + rank)
+    w = inputs.config(args.config, replica_seed(args.seed, rank))
     if args.dtype == "fp16":
         # the same draws held as fp16 (fp16 storage and fp16 tensor-core inputs)
         w.q, w.k, w.v, w.dout = (t.to(torch.float16) for t in (w.q, w.k, w.v, w.dout))
@@ -356,11 +381,7 @@ def our_arm(args):
     ms = statistics.mean(per_step)
     if psf.device_status() != 0:
         raise RuntimeError("device status after the timed steps is not OK")
-    ms_max = ms
-    if dist:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_max = float(t.item())
+    ms_max = max_over_ranks(ms, dist, dev)
 
     # ---- end to end through the public API: every step copies its inputs in
     # from pinned host memory and its results (out, lse, dq, dk, dv) back out.
@@ -422,11 +443,7 @@ def our_arm(args):
     comp_s.wait_event(d2h_done)
     e_stop.record(comp_s)
     torch.cuda.synchronize()
-    e2e_ms = e_start.elapsed_time(e_stop) / e2e_steps
-    if dist:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e_start.elapsed_time(e_stop) / e2e_steps, dist, dev)
 
     if rank != 0:
         if dist:
@@ -451,7 +468,7 @@ def our_arm(args):
     roofline["traffic"] = cap[1] if cap and cap[0] == kernel_source_hash(dominant) else None
     other = [n for n in roof if n != dominant][0]
 
-    value = world * flops / (ms_max * 1e-3) / 1e12
+    value = whole_job_value(world, flops, ms_max)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
@@ -464,7 +481,7 @@ def our_arm(args):
         "timing": ("each step replayed as one captured CUDA graph" if graph is not None else graph_note),
         "ms_per_step_eager": statistics.mean(eager_steps),
         "roofline": roofline, "roofline_other": dict(roof[other], kernel=other),
-        "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+        "e2e": {"value": whole_job_value(world, flops, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms,
                 "timing": "steps pipelined: uploads and downloads overlap neighbouring steps' compute"},
         "gpu_launches": 6 * args.steps,

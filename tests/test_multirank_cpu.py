@@ -1,0 +1,86 @@
+"""The benchmark's multi-rank host logic on CPU: two gloo ranks (one process
+each), as the N > 1 launch runs one replica per GPU. Each rank draws its own
+replica, the step time is the slowest rank's, the whole-job value counts every
+replica's work, and the reference arm runs on rank 0 only."""
+import importlib.util
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _bench():
+    spec = importlib.util.spec_from_file_location("bench_under_test", os.path.join(ROOT, "bench.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+_WORKER = r"""
+import json, os, sys
+sys.path.insert(0, {root!r})
+import importlib.util
+import torch
+import torch.distributed as dist
+spec = importlib.util.spec_from_file_location("b", os.path.join({root!r}, "bench.py"))
+b = importlib.util.module_from_spec(spec); spec.loader.exec_module(b)
+dist.init_process_group("gloo")
+rank, world = dist.get_rank(), dist.get_world_size()
+ms = [3.0, 5.0][rank]
+ms_max = b.max_over_ranks(ms, dist, "cpu")
+from packed_sequence_flash_gb300 import inputs
+w = inputs.config(2, b.replica_seed(0, rank))
+print(json.dumps({{"rank": rank, "ms_max": ms_max, "value": b.whole_job_value(world, 1e12, ms_max),
+                  "first_len": int(w.extra["lengths"][0])}}))
+dist.destroy_process_group()
+"""
+
+
+def test_two_gloo_ranks_share_the_slowest_step_and_draw_their_own_replicas(tmp_path):
+    script = tmp_path / "worker.py"
+    script.write_text(_WORKER.format(root=ROOT))
+    port = _free_port()
+    procs = []
+    for rank in range(2):
+        env = dict(os.environ, RANK=str(rank), WORLD_SIZE="2", LOCAL_RANK=str(rank), MASTER_ADDR="127.0.0.1",
+                   MASTER_PORT=str(port), CUDA_VISIBLE_DEVICES="")
+        procs.append(subprocess.Popen([sys.executable, str(script)], env=env, stdout=subprocess.PIPE,
+                                      stderr=subprocess.PIPE, text=True))
+    outs = []
+    for p in procs:
+        o, e = p.communicate(timeout=240)
+        assert p.returncode == 0, e
+        outs.append(json.loads(o.strip().splitlines()[-1]))
+    for o in outs:
+        assert o["ms_max"] == 5.0                          # the slowest rank's time on every rank
+        assert abs(o["value"] - 2 * 1e12 / 5e-3 / 1e12) < 1e-9  # both replicas' work over that time
+    assert outs[0]["first_len"] != outs[1]["first_len"]    # each rank its own draws
+
+
+def test_reference_arm_runs_on_rank_zero_only(monkeypatch, capsys):
+    b = _bench()
+    monkeypatch.setenv("RANK", "1")
+
+    class Args:
+        config, seed, warmup, steps, gpus, softcap = 2, 0, 3, 1, 2, None
+
+    assert b.reference_arm(Args()) == 0
+    assert capsys.readouterr().out == ""
+
+
+def test_single_rank_needs_no_process_group():
+    b = _bench()
+    assert b.max_over_ranks(4.25) == 4.25
+    assert b.replica_seed(7, 0) == 7
+    assert b.whole_job_value(1, 2e9, 1.0) == pytest.approx(2.0)
