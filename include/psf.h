@@ -83,6 +83,18 @@ int psf_device_status(int clear);
 void psf_set_wait_limit_ns(uint64_t ns);
 
 /*
+ * Check of the failure path every pipeline wait takes, without a fault: one
+ * CTA of 64 threads on `stream` whose warp 0 waits on an mbarrier that expects
+ * one arrival. With arrive != 0 warp 1 arrives and the kernel ends at once;
+ * with arrive == 0 nothing arrives, the wait gives up after the current wait
+ * limit (psf_set_wait_limit_ns), records PSF_ETIMEOUT in the status word that
+ * psf_device_status() reads, and the kernel returns normally, leaving the
+ * context usable. Returns PSF_OK once launched (PSF_EUNSUPPORTED on another
+ * device, PSF_ECUDA if the launch fails).
+ */
+int psf_check_pipeline_wait(int arrive, void* stream);
+
+/*
  * Kernel timing for profiling. psf_kernel_timing(1) clears the record and
  * starts it: from then on every attention call records two CUDA events on its
  * stream, immediately before and after its main kernel (kind 0: forward main

@@ -8,7 +8,7 @@ this package only marshals arguments.
 """
 from .attention import (NO_WINDOW, attn_dense_bwd, attn_dense_fwd, attn_varlen_bwd, attn_varlen_fwd,
                         build_cross_segments, build_doc_segments, bwd_workspace_size, check_device_status,
-                        chunk_attention, chunk_attention_backward, chunk_dense_eligible,
+                        check_pipeline_wait, chunk_attention, chunk_attention_backward, chunk_dense_eligible,
                         device_status, document_causal_attention, document_causal_attention_backward,
                         fwd_workspace_size, grad_add_live_rows, lse_merge, lse_merge_live_rows, pad_fixup,
                         set_wait_limit_ns)
@@ -17,7 +17,7 @@ from ._lib import PSFError
 __all__ = [
     "NO_WINDOW", "PSFError", "attn_dense_bwd", "attn_dense_fwd", "attn_varlen_bwd", "attn_varlen_fwd",
     "build_cross_segments", "build_doc_segments", "bwd_workspace_size", "check_device_status",
-    "chunk_attention", "chunk_attention_backward", "chunk_dense_eligible", "device_status",
+    "check_pipeline_wait", "chunk_attention", "chunk_attention_backward", "chunk_dense_eligible", "device_status",
     "document_causal_attention", "document_causal_attention_backward", "fwd_workspace_size",
     "grad_add_live_rows", "lse_merge", "lse_merge_live_rows", "pad_fixup", "set_wait_limit_ns",
 ]

@@ -27,6 +27,7 @@ SIGNATURES = {
     "psf_device_supported": (I, []),
     "psf_device_status": (I, [I]),
     "psf_set_wait_limit_ns": (None, [U64]),
+    "psf_check_pipeline_wait": (I, [I, P]),
     "psf_kernel_timing": (I, [I]),
     "psf_kernel_times_ms": (I, [I, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int)]),
     "psf_attn_fwd_workspace_size": (SZ, [I64, I]),

@@ -79,6 +79,13 @@ def set_wait_limit_ns(ns: int) -> None:
     _lib.load().psf_set_wait_limit_ns(int(ns))
 
 
+def check_pipeline_wait(arrive: bool) -> None:
+    """Launch the bounded-wait check on the current stream: with arrive=False
+    its wait runs out after the wait limit and records PSF_ETIMEOUT, which
+    device_status() then returns; with arrive=True it records nothing."""
+    check(_lib.load().psf_check_pipeline_wait(1 if arrive else 0, _stream()))
+
+
 def fwd_workspace_size(total_q_rows: int, nseg: int) -> int:
     return int(_lib.load().psf_attn_fwd_workspace_size(int(total_q_rows), int(nseg)))
 

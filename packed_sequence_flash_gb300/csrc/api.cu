@@ -493,6 +493,14 @@ int psf_device_status(int clear) {
 
 void psf_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns = ns > 0 ? ns : 1; }
 
+int psf_check_pipeline_wait(int arrive, void* stream) {
+  DeviceInfo* dev = nullptr;
+  int rc = device_info(&dev);
+  if (rc) return rc;
+  cudaError_t e = launch_wait_check(arrive != 0, g_wait_limit_ns, dev->status, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PSF_OK : cuda_fail(e, "wait-check launch");
+}
+
 int psf_kernel_timing(int enable) {
   std::lock_guard<std::mutex> lk(g_timing_mu);
   if (enable) timing_clear_locked();

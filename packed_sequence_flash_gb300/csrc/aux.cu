@@ -987,4 +987,35 @@ cudaError_t launch_bwd_convert(const float* dq_acc, void* dq, bool have_q, int B
   return cudaGetLastError();
 }
 
+
+namespace {
+
+// Check of the bounded pipeline wait: warp 0 waits on an mbarrier that expects
+// one arrival, which warp 1 makes only when `arrive` is set. Without it the
+// wait runs out after limit_ns, records kStatusTimeout in the status word and
+// the kernel returns, as every pipeline wait in the attention kernels does.
+__global__ void __launch_bounds__(64, 1) wait_check_kernel(int arrive, uint64_t limit_ns, int* status) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x >= 32) {
+    if (arrive && threadIdx.x == 32) mbar_arrive(&bar);
+    return;
+  }
+  const Ctl c{status, limit_ns, &abort_flag};
+  wait_bar(&bar, 0, c);
+}
+
+}  // namespace
+
+cudaError_t launch_wait_check(int arrive, uint64_t limit_ns, int* status, cudaStream_t st) {
+  wait_check_kernel<<<1, 64, 0, st>>>(arrive, limit_ns, status);
+  return cudaGetLastError();
+}
+
 }  // namespace psf

@@ -70,4 +70,8 @@ cudaError_t launch_bwd_convert(const float* dq_acc, void* dq, bool have_q, int B
                                int64_t k_sh, int64_t v_sb, int64_t v_ss, int64_t v_sh, float scale, int f16,
                                cudaStream_t st);
 
+// One CTA whose warp 0 makes one bounded pipeline wait; it runs out (and
+// records kStatusTimeout in *status) unless `arrive` is set.
+cudaError_t launch_wait_check(int arrive, uint64_t limit_ns, int* status, cudaStream_t st);
+
 }  // namespace psf

@@ -146,6 +146,24 @@ def test_builder_capacity_too_small_reports_device_args():
     assert psf.device_status() == -4
 
 
+def test_pipeline_wait_runs_out_and_reports_timeout():
+    # The failure path of every bounded pipeline wait, without a fault: a wait
+    # that nothing completes gives up after the limit, the status word reads
+    # PSF_ETIMEOUT, and the context stays usable.
+    assert psf.device_status() == 0
+    psf.set_wait_limit_ns(2_000_000)
+    try:
+        psf.check_pipeline_wait(arrive=True)
+        assert psf.device_status() == 0
+        psf.check_pipeline_wait(arrive=False)
+        assert psf.device_status() == -5
+        assert psf.device_status() == 0
+    finally:
+        psf.set_wait_limit_ns(2_000_000_000)
+    w = inputs.small_document_workload(500, 2, 1, 64, 64, 4, max_len=200)
+    doc_case(w)
+
+
 # ---------------------------------------------------------------- forward + backward, varlen
 
 def _rand_segments(r, nseg, max_len, allow_empty=True):
