@@ -566,29 +566,43 @@ __global__ void __launch_bounds__(512, 1) attn_bwd_dual_kernel(const __grid_cons
         tc_fence_after();
         const uint32_t rq = tmem + lane_base + C::T_B;
         const int fq = t.cq0 + qt * qrows + ((32 * wq) & (qrows - 1)), bq = fq / p.seg.Sq, sq = fq - bq * p.seg.Sq;
+        // One 32 x 32 fp32 box of dQ into the staging box and on to the
+        // accumulator by TMA reduce-add (after the box's previous reduce has
+        // read it).
+        auto reduce_box = [&](const uint32_t(&v)[32], int cchunk) {
+          if (lane == 0) bulk_wait_group_read0();
+          __syncwarp();
 #pragma unroll
-        for (int rnd = 0; rnd < DQK / 64; ++rnd) {
-          uint32_t a[2][32];
-          tmem_ld32x2(rq + rnd * 64, rq + rnd * 64 + 32, a[0], a[1]);
-          // These 64 columns of B are read: they can take the next dP half.
+          for (int u = 0; u < 8; ++u)
+            *reinterpret_cast<uint4*>(box + sw128_offset(lane, u)) =
+                make_uint4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_reduce_add_4d(&p.tm_dq, box, cchunk * 32, sq, h, bq);
+            bulk_commit_group();
+          }
+        };
+        // Columns 0-63 of B, then (Dqk = 128) columns 64-127 as soon as the
+        // first box is on its way, so both dP halves can follow the dQ MMA
+        // without waiting for the boxes' reduce traffic.
+        uint32_t a[2][32];
+        tmem_ld32x2(rq, rq + 32, a[0], a[1]);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&dq_free[0]);
+        reduce_box(a[0], 0);
+        if constexpr (DQK > 64) {
+          uint32_t b[2][32];
+          tmem_ld32x2(rq + 64, rq + 96, b[0], b[1]);
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&dq_free[rnd]);
-#pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            if (lane == 0) bulk_wait_group_read0();
-            __syncwarp();
-#pragma unroll
-            for (int u = 0; u < 8; ++u)
-              *reinterpret_cast<uint4*>(box + sw128_offset(lane, u)) =
-                  make_uint4(a[c][4 * u], a[c][4 * u + 1], a[c][4 * u + 2], a[c][4 * u + 3]);
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-              tma_reduce_add_4d(&p.tm_dq, box, (rnd * 2 + c) * 32, sq, h, bq);
-              bulk_commit_group();
-            }
-          }
+          if (lane == 0) mbar_arrive(&dq_free[1]);
+          reduce_box(a[1], 1);
+          reduce_box(b[0], 2);
+          reduce_box(b[1], 3);
+        } else {
+          reduce_box(a[1], 1);
         }
       }
     }
