@@ -45,12 +45,19 @@ FALLBACK_BF16_TFLOPS = 1900.0
 FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 256 << 20
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of a main kernel from
-# one ncu capture: kernel -> (hash of the kernel's sources when captured, bytes).
-# Reported as null once the sources change.
+# one ncu capture: (kernel, workload) -> (hash of the kernel's sources when
+# captured, bytes). Reported as null for other workloads and once the sources
+# change.
 NCU_TRAFFIC = {
-    "attn_bwd_dual_kernel": ("ad639a2fde5cd4cc", 388020736),  # ncu capture on workload 2
-    "attn_fwd_duo_kernel": ("040e8ca8f1df30e3", 53567744),  # ncu capture on workload 2
+    ("attn_bwd_dual_kernel", "cfg2_doc_causal_t8192_d128"): ("ad639a2fde5cd4cc", 388020736),
+    ("attn_fwd_duo_kernel", "cfg2_doc_causal_t8192_d128"): ("040e8ca8f1df30e3", 53567744),
 }
+
+
+def ncu_traffic(kernel: str, workload: str):
+    """Captured DRAM bytes per launch of `kernel` on `workload`, or None."""
+    cap = NCU_TRAFFIC.get((kernel, workload))
+    return cap[1] if cap and cap[0] == kernel_source_hash(kernel) else None
 
 # Sources each main kernel is compiled from (for the hash above).
 KERNEL_SOURCES = {
@@ -464,9 +471,9 @@ def our_arm(args):
     dominant = bwd_name if bwd_ms >= fwd_ms else fwd_name
     roofline = dict(roof[dominant])
     roofline["kernel"] = dominant
-    cap = NCU_TRAFFIC.get(dominant)
-    roofline["traffic"] = cap[1] if cap and cap[0] == kernel_source_hash(dominant) else None
+    roofline["traffic"] = ncu_traffic(dominant, w.name)
     other = [n for n in roof if n != dominant][0]
+    roof[other]["traffic"] = ncu_traffic(other, w.name)
 
     value = whole_job_value(world, flops, ms_max)
     line = {

@@ -84,3 +84,11 @@ def test_single_rank_needs_no_process_group():
     assert b.max_over_ranks(4.25) == 4.25
     assert b.replica_seed(7, 0) == 7
     assert b.whole_job_value(1, 2e9, 1.0) == pytest.approx(2.0)
+
+
+def test_captured_traffic_is_reported_only_for_its_workload_and_sources():
+    b = _bench()
+    for (kernel, workload), (digest, nbytes) in b.NCU_TRAFFIC.items():
+        assert b.ncu_traffic(kernel, workload) == (nbytes if digest == b.kernel_source_hash(kernel) else None)
+        assert b.ncu_traffic(kernel, "another_workload") is None
+    assert b.ncu_traffic("attn_bwd_kernel", "cfg2_doc_causal_t8192_d128") is None
