@@ -416,7 +416,8 @@ __global__ void __launch_bounds__(512, 1) attn_bwd_dual_kernel(const __grid_cons
           for (int c = 0; c < 2; ++c) {
             uint32_t(&cur)[32] = c ? sb : sa;
             tmem_wait_ld32(cur);
-            uint32_t pk[16], pfk[16];
+            uint32_t pk[16];
+            [[maybe_unused]] uint32_t pfk[16];  // CAP only
 #pragma unroll
             for (int e4 = 0; e4 < 8; ++e4) {
               const float4 nl = *reinterpret_cast<const float4*>(my_nlse + c * 32 + e4 * 4);
@@ -424,7 +425,8 @@ __global__ void __launch_bounds__(512, 1) attn_bwd_dual_kernel(const __grid_cons
               for (int hf = 0; hf < 2; ++hf) {
                 const int e = e4 * 2 + hf;
                 const float2 nl2 = hf ? make_float2(nl.z, nl.w) : make_float2(nl.x, nl.y);
-                float2 x, fac = one2;
+                float2 x;
+                [[maybe_unused]] float2 fac = one2;  // CAP only
                 if constexpr (CAP) {
                   const float2 y = make_float2(softcap_log2(__uint_as_float(cur[2 * e]), cap_k1, cap_c2),
                                                softcap_log2(__uint_as_float(cur[2 * e + 1]), cap_k1, cap_c2));
