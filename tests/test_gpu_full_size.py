@@ -226,3 +226,41 @@ def test_workload5_cross_chunk_merge():
     for a, b, n in ((dq, gu[0], "dq"), (dk, gu[1], "dk"), (dv, gu[2], "dv")):
         e = float(torch.linalg.norm(a.float() - b.float()) / torch.linalg.norm(b.float()))
         assert e <= GRAD_TOL, f"{n}: chunked vs unsplit relative Frobenius {e:.3e}"
+
+
+def test_workload5_full_shard_lse_merge_and_pad_fixup():
+    # The plain two-result merge over the whole query shard of workload 5 (the
+    # local chunk's and the cross chunk's results, every row), against the
+    # oracle's merge of the same inputs on sampled rows and against the
+    # live-row merge on every row; then the literal pad fixup over the local
+    # result, which must leave it unchanged (padding rows are already zero).
+    w = inputs.config(5, seed=0)
+    dev = "cuda"
+    S = w.k.shape[0]
+    split = S // 2
+    Lq = S - split
+    q, k, v = (t.to(dev) for t in (w.q[split:], w.k, w.v))
+    ids_local = torch.from_numpy(np.ascontiguousarray(w.doc_ids[:, split:])).to(dev)
+    out1, lse1, _ = psf.document_causal_attention(q, k[split:], v[split:], ids_local, ids_local, 0, w.scale)
+    ids = torch.from_numpy(w.doc_ids).to(dev)
+    cq2, ck2, meta2 = psf.build_cross_segments(ids, split, Lq, 0, split)
+    out2, lse2 = psf.attn_varlen_fwd(q, k[:split], v[:split], cq2, ck2, -1, -1, w.scale, False, dev_meta=meta2)
+    of, ob, lm = psf.lse_merge(out1, lse1, out2, lse2, want_f32=True, want_bf16=True)
+    out_m, lse_m = out1.clone(), lse1.clone()
+    psf.lse_merge_live_rows(out_m, lse_m, out2, lse2, cq2, ck2, dev_meta=meta2)
+    assert psf.device_status() == 0
+    rows = _rows(Lq, 256, 11, must=[0, Lq - 1, int(cq2[2].item()) - 1, int(cq2[2].item())])
+    o_ref, l_ref = oracle.lse_merge(np64(out1)[rows], np64(lse1)[:, rows], np64(out2)[rows], np64(lse2)[:, rows])
+    assert np.max(np.abs(np64(of)[rows] - o_ref)) <= 1e-5
+    assert np.array_equal(np.isneginf(np64(lm)[:, rows]), np.isneginf(l_ref))
+    fin = np.isfinite(l_ref)
+    assert np.max(np.abs(np64(lm)[:, rows][fin] - l_ref[fin])) <= 1e-5
+    assert float((ob.float() - of).abs().max()) <= 2.0 ** -7 * max(1.0, float(of.abs().max()))
+    assert float((out_m.float() - ob.float()).abs().max()) <= 2.0 ** -7 * max(1.0, float(of.abs().max()))
+    assert torch.equal(torch.isneginf(lse_m), torch.isneginf(lm))
+    fin_t = torch.isfinite(lm)
+    assert float((lse_m[fin_t] - lm[fin_t]).abs().max()) <= 1e-5
+    before_o, before_l = out1.clone(), lse1.clone()
+    psf.pad_fixup(out1, lse1, ids_local[0].contiguous())
+    assert psf.device_status() == 0
+    assert torch.equal(out1, before_o) and torch.equal(lse1, before_l)
