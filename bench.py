@@ -105,10 +105,22 @@ def visible_pairs(doc_ids: np.ndarray, q0: int, Lq: int, window=None) -> int:
     return total
 
 
+def dense_pairs(Nq: int, Nk: int, causal: bool) -> int:
+    """Visible pairs of one dense [Nq x Nk] problem (causal: bottom-right aligned)."""
+    if not causal:
+        return Nq * Nk
+    return sum(max(0, min(Nk, i + Nk - Nq + 1)) for i in range(Nq))
+
+
 def workload_flops(w):
-    Lq = w.q.shape[0]
-    Hq, Dqk, Dv = w.q.shape[1], w.q.shape[2], w.v.shape[2]
-    pairs = visible_pairs(w.doc_ids, w.q_global_start, Lq, w.window) * Hq
+    if w.kind == "dense":
+        B, Hq, Nq, Dqk = w.q.shape
+        Nk, Dv = w.k.shape[2], w.v.shape[3]
+        pairs = B * Hq * dense_pairs(Nq, Nk, w.causal)
+    else:
+        Lq = w.q.shape[0]
+        Hq, Dqk, Dv = w.q.shape[1], w.q.shape[2], w.v.shape[2]
+        pairs = visible_pairs(w.doc_ids, w.q_global_start, Lq, w.window) * Hq
     return pairs, pairs * 2 * (Dqk + Dv), pairs * (6 * Dqk + 4 * Dv)
 
 
@@ -188,10 +200,28 @@ def cpu_sample_workload(w, frac=0.25, offset_docs=0):
     return sub, i - offset_docs
 
 
+def cpu_sample_dense(w, n_max=1024):
+    """Batch 0, the first KV head and its query heads, the leading n x n block
+    (itself a causal problem when Nq = Nk)."""
+    B, Hq, Nq, _ = w.q.shape
+    Hkv, Nk = w.k.shape[1], w.k.shape[2]
+    G = Hq // Hkv
+    n = min(Nq, Nk, n_max)
+    sub = inputs.Workload(f"{w.name}[b0, kv head 0, {n} rows]", "dense", w.q[:1, :G, :n], w.k[:1, :1, :n],
+                          w.v[:1, :1, :n], w.dout[:1, :G, :n], w.scale, w.causal)
+    return sub
+
+
 def run_oracle(sub, nthreads, softcap=None):
     import oracle
 
     t = time.perf_counter()
+    if sub.kind == "dense":
+        out, lse = oracle.attn_fwd_dense(sub.q, sub.k, sub.v, sub.scale, sub.causal, nthreads=nthreads,
+                                         softcap=softcap)
+        oracle.attn_bwd_dense(sub.dout, sub.q, sub.k, sub.v, out, lse, sub.scale, sub.causal, nthreads=nthreads,
+                              softcap=softcap)
+        return time.perf_counter() - t
     out, lse = oracle.attn_fwd_document(sub.q, sub.k, sub.v, sub.doc_ids, 0, sub.scale, sub.window,
                                         nthreads=nthreads, softcap=softcap)
     oracle.attn_bwd_document(sub.dout, sub.q, sub.k, sub.v, out, lse, sub.doc_ids, 0, sub.scale, sub.window,
@@ -207,16 +237,28 @@ def cores():
 
 
 def cpu_baseline(w, softcap=None):
-    sub, ndocs = cpu_sample_workload(w, 1.0)
+    if w.kind == "dense":
+        sub = cpu_sample_dense(w)
+        what = f"{sub.name}"
+    else:
+        sub, ndocs = cpu_sample_workload(w, 1.0)
+        what = f"all {ndocs} documents of the step ({sub.q.shape[0]} tokens"
     _, f, b = workload_flops(sub)
     c = cores()
     secs = run_oracle(sub, c, softcap)
+    what = what + (")" if w.kind != "dense" else "")
     return {"value": (f + b) / secs / 1e12, "unit": UNIT, "cores": c, "kind": "oracle",
-            "sample": f"fp64 oracle fwd+bwd on all {ndocs} documents of the step ({sub.q.shape[0]} tokens, "
-                      f"{(f + b) / 1e9:.1f} GFLOP), once, {secs:.1f} s"}
+            "sample": f"fp64 oracle fwd+bwd on {what}, {(f + b) / 1e9:.1f} GFLOP, once, {secs:.1f} s"}
 
 
 def config_dict(w, args, pairs, n_docs):
+    if w.kind == "dense":
+        B, Hq, Nq, Dqk = w.q.shape
+        return {"workload": w.name, "batch": int(B), "q_rows": int(Nq), "k_rows": int(w.k.shape[2]),
+                "Hq": int(Hq), "Hkv": int(w.k.shape[1]), "Dqk": int(Dqk), "Dv": int(w.v.shape[3]),
+                "causal": bool(w.causal), "visible_pairs_x_heads": int(pairs), "seed": args.seed,
+                "l2": "flushed between steps (256 MiB write)", "pack_gqa": bool(getattr(args, "pack_gqa", False)),
+                "softcap": getattr(args, "softcap", None)}
     return {"workload": w.name, "tokens": int(w.k.shape[0]), "q_tokens": int(w.q.shape[0]),
             "q_global_start": int(w.q_global_start), "Hq": int(w.q.shape[1]), "Hkv": int(w.k.shape[1]),
             "Dqk": int(w.q.shape[2]), "Dv": int(w.v.shape[2]), "window": w.window, "documents": n_docs,
@@ -260,9 +302,13 @@ def reference_arm(args):
     c = cores()
     total_f, total_s = 0.0, 0.0
     per = []
-    ndocs_total = len(w.extra["lengths"])
+    dense = w.kind == "dense"
+    ndocs_total = 0 if dense else len(w.extra["lengths"])
     for s in range(args.warmup + args.steps):
-        sub, nd = cpu_sample_workload(w, 0.06, offset_docs=s % max(ndocs_total - 1, 1))
+        if dense:
+            sub = cpu_sample_dense(w, 512)
+        else:
+            sub, nd = cpu_sample_workload(w, 0.06, offset_docs=s % max(ndocs_total - 1, 1))
         _, f, b = workload_flops(sub)
         secs = run_oracle(sub, c, args.softcap)
         if s >= args.warmup:
@@ -275,8 +321,10 @@ def reference_arm(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
             "config": config_dict(w, args, pairs, ndocs_total),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": c, "kind": "oracle",
-                             "sample": "each step: fp64 oracle fwd+bwd on a run of whole documents covering "
-                                       "about 6% of the workload's pairs, rotating through the row"},
+                             "sample": (f"each step: fp64 oracle fwd+bwd on {sub.name} (batch 0, the first KV "
+                                        "head and its query heads, the leading causal block)" if dense else
+                                        "each step: fp64 oracle fwd+bwd on a run of whole documents covering "
+                                        "about 6% of the workload's pairs, rotating through the row")},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "gpu_launches": 0}
     print(json.dumps(line))
@@ -311,11 +359,21 @@ def our_arm(args):
     flops = f_fwd + f_bwd
     Lq = w.q.shape[0]
     q, k, v, do = (t.to(dev) for t in (w.q, w.k, w.v, w.dout))
-    ids = torch.from_numpy(np.ascontiguousarray(w.doc_ids)).to(dev)
-    qids = ids[:, w.q_global_start:w.q_global_start + Lq].contiguous()
+    dense = w.kind == "dense"
+    if dense:
+        ids = qids = None
+    else:
+        ids = torch.from_numpy(np.ascontiguousarray(w.doc_ids)).to(dev)
+        qids = ids[:, w.q_global_start:w.q_global_start + Lq].contiguous()
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
     def step(qq, kk, vv, dd, ii, qi):
+        if dense:
+            out, lse = psf.attn_dense_fwd(qq, kk, vv, w.scale, w.causal, pack_gqa=args.pack_gqa,
+                                          softcap=args.softcap)
+            grads = psf.attn_dense_bwd(dd, qq, kk, vv, out, lse, w.scale, w.causal, softcap=args.softcap,
+                                       pack_gqa=args.pack_gqa)
+            return out, lse, grads
         out, lse, seg = psf.document_causal_attention(qq, kk, vv, qi, ii, w.q_global_start, w.scale, w.window,
                                                       pack_gqa=args.pack_gqa, softcap=args.softcap)
         grads = psf.document_causal_attention_backward(dd, qq, kk, vv, out, lse, seg, w.scale, w.window,
@@ -397,12 +455,13 @@ def our_arm(args):
     # another while step i computes (device inputs double-buffered). No L2
     # flush here: each step's inputs arrive fresh from the host.
     hq, hk, hv, hd = (t.pin_memory() for t in (w.q, w.k, w.v, w.dout))
-    hids = torch.from_numpy(np.ascontiguousarray(w.doc_ids)).pin_memory()
-    host_in = (hq, hk, hv, hd, hids)
+    host_in = (hq, hk, hv, hd)
+    if not dense:
+        host_in += (torch.from_numpy(np.ascontiguousarray(w.doc_ids)).pin_memory(),)
     comp_s = torch.cuda.current_stream()
     h2d_s, d2h_s = torch.cuda.Stream(), torch.cuda.Stream()
     nbuf = 2
-    dev_in = [tuple(torch.empty_like(t) for t in (q, k, v, do, ids)) for _ in range(nbuf)]
+    dev_in = [tuple(torch.empty_like(t) for t in (q, k, v, do) + (() if dense else (ids,))) for _ in range(nbuf)]
     in_ready = [torch.cuda.Event() for _ in range(nbuf)]
     in_free = [torch.cuda.Event() for _ in range(nbuf)]
     out_ready = [torch.cuda.Event() for _ in range(nbuf)]
@@ -420,8 +479,9 @@ def our_arm(args):
                 dst.copy_(src, non_blocking=True)
             in_ready[b].record(h2d_s)
         comp_s.wait_event(in_ready[b])
-        dq_, dk_, dv_, dd_, di_ = dev_in[b]
-        qi_ = di_[:, w.q_global_start:w.q_global_start + Lq].contiguous()
+        dq_, dk_, dv_, dd_ = dev_in[b][:4]
+        di_ = None if dense else dev_in[b][4]
+        qi_ = None if dense else di_[:, w.q_global_start:w.q_global_start + Lq].contiguous()
         out, lse, grads = step(dq_, dk_, dv_, dd_, di_, qi_)
         in_free[b].record(comp_s)
         out_ready[b].record(comp_s)
@@ -480,7 +540,7 @@ def our_arm(args):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": args.dtype, "data": "synthetic", "impl": "ours",
-        "config": dict(config_dict(w, args, pairs, len(w.extra["lengths"])),
+        "config": dict(config_dict(w, args, pairs, 0 if dense else len(w.extra["lengths"])),
                        parallelism=f"replicas{world}" if world > 1 else "single GPU"),
         "fwd_tflops": f_fwd / (fwd_ms * 1e-3) / 1e12 if fwd_ms > 0 else None,
         "bwd_tflops": f_bwd / (bwd_ms * 1e-3) / 1e12 if bwd_ms > 0 else None,
@@ -491,7 +551,9 @@ def our_arm(args):
         "e2e": {"value": whole_job_value(world, flops, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms,
                 "timing": "steps pipelined: uploads and downloads overlap neighbouring steps' compute"},
-        "gpu_launches": 6 * args.steps,
+        # per step: (builder,) forward preparation + attention, backward
+        # preparation + attention + convert
+        "gpu_launches": (5 if dense else 6) * args.steps,
         "clocks": clocks,
     }
     if world == 1 and not args.no_cpu:

@@ -92,3 +92,33 @@ def test_captured_traffic_is_reported_only_for_its_workload_and_sources():
         assert b.ncu_traffic(kernel, workload) == (nbytes if digest == b.kernel_source_hash(kernel) else None)
         assert b.ncu_traffic(kernel, "another_workload") is None
     assert b.ncu_traffic("attn_bwd_kernel", "cfg2_doc_causal_t8192_d128") is None
+
+
+def test_dense_workload_flops_and_reference_sample():
+    b = _bench()
+    from packed_sequence_flash_gb300 import inputs
+
+    assert b.dense_pairs(128, 128, True) == 128 * 129 // 2
+    assert b.dense_pairs(3, 5, True) == 3 + 4 + 5  # bottom-right: query i sees keys 0..i+2
+    assert b.dense_pairs(5, 3, True) == 0 + 0 + 1 + 2 + 3
+    assert b.dense_pairs(4, 6, False) == 24
+    w = inputs.config(1, 0)
+    pairs, f, bw = b.workload_flops(w)
+    assert pairs == 16512 and f == pairs * 2 * (64 + 64) and bw == pairs * (6 * 64 + 4 * 64)
+    sub = b.cpu_sample_dense(w, 64)
+    assert tuple(sub.q.shape) == (1, 2, 64, 64) and tuple(sub.k.shape) == (1, 1, 64, 64)
+    assert b.config_dict(w, type("A", (), {"seed": 0})(), pairs, 0)["visible_pairs_x_heads"] == 16512
+
+
+def test_reference_arm_times_the_oracle_on_a_dense_workload(monkeypatch, capsys):
+    b = _bench()
+    monkeypatch.setenv("RANK", "0")
+
+    class Args:
+        config, seed, warmup, steps, gpus, softcap = 1, 0, 0, 1, 1, None
+
+    assert b.reference_arm(Args()) == 0
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["value"] > 0
+    assert line["config"]["workload"] == "cfg1_dense_causal_n128_d64"
+    assert "[b0, kv head 0, 128 rows]" in line["cpu_baseline"]["sample"]
