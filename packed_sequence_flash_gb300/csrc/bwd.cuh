@@ -168,7 +168,9 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_kernel(const __grid_constant_
       tma_prefetch_desc(&p.tm_do);
       uint32_t nz = 0, gstep = 0;
       bool ok = true;
-      for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+      for (int wi = 0; wi * (int)gridDim.x < total && ok; ++wi) {
+        const int w = snake_item(wi);
+        if (w >= total) continue;
         const BwdItem t = bwd_decode(p, w);
         if (t.k1 == t.k0) continue;
         if (!wait_bar(&kv_empty, (nz & 1) ^ 1, ctl)) break;
@@ -208,7 +210,9 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_kernel(const __grid_constant_
       const uint32_t do_a = sbase + C::DO_OFF, pt_a = sbase + C::PT_OFF, ds_a = sbase + C::DS_OFF;
       uint32_t nz = 0, gstep = 0;
       bool ok = true;
-      for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+      for (int wi = 0; wi * (int)gridDim.x < total && ok; ++wi) {
+        const int w = snake_item(wi);
+        if (w >= total) continue;
         const BwdItem t = bwd_decode(p, w);
         if (t.k1 == t.k0) continue;
         if (!wait_bar(&kv_full, nz & 1, ctl)) break;
@@ -319,7 +323,9 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_kernel(const __grid_constant_
     };
     uint32_t nz = 0, gstep = 0;
     bool ok = true;
-    for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+    for (int wi = 0; wi * (int)gridDim.x < total && ok; ++wi) {
+      const int w = snake_item(wi);
+      if (w >= total) continue;
       const BwdItem t = bwd_decode(p, w);
       const int j = t.kt * kBN + r;  // segment-local key index
       const bool valid = j < t.n;
@@ -536,7 +542,9 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_kernel(const __grid_constant_
     uint8_t* stg = smem + C::STG_OFF + wq * 4096;
     uint32_t gstep = 0;
     bool ok = true;
-    for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+    for (int wi = 0; wi * (int)gridDim.x < total && ok; ++wi) {
+      const int w = snake_item(wi);
+      if (w >= total) continue;
       const BwdItem t = bwd_decode(p, w);
       if (t.k1 == t.k0) continue;
       {

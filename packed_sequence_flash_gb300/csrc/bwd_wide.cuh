@@ -112,7 +112,9 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_wide_kernel(const __grid_cons
         ++it;
         return true;
       };
-      for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+      for (int wi = 0; wi * (int)gridDim.x < total && ok; ++wi) {
+        const int w = snake_item(wi);
+        if (w >= total) continue;
         int part;
         const BwdItem t = decode(w, part);
         if (t.k1 == t.k0) continue;
@@ -156,7 +158,9 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_wide_kernel(const __grid_cons
         mma_commit(&ring_empty[it % NST]);
         ++it;
       };
-      for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+      for (int wi = 0; wi * (int)gridDim.x < total && ok; ++wi) {
+        const int w = snake_item(wi);
+        if (w >= total) continue;
         int part;
         const BwdItem t = decode(w, part);
         if (t.k1 == t.k0) continue;
@@ -260,7 +264,9 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_wide_kernel(const __grid_cons
     const float cap_k1 = CAP ? 2.f * sl2 / p.softcap : 0.f, cap_ic2 = CAP ? 1.f / cap_c2 : 0.f;
     uint32_t nz = 0, gstep = 0;
     bool ok = true;
-    for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+    for (int wi = 0; wi * (int)gridDim.x < total && ok; ++wi) {
+      const int w = snake_item(wi);
+      if (w >= total) continue;
       int part;
       const BwdItem t = decode(w, part);
       const int j = t.kt * kBN + r;
@@ -399,7 +405,9 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_wide_kernel(const __grid_cons
     uint8_t* stg = smem + C::PT_OFF + wq * 8192;
     uint32_t gstep = 0;
     bool ok = true;
-    for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+    for (int wi = 0; wi * (int)gridDim.x < total && ok; ++wi) {
+      const int w = snake_item(wi);
+      if (w >= total) continue;
       int part;
       const BwdItem t = decode(w, part);
       if (t.k1 == t.k0) continue;

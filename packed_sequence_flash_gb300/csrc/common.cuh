@@ -68,6 +68,14 @@ __device__ __forceinline__ float softcap_log2(float s, float k1, float c2) {
   return s == -CUDART_INF_F ? -CUDART_INF_F : y;
 }
 
+// Static work assignment over a heaviest-first list: in round i CTA b takes
+// item i * G + b when i is even and i * G + (G - 1 - b) when i is odd (G CTAs),
+// so each CTA's heavy and light items pair up and the CTAs' sums stay close.
+__device__ __forceinline__ int snake_item(int i) {
+  const int g = (int)gridDim.x, b = (int)blockIdx.x;
+  return i * g + ((i & 1) ? g - 1 - b : b);
+}
+
 // Compile-time flag for element passes that exist in a masked and an unmasked
 // form (mask arithmetic inside the common, unmasked loop costs throughput even
 // when it never fires).

@@ -157,7 +157,9 @@ __global__ void __launch_bounds__(256, 1) attn_fwd_kernel(const __grid_constant_
         ++kvit;
         return true;
       };
-      for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+      for (int wi = 0; wi * (int)gridDim.x < total && ok; ++wi) {
+        const int w = snake_item(wi);
+        if (w >= total) continue;
         FwdTile t = fwd_decode(p, w);
         if (t.nk == 0) continue;
         int qb = qcnt % NQB;
@@ -196,7 +198,9 @@ __global__ void __launch_bounds__(256, 1) attn_fwd_kernel(const __grid_constant_
       constexpr uint32_t idesc_pv = idesc_f32acc<T>(128, 64, 0, 1);
       uint32_t qcnt = 0, kvit = 0, scnt = 0, pcnt = 0, ntile = 0;
       bool ok = true;
-      for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+      for (int wi = 0; wi * (int)gridDim.x < total && ok; ++wi) {
+        const int w = snake_item(wi);
+        if (w >= total) continue;
         FwdTile t = fwd_decode(p, w);
         if (t.nk == 0) continue;
         int qb = qcnt % NQB;
@@ -275,7 +279,9 @@ __global__ void __launch_bounds__(256, 1) attn_fwd_kernel(const __grid_constant_
     const float sl2 = p.scale_log2;
     uint32_t scnt = 0, pvcnt = 0;
     bool ok = true;
-    for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+    for (int wi = 0; wi * (int)gridDim.x < total && ok; ++wi) {
+      const int w = snake_item(wi);
+      if (w >= total) continue;
       FwdTile t = fwd_decode(p, w);
       const int i = t.qt * kBM + row;  // segment-local query index
       const bool valid = i < t.m;
