@@ -49,8 +49,8 @@ L2_FLUSH_BYTES = 256 << 20
 # captured, bytes). Reported as null for other workloads and once the sources
 # change.
 NCU_TRAFFIC = {
-    ("attn_bwd_dual_kernel", "cfg2_doc_causal_t8192_d128"): ("1332a4fb1b5a35ab", 396467968),
-    ("attn_fwd_duo_kernel", "cfg2_doc_causal_t8192_d128"): ("040e8ca8f1df30e3", 53567744),
+    ("attn_bwd_dual_kernel", "cfg2_doc_causal_t8192_d128"): ("a26bda6aae0f3cb4", 405444608),
+    ("attn_fwd_duo_kernel", "cfg2_doc_causal_t8192_d128"): ("ba5c514a195b41fb", 53346304),
 }
 
 
