@@ -282,6 +282,19 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, void* out, float*
   const View vq = tensor_view(layout, Sq, Hq, Dqk), vk = tensor_view(layout, Sk, Hkv, Dqk);
   const View vv = tensor_view(layout, Sk, Hkv, Dv), vo = tensor_view(layout, Sq, Hq, Dv);
   const View vl = lse_view(layout, Sq, Hq);
+  if (k_rows == 0) {
+    // No keys at all: every query row sees none, so out = 0 and lse = -inf
+    // everywhere. The preparation kernel writes exactly that for the rows past
+    // the last segment; run it with no segments and launch no attention kernel
+    // (which would hold key-side tensor maps over no memory).
+    SegInfo none = g;
+    none.cu_q = none.cu_k = nullptr;
+    none.dev_meta = nullptr;
+    none.nseg = 0;
+    cudaError_t e0 = launch_fwd_prep(none, w.items, w.n_items, w.seg_prefix, w.item_cap, dev->status, out, vo.sb,
+                                     vo.ss, vo.sh, lse, vl.sb, vl.sh, Hq, Dv, st);
+    return e0 == cudaSuccess ? PSF_OK : cuda_fail(e0, "forward preparation launch");
+  }
   cudaError_t e = launch_fwd_prep(g, w.items, w.n_items, w.seg_prefix, w.item_cap, dev->status,
                                   out, vo.sb, vo.ss, vo.sh, lse, vl.sb, vl.sh, Hq, Dv, st);
   if (e != cudaSuccess) return cuda_fail(e, "forward preparation launch");
@@ -371,6 +384,20 @@ int attn_bwd_impl(const void* dout, const void* q, const void* k, const void* v,
   const View vq = tensor_view(layout, Sq, Hq, Dqk), vk = tensor_view(layout, Sk, Hkv, Dqk);
   const View vv = tensor_view(layout, Sk, Hkv, Dv), vo = tensor_view(layout, Sq, Hq, Dv);
   const View vl = lse_view(layout, Sq, Hq);
+  if (q_rows == 0) {
+    // No queries: every gradient is zero. The preparation kernel zeroes dK and
+    // dV rows past the last segment; run it with no segments and without the
+    // accumulators, and launch no attention kernel (which would hold
+    // query-side tensor maps over no memory).
+    SegInfo none = g;
+    none.cu_q = none.cu_k = nullptr;
+    none.dev_meta = nullptr;
+    none.nseg = 0;
+    cudaError_t e0 = launch_bwd_prep(none, Hq / Hkv, Hkv, 0, w.items, w.n_items, w.seg_prefix, w.item_cap,
+                                     dev->status, dout, out, vo.sb, vo.ss, vo.sh, w.delta, w.dq_acc, Hq, Dqk, Dv,
+                                     nullptr, nullptr, dk, dv, vk.sb, vk.ss, vk.sh, vv.sb, vv.ss, vv.sh, f16, st);
+    return e0 == cudaSuccess ? PSF_OK : cuda_fail(e0, "backward preparation launch");
+  }
   cudaError_t e = launch_bwd_prep(
       g, Hq / Hkv, Hkv, accumulate ? kSplitPerSm * dev->sms : 0, w.items, w.n_items, w.seg_prefix, w.item_cap,
       dev->status, dout, out, vo.sb, vo.ss,

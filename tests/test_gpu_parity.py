@@ -212,6 +212,38 @@ def test_varlen_many_small_and_empty_segments():
     _varlen_case(11, 128, 128, 2, 1, True, None, nseg=40, max_len=40)
 
 
+@pytest.mark.parametrize("D", [64, 128, 512])
+def test_degenerate_calls_no_rows_no_segments_no_keys(D):
+    # Calls with nothing to attend: no query rows, no segments, no keys, and a
+    # backward with no queries. Every query row comes out 0 with lse = -inf
+    # and every gradient is 0 (rows that see no key carry no probability).
+    dev, dt, H, Hkv = "cuda", torch.bfloat16, 4, 2
+    g = torch.Generator().manual_seed(5)
+    rnd = lambda *s: torch.randn(*s, generator=g).to(dt).to(dev)
+    z = lambda *s: torch.tensor(s, dtype=torch.int32, device=dev)
+    scale = D ** -0.5
+    # no query rows (keys present)
+    q0, k, v = rnd(0, H, D), rnd(10, Hkv, D), rnd(10, Hkv, D)
+    out, lse = psf.attn_varlen_fwd(q0, k, v, z(0, 0), z(0, 10), 0, 10, scale, True)
+    assert out.shape == (0, H, D) and lse.shape == (H, 0)
+    dq, dk, dv = psf.attn_varlen_bwd(q0.clone(), q0, k, v, out, lse, z(0, 0), z(0, 10), 0, 10, scale, True)
+    assert dq.shape == (0, H, D) and not dk.any() and not dv.any()
+    # no segments at all: every row is uncovered
+    q = rnd(50, H, D)
+    out, lse = psf.attn_varlen_fwd(q, k, v, z(0), z(0), 0, 0, scale, True)
+    assert not out.any() and bool(torch.isneginf(lse).all())
+    dq, dk, dv = psf.attn_varlen_bwd(rnd(50, H, D), q, k, v, out, lse, z(0), z(0), 0, 0, scale, True)
+    assert not dq.any() and not dk.any() and not dv.any()
+    # no keys: segments with queries and zero keys
+    k0, v0 = rnd(0, Hkv, D), rnd(0, Hkv, D)
+    out, lse = psf.attn_varlen_fwd(q, k0, v0, z(0, 20, 50), z(0, 0, 0), 30, 0, scale, False)
+    assert not out.any() and bool(torch.isneginf(lse).all())
+    dq, dk, dv = psf.attn_varlen_bwd(rnd(50, H, D), q, k0, v0, out, lse, z(0, 20, 50), z(0, 0, 0), 30, 0, scale,
+                                     False)
+    assert not dq.any() and dk.shape == (0, Hkv, D) and dv.shape == (0, Hkv, D)
+    assert psf.device_status() == 0
+
+
 # ---------------------------------------------------------------- document-causal composition
 
 @pytest.mark.parametrize("seed,skip_pad", [(0, True), (1, True), (1, False)])
