@@ -582,7 +582,9 @@ def main():
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", type=int, default=2, help="workload number (2 = the headline workload)")
+    ap.add_argument("--config", type=int, default=2,
+                    help="workload number: 2 = the headline workload (8192 tokens, D 128); 3 = dense causal D 512; "
+                         "4 = 192/128 shard; 5 = 65536 tokens with a window; 6 = short documents")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--dtype", choices=["bf16", "fp16"], default="bf16",
                     help="16-bit type of q, k, v, dO and the outputs (the headline is bf16)")
