@@ -11,6 +11,14 @@
  *  - Pointers are DEVICE pointers owned by the caller; the library allocates
  *    nothing. Outputs and workspaces are caller-allocated. Tensor base pointers
  *    must be 16-byte aligned (a TMA requirement).
+ *  - Strides: the attention calls take `strides`, NULL for the layout's
+ *    contiguous strides, else an int64 array of element strides, three per
+ *    tensor in the order (batch, head, row), tensors in the order each call
+ *    lists. The head dim is always contiguous. A stride of a dimension of
+ *    extent 1 (the batch of a packed THD tensor, a single head or row) is
+ *    ignored; every other one must be a positive multiple of 8 elements
+ *    (16 bytes) below 2^38, and an output's strides must not make it overlap
+ *    itself (PSF_EINVAL otherwise). lse stays contiguous.
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
  *    Every call is asynchronous on that stream.
  *  - Return value: PSF_OK (0) after a successful launch, or a negative code.
@@ -101,6 +109,9 @@ int psf_check_pipeline_wait(int arrive, void* stream);
  * kernel, kind 1: backward main kernel). psf_kernel_timing(0) stops recording.
  * psf_kernel_times_ms() waits for the recorded events of `kind` and returns
  * their summed device time in *total_ms and their number in *launches.
+ * Calls made while a stream capture is active record the pair as event-record
+ * nodes of the captured graph: each replay of the graph re-records them, and
+ * psf_kernel_times_ms() after a replay returns that replay's kernel times.
  */
 int psf_kernel_timing(int enable);
 int psf_kernel_times_ms(int kind, double* total_ms, int* launches);
@@ -144,13 +155,16 @@ size_t psf_attn_bwd_workspace_size(int64_t total_q_rows, int64_t total_k_rows, i
  *                           [ffpa_attention page, `_ffpa_varlen_fwd`: the
  *                            pack-GQA sentinel the pages fix off]
  *  Any other bit is PSF_EINVAL.
+ *  strides: NULL, or 12 element strides (batch, head, row) of q, k, v, out;
+ *  for THD the row stride steps tokens and the batch stride is ignored.
  *  workspace: psf_attn_fwd_workspace_size(Tq, nseg) bytes (enough for either flag).
  */
 #define PSF_FWD_PACK_GQA 1
 int psf_attn_varlen_fwd(const void* q, const void* k, const void* v, void* out, float* lse, const int32_t* cu_q,
                         const int32_t* cu_k, const int32_t* dev_meta, int nseg, int max_q, int max_k, int layout,
-                        int dtype, int B, int Sq, int Sk, int Hq, int Hkv, int Dqk, int Dv, float scale, int causal,
-                        int32_t window_left, float softcap, int flags, void* workspace, size_t ws_bytes, void* stream);
+                        int dtype, int B, int Sq, int Sk, int Hq, int Hkv, int Dqk, int Dv, const int64_t* strides,
+                        float scale, int causal, int32_t window_left, float softcap, int flags, void* workspace,
+                        size_t ws_bytes, void* stream);
 
 /*
  * Varlen forward that allocates nothing and takes no workspace.
@@ -160,8 +174,8 @@ int psf_attn_varlen_fwd(const void* q, const void* k, const void* v, void* out, 
  *  device memory up front and hand out nothing afterwards, plugin hosts that
  *  own every allocation, or code that must not touch the allocator while a
  *  step runs. This entry point behaves like psf_attn_varlen_fwd (same
- *  arguments minus softcap, flags, workspace and ws_bytes: no softcap, one
- *  query head per tile, same results) but keeps its tile
+ *  arguments minus strides, softcap, flags, workspace and ws_bytes: contiguous
+ *  tensors, no softcap, one query head per tile, same results) but keeps its tile
  *  schedule in a fixed array in the library's device memory (852,736 bytes,
  *  held on every GPU that loads the library until the process exits).
  *  Limits: B * Sq <= PSF_NOALLOC_MAX_Q_ROWS and nseg <= PSF_NOALLOC_MAX_SEGMENTS;
@@ -195,6 +209,8 @@ int psf_attn_varlen_fwd_noalloc(const void* q, const void* k, const void* v, voi
  *  of its KV head, 128 / G rows each (head dims up to 128 with G = 2 or 4 and
  *  no softcap; other calls take one head per step). Same results; for short segments,
  *  where one head's rows fill little of a 128-row step. Other bits: PSF_EINVAL.
+ *  strides: NULL, or 24 element strides (batch, head, row) of q, k, v, out,
+ *  dout, dq, dk, dv.
  *  workspace: psf_attn_bwd_workspace_size(Tq, Tk, nseg, Hq, Hkv, Dqk, Dv) bytes
  *  (holds the fp32 dQ, dK and dV accumulators, Delta = rowsum(dO * out) and the
  *  tile schedule).
@@ -202,8 +218,9 @@ int psf_attn_varlen_fwd_noalloc(const void* q, const void* k, const void* v, voi
 int psf_attn_varlen_bwd(const void* dout, const void* q, const void* k, const void* v, const void* out,
                         const float* lse, void* dq, void* dk, void* dv, const int32_t* cu_q, const int32_t* cu_k,
                         const int32_t* dev_meta, int nseg, int max_q, int max_k, int layout, int dtype, int B, int Sq,
-                        int Sk, int Hq, int Hkv, int Dqk, int Dv, float scale, int causal, int32_t window_left,
-                        float softcap, int flags, void* workspace, size_t ws_bytes, void* stream);
+                        int Sk, int Hq, int Hkv, int Dqk, int Dv, const int64_t* strides, float scale, int causal,
+                        int32_t window_left, float softcap, int flags, void* workspace, size_t ws_bytes,
+                        void* stream);
 #define PSF_BWD_PACK_GQA 1
 
 /*
@@ -214,23 +231,30 @@ int psf_attn_varlen_bwd(const void* dout, const void* q, const void* k, const vo
  *                            fa4 page, `causal_fa4_attention`]
  *  q [B,Hq,Nq,Dqk], k [B,Hkv,Nk,Dqk], v [B,Hkv,Nk,Dv], out [B,Hq,Nq,Dv],
  *  lse [B,Hq,Nq]. Causal is bottom-right aligned when Nq != Nk.
+ *  strides: NULL (contiguous [B,H,N,D]) or 12 element strides (batch, head,
+ *  row) of q, k, v, out: for example a [B,N,H,D] tensor seen as [B,H,N,D]
+ *  (strides N*H*D, D, H*D) is read in place.
  *  softcap, flags: as for psf_attn_varlen_fwd.
  *  workspace: psf_attn_fwd_workspace_size(B * Nq, B) bytes.
  */
 int psf_attn_dense_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq, int Hkv,
-                       int Nq, int Nk, int Dqk, int Dv, int dtype, float scale, int causal, int32_t window_left,
-                       float softcap, int flags, void* workspace, size_t ws_bytes, void* stream);
+                       int Nq, int Nk, int Dqk, int Dv, const int64_t* strides, int dtype, float scale, int causal,
+                       int32_t window_left, float softcap, int flags, void* workspace, size_t ws_bytes,
+                       void* stream);
 
 /*
  * Dense backward.           [ffpa_attention page, `_ffpa_dense_bwd`: returns
  *                            (dq, dk, dv) in [B,H,N,D], dK/dV reduced to Hkv]
+ *  strides: NULL or 24 element strides (batch, head, row) of q, k, v, out,
+ *  dout, dq, dk, dv.
  *  softcap, flags: as for psf_attn_varlen_bwd.
  *  workspace: psf_attn_bwd_workspace_size(B * Nq, B * Nk, B, Hq, Hkv, Dqk, Dv) bytes.
  */
 int psf_attn_dense_bwd(const void* dout, const void* q, const void* k, const void* v, const void* out,
                        const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Nq, int Nk,
-                       int Dqk, int Dv, int dtype, float scale, int causal, int32_t window_left, float softcap,
-                       int flags, void* workspace, size_t ws_bytes, void* stream);
+                       int Dqk, int Dv, const int64_t* strides, int dtype, float scale, int causal,
+                       int32_t window_left, float softcap, int flags, void* workspace, size_t ws_bytes,
+                       void* stream);
 
 /*
  * Doc ids -> varlen segments, on the GPU.

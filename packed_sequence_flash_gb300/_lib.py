@@ -32,12 +32,13 @@ SIGNATURES = {
     "psf_kernel_times_ms": (I, [I, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int)]),
     "psf_attn_fwd_workspace_size": (SZ, [I64, I]),
     "psf_attn_bwd_workspace_size": (SZ, [I64, I64, I, I, I, I, I]),
-    "psf_attn_varlen_fwd": (I, [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, I, I, I, F, I, I32, F, I, P, SZ, P]),
+    "psf_attn_varlen_fwd": (I, [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, I, I, I, P, F, I, I32, F, I, P, SZ,
+                                P]),
     "psf_attn_varlen_fwd_noalloc": (I, [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, I, I, I, F, I, I32, P]),
-    "psf_attn_varlen_bwd": (I, [P, P, P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, I, I, I, F, I, I32,
-                                F, I, P, SZ, P]),
-    "psf_attn_dense_fwd": (I, [P, P, P, P, P, I, I, I, I, I, I, I, I, F, I, I32, F, I, P, SZ, P]),
-    "psf_attn_dense_bwd": (I, [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, F, I, I32, F, I, P, SZ, P]),
+    "psf_attn_varlen_bwd": (I, [P, P, P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, I, I, I, P, F, I,
+                                I32, F, I, P, SZ, P]),
+    "psf_attn_dense_fwd": (I, [P, P, P, P, P, I, I, I, I, I, I, I, P, I, F, I, I32, F, I, P, SZ, P]),
+    "psf_attn_dense_bwd": (I, [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, I, F, I, I32, F, I, P, SZ, P]),
     "psf_build_doc_segments": (I, [P, I, I, I, I, P, P, I, P, P, I, P]),
     "psf_chunk_dense_flags": (I, [P, I, I, I, I, I, I, P, P]),
     "psf_pad_fixup": (I, [P, P, P, I, I, I, I, I, P]),

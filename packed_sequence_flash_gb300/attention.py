@@ -15,6 +15,8 @@ Layouts follow the pages:
 """
 from __future__ import annotations
 
+import ctypes
+
 import torch
 
 from . import _lib
@@ -41,14 +43,21 @@ def _window(window) -> int:
 _DTYPES = {torch.bfloat16: PSF_DTYPE_BF16, torch.float16: PSF_DTYPE_F16}
 
 
-def _dtype_code(tensors):
-    """PSF_DTYPE_* of a call's 16-bit tensors ((tensor, name) pairs), which must share one type."""
+def _dtype_code(tensors, strided=False):
+    """PSF_DTYPE_* of a call's 16-bit tensors ((tensor, name) pairs), which must share one type.
+    strided: the call takes strides (else every tensor must be contiguous)."""
     t0, n0 = tensors[0]
     if t0.dtype not in _DTYPES:
         raise ValueError(f"{n0} must be bfloat16 or float16, got {t0.dtype}")
     for t, n in tensors:
-        _need(t, n, t0.dtype)
+        (_need_view if strided else _need)(t, n, t0.dtype)
     return _DTYPES[t0.dtype]
+
+
+def _grads_like(q, k, v):
+    """Gradient buffers with their inputs' strides where those are non-overlapping
+    and dense, else in a dense layout (torch.empty_like's rule)."""
+    return tuple(torch.empty_like(t) for t in (q, k, v))
 
 
 def _need(t, name, dtype=None):
@@ -63,6 +72,34 @@ def _need(t, name, dtype=None):
 def _i32(t, name):
     _need(t, name, torch.int32)
     return t
+
+
+def _need_view(t, name, dtype=None):
+    """A strided CUDA tensor whose head dim is contiguous and whose data starts on a 16-byte boundary
+    (the kernels read every tensor through TMA views built from its strides)."""
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.shape[-1] > 1 and t.stride(-1) != 1:
+        raise ValueError(f"{name}: the last (head) dim must be contiguous")
+    if t.data_ptr() % 16:
+        raise ValueError(f"{name}: data must start on a 16-byte boundary")
+
+
+def _strides(tensors, layout):
+    """The C ABI's strides argument: NULL when every tensor is contiguous, else
+    int64 (batch, head, row) element strides per tensor ([T, H, D] tensors have
+    no batch dim: its stride is ignored)."""
+    if all(t.is_contiguous() for t in tensors):
+        return None
+    vals = []
+    for t in tensors:
+        if layout == PSF_LAYOUT_THD:
+            vals += [0, t.stride(1), t.stride(0)]
+        else:
+            vals += [t.stride(0), t.stride(1), t.stride(2)]
+    return (ctypes.c_int64 * len(vals))(*vals)
 
 
 def device_status(clear: bool = True) -> int:
@@ -123,20 +160,23 @@ def attn_varlen_fwd(q, k, v, cu_q, cu_k, max_q, max_k, scale, causal, window=Non
     q, k, v: bf16 or fp16 (one type); out has their type, lse is fp32.
     pack_gqa: the query heads of a KV head share one tile (same results; for
     short segments). softcap > 0 caps each logit as softcap * tanh(logit / softcap)."""
-    dt = _dtype_code([(q, "q"), (k, "k"), (v, "v")])
+    dt = _dtype_code([(q, "q"), (k, "k"), (v, "v")], strided=True)
     _i32(cu_q, "cu_q")
     _i32(cu_k, "cu_k")
     lay, B, Sq, Sk, Hq, Hkv, Dqk, Dv = _varlen_dims(q, k, v, layout)
     nseg = cu_q.numel() - 1
     if out is None:
         out = torch.empty(*q.shape[:-1], Dv, dtype=q.dtype, device=q.device)
+    else:
+        _need_view(out, "out", q.dtype)
     if lse is None:
         lse = torch.empty((Hq, Sq) if lay == PSF_LAYOUT_THD else (B, Hq, Sq), dtype=torch.float32, device=q.device)
     if workspace is None:
         workspace = _workspace(fwd_workspace_size(B * Sq, nseg), q.device)
     rc = _lib.load().psf_attn_varlen_fwd(
         _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(cu_q), _ptr(cu_k), _ptr(dev_meta), nseg,
-        int(max_q), int(max_k), lay, dt, B, Sq, Sk, Hq, Hkv, Dqk, Dv, float(scale), int(bool(causal)),
+        int(max_q), int(max_k), lay, dt, B, Sq, Sk, Hq, Hkv, Dqk, Dv, _strides((q, k, v, out), lay), float(scale),
+        int(bool(causal)),
         _window(window), _cap(softcap), PSF_FWD_PACK_GQA if pack_gqa else 0, _ptr(workspace), workspace.numel(),
         _stream())
     check(rc)
@@ -147,21 +187,19 @@ def attn_varlen_bwd(dout, q, k, v, out, lse, cu_q, cu_k, max_q, max_k, scale, ca
                     dev_meta=None, layout="thd", workspace=None, softcap=None, pack_gqa=False):
     """Packed varlen backward from caller-supplied out/lse -> (dq, dk, dv) in the inputs' type.
     pack_gqa: each step takes a KV head's query heads together (same results)."""
-    dt = _dtype_code([(dout, "dout"), (q, "q"), (k, "k"), (v, "v"), (out, "out")])
+    dt = _dtype_code([(dout, "dout"), (q, "q"), (k, "k"), (v, "v"), (out, "out")], strided=True)
     _need(lse, "lse", torch.float32)
     _i32(cu_q, "cu_q")
     _i32(cu_k, "cu_k")
     lay, B, Sq, Sk, Hq, Hkv, Dqk, Dv = _varlen_dims(q, k, v, layout)
     nseg = cu_q.numel() - 1
-    dq = torch.empty_like(q)
-    dk = torch.empty_like(k)
-    dv = torch.empty_like(v)
+    dq, dk, dv = _grads_like(q, k, v)
     if workspace is None:
         workspace = _workspace(bwd_workspace_size(B * Sq, B * Sk, nseg, Hq, Hkv, Dqk, Dv), q.device)
     rc = _lib.load().psf_attn_varlen_bwd(
         _ptr(dout), _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(cu_q),
-        _ptr(cu_k), _ptr(dev_meta), nseg, int(max_q), int(max_k), lay, dt, B, Sq, Sk, Hq, Hkv, Dqk, Dv, float(scale),
-        int(bool(causal)), _window(window), _cap(softcap), PSF_BWD_PACK_GQA if pack_gqa else 0, _ptr(workspace),
+        _ptr(cu_k), _ptr(dev_meta), nseg, int(max_q), int(max_k), lay, dt, B, Sq, Sk, Hq, Hkv, Dqk, Dv,
+        _strides((q, k, v, out, dout, dq, dk, dv), lay), float(scale), int(bool(causal)), _window(window), _cap(softcap), PSF_BWD_PACK_GQA if pack_gqa else 0, _ptr(workspace),
         workspace.numel(), _stream())
     check(rc)
     return dq, dk, dv
@@ -171,8 +209,10 @@ def attn_varlen_bwd(dout, q, k, v, out, lse, cu_q, cu_k, max_q, max_k, scale, ca
 # dense [B, H, N, D]
 
 def attn_dense_fwd(q, k, v, scale, causal, window=None, workspace=None, pack_gqa=False, softcap=None):
-    """Dense forward -> (out [B,Hq,Nq,Dv] in the inputs' type, lse [B,Hq,Nq] fp32)."""
-    dt = _dtype_code([(q, "q"), (k, "k"), (v, "v")])
+    """Dense forward -> (out [B,Hq,Nq,Dv] in the inputs' type, lse [B,Hq,Nq] fp32).
+    q, k, v may be strided views (for example ``x.transpose(1, 2)`` of a [B, N, H, D]
+    tensor) whose head dim is contiguous; they are read in place."""
+    dt = _dtype_code([(q, "q"), (k, "k"), (v, "v")], strided=True)
     B, Hq, Nq, Dqk = q.shape
     Hkv, Nk = k.shape[1], k.shape[2]
     Dv = v.shape[3]
@@ -181,7 +221,7 @@ def attn_dense_fwd(q, k, v, scale, causal, window=None, workspace=None, pack_gqa
     if workspace is None:
         workspace = _workspace(fwd_workspace_size(B * Nq, B), q.device)
     rc = _lib.load().psf_attn_dense_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, Nq, Nk, Dqk,
-                                        Dv, dt, float(scale), int(bool(causal)), _window(window), _cap(softcap),
+                                        Dv, _strides((q, k, v, out), PSF_LAYOUT_BHSD), dt, float(scale), int(bool(causal)), _window(window), _cap(softcap),
                                         PSF_FWD_PACK_GQA if pack_gqa else 0, _ptr(workspace), workspace.numel(),
                                         _stream())
     check(rc)
@@ -190,17 +230,19 @@ def attn_dense_fwd(q, k, v, scale, causal, window=None, workspace=None, pack_gqa
 
 def attn_dense_bwd(dout, q, k, v, out, lse, scale, causal, window=None, workspace=None, softcap=None,
                    pack_gqa=False):
-    """Dense backward -> (dq, dk, dv) in [B,H,N,D], dk/dv at Hkv heads."""
-    dt = _dtype_code([(dout, "dout"), (q, "q"), (k, "k"), (v, "v"), (out, "out")])
+    """Dense backward -> (dq, dk, dv) in [B,H,N,D], dk/dv at Hkv heads; each
+    gradient has its input's strides (strided inputs are read in place)."""
+    dt = _dtype_code([(dout, "dout"), (q, "q"), (k, "k"), (v, "v"), (out, "out")], strided=True)
     _need(lse, "lse", torch.float32)
     B, Hq, Nq, Dqk = q.shape
     Hkv, Nk = k.shape[1], k.shape[2]
     Dv = v.shape[3]
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    dq, dk, dv = _grads_like(q, k, v)
     if workspace is None:
         workspace = _workspace(bwd_workspace_size(B * Nq, B * Nk, B, Hq, Hkv, Dqk, Dv), q.device)
     rc = _lib.load().psf_attn_dense_bwd(_ptr(dout), _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dq),
-                                        _ptr(dk), _ptr(dv), B, Hq, Hkv, Nq, Nk, Dqk, Dv, dt, float(scale),
+                                        _ptr(dk), _ptr(dv), B, Hq, Hkv, Nq, Nk, Dqk, Dv,
+                                        _strides((q, k, v, out, dout, dq, dk, dv), PSF_LAYOUT_BHSD), dt, float(scale),
                                         int(bool(causal)), _window(window), _cap(softcap),
                                         PSF_BWD_PACK_GQA if pack_gqa else 0, _ptr(workspace), workspace.numel(),
                                         _stream())

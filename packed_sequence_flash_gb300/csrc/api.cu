@@ -91,6 +91,17 @@ std::mutex g_timing_mu;
 bool g_timing_on = false;
 std::vector<TimedLaunch> g_timed;
 
+// Inside a stream capture the record becomes an event-record node of the
+// graph (external flag), so every replay of the graph re-records the pair and
+// the kernel's time can be read after each replay.
+void record_timing_event(cudaEvent_t ev, cudaStream_t st) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusActive)
+    cudaEventRecordWithFlags(ev, st, cudaEventRecordExternal);
+  else
+    cudaEventRecord(ev, st);
+}
+
 bool timing_begin(int kind, cudaStream_t st, TimedLaunch* t) {
   std::lock_guard<std::mutex> lk(g_timing_mu);
   if (!g_timing_on) return false;
@@ -100,11 +111,11 @@ bool timing_begin(int kind, cudaStream_t st, TimedLaunch* t) {
     cudaEventDestroy(t->start);
     return false;
   }
-  cudaEventRecord(t->start, st);
+  record_timing_event(t->start, st);
   return true;
 }
 void timing_end(TimedLaunch* t, cudaStream_t st) {
-  cudaEventRecord(t->stop, st);
+  record_timing_event(t->stop, st);
   std::lock_guard<std::mutex> lk(g_timing_mu);
   g_timed.push_back(*t);
 }
@@ -116,7 +127,7 @@ void timing_clear_locked() {
   g_timed.clear();
 }
 
-size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+constexpr size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
@@ -139,15 +150,68 @@ View lse_view(int layout, int S, int H) {
   return View{(int64_t)H * S, 1, (int64_t)S};
 }
 
+// Tensor idx of a call: its element strides from the caller's (batch, head,
+// row) triple strides[3 idx .. 3 idx + 2], or the layout's contiguous strides
+// when strides is NULL. A dimension of extent 1 is never stepped over and keeps
+// its packed stride. Other strides must be positive multiples of 8 elements
+// (16 bytes: the TMA global-stride rule, and the kernels' 16-byte vector
+// accesses) below 2^38; an output's view must not overlap itself.
+int strided_view(const int64_t* strides, int idx, const char* name, int layout, int B, int S, int H, int D,
+                 bool output, View* v) {
+  *v = tensor_view(layout, S, H, D);
+  if (!strides) return PSF_OK;
+  const int64_t* t = strides + 3 * idx;
+  const int64_t ext[3] = {layout == PSF_LAYOUT_THD ? 1 : B, H, S};
+  int64_t st[3] = {v->sb, v->sh, v->ss};
+  static const char* dim_name[3] = {"batch", "head", "row"};
+  for (int i = 0; i < 3; ++i) {
+    if (ext[i] <= 1) continue;
+    if (t[i] <= 0 || t[i] % 8 != 0 || t[i] >= ((int64_t)1 << 38))
+      return fail(PSF_EINVAL, "%s: %s stride %lld must be a positive multiple of 8 elements below 2^38", name,
+                  dim_name[i], (long long)t[i]);
+    st[i] = t[i];
+  }
+  if (output) {
+    // Dimensions by increasing stride: each must step past everything the
+    // smaller ones (and the contiguous head dim) cover.
+    int ord[3] = {0, 1, 2};
+    for (int a = 0; a < 3; ++a)
+      for (int b = a + 1; b < 3; ++b)
+        if (st[ord[b]] < st[ord[a]]) {
+          const int x = ord[a];
+          ord[a] = ord[b];
+          ord[b] = x;
+        }
+    int64_t span = D;
+    for (int i = 0; i < 3; ++i) {
+      const int d = ord[i];
+      if (ext[d] <= 1) continue;
+      if (st[d] < span) return fail(PSF_EINVAL, "%s: the strided view overlaps itself (an output must not)", name);
+      span += st[d] * (ext[d] - 1);
+    }
+  }
+  v->sb = st[0];
+  v->sh = st[1];
+  v->ss = st[2];
+  return PSF_OK;
+}
+
 struct FwdWorkspace {
   int* n_items;
   int* seg_prefix;
   int2* items;
   int item_cap;
 };
+// Bytes of the forward workspace: the 256-byte header (item count, work
+// counter), the per-segment tile prefix and the (segment, tile) item list;
 // qrows: query rows per tile (kBM, or fewer when query heads share a tile).
+constexpr int64_t fwd_item_cap(int64_t rows, int nseg, int qrows) { return (rows + qrows - 1) / qrows + nseg + 1; }
+constexpr size_t fwd_ws_bytes(int64_t rows, int nseg, int qrows) {
+  return 256 + align256(sizeof(int) * (size_t)(nseg + 2)) +
+         align256(sizeof(int2) * (size_t)fwd_item_cap(rows, nseg, qrows));
+}
 size_t fwd_ws_layout(int64_t rows, int nseg, FwdWorkspace* w, void* base, int qrows = kBM) {
-  const int64_t cap = (rows + qrows - 1) / qrows + nseg + 1;
+  const int64_t cap = fwd_item_cap(rows, nseg, qrows);
   size_t off = 256;
   size_t prefix_off = off;
   off += align256(sizeof(int) * (size_t)(nseg + 2));
@@ -249,9 +313,15 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, void* out, float*
                   const int32_t* cu_k, const int32_t* dev_meta, int nseg, int max_q, int max_k, int layout, int dtype,
                   int B,
                   int Sq, int Sk, int Hq, int Hkv, int Dqk, int Dv, float scale, int causal, int32_t window, void* ws,
-                  size_t ws_bytes, void* stream, int flags = 0, float softcap = 0.f) {
+                  size_t ws_bytes, void* stream, int flags = 0, float softcap = 0.f, const int64_t* strides = nullptr) {
   int rc = check_common(layout, B, Sq, Sk, Hq, Hkv, Dqk, Dv, scale, window, nseg);
   if (rc) return rc;
+  View vq, vk, vv, vo;
+  if ((rc = strided_view(strides, 0, "q", layout, B, Sq, Hq, Dqk, false, &vq)) ||
+      (rc = strided_view(strides, 1, "k", layout, B, Sk, Hkv, Dqk, false, &vk)) ||
+      (rc = strided_view(strides, 2, "v", layout, B, Sk, Hkv, Dv, false, &vv)) ||
+      (rc = strided_view(strides, 3, "out", layout, B, Sq, Hq, Dv, true, &vo)))
+    return rc;
   if ((rc = check_softcap(softcap))) return rc;
   if ((rc = check_dtype(dtype))) return rc;
   if (flags & ~PSF_FWD_PACK_GQA) return fail(PSF_EINVAL, "unknown forward flags 0x%x", flags);
@@ -279,8 +349,6 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, void* out, float*
   FwdWorkspace w;
   fwd_ws_layout(q_rows, nseg, &w, ws, qrows);
   SegInfo g{cu_q, cu_k, dev_meta, nseg, max_q, max_k, B, Sq, Sk, causal ? 1 : 0, window > 0 ? (int)window : 0, qrows};
-  const View vq = tensor_view(layout, Sq, Hq, Dqk), vk = tensor_view(layout, Sk, Hkv, Dqk);
-  const View vv = tensor_view(layout, Sk, Hkv, Dv), vo = tensor_view(layout, Sq, Hq, Dv);
   const View vl = lse_view(layout, Sq, Hq);
   if (k_rows == 0) {
     // No keys at all: every query row sees none, so out = 0 and lse = -inf
@@ -342,9 +410,20 @@ int attn_bwd_impl(const void* dout, const void* q, const void* k, const void* v,
                   void* dq, void* dk, void* dv, const int32_t* cu_q, const int32_t* cu_k, const int32_t* dev_meta,
                   int nseg, int max_q, int max_k, int layout, int dtype, int B, int Sq, int Sk, int Hq, int Hkv,
                   int Dqk, int Dv, float scale, int causal, int32_t window, void* ws, size_t ws_bytes, void* stream,
-                  float softcap = 0.f, int flags = 0) {
+                  float softcap = 0.f, int flags = 0, const int64_t* strides = nullptr) {
   int rc = check_common(layout, B, Sq, Sk, Hq, Hkv, Dqk, Dv, scale, window, nseg);
   if (rc) return rc;
+  // Tensor order of the strides array: q, k, v, out, dout, dq, dk, dv.
+  View vq, vk, vv, vo, vdo, vdq, vdk, vdv;
+  if ((rc = strided_view(strides, 0, "q", layout, B, Sq, Hq, Dqk, false, &vq)) ||
+      (rc = strided_view(strides, 1, "k", layout, B, Sk, Hkv, Dqk, false, &vk)) ||
+      (rc = strided_view(strides, 2, "v", layout, B, Sk, Hkv, Dv, false, &vv)) ||
+      (rc = strided_view(strides, 3, "out", layout, B, Sq, Hq, Dv, false, &vo)) ||
+      (rc = strided_view(strides, 4, "dout", layout, B, Sq, Hq, Dv, false, &vdo)) ||
+      (rc = strided_view(strides, 5, "dq", layout, B, Sq, Hq, Dqk, true, &vdq)) ||
+      (rc = strided_view(strides, 6, "dk", layout, B, Sk, Hkv, Dqk, true, &vdk)) ||
+      (rc = strided_view(strides, 7, "dv", layout, B, Sk, Hkv, Dv, true, &vdv)))
+    return rc;
   if ((rc = check_softcap(softcap))) return rc;
   if (flags & ~PSF_BWD_PACK_GQA) return fail(PSF_EINVAL, "unknown backward flags 0x%x", flags);
   if ((rc = check_dtype(dtype))) return rc;
@@ -381,8 +460,6 @@ int attn_bwd_impl(const void* dout, const void* q, const void* k, const void* v,
   BwdWorkspace w;
   bwd_ws_layout(q_rows, k_rows, nseg, Hq, Hkv, Dqk, Dv, dev->sms, &w, ws);
   SegInfo g{cu_q, cu_k, dev_meta, nseg, max_q, max_k, B, Sq, Sk, causal ? 1 : 0, window > 0 ? (int)window : 0, qrows};
-  const View vq = tensor_view(layout, Sq, Hq, Dqk), vk = tensor_view(layout, Sk, Hkv, Dqk);
-  const View vv = tensor_view(layout, Sk, Hkv, Dv), vo = tensor_view(layout, Sq, Hq, Dv);
   const View vl = lse_view(layout, Sq, Hq);
   if (q_rows == 0) {
     // No queries: every gradient is zero. The preparation kernel zeroes dK and
@@ -394,15 +471,16 @@ int attn_bwd_impl(const void* dout, const void* q, const void* k, const void* v,
     none.dev_meta = nullptr;
     none.nseg = 0;
     cudaError_t e0 = launch_bwd_prep(none, Hq / Hkv, Hkv, 0, w.items, w.n_items, w.seg_prefix, w.item_cap,
-                                     dev->status, dout, out, vo.sb, vo.ss, vo.sh, w.delta, w.dq_acc, Hq, Dqk, Dv,
-                                     nullptr, nullptr, dk, dv, vk.sb, vk.ss, vk.sh, vv.sb, vv.ss, vv.sh, f16, st);
+                                     dev->status, dout, vdo.sb, vdo.ss, vdo.sh, out, vo.sb, vo.ss, vo.sh, w.delta,
+                                     w.dq_acc, Hq, Dqk, Dv, nullptr, nullptr, dk, dv, vdk.sb, vdk.ss, vdk.sh, vdv.sb,
+                                     vdv.ss, vdv.sh, f16, st);
     return e0 == cudaSuccess ? PSF_OK : cuda_fail(e0, "backward preparation launch");
   }
   cudaError_t e = launch_bwd_prep(
       g, Hq / Hkv, Hkv, accumulate ? kSplitPerSm * dev->sms : 0, w.items, w.n_items, w.seg_prefix, w.item_cap,
-      dev->status, dout, out, vo.sb, vo.ss,
-      vo.sh, w.delta, w.dq_acc, Hq, Dqk, Dv, accumulate ? w.dk_acc : nullptr, accumulate ? w.dv_acc : nullptr,
-      dk, dv, vk.sb, vk.ss, vk.sh, vv.sb, vv.ss, vv.sh, f16, st);
+      dev->status, dout, vdo.sb, vdo.ss, vdo.sh, out, vo.sb, vo.ss, vo.sh, w.delta, w.dq_acc, Hq, Dqk, Dv,
+      accumulate ? w.dk_acc : nullptr, accumulate ? w.dv_acc : nullptr, dk, dv, vdk.sb, vdk.ss, vdk.sh, vdv.sb,
+      vdv.ss, vdv.sh, f16, st);
   if (e != cudaSuccess) return cuda_fail(e, "backward preparation launch");
 
   if (k_rows > 0) {
@@ -410,7 +488,7 @@ int attn_bwd_impl(const void* dout, const void* q, const void* k, const void* v,
     memset(&p, 0, sizeof(p));
     if (q_rows > 0) {
       if ((rc = make_map16(&p.tm_q, q, Dqk, Sq, Hq, B, vq, 64, dtype, qrows, pack))) return rc;
-      if ((rc = make_map16(&p.tm_do, dout, Dv, Sq, Hq, B, vo, 64, dtype, qrows, pack))) return rc;
+      if ((rc = make_map16(&p.tm_do, dout, Dv, Sq, Hq, B, vdo, 64, dtype, qrows, pack))) return rc;
       int r2 = make_tmap_4d(&p.tm_dq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, w.dq_acc, Dqk, Sq, Hq, B, (int64_t)Hq * Dqk,
                             Dqk, (int64_t)Sq * Hq * Dqk, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B);
       if (r2) return fail(PSF_ECUDA, "cuTensorMapEncodeTiled failed (%d) for the dQ accumulator", r2);
@@ -431,13 +509,13 @@ int attn_bwd_impl(const void* dout, const void* q, const void* k, const void* v,
     p.delta = w.delta;
     p.q_rows = (int)q_rows;
     p.dk = dk;
-    p.k_sb = vk.sb;
-    p.k_ss = vk.ss;
-    p.k_sh = vk.sh;
+    p.k_sb = vdk.sb;
+    p.k_ss = vdk.ss;
+    p.k_sh = vdk.sh;
     p.dv = dv;
-    p.v_sb = vv.sb;
-    p.v_ss = vv.ss;
-    p.v_sh = vv.sh;
+    p.v_sb = vdv.sb;
+    p.v_ss = vdv.ss;
+    p.v_sh = vdv.sh;
     p.Hq = Hq;
     p.Hkv = Hkv;
     p.scale = scale;
@@ -455,9 +533,9 @@ int attn_bwd_impl(const void* dout, const void* q, const void* k, const void* v,
     if (timed) timing_end(&tl, st);
     if (e != cudaSuccess) return cuda_fail(e, "backward launch");
   }
-  e = launch_bwd_convert(w.dq_acc, dq, q_rows > 0, B, Sq, Hq, Dqk, vq.sb, vq.ss, vq.sh, accumulate ? w.dk_acc : nullptr,
-                         dk, accumulate ? w.dv_acc : nullptr, dv, Sk, Hkv, Dv, vk.sb, vk.ss, vk.sh, vv.sb, vv.ss,
-                         vv.sh, scale, f16, st);
+  e = launch_bwd_convert(w.dq_acc, dq, q_rows > 0, B, Sq, Hq, Dqk, vdq.sb, vdq.ss, vdq.sh,
+                         accumulate ? w.dk_acc : nullptr, dk, accumulate ? w.dv_acc : nullptr, dv, Sk, Hkv, Dv, vdk.sb,
+                         vdk.ss, vdk.sh, vdv.sb, vdv.ss, vdv.sh, scale, f16, st);
   if (e != cudaSuccess) return cuda_fail(e, "convert launch");
   return PSF_OK;
 }
@@ -465,10 +543,8 @@ int attn_bwd_impl(const void* dout, const void* q, const void* k, const void* v,
 // Fixed scratch of psf_attn_varlen_fwd_noalloc: the forward's tile schedule
 // (item count, per-segment tile prefix, (segment, tile) list) for up to
 // PSF_NOALLOC_MAX_Q_ROWS query rows and PSF_NOALLOC_MAX_SEGMENTS segments.
-constexpr size_t kNoAllocScratchBytes =
-    256 + ((sizeof(int) * (size_t)(PSF_NOALLOC_MAX_SEGMENTS + 2) + 255) & ~size_t(255)) +
-    ((sizeof(int2) * (size_t)((PSF_NOALLOC_MAX_Q_ROWS + kBM - 1) / kBM + PSF_NOALLOC_MAX_SEGMENTS + 1) + 255) &
-     ~size_t(255));
+constexpr size_t kNoAllocScratchBytes = fwd_ws_bytes(PSF_NOALLOC_MAX_Q_ROWS, PSF_NOALLOC_MAX_SEGMENTS, kBM);
+static_assert(kNoAllocScratchBytes == 852736, "the header documents the scratch array's size");
 static __device__ __align__(256) unsigned char g_noalloc_fwd_scratch[kNoAllocScratchBytes];
 
 // Device address of the scratch array, looked up once per device with that
@@ -568,11 +644,12 @@ size_t psf_attn_bwd_workspace_size(int64_t total_q_rows, int64_t total_k_rows, i
 
 int psf_attn_varlen_fwd(const void* q, const void* k, const void* v, void* out, float* lse, const int32_t* cu_q,
                         const int32_t* cu_k, const int32_t* dev_meta, int nseg, int max_q, int max_k, int layout,
-                        int dtype, int B, int Sq, int Sk, int Hq, int Hkv, int Dqk, int Dv, float scale, int causal,
-                        int32_t window_left, float softcap, int flags, void* workspace, size_t ws_bytes, void* stream) {
+                        int dtype, int B, int Sq, int Sk, int Hq, int Hkv, int Dqk, int Dv, const int64_t* strides,
+                        float scale, int causal, int32_t window_left, float softcap, int flags, void* workspace,
+                        size_t ws_bytes, void* stream) {
   if (!cu_q || !cu_k) return fail(PSF_EINVAL, "varlen calls need cu_q and cu_k");
   return attn_fwd_impl(q, k, v, out, lse, cu_q, cu_k, dev_meta, nseg, max_q, max_k, layout, dtype, B, Sq, Sk, Hq, Hkv,
-                       Dqk, Dv, scale, causal, window_left, workspace, ws_bytes, stream, flags, softcap);
+                       Dqk, Dv, scale, causal, window_left, workspace, ws_bytes, stream, flags, softcap, strides);
 }
 
 int psf_attn_varlen_fwd_noalloc(const void* q, const void* k, const void* v, void* out, float* lse,
@@ -597,28 +674,31 @@ int psf_attn_varlen_fwd_noalloc(const void* q, const void* k, const void* v, voi
 int psf_attn_varlen_bwd(const void* dout, const void* q, const void* k, const void* v, const void* out,
                         const float* lse, void* dq, void* dk, void* dv, const int32_t* cu_q, const int32_t* cu_k,
                         const int32_t* dev_meta, int nseg, int max_q, int max_k, int layout, int dtype, int B, int Sq,
-                        int Sk, int Hq, int Hkv, int Dqk, int Dv, float scale, int causal, int32_t window_left,
-                        float softcap, int flags, void* workspace, size_t ws_bytes, void* stream) {
+                        int Sk, int Hq, int Hkv, int Dqk, int Dv, const int64_t* strides, float scale, int causal,
+                        int32_t window_left, float softcap, int flags, void* workspace, size_t ws_bytes,
+                        void* stream) {
   if (!cu_q || !cu_k) return fail(PSF_EINVAL, "varlen calls need cu_q and cu_k");
   return attn_bwd_impl(dout, q, k, v, out, lse, dq, dk, dv, cu_q, cu_k, dev_meta, nseg, max_q, max_k, layout, dtype, B,
                        Sq, Sk, Hq, Hkv, Dqk, Dv, scale, causal, window_left, workspace, ws_bytes, stream, softcap,
-                       flags);
+                       flags, strides);
 }
 
 int psf_attn_dense_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq, int Hkv,
-                       int Nq, int Nk, int Dqk, int Dv, int dtype, float scale, int causal, int32_t window_left,
-                       float softcap, int flags, void* workspace, size_t ws_bytes, void* stream) {
+                       int Nq, int Nk, int Dqk, int Dv, const int64_t* strides, int dtype, float scale, int causal,
+                       int32_t window_left, float softcap, int flags, void* workspace, size_t ws_bytes,
+                       void* stream) {
   return attn_fwd_impl(q, k, v, out, lse, nullptr, nullptr, nullptr, B, Nq, Nk, PSF_LAYOUT_BHSD, dtype, B, Nq, Nk, Hq,
-                       Hkv, Dqk, Dv, scale, causal, window_left, workspace, ws_bytes, stream, flags, softcap);
+                       Hkv, Dqk, Dv, scale, causal, window_left, workspace, ws_bytes, stream, flags, softcap, strides);
 }
 
 int psf_attn_dense_bwd(const void* dout, const void* q, const void* k, const void* v, const void* out,
                        const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Nq, int Nk,
-                       int Dqk, int Dv, int dtype, float scale, int causal, int32_t window_left, float softcap,
-                       int flags, void* workspace, size_t ws_bytes, void* stream) {
+                       int Dqk, int Dv, const int64_t* strides, int dtype, float scale, int causal,
+                       int32_t window_left, float softcap, int flags, void* workspace, size_t ws_bytes,
+                       void* stream) {
   return attn_bwd_impl(dout, q, k, v, out, lse, dq, dk, dv, nullptr, nullptr, nullptr, B, Nq, Nk, PSF_LAYOUT_BHSD,
                        dtype, B, Nq, Nk, Hq, Hkv, Dqk, Dv, scale, causal, window_left, workspace, ws_bytes, stream,
-                       softcap, flags);
+                       softcap, flags, strides);
 }
 
 int psf_build_doc_segments(const int32_t* kv_doc_ids, int B, int Sk, int q_length, int q_global_start,

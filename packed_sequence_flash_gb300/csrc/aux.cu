@@ -263,7 +263,9 @@ __device__ void bwd_schedule_body(SegInfo g, int G, int Hkv, int split_target,
 __device__ void fwd_tail_body(SegInfo g, uint16_t* out, int64_t o_sb, int64_t o_ss, int64_t o_sh, float* lse,
                               int64_t l_sb, int64_t l_sh, int Hq, int Dv, int bid, int nblk) {
   const int nseg = seg_count(g);
-  const int first = cu_q_at(g, nseg);
+  // Clamped: with invalid segment arrays (which the schedule rejects) this
+  // still writes only rows of the tensor.
+  const int first = max(cu_q_at(g, nseg), 0);
   const int64_t rows = (int64_t)g.B * g.Sq - first;
   if (rows <= 0) return;
   const int groups = Dv / 8;
@@ -470,8 +472,8 @@ __global__ void lse_merge_kernel(const E* o1, const float* l1, const E* o2, cons
 // Delta = rowsum(dO * O) and the zeroed accumulators; blocks bid of nblk.
 constexpr int kDeltaUnroll = 2;
 template <typename E>
-__device__ void bwd_pre_body(SegInfo g, const E* dout, const E* out, int64_t o_sb,
-                             int64_t o_ss, int64_t o_sh, float* delta, float* dq_acc, int Hq, int Dqk, int Dv,
+__device__ void bwd_pre_body(SegInfo g, const E* dout, int64_t d_sb, int64_t d_ss, int64_t d_sh, const E* out,
+                             int64_t o_sb, int64_t o_ss, int64_t o_sh, float* delta, float* dq_acc, int Hq, int Dqk, int Dv,
                              float* dk_acc, float* dv_acc, uint16_t* dk, uint16_t* dv, int64_t k_sb,
                              int64_t k_ss, int64_t k_sh, int64_t v_sb, int64_t v_ss, int64_t v_sh, int Hkv, int bid,
                              int nblk) {
@@ -485,7 +487,7 @@ __device__ void bwd_pre_body(SegInfo g, const E* dout, const E* out, int64_t o_s
   constexpr int U = kDeltaUnroll;
   for (int64_t base = (bid * (int64_t)blockDim.x + threadIdx.x) / 32 * per_warp; base < n; base += stride * U) {
     float acc[U];
-    int64_t off[U];
+    int64_t off[U], doff[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       acc[u] = 0.f;
@@ -493,14 +495,16 @@ __device__ void bwd_pre_body(SegInfo g, const E* dout, const E* out, int64_t o_s
       const int64_t f = wrk / Hq;
       const int h = (int)(wrk - f * Hq);
       const int b = (int)(f / g.Sq), s = (int)(f - (int64_t)b * g.Sq);
-      off[u] = wrk < n && grp < per_warp ? b * o_sb + (int64_t)s * o_ss + h * o_sh : -1;
+      const bool live = wrk < n && grp < per_warp;
+      off[u] = live ? b * o_sb + (int64_t)s * o_ss + h * o_sh : -1;
+      doff[u] = live ? b * d_sb + (int64_t)s * d_ss + h * d_sh : -1;
     }
     for (int d = sub * 8; d < Dv; d += lanes * 8) {
       uint4 ug[U], uo[U];
 #pragma unroll
       for (int u = 0; u < U; ++u)
         if (off[u] >= 0) {
-          ug[u] = *reinterpret_cast<const uint4*>(dout + off[u] + d);
+          ug[u] = *reinterpret_cast<const uint4*>(dout + doff[u] + d);
           uo[u] = *reinterpret_cast<const uint4*>(out + off[u] + d);
         }
 #pragma unroll
@@ -538,7 +542,7 @@ __device__ void bwd_pre_body(SegInfo g, const E* dout, const E* out, int64_t o_s
     for (int64_t x = tid; x < nv4; x += nthr) reinterpret_cast<float4*>(dv_acc)[x] = z4;
     return;
   }
-  const int first = cu_k_at(g, seg_count(g));
+  const int first = max(cu_k_at(g, seg_count(g)), 0);  // clamped as in fwd_tail_body
   const int64_t krows = krows_all - first;
   if (krows > 0) {
     const int gk = Dqk / 8, gv = Dv / 8;
@@ -841,13 +845,13 @@ __global__ void __launch_bounds__(kScanThreads) fwd_prep_kernel(SegInfo g, int2*
 template <typename E>
 __global__ void __launch_bounds__(kScanThreads) bwd_prep_kernel(
     SegInfo g, int G, int Hkv, int split_target, int4* items, int* n_items, int* seg_prefix, int item_cap, int* status,
-    const E* dout, const E* out, int64_t o_sb, int64_t o_ss, int64_t o_sh, float* delta,
-    float* dq_acc, int Hq, int Dqk, int Dv, float* dk_acc, float* dv_acc, uint16_t* dk, uint16_t* dv,
+    const E* dout, int64_t d_sb, int64_t d_ss, int64_t d_sh, const E* out, int64_t o_sb, int64_t o_ss, int64_t o_sh,
+    float* delta, float* dq_acc, int Hq, int Dqk, int Dv, float* dk_acc, float* dv_acc, uint16_t* dk, uint16_t* dv,
     int64_t k_sb, int64_t k_ss, int64_t k_sh, int64_t v_sb, int64_t v_ss, int64_t v_sh) {
   if (blockIdx.x == 0)
     bwd_schedule_body(g, G, Hkv, split_target, items, n_items, seg_prefix, item_cap, status);
   else
-    bwd_pre_body(g, dout, out, o_sb, o_ss, o_sh, delta, dq_acc, Hq, Dqk, Dv, dk_acc, dv_acc, dk, dv, k_sb, k_ss, k_sh,
+    bwd_pre_body(g, dout, d_sb, d_ss, d_sh, out, o_sb, o_ss, o_sh, delta, dq_acc, Hq, Dqk, Dv, dk_acc, dv_acc, dk, dv, k_sb, k_ss, k_sh,
                  v_sb, v_ss, v_sh, Hkv, blockIdx.x - 1, gridDim.x - 1);
 }
 
@@ -905,10 +909,11 @@ cudaError_t launch_lse_merge(const void* o1, const float* l1, const void* o2, co
 }
 
 cudaError_t launch_bwd_prep(const SegInfo& g, int G, int Hkv, int split_target, int4* items, int* n_items,
-                            int* seg_prefix, int item_cap, int* status, const void* dout, const void* out, int64_t o_sb,
-                            int64_t o_ss, int64_t o_sh, float* delta, float* dq_acc, int Hq, int Dqk, int Dv,
-                            float* dk_acc, float* dv_acc, void* dk, void* dv, int64_t k_sb, int64_t k_ss, int64_t k_sh,
-                            int64_t v_sb, int64_t v_ss, int64_t v_sh, int f16, cudaStream_t st) {
+                            int* seg_prefix, int item_cap, int* status, const void* dout, int64_t d_sb, int64_t d_ss,
+                            int64_t d_sh, const void* out, int64_t o_sb, int64_t o_ss, int64_t o_sh, float* delta,
+                            float* dq_acc, int Hq, int Dqk, int Dv, float* dk_acc, float* dv_acc, void* dk, void* dv,
+                            int64_t k_sb, int64_t k_ss, int64_t k_sh, int64_t v_sb, int64_t v_ss, int64_t v_sh, int f16,
+                            cudaStream_t st) {
   // One 1024-thread block per SM fits (the schedule block's registers and
   // shared memory), so the fill takes one wave beside it.
   const int64_t work = (int64_t)g.B * g.Sq * Hq * Dqk / 4 + (int64_t)g.B * g.Sk * Hkv * (Dqk + Dv) / 4;
@@ -918,12 +923,13 @@ cudaError_t launch_bwd_prep(const SegInfo& g, int G, int Hkv, int split_target, 
   if (f16)
     bwd_prep_kernel<__half><<<1 + fill, kScanThreads, 0, st>>>(
         g, G, Hkv, split_target, items, n_items, seg_prefix, item_cap, status, static_cast<const __half*>(dout),
-        static_cast<const __half*>(out), o_sb, o_ss, o_sh, delta, dq_acc, Hq, Dqk, Dv, dk_acc, dv_acc, dk16, dv16,
+        d_sb, d_ss, d_sh, static_cast<const __half*>(out), o_sb, o_ss, o_sh, delta, dq_acc, Hq, Dqk, Dv, dk_acc, dv_acc, dk16, dv16,
         k_sb, k_ss, k_sh, v_sb, v_ss, v_sh);
   else
     bwd_prep_kernel<__nv_bfloat16><<<1 + fill, kScanThreads, 0, st>>>(
         g, G, Hkv, split_target, items, n_items, seg_prefix, item_cap, status,
-        static_cast<const __nv_bfloat16*>(dout), static_cast<const __nv_bfloat16*>(out), o_sb, o_ss, o_sh, delta,
+        static_cast<const __nv_bfloat16*>(dout), d_sb, d_ss, d_sh, static_cast<const __nv_bfloat16*>(out), o_sb,
+        o_ss, o_sh, delta,
         dq_acc, Hq, Dqk, Dv, dk_acc, dv_acc, dk16, dv16, k_sb, k_ss, k_sh, v_sb, v_ss, v_sh);
   return cudaGetLastError();
 }

@@ -42,9 +42,9 @@ struct BwdParams {
   const float* delta;  // [Hq][q_rows]
   int q_rows;
   void* dk;  // T
-  int64_t k_sb, k_ss, k_sh;
+  int64_t k_sb, k_ss, k_sh;  // element strides of dk (batch, row, head)
   void* dv;  // T
-  int64_t v_sb, v_ss, v_sh;
+  int64_t v_sb, v_ss, v_sh;  // element strides of dv
   int Hq, Hkv;
   float scale, scale_log2;
   int pack;       // query heads per step: 1, or Hq / Hkv when a KV head's query heads share one tile

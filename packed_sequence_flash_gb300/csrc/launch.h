@@ -21,14 +21,16 @@ cudaError_t launch_fwd_prep(const SegInfo& g, int2* items, int* n_items, int* se
 // Backward preparation in one launch: the work list of key tiles, split into
 // (first step, end step) sub-ranges when split_target > 0 (items are int4
 // (segment, key tile, first, end); n_items[1] zeroed as above); Delta =
-// rowsum(dO * O) (fp32, [Hq][rows]); the zeroed dQ accumulator, and either the
+// rowsum(dO * O) (fp32, [Hq][rows]; dO and O each with their own element
+// strides); the zeroed dQ accumulator, and either the
 // zeroed dK/dV accumulators (when given) or zeroed dK / dV rows at or past
 // cu_k[nseg].
 cudaError_t launch_bwd_prep(const SegInfo& g, int G, int Hkv, int split_target, int4* items, int* n_items,
-                            int* seg_prefix, int item_cap, int* status, const void* dout, const void* out, int64_t o_sb,
-                            int64_t o_ss, int64_t o_sh, float* delta, float* dq_acc, int Hq, int Dqk, int Dv,
-                            float* dk_acc, float* dv_acc, void* dk, void* dv, int64_t k_sb, int64_t k_ss, int64_t k_sh,
-                            int64_t v_sb, int64_t v_ss, int64_t v_sh, int f16, cudaStream_t st);
+                            int* seg_prefix, int item_cap, int* status, const void* dout, int64_t d_sb, int64_t d_ss,
+                            int64_t d_sh, const void* out, int64_t o_sb, int64_t o_ss, int64_t o_sh, float* delta,
+                            float* dq_acc, int Hq, int Dqk, int Dv, float* dk_acc, float* dv_acc, void* dk, void* dv,
+                            int64_t k_sb, int64_t k_ss, int64_t k_sh, int64_t v_sb, int64_t v_ss, int64_t v_sh, int f16,
+                            cudaStream_t st);
 // Grid: one CTA per SM (two for head dims 64 and 128), at most max_work.
 // f16 selects fp16 inputs and outputs (else bf16).
 cudaError_t launch_fwd(const FwdParams& p, int dqk, int dvc, int sms, int64_t max_work, int f16, cudaStream_t st);

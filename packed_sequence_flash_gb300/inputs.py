@@ -142,7 +142,9 @@ def config(n: int, seed: int = 0) -> Workload:
     3. dense causal, B=2, Hq=8, Hkv=2, N=4096, D=512, inputs times 0.5;
     4. 16384-token row, lognormal lengths (median 1024), queries 8192..16383, Dqk=192, Dv=128,
        Hq=Hkv=16;
-    5. 65536 tokens, Pareto(1.2) lengths in [256, 32768], Hq=32, Hkv=8, D=128, left window 4096;
+    5. 65536 tokens, Pareto(1.2) lengths in [256, 32768], Hq=32, Hkv=8, D=128, left window 4096,
+       plus a run without window of the query shard 32768..65535 split into a local and a cross
+       key chunk (``extra["cross_split"]``);
     6. short documents: 65536 tokens, lengths uniform in [16, 64], Hq=32, Hkv=8, D=128 (the
        workload that packing a KV head's query heads into one tile is for).
     """
@@ -158,8 +160,12 @@ def config(n: int, seed: int = 0) -> Workload:
         return document_workload("lognormal1024", 16384, 16, 16, 192, 128, seed, q_global_start=8192,
                                  name="cfg4_doc_causal_shard_dqk192_dv128")
     if n == 5:
-        return document_workload("pareto256", 65536, 32, 8, 128, 128, seed, window=4096,
-                                 name="cfg5_doc_causal_t65536_w4096")
+        w = document_workload("pareto256", 65536, 32, 8, 128, 128, seed, window=4096,
+                              name="cfg5_doc_causal_t65536_w4096")
+        # the second half of the row is the query shard of the cross-chunk run:
+        # keys [32768, 65536) are its local chunk, keys [0, 32768) the cross chunk
+        w.extra["cross_split"] = 32768
+        return w
     if n == 6:
         return document_workload("uniform16_64", 65536, 32, 8, 128, 128, seed,
                                  name="short_docs_t65536_len16_64_d128")

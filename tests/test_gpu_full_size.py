@@ -1,8 +1,9 @@
 """Full-size parity: the five workloads at their stated sizes (and the
 short-document workload with packed query heads), run through the same calls
-the benchmark times, checked against the oracle on sampled rows
-(the oracle evaluates forward rows and dQ rows one query at a time and dK/dV
-rows one key at a time).
+the benchmark times, checked against the oracle on every row where the oracle
+takes seconds (workloads 2 and 4; workload 1 is checked whole in the parity
+tests) and on sampled rows elsewhere (the oracle evaluates forward rows and dQ
+rows one query at a time and dK/dV rows one key at a time).
 
 Workload 5 also runs the cross-chunk decomposition of the cp_attention page on
 one GPU: the query shard 32768..65535 attends its own key chunk causally
@@ -51,8 +52,10 @@ def _check_grad_rows(g, ref, rows, name):
     assert e <= GRAD_TOL, f"{name} relative Frobenius error {e:.3e} on sampled rows"
 
 
-def _doc_full(cfg, n_rows=192, softcap=None, pack_gqa=False):
-    w = inputs.config(cfg, seed=0)
+def _doc_full(cfg, n_rows=192, softcap=None, pack_gqa=False, seed=0, every_row=False):
+    """Workload `cfg` through the document path against the oracle: on sampled
+    rows, or on every query and key row (every_row) where the oracle is cheap."""
+    w = inputs.config(cfg, seed=seed)
     dev = "cuda"
     q, k, v, do = (t.to(dev) for t in (w.q, w.k, w.v, w.dout))
     ids = torch.from_numpy(w.doc_ids).to(dev)
@@ -65,8 +68,13 @@ def _doc_full(cfg, n_rows=192, softcap=None, pack_gqa=False):
     assert psf.device_status() == 0
     # sample rows, always including document edges and the shard edges
     starts = np.cumsum([0] + w.extra["lengths"])
-    q_rows = _rows(Lq, n_rows, 1, must=[0, Lq - 1] + [s - w.q_global_start for s in starts])
-    k_rows = _rows(w.k.shape[0], n_rows, 2, must=[0, w.k.shape[0] - 1] + list(starts[:-1]) + list(starts[1:] - 1))
+    if every_row:
+        q_rows = np.arange(Lq, dtype=np.int32)
+        k_rows = np.arange(w.k.shape[0], dtype=np.int32)
+    else:
+        q_rows = _rows(Lq, n_rows, 1, must=[0, Lq - 1] + [s - w.q_global_start for s in starts])
+        k_rows = _rows(w.k.shape[0], n_rows, 2,
+                       must=[0, w.k.shape[0] - 1] + list(starts[:-1]) + list(starts[1:] - 1))
     out_o, lse_o = oracle.attn_fwd_document(w.q, w.k, w.v, w.doc_ids, w.q_global_start, w.scale, w.window,
                                             rows=q_rows, softcap=softcap)
     _check_fwd_rows(out, lse, out_o, lse_o, q_rows)
@@ -81,12 +89,13 @@ def _doc_full(cfg, n_rows=192, softcap=None, pack_gqa=False):
     _check_grad_rows(grads[2], dv_o, k_rows, "dv")
 
 
-def test_workload2_full_size():
-    _doc_full(2)
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_workload2_full_size_every_row(seed):
+    _doc_full(2, seed=seed, every_row=True)
 
 
-def test_workload4_full_size_shard_unequal_dims():
-    _doc_full(4)
+def test_workload4_full_size_shard_unequal_dims_every_row():
+    _doc_full(4, every_row=True)
 
 
 def test_workload2_full_size_softcap():
