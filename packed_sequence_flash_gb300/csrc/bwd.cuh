@@ -56,31 +56,30 @@ struct BwdParams {
   uint64_t limit_ns;
 };
 
+// Shared-memory and TMEM plan of attn_bwd_kernel (Dqk = 192, Dv = 128).
 template <int DQK, int DV>
 struct BwdCfg {
   static constexpr int KCH = DQK / 64;
   static constexpr int VCH = DV / 64;
-  static constexpr bool DUAL = DQK <= 128 && DV <= 128;
   static constexpr int K_OFF = 0;
   static constexpr int V_OFF = K_OFF + KCH * kChunkBytes;
   static constexpr int Q_OFF = V_OFF + VCH * kChunkBytes;
   static constexpr int DO_OFF = Q_OFF + KCH * kChunkBytes;
-  static constexpr int PT_OFF = DO_OFF + VCH * kChunkBytes;
-  // The single-region plan writes dS^T over P^T once the dV MMA has read it,
-  // and stages dQ in that same buffer once the dQ MMA has read dS.
-  static constexpr int DS_OFF = DUAL ? PT_OFF + 2 * kChunkBytes : PT_OFF;
-  static constexpr int STG_OFF = DUAL ? DS_OFF + 2 * kChunkBytes : PT_OFF;  // 4 x 4 KB dQ staging
-  static constexpr int ROWV_OFF = DUAL ? STG_OFF + 4 * 4096 : PT_OFF + 2 * kChunkBytes;
-  static constexpr int SMEM_BYTES = ROWV_OFF + 2 * 4 * 128 * 4 + 1024;
-  // TMEM columns
+  // dS^T (bf16, two 64-query chunks); between steps each compute warp stages
+  // its share of the dQ read-out in its own 32 rows of this buffer.
+  static constexpr int DS_OFF = DO_OFF + VCH * kChunkBytes;
+  static constexpr int STG_OFF = DS_OFF + 2 * kChunkBytes;  // dQ staging of the read-out warps (4 x 4 KB)
+  static constexpr int ROWV_OFF = STG_OFF + 4 * 4096;       // -lse log2 e and -Delta, 8 warps x 64 each
+  static constexpr int SMEM_BYTES = ROWV_OFF + 2 * 8 * 64 * 4 + 1024;
+  // TMEM columns: dV [0, 128) | dK [128, 320) | R [320, 512). R holds S^T
+  // (first 128 columns), then dP^T (same columns), then dQ (all 192); P^T
+  // (packed 16-bit) sits in its last 64 columns between S^T and dQ.
   static constexpr int T_DV = 0;
-  static constexpr int T_DK = DUAL ? DV : 128;
-  static constexpr int T_A = DUAL ? 256 : 320;
-  static constexpr int T_B = DUAL ? 384 : 320;
-  // Single-region plan with a softcap: P^T (1 - tanh^2), packed, between the passes.
-  static constexpr int T_PF = 448;
+  static constexpr int T_DK = 128;
+  static constexpr int T_R = 320;
+  static constexpr int T_P = T_R + 128;
+  static_assert(DQK == 192 && DV == 128, "single-region plan is laid out for (192, 128)");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-  static_assert(DUAL || (DQK == 192 && DV == 128), "single-region plan is laid out for (192, 128)");
 };
 
 // One work unit: a key tile of one KV head and a range [k0, k1) of its steps.
@@ -113,15 +112,28 @@ __device__ __forceinline__ BwdItem bwd_decode(const BwdParams& p, int w) {
 }
 
 // CAP: logits softcapped (p.softcap > 0); dS carries the cap's 1 - tanh^2.
+//
+// Per step (one 128-query tile of one query head against the resident key
+// tile), thread r of a compute warpgroup owning key row r (TMEM lane r):
+//   S^T  = K Q^T -> R[0, 128)          P^T = exp2(S^T scale log2 e - lse log2 e)
+//   P^T (16-bit, packed) -> R[128, 192) (the TMEM operand of dV += P^T dO)
+//   dP^T = V dO^T -> R[0, 128)          dS^T = P^T (dP^T - Delta) -> shared memory
+//   dK  += dS^T Q,  dQ = dS K -> R[0, 192)
+// Two compute warpgroups split the 128 query columns of every step (warps
+// 4-7 columns 0-63, warps 12-15 columns 64-127); the dQ read-out is split over
+// twelve warps (the two compute warpgroups and warps 8-11, two 32-column
+// chunks each), which release R as soon as their chunks are in registers so
+// that the next step's S^T can start while the chunks go out by TMA
+// reduce-add. Warps: 0 TMA producer, 1 MMA issuer, 2 TMEM allocator.
 template <typename T, int DQK, int DV, bool CAP>
-__global__ void __launch_bounds__(384, 1) attn_bwd_kernel(const __grid_constant__ BwdParams p) {
+__global__ void __launch_bounds__(512, 1) attn_bwd_kernel(const __grid_constant__ BwdParams p) {
   using C = BwdCfg<DQK, DV>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  float* lse_s = reinterpret_cast<float*>(smem + C::ROWV_OFF);  // [4 warps][128]
-  float* dl_s = lse_s + 4 * 128;
+  float* l2_s = reinterpret_cast<float*>(smem + C::ROWV_OFF);  // [8 compute warps][64]: lse * log2 e (+inf: no mass)
+  float* dl_s = l2_s + 8 * 64;                                   // [8 compute warps][64]: Delta
 
-  __shared__ uint64_t kv_full, kv_empty, q_full, q_empty, s_full, dp_full, p_full, pt_read, ds_full, ds_free,
+  __shared__ uint64_t kv_full, kv_empty, q_full, q_empty, do_full, do_empty, s_full, p_full, dp_full, ds_full,
       dq_full, dq_free, acc_done, acc_free, drain;
   __shared__ uint32_t tmem_base_smem;
   __shared__ int abort_flag;
@@ -132,16 +144,16 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_kernel(const __grid_constant_
     mbar_init(&kv_empty, 1);
     mbar_init(&q_full, 1);
     mbar_init(&q_empty, 1);
+    mbar_init(&do_full, 1);
+    mbar_init(&do_empty, 1);
     mbar_init(&s_full, 1);
+    mbar_init(&p_full, 8);
     mbar_init(&dp_full, 1);
-    mbar_init(&p_full, 4);
-    mbar_init(&pt_read, 1);
-    mbar_init(&ds_full, 4);
-    mbar_init(&ds_free, 1);
+    mbar_init(&ds_full, 8);
     mbar_init(&dq_full, 1);
-    mbar_init(&dq_free, 4);
+    mbar_init(&dq_free, 12);
     mbar_init(&acc_done, 1);
-    mbar_init(&acc_free, 4);
+    mbar_init(&acc_free, 8);
     mbar_init(&drain, 1);
     abort_flag = 0;
     fence_mbar_init();
@@ -158,6 +170,42 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_kernel(const __grid_constant_
   const int total = (*p.n_items) * p.Hkv;
   const int G = p.Hq / p.Hkv;
   const uint32_t sbase = smem_u32(smem);
+
+  // One 32 x 32 fp32 chunk of dQ (query rows = TMEM lanes of this warp) into
+  // the warp's staging box and on to the accumulator by TMA reduce-add.
+  auto reduce_box = [&](uint8_t* box, const uint32_t(&v)[32], int dcol, int sq, int h, int bq) {
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      *reinterpret_cast<uint4*>(box + sw128_offset(lane, u)) = make_uint4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_reduce_add_4d(&p.tm_dq, box, dcol, sq, h, bq);
+      bulk_commit_group();
+    }
+  };
+  // The read-out of one step: this warp's two dQ chunks [c0, c0 + 2) (32
+  // columns each) into registers, R released, then both chunks staged through
+  // `box` (each staging waits until the box's previous reduce has read it).
+  auto dq_readout = [&](const BwdItem& t, int k, uint32_t gstep, int wq, int c0, uint8_t* box) -> bool {
+    if (!wait_bar(&dq_full, gstep & 1, ctl)) return false;
+    tc_fence_after();
+    uint32_t a[2][32];
+    const uint32_t rq = tmem + ((uint32_t)(32 * wq) << 16) + C::T_R + c0 * 32;
+    tmem_ld32x2(rq, rq + 32, a[0], a[1]);
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&dq_free);
+    const int h = t.hk * G + k / t.nqt, qt = t.qt0 + k % t.nqt;
+    const int fq = t.cq0 + qt * kBM + 32 * wq, bq = fq / p.seg.Sq, sq = fq - bq * p.seg.Sq;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      if (lane == 0) bulk_wait_group_read0();
+      __syncwarp();
+      reduce_box(box, a[i], (c0 + i) * 32, sq, h, bq);
+    }
+    return true;
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -181,33 +229,42 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_kernel(const __grid_constant_
         for (int c = 0; c < C::VCH; ++c)
           tma_load_4d(smem + C::V_OFF + c * kChunkBytes, &p.tm_v, &kv_full, c * 64, sk, t.hk, bk);
         ++nz;
-        for (int k = t.k0; k < t.k1; ++k) {
+        for (int k = t.k0; k < t.k1; ++k, ++gstep) {
           const int h = t.hk * G + k / t.nqt, qt = t.qt0 + k % t.nqt;
+          const int fq = t.cq0 + qt * kBM, bq = fq / p.seg.Sq, sq = fq - bq * p.seg.Sq;
+          // dO(g) once dV(g-1) has read dO(g-1), then Q(g) once dK(g-1) has read Q(g-1).
+          if (!wait_bar(&do_empty, (gstep & 1) ^ 1, ctl)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&do_full, C::VCH * kChunkBytes);
+          for (int c = 0; c < C::VCH; ++c)
+            tma_load_4d(smem + C::DO_OFF + c * kChunkBytes, &p.tm_do, &do_full, c * 64, sq, h, bq);
           if (!wait_bar(&q_empty, (gstep & 1) ^ 1, ctl)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&q_full, (C::KCH + C::VCH) * kChunkBytes);
-          const int fq = t.cq0 + qt * kBM, bq = fq / p.seg.Sq, sq = fq - bq * p.seg.Sq;
+          mbar_arrive_expect_tx(&q_full, C::KCH * kChunkBytes);
           for (int c = 0; c < C::KCH; ++c)
             tma_load_4d(smem + C::Q_OFF + c * kChunkBytes, &p.tm_q, &q_full, c * 64, sq, h, bq);
-          for (int c = 0; c < C::VCH; ++c)
-            tma_load_4d(smem + C::DO_OFF + c * kChunkBytes, &p.tm_do, &q_full, c * 64, sq, h, bq);
-          ++gstep;
         }
       }
       if (nz > 0) wait_bar_drain(&kv_full, (nz - 1) & 1, p.limit_ns);
-      if (gstep > 0) wait_bar_drain(&q_full, (gstep - 1) & 1, p.limit_ns);
+      if (gstep > 0) {
+        wait_bar_drain(&do_full, (gstep - 1) & 1, p.limit_ns);
+        wait_bar_drain(&q_full, (gstep - 1) & 1, p.limit_ns);
+      }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t id_sq = idesc_f32acc<T>(128, 128, 0, 0);  // S^T, dP^T
-      constexpr uint32_t id_dv = idesc_f32acc<T>(128, DV, 0, 1);   // dV += P^T dO
+      constexpr uint32_t id_sq = idesc_f32acc<T>(128, 128, 0, 0);  // S^T = K Q^T, dP^T = V dO^T
+      constexpr uint32_t id_dv = idesc_f32acc<T>(128, DV, 0, 1);   // dV += P^T (TMEM) dO
       constexpr uint32_t id_dk = idesc_f32acc<T>(128, DQK, 0, 1);  // dK += dS^T Q
-      constexpr uint32_t id_dq = idesc_f32acc<T>(128, DQK, 1, 1);  // dQ = dS K
+      constexpr uint32_t id_dq = idesc_f32acc<T>(128, DQK, 1, 1);  // dQ  = dS K
       const uint32_t k_a = sbase + C::K_OFF, v_a = sbase + C::V_OFF, q_a = sbase + C::Q_OFF;
-      const uint32_t do_a = sbase + C::DO_OFF, pt_a = sbase + C::PT_OFF, ds_a = sbase + C::DS_OFF;
+      const uint32_t do_a = sbase + C::DO_OFF, ds_a = sbase + C::DS_OFF;
+      const uint32_t rr = tmem + C::T_R, rp = tmem + C::T_P;
       uint32_t nz = 0, gstep = 0;
       bool ok = true;
       for (int wi = 0; wi * (int)gridDim.x < total && ok; ++wi) {
@@ -219,74 +276,55 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_kernel(const __grid_constant_
         if (nz > 0 && !wait_bar(&acc_free, (nz - 1) & 1, ctl)) break;
         tc_fence_after();
         for (int k = t.k0; k < t.k1 && ok; ++k, ++gstep) {
-          if (!wait_bar(&q_full, gstep & 1, ctl)) {
+          // S^T(g) once Q(g) has landed and the previous dQ has left R.
+          if (!wait_bar(&q_full, gstep & 1, ctl) || (gstep > 0 && !wait_bar(&dq_free, (gstep - 1) & 1, ctl))) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t rs = tmem + (C::DUAL ? ((gstep & 1) ? C::T_B : C::T_A) : C::T_A);  // S (and dQ)
-          const uint32_t rp = tmem + (C::DUAL ? ((gstep & 1) ? C::T_A : C::T_B) : C::T_A);  // dP
-          if (!C::DUAL && gstep > 0 && !wait_bar(&dq_free, (gstep - 1) & 1, ctl)) {
-            ok = false;
-            break;
-          }
           for (int c = 0; c < C::KCH; ++c) {
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              mma_ss(rs, sdesc_sw128(k_a + c * kChunkBytes + kk * 32, 16, 1024),
+              mma_ss(rr, sdesc_sw128(k_a + c * kChunkBytes + kk * 32, 16, 1024),
                      sdesc_sw128(q_a + c * kChunkBytes + kk * 32, 16, 1024), id_sq, (c | kk) != 0);
           }
           mma_commit(&s_full);
-          if (C::DUAL) {
-            if (gstep > 0 && !wait_bar(&dq_free, (gstep - 1) & 1, ctl)) {
-              ok = false;
-              break;
-            }
-          } else {
-            if (!wait_bar(&p_full, gstep & 1, ctl)) {
-              ok = false;
-              break;
-            }
+          // dP^T over S^T once the first pass has read it and written P^T;
+          // then dV from the packed P^T.
+          if (!wait_bar(&do_full, gstep & 1, ctl) || !wait_bar(&p_full, gstep & 1, ctl)) {
+            ok = false;
+            break;
           }
           tc_fence_after();
           for (int c = 0; c < C::VCH; ++c) {
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              mma_ss(rp, sdesc_sw128(v_a + c * kChunkBytes + kk * 32, 16, 1024),
+              mma_ss(rr, sdesc_sw128(v_a + c * kChunkBytes + kk * 32, 16, 1024),
                      sdesc_sw128(do_a + c * kChunkBytes + kk * 32, 16, 1024), id_sq, (c | kk) != 0);
           }
           mma_commit(&dp_full);
           const uint32_t first = (k == t.k0) ? 1u : 0u;
-          if (!C::DUAL) {
-            // P^T is already in shared memory: dV can start while dS is computed.
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              mma_ss(tmem + C::T_DV, sdesc_sw128(pt_a + (kk >> 2) * kChunkBytes + (kk & 3) * 32, 16, 1024),
-                     sdesc_sw128(do_a + kk * 2048, kChunkBytes, 1024), id_dv, !(first && kk == 0));
-            mma_commit(&pt_read);
-          }
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ts(tmem + C::T_DV, rp + kk * 8, sdesc_sw128(do_a + kk * 2048, kChunkBytes, 1024), id_dv,
+                   !(first && kk == 0));
+          mma_commit(&do_empty);
+          // dK, then dQ over all of R, once dS^T is in shared memory.
           if (!wait_bar(&ds_full, gstep & 1, ctl)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          if (C::DUAL) {
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              mma_ss(tmem + C::T_DV, sdesc_sw128(pt_a + (kk >> 2) * kChunkBytes + (kk & 3) * 32, 16, 1024),
-                     sdesc_sw128(do_a + kk * 2048, kChunkBytes, 1024), id_dv, !(first && kk == 0));
-          }
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
             mma_ss(tmem + C::T_DK, sdesc_sw128(ds_a + (kk >> 2) * kChunkBytes + (kk & 3) * 32, 16, 1024),
                    sdesc_sw128(q_a + kk * 2048, kChunkBytes, 1024), id_dk, !(first && kk == 0));
+          mma_commit(&q_empty);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            mma_ss(rs, sdesc_sw128(ds_a + kk * 2048, kChunkBytes, 1024), sdesc_sw128(k_a + kk * 2048, kChunkBytes, 1024),
+            mma_ss(rr, sdesc_sw128(ds_a + kk * 2048, kChunkBytes, 1024), sdesc_sw128(k_a + kk * 2048, kChunkBytes, 1024),
                    id_dq, kk > 0);
-          mma_commit(&ds_free);
           mma_commit(&dq_full);
-          mma_commit(&q_empty);
         }
         if (!ok) break;
         mma_commit(&acc_done);
@@ -296,31 +334,21 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_kernel(const __grid_constant_
       mma_commit(&drain);
       wait_bar_drain(&drain, 0, p.limit_ns);
     }
-  } else if (warp >= 4 && warp < 8) {
-    // ------------------------------------------------------------ compute warpgroup
-    const int wq = warp - 4;
-    const int r = threadIdx.x - 128;  // key row within the tile
+  } else if (warp >= 4 && (warp < 8 || warp >= 12)) {
+    // ------------------------------------------------------------ compute warpgroups
+    const int half = warp >= 12 ? 1 : 0;
+    const int wq = warp & 3;
+    const int cb = half * 64;         // first query column of this warpgroup
+    const int r = 32 * wq + lane;     // key row within the tile
     const uint32_t lane_base = (uint32_t)(32 * wq) << 16;
-    float* my_lse = lse_s + wq * 128;
-    float* my_dl = dl_s + wq * 128;
-    uint8_t* pt_s = smem + C::PT_OFF;
-    uint8_t* ds_s = smem + C::DS_OFF;
+    float* my_l2 = l2_s + (half * 4 + wq) * 64;
+    float* my_dl = dl_s + (half * 4 + wq) * 64;
+    uint8_t* ds_s = smem + C::DS_OFF + half * kChunkBytes;
+    uint8_t* box = ds_s + wq * 4096;  // this warp's own 32 rows of dS^T
+    const uint32_t rr = tmem + lane_base + C::T_R + cb, rp = tmem + lane_base + C::T_P + half * 32;
     const float sl2 = p.scale_log2;
     const float cap_c2 = CAP ? p.softcap * 1.4426950408889634f : 0.f;
     const float cap_k1 = CAP ? 2.f * sl2 / p.softcap : 0.f, cap_ic2 = CAP ? 1.f / cap_c2 : 0.f;
-    // P (and, with CAP, the factor 1 - tanh^2 of the capped logit) of score s
-    // for a row whose lse (log2 units) is l2.
-    auto prob = [&](float s, float l2, float& fac) -> float {
-      if constexpr (CAP) {
-        const float y = softcap_log2(s, cap_k1, cap_c2);
-        const float tt = y * cap_ic2;
-        fac = fmaf(-tt, tt, 1.f);
-        return ex2_approx(y - l2);
-      } else {
-        fac = 1.f;
-        return ex2_approx(fmaf(s, sl2, -l2));
-      }
-    };
     uint32_t nz = 0, gstep = 0;
     bool ok = true;
     for (int wi = 0; wi * (int)gridDim.x < total && ok; ++wi) {
@@ -333,20 +361,23 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_kernel(const __grid_constant_
       T* dk_row = static_cast<T*>(p.dk) + bk * p.k_sb + (int64_t)sk * p.k_ss + t.hk * p.k_sh;
       T* dv_row = static_cast<T*>(p.dv) + bk * p.v_sb + (int64_t)sk * p.v_ss + t.hk * p.v_sh;
       if (t.k1 == t.k0) {
+        // No query sees this key tile: dV (warps 4-7) and dK (warps 12-15) are zero.
         if (valid) {
-          for (int c = 0; c < DQK / 8; ++c) reinterpret_cast<uint4*>(dk_row)[c] = make_uint4(0, 0, 0, 0);
-          for (int c = 0; c < DV / 8; ++c) reinterpret_cast<uint4*>(dv_row)[c] = make_uint4(0, 0, 0, 0);
+          if (half == 0)
+            for (int c = 0; c < DV / 8; ++c) reinterpret_cast<uint4*>(dv_row)[c] = make_uint4(0, 0, 0, 0);
+          else
+            for (int c = 0; c < DQK / 8; ++c) reinterpret_cast<uint4*>(dk_row)[c] = make_uint4(0, 0, 0, 0);
         }
         continue;
       }
       const int delta = t.n - t.m;
-      // lse and Delta of 4 query columns per lane, loaded one step ahead and
-      // left in flight until the step stages them (-inf / 0 outside the segment).
-      auto fetch_rows = [&](int k, float (&lv)[4], float (&dv)[4]) {
+      // lse and Delta of 2 of this warpgroup's query columns per lane, loaded
+      // one step ahead and left in flight (-inf / 0 outside the segment).
+      auto fetch_rows = [&](int k, float (&lv)[2], float (&dv)[2]) {
         const int h = t.hk * G + k / t.nqt, i0 = (t.qt0 + k % t.nqt) * kBM;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int qc = lane * 4 + e;
+        for (int e = 0; e < 2; ++e) {
+          const int qc = cb + lane * 2 + e;
           const int f = t.cq0 + i0 + qc;
           const bool in = i0 + qc < t.m && f < p.q_rows;
           const int fs = in ? f : 0;
@@ -357,171 +388,132 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_kernel(const __grid_constant_
           ldg_pred_f32(dv[e], p.delta + (int64_t)h * p.q_rows + fs, in);
         }
       };
-      float rlv[4], rdv[4];
+      float rlv[2], rdv[2];
       fetch_rows(t.k0, rlv, rdv);
-      {
-        for (int k = t.k0; k < t.k1; ++k, ++gstep) {
-          const int i0 = (t.qt0 + k % t.nqt) * kBM;
-          // Per-key visible query columns [q_lo, q_hi) of this tile.
-          int q_lo = p.seg.causal ? j - delta - i0 : -0x40000000;
-          int q_hi = t.m - i0;
-          if (p.seg.window > 0) q_hi = min(q_hi, j - delta + p.seg.window - i0);
-          if (!valid) q_lo = q_hi = 0;
-          const bool masked = q_lo > 0 || q_hi < kBM;
-          // lse * log2(e) (+inf for rows without mass) and Delta for this step.
+      for (int k = t.k0; k < t.k1; ++k, ++gstep) {
+        const int i0 = (t.qt0 + k % t.nqt) * kBM;
+        // Visible query columns [q_lo, q_hi) of this key row in the tile.
+        int q_lo = p.seg.causal ? j - delta - i0 : -0x40000000;
+        int q_hi = t.m - i0;
+        if (p.seg.window > 0) q_hi = min(q_hi, j - delta + p.seg.window - i0);
+        if (!valid) q_lo = q_hi = 0;
+        const bool masked = __any_sync(0xffffffffu, q_lo > cb || q_hi < cb + 64);
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int qc = lane * 4 + e;
-            my_lse[qc] = rlv[e] == -CUDART_INF_F ? CUDART_INF_F : rlv[e] * 1.4426950408889634f;
-            my_dl[qc] = rdv[e];
-          }
-          if (k + 1 < t.k1) fetch_rows(k + 1, rlv, rdv);
-          __syncwarp();
-          if (!wait_bar(&s_full, gstep & 1, ctl)) {
-            ok = false;
-            break;
-          }
-          if (gstep > 0 && !wait_bar(&ds_free, (gstep - 1) & 1, ctl)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t rs = tmem + lane_base + (C::DUAL ? ((gstep & 1) ? C::T_B : C::T_A) : C::T_A);
-          const uint32_t rp = tmem + lane_base + (C::DUAL ? ((gstep & 1) ? C::T_A : C::T_B) : C::T_A);
-          if (C::DUAL) {
-            if (!wait_bar(&dp_full, gstep & 1, ctl)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-#pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
-              uint32_t sv[32], pv[32];
-              tmem_ld32(rs + c * 32, sv);
-              tmem_ld32(rp + c * 32, pv);
-              uint32_t pk[16], dk2[16];
+        for (int e = 0; e < 2; ++e) {
+          my_l2[lane * 2 + e] = rlv[e] == -CUDART_INF_F ? CUDART_INF_F : rlv[e] * 1.4426950408889634f;
+          my_dl[lane * 2 + e] = rdv[e];
+        }
+        __syncwarp();
+        if (k + 1 < t.k1) fetch_rows(k + 1, rlv, rdv);
+        if (!wait_bar(&s_full, gstep & 1, ctl)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        // Pass 1: P^T of this warpgroup's 64 columns -> R[128 + 32 half, +32)
+        // packed; with CAP the factor P (1 - tanh^2) stays in registers.
+        [[maybe_unused]] uint32_t pf_keep[2][16];  // CAP only
+        {
+          uint32_t sa[32], sb[32];
+          tmem_ld32_async(rr, sa);
+          tmem_ld32_async(rr + 32, sb);
+          tmem_wait_ld32(sa);
+          tmem_wait_ld32(sb);
 #pragma unroll
-              for (int e = 0; e < 16; ++e) {
-                float pr[2], dr[2];
+          for (int c = 0; c < 2; ++c) {
+            uint32_t(&cur)[32] = c ? sb : sa;
+            uint32_t pk[16];
 #pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                  const int qc = c * 32 + 2 * e + u;
-                  float fe;
-                  float pe = prob(__uint_as_float(sv[2 * e + u]), my_lse[qc], fe);
-                  if (masked && (qc < q_lo || qc >= q_hi)) pe = 0.f;
-                  pr[u] = pe;
-                  dr[u] = pe * fe * (__uint_as_float(pv[2 * e + u]) - my_dl[qc]);
+            for (int e = 0; e < 16; ++e) {
+              float pr[2], pf[2];
+#pragma unroll
+              for (int u = 0; u < 2; ++u) {
+                const int ql = c * 32 + 2 * e + u;  // column within this warpgroup's 64
+                const float sc = __uint_as_float(cur[2 * e + u]);
+                float pe, fac = 1.f;
+                if constexpr (CAP) {
+                  const float y = softcap_log2(sc, cap_k1, cap_c2);
+                  const float tt = y * cap_ic2;
+                  fac = fmaf(-tt, tt, 1.f);
+                  pe = ex2_approx(y - my_l2[ql]);
+                } else {
+                  pe = ex2_approx(fmaf(sc, sl2, -my_l2[ql]));
                 }
-                pk[e] = pack2<T>(pr[0], pr[1]);
-                dk2[e] = pack2<T>(dr[0], dr[1]);
+                if (masked && (cb + ql < q_lo || cb + ql >= q_hi)) pe = 0.f;
+                pr[u] = pe;
+                pf[u] = pe * fac;
               }
-              const int chunk = c >> 1, g0 = (c & 1) * 4;
-#pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                const uint32_t off = chunk * kChunkBytes + sw128_offset(r, g0 + u);
-                *reinterpret_cast<uint4*>(pt_s + off) = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-                *reinterpret_cast<uint4*>(ds_s + off) =
-                    make_uint4(dk2[4 * u], dk2[4 * u + 1], dk2[4 * u + 2], dk2[4 * u + 3]);
-              }
+              pk[e] = pack2<T>(pr[0], pr[1]);
+              if constexpr (CAP) pf_keep[c][e] = pack2<T>(pf[0], pf[1]);
             }
+            tmem_st16_async(rp + c * 16, pk);
+          }
+          tmem_wait_st();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_full);
+        // Pass 2: dS^T = P^T (dP^T - Delta) into this warpgroup's 64-column
+        // chunk of the dS^T buffer, once dP^T is ready and this warp's
+        // previous dQ boxes have been read out of its rows.
+        if (lane == 0) bulk_wait_group_read0();
+        __syncwarp();
+        if (!wait_bar(&dp_full, gstep & 1, ctl)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t dpv[32];
+          uint32_t pw[16];
+          tmem_ld32_async(rr + c * 32, dpv);
+          if constexpr (CAP) {
+            tmem_wait_ld32(dpv);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) pw[e] = pf_keep[c][e];
           } else {
-#pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
-              uint32_t sv[32];
-              tmem_ld32(rs + c * 32, sv);
-              uint32_t pk[16], pfk[16];
-#pragma unroll
-              for (int e = 0; e < 16; ++e) {
-                float pr[2], pf[2];
-#pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                  const int qc = c * 32 + 2 * e + u;
-                  float fe;
-                  float pe = prob(__uint_as_float(sv[2 * e + u]), my_lse[qc], fe);
-                  if (masked && (qc < q_lo || qc >= q_hi)) pe = 0.f;
-                  pr[u] = pe;
-                  pf[u] = pe * fe;
-                }
-                pk[e] = pack2<T>(pr[0], pr[1]);
-                if constexpr (CAP) pfk[e] = pack2<T>(pf[0], pf[1]);
-              }
-              const int chunk = c >> 1, g0 = (c & 1) * 4;
-#pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                const uint32_t off = chunk * kChunkBytes + sw128_offset(r, g0 + u);
-                *reinterpret_cast<uint4*>(pt_s + off) = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-              }
-              // With CAP, P^T (1 - tanh^2) waits in TMEM (the dS^T buffer is
-              // P^T's own in this plan) for the second pass.
-              if constexpr (CAP) tmem_st16(tmem + lane_base + C::T_PF + c * 16, pfk);
-            }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&p_full);
-            if (!wait_bar(&dp_full, gstep & 1, ctl) || !wait_bar(&pt_read, gstep & 1, ctl)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-#pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
-              uint32_t pv[32];
-              tmem_ld32(rp + c * 32, pv);
-              const int chunk = c >> 1, g0 = (c & 1) * 4;
-              uint32_t dk2[16], pfw[16];
-              if constexpr (CAP) tmem_ld16(tmem + lane_base + C::T_PF + c * 16, pfw);
-#pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                const uint4 pp = CAP ? make_uint4(pfw[4 * u], pfw[4 * u + 1], pfw[4 * u + 2], pfw[4 * u + 3])
-                                     : *reinterpret_cast<const uint4*>(pt_s + chunk * kChunkBytes + sw128_offset(r, g0 + u));
-                const uint32_t pw[4] = {pp.x, pp.y, pp.z, pp.w};
-#pragma unroll
-                for (int e2 = 0; e2 < 4; ++e2) {
-                  const int e = 4 * u + e2;
-                  float2 pf = unpack2<T>(pw[e2]);
-                  const int qc = c * 32 + 2 * e;
-                  dk2[e] = pack2<T>(pf.x * (__uint_as_float(pv[2 * e]) - my_dl[qc]),
-                                       pf.y * (__uint_as_float(pv[2 * e + 1]) - my_dl[qc + 1]));
-                }
-              }
-#pragma unroll
-              for (int u = 0; u < 4; ++u)
-                *reinterpret_cast<uint4*>(ds_s + chunk * kChunkBytes + sw128_offset(r, g0 + u)) =
-                    make_uint4(dk2[4 * u], dk2[4 * u + 1], dk2[4 * u + 2], dk2[4 * u + 3]);
-            }
+            tmem_ld16_async(rp + c * 16, pw);
+            tmem_wait_ld32_16(dpv, pw);
           }
-          fence_proxy_async_smem();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&ds_full);
+          uint32_t dk2[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int ql = c * 32 + 2 * e;
+            const float2 pf = unpack2<T>(pw[e]);
+            dk2[e] = pack2<T>(pf.x * (__uint_as_float(dpv[2 * e]) - my_dl[ql]),
+                              pf.y * (__uint_as_float(dpv[2 * e + 1]) - my_dl[ql + 1]));
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            *reinterpret_cast<uint4*>(ds_s + sw128_offset(r, c * 4 + u)) =
+                make_uint4(dk2[4 * u], dk2[4 * u + 1], dk2[4 * u + 2], dk2[4 * u + 3]);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ds_full);
+        // This warp's share of the dQ read-out: chunks 0-1 (warps 4-7) or 4-5
+        // (warps 12-15), staged in its own rows of the dS^T buffer, which the
+        // dK and dQ products have finished reading when dQ is ready.
+        if (!dq_readout(t, k, gstep, wq, half ? 4 : 0, box)) {
+          ok = false;
+          break;
         }
       }
       if (!ok) break;
-      // dK / dV epilogue for this key tile.
+      // dV (warps 4-7) or dK (warps 12-15, scale applied) of this key tile.
       if (!wait_bar(&acc_done, nz & 1, ctl)) break;
       tc_fence_after();
+      const int nch = half ? DQK / 32 : DV / 32;
+      const float sc = half ? p.scale : 1.f;
+      T* row = half ? dk_row : dv_row;
 #pragma unroll 1
-      for (int c = 0; c < DV / 32; ++c) {
+      for (int c = 0; c < nch; ++c) {
         uint32_t a[32];
-        tmem_ld32(tmem + lane_base + C::T_DV + c * 32, a);
+        tmem_ld32(tmem + lane_base + (half ? C::T_DK : C::T_DV) + c * 32, a);
         if (valid) {
-          uint4* dst = reinterpret_cast<uint4*>(dv_row + c * 32);
-#pragma unroll
-          for (int u = 0; u < 4; ++u)
-            dst[u] = make_uint4(pack2<T>(__uint_as_float(a[8 * u]), __uint_as_float(a[8 * u + 1])),
-                                pack2<T>(__uint_as_float(a[8 * u + 2]), __uint_as_float(a[8 * u + 3])),
-                                pack2<T>(__uint_as_float(a[8 * u + 4]), __uint_as_float(a[8 * u + 5])),
-                                pack2<T>(__uint_as_float(a[8 * u + 6]), __uint_as_float(a[8 * u + 7])));
-        }
-      }
-      const float sc = p.scale;
-#pragma unroll 1
-      for (int c = 0; c < DQK / 32; ++c) {
-        uint32_t a[32];
-        tmem_ld32(tmem + lane_base + C::T_DK + c * 32, a);
-        if (valid) {
-          uint4* dst = reinterpret_cast<uint4*>(dk_row + c * 32);
+          uint4* dst = reinterpret_cast<uint4*>(row + c * 32);
 #pragma unroll
           for (int u = 0; u < 4; ++u)
             dst[u] = make_uint4(pack2<T>(__uint_as_float(a[8 * u]) * sc, __uint_as_float(a[8 * u + 1]) * sc),
@@ -535,51 +527,21 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_kernel(const __grid_constant_
       if (lane == 0) mbar_arrive(&acc_free);
       ++nz;
     }
-  } else if (warp >= 8) {
-    // ------------------------------------------------------------ dQ read-out
+    if (lane == 0) bulk_wait_group0();
+  } else if (warp >= 8 && warp < 12) {
+    // ------------------------------------------------------------ dQ read-out, chunks 2-3
     const int wq = warp - 8;
-    const uint32_t lane_base = (uint32_t)(32 * wq) << 16;
-    uint8_t* stg = smem + C::STG_OFF + wq * 4096;
+    uint8_t* box = smem + C::STG_OFF + wq * 4096;
     uint32_t gstep = 0;
     bool ok = true;
     for (int wi = 0; wi * (int)gridDim.x < total && ok; ++wi) {
       const int w = snake_item(wi);
       if (w >= total) continue;
       const BwdItem t = bwd_decode(p, w);
-      if (t.k1 == t.k0) continue;
-      {
-        for (int k = t.k0; k < t.k1; ++k, ++gstep) {
-          const int h = t.hk * G + k / t.nqt, qt = t.qt0 + k % t.nqt;
-          if (!wait_bar(&dq_full, gstep & 1, ctl)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t rq = tmem + lane_base + (C::DUAL ? ((gstep & 1) ? C::T_B : C::T_A) : C::T_A);
-          const int fq = t.cq0 + qt * kBM + 32 * wq, bq = fq / p.seg.Sq, sq = fq - bq * p.seg.Sq;
-#pragma unroll 1
-          for (int c = 0; c < DQK / 32; ++c) {
-            uint32_t a[32];
-            tmem_ld32(rq + c * 32, a);
-            if (c > 0) {
-              if (lane == 0) bulk_wait_group_read0();
-              __syncwarp();
-            }
-#pragma unroll
-            for (int u = 0; u < 8; ++u)
-              *reinterpret_cast<uint4*>(stg + sw128_offset(lane, u)) =
-                  make_uint4(a[4 * u], a[4 * u + 1], a[4 * u + 2], a[4 * u + 3]);
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-              tma_reduce_add_4d(&p.tm_dq, stg, c * 32, sq, h, bq);
-              bulk_commit_group();
-            }
-          }
-          if (lane == 0) bulk_wait_group_read0();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&dq_free);
+      for (int k = t.k0; k < t.k1; ++k, ++gstep) {
+        if (!dq_readout(t, k, gstep, wq, 2, box)) {
+          ok = false;
+          break;
         }
       }
     }

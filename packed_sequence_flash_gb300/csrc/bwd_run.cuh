@@ -33,7 +33,7 @@ cudaError_t run_single(const BwdParams& p, int grid, cudaStream_t st) {
   cudaError_t e =
       cudaFuncSetAttribute(attn_bwd_kernel<T, DQK, DV, CAP>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  attn_bwd_kernel<T, DQK, DV, CAP><<<grid, 384, smem, st>>>(p);
+  attn_bwd_kernel<T, DQK, DV, CAP><<<grid, 512, smem, st>>>(p);
   return cudaGetLastError();
 }
 template <typename T, bool CAP>
