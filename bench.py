@@ -77,6 +77,7 @@ def ncu_traffic(kernel: str, workload: str):
 KERNEL_SOURCES = {
     "attn_fwd_duo_kernel": ("fwd.cuh", "fwd_duo.cuh", "common.cuh", "ptx.cuh"),
     "attn_fwd_kernel": ("fwd.cuh", "common.cuh", "ptx.cuh"),
+    "attn_fwd_pair_kernel": ("fwd.cuh", "fwd_pair.cuh", "common.cuh", "ptx.cuh"),
     "attn_bwd_dual_kernel": ("bwd.cuh", "bwd_dual.cuh", "common.cuh", "ptx.cuh"),
     "attn_bwd_kernel": ("bwd.cuh", "common.cuh", "ptx.cuh"),
     "attn_bwd_wide_kernel": ("bwd.cuh", "bwd_wide.cuh", "common.cuh", "ptx.cuh"),
@@ -93,7 +94,12 @@ def kernel_source_hash(kernel: str) -> str:
 
 def main_kernels(dqk: int, dv: int) -> tuple[str, str]:
     """Names of the forward and backward kernels the library runs for these head dims."""
-    fwd = "attn_fwd_duo_kernel" if dqk == dv and dqk in (64, 128) else "attn_fwd_kernel"
+    if dqk == dv and dqk in (64, 128):
+        fwd = "attn_fwd_duo_kernel"
+    elif (dqk, dv) == (192, 128):
+        fwd = "attn_fwd_pair_kernel"
+    else:
+        fwd = "attn_fwd_kernel"
     if dqk <= 128 and dv <= 128:
         bwd = "attn_bwd_dual_kernel"
     elif dqk == 512 and dv == 512:

@@ -333,7 +333,10 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, void* out, float*
                     (Dqk == 64 || Dqk == 128))
                        ? G
                        : 1;
-  const int qrows = kBM / pack;
+  // Dqk = 192, Dv = 128 runs two 128-row halves of a 256-row item side by side
+  // (attn_fwd_pair_kernel); the schedule then lists 256-row tiles.
+  const bool pair = Dqk == 192 && Dv == 128;
+  const int qrows = pair ? 2 * kBM : kBM / pack;
   const int64_t q_rows = (int64_t)B * Sq, k_rows = (int64_t)B * Sk;
   if (q_rows == 0) return PSF_OK;
   if (!q || !out || !lse || (k_rows > 0 && (!k || !v))) return fail(PSF_EINVAL, "null tensor pointer");
@@ -369,7 +372,7 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, void* out, float*
 
   FwdParams p;
   memset(&p, 0, sizeof(p));
-  if ((rc = make_map16(&p.tm_q, q, Dqk, Sq, Hq, B, vq, 64, dtype, qrows, pack))) return rc;
+  if ((rc = make_map16(&p.tm_q, q, Dqk, Sq, Hq, B, vq, 64, dtype, pair ? kBM : qrows, pack))) return rc;
   // The two-CTA kernel (head dims 64, 128) stores out in 32 x 32 boxes.
   if (Dqk == Dv && (Dv == 64 || Dv == 128) &&
       (rc = make_map16(&p.tm_o, out, Dv, Sq, Hq, B, vo, 32, dtype, 32, 1, CU_TENSOR_MAP_SWIZZLE_64B)))

@@ -4,6 +4,7 @@
 
 #include "fwd.cuh"
 #include "fwd_duo.cuh"
+#include "fwd_pair.cuh"
 
 namespace psf {
 namespace fwd_run {
@@ -26,11 +27,20 @@ cudaError_t run_duo(const FwdParams& p, int grid, cudaStream_t st) {
   attn_fwd_duo_kernel<T, D, CAP><<<grid, 192, smem, st>>>(p);
   return cudaGetLastError();
 }
+template <typename T, int DQK, int DV, bool CAP>
+cudaError_t run_pair(const FwdParams& p, int grid, cudaStream_t st) {
+  const int smem = FwdPairCfg<DQK, DV>::SMEM_BYTES;
+  cudaError_t e =
+      cudaFuncSetAttribute(attn_fwd_pair_kernel<T, DQK, DV, CAP>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  attn_fwd_pair_kernel<T, DQK, DV, CAP><<<grid, 320, smem, st>>>(p);
+  return cudaGetLastError();
+}
 template <typename T, bool CAP>
 cudaError_t run_any(const FwdParams& p, int dqk, int dvc, int grid, cudaStream_t st) {
   if (dqk == 64 && dvc == 64) return run_duo<T, 64, CAP>(p, grid, st);
   if (dqk == 128 && dvc == 128) return run_duo<T, 128, CAP>(p, grid, st);
-  if (dqk == 192 && dvc == 128) return run<T, 192, 128, CAP>(p, grid, st);
+  if (dqk == 192 && dvc == 128) return run_pair<T, 192, 128, CAP>(p, grid, st);
   if (dqk == 512 && dvc == 256) return run<T, 512, 256, CAP>(p, grid, st);
   return cudaErrorInvalidValue;
 }
