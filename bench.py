@@ -58,13 +58,20 @@ CPU_SAMPLE_GFLOP = 300.0
 REF_STEP_GFLOP = 100.0
 FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 256 << 20
-# dram__bytes_read.sum + dram__bytes_write.sum per launch of a main kernel from
-# one ncu capture: (kernel, workload) -> (hash of the kernel's sources when
-# captured, bytes). Reported as null for other workloads and once the sources
-# change.
+# dram__bytes_read.sum + dram__bytes_write.sum of a main kernel per step (the
+# sum over the step's launches of it) from one ncu capture: (kernel, workload)
+# -> (hash of the kernel's sources when captured, bytes). Reported as null for
+# other workloads and once the sources change.
 NCU_TRAFFIC = {
-    ("attn_bwd_dual_kernel", "cfg2_doc_causal_t8192_d128"): ("a26bda6aae0f3cb4", 405444608),
-    ("attn_fwd_duo_kernel", "cfg2_doc_causal_t8192_d128"): ("ba5c514a195b41fb", 53346304),
+    # the document path's default: a KV head's query heads packed into one tile
+    ("attn_bwd_dual_kernel", "cfg5_doc_causal_t65536_w4096"): ("74d26f9003e23c8c", 40045062400),
+    ("attn_fwd_duo_kernel", "cfg5_doc_causal_t65536_w4096"): ("ba5c514a195b41fb", 3784822528),
+    ("attn_bwd_dual_kernel", "cfg2_doc_causal_t8192_d128"): ("74d26f9003e23c8c", 359169280),
+    ("attn_fwd_duo_kernel", "cfg2_doc_causal_t8192_d128"): ("ba5c514a195b41fb", 52814080),
+    ("attn_bwd_kernel", "cfg4_doc_causal_shard_dqk192_dv128"): ("64e9dca48875161a", 790401792),
+    ("attn_fwd_pair_kernel", "cfg4_doc_causal_shard_dqk192_dv128"): ("cc80d554cb59b181", 190336512),
+    ("attn_bwd_wide_kernel", "cfg3_dense_causal_n4096_d512"): ("bc3f0b6b52c5de97", 1021756672),
+    ("attn_fwd_kernel", "cfg3_dense_causal_n4096_d512"): ("c5813fd46184e0a7", 127845376),
 }
 
 
@@ -612,7 +619,7 @@ def our_arm(args):
                 hdst.copy_(r, non_blocking=True)
         keep[b] = results
 
-    for i in range(nbuf):  # warm the pipeline (pinned buffers, allocator)
+    for i in range(2 * nbuf):  # warm the pipeline (pinned buffers, the allocator's blocks for in-flight results)
         e2e_step(i)
     torch.cuda.synchronize()
     e2e_steps = max(3, min(args.steps, 50))
@@ -720,9 +727,9 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--softcap", type=float, default=None,
                     help="cap the logits as softcap * tanh(logit / softcap) (off by default)")
-    ap.add_argument("--pack-gqa", action="store_true",
-                    help="forward and backward with a KV head's query heads packed into one tile (for short "
-                         "documents, --config 6)")
+    ap.add_argument("--pack-gqa", action=argparse.BooleanOptionalAction, default=True,
+                    help="forward and backward with a KV head's query heads packed into one tile where the shape "
+                         "allows it (the default; same results, faster on packed documents)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

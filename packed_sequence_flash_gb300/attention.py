@@ -418,7 +418,7 @@ def grad_add_live_rows(dst, src, cu_q, cu_k, dev_meta=None):
 # document-causal composition [fa4 page, document_causal_fa4_attention]
 
 def document_causal_attention(q, k, v, q_doc_ids, kv_doc_ids, q_global_start, scale, window=None, skip_pad=True,
-                              pack_gqa=False, softcap=None):
+                              pack_gqa=True, softcap=None):
     """Causal per-document attention of a local query shard against global keys.
 
     q [B, Hq, Lq, Dqk], k [B, Hkv, Sk, Dqk], v [B, Hkv, Sk, Dv] (or packed
@@ -430,8 +430,10 @@ def document_causal_attention(q, k, v, q_doc_ids, kv_doc_ids, q_global_start, sc
     queries, so the attention writes their zero rows itself and computes no
     padding pairs; False runs padding runs as ordinary segments and zeroes
     the padding queries afterwards with pad_fixup (q_doc_ids is read only then).
-    pack_gqa: the forward packs a KV head's query heads into one tile (short
-    documents). softcap > 0 caps the logits (pass the same value to the backward).
+    pack_gqa (default): the forward packs a KV head's query heads into one
+    tile where the shape allows it (head dims 64 and 128); the results are the
+    same and packed documents run faster; False takes one head per tile.
+    softcap > 0 caps the logits (pass the same value to the backward).
     """
     layout = "thd" if q.dim() == 3 else "bhsd"
     if kv_doc_ids.dim() == 1:
@@ -448,8 +450,11 @@ def document_causal_attention(q, k, v, q_doc_ids, kv_doc_ids, q_global_start, sc
 
 
 def document_causal_attention_backward(dout, q, k, v, out, lse, segments, scale, window=None, softcap=None,
-                                       pack_gqa=False):
-    """Backward of document_causal_attention from its out/lse -> (dq, dk, dv)."""
+                                       pack_gqa=True):
+    """Backward of document_causal_attention from its out/lse -> (dq, dk, dv).
+    pack_gqa (default): a step takes the query heads of a KV head together where
+    the shape allows it (head dims up to 128, 2 or 4 query heads per KV head, no
+    softcap); same results."""
     layout = "thd" if q.dim() == 3 else "bhsd"
     cu_q, cu_k, meta = segments
     return attn_varlen_bwd(dout, q, k, v, out, lse, cu_q, cu_k, -1, -1, scale, True, window, dev_meta=meta,

@@ -94,6 +94,11 @@ def test_workload2_full_size_every_row(seed):
     _doc_full(2, seed=seed, every_row=True)
 
 
+def test_workload2_full_size_every_row_packed_heads():
+    # the document path's default: a KV head's query heads share a tile
+    _doc_full(2, every_row=True, pack_gqa=True)
+
+
 def test_workload4_full_size_shard_unequal_dims_every_row():
     _doc_full(4, every_row=True)
 
