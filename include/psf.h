@@ -212,8 +212,9 @@ int psf_attn_varlen_fwd_noalloc(const void* q, const void* k, const void* v, voi
  *  strides: NULL, or 24 element strides (batch, head, row) of q, k, v, out,
  *  dout, dq, dk, dv.
  *  workspace: psf_attn_bwd_workspace_size(Tq, Tk, nseg, Hq, Hkv, Dqk, Dv) bytes
- *  (holds the fp32 dQ, dK and dV accumulators, Delta = rowsum(dO * out) and the
- *  tile schedule).
+ *  (holds the fp32 dQ accumulator, Delta = rowsum(dO * out), the tile schedule
+ *  and, for head dims up to 128, the fp32 dK/dV partial sums of key tiles cut
+ *  across SMs; its size grows with Tq, not with Tk beyond the schedule).
  */
 int psf_attn_varlen_bwd(const void* dout, const void* q, const void* k, const void* v, const void* out,
                         const float* lse, void* dq, void* dk, void* dv, const int32_t* cu_q, const int32_t* cu_k,
@@ -292,10 +293,10 @@ int psf_build_doc_segments(const int32_t* kv_doc_ids, int B, int Sk, int q_lengt
  * Dense-kernel eligibility of one ring chunk, on the GPU.
  *                           [cp_attention page, `_build_packed_ring_segments`
  *                            (the dense_local / dense_cross flags and pad_rows)
- *                            and `_chunk_dense_eligible`; the row predicates
- *                            "exactly one document with no padding" and "real
- *                            tokens are one document forming a contiguous
- *                            prefix, padding a trailing suffix"]
+ *                            and `_chunk_dense_eligible`; the row predicates:
+ *                            one document and no padding, or the real tokens
+ *                            one document that forms a contiguous prefix with
+ *                            padding only as a trailing suffix]
  *  kv_doc_ids: int32 [B, S] (1-based ids, 0 = padding); the query shard is
  *  [q_start, q_start + q_length) and the key chunk [k_start, k_start + k_length)
  *  of every row. Writes flags, a device int32[2], 1 = eligible:
@@ -318,8 +319,8 @@ int psf_chunk_dense_flags(const int32_t* kv_doc_ids, int B, int S, int q_start, 
  * Zero the padding queries of a document-causal result: rows whose query
  * document id is 0 get out = 0 and lse = -inf.
  *                           [fa4 page, `document_causal_fa4_attention`:
- *                            "padding queries are zero"; cp_attention page,
- *                            lse "-inf for non-participating rows"]
+ *                            padding queries give zero output; cp_attention
+ *                            page: rows that take no part get lse = -inf]
  *  q_doc_ids: int32 [B, Lq]; out / lse in `layout` with S = Lq.
  */
 int psf_pad_fixup(void* out, float* lse, const int32_t* q_doc_ids, int layout, int B, int Lq, int Hq, int Dv,

@@ -13,7 +13,7 @@
  *    (natural log of the scaled logits). A query with no visible key gives
  *    out = 0 and lse = -inf.
  *      [nemo_automodel.components.attention.ffpa_attention, `_ffpa_varlen_fwd`,
- *       `_ffpa_dense_fwd`: "Returns (out[T,Hq,D], lse[Hq,T])", lse fp32]
+ *       `_ffpa_dense_fwd`: the return value, out [T, Hq, D] and an fp32 lse [Hq, T]]
  *  - visibility, "segments" mode: query row i and key row j of one segment
  *    (local indices, m queries and n keys, delta = n - m) see each other when
  *    (not causal or j <= i + delta) and (no window or j >= i + delta - W + 1):
@@ -28,8 +28,8 @@
  *    same maximal run of equal id as p, j <= p, and p - j < W if a window is
  *    set. Padding queries (id 0) give zero output and lse = -inf.
  *      [nemo_automodel.components.attention.fa4, `document_causal_fa4_attention`
- *       ("padding queries are zero") and module docstring bullet 2 ("query at
- *       global position p sees keys of its document up to p")]
+ *       (padding queries give zero output) and module docstring bullet 2 (a
+ *       query at global position p sees the keys of its own document up to p)]
  *  - softcap c > 0 (off by default): each logit z = scale * q . k becomes
  *    c * tanh(z / c) before the mask and the softmax, and the backward carries
  *    the factor 1 - tanh(z / c)^2 into dS.
@@ -41,8 +41,8 @@
  *      dV_j = sum_i P_ij dO_i, with dK/dV summed over the query heads that
  *      share a KV head (query head h uses KV head h / (Hq/Hkv)).
  *      [nemo_automodel.components.attention.ffpa_attention, `_ffpa_varlen_bwd`,
- *       `_ffpa_dense_bwd`: "using the caller-supplied out/lse", "dK/dV reduced
- *       to Hkv for GQA"]
+ *       `_ffpa_dense_bwd`: gradients from the out and lse the caller passes in,
+ *       dK/dV summed over the query heads of each KV head]
  *    dQ is computed row by row (per query) and dK/dV column by column (per key),
  *    so either can be evaluated on a sample of rows.
  *  - segment builder: every document run of a batch row (padding runs too) is
@@ -54,7 +54,7 @@
  *  - lse merge: l = logaddexp(l1, l2), o = o1 exp(l1 - l) + o2 exp(l2 - l);
  *    a row with both inputs -inf stays 0 with lse -inf.
  *      [nemo_automodel.components.models.gemma4_moe.cp_attention, the
- *       "-inf-safe online-softmax merge" docstring]
+ *       docstring of its online-softmax merge, which handles -inf]
  *  - cross-chunk segment builder: a query shard [q0, q0 + Lq) and an earlier
  *    key chunk [k0, k0 + Lk) (k0 + Lk <= q0) of every batch row; a document
  *    (a maximal run of one nonzero id) present in both pairs its shard queries
@@ -66,8 +66,8 @@
  *    its chunk keys), (the other shard queries x no keys); the middle one is
  *    empty when no document is shared.
  *      [nemo_automodel.components.models.gemma4_moe.cp_attention,
- *       `_build_packed_ring_segments`: "for each doc present in both", paired
- *       query and key tokens, cu_q[i] pairing cu_k[i]]
+ *       `_build_packed_ring_segments`: documents present in both the shard and
+ *       the chunk, their query and key tokens paired, cu_q[i] with cu_k[i]]
  *
  * Layouts: q [Tq, Hq, Dqk], k [Tk, Hkv, Dqk], v [Tk, Hkv, Dv], out [Tq, Hq, Dv],
  * lse [Hq, Tq], all row-major and contiguous, double precision.

@@ -228,44 +228,55 @@ size_t fwd_ws_layout(int64_t rows, int nseg, FwdWorkspace* w, void* base, int qr
 }
 
 struct BwdWorkspace {
-  int* n_items;
-  int* seg_prefix;
-  int4* items;
-  int item_cap;
+  BwdSchedule sc;
   float* delta;
   float* dq_acc;
-  float* dk_acc;
-  float* dv_acc;
+  float* pk;  // dK partial-sum slots [slot][Hkv][128][Dqk] (head dims <= 128)
+  float* pv;  // dV partial-sum slots [slot][Hkv][128][Dv]
 };
 // Heavy key tiles are split into at most this many sub-ranges' worth of work
-// per SM (see bwd_schedule_kernel); the item capacity follows from it.
+// per SM (see bwd_schedule_body); the item capacity follows from it.
 constexpr int kSplitPerSm = 2;
+// Partial-sum slots: a cut tile has more steps than the cap per sub-range,
+// steps * Hkv / (kSplitPerSm * sms) or more, and fewer than twice its steps
+// over that cap in sub-ranges, so all cut tiles' sub-ranges of one KV head
+// number fewer than 2 * kSplitPerSm * sms / Hkv.
+constexpr int bwd_slot_cap(int sms, int Hkv) { return 2 * kSplitPerSm * sms / Hkv + 2; }
 size_t bwd_ws_layout(int64_t q_rows, int64_t k_rows, int nseg, int Hq, int Hkv, int Dqk, int Dv, int sms,
                      BwdWorkspace* w, void* base) {
   const int64_t cap = (k_rows + kBN - 1) / kBN + nseg + (int64_t)kSplitPerSm * sms + 2;
+  // Only the head-dim <= 128 kernel cuts key tiles.
+  const int slot_cap = (Dqk <= 128 && Dv <= 128) ? bwd_slot_cap(sms, Hkv) : 0;
   size_t off = 256;
   const size_t prefix_off = off;
   off += align256(sizeof(int) * (size_t)(nseg + 2));
   const size_t items_off = off;
   off += align256(sizeof(int4) * (size_t)cap);
+  const size_t slot_off = off;
+  off += align256(sizeof(int) * (size_t)cap);
+  const size_t splits_off = off;
+  off += align256(sizeof(int4) * (size_t)(slot_cap / 2 + 1));
   const size_t delta_off = off;
   off += align256(sizeof(float) * (size_t)Hq * (size_t)q_rows);
   const size_t dq_off = off;
   off += align256(sizeof(float) * (size_t)q_rows * Hq * Dqk);
-  const size_t dk_off = off;
-  off += align256(sizeof(float) * (size_t)k_rows * Hkv * Dqk);
-  const size_t dv_off = off;
-  off += align256(sizeof(float) * (size_t)k_rows * Hkv * Dv);
+  const size_t pk_off = off;
+  off += align256(sizeof(float) * (size_t)slot_cap * Hkv * kBN * Dqk);
+  const size_t pv_off = off;
+  off += align256(sizeof(float) * (size_t)slot_cap * Hkv * kBN * Dv);
   if (w && base) {
     char* b = static_cast<char*>(base);
-    w->n_items = reinterpret_cast<int*>(b);
-    w->seg_prefix = reinterpret_cast<int*>(b + prefix_off);
-    w->items = reinterpret_cast<int4*>(b + items_off);
-    w->item_cap = (int)cap;
+    w->sc.n_items = reinterpret_cast<int*>(b);
+    w->sc.seg_prefix = reinterpret_cast<int*>(b + prefix_off);
+    w->sc.items = reinterpret_cast<int4*>(b + items_off);
+    w->sc.item_slot = reinterpret_cast<int*>(b + slot_off);
+    w->sc.splits = reinterpret_cast<int4*>(b + splits_off);
+    w->sc.item_cap = (int)cap;
+    w->sc.slot_cap = slot_cap;
     w->delta = reinterpret_cast<float*>(b + delta_off);
     w->dq_acc = reinterpret_cast<float*>(b + dq_off);
-    w->dk_acc = reinterpret_cast<float*>(b + dk_off);
-    w->dv_acc = reinterpret_cast<float*>(b + dv_off);
+    w->pk = reinterpret_cast<float*>(b + pk_off);
+    w->pv = reinterpret_cast<float*>(b + pv_off);
   }
   return off;
 }
@@ -450,8 +461,8 @@ int attn_bwd_impl(const void* dout, const void* q, const void* k, const void* v,
   if (dev->sms > kMaxSms) return fail(PSF_EUNSUPPORTED, "more than %d SMs", kMaxSms);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
-  // Head dims up to 128 run the kernel that adds dK/dV partial sums into fp32
-  // accumulators, which lets heavy key tiles be split across SMs.
+  // Head dims up to 128 run the kernel that can cut heavy key tiles across
+  // SMs, their sub-ranges' dK/dV partial sums added up by the convert.
   const bool accumulate = Dqk <= 128 && Dv <= 128;
   // Packed query heads: a step of the head-dim-<=-128 kernel takes the G = Hq / Hkv
   // query heads of its KV head, 128 / G rows each (G in {2, 4}, so that a dQ
@@ -473,17 +484,14 @@ int attn_bwd_impl(const void* dout, const void* q, const void* k, const void* v,
     none.cu_q = none.cu_k = nullptr;
     none.dev_meta = nullptr;
     none.nseg = 0;
-    cudaError_t e0 = launch_bwd_prep(none, Hq / Hkv, Hkv, 0, w.items, w.n_items, w.seg_prefix, w.item_cap,
-                                     dev->status, dout, vdo.sb, vdo.ss, vdo.sh, out, vo.sb, vo.ss, vo.sh, w.delta,
-                                     w.dq_acc, Hq, Dqk, Dv, nullptr, nullptr, dk, dv, vdk.sb, vdk.ss, vdk.sh, vdv.sb,
-                                     vdv.ss, vdv.sh, f16, st);
+    cudaError_t e0 = launch_bwd_prep(none, Hq / Hkv, Hkv, 0, w.sc, dev->status, dout, vdo.sb, vdo.ss, vdo.sh, out,
+                                     vo.sb, vo.ss, vo.sh, w.delta, w.dq_acc, Hq, Dqk, Dv, dk, dv, vdk.sb, vdk.ss,
+                                     vdk.sh, vdv.sb, vdv.ss, vdv.sh, f16, st);
     return e0 == cudaSuccess ? PSF_OK : cuda_fail(e0, "backward preparation launch");
   }
-  cudaError_t e = launch_bwd_prep(
-      g, Hq / Hkv, Hkv, accumulate ? kSplitPerSm * dev->sms : 0, w.items, w.n_items, w.seg_prefix, w.item_cap,
-      dev->status, dout, vdo.sb, vdo.ss, vdo.sh, out, vo.sb, vo.ss, vo.sh, w.delta, w.dq_acc, Hq, Dqk, Dv,
-      accumulate ? w.dk_acc : nullptr, accumulate ? w.dv_acc : nullptr, dk, dv, vdk.sb, vdk.ss, vdk.sh, vdv.sb,
-      vdv.ss, vdv.sh, f16, st);
+  cudaError_t e = launch_bwd_prep(g, Hq / Hkv, Hkv, accumulate ? kSplitPerSm * dev->sms : 0, w.sc, dev->status, dout,
+                                  vdo.sb, vdo.ss, vdo.sh, out, vo.sb, vo.ss, vo.sh, w.delta, w.dq_acc, Hq, Dqk, Dv, dk,
+                                  dv, vdk.sb, vdk.ss, vdk.sh, vdv.sb, vdv.ss, vdv.sh, f16, st);
   if (e != cudaSuccess) return cuda_fail(e, "backward preparation launch");
 
   if (k_rows > 0) {
@@ -497,11 +505,12 @@ int attn_bwd_impl(const void* dout, const void* q, const void* k, const void* v,
       if (r2) return fail(PSF_ECUDA, "cuTensorMapEncodeTiled failed (%d) for the dQ accumulator", r2);
     }
     if (accumulate) {
-      int r2 = make_tmap_4d(&p.tm_dk, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, w.dk_acc, Dqk, Sk, Hkv, B,
-                            (int64_t)Hkv * Dqk, Dqk, (int64_t)Sk * Hkv * Dqk, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B);
-      r2 |= make_tmap_4d(&p.tm_dv, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, w.dv_acc, Dv, Sk, Hkv, B, (int64_t)Hkv * Dv,
-                         Dv, (int64_t)Sk * Hkv * Dv, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B);
-      if (r2) return fail(PSF_ECUDA, "cuTensorMapEncodeTiled failed for the dK/dV accumulators");
+      const int ns = w.sc.slot_cap;
+      int r2 = make_tmap_4d(&p.tm_dk, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, w.pk, Dqk, kBN, Hkv, ns, Dqk,
+                            (int64_t)kBN * Dqk, (int64_t)Hkv * kBN * Dqk, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B);
+      r2 |= make_tmap_4d(&p.tm_dv, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, w.pv, Dv, kBN, Hkv, ns, Dv,
+                         (int64_t)kBN * Dv, (int64_t)Hkv * kBN * Dv, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B);
+      if (r2) return fail(PSF_ECUDA, "cuTensorMapEncodeTiled failed for the dK/dV partial-sum slots");
     }
     if ((rc = make_map16(&p.tm_k, k, Dqk, Sk, Hkv, B, vk, 64, dtype))) return rc;
     if ((rc = make_map16(&p.tm_v, v, Dv, Sk, Hkv, B, vv, 64, dtype))) return rc;
@@ -525,20 +534,21 @@ int attn_bwd_impl(const void* dout, const void* q, const void* k, const void* v,
     p.scale_log2 = scale * 1.4426950408889634f;
     p.softcap = softcap;
     p.pack = pack;
-    p.items = w.items;
-    p.n_items = w.n_items;
-    p.work_next = w.n_items + 1;
+    p.items = w.sc.items;
+    p.item_slot = w.sc.item_slot;
+    p.n_items = w.sc.n_items;
+    p.work_next = w.sc.n_items + 1;
     p.status = dev->status;
     p.limit_ns = g_wait_limit_ns;
     TimedLaunch tl;
     const bool timed = timing_begin(1, st, &tl);
-    e = launch_bwd(p, Dqk, Dv, dev->sms, w.item_cap, f16, st);
+    e = launch_bwd(p, Dqk, Dv, dev->sms, w.sc.item_cap, f16, st);
     if (timed) timing_end(&tl, st);
     if (e != cudaSuccess) return cuda_fail(e, "backward launch");
   }
-  e = launch_bwd_convert(w.dq_acc, dq, q_rows > 0, B, Sq, Hq, Dqk, vdq.sb, vdq.ss, vdq.sh,
-                         accumulate ? w.dk_acc : nullptr, dk, accumulate ? w.dv_acc : nullptr, dv, Sk, Hkv, Dv, vdk.sb,
-                         vdk.ss, vdk.sh, vdv.sb, vdv.ss, vdv.sh, scale, f16, st);
+  e = launch_bwd_convert(w.dq_acc, dq, q_rows > 0, B, Sq, Hq, Dqk, vdq.sb, vdq.ss, vdq.sh, g,
+                         accumulate && k_rows > 0 ? &w.sc : nullptr, w.pk, w.pv, dk, dv, Hkv, Dv, vdk.sb, vdk.ss,
+                         vdk.sh, vdv.sb, vdv.ss, vdv.sh, scale, f16, st);
   if (e != cudaSuccess) return cuda_fail(e, "convert launch");
   return PSF_OK;
 }

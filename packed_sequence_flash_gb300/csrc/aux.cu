@@ -96,7 +96,10 @@ __device__ void schedule_body(SegInfo g, int over_keys, int2* items, int* n_item
   const int max_k = g.dev_meta ? g.dev_meta[2] : g.max_k;
   const int Tq = g.B * g.Sq, Tk = g.B * g.Sk;
   hist[tid] = 0;
-  if (tid == 0) n_items[1] = 0;  // work counter of kernels that take items dynamically
+  if (tid == 0) {
+    n_items[1] = 0;  // work counter of kernels that take items dynamically
+    n_items[2] = 0;  // cut tiles
+  }
   if (tid == 0) bad = (g.cu_q && nseg >= 0 && (g.cu_q[0] != 0 || g.cu_k[0] != 0)) ? 1 : 0;
   __syncthreads();
   int carry = 0;
@@ -154,10 +157,14 @@ __device__ void schedule_body(SegInfo g, int over_keys, int2* items, int* n_item
 // (query head, query tile) steps when it holds more than its share of the
 // total (split_target > 0: aim at split_target sub-items' worth of steps),
 // heaviest first. Items are (segment, key tile, first step, end step).
+// The sub-ranges of a cut tile write their dK/dV partial sums to slots of
+// their own: item_slot[i] is item i's slot (-1: the tile is whole and its
+// unit writes dK/dV itself), and splits[0, n_items[2]) lists the cut tiles as
+// (segment, key tile, first slot, slot count) for the convert kernel.
 // Runs in one 1024-thread block (block 0 of bwd_prep_kernel).
-__device__ void bwd_schedule_body(SegInfo g, int G, int Hkv, int split_target,
-                                                                    int4* items, int* n_items, int* seg_prefix,
-                                                                    int item_cap, int* status) {
+__device__ void bwd_schedule_body(SegInfo g, int G, int Hkv, int split_target, int4* items, int* item_slot,
+                                  int4* splits, int slot_cap, int* n_items, int* seg_prefix, int item_cap,
+                                  int* status) {
   __shared__ int hist[kBuckets];
   __shared__ int start[kBuckets];
   __shared__ int bad;
@@ -173,7 +180,10 @@ __device__ void bwd_schedule_body(SegInfo g, int G, int Hkv, int split_target,
   // head, or kBM / qrows heads packed into one tile.
   const int Gs = G / (kBM / g.qrows);
   hist[tid] = 0;
-  if (tid == 0) n_items[1] = 0;  // work counter of kernels that take items dynamically
+  if (tid == 0) {
+    n_items[1] = 0;  // work counter of kernels that take items dynamically
+    n_items[2] = 0;  // cut tiles
+  }
   if (tid == 0) {
     bad = (g.cu_q && nseg >= 0 && (g.cu_q[0] != 0 || g.cu_k[0] != 0)) ? 1 : 0;
     total_steps = 0;
@@ -219,20 +229,26 @@ __device__ void bwd_schedule_body(SegInfo g, int G, int Hkv, int split_target,
     const unsigned long long want = (total_steps * (unsigned long long)Hkv + split_target - 1) / split_target;
     smax = (int)(want < 4 ? 4 : (want > 0x7fffffffull ? 0x7fffffffull : want));
   }
-  int nsub_total = 0;
+  int nsub_total = 0, slots_mine = 0, cut_mine = 0;
   for (int x = tid; x < carry; x += kScanThreads) {
     const int s = find_segment(pref, nseg, x);
     const int steps = Gs * tile_cost(g, s, x - pref[s], 1);
     const int nsub = steps == 0 ? 1 : (int)(((long long)steps + smax - 1) / smax);
     nsub_total += nsub;
+    if (nsub > 1) {
+      slots_mine += nsub;
+      ++cut_mine;
+    }
     for (int i = 0; i < nsub; ++i) {
       const int c = (int)((long long)steps * (i + 1) / nsub - (long long)steps * i / nsub);
       atomicAdd(&hist[min(c, kBuckets - 1)], 1);
     }
   }
-  int n_all;
+  int n_all, slots_all, cut_all;
   block_excl_scan(nsub_total, &n_all);
-  if (n_all > item_cap) {
+  int slot_next = block_excl_scan(slots_mine, &slots_all);
+  int cut_next = block_excl_scan(cut_mine, &cut_all);
+  if (n_all > item_cap || slots_all > slot_cap) {
     if (tid == 0) {
       record_status(status, kStatusDeviceArgs);
       *n_items = 0;
@@ -250,13 +266,20 @@ __device__ void bwd_schedule_body(SegInfo g, int G, int Hkv, int split_target,
     const int t = x - pref[s];
     const int steps = Gs * tile_cost(g, s, t, 1);
     const int nsub = steps == 0 ? 1 : (int)(((long long)steps + smax - 1) / smax);
+    if (nsub > 1) splits[cut_next++] = make_int4(s, t, slot_next, nsub);
     for (int i = 0; i < nsub; ++i) {
       const int a = (int)((long long)steps * i / nsub), e = (int)((long long)steps * (i + 1) / nsub);
       const int b = min(e - a, kBuckets - 1);
-      items[start[b] + atomicAdd(&hist[b], 1)] = make_int4(s, t, a, e);
+      const int at = start[b] + atomicAdd(&hist[b], 1);
+      items[at] = make_int4(s, t, a, e);
+      item_slot[at] = nsub > 1 ? slot_next + i : -1;
     }
+    if (nsub > 1) slot_next += nsub;
   }
-  if (tid == 0) *n_items = n_all;
+  if (tid == 0) {
+    *n_items = n_all;
+    n_items[2] = cut_all;
+  }
 }
 
 // out = 0, lse = -inf for query rows at or past cu_q[nseg]; blocks bid of nblk.
@@ -474,7 +497,7 @@ constexpr int kDeltaUnroll = 2;
 template <typename E>
 __device__ void bwd_pre_body(SegInfo g, const E* dout, int64_t d_sb, int64_t d_ss, int64_t d_sh, const E* out,
                              int64_t o_sb, int64_t o_ss, int64_t o_sh, float* delta, float* dq_acc, int Hq, int Dqk, int Dv,
-                             float* dk_acc, float* dv_acc, uint16_t* dk, uint16_t* dv, int64_t k_sb,
+                             uint16_t* dk, uint16_t* dv, int64_t k_sb,
                              int64_t k_ss, int64_t k_sh, int64_t v_sb, int64_t v_ss, int64_t v_sh, int Hkv, int bid,
                              int nblk) {
   const int64_t rows = (int64_t)g.B * g.Sq;
@@ -535,13 +558,9 @@ __device__ void bwd_pre_body(SegInfo g, const E* dout, int64_t d_sb, int64_t d_s
   const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
   const int64_t n4 = rows * Hq * Dqk / 4;
   for (int64_t x = tid; x < n4; x += nthr) reinterpret_cast<float4*>(dq_acc)[x] = z4;
+  // dK / dV rows inside segments are written by the attention kernel (or the
+  // convert, for cut key tiles); rows past the last segment are zero.
   const int64_t krows_all = (int64_t)g.B * g.Sk;
-  if (dk_acc) {
-    const int64_t nk4 = krows_all * Hkv * Dqk / 4, nv4 = krows_all * Hkv * Dv / 4;
-    for (int64_t x = tid; x < nk4; x += nthr) reinterpret_cast<float4*>(dk_acc)[x] = z4;
-    for (int64_t x = tid; x < nv4; x += nthr) reinterpret_cast<float4*>(dv_acc)[x] = z4;
-    return;
-  }
   const int first = max(cu_k_at(g, seg_count(g)), 0);  // clamped as in fwd_tail_body
   const int64_t krows = krows_all - first;
   if (krows > 0) {
@@ -591,26 +610,65 @@ __device__ __forceinline__ void convert_row(const float* __restrict__ acc, E* __
   }
 }
 
-// dQ = scale * dQacc, and (when accumulated) dK = scale * dKacc, dV = dVacc;
-// a warp per packed row of dQ, then of dK, then of dV.
+// dK = scale * (sum of the partial-sum slots) and dV = (sum of its slots) for
+// the key rows of every cut key tile, a warp per (tile, KV head, key row),
+// then dQ = scale * dQacc, a warp per packed row. The cut tiles come first so
+// that their short dependent reads overlap the dQ rows' streaming. A slot
+// holds [Hkv][128][D] fp32 rows.
 template <typename E>
 __global__ void __launch_bounds__(256, 4) bwd_convert_kernel(const float* dq_acc, E* dq, int64_t nq, int Sq, int Hq, int Dqk,
-                                   int64_t q_sb, int64_t q_ss, int64_t q_sh, const float* dk_acc, E* dk,
-                                   const float* dv_acc, E* dv, int64_t nk, int Sk, int Hkv, int Dv,
+                                   int64_t q_sb, int64_t q_ss, int64_t q_sh, SegInfo g, const int4* splits,
+                                   const int* n_split, const float* pk, const float* pv, E* dk, E* dv, int Hkv, int Dv,
                                    int64_t k_sb, int64_t k_ss, int64_t k_sh, int64_t v_sb, int64_t v_ss, int64_t v_sh,
                                    float scale) {
-  const int64_t nkr = dk_acc ? nk : 0;
-  const int64_t total = nq + 2 * nkr;
   const int64_t nw = (int64_t)gridDim.x * (blockDim.x / 32);
-  for (int64_t r = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) / 32; r < total; r += nw) {
-    const bool is_q = r < nq, is_k = !is_q && r < nq + nkr;
-    const float* acc = is_q ? dq_acc : is_k ? dk_acc : dv_acc;
-    E* dst = is_q ? dq : is_k ? dk : dv;
-    const int64_t f = is_q ? r : is_k ? r - nq : r - nq - nkr;
-    const int Sr = is_q ? Sq : Sk, H = is_q ? Hq : Hkv, D = is_q || is_k ? Dqk : Dv;
-    const int64_t sb = is_q ? q_sb : is_k ? k_sb : v_sb, ss = is_q ? q_ss : is_k ? k_ss : v_ss;
-    const int64_t sh = is_q ? q_sh : is_k ? k_sh : v_sh;
-    convert_row(acc, dst, f, Sr, H, D, sb, ss, sh, is_q || is_k ? scale : 1.f);
+  const int lane = threadIdx.x & 31;
+  const int64_t per_tile = (int64_t)Hkv * kBN;
+  const int64_t ncut = splits ? (int64_t)(*n_split) * per_tile : 0;
+  for (int64_t x = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) / 32; x < ncut + nq; x += nw) {
+    if (x >= ncut) {
+      convert_row(dq_acc, dq, x - ncut, Sq, Hq, Dqk, q_sb, q_ss, q_sh, scale);
+      continue;
+    }
+    const int e = (int)(x / per_tile);
+    const int rem = (int)(x - e * per_tile), hk = rem / kBN, r = rem % kBN;
+    const int4 sp = splits[e];
+    const int k0 = cu_k_at(g, sp.x), n = cu_k_at(g, sp.x + 1) - k0, j = sp.y * kBN + r;
+    if (j >= n) continue;
+    const int f = k0 + j, b = f / g.Sk, sr = f - b * g.Sk;
+    // Lane l holds elements [4l, 4l + 4) of the dK row and of the dV row; the
+    // slots' loads go out four at a time.
+    const bool on_k = lane * 4 < Dqk, on_v = lane * 4 < Dv;
+    const float* srck = pk + (((int64_t)sp.z * Hkv + hk) * kBN + r) * Dqk + lane * 4;
+    const float* srcv = pv + (((int64_t)sp.z * Hkv + hk) * kBN + r) * Dv + lane * 4;
+    const int64_t stk = (int64_t)Hkv * kBN * Dqk, stv = (int64_t)Hkv * kBN * Dv;
+    float4 ak = make_float4(0.f, 0.f, 0.f, 0.f), av = ak;
+    for (int i0 = 0; i0 < sp.w; i0 += 4) {
+      float4 lk[4], lv[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const bool in = i0 + u < sp.w;
+        lk[u] = in && on_k ? *reinterpret_cast<const float4*>(srck + (i0 + u) * stk) : make_float4(0.f, 0.f, 0.f, 0.f);
+        lv[u] = in && on_v ? *reinterpret_cast<const float4*>(srcv + (i0 + u) * stv) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        ak.x += lk[u].x;
+        ak.y += lk[u].y;
+        ak.z += lk[u].z;
+        ak.w += lk[u].w;
+        av.x += lv[u].x;
+        av.y += lv[u].y;
+        av.z += lv[u].z;
+        av.w += lv[u].w;
+      }
+    }
+    if (on_k)
+      *reinterpret_cast<uint2*>(dk + b * k_sb + (int64_t)sr * k_ss + hk * k_sh + lane * 4) =
+          make_uint2(pack2<E>(ak.x * scale, ak.y * scale), pack2<E>(ak.z * scale, ak.w * scale));
+    if (on_v)
+      *reinterpret_cast<uint2*>(dv + b * v_sb + (int64_t)sr * v_ss + hk * v_sh + lane * 4) =
+          make_uint2(pack2<E>(av.x, av.y), pack2<E>(av.z, av.w));
   }
 }
 
@@ -844,15 +902,16 @@ __global__ void __launch_bounds__(kScanThreads) fwd_prep_kernel(SegInfo g, int2*
 // latency behind that traffic.
 template <typename E>
 __global__ void __launch_bounds__(kScanThreads) bwd_prep_kernel(
-    SegInfo g, int G, int Hkv, int split_target, int4* items, int* n_items, int* seg_prefix, int item_cap, int* status,
-    const E* dout, int64_t d_sb, int64_t d_ss, int64_t d_sh, const E* out, int64_t o_sb, int64_t o_ss, int64_t o_sh,
-    float* delta, float* dq_acc, int Hq, int Dqk, int Dv, float* dk_acc, float* dv_acc, uint16_t* dk, uint16_t* dv,
-    int64_t k_sb, int64_t k_ss, int64_t k_sh, int64_t v_sb, int64_t v_ss, int64_t v_sh) {
+    SegInfo g, int G, int Hkv, int split_target, int4* items, int* item_slot, int4* splits, int slot_cap,
+    int* n_items, int* seg_prefix, int item_cap, int* status, const E* dout, int64_t d_sb, int64_t d_ss, int64_t d_sh,
+    const E* out, int64_t o_sb, int64_t o_ss, int64_t o_sh, float* delta, float* dq_acc, int Hq, int Dqk, int Dv,
+    uint16_t* dk, uint16_t* dv, int64_t k_sb, int64_t k_ss, int64_t k_sh, int64_t v_sb, int64_t v_ss, int64_t v_sh) {
   if (blockIdx.x == 0)
-    bwd_schedule_body(g, G, Hkv, split_target, items, n_items, seg_prefix, item_cap, status);
+    bwd_schedule_body(g, G, Hkv, split_target, items, item_slot, splits, slot_cap, n_items, seg_prefix, item_cap,
+                      status);
   else
-    bwd_pre_body(g, dout, d_sb, d_ss, d_sh, out, o_sb, o_ss, o_sh, delta, dq_acc, Hq, Dqk, Dv, dk_acc, dv_acc, dk, dv, k_sb, k_ss, k_sh,
-                 v_sb, v_ss, v_sh, Hkv, blockIdx.x - 1, gridDim.x - 1);
+    bwd_pre_body(g, dout, d_sb, d_ss, d_sh, out, o_sb, o_ss, o_sh, delta, dq_acc, Hq, Dqk, Dv, dk, dv, k_sb, k_ss,
+                 k_sh, v_sb, v_ss, v_sh, Hkv, blockIdx.x - 1, gridDim.x - 1);
 }
 
 int grid_for(int64_t work, int threads) {
@@ -908,29 +967,28 @@ cudaError_t launch_lse_merge(const void* o1, const float* l1, const void* o2, co
   return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_prep(const SegInfo& g, int G, int Hkv, int split_target, int4* items, int* n_items,
-                            int* seg_prefix, int item_cap, int* status, const void* dout, int64_t d_sb, int64_t d_ss,
-                            int64_t d_sh, const void* out, int64_t o_sb, int64_t o_ss, int64_t o_sh, float* delta,
-                            float* dq_acc, int Hq, int Dqk, int Dv, float* dk_acc, float* dv_acc, void* dk, void* dv,
-                            int64_t k_sb, int64_t k_ss, int64_t k_sh, int64_t v_sb, int64_t v_ss, int64_t v_sh, int f16,
-                            cudaStream_t st) {
+cudaError_t launch_bwd_prep(const SegInfo& g, int G, int Hkv, int split_target, const BwdSchedule& sc, int* status,
+                            const void* dout, int64_t d_sb, int64_t d_ss, int64_t d_sh, const void* out, int64_t o_sb,
+                            int64_t o_ss, int64_t o_sh, float* delta, float* dq_acc, int Hq, int Dqk, int Dv, void* dk,
+                            void* dv, int64_t k_sb, int64_t k_ss, int64_t k_sh, int64_t v_sb, int64_t v_ss,
+                            int64_t v_sh, int f16, cudaStream_t st) {
   // One 1024-thread block per SM fits (the schedule block's registers and
   // shared memory), so the fill takes one wave beside it.
-  const int64_t work = (int64_t)g.B * g.Sq * Hq * Dqk / 4 + (int64_t)g.B * g.Sk * Hkv * (Dqk + Dv) / 4;
+  const int64_t work = (int64_t)g.B * g.Sq * Hq * (Dqk + Dv) / 4;
   const int fill = min(grid_for(work, kScanThreads), 152 - 1);
   uint16_t* dk16 = static_cast<uint16_t*>(dk);
   uint16_t* dv16 = static_cast<uint16_t*>(dv);
   if (f16)
     bwd_prep_kernel<__half><<<1 + fill, kScanThreads, 0, st>>>(
-        g, G, Hkv, split_target, items, n_items, seg_prefix, item_cap, status, static_cast<const __half*>(dout),
-        d_sb, d_ss, d_sh, static_cast<const __half*>(out), o_sb, o_ss, o_sh, delta, dq_acc, Hq, Dqk, Dv, dk_acc, dv_acc, dk16, dv16,
-        k_sb, k_ss, k_sh, v_sb, v_ss, v_sh);
+        g, G, Hkv, split_target, sc.items, sc.item_slot, sc.splits, sc.slot_cap, sc.n_items, sc.seg_prefix,
+        sc.item_cap, status, static_cast<const __half*>(dout), d_sb, d_ss, d_sh, static_cast<const __half*>(out), o_sb,
+        o_ss, o_sh, delta, dq_acc, Hq, Dqk, Dv, dk16, dv16, k_sb, k_ss, k_sh, v_sb, v_ss, v_sh);
   else
     bwd_prep_kernel<__nv_bfloat16><<<1 + fill, kScanThreads, 0, st>>>(
-        g, G, Hkv, split_target, items, n_items, seg_prefix, item_cap, status,
-        static_cast<const __nv_bfloat16*>(dout), d_sb, d_ss, d_sh, static_cast<const __nv_bfloat16*>(out), o_sb,
-        o_ss, o_sh, delta,
-        dq_acc, Hq, Dqk, Dv, dk_acc, dv_acc, dk16, dv16, k_sb, k_ss, k_sh, v_sb, v_ss, v_sh);
+        g, G, Hkv, split_target, sc.items, sc.item_slot, sc.splits, sc.slot_cap, sc.n_items, sc.seg_prefix,
+        sc.item_cap, status, static_cast<const __nv_bfloat16*>(dout), d_sb, d_ss, d_sh,
+        static_cast<const __nv_bfloat16*>(out), o_sb, o_ss, o_sh, delta, dq_acc, Hq, Dqk, Dv, dk16, dv16, k_sb, k_ss,
+        k_sh, v_sb, v_ss, v_sh);
   return cudaGetLastError();
 }
 cudaError_t launch_cross_segments(const int32_t* ids, int B, int S, int q0, int Lq, int k0, int Lk, int32_t* cu_q,
@@ -973,26 +1031,29 @@ cudaError_t launch_grad_add_live(void* dst, const void* src, const int32_t* cu_q
   return cudaGetLastError();
 }
 cudaError_t launch_bwd_convert(const float* dq_acc, void* dq, bool have_q, int B, int Sq, int Hq, int Dqk,
-                               int64_t q_sb, int64_t q_ss, int64_t q_sh, const float* dk_acc, void* dk,
-                               const float* dv_acc, void* dv, int Sk, int Hkv, int Dv, int64_t k_sb, int64_t k_ss,
-                               int64_t k_sh, int64_t v_sb, int64_t v_ss, int64_t v_sh, float scale, int f16,
-                               cudaStream_t st) {
-  const int64_t nq = have_q ? (int64_t)B * Sq : 0, nk = (int64_t)B * Sk;
-  const int64_t rows = nq + (dk_acc ? 2 * nk : 0);
+                               int64_t q_sb, int64_t q_ss, int64_t q_sh, const SegInfo& g, const BwdSchedule* sc,
+                               const float* pk, const float* pv, void* dk, void* dv, int Hkv, int Dv, int64_t k_sb,
+                               int64_t k_ss, int64_t k_sh, int64_t v_sb, int64_t v_ss, int64_t v_sh, float scale,
+                               int f16, cudaStream_t st) {
+  const int64_t nq = have_q ? (int64_t)B * Sq : 0;
+  // Cut tiles: at most slot_cap / 2 of them (each has two slots or more).
+  const int64_t split_rows = sc ? (int64_t)(sc->slot_cap / 2) * Hkv * kBN : 0;
+  const int64_t rows = nq + split_rows;
   if (rows == 0) return cudaSuccess;
   const int64_t work = rows * 32;  // a warp per row
+  const int4* splits = sc ? sc->splits : nullptr;
+  const int* n_split = sc ? sc->n_items + 2 : nullptr;
   if (f16)
     bwd_convert_kernel<__half><<<grid_for(work, 256), 256, 0, st>>>(
-        dq_acc, static_cast<__half*>(dq), nq, Sq, Hq, Dqk, q_sb, q_ss, q_sh, dk_acc, static_cast<__half*>(dk), dv_acc,
-        static_cast<__half*>(dv), nk, Sk, Hkv, Dv, k_sb, k_ss, k_sh, v_sb, v_ss, v_sh, scale);
+        dq_acc, static_cast<__half*>(dq), nq, Sq, Hq, Dqk, q_sb, q_ss, q_sh, g, splits, n_split, pk, pv,
+        static_cast<__half*>(dk), static_cast<__half*>(dv), Hkv, Dv, k_sb, k_ss, k_sh, v_sb, v_ss, v_sh, scale);
   else
     bwd_convert_kernel<__nv_bfloat16><<<grid_for(work, 256), 256, 0, st>>>(
-        dq_acc, static_cast<__nv_bfloat16*>(dq), nq, Sq, Hq, Dqk, q_sb, q_ss, q_sh, dk_acc,
-        static_cast<__nv_bfloat16*>(dk), dv_acc, static_cast<__nv_bfloat16*>(dv), nk, Sk, Hkv, Dv, k_sb, k_ss, k_sh,
-        v_sb, v_ss, v_sh, scale);
+        dq_acc, static_cast<__nv_bfloat16*>(dq), nq, Sq, Hq, Dqk, q_sb, q_ss, q_sh, g, splits, n_split, pk, pv,
+        static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(dv), Hkv, Dv, k_sb, k_ss, k_sh, v_sb, v_ss,
+        v_sh, scale);
   return cudaGetLastError();
 }
-
 
 namespace {
 

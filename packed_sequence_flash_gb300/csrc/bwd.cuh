@@ -1,7 +1,7 @@
 // bwd.cuh -- attention backward for sm_103a, from the caller-supplied out/lse.
 //   [nemo_automodel.components.attention.ffpa_attention, `_ffpa_varlen_bwd`,
-//    `_ffpa_dense_bwd`: gradients "using the caller-supplied out/lse", "dK/dV
-//    reduced to Hkv for GQA"]
+//    `_ffpa_dense_bwd`: gradients from the out and lse the caller passes in,
+//    dK/dV summed over the query heads of each KV head]
 //
 // Per (segment, KV head, 128-row key tile) a CTA keeps K and V in shared
 // memory and walks every (query head of the GQA group, 128-row query tile)
@@ -28,6 +28,8 @@
 
 #include <math_constants.h>
 
+#include <type_traits>
+
 #include "common.cuh"
 
 namespace psf {
@@ -35,7 +37,7 @@ namespace psf {
 struct BwdParams {
   CUtensorMap tm_q, tm_k, tm_v, tm_do;  // bf16 (d, s, h, b) views, box (64, 128)
   CUtensorMap tm_dq;                    // fp32 dQ accumulator [rows][Hq][Dqk], box (32, 32)
-  CUtensorMap tm_dk, tm_dv;             // fp32 dK / dV accumulators [rows][Hkv][D], box (32, 32)
+  CUtensorMap tm_dk, tm_dv;             // fp32 dK / dV partial-sum slots [slot][Hkv][128][D], box (32, 32)
   SegInfo seg;
   const float* lse;
   int64_t l_sb, l_sh;
@@ -50,6 +52,7 @@ struct BwdParams {
   int pack;       // query heads per step: 1, or Hq / Hkv when a KV head's query heads share one tile
   float softcap;  // > 0: logits capped as softcap * tanh(logit / softcap) (the CAP kernels)
   const int4* items;  // (segment, key tile, first step, end step), heaviest first
+  const int* item_slot;  // per item: its dK/dV partial-sum slot, -1 when its key tile is whole
   const int* n_items;
   int* work_next;  // zeroed by the schedule kernel; kernels that take work dynamically count on it
   int* status;
@@ -89,6 +92,7 @@ struct BwdItem {
   int cq0, ck0, m, n;
   int qt0, nqt;  // query tiles [qt0, qt0 + nqt) (of p.seg.qrows rows) see this key tile
   int k0, k1;
+  int slot;  // dK/dV partial-sum slot of a cut key tile's sub-range; -1: the whole tile
 };
 
 __device__ __forceinline__ BwdItem bwd_decode(const BwdParams& p, int w) {
@@ -100,6 +104,7 @@ __device__ __forceinline__ BwdItem bwd_decode(const BwdParams& p, int w) {
   t.kt = it.y;
   t.k0 = it.z;
   t.k1 = it.w;
+  t.slot = p.item_slot[item];
   t.cq0 = cu_q_at(p.seg, t.s);
   t.ck0 = cu_k_at(p.seg, t.s);
   t.m = cu_q_at(p.seg, t.s + 1) - t.cq0;
@@ -121,10 +126,12 @@ __device__ __forceinline__ BwdItem bwd_decode(const BwdParams& p, int w) {
 //   dK  += dS^T Q,  dQ = dS K -> R[0, 192)
 // Two compute warpgroups split the 128 query columns of every step (warps
 // 4-7 columns 0-63, warps 12-15 columns 64-127); the dQ read-out is split over
-// twelve warps (the two compute warpgroups and warps 8-11, two 32-column
-// chunks each), which release R as soon as their chunks are in registers so
-// that the next step's S^T can start while the chunks go out by TMA
-// reduce-add. Warps: 0 TMA producer, 1 MMA issuer, 2 TMEM allocator.
+// twelve warps (warps 8-11 four 32-column chunks, each compute warpgroup one),
+// which release R as soon as their chunks are in registers so that the next
+// step's S^T can start while the chunks go out by TMA reduce-add. Q arrives
+// and is released in 64-column chunks, so the next step's Q loads while this
+// step's dK and dQ products run. Warps: 0 TMA producer, 1 MMA issuer, 2 TMEM
+// allocator.
 template <typename T, int DQK, int DV, bool CAP>
 __global__ void __launch_bounds__(512, 1) attn_bwd_kernel(const __grid_constant__ BwdParams p) {
   using C = BwdCfg<DQK, DV>;
@@ -133,8 +140,10 @@ __global__ void __launch_bounds__(512, 1) attn_bwd_kernel(const __grid_constant_
   float* l2_s = reinterpret_cast<float*>(smem + C::ROWV_OFF);  // [8 compute warps][64]: lse * log2 e (+inf: no mass)
   float* dl_s = l2_s + 8 * 64;                                   // [8 compute warps][64]: Delta
 
-  __shared__ uint64_t kv_full, kv_empty, q_full, q_empty, do_full, do_empty, s_full, p_full, dp_full, ds_full,
-      dq_full, dq_free, acc_done, acc_free, drain;
+  // Q moves in its three 64-column chunks, each with its own barriers, so the
+  // next step's chunk c loads as soon as this step's dK products are done with it.
+  __shared__ uint64_t kv_full, kv_empty, q_full[C::KCH], q_empty[C::KCH], do_full, do_empty, s_full, p_full,
+      dp_full, ds_full, dq_full, dq_free, acc_done, acc_free, drain;
   __shared__ uint32_t tmem_base_smem;
   __shared__ int abort_flag;
 
@@ -142,8 +151,10 @@ __global__ void __launch_bounds__(512, 1) attn_bwd_kernel(const __grid_constant_
   if (threadIdx.x == 0) {
     mbar_init(&kv_full, 1);
     mbar_init(&kv_empty, 1);
-    mbar_init(&q_full, 1);
-    mbar_init(&q_empty, 1);
+    for (int c = 0; c < C::KCH; ++c) {
+      mbar_init(&q_full[c], 1);
+      mbar_init(&q_empty[c], 1);
+    }
     mbar_init(&do_full, 1);
     mbar_init(&do_empty, 1);
     mbar_init(&s_full, 1);
@@ -184,22 +195,28 @@ __global__ void __launch_bounds__(512, 1) attn_bwd_kernel(const __grid_constant_
       bulk_commit_group();
     }
   };
-  // The read-out of one step: this warp's two dQ chunks [c0, c0 + 2) (32
-  // columns each) into registers, R released, then both chunks staged through
-  // `box` (each staging waits until the box's previous reduce has read it).
-  auto dq_readout = [&](const BwdItem& t, int k, uint32_t gstep, int wq, int c0, uint8_t* box) -> bool {
+  // The read-out of one step: this warp's N dQ chunks [c0, c0 + N) (32
+  // columns each) into registers, R released, then the chunks staged through
+  // `box` in turn (each staging waits until the box's previous reduce has read it).
+  auto dq_readout = [&](auto nch, const BwdItem& t, int k, uint32_t gstep, int wq, int c0, uint8_t* box) -> bool {
+    constexpr int N = decltype(nch)::value;
     if (!wait_bar(&dq_full, gstep & 1, ctl)) return false;
     tc_fence_after();
-    uint32_t a[2][32];
+    uint32_t a[N][32];
     const uint32_t rq = tmem + ((uint32_t)(32 * wq) << 16) + C::T_R + c0 * 32;
-    tmem_ld32x2(rq, rq + 32, a[0], a[1]);
+    if constexpr (N == 1) {
+      tmem_ld32(rq, a[0]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < N; i += 2) tmem_ld32x2(rq + i * 32, rq + i * 32 + 32, a[i], a[i + 1]);
+    }
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(&dq_free);
     const int h = t.hk * G + k / t.nqt, qt = t.qt0 + k % t.nqt;
     const int fq = t.cq0 + qt * kBM + 32 * wq, bq = fq / p.seg.Sq, sq = fq - bq * p.seg.Sq;
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < N; ++i) {
       if (lane == 0) bulk_wait_group_read0();
       __syncwarp();
       reduce_box(box, a[i], (c0 + i) * 32, sq, h, bq);
@@ -207,6 +224,11 @@ __global__ void __launch_bounds__(512, 1) attn_bwd_kernel(const __grid_constant_
     return true;
   };
 
+  // Register budgets per warpgroup (launch: 128 per thread, 512 threads):
+  // warps 0-3 96, compute warpgroups 128, dQ read-out warps 160, which hold
+  // four 32-column chunks at once: 96 + 128 + 160 + 128 = 4 x 128.
+  if (warp < 4) {
+    setmaxnreg_dec<96>();
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
@@ -240,19 +262,21 @@ __global__ void __launch_bounds__(512, 1) attn_bwd_kernel(const __grid_constant_
           mbar_arrive_expect_tx(&do_full, C::VCH * kChunkBytes);
           for (int c = 0; c < C::VCH; ++c)
             tma_load_4d(smem + C::DO_OFF + c * kChunkBytes, &p.tm_do, &do_full, c * 64, sq, h, bq);
-          if (!wait_bar(&q_empty, (gstep & 1) ^ 1, ctl)) {
-            ok = false;
-            break;
+          for (int c = 0; c < C::KCH && ok; ++c) {
+            if (!wait_bar(&q_empty[c], (gstep & 1) ^ 1, ctl)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&q_full[c], kChunkBytes);
+            tma_load_4d(smem + C::Q_OFF + c * kChunkBytes, &p.tm_q, &q_full[c], c * 64, sq, h, bq);
           }
-          mbar_arrive_expect_tx(&q_full, C::KCH * kChunkBytes);
-          for (int c = 0; c < C::KCH; ++c)
-            tma_load_4d(smem + C::Q_OFF + c * kChunkBytes, &p.tm_q, &q_full, c * 64, sq, h, bq);
+          if (!ok) break;
         }
       }
       if (nz > 0) wait_bar_drain(&kv_full, (nz - 1) & 1, p.limit_ns);
       if (gstep > 0) {
         wait_bar_drain(&do_full, (gstep - 1) & 1, p.limit_ns);
-        wait_bar_drain(&q_full, (gstep - 1) & 1, p.limit_ns);
+        for (int c = 0; c < C::KCH; ++c) wait_bar_drain(&q_full[c], (gstep - 1) & 1, p.limit_ns);
       }
     }
   } else if (warp == 1) {
@@ -260,7 +284,7 @@ __global__ void __launch_bounds__(512, 1) attn_bwd_kernel(const __grid_constant_
     if (lane == 0) {
       constexpr uint32_t id_sq = idesc_f32acc<T>(128, 128, 0, 0);  // S^T = K Q^T, dP^T = V dO^T
       constexpr uint32_t id_dv = idesc_f32acc<T>(128, DV, 0, 1);   // dV += P^T (TMEM) dO
-      constexpr uint32_t id_dk = idesc_f32acc<T>(128, DQK, 0, 1);  // dK += dS^T Q
+      constexpr uint32_t id_dk64 = idesc_f32acc<T>(128, 64, 0, 1);  // dK[:, 64c, +64) += dS^T Q_c
       constexpr uint32_t id_dq = idesc_f32acc<T>(128, DQK, 1, 1);  // dQ  = dS K
       const uint32_t k_a = sbase + C::K_OFF, v_a = sbase + C::V_OFF, q_a = sbase + C::Q_OFF;
       const uint32_t do_a = sbase + C::DO_OFF, ds_a = sbase + C::DS_OFF;
@@ -276,18 +300,23 @@ __global__ void __launch_bounds__(512, 1) attn_bwd_kernel(const __grid_constant_
         if (nz > 0 && !wait_bar(&acc_free, (nz - 1) & 1, ctl)) break;
         tc_fence_after();
         for (int k = t.k0; k < t.k1 && ok; ++k, ++gstep) {
-          // S^T(g) once Q(g) has landed and the previous dQ has left R.
-          if (!wait_bar(&q_full, gstep & 1, ctl) || (gstep > 0 && !wait_bar(&dq_free, (gstep - 1) & 1, ctl))) {
+          // S^T(g) once the previous dQ has left R, chunk by chunk of Q(g) as they land.
+          if (gstep > 0 && !wait_bar(&dq_free, (gstep - 1) & 1, ctl)) {
             ok = false;
             break;
           }
-          tc_fence_after();
-          for (int c = 0; c < C::KCH; ++c) {
+          for (int c = 0; c < C::KCH && ok; ++c) {
+            if (!wait_bar(&q_full[c], gstep & 1, ctl)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
               mma_ss(rr, sdesc_sw128(k_a + c * kChunkBytes + kk * 32, 16, 1024),
                      sdesc_sw128(q_a + c * kChunkBytes + kk * 32, 16, 1024), id_sq, (c | kk) != 0);
           }
+          if (!ok) break;
           mma_commit(&s_full);
           // dP^T over S^T once the first pass has read it and written P^T;
           // then dV from the packed P^T.
@@ -315,11 +344,15 @@ __global__ void __launch_bounds__(512, 1) attn_bwd_kernel(const __grid_constant_
             break;
           }
           tc_fence_after();
+          // dK one 64-column chunk of Q at a time, each chunk released to the
+          // producer as soon as its products are done with it.
+          for (int c = 0; c < C::KCH; ++c) {
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_ss(tmem + C::T_DK, sdesc_sw128(ds_a + (kk >> 2) * kChunkBytes + (kk & 3) * 32, 16, 1024),
-                   sdesc_sw128(q_a + kk * 2048, kChunkBytes, 1024), id_dk, !(first && kk == 0));
-          mma_commit(&q_empty);
+            for (int kk = 0; kk < 8; ++kk)
+              mma_ss(tmem + C::T_DK + c * 64, sdesc_sw128(ds_a + (kk >> 2) * kChunkBytes + (kk & 3) * 32, 16, 1024),
+                     sdesc_sw128(q_a + c * kChunkBytes + kk * 2048, kChunkBytes, 1024), id_dk64, !(first && kk == 0));
+            mma_commit(&q_empty[c]);
+          }
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
             mma_ss(rr, sdesc_sw128(ds_a + kk * 2048, kChunkBytes, 1024), sdesc_sw128(k_a + kk * 2048, kChunkBytes, 1024),
@@ -334,6 +367,7 @@ __global__ void __launch_bounds__(512, 1) attn_bwd_kernel(const __grid_constant_
       mma_commit(&drain);
       wait_bar_drain(&drain, 0, p.limit_ns);
     }
+  }
   } else if (warp >= 4 && (warp < 8 || warp >= 12)) {
     // ------------------------------------------------------------ compute warpgroups
     const int half = warp >= 12 ? 1 : 0;
@@ -493,10 +527,10 @@ __global__ void __launch_bounds__(512, 1) attn_bwd_kernel(const __grid_constant_
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&ds_full);
-        // This warp's share of the dQ read-out: chunks 0-1 (warps 4-7) or 4-5
+        // This warp's share of the dQ read-out: chunk 0 (warps 4-7) or 5
         // (warps 12-15), staged in its own rows of the dS^T buffer, which the
         // dK and dQ products have finished reading when dQ is ready.
-        if (!dq_readout(t, k, gstep, wq, half ? 4 : 0, box)) {
+        if (!dq_readout(std::integral_constant<int, 1>{}, t, k, gstep, wq, half ? 5 : 0, box)) {
           ok = false;
           break;
         }
@@ -528,8 +562,9 @@ __global__ void __launch_bounds__(512, 1) attn_bwd_kernel(const __grid_constant_
       ++nz;
     }
     if (lane == 0) bulk_wait_group0();
-  } else if (warp >= 8 && warp < 12) {
-    // ------------------------------------------------------------ dQ read-out, chunks 2-3
+  } else {
+    // ------------------------------------------------------------ dQ read-out, chunks 1-4
+    setmaxnreg_inc<160>();
     const int wq = warp - 8;
     uint8_t* box = smem + C::STG_OFF + wq * 4096;
     uint32_t gstep = 0;
@@ -539,7 +574,7 @@ __global__ void __launch_bounds__(512, 1) attn_bwd_kernel(const __grid_constant_
       if (w >= total) continue;
       const BwdItem t = bwd_decode(p, w);
       for (int k = t.k0; k < t.k1; ++k, ++gstep) {
-        if (!dq_readout(t, k, gstep, wq, 2, box)) {
+        if (!dq_readout(std::integral_constant<int, 4>{}, t, k, gstep, wq, 1, box)) {
           ok = false;
           break;
         }

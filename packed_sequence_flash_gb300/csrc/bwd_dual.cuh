@@ -27,8 +27,9 @@
 //          query tile) steps; the scheduler cuts heavy key tiles into several
 //          ranges so that the SMs finish together. dV and dK accumulate in
 //          TMEM across the range (all query heads of the GQA group when the
-//          range covers them) and are added into fp32 accumulators with TMA
-//          reduce-add; a convert kernel writes the bf16 results.
+//          range covers them); a whole key tile writes them to the outputs
+//          from TMEM, a cut tile's sub-ranges store fp32 partial sums to
+//          slots of their own, which the convert kernel adds up.
 //   Warps  0 TMA producer, 1 MMA issuer, 2 TMEM allocator, 4-7 compute
 //          (thread = key row: P, dS, then the dK/dV epilogue), 8-11 dQ read-out.
 //   Work   a CTA starts on unit blockIdx.x of the heaviest-first list, then takes
@@ -377,9 +378,18 @@ __global__ void __launch_bounds__(512, 1) attn_bwd_dual_kernel(const __grid_cons
       BwdItem t;
       const int w = next_work(ok, t);
       if (w < 0) break;
-      if (t.k1 == t.k0) continue;
       const int j = t.kt * kBN + r;  // segment-local key index
       const bool valid = j < t.n;
+      // This key row's dV (warps 4-7) or dK (warps 12-15) in the output.
+      const int fk = t.ck0 + j, bk = fk / p.seg.Sk, sk = fk - bk * p.seg.Sk;
+      T* const out_row = half ? static_cast<T*>(p.dk) + bk * p.k_sb + (int64_t)sk * p.k_ss + t.hk * p.k_sh
+                              : static_cast<T*>(p.dv) + bk * p.v_sb + (int64_t)sk * p.v_ss + t.hk * p.v_sh;
+      if (t.k1 == t.k0) {
+        // No query sees this key tile (never cut): its dK and dV are zero.
+        if (valid)
+          for (int c = 0; c < (half ? DQK : DV) / 8; ++c) reinterpret_cast<uint4*>(out_row)[c] = make_uint4(0, 0, 0, 0);
+        continue;
+      }
       const int delta = t.n - t.m;
       float nlv[2], ndv[2];
       fetch_rows(t, t.k0, nlv, ndv);
@@ -509,40 +519,64 @@ __global__ void __launch_bounds__(512, 1) attn_bwd_dual_kernel(const __grid_cons
         if (lane == 0) mbar_arrive(&ds_full);
       }
       if (!ok) break;
-      // Epilogue: add this range's dV (warps 4-7) or dK (warps 12-15), scale
-      // applied by the convert, into the fp32 accumulators in 32 x 32 boxes.
+      // Epilogue: this range's dV (warps 4-7) or dK (warps 12-15). A whole key
+      // tile writes its rows straight to the output (dK scaled); a cut tile's
+      // sub-range stores its fp32 partial sums to its own slot in 32 x 32
+      // boxes, and the convert adds the slots up.
       if (!wait_bar(&acc_done, nz & 1, ctl)) break;
       tc_fence_after();
-      const int fk = t.ck0 + t.kt * kBN + 32 * wq, bk = fk / p.seg.Sk, sk = fk - bk * p.seg.Sk;
       constexpr int NCV = DV / 32, NCK = DQK / 32;
       const int nc = half ? NCK : NCV;
+      if (t.slot < 0) {
+        const float sc = half ? p.scale : 1.f;
 #pragma unroll 1
-      for (int c = 0; c < nc; ++c) {
-        uint32_t a[32];
-        tmem_ld32(tmem + lane_base + (half ? C::T_DK : C::T_DV) + c * 32, a);
-        if (c == nc - 1) {
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&acc_free);
-        }
-        if (c >= 1) {
-          if (lane == 0) bulk_wait_group_read0();
-          __syncwarp();
-        }
+        for (int c = 0; c < nc; ++c) {
+          uint32_t a[32];
+          tmem_ld32(tmem + lane_base + (half ? C::T_DK : C::T_DV) + c * 32, a);
+          if (c == nc - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_free);
+          }
+          if (valid) {
+            uint4* dst = reinterpret_cast<uint4*>(out_row + c * 32);
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
-          *reinterpret_cast<uint4*>(epi + sw128_offset(lane, u)) =
-              make_uint4(a[4 * u], a[4 * u + 1], a[4 * u + 2], a[4 * u + 3]);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          tma_reduce_add_4d(half ? &p.tm_dk : &p.tm_dv, epi, c * 32, sk, t.hk, bk);
-          bulk_commit_group();
+            for (int u = 0; u < 4; ++u)
+              dst[u] = make_uint4(pack2<T>(__uint_as_float(a[8 * u]) * sc, __uint_as_float(a[8 * u + 1]) * sc),
+                                  pack2<T>(__uint_as_float(a[8 * u + 2]) * sc, __uint_as_float(a[8 * u + 3]) * sc),
+                                  pack2<T>(__uint_as_float(a[8 * u + 4]) * sc, __uint_as_float(a[8 * u + 5]) * sc),
+                                  pack2<T>(__uint_as_float(a[8 * u + 6]) * sc, __uint_as_float(a[8 * u + 7]) * sc));
+          }
         }
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < nc; ++c) {
+          uint32_t a[32];
+          tmem_ld32(tmem + lane_base + (half ? C::T_DK : C::T_DV) + c * 32, a);
+          if (c == nc - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_free);
+          }
+          if (c >= 1) {
+            if (lane == 0) bulk_wait_group_read0();
+            __syncwarp();
+          }
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            *reinterpret_cast<uint4*>(epi + sw128_offset(lane, u)) =
+                make_uint4(a[4 * u], a[4 * u + 1], a[4 * u + 2], a[4 * u + 3]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_4d(half ? &p.tm_dk : &p.tm_dv, epi, c * 32, 32 * wq, t.hk, t.slot);
+            bulk_commit_group();
+          }
+        }
+        // The boxes sit in the dS^T buffer: drain them before the next dS^T.
+        if (lane == 0) bulk_wait_group_read0();
+        __syncwarp();
       }
-      // The boxes sit in the dS^T buffer: drain them before the next dS^T.
-      if (lane == 0) bulk_wait_group_read0();
-      __syncwarp();
       ++nz;
     }
     if (lane == 0) bulk_wait_group0();

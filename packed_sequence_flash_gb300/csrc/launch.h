@@ -18,19 +18,30 @@ struct BwdParams;
 cudaError_t launch_fwd_prep(const SegInfo& g, int2* items, int* n_items, int* seg_prefix, int item_cap, int* status,
                             void* out, int64_t o_sb, int64_t o_ss, int64_t o_sh, float* lse, int64_t l_sb,
                             int64_t l_sh, int Hq, int Dv, cudaStream_t st);
-// Backward preparation in one launch: the work list of key tiles, split into
-// (first step, end step) sub-ranges when split_target > 0 (items are int4
-// (segment, key tile, first, end); n_items[1] zeroed as above); Delta =
-// rowsum(dO * O) (fp32, [Hq][rows]; dO and O each with their own element
-// strides); the zeroed dQ accumulator, and either the
-// zeroed dK/dV accumulators (when given) or zeroed dK / dV rows at or past
-// cu_k[nseg].
-cudaError_t launch_bwd_prep(const SegInfo& g, int G, int Hkv, int split_target, int4* items, int* n_items,
-                            int* seg_prefix, int item_cap, int* status, const void* dout, int64_t d_sb, int64_t d_ss,
-                            int64_t d_sh, const void* out, int64_t o_sb, int64_t o_ss, int64_t o_sh, float* delta,
-                            float* dq_acc, int Hq, int Dqk, int Dv, float* dk_acc, float* dv_acc, void* dk, void* dv,
-                            int64_t k_sb, int64_t k_ss, int64_t k_sh, int64_t v_sb, int64_t v_ss, int64_t v_sh, int f16,
-                            cudaStream_t st);
+// Backward work list in the workspace: items (segment, key tile, first step,
+// end step), heaviest first, with item_slot[i] the dK/dV partial-sum slot of
+// item i (-1: its key tile is whole); splits lists the cut key tiles as
+// (segment, key tile, first slot, slot count). n_items[0] = items, n_items[1]
+// the work counter of kernels that take items dynamically, n_items[2] = cut
+// tiles.
+struct BwdSchedule {
+  int4* items;
+  int* item_slot;
+  int4* splits;
+  int* n_items;
+  int* seg_prefix;
+  int item_cap;
+  int slot_cap;
+};
+// Backward preparation in one launch: the work list (key tiles cut into
+// sub-ranges when split_target > 0; n_items[1] zeroed); Delta = rowsum(dO * O)
+// (fp32, [Hq][rows]; dO and O each with their own element strides); the zeroed
+// dQ accumulator; zeroed dK / dV rows at or past cu_k[nseg].
+cudaError_t launch_bwd_prep(const SegInfo& g, int G, int Hkv, int split_target, const BwdSchedule& sc, int* status,
+                            const void* dout, int64_t d_sb, int64_t d_ss, int64_t d_sh, const void* out, int64_t o_sb,
+                            int64_t o_ss, int64_t o_sh, float* delta, float* dq_acc, int Hq, int Dqk, int Dv, void* dk,
+                            void* dv, int64_t k_sb, int64_t k_ss, int64_t k_sh, int64_t v_sb, int64_t v_ss,
+                            int64_t v_sh, int f16, cudaStream_t st);
 // Grid: one CTA per SM (two for head dims 64 and 128), at most max_work.
 // f16 selects fp16 inputs and outputs (else bf16).
 cudaError_t launch_fwd(const FwdParams& p, int dqk, int dvc, int sms, int64_t max_work, int f16, cudaStream_t st);
@@ -64,13 +75,14 @@ cudaError_t launch_lse_merge_live(float* o_acc, void* o_run, float* l_acc, const
                                   int H, int D, int f16, cudaStream_t st);
 cudaError_t launch_grad_add_live(void* dst, const void* src, const int32_t* cu_q, const int32_t* cu_k,
                                  const int32_t* dev_meta, int nseg, int T, int H, int D, int f16, cudaStream_t st);
-// dQ = scale * dQacc (bf16, q's layout); with accumulators also dK = scale *
-// dKacc and dV = dVacc.
+// dQ = scale * dQacc (q's dtype and layout); with a schedule (sc), dK = scale *
+// the sum of each cut key tile's partial-sum slots and dV = the sum of its
+// slots (pk / pv: [slot][Hkv][128][D] fp32) for the tile's key rows.
 cudaError_t launch_bwd_convert(const float* dq_acc, void* dq, bool have_q, int B, int Sq, int Hq, int Dqk,
-                               int64_t q_sb, int64_t q_ss, int64_t q_sh, const float* dk_acc, void* dk,
-                               const float* dv_acc, void* dv, int Sk, int Hkv, int Dv, int64_t k_sb, int64_t k_ss,
-                               int64_t k_sh, int64_t v_sb, int64_t v_ss, int64_t v_sh, float scale, int f16,
-                               cudaStream_t st);
+                               int64_t q_sb, int64_t q_ss, int64_t q_sh, const SegInfo& g, const BwdSchedule* sc,
+                               const float* pk, const float* pv, void* dk, void* dv, int Hkv, int Dv, int64_t k_sb,
+                               int64_t k_ss, int64_t k_sh, int64_t v_sb, int64_t v_ss, int64_t v_sh, float scale,
+                               int f16, cudaStream_t st);
 
 // One CTA whose warp 0 makes one bounded pipeline wait; it runs out (and
 // records kStatusTimeout in *status) unless `arrive` is set.
