@@ -64,14 +64,14 @@ L2_FLUSH_BYTES = 256 << 20
 # other workloads and once the sources change.
 NCU_TRAFFIC = {
     # the document path's default: a KV head's query heads packed into one tile
-    ("attn_bwd_dual_kernel", "cfg5_doc_causal_t65536_w4096"): ("74d26f9003e23c8c", 40045062400),
-    ("attn_fwd_duo_kernel", "cfg5_doc_causal_t65536_w4096"): ("ba5c514a195b41fb", 3784822528),
-    ("attn_bwd_dual_kernel", "cfg2_doc_causal_t8192_d128"): ("74d26f9003e23c8c", 359169280),
-    ("attn_fwd_duo_kernel", "cfg2_doc_causal_t8192_d128"): ("ba5c514a195b41fb", 52814080),
-    ("attn_bwd_kernel", "cfg4_doc_causal_shard_dqk192_dv128"): ("64e9dca48875161a", 790401792),
-    ("attn_fwd_pair_kernel", "cfg4_doc_causal_shard_dqk192_dv128"): ("cc80d554cb59b181", 190336512),
-    ("attn_bwd_wide_kernel", "cfg3_dense_causal_n4096_d512"): ("bc3f0b6b52c5de97", 1021756672),
-    ("attn_fwd_kernel", "cfg3_dense_causal_n4096_d512"): ("c5813fd46184e0a7", 127845376),
+    ("attn_bwd_dual_kernel", "cfg5_doc_causal_t65536_w4096"): ("82604bf037e08438", 34290653696),
+    ("attn_fwd_duo_kernel", "cfg5_doc_causal_t65536_w4096"): ("442dc45691a70b8a", 3773222144),
+    ("attn_bwd_dual_kernel", "cfg2_doc_causal_t8192_d128"): ("82604bf037e08438", 367806976),
+    ("attn_fwd_duo_kernel", "cfg2_doc_causal_t8192_d128"): ("442dc45691a70b8a", 52287232),
+    ("attn_bwd_kernel", "cfg4_doc_causal_shard_dqk192_dv128"): ("1e244dae713df4b8", 763610624),
+    ("attn_fwd_pair_kernel", "cfg4_doc_causal_shard_dqk192_dv128"): ("536706aeab01fc99", 179188480),
+    ("attn_bwd_wide_kernel", "cfg3_dense_causal_n4096_d512"): ("2e9089db2122fc5f", 958902016),
+    ("attn_fwd_kernel", "cfg3_dense_causal_n4096_d512"): ("b62559f39a5d9209", 126914048),
 }
 
 
