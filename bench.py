@@ -69,7 +69,7 @@ NCU_TRAFFIC = {
     ("attn_bwd_dual_kernel", "cfg2_doc_causal_t8192_d128"): ("82604bf037e08438", 367806976),
     ("attn_fwd_duo_kernel", "cfg2_doc_causal_t8192_d128"): ("442dc45691a70b8a", 52287232),
     ("attn_bwd_kernel", "cfg4_doc_causal_shard_dqk192_dv128"): ("1e244dae713df4b8", 763610624),
-    ("attn_fwd_pair_kernel", "cfg4_doc_causal_shard_dqk192_dv128"): ("536706aeab01fc99", 179188480),
+    ("attn_fwd_pair_kernel", "cfg4_doc_causal_shard_dqk192_dv128"): ("13e4409971f3398f", 181557504),
     ("attn_bwd_wide_kernel", "cfg3_dense_causal_n4096_d512"): ("2e9089db2122fc5f", 958902016),
     ("attn_fwd_kernel", "cfg3_dense_causal_n4096_d512"): ("b62559f39a5d9209", 126914048),
 }

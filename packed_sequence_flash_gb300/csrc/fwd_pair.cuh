@@ -11,15 +11,17 @@
 // accumulator, over the union of the two halves' key ranges (a half skips the
 // key tiles it cannot see). Per key tile j each half runs
 //   S_X(j) = Q_X K_j^T  ->  softmax  ->  O_X += P_X V_j
-// and the MMA thread issues, for each half in turn, PV_X(j) and then S_X(j+1)
-// as soon as that half's P_X(j) is written, so one half's softmax overlaps the
-// other half's products and both read each K_j / V_j from shared memory once.
+// and each half's MMA thread issues PV_X(j) and then S_X(j+1) as soon as that
+// half's P_X(j) is written, so one half's softmax overlaps the other half's
+// products, neither half's issue waits behind the other's, and both read each
+// K_j / V_j from shared memory once.
 //   TMEM  S_A [0, 128) | S_B [128, 256) | O_A [256, 256 + Dv) | O_B [256 + Dv, ...);
 //         P_X (16-bit) is written over the first 64 columns of S_X.
 //   SMEM  Q_A, Q_B (Dqk / 64 chunks each), then a ring of 16 KB chunks that
 //         K_0, V_0, K_1, V_1, ... pass through in order.
 //   warps 0-3 softmax of half A, 4-7 half B (thread = query row = TMEM lane),
-//         8 TMA producer, 9 TMEM allocator and MMA issuer.
+//         8 TMA producer, 9 TMEM allocator and MMA issuer of half A, 10 MMA
+//         issuer of half B.
 // The commit that signals S_X(j+1) also covers PV_X(j) (a commit tracks every
 // earlier MMA of the issuing thread), so the softmax may rescale O_X as soon
 // as S_X(j+1) is ready. Items are taken in snake order from the heaviest-first
@@ -69,7 +71,7 @@ __device__ __forceinline__ PairHalf pair_half(const FwdParams& p, const FwdTile&
 // CAP: logits softcapped (p.softcap > 0), applied to the score registers in
 // place before the row maximum.
 template <typename T, int DQK, int DV, bool CAP>
-__global__ void __launch_bounds__(320, 1) attn_fwd_pair_kernel(const __grid_constant__ FwdParams p) {
+__global__ void __launch_bounds__(352, 1) attn_fwd_pair_kernel(const __grid_constant__ FwdParams p) {
   using C = FwdPairCfg<DQK, DV>;
   constexpr int NST = C::NST;
   extern __shared__ uint8_t smem_raw[];
@@ -84,10 +86,10 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_pair_kernel(const __grid_cons
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) {
     mbar_init(&q_full, 1);
-    mbar_init(&q_empty, 1);
+    mbar_init(&q_empty, 2);  // both MMA issuers
     for (int i = 0; i < NST; ++i) {
       mbar_init(&kv_full[i], 1);
-      mbar_init(&kv_empty[i], 1);
+      mbar_init(&kv_empty[i], 2);
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(&s_full[x], 1);
@@ -95,7 +97,7 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_pair_kernel(const __grid_cons
       mbar_init(&pv_done[x], 1);
       mbar_init(&o_free[x], 4);
     }
-    mbar_init(&drain, 1);
+    mbar_init(&drain, 2);
     abort_flag = 0;
     fence_mbar_init();
   }
@@ -161,14 +163,22 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_pair_kernel(const __grid_cons
         wait_bar_drain(&kv_full[i % NST], (i / NST) & 1, p.limit_ns);
       if (qcnt > 0) wait_bar_drain(&q_full, (qcnt - 1) & 1, p.limit_ns);
     }
-  } else if (warp == 9) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 9 || warp == 10) {
+    // ------------------------------------------------------------ MMA issuers (warp 9: half A, 10: half B)
+    // Each half's products come from its own thread, so one half's issue
+    // never waits behind the other half's P. Both walk the ring in load order
+    // (per key tile: K_j, then V_j) and each releases every chunk once (the
+    // ring's empty barriers count two arrivals): by a commit when its products
+    // read the chunk, else by a plain arrival once the chunk has landed (so
+    // the arrival cannot count towards the slot's previous round).
     if (lane == 0) {
+      const int x = warp - 9;
       constexpr uint32_t id_qk = idesc_f32acc<T>(128, 128, 0, 0);
       constexpr uint32_t id_pv = idesc_f32acc<T>(128, DV, 0, 1);
       constexpr uint32_t id_pv64 = idesc_f32acc<T>(128, 64, 0, 1);
-      const uint32_t ring_a = smem_u32(ring), q_a = smem_u32(smem);
-      uint32_t qcnt = 0, it = 0, nkv[2] = {0, 0}, ntile[2] = {0, 0};
+      const uint32_t ring_a = smem_u32(ring), qx = smem_u32(smem) + x * C::Q_BYTES;
+      const uint32_t ts = tmem + x * 128, to = tmem + C::T_O + x * DV;
+      uint32_t qcnt = 0, it = 0, nkv = 0, ntile = 0;
       bool ok = true;
       // Wait for the next n chunks of the ring (in load order); returns the first one's index.
       auto take = [&](int n) -> uint32_t {
@@ -178,105 +188,88 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_pair_kernel(const __grid_cons
         tc_fence_after();
         return first;
       };
-      auto release = [&](uint32_t first, int n) {
-        for (int c = 0; c < n; ++c) mma_commit(&kv_empty[(first + c) % NST]);
+      auto release = [&](uint32_t first, int n, bool used) {
+        for (int c = 0; c < n; ++c) {
+          if (used)
+            mma_commit(&kv_empty[(first + c) % NST]);
+          else
+            mbar_arrive(&kv_empty[(first + c) % NST]);
+        }
       };
       for (int wi = 0; wi * (int)gridDim.x < total && ok; ++wi) {
         const int w = snake_item(wi);
         if (w >= total) continue;
         const FwdTile t = fwd_decode(p, w);
         if (t.nk == 0) continue;
-        const PairHalf hx[2] = {pair_half(p, t, 0), pair_half(p, t, 1)};
-        auto active = [&](int x, int jj) { return jj >= hx[x].a && jj < hx[x].b; };
+        const PairHalf hx = pair_half(p, t, x);
         if (!wait_bar(&q_full, qcnt & 1, ctl)) break;
         tc_fence_after();
-        auto issue_s = [&](int x, uint32_t k_first) {
-          const uint32_t qx = q_a + x * C::Q_BYTES;
-#pragma unroll
-          for (int c = 0; c < C::QCH; ++c) {
-            const uint32_t k_addr = ring_a + ((k_first + c) % NST) * kChunkBytes;
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_ss(tmem + x * 128, sdesc_sw128(qx + c * kChunkBytes + kk * 32, 16, 1024),
-                     sdesc_sw128(k_addr + kk * 32, 16, 1024), id_qk, (c | kk) != 0);
-          }
-          mma_commit(&s_full[x]);
-        };
-        // S of the first key tile for both halves.
-        uint32_t k_first = take(C::QCH);
-        if (!ok) break;
-        for (int x = 0; x < 2; ++x)
-          if (active(x, 0)) issue_s(x, k_first);
-        release(k_first, C::QCH);
-        bool first_pv[2] = {true, true};
+        bool first_pv = true;
         for (int jj = 0; jj < t.nk && ok; ++jj) {
+          const bool act = jj >= hx.a && jj < hx.b;
+          // S_X(j) = Q_X K_j^T; its commit also covers PV_X(j-1), issued just before.
+          const uint32_t k_first = take(C::QCH);
+          if (!ok) break;
+          if (act) {
+#pragma unroll
+            for (int c = 0; c < C::QCH; ++c) {
+              const uint32_t k_addr = ring_a + ((k_first + c) % NST) * kChunkBytes;
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                mma_ss(ts, sdesc_sw128(qx + c * kChunkBytes + kk * 32, 16, 1024),
+                       sdesc_sw128(k_addr + kk * 32, 16, 1024), id_qk, (c | kk) != 0);
+            }
+            mma_commit(&s_full[x]);
+          }
+          release(k_first, C::QCH, act);
+          // O_X (+)= P_X V_j once the softmax has written P_X (and, on the
+          // half's first key tile, once the previous item's epilogue has read O_X).
           const uint32_t v_first = take(C::VCH);
           if (!ok) break;
-          const bool more = jj + 1 < t.nk;
-          bool k_taken = false;
-          for (int x = 0; x < 2 && ok; ++x) {
-            if (active(x, jj)) {
-              if (!wait_bar(&p_full[x], nkv[x] & 1, ctl)) {
-                ok = false;
-                break;
-              }
-              ++nkv[x];
-              if (first_pv[x] && ntile[x] > 0 && !wait_bar(&o_free[x], (ntile[x] - 1) & 1, ctl)) {
-                ok = false;
-                break;
-              }
-              tc_fence_after();
-              const uint32_t vs = v_first % NST;
-              if (vs + C::VCH <= (uint32_t)NST) {
-                // V's chunks sit in consecutive slots: one N = Dv chain, the
-                // B operand's 64-column chunks reached through the leading-byte offset.
-                const uint32_t v_addr = ring_a + vs * kChunkBytes;
+          if (act) {
+            if (!wait_bar(&p_full[x], nkv & 1, ctl)) {
+              ok = false;
+              break;
+            }
+            ++nkv;
+            if (first_pv && ntile > 0 && !wait_bar(&o_free[x], (ntile - 1) & 1, ctl)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t vs = v_first % NST;
+            if (vs + C::VCH <= (uint32_t)NST) {
+              // V's chunks sit in consecutive slots: one N = Dv chain, the
+              // B operand's 64-column chunks reached through the leading-byte offset.
+              const uint32_t v_addr = ring_a + vs * kChunkBytes;
+#pragma unroll
+              for (int kk = 0; kk < 8; ++kk)
+                mma_ts(to, ts + kk * 8, sdesc_sw128(v_addr + kk * 2048, kChunkBytes, 1024), id_pv,
+                       !(first_pv && kk == 0));
+            } else {
+              // V wraps around the ring: one N = 64 chain per chunk.
+#pragma unroll
+              for (int c = 0; c < C::VCH; ++c) {
+                const uint32_t v_addr = ring_a + ((v_first + c) % NST) * kChunkBytes;
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                  mma_ts(tmem + C::T_O + x * DV, tmem + x * 128 + kk * 8,
-                         sdesc_sw128(v_addr + kk * 2048, kChunkBytes, 1024), id_pv, !(first_pv[x] && kk == 0));
-              } else {
-                // V wraps around the ring: one N = 64 chain per chunk.
-#pragma unroll
-                for (int c = 0; c < C::VCH; ++c) {
-                  const uint32_t v_addr = ring_a + ((v_first + c) % NST) * kChunkBytes;
-#pragma unroll
-                  for (int kk = 0; kk < 8; ++kk)
-                    mma_ts(tmem + C::T_O + x * DV + c * 64, tmem + x * 128 + kk * 8,
-                           sdesc_sw128(v_addr + kk * 2048, kChunkBytes, 1024), id_pv64, !(first_pv[x] && kk == 0));
-                }
+                  mma_ts(to + c * 64, ts + kk * 8, sdesc_sw128(v_addr + kk * 2048, kChunkBytes, 1024), id_pv64,
+                         !(first_pv && kk == 0));
               }
-              first_pv[x] = false;
             }
-            if (more && active(x, jj + 1)) {
-              if (!k_taken) {
-                k_first = take(C::QCH);
-                k_taken = true;
-                if (!ok) break;
-              }
-              issue_s(x, k_first);
-            }
+            first_pv = false;
           }
-          if (!ok) break;
-          release(v_first, C::VCH);
-          if (more) {
-            if (!k_taken) {  // a key tile neither half sees: its chunks are only passed through
-              k_first = take(C::QCH);
-              if (!ok) break;
-            }
-            release(k_first, C::QCH);
-          }
+          release(v_first, C::VCH, act);
         }
         if (!ok) break;
         mma_commit(&q_empty);
-        for (int x = 0; x < 2; ++x)
-          if (hx[x].b > hx[x].a) {
-            mma_commit(&pv_done[x]);
-            ++ntile[x];
-          }
+        if (hx.b > hx.a) {
+          mma_commit(&pv_done[x]);
+          ++ntile;
+        }
         ++qcnt;
       }
-      // Wind down: wait until every MMA this thread issued has finished.
+      // Wind down: wait until every MMA either thread issued has finished.
       mma_commit(&drain);
       wait_bar_drain(&drain, 0, p.limit_ns);
     }

@@ -33,7 +33,7 @@ cudaError_t run_pair(const FwdParams& p, int grid, cudaStream_t st) {
   cudaError_t e =
       cudaFuncSetAttribute(attn_fwd_pair_kernel<T, DQK, DV, CAP>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  attn_fwd_pair_kernel<T, DQK, DV, CAP><<<grid, 320, smem, st>>>(p);
+  attn_fwd_pair_kernel<T, DQK, DV, CAP><<<grid, 352, smem, st>>>(p);
   return cudaGetLastError();
 }
 template <typename T, bool CAP>
