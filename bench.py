@@ -589,7 +589,6 @@ def our_arm(args):
     in_ready = [torch.cuda.Event() for _ in range(nbuf)]
     in_free = [torch.cuda.Event() for _ in range(nbuf)]
     out_ready = [torch.cuda.Event() for _ in range(nbuf)]
-    out_done = [torch.cuda.Event() for _ in range(nbuf)]
     out_used = [False] * nbuf
     host_out = [None] * nbuf
     keep = [None] * nbuf
@@ -599,11 +598,12 @@ def our_arm(args):
     def e2e_step(i):
         nonlocal d2h
         b = i % nbuf
-        # The host takes step i - nbuf's results before it queues step i, as a
-        # consumer of the results would: this bounds how far the host runs
-        # ahead, so the results' memory is reused instead of allocated anew.
+        # The host queues step i only once step i - nbuf's compute is done:
+        # this bounds how far the host runs ahead (and so how many steps'
+        # results are alive at once) without tying the copies of one step to
+        # those of another.
         if out_used[b]:
-            out_done[b].synchronize()
+            in_free[b].synchronize()
         with torch.cuda.stream(h2d_s):
             h2d_s.wait_event(in_free[b])
             for dst, src in zip(dev_in[b], host_in):
@@ -624,7 +624,6 @@ def our_arm(args):
             for hdst, r in zip(host_out[b], results):
                 r.record_stream(d2h_s)
                 hdst.copy_(r, non_blocking=True)
-            out_done[b].record(d2h_s)
         out_used[b] = True
         keep[b] = results
 
@@ -686,7 +685,7 @@ def our_arm(args):
         "e2e": {"value": whole_job_value(world, flops, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms,
                 "timing": "steps pipelined: uploads and downloads overlap neighbouring steps' compute; the host "
-                          "takes step i-2's results before it queues step i"},
+                          "queues step i once step i-2's compute is done"},
         "gpu_launches": launches_per_step(dense, bool(split)) * args.steps,
         "clocks": clocks,
     }

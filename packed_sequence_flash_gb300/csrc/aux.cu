@@ -160,7 +160,7 @@ __device__ void schedule_body(SegInfo g, int over_keys, int2* items, int* n_item
 // The sub-ranges of a cut tile write their dK/dV partial sums to slots of
 // their own: item_slot[i] is item i's slot (-1: the tile is whole and its
 // unit writes dK/dV itself), and splits[0, n_items[2]) lists the cut tiles as
-// (segment, key tile, first slot, slot count) for the convert kernel.
+// (first key row, key rows, first slot, slot count) for the convert kernel.
 // Runs in one 1024-thread block (block 0 of bwd_prep_kernel).
 __device__ void bwd_schedule_body(SegInfo g, int G, int Hkv, int split_target, int4* items, int* item_slot,
                                   int4* splits, int slot_cap, int* n_items, int* seg_prefix, int item_cap,
@@ -266,7 +266,10 @@ __device__ void bwd_schedule_body(SegInfo g, int G, int Hkv, int split_target, i
     const int t = x - pref[s];
     const int steps = Gs * tile_cost(g, s, t, 1);
     const int nsub = steps == 0 ? 1 : (int)(((long long)steps + smax - 1) / smax);
-    if (nsub > 1) splits[cut_next++] = make_int4(s, t, slot_next, nsub);
+    if (nsub > 1) {
+      const int k0 = cu_k_at(g, s) + t * kBN;
+      splits[cut_next++] = make_int4(k0, min(kBN, cu_k_at(g, s + 1) - k0), slot_next, nsub);
+    }
     for (int i = 0; i < nsub; ++i) {
       const int a = (int)((long long)steps * i / nsub), e = (int)((long long)steps * (i + 1) / nsub);
       const int b = min(e - a, kBuckets - 1);
@@ -490,9 +493,9 @@ __global__ void lse_merge_kernel(const E* o1, const float* l1, const E* o2, cons
 }
 
 // Delta = sum_d dO * O in fp32, by groups of min(32, Dv/8) lanes per
-// (row, head); then grid-stride zeroing of the fp32 accumulators. When dK/dV
-// are written directly (no accumulators), rows no segment covers are zeroed.
-// Delta = rowsum(dO * O) and the zeroed accumulators; blocks bid of nblk.
+// (row, head), with the grid-stride zeroing of the fp32 dQ accumulator spread
+// over the Delta passes; then the zeroed dK / dV rows past the last segment.
+// Blocks bid of nblk.
 constexpr int kDeltaUnroll = 2;
 template <typename E>
 __device__ void bwd_pre_body(SegInfo g, const E* dout, int64_t d_sb, int64_t d_ss, int64_t d_sh, const E* out,
@@ -508,7 +511,20 @@ __device__ void bwd_pre_body(SegInfo g, const E* dout, int64_t d_sb, int64_t d_s
   const int64_t n = rows * Hq, stride = nwarps * per_warp;
   // kDeltaUnroll (row, head) pairs per lane group and pass, all loads issued together.
   constexpr int U = kDeltaUnroll;
+  // The dQ accumulator's zero stores go out a few per pass, between the
+  // passes' loads, so the writes overlap the reads' latency.
+  const int64_t tid = bid * (int64_t)blockDim.x + threadIdx.x;
+  const int64_t nthr = (int64_t)nblk * blockDim.x;
+  const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+  const int64_t n4 = rows * Hq * Dqk / 4;
+  int64_t zx = tid;
   for (int64_t base = (bid * (int64_t)blockDim.x + threadIdx.x) / 32 * per_warp; base < n; base += stride * U) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      if (zx < n4) {
+        reinterpret_cast<float4*>(dq_acc)[zx] = z4;
+        zx += nthr;
+      }
     float acc[U];
     int64_t off[U], doff[U];
 #pragma unroll
@@ -553,11 +569,7 @@ __device__ void bwd_pre_body(SegInfo g, const E* dout, int64_t d_sb, int64_t d_s
       }
     }
   }
-  const int64_t tid = bid * (int64_t)blockDim.x + threadIdx.x;
-  const int64_t nthr = (int64_t)nblk * blockDim.x;
-  const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
-  const int64_t n4 = rows * Hq * Dqk / 4;
-  for (int64_t x = tid; x < n4; x += nthr) reinterpret_cast<float4*>(dq_acc)[x] = z4;
+  for (; zx < n4; zx += nthr) reinterpret_cast<float4*>(dq_acc)[zx] = z4;
   // dK / dV rows inside segments are written by the attention kernel (or the
   // convert, for cut key tiles); rows past the last segment are zero.
   const int64_t krows_all = (int64_t)g.B * g.Sk;
@@ -610,11 +622,11 @@ __device__ __forceinline__ void convert_row(const float* __restrict__ acc, E* __
   }
 }
 
-// dK = scale * (sum of the partial-sum slots) and dV = (sum of its slots) for
-// the key rows of every cut key tile, a warp per (tile, KV head, key row),
-// then dQ = scale * dQacc, a warp per packed row. The cut tiles come first so
-// that their short dependent reads overlap the dQ rows' streaming. A slot
-// holds [Hkv][128][D] fp32 rows.
+// dQ = scale * dQacc, a warp per packed row; then dK = scale * (sum of the
+// partial-sum slots) and dV = (sum of its slots) for the key rows of every
+// cut key tile, a warp per (tile, KV head, key row). The dQ rows come first,
+// so they need neither the cut-tile count nor the list. A slot holds
+// [Hkv][128][D] fp32 rows.
 template <typename E>
 __global__ void __launch_bounds__(256, 4) bwd_convert_kernel(const float* dq_acc, E* dq, int64_t nq, int Sq, int Hq, int Dqk,
                                    int64_t q_sb, int64_t q_ss, int64_t q_sh, SegInfo g, const int4* splits,
@@ -624,18 +636,17 @@ __global__ void __launch_bounds__(256, 4) bwd_convert_kernel(const float* dq_acc
   const int64_t nw = (int64_t)gridDim.x * (blockDim.x / 32);
   const int lane = threadIdx.x & 31;
   const int64_t per_tile = (int64_t)Hkv * kBN;
-  const int64_t ncut = splits ? (int64_t)(*n_split) * per_tile : 0;
-  for (int64_t x = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) / 32; x < ncut + nq; x += nw) {
-    if (x >= ncut) {
-      convert_row(dq_acc, dq, x - ncut, Sq, Hq, Dqk, q_sb, q_ss, q_sh, scale);
-      continue;
-    }
+  const int64_t w0 = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) / 32;
+  int64_t x = w0;
+  for (; x < nq; x += nw) convert_row(dq_acc, dq, x, Sq, Hq, Dqk, q_sb, q_ss, q_sh, scale);
+  if (!splits) return;
+  const int64_t ncut = (int64_t)(*n_split) * per_tile;
+  for (x -= nq; x < ncut; x += nw) {
     const int e = (int)(x / per_tile);
     const int rem = (int)(x - e * per_tile), hk = rem / kBN, r = rem % kBN;
-    const int4 sp = splits[e];
-    const int k0 = cu_k_at(g, sp.x), n = cu_k_at(g, sp.x + 1) - k0, j = sp.y * kBN + r;
-    if (j >= n) continue;
-    const int f = k0 + j, b = f / g.Sk, sr = f - b * g.Sk;
+    const int4 sp = splits[e];  // (first key row, key rows, first slot, slot count)
+    if (r >= sp.y) continue;
+    const int f = sp.x + r, b = f / g.Sk, sr = f - b * g.Sk;
     // Lane l holds elements [4l, 4l + 4) of the dK row and of the dV row; the
     // slots' loads go out four at a time.
     const bool on_k = lane * 4 < Dqk, on_v = lane * 4 < Dv;

@@ -21,7 +21,7 @@ cudaError_t launch_fwd_prep(const SegInfo& g, int2* items, int* n_items, int* se
 // Backward work list in the workspace: items (segment, key tile, first step,
 // end step), heaviest first, with item_slot[i] the dK/dV partial-sum slot of
 // item i (-1: its key tile is whole); splits lists the cut key tiles as
-// (segment, key tile, first slot, slot count). n_items[0] = items, n_items[1]
+// (first key row, key rows, first slot, slot count). n_items[0] = items, n_items[1]
 // the work counter of kernels that take items dynamically, n_items[2] = cut
 // tiles.
 struct BwdSchedule {
