@@ -356,6 +356,22 @@ def max_over_ranks(x: float, dist=None, device=None) -> float:
     return float(t.item())
 
 
+def roofline_peak(peaks: dict, src: str, ms_per_step: float, steps: int):
+    """(peak, burst peak, description) in TFLOP/s for the main kernels' roofline.
+
+    The kernels are timed inside the step: for a long step (10 ms or more,
+    back-to-back launches under the power cap) or a timed loop of seconds the
+    sustained peak is the denominator, else the burst peak; the caller reports
+    the fraction of the burst peak as well."""
+    measured = src == "measured"
+    burst = float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS)) if measured else FALLBACK_BF16_TFLOPS
+    sustained = (float(peaks.get("bf16_tflops_sustained", FALLBACK_BF16_TFLOPS_SUSTAINED)) if measured
+                 else FALLBACK_BF16_TFLOPS_SUSTAINED)
+    long_loop = ms_per_step >= 10.0 or steps * ms_per_step >= 1000.0
+    kind = "bf16 dense sustained (kernels timed inside a long step)" if long_loop else "bf16 dense burst"
+    return (sustained if long_loop else burst), burst, f"{kind}, {'of measured' if measured else 'of fallback'}"
+
+
 def whole_job_value(world: int, flops_per_replica: float, ms_max: float) -> float:
     """Whole-job TFLOP/s: every replica's work over the slowest replica's time."""
     return world * flops_per_replica / (ms_max * 1e-3) / 1e12
@@ -655,17 +671,7 @@ def our_arm(args):
             dist.destroy_process_group()
         return 0
 
-    peaks, src = measured_peaks()
-    burst = float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS)) if src == "measured" else FALLBACK_BF16_TFLOPS
-    sustained = (float(peaks.get("bf16_tflops_sustained", FALLBACK_BF16_TFLOPS_SUSTAINED)) if src == "measured"
-                 else FALLBACK_BF16_TFLOPS_SUSTAINED)
-    # The main kernels are timed inside the step: for a long step (10 ms or
-    # more, back-to-back launches under the power cap) or a timed loop of
-    # seconds the sustained peak is the denominator, else the burst peak; the
-    # fraction of the burst peak is reported as well.
-    long_loop = ms_max >= 10.0 or args.steps * ms_max >= 1000.0
-    peak = sustained if long_loop else burst
-    peak_kind = "bf16 dense sustained (kernels timed inside a long step)" if long_loop else "bf16 dense burst"
+    peak, burst, peak_kind = roofline_peak(*measured_peaks(), ms_max, args.steps)
     # per step: the main kernels' summed launch times (a step may launch a
     # main kernel more than once; its flops are those of all its launches)
     fwd_ms = kt["fwd"][0] / args.steps
@@ -678,7 +684,7 @@ def our_arm(args):
                       "frac": ach / peak, "frac_of_burst": ach / burst, "ms_per_step": kms,
                       "launches_per_step": nl / args.steps, "algorithmic_tflop_per_step": kfl / 1e12,
                       "timed_in": kt_src,
-                      "peak_source": f"{peak_kind}, {'of measured' if src == 'measured' else 'of fallback'}"}
+                      "peak_source": peak_kind}
     dominant = bwd_name if bwd_ms >= fwd_ms else fwd_name
     roofline = dict(roof[dominant])
     roofline["kernel"] = dominant

@@ -122,3 +122,32 @@ def test_reference_arm_times_the_oracle_on_a_dense_workload(monkeypatch, capsys)
     assert line["impl"] == "reference" and line["value"] > 0
     assert line["config"]["workload"] == "cfg1_dense_causal_n128_d64"
     assert "[b0, kv head 0, 128 rows]" in line["cpu_baseline"]["sample"]
+
+
+def test_roofline_peak_is_sustained_inside_a_long_step_and_burst_otherwise():
+    b = _bench()
+    peaks = {"bf16_tflops": 2000.0, "bf16_tflops_sustained": 1800.0}
+    # a 34 ms step: the sustained figure, whatever the number of steps
+    assert b.roofline_peak(peaks, "measured", 34.0, 3)[:2] == (1800.0, 2000.0)
+    # a 0.3 ms step: burst, unless the timed loop itself lasts seconds
+    assert b.roofline_peak(peaks, "measured", 0.3, 300)[:2] == (2000.0, 2000.0)
+    assert b.roofline_peak(peaks, "measured", 0.3, 5000)[0] == 1800.0
+    peak, burst, kind = b.roofline_peak({}, "fallback", 34.0, 3)
+    assert (peak, burst) == (b.FALLBACK_BF16_TFLOPS_SUSTAINED, b.FALLBACK_BF16_TFLOPS) and "of fallback" in kind
+
+
+def test_document_sample_stays_within_its_budget():
+    b = _bench()
+    from packed_sequence_flash_gb300 import inputs
+
+    w = inputs.config(5, 0)
+    Hq, Dqk, Dv = w.q.shape[1], w.q.shape[2], w.v.shape[2]
+    per_pair = Hq * (2 * (Dqk + Dv) + 6 * Dqk + 4 * Dv)
+    for gflop in (2.0, 6.6, 100.0):
+        for offset in (0, 5):
+            sub, nd = b.cpu_sample_workload(w, gflop, offset_docs=offset)
+            flops = sum(b.doc_pairs(n, w.window) for n in sub.extra["lengths"]) * per_pair
+            # whole documents within the budget, or the leading tokens of one
+            assert nd >= 1 and (flops <= gflop * 1e9 or len(sub.extra["lengths"]) == 1)
+            _, f, bw = b.workload_flops(sub)
+            assert f + bw == flops
