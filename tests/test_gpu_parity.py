@@ -212,6 +212,37 @@ def test_varlen_many_small_and_empty_segments():
     _varlen_case(11, 128, 128, 2, 1, True, None, nseg=40, max_len=40)
 
 
+@pytest.mark.parametrize("D,Hq,causal,pack,dtype", [(128, 1, True, False, torch.bfloat16),
+                                                    (128, 1, False, False, torch.bfloat16),
+                                                    (64, 2, True, False, torch.float16),
+                                                    (128, 4, True, True, torch.bfloat16)])
+def test_backward_cut_key_tiles_match_oracle(D, Hq, causal, pack, dtype):
+    """One KV head and one long segment plus a short one: the schedule cuts
+    almost every key tile of the long segment into sub-ranges (the per-range
+    step cap is at its floor of 4), so most dK/dV rows come from the convert's
+    sum of partial-sum slots, and the short segment's tiles and the ragged
+    last tile from the attention kernel's direct writes."""
+    Hkv = 1
+    cu_q = np.array([0, 2048 - 37, 2048 - 37 + 150], dtype=np.int32)
+    cu_k = np.array([0, 2048 - 37, 2048 - 37 + 150], dtype=np.int32)
+    Tq, Tk = int(cu_q[-1]), int(cu_k[-1])
+    q = inputs.randn16((Tq, Hq, D), 901, dtype=dtype)
+    k = inputs.randn16((Tk, Hkv, D), 902, dtype=dtype)
+    v = inputs.randn16((Tk, Hkv, D), 903, dtype=dtype)
+    do = inputs.randn16((Tq, Hq, D), 904, dtype=dtype)
+    scale = 1.0 / np.sqrt(D)
+    cq, ck = torch.from_numpy(cu_q).cuda(), torch.from_numpy(cu_k).cuda()
+    mq, mk = int(np.diff(cu_q).max()), int(np.diff(cu_k).max())
+    out, lse = psf.attn_varlen_fwd(cuda(q), cuda(k), cuda(v), cq, ck, mq, mk, scale, causal)
+    out_o, lse_o = oracle.attn_fwd_segments(q, k, v, cu_q, cu_k, scale, causal, None)
+    assert_fwd(out, lse, out_o, lse_o)
+    grads = psf.attn_varlen_bwd(cuda(do), cuda(q), cuda(k), cuda(v), out, lse, cq, ck, mq, mk, scale, causal,
+                                pack_gqa=pack)
+    ref = oracle.attn_bwd_segments(do, q, k, v, out_o, lse_o, cu_q, cu_k, scale, causal, None)
+    assert_grads(grads, ref)
+    assert psf.device_status() == 0
+
+
 @pytest.mark.parametrize("D", [64, 128, 512])
 def test_degenerate_calls_no_rows_no_segments_no_keys(D):
     # Calls with nothing to attend: no query rows, no segments, no keys, and a
