@@ -240,11 +240,16 @@ constexpr int kSplitPerSm = 2;
 // Partial-sum slots: a cut tile has more steps than the cap per sub-range,
 // steps * Hkv / (kSplitPerSm * sms) or more, and fewer than twice its steps
 // over that cap in sub-ranges, so all cut tiles' sub-ranges of one KV head
-// number fewer than 2 * kSplitPerSm * sms / Hkv.
-constexpr int bwd_slot_cap(int sms, int Hkv) { return 2 * kSplitPerSm * sms / Hkv + 2; }
+// number fewer than 2 * kSplitPerSm * sms / Hkv. The last-wave fill cuts at
+// most ceil(sms / (2 Hkv)) more tiles, into four each.
+constexpr int bwd_wave_fill_tiles(int sms, int Hkv) { return sms / (2 * Hkv) + 1; }
+constexpr int bwd_slot_cap(int sms, int Hkv) {
+  return 2 * kSplitPerSm * sms / Hkv + 2 + 4 * bwd_wave_fill_tiles(sms, Hkv);
+}
 size_t bwd_ws_layout(int64_t q_rows, int64_t k_rows, int nseg, int Hq, int Hkv, int Dqk, int Dv, int sms,
                      BwdWorkspace* w, void* base) {
-  const int64_t cap = (k_rows + kBN - 1) / kBN + nseg + (int64_t)kSplitPerSm * sms + 2;
+  const int64_t cap = (k_rows + kBN - 1) / kBN + nseg + (int64_t)kSplitPerSm * sms + 2 +
+                      3 * (int64_t)bwd_wave_fill_tiles(sms, Hkv);
   // Only the head-dim <= 128 kernel cuts key tiles.
   const int slot_cap = (Dqk <= 128 && Dv <= 128) ? bwd_slot_cap(sms, Hkv) : 0;
   size_t off = 256;
@@ -273,6 +278,7 @@ size_t bwd_ws_layout(int64_t q_rows, int64_t k_rows, int nseg, int Hq, int Hkv, 
     w->sc.splits = reinterpret_cast<int4*>(b + splits_off);
     w->sc.item_cap = (int)cap;
     w->sc.slot_cap = slot_cap;
+    w->sc.nctas = sms;
     w->delta = reinterpret_cast<float*>(b + delta_off);
     w->dq_acc = reinterpret_cast<float*>(b + dq_off);
     w->pk = reinterpret_cast<float*>(b + pk_off);

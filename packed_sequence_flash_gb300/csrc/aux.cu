@@ -15,6 +15,9 @@ constexpr int kBuckets = 1024;
 // Per-segment tile prefixes live in shared memory when they fit (the common
 // case); the workspace copy is used beyond that.
 constexpr int kSmemPrefix = 6144;
+// Tiles shorter than this many steps are never cut to fill the last wave (a
+// cut costs a partial-sum slot round trip; short tiles leave short tails).
+constexpr int kWaveFillMinSteps = 256;
 
 // Exclusive block-wide prefix sum over kScanThreads threads; *total gets the sum.
 __device__ int block_excl_scan(int v, int* total) {
@@ -161,10 +164,14 @@ __device__ void schedule_body(SegInfo g, int over_keys, int2* items, int* n_item
 // their own: item_slot[i] is item i's slot (-1: the tile is whole and its
 // unit writes dK/dV itself), and splits[0, n_items[2]) lists the cut tiles as
 // (first key row, key rows, first slot, slot count) for the convert kernel.
+// When tiles of one size carry most of the work, their units (tiles x KV
+// heads) fill whole waves of the nctas CTAs but the last: if that wave is less
+// than half full, enough of those tiles are cut into four that its units
+// become quarter-length ones, which the heaviest-first order takes last.
 // Runs in one 1024-thread block (block 0 of bwd_prep_kernel).
-__device__ void bwd_schedule_body(SegInfo g, int G, int Hkv, int split_target, int4* items, int* item_slot,
-                                  int4* splits, int slot_cap, int* n_items, int* seg_prefix, int item_cap,
-                                  int* status) {
+__device__ void bwd_schedule_body(SegInfo g, int G, int Hkv, int split_target, int nctas, int4* items,
+                                  int* item_slot, int4* splits, int slot_cap, int* n_items, int* seg_prefix,
+                                  int item_cap, int* status) {
   __shared__ int hist[kBuckets];
   __shared__ int start[kBuckets];
   __shared__ int bad;
@@ -229,11 +236,47 @@ __device__ void bwd_schedule_body(SegInfo g, int G, int Hkv, int split_target, i
     const unsigned long long want = (total_steps * (unsigned long long)Hkv + split_target - 1) / split_target;
     smax = (int)(want < 4 ? 4 : (want > 0x7fffffffull ? 0x7fffffffull : want));
   }
-  int nsub_total = 0, slots_mine = 0, cut_mine = 0;
+  // The last wave of the largest uncut tiles' units: `extra` of those tiles
+  // (a fixed choice: ranked by thread, then by each thread's tiles in order)
+  // are cut into four.
+  int lmax_mine = 0;
   for (int x = tid; x < carry; x += kScanThreads) {
     const int s = find_segment(pref, nseg, x);
     const int steps = Gs * tile_cost(g, s, x - pref[s], 1);
-    const int nsub = steps == 0 ? 1 : (int)(((long long)steps + smax - 1) / smax);
+    if (steps <= smax) lmax_mine = max(lmax_mine, steps);
+  }
+  const int lmax = block_max(lmax_mine);
+  int nmax_mine = 0;
+  for (int x = tid; x < carry; x += kScanThreads) {
+    const int s = find_segment(pref, nseg, x);
+    if (Gs * tile_cost(g, s, x - pref[s], 1) == lmax) ++nmax_mine;
+  }
+  int nmax;
+  const int cand_base = block_excl_scan(nmax_mine, &nmax);
+  int extra = 0;
+  if (split_target > 0 && nctas > 0 && lmax >= kWaveFillMinSteps) {
+    const long long units = (long long)nmax * Hkv;
+    if (units >= nctas && 2 * units * lmax >= (long long)(total_steps * (unsigned long long)Hkv)) {
+      const long long r = units % nctas;
+      if (r > 0 && 2 * r <= nctas) extra = (int)((r + Hkv - 1) / Hkv);
+    }
+  }
+  // Sub-ranges of tile x (steps of it): the cap's cut, or four for the chosen
+  // largest tiles; `cand` walks this thread's largest tiles in list order.
+  auto sub_ranges = [&](int steps, int& cand) {
+    int nsub = steps == 0 ? 1 : (int)(((long long)steps + smax - 1) / smax);
+    if (extra > 0 && steps == lmax && nsub == 1) {
+      if (cand < extra) nsub = 4;
+      ++cand;
+    }
+    return nsub;
+  };
+  int nsub_total = 0, slots_mine = 0, cut_mine = 0;
+  int cand = cand_base;
+  for (int x = tid; x < carry; x += kScanThreads) {
+    const int s = find_segment(pref, nseg, x);
+    const int steps = Gs * tile_cost(g, s, x - pref[s], 1);
+    const int nsub = sub_ranges(steps, cand);
     nsub_total += nsub;
     if (nsub > 1) {
       slots_mine += nsub;
@@ -261,11 +304,12 @@ __device__ void bwd_schedule_body(SegInfo g, int G, int Hkv, int split_target, i
   start[rb] = ex;
   hist[rb] = 0;
   __syncthreads();
+  cand = cand_base;
   for (int x = tid; x < carry; x += kScanThreads) {
     const int s = find_segment(pref, nseg, x);
     const int t = x - pref[s];
     const int steps = Gs * tile_cost(g, s, t, 1);
-    const int nsub = steps == 0 ? 1 : (int)(((long long)steps + smax - 1) / smax);
+    const int nsub = sub_ranges(steps, cand);
     if (nsub > 1) {
       const int k0 = cu_k_at(g, s) + t * kBN;
       splits[cut_next++] = make_int4(k0, min(kBN, cu_k_at(g, s + 1) - k0), slot_next, nsub);
@@ -913,13 +957,14 @@ __global__ void __launch_bounds__(kScanThreads) fwd_prep_kernel(SegInfo g, int2*
 // latency behind that traffic.
 template <typename E>
 __global__ void __launch_bounds__(kScanThreads) bwd_prep_kernel(
-    SegInfo g, int G, int Hkv, int split_target, int4* items, int* item_slot, int4* splits, int slot_cap,
-    int* n_items, int* seg_prefix, int item_cap, int* status, const E* dout, int64_t d_sb, int64_t d_ss, int64_t d_sh,
+    SegInfo g, int G, int Hkv, int split_target, int nctas, int4* items, int* item_slot, int4* splits,
+    int slot_cap, int* n_items, int* seg_prefix, int item_cap, int* status, const E* dout, int64_t d_sb, int64_t d_ss,
+    int64_t d_sh,
     const E* out, int64_t o_sb, int64_t o_ss, int64_t o_sh, float* delta, float* dq_acc, int Hq, int Dqk, int Dv,
     uint16_t* dk, uint16_t* dv, int64_t k_sb, int64_t k_ss, int64_t k_sh, int64_t v_sb, int64_t v_ss, int64_t v_sh) {
   if (blockIdx.x == 0)
-    bwd_schedule_body(g, G, Hkv, split_target, items, item_slot, splits, slot_cap, n_items, seg_prefix, item_cap,
-                      status);
+    bwd_schedule_body(g, G, Hkv, split_target, nctas, items, item_slot, splits, slot_cap, n_items, seg_prefix,
+                      item_cap, status);
   else
     bwd_pre_body(g, dout, d_sb, d_ss, d_sh, out, o_sb, o_ss, o_sh, delta, dq_acc, Hq, Dqk, Dv, dk, dv, k_sb, k_ss,
                  k_sh, v_sb, v_ss, v_sh, Hkv, blockIdx.x - 1, gridDim.x - 1);
@@ -991,12 +1036,12 @@ cudaError_t launch_bwd_prep(const SegInfo& g, int G, int Hkv, int split_target, 
   uint16_t* dv16 = static_cast<uint16_t*>(dv);
   if (f16)
     bwd_prep_kernel<__half><<<1 + fill, kScanThreads, 0, st>>>(
-        g, G, Hkv, split_target, sc.items, sc.item_slot, sc.splits, sc.slot_cap, sc.n_items, sc.seg_prefix,
+        g, G, Hkv, split_target, sc.nctas, sc.items, sc.item_slot, sc.splits, sc.slot_cap, sc.n_items, sc.seg_prefix,
         sc.item_cap, status, static_cast<const __half*>(dout), d_sb, d_ss, d_sh, static_cast<const __half*>(out), o_sb,
         o_ss, o_sh, delta, dq_acc, Hq, Dqk, Dv, dk16, dv16, k_sb, k_ss, k_sh, v_sb, v_ss, v_sh);
   else
     bwd_prep_kernel<__nv_bfloat16><<<1 + fill, kScanThreads, 0, st>>>(
-        g, G, Hkv, split_target, sc.items, sc.item_slot, sc.splits, sc.slot_cap, sc.n_items, sc.seg_prefix,
+        g, G, Hkv, split_target, sc.nctas, sc.items, sc.item_slot, sc.splits, sc.slot_cap, sc.n_items, sc.seg_prefix,
         sc.item_cap, status, static_cast<const __nv_bfloat16*>(dout), d_sb, d_ss, d_sh,
         static_cast<const __nv_bfloat16*>(out), o_sb, o_ss, o_sh, delta, dq_acc, Hq, Dqk, Dv, dk16, dv16, k_sb, k_ss,
         k_sh, v_sb, v_ss, v_sh);

@@ -32,6 +32,7 @@ struct BwdSchedule {
   int* seg_prefix;
   int item_cap;
   int slot_cap;
+  int nctas;  // CTAs of the attention kernel the list is for
 };
 // Backward preparation in one launch: the work list (key tiles cut into
 // sub-ranges when split_target > 0; n_items[1] zeroed); Delta = rowsum(dO * O)
