@@ -69,8 +69,8 @@ L2_FLUSH_BYTES = 256 << 20
 # other workloads and once the sources change.
 NCU_TRAFFIC = {
     # the document path's default: a KV head's query heads packed into one tile
-    ("attn_bwd_dual_kernel", "cfg5_doc_causal_t65536_w4096"): ("82604bf037e08438", 34290653696),
-    ("attn_fwd_duo_kernel", "cfg5_doc_causal_t65536_w4096"): ("442dc45691a70b8a", 3773222144),
+    ("attn_bwd_dual_kernel", "cfg5_doc_causal_t65536_w4096"): ("82604bf037e08438", 37635040256),
+    ("attn_fwd_duo_kernel", "cfg5_doc_causal_t65536_w4096"): ("442dc45691a70b8a", 3748686080),
     ("attn_bwd_dual_kernel", "cfg2_doc_causal_t8192_d128"): ("82604bf037e08438", 367806976),
     ("attn_fwd_duo_kernel", "cfg2_doc_causal_t8192_d128"): ("442dc45691a70b8a", 52287232),
     ("attn_bwd_kernel", "cfg4_doc_causal_shard_dqk192_dv128"): ("1e244dae713df4b8", 763610624),
