@@ -18,13 +18,41 @@ cudaError_t run_dual(const BwdParams& p, int grid, cudaStream_t st) {
   attn_bwd_dual_kernel<T, DQK, DV, CAP, PACK><<<grid, 512, smem, st>>>(p);
   return cudaGetLastError();
 }
+// The 512 kernel runs as four-CTA clusters; `grid` CTAs is rounded down to
+// whole clusters and capped at the clusters that can be resident at once
+// (the clusters take their units statically, so a cluster that had to wait
+// for a free GPC would add a whole pass of units at the end).
 template <typename T, int D, bool CAP>
 cudaError_t run_wide(const BwdParams& p, int grid, cudaStream_t st) {
   const int smem = BwdWideCfg<D>::SMEM_BYTES;
-  cudaError_t e =
-      cudaFuncSetAttribute(attn_bwd_wide_kernel<T, D, CAP>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  auto kern = attn_bwd_wide_kernel<T, D, CAP>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  attn_bwd_wide_kernel<T, D, CAP><<<grid, 384, smem, st>>>(p);
+  static int resident[64] = {};  // per device: clusters resident at once (0: not yet asked)
+  int dev = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (resident[dev] == 0) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = BwdWideCfg<D>::NP;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(BwdWideCfg<D>::NP * 64);
+    cfg.blockDim = dim3(384);
+    cfg.dynamicSmemBytes = smem;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if ((e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg)) != cudaSuccess) return e;
+    if (n <= 0) return cudaErrorInvalidConfiguration;
+    resident[dev] = n;
+  }
+  int clusters = grid / BwdWideCfg<D>::NP;
+  if (clusters > resident[dev]) clusters = resident[dev];
+  if (clusters < 1) clusters = 1;
+  kern<<<clusters * BwdWideCfg<D>::NP, 384, smem, st>>>(p);
   return cudaGetLastError();
 }
 template <typename T, int DQK, int DV, bool CAP>

@@ -1,75 +1,127 @@
-// bwd_wide.cuh -- attention backward for Dqk = Dv = 512 (sm_103a).
+// bwd_wide.cuh -- attention backward for Dqk = Dv = 512 (sm_103a), one
+// four-CTA thread-block cluster per (key tile, KV head).
 //   [nemo_automodel.components.attention.ffpa_attention: the FFPA kernel the
 //    page routes head_dim = 512 layers to; `_ffpa_dense_bwd`,
 //    `_ffpa_varlen_bwd`: gradients from the caller-supplied out/lse]
 //
 // The dK and dV accumulators of a 128-row key tile at head dim 512 would need
-// 1024 TMEM columns, twice what an SM has. Each CTA therefore owns one
-// 128-column slice ("part") of dV, dK and dQ and recomputes the full S^T and
-// dP^T for it:
-//   TMEM  dV part [0,128) | dK part [128,256) | S^T, then dQ part [256,384) | dP^T [384,512)
-//   per step (query head of the group x query tile):
-//     S^T  = sum_c K_c Q_c^T over eight 64-column chunks c
-//     dP^T = sum_c V_c dO_c^T
-//     P^T, dS^T -> shared memory (bf16, 128-byte swizzled)
-//     dV_part += P^T dO_part, dK_part += dS^T Q_part, dQ_part = dS K_part
-// K, Q, V and dO all stream through one ring of 16 KB chunks in the order the
-// MMA warp consumes them; nothing but P^T and dS^T stays in shared memory.
-// Roles as in bwd.cuh: warp 0 producer, warp 1 MMA, warp 2 TMEM, warps 4-7
-// compute (+ dK/dV epilogue), warps 8-11 dQ read-out (TMA reduce-add).
+// 1024 TMEM columns, twice what an SM has. The four CTAs of a cluster each own
+// one 128-column part r of the head dim -- the slices K_r, V_r, Q_r, dO_r and
+// part r of dV, dK and dQ -- and split the 512-wide contractions of S and dP:
+//   S_r^T  = K_r Q_r^T,   dP_r^T = V_r dO_r^T        (partial sums over part r)
+// CTA r owns the query columns [32r, 32r + 32) of a step. Every CTA stores the
+// other CTAs' columns of its partial S^T, then of its partial dP^T, into their
+// shared memory (st.async, counted in bytes on the receiver's mbarrier) and
+// adds the three partials it receives to its own columns:
+//   P^T  = exp2(S^T scale log2 e - lse log2 e),   dS^T = P^T (dP^T - Delta)
+// It writes its columns of P^T, as soon as they exist, and then of dS^T
+// (16-bit) into all four CTAs' P^T / dS^T buffers, and each CTA runs
+//   dV_r += P^T dO_r (once P^T is complete),
+//   dK_r += dS^T Q_r,  dQ_r = dS K_r (once dS^T is complete).
+// Each of the five products is computed once, and a CTA streams only its
+// quarter of Q, dO and V per step (K_r stays for the whole key tile). The
+// exchange of S^T overlaps the dP product, and the exchange of dP^T the dV
+// product.
+//
+// TMEM: dV_r [0,128) | dK_r [128,256) | S_r^T, then dQ_r [256,384) | dP_r^T [384,512)
+// Shared memory: K_r, Q_r, dO_r, P^T (32 KB each); the dS^T buffer (32 KB),
+// which holds V_r until the step's dP product has read it; X (48 KB), the
+// columns received from the three other CTAs (S^T, then dP^T); dQ staging
+// (4 KB per read-out warp). P^T and dS^T are four 32-query chunks of 64-byte
+// rows (64-byte swizzle), so CTA r's columns are chunk r: one contiguous 8 KB
+// block.
+// Warps: 0 TMA producer, 1 MMA issuer, 2 TMEM allocator, 4-7 compute (the
+// exchange, P, dS, the dK/dV epilogue), 8-11 dQ read-out (TMA reduce-add).
+//
+// Signals between the CTAs of a cluster (every wait bounded):
+//   rx_s[q]  CTA q has summed the dP^T columns of the previous step: its X
+//            may take this step's S^T columns
+//   rx_d[q]  CTA q has summed this step's S^T columns: its X may take dP^T
+//   recv_full  the three others' columns (48 KB) have landed in X
+//   p_full / ds_full  the three others' P^T / dS^T columns (24 KB each) and
+//            this CTA's own are in place
+// The P^T and dS^T buffers need no signal of their own: a CTA sends its P^T
+// (dS^T) columns of a step only once it holds every other CTA's S^T (dP^T)
+// columns of that step, each sent after that CTA's S (dP) product of the
+// step, which completed after the products that last read its P^T (its V_r,
+// then dS^T).
 #pragma once
 
 #include <math_constants.h>
 
 #include "bwd.cuh"
+#include "cluster.cuh"
 
 namespace psf {
 
 template <int D>
 struct BwdWideCfg {
-  static constexpr int NCH = D / 64;   // chunks per full operand row
-  static constexpr int NP = D / 128;   // column parts
-  static constexpr int NST = 8;        // ring stages
-  static constexpr int RING_OFF = 0;
-  static constexpr int PT_OFF = RING_OFF + NST * kChunkBytes;  // P^T; dQ staging after the dQ MMA
-  static constexpr int DS_OFF = PT_OFF + 2 * kChunkBytes;
-  static constexpr int ROWV_OFF = DS_OFF + 2 * kChunkBytes;
-  static constexpr int SMEM_BYTES = ROWV_OFF + 2 * 4 * 128 * 4 + 1024;
+  static constexpr int NP = D / 128;    // column parts = CTAs per cluster
+  static constexpr int OWN = kBM / NP;  // query columns a CTA owns per step
+  static constexpr int K_OFF = 0;
+  static constexpr int Q_OFF = K_OFF + 2 * kChunkBytes;
+  static constexpr int DO_OFF = Q_OFF + 2 * kChunkBytes;
+  static constexpr int PT_OFF = DO_OFF + 2 * kChunkBytes;
+  static constexpr int DS_OFF = PT_OFF + 2 * kChunkBytes;  // V_r, then dS^T
+  static constexpr int X_OFF = DS_OFF + 2 * kChunkBytes;
+  static constexpr int SLOT_BYTES = kBN * OWN * 4;  // one sender's columns, fp32
+  static constexpr int X_BYTES = (NP - 1) * SLOT_BYTES;
+  static constexpr int STG_OFF = X_OFF + X_BYTES;
+  static constexpr int COL_BYTES = kBN * OWN * 2;           // one CTA's P^T (or dS^T) columns, 16-bit
+  static constexpr int HALF_TX = (NP - 1) * COL_BYTES;      // the three others' columns
+  // The barriers the other CTAs signal, at fixed offsets so that one mapped
+  // base address per CTA reaches them: recv_full, p_full, ds_full, rx_s[4], rx_d[4].
+  static constexpr int BAR_OFF = STG_OFF + 4 * 4096;
+  static constexpr int B_RECV = BAR_OFF, B_P = BAR_OFF + 8, B_DS = BAR_OFF + 16, B_RXS = BAR_OFF + 24,
+                       B_RXD = BAR_OFF + 56;
+  static constexpr int SMEM_BYTES = BAR_OFF + 88 + 1024;
   static constexpr int T_DV = 0, T_DK = 128, T_S = 256, T_DP = 384;
-  static constexpr int CHUNKS_PER_STEP = 4 * NCH + 6;
-  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+  static_assert(NP == 4 && OWN == 32, "laid out for a four-CTA cluster");
+  static_assert(SMEM_BYTES + 512 <= 232448, "shared memory budget (dynamic + static)");
 };
 
 // CAP: logits softcapped (p.softcap > 0); dS carries the cap's 1 - tanh^2.
 template <typename T, int D, bool CAP>
-__global__ void __launch_bounds__(384, 1) attn_bwd_wide_kernel(const __grid_constant__ BwdParams p) {
+__global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(384, 1)
+    attn_bwd_wide_kernel(const __grid_constant__ BwdParams p) {
   using C = BwdWideCfg<D>;
-  constexpr int NST = C::NST;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  float* lse_s = reinterpret_cast<float*>(smem + C::ROWV_OFF);
-  float* dl_s = lse_s + 4 * 128;
 
-  __shared__ uint64_t ring_full[NST], ring_empty[NST];
-  __shared__ uint64_t s_full, dp_full, ds_full, ds_free, dq_full, dq_free, acc_done, acc_free, drain;
+  __shared__ uint64_t k_full, k_empty, q_full, q_empty, v_full, v_free, s_full, dp_full;
+  __shared__ uint64_t dq_full, dq_free, acc_done, acc_free, drain;
+  uint64_t& recv_full = *reinterpret_cast<uint64_t*>(smem + C::B_RECV);
+  uint64_t& p_full = *reinterpret_cast<uint64_t*>(smem + C::B_P);
+  uint64_t& ds_full = *reinterpret_cast<uint64_t*>(smem + C::B_DS);
+  uint64_t* rx_s = reinterpret_cast<uint64_t*>(smem + C::B_RXS);
+  uint64_t* rx_d = reinterpret_cast<uint64_t*>(smem + C::B_RXD);
   __shared__ uint32_t tmem_base_smem;
   __shared__ int abort_flag;
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int rank = (int)cluster_ctarank();
+  const int ncl = (int)cluster_count_x(), cid = (int)cluster_id_x();
   if (threadIdx.x == 0) {
-    for (int i = 0; i < NST; ++i) {
-      mbar_init(&ring_full[i], 1);
-      mbar_init(&ring_empty[i], 1);
-    }
+    mbar_init(&k_full, 1);
+    mbar_init(&k_empty, 1);
+    mbar_init(&q_full, 1);
+    mbar_init(&q_empty, 1);
+    mbar_init(&v_full, 1);
+    mbar_init(&v_free, 1);
     mbar_init(&s_full, 1);
     mbar_init(&dp_full, 1);
-    mbar_init(&ds_full, 4);
-    mbar_init(&ds_free, 1);
     mbar_init(&dq_full, 1);
     mbar_init(&dq_free, 4);
     mbar_init(&acc_done, 1);
     mbar_init(&acc_free, 4);
     mbar_init(&drain, 1);
+    mbar_init(&recv_full, 1);
+    mbar_init(&p_full, 4);
+    mbar_init(&ds_full, 4);
+    for (int q = 0; q < 4; ++q) {
+      mbar_init(&rx_s[q], 4);
+      mbar_init(&rx_d[q], 4);
+    }
     abort_flag = 0;
     fence_mbar_init();
   }
@@ -79,22 +131,16 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_wide_kernel(const __grid_cons
   }
   tc_fence_before();
   __syncthreads();
+  cluster_sync();  // every CTA's barriers exist before any other CTA signals them
   tc_fence_after();
   const uint32_t tmem = tmem_base_smem;
   const Ctl ctl{p.status, p.limit_ns, &abort_flag};
-  const int per_item = p.Hkv * C::NP;
-  const int total = (*p.n_items) * per_item;
+  const int total = (*p.n_items) * p.Hkv;
   const int G = p.Hq / p.Hkv;
   const uint32_t sbase = smem_u32(smem);
-
-  // Work w -> (key tile item, KV head, column part).
-  auto decode = [&](int w, int& part) {
-    const int item = w / per_item;
-    const int rem = w - item * per_item;
-    part = rem % C::NP;
-    return bwd_decode(p, item * p.Hkv + rem / C::NP);
-  };
-
+  // The four CTAs of a cluster walk the same (key tile, KV head) units: in
+  // round i cluster c takes unit i * ncl + c (i even) or i * ncl + ncl - 1 - c.
+  auto unit = [&](int i) { return i * ncl + ((i & 1) ? ncl - 1 - cid : cid); };
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
@@ -102,150 +148,128 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_wide_kernel(const __grid_cons
       tma_prefetch_desc(&p.tm_k);
       tma_prefetch_desc(&p.tm_v);
       tma_prefetch_desc(&p.tm_do);
-      uint32_t it = 0;
+      uint32_t nk = 0, nv = 0, nq = 0;
       bool ok = true;
-      auto load = [&](const CUtensorMap* map, int c0, int row, int h, int b) -> bool {
-        const int st = it % NST;
-        if (!wait_bar(&ring_empty[st], ((it / NST) & 1) ^ 1, ctl)) return false;
-        mbar_arrive_expect_tx(&ring_full[st], kChunkBytes);
-        tma_load_4d(smem + C::RING_OFF + st * kChunkBytes, map, &ring_full[st], c0, row, h, b);
-        ++it;
-        return true;
-      };
-      for (int wi = 0; wi * (int)gridDim.x < total && ok; ++wi) {
-        const int w = snake_item(wi);
+      for (int wi = 0; wi * ncl < total && ok; ++wi) {
+        const int w = unit(wi);
         if (w >= total) continue;
-        int part;
-        const BwdItem t = decode(w, part);
+        const BwdItem t = bwd_decode(p, w);
         if (t.k1 == t.k0) continue;
         const int fk = t.ck0 + t.kt * kBN, bk = fk / p.seg.Sk, sk = fk - bk * p.seg.Sk;
-        {
-          for (int k = t.k0; k < t.k1 && ok; ++k) {
-            const int h = t.hk * G + k / t.nqt, qt = t.qt0 + k % t.nqt;
-            const int fq = t.cq0 + qt * kBM, bq = fq / p.seg.Sq, sq = fq - bq * p.seg.Sq;
-            for (int c = 0; c < C::NCH && ok; ++c) {
-              ok = load(&p.tm_k, c * 64, sk, t.hk, bk) && load(&p.tm_q, c * 64, sq, h, bq);
-            }
-            for (int c = 0; c < C::NCH && ok; ++c) {
-              ok = load(&p.tm_v, c * 64, sk, t.hk, bk) && load(&p.tm_do, c * 64, sq, h, bq);
-            }
-            for (int c = 0; c < 2 && ok; ++c) ok = load(&p.tm_do, part * 128 + c * 64, sq, h, bq);
-            for (int c = 0; c < 2 && ok; ++c) ok = load(&p.tm_q, part * 128 + c * 64, sq, h, bq);
-            for (int c = 0; c < 2 && ok; ++c) ok = load(&p.tm_k, part * 128 + c * 64, sk, t.hk, bk);
+        if (nk > 0 && !wait_bar(&k_empty, (nk - 1) & 1, ctl)) break;
+        mbar_arrive_expect_tx(&k_full, 2 * kChunkBytes);
+        for (int c = 0; c < 2; ++c)
+          tma_load_4d(smem + C::K_OFF + c * kChunkBytes, &p.tm_k, &k_full, rank * 128 + c * 64, sk, t.hk, bk);
+        ++nk;
+        for (int k = t.k0; k < t.k1; ++k) {
+          const int h = t.hk * G + k / t.nqt, qt = t.qt0 + k % t.nqt;
+          const int fq = t.cq0 + qt * kBM, bq = fq / p.seg.Sq, sq = fq - bq * p.seg.Sq;
+          if (nq > 0 && !wait_bar(&q_empty, (nq - 1) & 1, ctl)) {
+            ok = false;
+            break;
           }
+          mbar_arrive_expect_tx(&q_full, 4 * kChunkBytes);
+          for (int c = 0; c < 2; ++c)
+            tma_load_4d(smem + C::Q_OFF + c * kChunkBytes, &p.tm_q, &q_full, rank * 128 + c * 64, sq, h, bq);
+          for (int c = 0; c < 2; ++c)
+            tma_load_4d(smem + C::DO_OFF + c * kChunkBytes, &p.tm_do, &q_full, rank * 128 + c * 64, sq, h, bq);
+          ++nq;
+          // V_r of the step goes into the dS^T buffer once the previous step's dQ product has read it.
+          if (nv > 0 && !wait_bar(&v_free, (nv - 1) & 1, ctl)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&v_full, 2 * kChunkBytes);
+          for (int c = 0; c < 2; ++c)
+            tma_load_4d(smem + C::DS_OFF + c * kChunkBytes, &p.tm_v, &v_full, rank * 128 + c * 64, sk, t.hk, bk);
+          ++nv;
         }
       }
-      for (uint32_t i = it > (uint32_t)NST ? it - NST : 0; i < it; ++i)
-        wait_bar_drain(&ring_full[i % NST], (i / NST) & 1, p.limit_ns);
+      // Loads still in flight after an abort land before the CTA leaves.
+      if (nk > 0) wait_bar_drain(&k_full, (nk - 1) & 1, p.limit_ns);
+      if (nv > 0) wait_bar_drain(&v_full, (nv - 1) & 1, p.limit_ns);
+      if (nq > 0) wait_bar_drain(&q_full, (nq - 1) & 1, p.limit_ns);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t id_sq = idesc_f32acc<T>(128, 128, 0, 0);
-      constexpr uint32_t id_part64 = idesc_f32acc<T>(128, 64, 0, 1);  // dV, dK parts: B MN-major, N = 64
-      constexpr uint32_t id_dq64 = idesc_f32acc<T>(128, 64, 1, 1);         // dQ part: A (dS) M-major
-      const uint32_t ring = sbase + C::RING_OFF, pt_a = sbase + C::PT_OFF, ds_a = sbase + C::DS_OFF;
-      uint32_t it = 0, nz = 0, gstep = 0;
+      constexpr uint32_t id_part = idesc_f32acc<T>(128, 128, 0, 1);  // dV, dK parts: B MN-major
+      constexpr uint32_t id_dq = idesc_f32acc<T>(128, 128, 1, 1);    // dQ part: A (dS) M-major
+      const uint32_t k_a = sbase + C::K_OFF, q_a = sbase + C::Q_OFF, do_a = sbase + C::DO_OFF;
+      const uint32_t pt_a = sbase + C::PT_OFF, ds_a = sbase + C::DS_OFF;  // ds_a: V_r first
+      uint32_t ni = 0, gstep = 0;
       bool ok = true;
-      auto take = [&](uint32_t& addr) -> bool {
-        const int st = it % NST;
-        if (!wait_bar(&ring_full[st], (it / NST) & 1, ctl)) return false;
-        tc_fence_after();
-        addr = ring + st * kChunkBytes;
-        return true;
-      };
-      auto give = [&]() {
-        mma_commit(&ring_empty[it % NST]);
-        ++it;
-      };
-      for (int wi = 0; wi * (int)gridDim.x < total && ok; ++wi) {
-        const int w = snake_item(wi);
+      for (int wi = 0; wi * ncl < total && ok; ++wi) {
+        const int w = unit(wi);
         if (w >= total) continue;
-        int part;
-        const BwdItem t = decode(w, part);
+        const BwdItem t = bwd_decode(p, w);
         if (t.k1 == t.k0) continue;
-        if (nz > 0 && !wait_bar(&acc_free, (nz - 1) & 1, ctl)) break;
-        for (int k = t.k0; k < t.k1 && ok; ++k, ++gstep) {
-          if (gstep > 0 && !wait_bar(&dq_free, (gstep - 1) & 1, ctl)) {
+        if (!wait_bar(&k_full, ni & 1, ctl)) break;
+        for (int k = t.k0; k < t.k1; ++k, ++gstep) {
+          if (!wait_bar(&q_full, gstep & 1, ctl) || (gstep > 0 && !wait_bar(&dq_free, (gstep - 1) & 1, ctl))) {
             ok = false;
             break;
           }
           tc_fence_after();
-          // S^T = sum_c K_c Q_c^T
-          for (int c = 0; c < C::NCH && ok; ++c) {
-            uint32_t ka, qa;
-            if (!take(ka)) { ok = false; break; }
-            const int st_k = it % NST;
-            ++it;
-            if (!take(qa)) { ok = false; break; }
+          // S_r^T = K_r Q_r^T (128-wide contraction)
+#pragma unroll
+          for (int c = 0; c < 2; ++c)
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              mma_ss(tmem + C::T_S, sdesc_sw128(ka + kk * 32, 16, 1024), sdesc_sw128(qa + kk * 32, 16, 1024), id_sq,
-                     (c | kk) != 0);
-            mma_commit(&ring_empty[st_k]);
-            give();
-          }
-          if (!ok) break;
+              mma_ss(tmem + C::T_S, sdesc_sw128(k_a + c * kChunkBytes + kk * 32, 16, 1024),
+                     sdesc_sw128(q_a + c * kChunkBytes + kk * 32, 16, 1024), id_sq, (c | kk) != 0);
           mma_commit(&s_full);
-          // dP^T = sum_c V_c dO_c^T
-          for (int c = 0; c < C::NCH && ok; ++c) {
-            uint32_t va, da;
-            if (!take(va)) { ok = false; break; }
-            const int st_v = it % NST;
-            ++it;
-            if (!take(da)) { ok = false; break; }
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_ss(tmem + C::T_DP, sdesc_sw128(va + kk * 32, 16, 1024), sdesc_sw128(da + kk * 32, 16, 1024), id_sq,
-                     (c | kk) != 0);
-            mma_commit(&ring_empty[st_v]);
-            give();
-          }
-          if (!ok) break;
-          mma_commit(&dp_full);
-          if (!wait_bar(&ds_full, gstep & 1, ctl)) {
+          if (!wait_bar(&v_full, gstep & 1, ctl)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t first = (k == t.k0) ? 1u : 0u;
-          // dV_part += P^T dO_part (two 64-column halves)
-          for (int hh = 0; hh < 2 && ok; ++hh) {
-            uint32_t da;
-            if (!take(da)) { ok = false; break; }
+          // dP_r^T = V_r dO_r^T
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              mma_ss(tmem + C::T_DV + hh * 64, sdesc_sw128(pt_a + (kk >> 2) * kChunkBytes + (kk & 3) * 32, 16, 1024),
-                     sdesc_sw128(da + kk * 2048, kChunkBytes, 1024), id_part64, !(first && kk == 0));
-            give();
-          }
-          // dK_part += dS^T Q_part
-          for (int hh = 0; hh < 2 && ok; ++hh) {
-            uint32_t qa;
-            if (!take(qa)) { ok = false; break; }
+          for (int c = 0; c < 2; ++c)
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              mma_ss(tmem + C::T_DK + hh * 64, sdesc_sw128(ds_a + (kk >> 2) * kChunkBytes + (kk & 3) * 32, 16, 1024),
-                     sdesc_sw128(qa + kk * 2048, kChunkBytes, 1024), id_part64, !(first && kk == 0));
-            give();
+            for (int kk = 0; kk < 4; ++kk)
+              mma_ss(tmem + C::T_DP, sdesc_sw128(ds_a + c * kChunkBytes + kk * 32, 16, 1024),
+                     sdesc_sw128(do_a + c * kChunkBytes + kk * 32, 16, 1024), id_sq, (c | kk) != 0);
+          mma_commit(&dp_full);
+          const bool first = k == t.k0;
+          if ((first && ni > 0 && !wait_bar(&acc_free, (ni - 1) & 1, ctl)) || !wait_bar_cl(&p_full, gstep & 1, ctl)) {
+            ok = false;
+            break;
           }
-          // dQ_part = dS K_part, into the S^T columns (already consumed)
-          for (int hh = 0; hh < 2 && ok; ++hh) {
-            uint32_t ka;
-            if (!take(ka)) { ok = false; break; }
+          // The other CTAs' columns arrived by st.async: make them visible to the tensor core's reads.
+          fence_proxy_async_smem();
+          tc_fence_after();
+          // dV_r += P^T dO_r (B: the two 64-column chunks of dO_r, kChunkBytes apart)
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              mma_ss(tmem + C::T_S + hh * 64, sdesc_sw128(ds_a + kk * 2048, kChunkBytes, 1024),
-                     sdesc_sw128(ka + kk * 2048, kChunkBytes, 1024), id_dq64, kk > 0);
-            give();
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ss(tmem + C::T_DV, sdesc_sw64(pt_a + (kk >> 1) * C::COL_BYTES + (kk & 1) * 32, 16, 512),
+                   sdesc_sw128(do_a + kk * 2048, kChunkBytes, 1024), id_part, !(first && kk == 0));
+          if (!wait_bar_cl(&ds_full, gstep & 1, ctl)) {
+            ok = false;
+            break;
           }
-          if (!ok) break;
-          mma_commit(&ds_free);
+          fence_proxy_async_smem();
+          tc_fence_after();
+          // dK_r += dS^T Q_r
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ss(tmem + C::T_DK, sdesc_sw64(ds_a + (kk >> 1) * C::COL_BYTES + (kk & 1) * 32, 16, 512),
+                   sdesc_sw128(q_a + kk * 2048, kChunkBytes, 1024), id_part, !(first && kk == 0));
+          mma_commit(&q_empty);
+          // dQ_r = dS K_r, into the S^T columns (already read out)
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ss(tmem + C::T_S, sdesc_sw64(ds_a + kk * 1024, C::COL_BYTES, 512),
+                   sdesc_sw128(k_a + kk * 2048, kChunkBytes, 1024), id_dq, kk > 0);
           mma_commit(&dq_full);
+          mma_commit(&v_free);
         }
         if (!ok) break;
         mma_commit(&acc_done);
-        ++nz;
+        mma_commit(&k_empty);
+        ++ni;
       }
       mma_commit(&drain);
       wait_bar_drain(&drain, 0, p.limit_ns);
@@ -253,27 +277,89 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_wide_kernel(const __grid_cons
   } else if (warp >= 4 && warp < 8) {
     // ------------------------------------------------------------ compute warpgroup
     const int wq = warp - 4;
-    const int r = threadIdx.x - 128;
+    const int r = threadIdx.x - 128;  // key row of the tile (TMEM lane)
     const uint32_t lane_base = (uint32_t)(32 * wq) << 16;
-    float* my_lse = lse_s + wq * 128;
-    float* my_dl = dl_s + wq * 128;
-    uint8_t* pt_s = smem + C::PT_OFF;
-    uint8_t* ds_s = smem + C::DS_OFF;
+    const int c0 = rank * C::OWN;  // this CTA's query columns [c0, c0 + 32)
     const float sl2 = p.scale_log2;
     const float cap_c2 = CAP ? p.softcap * 1.4426950408889634f : 0.f;
     const float cap_k1 = CAP ? 2.f * sl2 / p.softcap : 0.f, cap_ic2 = CAP ? 1.f / cap_c2 : 0.f;
-    uint32_t nz = 0, gstep = 0;
+    // Shared-memory base of the other CTAs, in the order rank + 1, rank + 2,
+    // rank + 3; this CTA's columns go to slot 2 - i of the i-th one's X.
+    uint32_t pbase[3];
+    for (int i = 0; i < 3; ++i) pbase[i] = mapa_shared(sbase, (uint32_t)(rank + 1 + i) & 3u);
+    // A slot holds granule u (four consecutive columns) of row r at byte
+    // (u * 128 + r) * 16, so each store instruction of a warp covers 512
+    // contiguous bytes of the receiver's slot.
+    auto px = [&](int i) { return pbase[i] + C::X_OFF + (2 - i) * C::SLOT_BYTES + r * 16; };
+    const uint32_t xrow = sbase + C::X_OFF + r * 16;  // this row of slot 0 (slots SLOT_BYTES apart)
+    // Granule u (8 columns) of row r of this CTA's chunk of P^T / dS^T (64-byte swizzle).
+    auto col_off = [&](int u) { return (uint32_t)(rank * C::COL_BYTES + r * 64 + ((u ^ ((r >> 1) & 3)) << 4)); };
+    // Columns 32 q .. 32 q + 31 of a partial sum in TMEM, to the q-th CTA's X.
+    auto send_cols = [&](int i, uint32_t tcol) {
+      uint32_t v[32];
+      tmem_ld32(tmem + lane_base + tcol, v);
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        st_async_v4(px(i) + u * (kBN * 16), make_uint4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]),
+                    pbase[i] + C::B_RECV);
+    };
+    auto add_recv = [&](float (&a)[32]) {
+#pragma unroll
+      for (int s = 0; s < 3; ++s)
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const uint4 x = lds_v4(xrow + s * C::SLOT_BYTES + u * (kBN * 16));
+          a[4 * u] += __uint_as_float(x.x);
+          a[4 * u + 1] += __uint_as_float(x.y);
+          a[4 * u + 2] += __uint_as_float(x.z);
+          a[4 * u + 3] += __uint_as_float(x.w);
+        }
+    };
+    // This CTA's 16-bit columns (16 packed pairs) into its chunk of the
+    // buffer at `off0` of all four CTAs: the warp writes its 32 rows (2 KB,
+    // contiguous) here, then sends them as 512-byte store instructions. Lane
+    // 0 arrives on the local barrier at `bar_off` (warp 4 with the three
+    // others' bytes).
+    auto share_cols = [&](const uint32_t (&pk)[16], int off0, int bar_off) {
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        *reinterpret_cast<uint4*>(smem + off0 + col_off(u)) =
+            make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+      fence_proxy_async_smem();
+      __syncwarp();
+      const uint32_t rows = off0 + rank * C::COL_BYTES + wq * 2048;
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const uint32_t off = rows + m * 512 + lane * 16;
+        const uint4 v = lds_v4(sbase + off);
+#pragma unroll
+        for (int i = 0; i < 3; ++i) st_async_v4(pbase[i] + off, v, pbase[i] + bar_off);
+      }
+      if (lane == 0) {
+        uint64_t* b = reinterpret_cast<uint64_t*>(smem + bar_off);
+        if (wq == 0)
+          mbar_arrive_expect_tx(b, C::HALF_TX);
+        else
+          mbar_arrive(b);
+      }
+    };
+    // Every lane of the warp: a bounded wait by lane 0 on barrier `bar`.
+    auto warp_wait_cl = [&](uint64_t* bar, uint32_t parity) {
+      bool good = true;
+      if (lane == 0) good = wait_bar_cl(bar, parity, ctl);
+      return __shfl_sync(0xffffffffu, good, 0) != 0;
+    };
+    uint32_t ni = 0, gstep = 0;
     bool ok = true;
-    for (int wi = 0; wi * (int)gridDim.x < total && ok; ++wi) {
-      const int w = snake_item(wi);
+    for (int wi = 0; wi * ncl < total && ok; ++wi) {
+      const int w = unit(wi);
       if (w >= total) continue;
-      int part;
-      const BwdItem t = decode(w, part);
+      const BwdItem t = bwd_decode(p, w);
       const int j = t.kt * kBN + r;
       const bool valid = j < t.n;
       const int fk = t.ck0 + j, bk = fk / p.seg.Sk, sk = fk - bk * p.seg.Sk;
-      T* dk_row = static_cast<T*>(p.dk) + bk * p.k_sb + (int64_t)sk * p.k_ss + t.hk * p.k_sh + part * 128;
-      T* dv_row = static_cast<T*>(p.dv) + bk * p.v_sb + (int64_t)sk * p.v_ss + t.hk * p.v_sh + part * 128;
+      T* dk_row = static_cast<T*>(p.dk) + bk * p.k_sb + (int64_t)sk * p.k_ss + t.hk * p.k_sh + rank * 128;
+      T* dv_row = static_cast<T*>(p.dv) + bk * p.v_sb + (int64_t)sk * p.v_ss + t.hk * p.v_sh + rank * 128;
       if (t.k1 == t.k0) {
         if (valid) {
           for (int c = 0; c < 16; ++c) {
@@ -284,92 +370,139 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_wide_kernel(const __grid_cons
         continue;
       }
       const int delta = t.n - t.m;
-      // lse and Delta of 4 query columns per lane, loaded one step ahead and
-      // left in flight until the step stages them (-inf / 0 outside the segment).
-      auto fetch_rows = [&](int k, float (&lv)[4], float (&dv)[4]) {
+      // lse and Delta of query column c0 + lane, loaded one step ahead and
+      // left in flight until the step reads them (-inf / 0 outside the segment).
+      auto fetch_col = [&](int k, float& lv, float& dv) {
         const int h = t.hk * G + k / t.nqt, i0 = (t.qt0 + k % t.nqt) * kBM;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int qc = lane * 4 + e;
-          const int f = t.cq0 + i0 + qc;
-          const bool in = i0 + qc < t.m && f < p.q_rows;
-          const int fs = in ? f : 0;
-          const int bq = fs / p.seg.Sq, sq = fs - bq * p.seg.Sq;
-          lv[e] = -CUDART_INF_F;
-          dv[e] = 0.f;
-          ldg_pred_f32(lv[e], p.lse + bq * p.l_sb + h * p.l_sh + sq, in);
-          ldg_pred_f32(dv[e], p.delta + (int64_t)h * p.q_rows + fs, in);
-        }
+        const int qc = c0 + lane;
+        const int f = t.cq0 + i0 + qc;
+        const bool in = i0 + qc < t.m && f < p.q_rows;
+        const int fs = in ? f : 0;
+        const int bq = fs / p.seg.Sq, sq = fs - bq * p.seg.Sq;
+        lv = -CUDART_INF_F;
+        dv = 0.f;
+        ldg_pred_f32(lv, p.lse + bq * p.l_sb + h * p.l_sh + sq, in);
+        ldg_pred_f32(dv, p.delta + (int64_t)h * p.q_rows + fs, in);
       };
-      float rlv[4], rdv[4];
-      fetch_rows(t.k0, rlv, rdv);
-      {
-        for (int k = t.k0; k < t.k1; ++k, ++gstep) {
-          const int i0 = (t.qt0 + k % t.nqt) * kBM;
-          int q_lo = p.seg.causal ? j - delta - i0 : -0x40000000;
-          int q_hi = t.m - i0;
-          if (p.seg.window > 0) q_hi = min(q_hi, j - delta + p.seg.window - i0);
-          if (!valid) q_lo = q_hi = 0;
-          const bool masked = q_lo > 0 || q_hi < kBM;
-          // lse * log2(e) (+inf for rows without mass) and Delta for this step.
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int qc = lane * 4 + e;
-            my_lse[qc] = rlv[e] == -CUDART_INF_F ? CUDART_INF_F : rlv[e] * 1.4426950408889634f;
-            my_dl[qc] = rdv[e];
-          }
-          if (k + 1 < t.k1) fetch_rows(k + 1, rlv, rdv);
-          __syncwarp();
-          if (!wait_bar(&s_full, gstep & 1, ctl) || !wait_bar(&dp_full, gstep & 1, ctl) ||
-              (gstep > 0 && !wait_bar(&ds_free, (gstep - 1) & 1, ctl))) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-#pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
-            uint32_t sv[32], pv[32];
-            tmem_ld32(tmem + lane_base + C::T_S + c * 32, sv);
-            tmem_ld32(tmem + lane_base + C::T_DP + c * 32, pv);
-            uint32_t pk[16], dk2[16];
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              float pr[2], dr[2];
-#pragma unroll
-              for (int u = 0; u < 2; ++u) {
-                const int qc = c * 32 + 2 * e + u;
-                float pe, fe = 1.f;
-                if constexpr (CAP) {
-                  const float y = softcap_log2(__uint_as_float(sv[2 * e + u]), cap_k1, cap_c2);
-                  const float tt = y * cap_ic2;
-                  fe = fmaf(-tt, tt, 1.f);
-                  pe = ex2_approx(y - my_lse[qc]);
-                } else {
-                  pe = ex2_approx(fmaf(__uint_as_float(sv[2 * e + u]), sl2, -my_lse[qc]));
-                }
-                if (masked && (qc < q_lo || qc >= q_hi)) pe = 0.f;
-                pr[u] = pe;
-                dr[u] = pe * fe * (__uint_as_float(pv[2 * e + u]) - my_dl[qc]);
-              }
-              pk[e] = pack2<T>(pr[0], pr[1]);
-              dk2[e] = pack2<T>(dr[0], dr[1]);
-            }
-            const int chunk = c >> 1, g0 = (c & 1) * 4;
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const uint32_t off = chunk * kChunkBytes + sw128_offset(r, g0 + u);
-              *reinterpret_cast<uint4*>(pt_s + off) = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-              *reinterpret_cast<uint4*>(ds_s + off) = make_uint4(dk2[4 * u], dk2[4 * u + 1], dk2[4 * u + 2], dk2[4 * u + 3]);
-            }
-          }
-          fence_proxy_async_smem();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&ds_full);
+      float rlv, rdv;
+      fetch_col(t.k0, rlv, rdv);
+      for (int k = t.k0; k < t.k1; ++k, ++gstep) {
+        const int i0 = (t.qt0 + k % t.nqt) * kBM;
+        int q_lo = p.seg.causal ? j - delta - i0 : -0x40000000;
+        int q_hi = t.m - i0;
+        if (p.seg.window > 0) q_hi = min(q_hi, j - delta + p.seg.window - i0);
+        if (!valid) q_lo = q_hi = 0;
+        const bool masked = q_lo > c0 || q_hi < c0 + C::OWN;
+        const float l2 = rlv == -CUDART_INF_F ? CUDART_INF_F : rlv * 1.4426950408889634f;
+        const float dl = rdv;
+        if (k + 1 < t.k1) fetch_col(k + 1, rlv, rdv);
+        if (!wait_bar(&s_full, gstep & 1, ctl)) {
+          ok = false;
+          break;
         }
+        tc_fence_after();
+        // ---- S^T: the other CTAs' columns of the partial sum go to them
+        bool good = true;
+        for (int i = 0; i < 3 && good; ++i) {
+          const int q = (rank + 1 + i) & 3;
+          if (gstep > 0 && !(good = warp_wait_cl(&rx_s[q], (gstep - 1) & 1))) break;
+          send_cols(i, C::T_S + 32 * q);
+        }
+        if (!good) {
+          ok = false;
+          break;
+        }
+        float acc[32];
+        {
+          uint32_t v[32];
+          tmem_ld32(tmem + lane_base + C::T_S + c0, v);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) acc[e] = __uint_as_float(v[e]);
+        }
+        if (wq == 0 && lane == 0) mbar_arrive_expect_tx(&recv_full, C::X_BYTES);
+        if (!wait_bar_cl(&recv_full, 0, ctl)) {
+          ok = false;
+          break;
+        }
+        add_recv(acc);
+        // P (16-bit, packed, for P^T) and P (1 - tanh^2) in acc (for dS)
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          float pr[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int jj = 2 * e + u, qc = c0 + jj;
+            const float l2j = __shfl_sync(0xffffffffu, l2, jj);
+            float pe, fe = 1.f;
+            if constexpr (CAP) {
+              const float y = softcap_log2(acc[jj], cap_k1, cap_c2);
+              const float tt = y * cap_ic2;
+              fe = fmaf(-tt, tt, 1.f);
+              pe = ex2_approx(y - l2j);
+            } else {
+              pe = ex2_approx(fmaf(acc[jj], sl2, -l2j));
+            }
+            if (masked && (qc < q_lo || qc >= q_hi)) pe = 0.f;
+            pr[u] = pe;
+            acc[jj] = pe * fe;
+          }
+          pk[e] = pack2<T>(pr[0], pr[1]);
+        }
+        // This warp's rows of X are summed: the others may send dP^T columns.
+        __syncwarp();
+        if (lane == 0)
+          for (int i = 0; i < 3; ++i) mbar_arrive_remote(pbase[i] + C::B_RXD + 8 * rank);
+        // ---- dP^T: the same exchange as S^T
+        if (!wait_bar(&dp_full, gstep & 1, ctl)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        for (int i = 0; i < 3 && good; ++i) {
+          const int q = (rank + 1 + i) & 3;
+          if (!(good = warp_wait_cl(&rx_d[q], gstep & 1))) break;
+          send_cols(i, C::T_DP + 32 * q);
+        }
+        if (!good) {
+          ok = false;
+          break;
+        }
+        // ---- P^T columns to all four CTAs (the dV product can start) while
+        // the other CTAs' dP^T columns are on their way
+        share_cols(pk, C::PT_OFF, C::B_P);
+        float dpa[32];
+        {
+          uint32_t v[32];
+          tmem_ld32(tmem + lane_base + C::T_DP + c0, v);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) dpa[e] = __uint_as_float(v[e]);
+        }
+        // Last TMEM read of the step: the MMA may overwrite S^T and dP^T once
+        // the ds_full arrival below is seen.
+        tc_fence_before();
+        if (wq == 0 && lane == 0) mbar_arrive_expect_tx(&recv_full, C::X_BYTES);
+        if (!wait_bar_cl(&recv_full, 1, ctl)) {
+          ok = false;
+          break;
+        }
+        add_recv(dpa);
+        // This warp's rows of X are summed: the others may send the next step's S^T columns.
+        __syncwarp();
+        if (lane == 0)
+          for (int i = 0; i < 3; ++i) mbar_arrive_remote(pbase[i] + C::B_RXS + 8 * rank);
+        uint32_t dk2[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const float d0 = acc[2 * e] * (dpa[2 * e] - __shfl_sync(0xffffffffu, dl, 2 * e));
+          const float d1 = acc[2 * e + 1] * (dpa[2 * e + 1] - __shfl_sync(0xffffffffu, dl, 2 * e + 1));
+          dk2[e] = pack2<T>(d0, d1);
+        }
+        // ---- dS^T columns to all four CTAs (dK and dQ can start)
+        share_cols(dk2, C::DS_OFF, C::B_DS);
       }
       if (!ok) break;
-      if (!wait_bar(&acc_done, nz & 1, ctl)) break;
+      if (!wait_bar(&acc_done, ni & 1, ctl)) break;
       tc_fence_after();
       const float sc = p.scale;
 #pragma unroll 1
@@ -396,56 +529,49 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_wide_kernel(const __grid_cons
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_free);
-      ++nz;
+      ++ni;
     }
   } else if (warp >= 8) {
     // ------------------------------------------------------------ dQ read-out
     const int wq = warp - 8;
     const uint32_t lane_base = (uint32_t)(32 * wq) << 16;
-    uint8_t* stg = smem + C::PT_OFF + wq * 8192;
+    uint8_t* box = smem + C::STG_OFF + wq * 4096;
     uint32_t gstep = 0;
     bool ok = true;
-    for (int wi = 0; wi * (int)gridDim.x < total && ok; ++wi) {
-      const int w = snake_item(wi);
+    for (int wi = 0; wi * ncl < total && ok; ++wi) {
+      const int w = unit(wi);
       if (w >= total) continue;
-      int part;
-      const BwdItem t = decode(w, part);
+      const BwdItem t = bwd_decode(p, w);
       if (t.k1 == t.k0) continue;
-      {
-        for (int k = t.k0; k < t.k1; ++k, ++gstep) {
-          const int h = t.hk * G + k / t.nqt, qt = t.qt0 + k % t.nqt;
-          if (!wait_bar(&dq_full, gstep & 1, ctl)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const int fq = t.cq0 + qt * kBM + 32 * wq, bq = fq / p.seg.Sq, sq = fq - bq * p.seg.Sq;
-#pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
-            uint32_t a[32];
-            tmem_ld32(tmem + lane_base + C::T_S + c * 32, a);
-            uint8_t* box = stg + (c & 1) * 4096;
-            if (c >= 2) {
-              if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-              __syncwarp();
-            }
+      for (int k = t.k0; k < t.k1; ++k, ++gstep) {
+        const int h = t.hk * G + k / t.nqt, qt = t.qt0 + k % t.nqt;
+        if (!wait_bar(&dq_full, gstep & 1, ctl)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t a[4][32];
 #pragma unroll
-            for (int u = 0; u < 8; ++u)
-              *reinterpret_cast<uint4*>(box + sw128_offset(lane, u)) =
-                  make_uint4(a[4 * u], a[4 * u + 1], a[4 * u + 2], a[4 * u + 3]);
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-              tma_reduce_add_4d(&p.tm_dq, box, part * 128 + c * 32, sq, h, bq);
-              bulk_commit_group();
-            }
-          }
-          // The staging sits in the P^T buffer: the next step may write P^T
-          // only after these reduces have read it.
+        for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lane_base + C::T_S + c * 32, a[c]);
+        // dQ is in registers: the next step's S^T may take its columns.
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&dq_free);
+        const int fq = t.cq0 + qt * kBM + 32 * wq, bq = fq / p.seg.Sq, sq = fq - bq * p.seg.Sq;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
           if (lane == 0) bulk_wait_group_read0();
-          tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&dq_free);
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            *reinterpret_cast<uint4*>(box + sw128_offset(lane, u)) =
+                make_uint4(a[c][4 * u], a[c][4 * u + 1], a[c][4 * u + 2], a[c][4 * u + 3]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_reduce_add_4d(&p.tm_dq, box, rank * 128 + c * 32, sq, h, bq);
+            bulk_commit_group();
+          }
         }
       }
     }
@@ -453,6 +579,8 @@ __global__ void __launch_bounds__(384, 1) attn_bwd_wide_kernel(const __grid_cons
   }
   tc_fence_before();
   __syncthreads();
+  // No CTA leaves while another may still store into or signal its shared memory.
+  cluster_sync();
   if (warp == 2) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
