@@ -75,7 +75,7 @@ NCU_TRAFFIC = {
     ("attn_fwd_duo_kernel", "cfg2_doc_causal_t8192_d128"): ("442dc45691a70b8a", 52287232),
     ("attn_bwd_kernel", "cfg4_doc_causal_shard_dqk192_dv128"): ("1e244dae713df4b8", 763610624),
     ("attn_fwd_pair_kernel", "cfg4_doc_causal_shard_dqk192_dv128"): ("13e4409971f3398f", 181557504),
-    ("attn_bwd_wide_kernel", "cfg3_dense_causal_n4096_d512"): ("0e687bdd03301372", 943909120),
+    ("attn_bwd_wide_kernel", "cfg3_dense_causal_n4096_d512"): ("b8c1558d24e70732", 934560000),
     ("attn_fwd_kernel", "cfg3_dense_causal_n4096_d512"): ("b62559f39a5d9209", 126914048),
 }
 

@@ -20,11 +20,13 @@
 //   dK_r += dS^T Q_r,  dQ_r = dS K_r (once dS^T is complete).
 // Each of the five products is computed once, and a CTA streams only its
 // quarter of Q, dO and V per step (K_r stays for the whole key tile). The
-// exchange of S^T overlaps the dP product, and the exchange of dP^T the dV
-// product.
+// exchange of S^T overlaps the dP product, the exchange of dP^T the dV
+// product, and the next step's S^T product (its Q_r in the buffer this
+// step's dO_r leaves after dV) the exchange of dP^T and dS^T.
 //
-// TMEM: dV_r [0,128) | dK_r [128,256) | S_r^T, then dQ_r [256,384) | dP_r^T [384,512)
-// Shared memory: K_r, Q_r, dO_r, P^T (32 KB each); the dS^T buffer (32 KB),
+// TMEM: dV_r [0,128) | dK_r [128,256) | S_r^T [256,384) | dP_r^T, then dQ_r [384,512)
+// Shared memory: K_r, two buffers that take Q_r and dO_r in turn, P^T (32 KB
+// each); the dS^T buffer (32 KB),
 // which holds V_r until the step's dP product has read it; X (48 KB), the
 // columns received from the three other CTAs (S^T, then dP^T); dQ staging
 // (4 KB per read-out warp). P^T and dS^T are four 32-query chunks of 64-byte
@@ -59,9 +61,12 @@ struct BwdWideCfg {
   static constexpr int NP = D / 128;    // column parts = CTAs per cluster
   static constexpr int OWN = kBM / NP;  // query columns a CTA owns per step
   static constexpr int K_OFF = 0;
-  static constexpr int Q_OFF = K_OFF + 2 * kChunkBytes;
-  static constexpr int DO_OFF = Q_OFF + 2 * kChunkBytes;
-  static constexpr int PT_OFF = DO_OFF + 2 * kChunkBytes;
+  // Two 32 KB buffers that take Q_r and dO_r in turn: step g's Q_r in buffer
+  // g & 1 and its dO_r in the other, so the next step's Q_r loads as soon as
+  // this step's dV product has read dO_r.
+  static constexpr int QD_OFF = K_OFF + 2 * kChunkBytes;
+  static constexpr int QD_BYTES = 2 * kChunkBytes;
+  static constexpr int PT_OFF = QD_OFF + 2 * QD_BYTES;
   static constexpr int DS_OFF = PT_OFF + 2 * kChunkBytes;  // V_r, then dS^T
   static constexpr int X_OFF = DS_OFF + 2 * kChunkBytes;
   static constexpr int SLOT_BYTES = kBN * OWN * 4;  // one sender's columns, fp32
@@ -75,7 +80,7 @@ struct BwdWideCfg {
   static constexpr int B_RECV = BAR_OFF, B_P = BAR_OFF + 8, B_DS = BAR_OFF + 16, B_RXS = BAR_OFF + 24,
                        B_RXD = BAR_OFF + 56;
   static constexpr int SMEM_BYTES = BAR_OFF + 88 + 1024;
-  static constexpr int T_DV = 0, T_DK = 128, T_S = 256, T_DP = 384;
+  static constexpr int T_DV = 0, T_DK = 128, T_S = 256, T_DP = 384;  // T_DP: dP^T, then dQ
   static_assert(NP == 4 && OWN == 32, "laid out for a four-CTA cluster");
   static_assert(SMEM_BYTES + 512 <= 232448, "shared memory budget (dynamic + static)");
 };
@@ -88,7 +93,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(384, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
-  __shared__ uint64_t k_full, k_empty, q_full, q_empty, v_full, v_free, s_full, dp_full;
+  __shared__ uint64_t k_full, k_empty, qd_full[2], qd_empty[2], v_full, v_free, s_full, s_read, dp_full;
   __shared__ uint64_t dq_full, dq_free, acc_done, acc_free, drain;
   uint64_t& recv_full = *reinterpret_cast<uint64_t*>(smem + C::B_RECV);
   uint64_t& p_full = *reinterpret_cast<uint64_t*>(smem + C::B_P);
@@ -104,8 +109,11 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(384, 1)
   if (threadIdx.x == 0) {
     mbar_init(&k_full, 1);
     mbar_init(&k_empty, 1);
-    mbar_init(&q_full, 1);
-    mbar_init(&q_empty, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&qd_full[b], 1);
+      mbar_init(&qd_empty[b], 1);
+    }
+    mbar_init(&s_read, 4);
     mbar_init(&v_full, 1);
     mbar_init(&v_free, 1);
     mbar_init(&s_full, 1);
@@ -148,7 +156,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(384, 1)
       tma_prefetch_desc(&p.tm_k);
       tma_prefetch_desc(&p.tm_v);
       tma_prefetch_desc(&p.tm_do);
-      uint32_t nk = 0, nv = 0, nq = 0;
+      uint32_t nk = 0, nv = 0, ng = 0, nqd[2] = {0, 0};
       bool ok = true;
       for (int wi = 0; wi * ncl < total && ok; ++wi) {
         const int w = unit(wi);
@@ -164,16 +172,24 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(384, 1)
         for (int k = t.k0; k < t.k1; ++k) {
           const int h = t.hk * G + k / t.nqt, qt = t.qt0 + k % t.nqt;
           const int fq = t.cq0 + qt * kBM, bq = fq / p.seg.Sq, sq = fq - bq * p.seg.Sq;
-          if (nq > 0 && !wait_bar(&q_empty, (nq - 1) & 1, ctl)) {
-            ok = false;
-            break;
+          // Q_r into buffer g & 1 (it held dO_r of step g - 1: free after that
+          // step's dV), dO_r into the other (it held Q_r of step g - 1: free
+          // after that step's dK).
+          const int b0 = ng & 1;
+          for (int x = 0; x < 2 && ok; ++x) {
+            const int b = b0 ^ x;
+            if (ng > 0 && !wait_bar(&qd_empty[b], (ng - 1) & 1, ctl)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&qd_full[b], C::QD_BYTES);
+            for (int c = 0; c < 2; ++c)
+              tma_load_4d(smem + C::QD_OFF + b * C::QD_BYTES + c * kChunkBytes, x == 0 ? &p.tm_q : &p.tm_do,
+                          &qd_full[b], rank * 128 + c * 64, sq, h, bq);
+            ++nqd[b];
           }
-          mbar_arrive_expect_tx(&q_full, 4 * kChunkBytes);
-          for (int c = 0; c < 2; ++c)
-            tma_load_4d(smem + C::Q_OFF + c * kChunkBytes, &p.tm_q, &q_full, rank * 128 + c * 64, sq, h, bq);
-          for (int c = 0; c < 2; ++c)
-            tma_load_4d(smem + C::DO_OFF + c * kChunkBytes, &p.tm_do, &q_full, rank * 128 + c * 64, sq, h, bq);
-          ++nq;
+          if (!ok) break;
+          ++ng;
           // V_r of the step goes into the dS^T buffer once the previous step's dQ product has read it.
           if (nv > 0 && !wait_bar(&v_free, (nv - 1) & 1, ctl)) {
             ok = false;
@@ -188,7 +204,8 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(384, 1)
       // Loads still in flight after an abort land before the CTA leaves.
       if (nk > 0) wait_bar_drain(&k_full, (nk - 1) & 1, p.limit_ns);
       if (nv > 0) wait_bar_drain(&v_full, (nv - 1) & 1, p.limit_ns);
-      if (nq > 0) wait_bar_drain(&q_full, (nq - 1) & 1, p.limit_ns);
+      for (int b = 0; b < 2; ++b)
+        if (nqd[b] > 0) wait_bar_drain(&qd_full[b], (nqd[b] - 1) & 1, p.limit_ns);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -196,8 +213,18 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(384, 1)
       constexpr uint32_t id_sq = idesc_f32acc<T>(128, 128, 0, 0);
       constexpr uint32_t id_part = idesc_f32acc<T>(128, 128, 0, 1);  // dV, dK parts: B MN-major
       constexpr uint32_t id_dq = idesc_f32acc<T>(128, 128, 1, 1);    // dQ part: A (dS) M-major
-      const uint32_t k_a = sbase + C::K_OFF, q_a = sbase + C::Q_OFF, do_a = sbase + C::DO_OFF;
+      const uint32_t k_a = sbase + C::K_OFF, qd_a = sbase + C::QD_OFF;
       const uint32_t pt_a = sbase + C::PT_OFF, ds_a = sbase + C::DS_OFF;  // ds_a: V_r first
+      // S_r^T = K_r Q_r^T (128-wide contraction) from the buffer at q_a
+      auto issue_s = [&](uint32_t q_a) {
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ss(tmem + C::T_S, sdesc_sw128(k_a + c * kChunkBytes + kk * 32, 16, 1024),
+                   sdesc_sw128(q_a + c * kChunkBytes + kk * 32, 16, 1024), id_sq, (c | kk) != 0);
+        mma_commit(&s_full);
+      };
       uint32_t ni = 0, gstep = 0;
       bool ok = true;
       for (int wi = 0; wi * ncl < total && ok; ++wi) {
@@ -206,21 +233,22 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(384, 1)
         const BwdItem t = bwd_decode(p, w);
         if (t.k1 == t.k0) continue;
         if (!wait_bar(&k_full, ni & 1, ctl)) break;
+        bool s_issued = false;  // this step's S^T already issued during the previous step
         for (int k = t.k0; k < t.k1; ++k, ++gstep) {
-          if (!wait_bar(&q_full, gstep & 1, ctl) || (gstep > 0 && !wait_bar(&dq_free, (gstep - 1) & 1, ctl))) {
-            ok = false;
-            break;
+          const int b = gstep & 1;
+          const uint32_t q_a = qd_a + b * C::QD_BYTES, do_a = qd_a + (b ^ 1) * C::QD_BYTES;
+          if (!s_issued) {
+            if (!wait_bar(&qd_full[b], gstep & 1, ctl) || (gstep > 0 && !wait_bar(&s_read, (gstep - 1) & 1, ctl))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_s(q_a);
           }
-          tc_fence_after();
-          // S_r^T = K_r Q_r^T (128-wide contraction)
-#pragma unroll
-          for (int c = 0; c < 2; ++c)
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_ss(tmem + C::T_S, sdesc_sw128(k_a + c * kChunkBytes + kk * 32, 16, 1024),
-                     sdesc_sw128(q_a + c * kChunkBytes + kk * 32, 16, 1024), id_sq, (c | kk) != 0);
-          mma_commit(&s_full);
-          if (!wait_bar(&v_full, gstep & 1, ctl)) {
+          s_issued = false;
+          // dP^T's columns hold the previous step's dQ until it has been read out.
+          if (!wait_bar(&v_full, gstep & 1, ctl) || !wait_bar(&qd_full[b ^ 1], gstep & 1, ctl) ||
+              (gstep > 0 && !wait_bar(&dq_free, (gstep - 1) & 1, ctl))) {
             ok = false;
             break;
           }
@@ -246,6 +274,18 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(384, 1)
           for (int kk = 0; kk < 8; ++kk)
             mma_ss(tmem + C::T_DV, sdesc_sw64(pt_a + (kk >> 1) * C::COL_BYTES + (kk & 1) * 32, 16, 512),
                    sdesc_sw128(do_a + kk * 2048, kChunkBytes, 1024), id_part, !(first && kk == 0));
+          mma_commit(&qd_empty[b ^ 1]);
+          // The next step's S^T (same key tile) as soon as its Q_r has landed
+          // and this step's S^T has been read out, ahead of dK and dQ.
+          if (k + 1 < t.k1) {
+            if (!wait_bar(&qd_full[b ^ 1], (gstep + 1) & 1, ctl) || !wait_bar(&s_read, gstep & 1, ctl)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_s(do_a);
+            s_issued = true;
+          }
           if (!wait_bar_cl(&ds_full, gstep & 1, ctl)) {
             ok = false;
             break;
@@ -257,11 +297,11 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(384, 1)
           for (int kk = 0; kk < 8; ++kk)
             mma_ss(tmem + C::T_DK, sdesc_sw64(ds_a + (kk >> 1) * C::COL_BYTES + (kk & 1) * 32, 16, 512),
                    sdesc_sw128(q_a + kk * 2048, kChunkBytes, 1024), id_part, !(first && kk == 0));
-          mma_commit(&q_empty);
-          // dQ_r = dS K_r, into the S^T columns (already read out)
+          mma_commit(&qd_empty[b]);
+          // dQ_r = dS K_r, into the dP^T columns (already read out)
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            mma_ss(tmem + C::T_S, sdesc_sw64(ds_a + kk * 1024, C::COL_BYTES, 512),
+            mma_ss(tmem + C::T_DP, sdesc_sw64(ds_a + kk * 1024, C::COL_BYTES, 512),
                    sdesc_sw128(k_a + kk * 2048, kChunkBytes, 1024), id_dq, kk > 0);
           mma_commit(&dq_full);
           mma_commit(&v_free);
@@ -325,7 +365,6 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(384, 1)
       for (int u = 0; u < 4; ++u)
         *reinterpret_cast<uint4*>(smem + off0 + col_off(u)) =
             make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-      fence_proxy_async_smem();
       __syncwarp();
       const uint32_t rows = off0 + rank * C::COL_BYTES + wq * 2048;
 #pragma unroll
@@ -335,6 +374,9 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(384, 1)
 #pragma unroll
         for (int i = 0; i < 3; ++i) st_async_v4(pbase[i] + off, v, pbase[i] + bar_off);
       }
+      // The local copy is read by this CTA's tensor core.
+      fence_proxy_async_smem();
+      __syncwarp();
       if (lane == 0) {
         uint64_t* b = reinterpret_cast<uint64_t*>(smem + bar_off);
         if (wq == 0)
@@ -419,6 +461,10 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(384, 1)
 #pragma unroll
           for (int e = 0; e < 32; ++e) acc[e] = __uint_as_float(v[e]);
         }
+        // S^T is read out: the next step's S^T may take its columns.
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s_read);
         if (wq == 0 && lane == 0) mbar_arrive_expect_tx(&recv_full, C::X_BYTES);
         if (!wait_bar_cl(&recv_full, 0, ctl)) {
           ok = false;
@@ -453,6 +499,10 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(384, 1)
         __syncwarp();
         if (lane == 0)
           for (int i = 0; i < 3; ++i) mbar_arrive_remote(pbase[i] + C::B_RXD + 8 * rank);
+        // ---- P^T columns to all four CTAs (the dV product can start); the dP
+        // product, whose dO_r and V_r load only after the previous step's dK
+        // and dQ, is usually still running
+        share_cols(pk, C::PT_OFF, C::B_P);
         // ---- dP^T: the same exchange as S^T
         if (!wait_bar(&dp_full, gstep & 1, ctl)) {
           ok = false;
@@ -468,9 +518,6 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(384, 1)
           ok = false;
           break;
         }
-        // ---- P^T columns to all four CTAs (the dV product can start) while
-        // the other CTAs' dP^T columns are on their way
-        share_cols(pk, C::PT_OFF, C::B_P);
         float dpa[32];
         {
           uint32_t v[32];
@@ -552,8 +599,8 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(384, 1)
         tc_fence_after();
         uint32_t a[4][32];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lane_base + C::T_S + c * 32, a[c]);
-        // dQ is in registers: the next step's S^T may take its columns.
+        for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lane_base + C::T_DP + c * 32, a[c]);
+        // dQ is in registers: the next step's dP^T may take its columns.
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&dq_free);
