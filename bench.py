@@ -69,14 +69,14 @@ L2_FLUSH_BYTES = 256 << 20
 # other workloads and once the sources change.
 NCU_TRAFFIC = {
     # the document path's default: a KV head's query heads packed into one tile
-    ("attn_bwd_dual_kernel", "cfg5_doc_causal_t65536_w4096"): ("82604bf037e08438", 37635040256),
-    ("attn_fwd_duo_kernel", "cfg5_doc_causal_t65536_w4096"): ("442dc45691a70b8a", 3748686080),
-    ("attn_bwd_dual_kernel", "cfg2_doc_causal_t8192_d128"): ("82604bf037e08438", 367806976),
-    ("attn_fwd_duo_kernel", "cfg2_doc_causal_t8192_d128"): ("442dc45691a70b8a", 52287232),
-    ("attn_bwd_kernel", "cfg4_doc_causal_shard_dqk192_dv128"): ("1e244dae713df4b8", 763610624),
-    ("attn_fwd_pair_kernel", "cfg4_doc_causal_shard_dqk192_dv128"): ("13e4409971f3398f", 181557504),
-    ("attn_bwd_wide_kernel", "cfg3_dense_causal_n4096_d512"): ("b8c1558d24e70732", 934560000),
-    ("attn_fwd_kernel", "cfg3_dense_causal_n4096_d512"): ("b62559f39a5d9209", 126914048),
+    ("attn_fwd_duo_kernel", "cfg5_doc_causal_t65536_w4096"): ("88fbcdf5a2921253", 3777393920),
+    ("attn_bwd_dual_kernel", "cfg5_doc_causal_t65536_w4096"): ("3ecea61619644db9", 35805310720),
+    ("attn_fwd_duo_kernel", "cfg2_doc_causal_t8192_d128"): ("88fbcdf5a2921253", 52276992),
+    ("attn_bwd_dual_kernel", "cfg2_doc_causal_t8192_d128"): ("3ecea61619644db9", 362997760),
+    ("attn_fwd_pair_kernel", "cfg4_doc_causal_shard_dqk192_dv128"): ("5837d1098189c960", 185433856),
+    ("attn_bwd_kernel", "cfg4_doc_causal_shard_dqk192_dv128"): ("26951fb59a1df2f0", 775970048),
+    ("attn_fwd_kernel", "cfg3_dense_causal_n4096_d512"): ("776e62360b806358", 127129344),
+    ("attn_bwd_wide_kernel", "cfg3_dense_causal_n4096_d512"): ("df2714e7e1f258bb", 964107776),
 }
 
 
@@ -88,10 +88,10 @@ def ncu_traffic(kernel: str, workload: str):
 # Sources each main kernel is compiled from (for the hash above).
 KERNEL_SOURCES = {
     "attn_fwd_duo_kernel": ("fwd.cuh", "fwd_duo.cuh", "common.cuh", "ptx.cuh"),
-    "attn_fwd_kernel": ("fwd.cuh", "common.cuh", "ptx.cuh"),
+    "attn_fwd_kernel": ("fwd.cuh", "fwd512.cuh", "common.cuh", "ptx.cuh"),
     "attn_fwd_pair_kernel": ("fwd.cuh", "fwd_pair.cuh", "common.cuh", "ptx.cuh"),
     "attn_bwd_dual_kernel": ("bwd.cuh", "bwd_dual.cuh", "common.cuh", "ptx.cuh"),
-    "attn_bwd_kernel": ("bwd.cuh", "common.cuh", "ptx.cuh"),
+    "attn_bwd_kernel": ("bwd.cuh", "bwd192.cuh", "common.cuh", "ptx.cuh"),
     "attn_bwd_wide_kernel": ("bwd.cuh", "bwd_wide.cuh", "cluster.cuh", "common.cuh", "ptx.cuh"),
 }
 

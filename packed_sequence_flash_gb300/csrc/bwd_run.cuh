@@ -3,6 +3,7 @@
 // bwd_cap.cu with the cap, bwd_pack.cu with packed query heads.
 #pragma once
 
+#include "bwd192.cuh"
 #include "bwd_dual.cuh"
 #include "bwd_wide.cuh"
 

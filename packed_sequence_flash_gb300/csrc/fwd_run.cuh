@@ -2,7 +2,7 @@
 // the softcap flag; fwd.cu instantiates them without a cap, fwd_cap.cu with.
 #pragma once
 
-#include "fwd.cuh"
+#include "fwd512.cuh"
 #include "fwd_duo.cuh"
 #include "fwd_pair.cuh"
 
