@@ -26,12 +26,11 @@
 //
 // TMEM: dV_r [0,128) | dK_r [128,256) | S_r^T [256,384) | dP_r^T, then dQ_r [384,512)
 // Shared memory: K_r, two buffers that take Q_r and dO_r in turn, P^T (32 KB
-// each); the dS^T buffer (32 KB),
-// which holds V_r until the step's dP product has read it; X (48 KB), the
-// columns received from the three other CTAs (S^T, then dP^T); dQ staging
-// (4 KB per read-out warp). P^T and dS^T are four 32-query chunks of 64-byte
-// rows (64-byte swizzle), so CTA r's columns are chunk r: one contiguous 8 KB
-// block.
+// each); the dS^T buffer (32 KB), which holds V_r until the step's dP product
+// has read it; X (48 KB), the columns received from the three other CTAs
+// (S^T, then dP^T); dQ staging (4 KB per read-out warp). P^T and dS^T are four
+// 32-query chunks of 64-byte rows (64-byte swizzle), so CTA r's columns are
+// chunk r: one contiguous 8 KB block.
 // Warps: 0 TMA producer, 1 MMA issuer, 2 TMEM allocator, 4-7 compute (the
 // exchange, P, dS, the dK/dV epilogue), 8-11 dQ read-out (TMA reduce-add).
 //
