@@ -336,6 +336,15 @@ def test_varlen_d512_window_noncausal():
     _varlen_case(4, 512, 512, 2, 1, False, 90, nseg=3, max_len=260)
 
 
+@pytest.mark.parametrize("causal", [True, False])
+def test_dense_d512_more_units_than_clusters(causal):
+    # 2 batches x 4 KV heads x 6 key tiles = 48 (key tile, KV head) units for
+    # the at most 38 four-CTA clusters of the head-dim-512 backward: some
+    # clusters take a second unit (K_r reloaded, dV/dK read out and restarted,
+    # no early S^T across the unit boundary), every row checked
+    _dense_case(2, 8, 4, 768, 768, 512, 512, causal, seed=5, factor=0.5)
+
+
 # ---------------------------------------------------------------- pad fixup and merge
 
 def test_pad_fixup_zeroes_pad_rows():
