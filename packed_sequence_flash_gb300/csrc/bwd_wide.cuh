@@ -356,9 +356,10 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(384, 1)
     };
     // This CTA's 16-bit columns (16 packed pairs) into its chunk of the
     // buffer at `off0` of all four CTAs: the warp writes its 32 rows (2 KB,
-    // contiguous) here, then sends them as 512-byte store instructions. Lane
-    // 0 arrives on the local barrier at `bar_off` (warp 4 with the three
-    // others' bytes).
+    // contiguous) here, reads them back four 512-byte rows at a time, arrives
+    // on the local barrier at `bar_off` (warp 4 with the three others' bytes)
+    // and only then stores them into the other CTAs, so that the arrival does
+    // not wait for those stores.
     auto share_cols = [&](const uint32_t (&pk)[16], int off0, int bar_off) {
 #pragma unroll
       for (int u = 0; u < 4; ++u)
@@ -366,13 +367,9 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(384, 1)
             make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
       __syncwarp();
       const uint32_t rows = off0 + rank * C::COL_BYTES + wq * 2048;
+      uint4 v[4];
 #pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        const uint32_t off = rows + m * 512 + lane * 16;
-        const uint4 v = lds_v4(sbase + off);
-#pragma unroll
-        for (int i = 0; i < 3; ++i) st_async_v4(pbase[i] + off, v, pbase[i] + bar_off);
-      }
+      for (int m = 0; m < 4; ++m) v[m] = lds_v4(sbase + rows + m * 512 + lane * 16);
       // The local copy is read by this CTA's tensor core.
       fence_proxy_async_smem();
       __syncwarp();
@@ -383,6 +380,11 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(384, 1)
         else
           mbar_arrive(b);
       }
+#pragma unroll
+      for (int m = 0; m < 4; ++m)
+#pragma unroll
+        for (int i = 0; i < 3; ++i)
+          st_async_v4(pbase[i] + rows + m * 512 + lane * 16, v[m], pbase[i] + bar_off);
     };
     // Every lane of the warp: a bounded wait by lane 0 on barrier `bar`.
     auto warp_wait_cl = [&](uint64_t* bar, uint32_t parity) {
@@ -442,6 +444,9 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(384, 1)
           break;
         }
         tc_fence_after();
+        // Arm the receive barrier for this step's S^T columns before this
+        // thread's own stores, so that the arming does not wait for them.
+        if (wq == 0 && lane == 0) mbar_arrive_expect_tx(&recv_full, C::X_BYTES);
         // ---- S^T: the other CTAs' columns of the partial sum go to them
         bool good = true;
         for (int i = 0; i < 3 && good; ++i) {
@@ -464,11 +469,12 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(384, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&s_read);
-        if (wq == 0 && lane == 0) mbar_arrive_expect_tx(&recv_full, C::X_BYTES);
         if (!wait_bar_cl(&recv_full, 0, ctl)) {
           ok = false;
           break;
         }
+        // The S^T phase is complete: arm the barrier for the dP^T columns.
+        if (wq == 0 && lane == 0) mbar_arrive_expect_tx(&recv_full, C::X_BYTES);
         add_recv(acc);
         // P (16-bit, packed, for P^T) and P (1 - tanh^2) in acc (for dS)
         uint32_t pk[16];
@@ -495,9 +501,11 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(384, 1)
           pk[e] = pack2<T>(pr[0], pr[1]);
         }
         // This warp's rows of X are summed: the others may send dP^T columns.
+        // (A relaxed arrive: it only releases slots whose values are already
+        // in registers, and must not wait for this thread's S^T stores.)
         __syncwarp();
         if (lane == 0)
-          for (int i = 0; i < 3; ++i) mbar_arrive_remote(pbase[i] + C::B_RXD + 8 * rank);
+          for (int i = 0; i < 3; ++i) mbar_arrive_remote_relaxed(pbase[i] + C::B_RXD + 8 * rank);
         // ---- P^T columns to all four CTAs (the dV product can start); the dP
         // product, whose dO_r and V_r load only after the previous step's dK
         // and dQ, is usually still running
@@ -527,7 +535,6 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(384, 1)
         // Last TMEM read of the step: the MMA may overwrite S^T and dP^T once
         // the ds_full arrival below is seen.
         tc_fence_before();
-        if (wq == 0 && lane == 0) mbar_arrive_expect_tx(&recv_full, C::X_BYTES);
         if (!wait_bar_cl(&recv_full, 1, ctl)) {
           ok = false;
           break;
@@ -536,7 +543,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(384, 1)
         // This warp's rows of X are summed: the others may send the next step's S^T columns.
         __syncwarp();
         if (lane == 0)
-          for (int i = 0; i < 3; ++i) mbar_arrive_remote(pbase[i] + C::B_RXS + 8 * rank);
+          for (int i = 0; i < 3; ++i) mbar_arrive_remote_relaxed(pbase[i] + C::B_RXS + 8 * rank);
         uint32_t dk2[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {

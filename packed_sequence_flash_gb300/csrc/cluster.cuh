@@ -65,6 +65,13 @@ __device__ __forceinline__ uint64_t sdesc_sw64(uint32_t saddr, uint32_t lbo, uin
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t rbar) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(rbar) : "memory");
 }
+// Arrive on another CTA's mbarrier without ordering this thread's earlier
+// memory operations: for a signal that only says "values this thread has
+// already loaded into registers may be overwritten", which must not wait for
+// the thread's own stores still in flight.
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t rbar) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(rbar) : "memory");
+}
 // Phase tests with cluster-scope acquire, for barriers that other CTAs of the
 // cluster arrive on or store against.
 __device__ __forceinline__ bool mbar_test_cl(uint64_t* bar, uint32_t parity) {
