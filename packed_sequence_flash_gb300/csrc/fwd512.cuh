@@ -31,11 +31,12 @@ struct FwdCfg {
   static constexpr int QCH = DQK / 64;  // 16 KB chunks per Q (or K) tile
   static constexpr int VCH = DVC / 64;  // chunks per V tile slice
   static constexpr int NQB = DQK >= 512 ? 1 : 2;
-  static constexpr int NST = DQK >= 512 ? 5 : (DQK >= 192 ? 7 : 8);
+  static constexpr int NST = DQK >= 512 ? 6 : (DQK >= 192 ? 7 : 8);
   static constexpr int Q_BYTES = QCH * kChunkBytes;
   static constexpr int SMEM_BYTES = NQB * Q_BYTES + NST * kChunkBytes + 1024;
   static constexpr int TMEM_O = 256;
   static_assert(DVC <= 256, "O must fit next to two S buffers");
+  static_assert(SMEM_BYTES + 512 <= 232448, "shared memory budget (dynamic + static)");
 };
 
 // CAP: logits softcapped (p.softcap > 0), applied to the score registers in
