@@ -75,7 +75,7 @@ NCU_TRAFFIC = {
     ("attn_bwd_dual_kernel", "cfg2_doc_causal_t8192_d128"): ("3ecea61619644db9", 362997760),
     ("attn_fwd_pair_kernel", "cfg4_doc_causal_shard_dqk192_dv128"): ("5837d1098189c960", 185433856),
     ("attn_bwd_kernel", "cfg4_doc_causal_shard_dqk192_dv128"): ("26951fb59a1df2f0", 775970048),
-    ("attn_fwd_kernel", "cfg3_dense_causal_n4096_d512"): ("776e62360b806358", 127129344),
+    ("attn_fwd_kernel", "cfg3_dense_causal_n4096_d512"): ("cf0774645e2e7eda", 126322944),
     ("attn_bwd_wide_kernel", "cfg3_dense_causal_n4096_d512"): ("df0f829a9fa47815", 960428544),
 }
 
