@@ -30,6 +30,8 @@
  *  - dtype: bf16 or fp16 inputs and outputs (`out`, `dq`, `dk`, `dv`), chosen
  *    per call by a PSF_DTYPE_* argument; lse and the row-dot Delta are fp32.
  *  - Head dims (Dqk, Dv) supported: (64,64), (128,128), (192,128), (512,512).
+ *    The (512,512) backward launches four-CTA thread-block clusters, as many
+ *    as the device holds at once; where it holds none (PSF_ECUDA).
  *  - GQA: Hq % Hkv == 0; query head h uses KV head h / (Hq / Hkv).
  *  - Causal masks are aligned to the bottom-right corner of each segment
  *    (dense: of the Nq x Nk matrix): local query i of a segment with m queries
