@@ -336,6 +336,12 @@ def test_varlen_d512_window_noncausal():
     _varlen_case(4, 512, 512, 2, 1, False, 90, nseg=3, max_len=260)
 
 
+def test_dense_d512_gqa8_window():
+    # eight query heads per KV head (steps walk 8 heads x the query tiles of a
+    # key tile) under a left window that leaves some key tiles few queries
+    _dense_case(1, 8, 1, 520, 520, 512, 512, True, window=150, seed=6, factor=0.5)
+
+
 @pytest.mark.parametrize("causal", [True, False])
 def test_dense_d512_more_units_than_clusters(causal):
     # 2 batches x 4 KV heads x 6 key tiles = 48 (key tile, KV head) units for
